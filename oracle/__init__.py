@@ -1,0 +1,164 @@
+"""fp64 CPU oracle for the channelwise gated delta rule forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+package: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` use it.  It shares no code with the CUDA library.
+
+Two routines, both in float64:
+
+``recurrence``
+    The definition: the per-token four-sweep recurrence (decay, predict,
+    rank-one delta update, output) of the page "Reorder channelwise gated
+    delta rule chunked hot loops for autovectorization" (pytorch/executorch
+    PR #21021, first commit summary).  Implemented in C (gdr_oracle.c),
+    threaded over (batch, value head).  This is THE oracle.
+
+``chunked_wy``
+    The chunkwise WY/UT restatement named in the second commit summary of the
+    same page (per-channel log-decay prefixes, causal query/key terms, the
+    beta-folded triangular transform, WY pseudo-values, inter-chunk state
+    carry, ragged last chunk).  Written from the algebra of unrolling the
+    recurrence over a chunk; it exists to pin the recurrence (the two must
+    agree to rounding for every chunk size) and is never the parity target.
+
+Array layouts (numpy, C-contiguous):
+    q, k [B, T, HK, dk]; v [B, T, HV, dv]; g [B, T, HV, dk]; beta [B, T, HV];
+    h0 [B, HV, dk, dv] or None.  Returns (o [B, T, HV, dv], ht [B, HV, dk, dv]).
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _open(path):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.gdr_oracle_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + [ctypes.c_long] * 6 + [
+        ctypes.c_int]
+    lib.gdr_oracle_f64.restype = ctypes.c_int
+    lib.gdr_oracle_default_threads.argtypes = []
+    lib.gdr_oracle_default_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _open(_build.build())
+    return _lib
+
+
+def default_threads() -> int:
+    """Number of host threads the oracle uses when ``threads`` is not given."""
+    return int(_load().gdr_oracle_default_threads())
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def recurrence(q, k, v, g, beta, h0=None, threads=None, _lib_override=None):
+    """fp64 sequential token recurrence (the oracle).  See module docstring.
+
+    ``_lib_override`` lets the oracle's own tests run a deliberately broken
+    build of gdr_oracle.c through the same pins (mutation testing)."""
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    assert k.shape == q.shape and v.shape[:2] == (B, T)
+    assert g.shape == (B, T, HV, dk) and beta.shape == (B, T, HV)
+    if h0 is not None:
+        h0 = _f64(h0)
+        assert h0.shape == (B, HV, dk, dv)
+    out = np.zeros((B, T, HV, dv), dtype=np.float64)
+    ht = np.zeros((B, HV, dk, dv), dtype=np.float64)
+    lib = _load() if _lib_override is None else _lib_override
+    rc = lib.gdr_oracle_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                            _ptr(out), _ptr(ht), B, T, HK, HV, dk, dv,
+                            0 if threads is None else int(threads))
+    if rc != 0:
+        raise RuntimeError("gdr_oracle_f64 failed with status %d" % rc)
+    return out, ht
+
+
+def recurrence_heads(q, k, v, g, beta, h0, heads, threads=None):
+    """Oracle on a subset of (b, hv) pairs.
+
+    Heads are independent, so slicing the inputs down to one (b, hv) and its
+    key head gives exactly that head's result.  Returns a dict
+    {(b, hv): (o [T, dv], ht [dk, dv])}.
+    """
+    HK = q.shape[2]
+    HV = v.shape[2]
+    group = HV // HK
+    res = {}
+    for (b, hv) in heads:
+        hk = hv // group
+        sl = lambda x, h: x[b:b + 1, :, h:h + 1]
+        o, ht = recurrence(sl(q, hk), sl(k, hk), sl(v, hv), sl(g, hv), beta[b:b + 1, :, hv:hv + 1],
+                           None if h0 is None else h0[b:b + 1, hv:hv + 1], threads=threads)
+        res[(b, hv)] = (o[0, :, 0], ht[0, 0])
+    return res
+
+
+def chunked_wy(q, k, v, g, beta, h0=None, chunk=64):
+    """fp64 chunkwise WY/UT restatement of the same forward pass.
+
+    Per (b, hv) and per chunk of L <= chunk tokens, with S0 the state at the
+    chunk start and r, s local token indices:
+      G       = inclusive prefix sum of g over the chunk, per key channel
+      A[r,s]  = beta_r * sum_i k_ri k_si exp(G_ri - G_si)      (s < r, else 0)
+      P[r,s]  = sum_i q_ri k_si exp(G_ri - G_si)                (s <= r, else 0)
+      Kt      = exp(G) * k,   Qt = exp(G) * q,   Kh = exp(G_L - G) * k
+      (I + A) U = diag(beta) (V - Kt S0)          (unit-lower triangular solve)
+      O       = Qt S0 + P U
+      S_next  = diag(exp(G_L)) S0 + Kh^T U
+    The ragged final chunk (L < chunk) runs through the same code.
+    """
+    from scipy.linalg import solve_triangular
+
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    group = HV // HK
+    out = np.zeros((B, T, HV, dv))
+    ht = np.zeros((B, HV, dk, dv))
+    for b in range(B):
+        for hv in range(HV):
+            hk = hv // group
+            S = np.zeros((dk, dv)) if h0 is None else _f64(h0)[b, hv].copy()
+            for t0 in range(0, T, chunk):
+                t1 = min(T, t0 + chunk)
+                L = t1 - t0
+                K = k[b, t0:t1, hk]          # [L, dk]
+                Q = q[b, t0:t1, hk]
+                V = v[b, t0:t1, hv]          # [L, dv]
+                bet = beta[b, t0:t1, hv]     # [L]
+                G = np.cumsum(g[b, t0:t1, hv], axis=0)   # [L, dk]
+                causal = np.tril(np.ones((L, L)), 0)
+                strict = np.tril(np.ones((L, L)), -1)
+                # [r, s, i] = exp(G_ri - G_si) on s <= r; the exponent is masked
+                # to -inf above the diagonal so it can never overflow there
+                D = np.where(causal[:, :, None] > 0, G[:, None, :] - G[None, :, :], -np.inf)
+                E = np.exp(D)
+                A = bet[:, None] * np.einsum("ri,si,rsi->rs", K, K, E) * strict
+                P = np.einsum("ri,si,rsi->rs", Q, K, E) * causal
+                Kt = np.exp(G) * K
+                Qt = np.exp(G) * Q
+                Kh = np.exp(G[-1][None, :] - G) * K
+                rhs = bet[:, None] * (V - Kt @ S)
+                U = solve_triangular(np.eye(L) + A, rhs, lower=True, unit_diagonal=True)
+                out[b, t0:t1, hv] = Qt @ S + P @ U
+                S = np.exp(G[-1])[:, None] * S + Kh.T @ U
+            ht[b, hv] = S
+    return out, ht
