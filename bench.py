@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Throughput of the channelwise gated delta rule forward on GB300.
+
+One JSON line on stdout (rank 0).  The headline is prefill tokens/s on the
+long-prefill workload (B=4, T=16384, HK=16, HV=32, dk=dv=128, chunk 64, bf16
+q/k/v, float32 g/beta/state, beta near 1 and slow decay, nonzero h0): a step
+is one gdr_forward over that batch, inputs resident in HBM (2.7 GB, larger
+than L2, so no flush is needed).  The same line carries the decode half of
+the metric under "decode": one T=1 step for B=64 sequences with the float32
+state updated in place, reported as state GB/s (read + write); four input
+sets (4 x 134 MB of state) are rotated so each step streams its state from
+HBM rather than L2.
+
+    python bench.py [--steps K] [--warmup W] [--impl gdr|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload, in the same unit.
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "GDR prefill tokens/s (HV=32,d=128) and decode state HBM GB/s, 1×GB300"
+PREFILL = "prefill_t16k"
+DECODE = "decode_b64"
+
+# DRAM bytes (read + write) per launch from an ncu capture, keyed by kernel,
+# with the sha256 of the source file the capture was taken from: a kernel
+# whose source has changed since reports traffic null.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device = str(device_index)
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "", 1).isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[3 + i].lower().startswith("active")})
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": reasons, "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+def src_sha(name):
+    with open(os.path.join(ROOT, "channelwise_gated_delta_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+KERNEL_SOURCE = {"gdr_decode_kernel": "decode.cu", "gdr_chunk_prep": "prefill_generic.cu",
+                 "gdr_chunk_scan": "prefill_generic.cu"}
+
+
+def traffic_for(kernel):
+    rec = NCU_TRAFFIC.get(kernel)
+    src = KERNEL_SOURCE.get(kernel)
+    if not rec or not src or rec["sha"] != src_sha(src):
+        return None
+    return rec["bytes"]
+
+
+def prefill_bytes_per_launch(w):
+    """Algorithmic HBM bytes of one prefill call: every input read once, every
+    output written once (q, k per key head; v, g, beta, o per value head;
+    h0 read and ht written once per head)."""
+    es = torch.tensor([], dtype=w.dtype).element_size()
+    per_token = (2 * w.HK * w.dk * es + w.HV * w.dv * es + w.HV * w.dk * 4 + w.HV * 4 +
+                 w.HV * w.dv * es)
+    state = w.B * w.HV * w.dk * w.dv * 4 * (2 if w.h0 else 1)
+    return w.B * w.T * per_token + state, per_token
+
+
+def decode_bytes_per_launch(w):
+    es = torch.tensor([], dtype=w.dtype).element_size()
+    state = 2 * w.B * w.HV * w.dk * w.dv * 4
+    small = w.B * (2 * w.HK * w.dk * es + w.HV * w.dv * es + w.HV * w.dk * 4 + w.HV * 4 +
+                   w.HV * w.dv * es)
+    return state + small, state
+
+
+def roofline(kernel, launches, total_ms, bytes_per_launch, peak, peak_kind):
+    avg_s = total_ms / 1e3 / max(launches, 1)
+    achieved = bytes_per_launch / avg_s / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
+            "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel),
+            "avg_launch_us": round(avg_s * 1e6, 2), "launches": launches}
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU arm
+def bench_prefill(args, ws, rank, dev):
+    from channelwise_gated_delta_gb300 import gdr_forward, gdr_trace_enable, gdr_trace_read
+    from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw_workload
+
+    w = WORKLOADS[PREFILL]
+    d = draw_workload(w, seed=1000 + rank, device=dev)
+    out = torch.empty(w.B, w.T, w.HV, w.dv, dtype=w.dtype, device=dev)
+    ht = torch.empty(w.B, w.HV, w.dk, w.dv, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdr_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=out, ht=ht,
+                    chunk=w.chunk, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    gdr_trace_read()
+    clocks = ClockSampler(dev.index if ws == 1 else int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(True)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(False)
+    barrier(ws)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    trace = gdr_trace_read()
+    ms = max_over_ranks(ms, ws)
+    tokens = w.B * w.T * args.steps * ws
+    res = dict(w=w, ms=ms, tokens_per_s=tokens / (ms / 1e3), trace=trace, clocks=clk)
+
+    if not args.no_e2e:
+        res["e2e"] = bench_prefill_e2e(args, w, d, out, ht, stream, dev, ws)
+    del d
+    return res
+
+
+def bench_prefill_e2e(args, w, d, out, ht, stream, dev, ws):
+    """Same metric through the public API with host buffers: per step the
+    inputs are copied from pinned host memory, the forward runs, and the
+    output and final state are copied back to pinned host memory."""
+    from channelwise_gated_delta_gb300 import gdr_forward
+    names = ("q", "k", "v", "g", "beta", "h0")
+    host = {n: d[n].to("cpu").pin_memory() for n in names}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + ht_h.numel() * ht_h.element_size()
+    steps = max(1, min(args.steps, 5))
+
+    def step():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        gdr_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=out, ht=ht,
+                    chunk=w.chunk, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        ht_h.copy_(ht, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(t0.elapsed_time(t1), ws)
+    return {"value": round(w.B * w.T * steps * ws / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+def bench_decode(args, ws, rank, dev, peak, peak_kind):
+    from channelwise_gated_delta_gb300 import gdr_forward, gdr_trace_enable, gdr_trace_read
+    from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw_workload
+
+    w = WORKLOADS[DECODE]
+    nbuf = 4
+    sets = [draw_workload(w, seed=2000 + 10 * rank + i, device=dev) for i in range(nbuf)]
+    outs = [torch.empty(w.B, 1, w.HV, w.dv, dtype=w.dtype, device=dev) for _ in range(nbuf)]
+    stream = torch.cuda.current_stream(dev)
+    steps = max(args.steps, 20)
+
+    def step(i):
+        s = sets[i % nbuf]
+        gdr_forward(s["q"], s["k"], s["v"], s["g"], s["beta"], s["h0"], out=outs[i % nbuf],
+                    ht=s["h0"], chunk=w.chunk, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    gdr_trace_read()
+    barrier(ws)
+    gdr_trace_enable(True)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(False)
+    ms = max_over_ranks(t0.elapsed_time(t1), ws)
+    trace = gdr_trace_read()
+    total_bytes, state_bytes = decode_bytes_per_launch(w)
+    n, kms = trace.get("gdr_decode_kernel", (0, 0.0))
+    state_gbs = state_bytes * steps * ws / (ms / 1e3) / 1e9
+    res = {"workload": "decode B64 T1 HK16 HV32 dk=dv=128 bf16 q/k/v, f32 g/beta, f32 state in "
+                       "place; 4 rotating input sets (537 MB of state > L2)",
+           "value": round(state_gbs, 1), "unit": "GB/s (state read+write)",
+           "tokens_per_s": round(w.B * steps * ws / (ms / 1e3), 1),
+           "ms_per_step": round(ms / steps, 4), "steps": steps,
+           "roofline": roofline("gdr_decode_kernel", n, kms, total_bytes, peak, peak_kind),
+           "gpu_launches": sum(v[0] for v in trace.values())}
+    res["roofline"]["state_gbs_kernel"] = round(state_bytes / (kms / 1e3 / max(n, 1)) / 1e9, 1)
+    del sets
+    return res
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(w, heads, T, threads=None, seed=7):
+    """Times the fp64 oracle on `heads` value heads x T tokens of workload w's
+    distributions.  Returns (seconds, head_tokens, cores)."""
+    import oracle
+    from channelwise_gated_delta_gb300.inputs import draw, to_f64
+    HK = max(1, heads // max(1, w.HV // w.HK))
+    HV = HK * (w.HV // w.HK)
+    d = draw(1, T, HK, HV, w.dk, w.dv, dtype=w.dtype, h0=w.h0, seed=seed, g_mu=w.g_mu,
+             g_sigma=w.g_sigma, beta_mu=w.beta_mu, beta_sigma=w.beta_sigma)
+    arrs = [to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")]
+    h0 = to_f64(d["h0"])
+    cores = threads or oracle.default_threads()
+    t = time.perf_counter()
+    oracle.recurrence(*arrs, h0, threads=cores)
+    dt = time.perf_counter() - t
+    return dt, HV * T, min(cores, HV)
+
+
+def cpu_baseline(w):
+    import oracle
+    cores = oracle.default_threads()
+    heads = max(2, 2 * cores)
+    T = 4096
+    dt, head_tokens, used = oracle_sample(w, heads, T, threads=cores)
+    # aim for ~10 s of CPU work: grow the sample once if the first was short
+    if dt < 3.0:
+        T2 = min(w.T, int(T * min(8.0, 10.0 / max(dt, 1e-3))))
+        dt, head_tokens, used = oracle_sample(w, heads, T2, threads=cores)
+        T = T2
+    tok_s = head_tokens / dt / w.HV
+    return {"value": round(tok_s, 2), "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": "%d value heads x %d tokens of the %s distributions (fp64 recurrence, "
+                      "%.1f s)" % (head_tokens // T, T, w.name, dt)}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle on the host cores, same metric and unit."""
+    from channelwise_gated_delta_gb300.inputs import WORKLOADS
+    import oracle
+    w = WORKLOADS[PREFILL]
+    cores = oracle.default_threads()
+    heads = max(2, cores)
+    T = w.T
+    for _ in range(args.warmup):
+        oracle_sample(w, heads, 64, threads=cores)
+    total_s, total_ht = 0.0, 0
+    for i in range(args.steps):
+        dt, ht_, used = oracle_sample(w, heads, T, threads=cores, seed=100 + i)
+        total_s += dt
+        total_ht += ht_
+    tok_s = total_ht / total_s / w.HV
+    sample = "%d value heads x %d tokens per step of the %s distributions" % (
+        total_ht // (T * args.steps), T, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 3), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_s / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name + " (sampled)", "B": w.B, "T": w.T, "HK": w.HK,
+                       "HV": w.HV, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
+            "cpu_baseline": {"value": round(tok_s, 3), "unit": "tokens/s", "cores": used,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(tok_s, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
+    hbm_peak, _, peak_kind = load_peaks()
+
+    pre = bench_prefill(args, ws, rank, dev)
+    w = pre["w"]
+    dec = None if args.no_decode else bench_decode(args, ws, rank, dev, hbm_peak, peak_kind)
+
+    bytes_launch, per_token = prefill_bytes_per_launch(w)
+    trace = pre["trace"]
+    dom = max(trace.items(), key=lambda kv: kv[1][1]) if trace else ("none", (0, 0.0))
+    line = {
+        "metric": METRIC, "value": round(pre["tokens_per_s"], 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(pre["ms"] / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B4 T16384 HK16 HV32 dk=dv=128 chunk64, bf16 q/k/v, f32 "
+                               "g/beta/state, beta=sigmoid(N(2,0.5)), g=-softplus(N(-3,1)), "
+                               "h0=0.3N(0,1)",
+                   "B": w.B, "T": w.T, "HK": w.HK, "HV": w.HV, "dk": w.dk, "dv": w.dv,
+                   "chunk": w.chunk, "l2": "inputs 2.7 GB > L2 (no flush); decode rotates 4 "
+                                           "state sets (537 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "roofline": roofline(dom[0], dom[1][0], dom[1][1], bytes_launch, hbm_peak, peak_kind),
+        "kernels": {k: {"launches": v[0], "ms_total": round(v[1], 3)} for k, v in trace.items()},
+        "gpu_launches": sum(v[0] for v in trace.values()),
+        "clocks": pre["clocks"],
+    }
+    line["roofline"]["algorithmic_bytes_per_token"] = per_token
+    if "e2e" in pre:
+        line["e2e"] = pre["e2e"]
+    if dec is not None:
+        line["decode"] = dec
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+"""ctypes binding of libgdr.so (the C ABI in include/gdr.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their data pointers and the current CUDA stream are handed to the
+library, and a non-OK status becomes an exception.  Every step of the forward
+pass runs in the library's CUDA kernels; there is no fallback of any kind, and
+the first call raises if the library has not been built.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgdr.so")
+
+GDR_OK = 0
+GDR_F32 = 0
+GDR_BF16 = 1
+GDR_FLAG_FORCE_CHUNKED = 1
+GDR_FLAG_FORCE_GENERIC = 2
+
+STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_UNSUPPORTED",
+                4: "GDR_ERR_ALIGN", 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA",
+                7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_ALIAS"}
+
+EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_device_check",
+            "gdr_trace_enable", "gdr_trace_read", "gdr_status_string", "gdr_last_cuda_error",
+            "gdr_version")
+
+_lib = None
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(msg)
+        self.status = status
+
+
+def load_library(path=LIB_PATH):
+    """Loads libgdr.so and declares its signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "libgdr.so is not built (%s). Build it with `python -c \"import __graft_entry__ as g; "
+            "g.build()\"` or `python channelwise_gated_delta_gb300/build.py`." % path)
+    lib = ctypes.CDLL(path)
+    vp, sz, i, u = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint
+    fwd = [vp] * 8 + [i] * 7 + [vp, i]
+    lib.gdr_workspace_bytes.argtypes = [i] * 8 + [u]
+    lib.gdr_workspace_bytes.restype = sz
+    lib.gdr_forward_ex.argtypes = fwd + [vp, sz, u]
+    lib.gdr_forward_ex.restype = i
+    lib.gdr_forward.argtypes = fwd
+    lib.gdr_forward.restype = i
+    lib.gdr_device_check.argtypes = [vp]
+    lib.gdr_device_check.restype = i
+    lib.gdr_status_string.argtypes = [i]
+    lib.gdr_status_string.restype = ctypes.c_char_p
+    lib.gdr_last_cuda_error.argtypes = []
+    lib.gdr_last_cuda_error.restype = i
+    lib.gdr_version.argtypes = []
+    lib.gdr_version.restype = ctypes.c_char_p
+    lib.gdr_trace_enable.argtypes = [i]
+    lib.gdr_trace_enable.restype = i
+    lib.gdr_trace_read.argtypes = [i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i),
+                                   ctypes.POINTER(ctypes.c_double)]
+    lib.gdr_trace_read.restype = i
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _check(lib, st):
+    if st != GDR_OK:
+        msg = lib.gdr_status_string(st).decode()
+        if st == 6:
+            msg += " (cudaError %d)" % lib.gdr_last_cuda_error()
+        raise GdrError(st, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return GDR_BF16
+    if dt == torch.float32:
+        return GDR_F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % dt)
+
+
+def gdr_workspace_bytes(B, T, HK, HV, dk, dv, chunk=64, dtype=torch.bfloat16, flags=0):
+    lib = load_library()
+    return int(lib.gdr_workspace_bytes(B, T, HK, HV, dk, dv, chunk, _dtype_code(dtype), flags))
+
+
+def gdr_forward(q, k, v, g, beta, h0=None, out=None, ht=None, chunk=64, stream=None,
+                workspace=None, flags=0, store_ht=True):
+    """Channelwise gated delta rule forward on the GPU.
+
+    q, k [B, T, HK, dk]; v [B, T, HV, dv] (bf16 or f32, all the same dtype);
+    g [B, T, HV, dk] f32; beta [B, T, HV] f32; h0 [B, HV, dk, dv] f32 or None.
+    ``out`` / ``ht`` are allocated when not given (``ht=h0`` updates in place;
+    ``store_ht=False`` skips the final state).  The workspace, if the route
+    needs one, is allocated from torch's allocator unless passed in.
+    Enqueued on ``stream`` (default: torch's current stream).  Returns (out, ht).
+    """
+    lib = load_library()
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("out", out), ("ht", ht)):
+        if t is None:
+            continue
+        if t.device != dev or dev.type != "cuda":
+            raise ValueError("%s must be a CUDA tensor on %s" % (name, dev))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k must match q in shape and dtype; v must match q in dtype")
+    if tuple(v.shape[:2]) != (B, T) or tuple(g.shape) != (B, T, HV, dk) or \
+            tuple(beta.shape) != (B, T, HV):
+        raise ValueError("inconsistent shapes")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if h0 is not None and (tuple(h0.shape) != (B, HV, dk, dv) or h0.dtype != torch.float32):
+        raise ValueError("h0 must be float32 [B, HV, dk, dv]")
+    if out is None:
+        out = torch.empty(B, T, HV, dv, dtype=q.dtype, device=dev)
+    if ht is None and store_ht:
+        ht = torch.empty(B, HV, dk, dv, dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    need = int(lib.gdr_workspace_bytes(B, T, HK, HV, dk, dv, chunk, code, flags))
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
+    st = lib.gdr_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(out),
+                            _ptr(ht), B, T, HK, HV, dk, dv, chunk,
+                            ctypes.c_void_p(stream.cuda_stream), code, ws_ptr, ws_bytes, flags)
+    _check(lib, st)
+    return out, ht
+
+
+def gdr_device_check(stream=None):
+    """Waits for the stream and raises if a kernel reported a bounded-wait timeout."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _check(lib, lib.gdr_device_check(ctypes.c_void_p(stream.cuda_stream)))
+
+
+def gdr_trace_enable(on=True):
+    """Starts (or stops) recording CUDA events around every launch of the library."""
+    load_library().gdr_trace_enable(1 if on else 0)
+
+
+def gdr_trace_read():
+    """Waits for the traced launches and returns {kernel name: (launches, total ms)}
+    for every kernel kind launched since tracing was enabled (records are cleared)."""
+    lib = load_library()
+    n = 8
+    names = (ctypes.c_char_p * n)()
+    launches = (ctypes.c_int * n)()
+    total = (ctypes.c_double * n)()
+    got = lib.gdr_trace_read(n, names, launches, total)
+    if got < 0:
+        raise GdrError(6, "gdr_trace_read: a CUDA event query failed")
+    return {names[i].decode(): (launches[i], total[i]) for i in range(got) if launches[i] > 0}
+
+
+def gdr_version():
+    return load_library().gdr_version().decode()

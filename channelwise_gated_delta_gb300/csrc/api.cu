@@ -1,0 +1,310 @@
+// api.cu -- the C ABI declared in include/gdr.h: argument validation,
+// routing by sequence length (page "Reorder channelwise gated delta rule
+// chunked hot loops for autovectorization", pytorch/executorch PR #21021,
+// second commit summary: T == 1 runs the two-pass token recurrence, T != 1
+// the chunkwise WY/UT form), workspace management and launches.
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+#include <vector>
+
+#include "common.cuh"
+#include "gdr.h"
+
+// Device-wide error word: kernels that wait with a bounded spin set it
+// instead of hanging; gdr_device_check reads and clears it.
+__device__ int g_gdr_device_error = 0;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+gdr_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return GDR_ERR_CUDA;
+}
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+bool supported_chunk(int c) { return c == 16 || c == 32 || c == 64; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void *p, size_t bytes) {
+    return Range{(uintptr_t)p, (uintptr_t)p + bytes};
+}
+bool overlap(Range a, Range b) {
+    return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Validates shapes and pointers; fills `p`. Does not look at the workspace.
+gdr_status validate(const void *q, const void *k, const void *v, const float *g,
+                    const float *beta, const float *h0, void *out, float *ht, int B, int T,
+                    int HK, int HV, int dk, int dv, int chunk, int qkv_dtype, gdr::Problem *p) {
+    if (B < 0 || T < 0 || HK <= 0 || HV <= 0) return GDR_ERR_SHAPE;
+    if (HV % HK != 0) return GDR_ERR_SHAPE;
+    if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk))
+        return GDR_ERR_UNSUPPORTED;
+    // every element count must fit comfortably in 63 bits, and grids in 31
+    const long long BT = (long long)B * T;
+    if (BT > (1LL << 40) || (long long)B * HV > (1LL << 30)) return GDR_ERR_SHAPE;
+    const bool work = BT > 0;
+    if (work && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, h0, out, ht};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+
+    const size_t es = qkv_dtype == GDR_BF16 ? 2 : 4;
+    const Range rq = range_of(q, (size_t)BT * HK * dk * es);
+    const Range rk = range_of(k, (size_t)BT * HK * dk * es);
+    const Range rv = range_of(v, (size_t)BT * HV * dv * es);
+    const Range rg = range_of(g, (size_t)BT * HV * dk * 4);
+    const Range rb = range_of(beta, (size_t)BT * HV * 4);
+    const Range rs0 = h0 ? range_of(h0, (size_t)B * HV * dk * dv * 4) : Range{0, 0};
+    const Range ro = work ? range_of(out, (size_t)BT * HV * dv * es) : Range{0, 0};
+    const Range rst = ht ? range_of(ht, (size_t)B * HV * dk * dv * 4) : Range{0, 0};
+    const Range ins[] = {rq, rk, rv, rg, rb};
+    for (const Range &r : ins) {
+        if (overlap(ro, r) || overlap(rst, r)) return GDR_ERR_ALIAS;
+    }
+    if (overlap(ro, rs0) || overlap(ro, rst)) return GDR_ERR_ALIAS;
+    if (h0 && ht && h0 != ht && overlap(rs0, rst)) return GDR_ERR_ALIAS;
+
+    *p = gdr::Problem{q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
+                      qkv_dtype == GDR_BF16 ? 1 : 0};
+    return GDR_OK;
+}
+
+enum class Route { Nothing, EmptySequence, Decode, GenericPrefill };
+
+Route choose(const gdr::Problem &p, unsigned flags) {
+    if (p.B == 0) return Route::Nothing;
+    if (p.T == 0) return Route::EmptySequence;
+    if (p.T == 1 && !(flags & GDR_FLAG_FORCE_CHUNKED)) return Route::Decode;
+    return Route::GenericPrefill;
+}
+
+size_t route_workspace(const gdr::Problem &p, Route r) {
+    return r == Route::GenericPrefill ? gdr::generic_prefill_workspace_bytes(p) : 0;
+}
+
+gdr_status run(const gdr::Problem &p, Route r, void *ws, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    switch (r) {
+        case Route::Nothing:
+            return GDR_OK;
+        case Route::EmptySequence: {
+            if (!p.ht) return GDR_OK;
+            const size_t bytes = (size_t)p.B * p.HV * p.dk * p.dv * sizeof(float);
+            if (p.h0 == p.ht) return GDR_OK;
+            e = p.h0 ? cudaMemcpyAsync(p.ht, p.h0, bytes, cudaMemcpyDeviceToDevice, stream)
+                     : cudaMemsetAsync(p.ht, 0, bytes, stream);
+            break;
+        }
+        case Route::Decode:
+            e = gdr::launch_decode(p, stream);
+            break;
+        case Route::GenericPrefill:
+            e = gdr::launch_generic_prefill(p, ws, stream);
+            break;
+    }
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e);
+}
+
+// Library-owned workspace, one per device.
+struct OwnedWorkspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::vector<OwnedWorkspace> g_ws;
+
+// ---- launch tracing: a pair of CUDA events on the launching stream around
+// every kernel launch of this library, while enabled.
+struct TraceRec {
+    int kernel;
+    cudaEvent_t a, b;
+};
+std::mutex g_trace_mutex;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+thread_local cudaEvent_t t_pending_begin = nullptr;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_prep",
+                                              "gdr_chunk_scan", "gdr_prefill_fused"};
+
+}  // namespace
+
+namespace gdr {
+void trace_begin(int kernel, cudaStream_t stream) {
+    (void)kernel;
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    if (!g_trace_on) return;
+    cudaEvent_t e = take_event();
+    if (e && cudaEventRecord(e, stream) == cudaSuccess) t_pending_begin = e;
+}
+void trace_end(int kernel, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    if (!g_trace_on || !t_pending_begin) return;
+    cudaEvent_t e = take_event();
+    if (e && cudaEventRecord(e, stream) == cudaSuccess) {
+        g_trace.push_back(TraceRec{kernel, t_pending_begin, e});
+    }
+    t_pending_begin = nullptr;
+}
+}  // namespace gdr
+
+extern "C" {
+
+GDR_API gdr_status gdr_trace_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    g_trace_on = on != 0;
+    return GDR_OK;
+}
+
+GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, double *total_ms) {
+    std::vector<TraceRec> recs;
+    {
+        std::lock_guard<std::mutex> lock(g_trace_mutex);
+        recs.swap(g_trace);
+    }
+    const int n = max_kernels < gdr::kNumKernels ? max_kernels : gdr::kNumKernels;
+    for (int i = 0; i < n; ++i) {
+        if (names) names[i] = kKernelNames[i];
+        if (launches) launches[i] = 0;
+        if (total_ms) total_ms[i] = 0.0;
+    }
+    int status = 0;
+    for (const TraceRec &r : recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+            status = -1;
+        if (r.kernel < n) {
+            if (launches) launches[r.kernel] += 1;
+            if (total_ms) total_ms[r.kernel] += ms;
+        }
+    }
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    for (const TraceRec &r : recs) {
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    return status < 0 ? status : n;
+}
+
+GDR_API size_t gdr_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                   int qkv_dtype, unsigned flags) {
+    // shape-only validation: use a fake aligned, non-overlapping pointer set
+    gdr::Problem p;
+    if (B < 0 || T < 0 || HK <= 0 || HV <= 0 || HV % HK != 0) return 0;
+    if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk)) return 0;
+    p = gdr::Problem{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                     B, T, HK, HV, dk, dv, chunk, qkv_dtype == GDR_BF16 ? 1 : 0};
+    return route_workspace(p, choose(p, flags));
+}
+
+GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, const float *h0, void *out, float *ht,
+                                  int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                  void *stream, int qkv_dtype, void *workspace,
+                                  size_t workspace_bytes, unsigned flags) {
+    gdr::Problem p;
+    gdr_status st = validate(q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
+                             qkv_dtype, &p);
+    if (st != GDR_OK) return st;
+    const Route r = choose(p, flags);
+    const size_t need = route_workspace(p, r);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return GDR_ERR_WORKSPACE;
+        if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGN;
+    }
+    return run(p, r, workspace, static_cast<cudaStream_t>(stream));
+}
+
+GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, const float *h0, void *out, float *ht, int B,
+                               int T, int HK, int HV, int dk, int dv, int chunk, void *stream,
+                               int qkv_dtype) {
+    gdr::Problem p;
+    gdr_status st = validate(q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
+                             qkv_dtype, &p);
+    if (st != GDR_OK) return st;
+    const Route r = choose(p, 0u);
+    const size_t need = route_workspace(p, r);
+    void *ws = nullptr;
+    if (need > 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
+        OwnedWorkspace &w = g_ws[dev];
+        if (w.bytes < need) {
+            if (w.ptr) {
+                // the old buffer may still be in use by earlier launches
+                e = cudaDeviceSynchronize();
+                if (e != cudaSuccess) return cuda_fail(e);
+                cudaFree(w.ptr);
+                w.ptr = nullptr;
+                w.bytes = 0;
+            }
+            e = cudaMalloc(&w.ptr, need);
+            if (e != cudaSuccess) return cuda_fail(e);
+            w.bytes = need;
+        }
+        ws = w.ptr;
+    }
+    return run(p, r, ws, static_cast<cudaStream_t>(stream));
+}
+
+GDR_API gdr_status gdr_device_check(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_gdr_device_error, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_gdr_device_error, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return GDR_ERR_TIMEOUT;
+    }
+    return GDR_OK;
+}
+
+GDR_API const char *gdr_status_string(int status) {
+    switch (status) {
+        case GDR_OK: return "GDR_OK";
+        case GDR_ERR_NULL: return "GDR_ERR_NULL: a required pointer is NULL";
+        case GDR_ERR_SHAPE: return "GDR_ERR_SHAPE: invalid or overflowing shape (or HV % HK != 0)";
+        case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: dk, dv, chunk or dtype not supported";
+        case GDR_ERR_ALIGN: return "GDR_ERR_ALIGN: pointer not 16-byte aligned (workspace: 256)";
+        case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace missing or too small";
+        case GDR_ERR_CUDA: return "GDR_ERR_CUDA: a CUDA call or launch failed";
+        case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+        case GDR_ERR_ALIAS: return "GDR_ERR_ALIAS: an output overlaps another argument";
+        default: return "unknown gdr_status";
+    }
+}
+
+GDR_API int gdr_last_cuda_error(void) { return t_last_cuda_error; }
+
+GDR_API const char *gdr_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// common.cuh -- small device helpers shared by the kernels of this library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdr {
+
+// Element loads/stores for the q/k/v/out dtype.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Four consecutive elements starting at a 4-element-aligned index, as fp32.
+__device__ __forceinline__ float4 load4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
+    __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
+    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float *p, float4 x) {
+    *reinterpret_cast<float4 *>(p) = x;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&lo);
+    raw.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = raw;
+}
+
+// Streaming (evict-first) 16-byte global accesses for data touched once.
+__device__ __forceinline__ float4 ldg_stream4(const float *p) {
+    float4 r;
+    asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void stg_stream4(float *p, float4 x) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x.x), "f"(x.y),
+                 "f"(x.z), "f"(x.w)
+                 : "memory");
+}
+
+}  // namespace gdr
+
+// Launchers implemented in the .cu files (host side, C++ linkage).
+namespace gdr {
+// Kernel identities for launch tracing (gdr_trace_enable / gdr_trace_read).
+enum KernelId { kKernDecode = 0, kKernChunkPrep = 1, kKernChunkScan = 2, kKernFused = 3, kNumKernels = 4 };
+// Called by the launchers around each launch; no-ops unless tracing is on.
+void trace_begin(int kernel, cudaStream_t stream);
+void trace_end(int kernel, cudaStream_t stream);
+
+struct Problem {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    void *out;
+    float *ht;
+    int B, T, HK, HV, dk, dv, chunk;
+    int bf16;  // 1: q/k/v/out are bfloat16, 0: float32
+};
+
+cudaError_t launch_decode(const Problem &p, cudaStream_t stream);
+size_t generic_prefill_workspace_bytes(const Problem &p);
+cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream);
+}  // namespace gdr

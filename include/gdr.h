@@ -1,0 +1,149 @@
+/*
+ * gdr.h -- C ABI of the GB300 channelwise gated delta rule forward library.
+ *
+ * The operation (page "Reorder channelwise gated delta rule chunked hot loops
+ * for autovectorization", pytorch/executorch PR #21021): each value head keeps
+ * a float32 state S[dk][dv] (row i = key channel, column j = value channel).
+ * Every token t, in order,
+ *     decays the rows of S by exp(g_t[i])            (per key channel),
+ *     predicts  vhat = S^T k_t                      (from the decayed state),
+ *     updates   S += beta_t * k_t (v_t - vhat)^T    (rank-one delta correction),
+ *     outputs   o_t = S^T q_t                       (from the updated state).
+ * There is no 1/sqrt(dk) query scale: fold one into q if wanted.
+ *
+ * Routing (same page, second commit summary): T == 1 runs the single-token
+ * decode kernel, which streams the state once; T > 1 runs the chunkwise
+ * WY/UT prefill (per-channel log-decay prefix sums, causal query/key terms,
+ * the beta-folded unit-lower triangular transform, WY pseudo-keys and
+ * pseudo-values, inter-chunk state carry, ragged last chunk).
+ *
+ * Grouped heads (trymirai/uzu PR #576, review thread on the per-value-head
+ * gram): HK key/query heads serve HV value heads, G = HV / HK; value head hv
+ * reads key/query head hv / G (contiguous groups).
+ *
+ * Memory and layouts.  Every pointer is DEVICE memory owned by the caller,
+ * 16-byte aligned, densely packed row-major with the last index fastest:
+ *     q, k   [B][T][HK][dk]   dtype qkv_dtype
+ *     v      [B][T][HV][dv]   dtype qkv_dtype
+ *     g      [B][T][HV][dk]   float32, natural-log decay (<= 0 expected, not checked)
+ *     beta   [B][T][HV]       float32, used as given (no sigmoid applied)
+ *     h0     [B][HV][dk][dv]  float32 initial state, or NULL for zeros
+ *     out    [B][T][HV][dv]   dtype qkv_dtype (rounded to nearest even for bf16)
+ *     ht     [B][HV][dk][dv]  float32 final state, or NULL to skip storing it
+ * ht == h0 (the same pointer) updates the state in place.  Any other overlap
+ * between an output (out, ht) and any other argument is rejected.
+ *
+ * Supported shapes: B >= 0, T >= 0, HK >= 1, HV % HK == 0, dk and dv in
+ * {32, 64, 128}, chunk in {16, 32, 64} (the prefill chunk length; the result
+ * does not depend on it beyond rounding).  B == 0 does nothing.  T == 0
+ * writes ht = h0 (or zeros) and nothing else.
+ *
+ * Streams and errors.  All work is enqueued on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and the calls return without waiting for it.
+ * Argument errors are detected before anything is enqueued and leave every
+ * output untouched.  GDR_ERR_CUDA means a CUDA runtime call or launch failed;
+ * gdr_last_cuda_error() gives the cudaError_t code.  No call allocates device
+ * memory except gdr_forward, which owns a per-device workspace (see there).
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GDR_API __attribute__((visibility("default")))
+#else
+#define GDR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdr_status {
+    GDR_OK = 0,
+    GDR_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDR_ERR_SHAPE = 2,       /* negative size, HV % HK != 0, or a size that overflows */
+    GDR_ERR_UNSUPPORTED = 3, /* dk, dv, chunk or dtype outside the supported set */
+    GDR_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    GDR_ERR_WORKSPACE = 5,   /* caller workspace NULL or smaller than gdr_workspace_bytes */
+    GDR_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+    GDR_ERR_TIMEOUT = 7,     /* a kernel gave up on a bounded wait (see gdr_device_check) */
+    GDR_ERR_ALIAS = 8        /* an output overlaps another argument (other than ht == h0) */
+} gdr_status;
+
+typedef enum gdr_dtype {
+    GDR_F32 = 0,  /* q, k, v, out are float32 */
+    GDR_BF16 = 1  /* q, k, v, out are bfloat16; g, beta, h0, ht stay float32 */
+} gdr_dtype;
+
+/* Flags for gdr_forward_ex (test and diagnosis use; 0 in normal calls). */
+#define GDR_FLAG_FORCE_CHUNKED 1u /* run the chunked prefill even when T == 1 */
+#define GDR_FLAG_FORCE_GENERIC 2u /* use the CUDA-core prefill even where the tensor-core one applies */
+
+/*
+ * Bytes of device workspace gdr_forward_ex needs for this call (0 when the
+ * chosen route needs none).  Returns 0 for arguments gdr_forward_ex would
+ * reject.  Same shape arguments and flags as gdr_forward_ex.
+ */
+GDR_API size_t gdr_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                   int qkv_dtype, unsigned flags);
+
+/*
+ * The forward pass with a caller-owned workspace.  `workspace` is device
+ * memory of at least gdr_workspace_bytes(...) bytes (may be NULL when that is
+ * 0), 256-byte aligned, not overlapping any other argument, and must not be
+ * used by anything else until the enqueued work is done.  Allocates nothing.
+ */
+GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, const float *h0, void *out, float *ht,
+                                  int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                  void *stream, int qkv_dtype, void *workspace,
+                                  size_t workspace_bytes, unsigned flags);
+
+/*
+ * The forward pass with the library's own workspace.  The library keeps one
+ * workspace per device and grows it with cudaMalloc when a call needs more
+ * (cudaMalloc synchronises the device, so a growing call is not
+ * asynchronous).  Calls that share the library workspace must be ordered:
+ * issue them on one stream per device, or use gdr_forward_ex.
+ */
+GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, const float *h0, void *out, float *ht,
+                               int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                               void *stream, int qkv_dtype);
+
+/*
+ * Waits for `stream`, then reads and clears the library's device error word
+ * on the current device.  Returns GDR_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last check, GDR_ERR_CUDA if the stream reported an
+ * error, else GDR_OK.
+ */
+GDR_API gdr_status gdr_device_check(void *stream);
+
+/*
+ * Launch tracing.  While enabled (process-wide), every kernel launch made by
+ * this library is bracketed by two CUDA events recorded on the launching
+ * stream.  gdr_trace_read waits for the recorded events, writes per kernel
+ * kind its name, launch count and summed event-to-event milliseconds into
+ * the caller's arrays (each of max_kernels entries; any may be NULL),
+ * forgets the records, and returns the number of kernel kinds written, or
+ * -1 if a CUDA event query failed.  Tracing adds two event records per launch.
+ */
+GDR_API gdr_status gdr_trace_enable(int on);
+GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, double *total_ms);
+
+/* Human-readable name of a gdr_status value (static string, never NULL). */
+GDR_API const char *gdr_status_string(int status);
+
+/* cudaError_t code of the last CUDA failure seen by this thread (0 if none). */
+GDR_API int gdr_last_cuda_error(void);
+
+/* Library version string, e.g. "0.1.0" (static string). */
+GDR_API const char *gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

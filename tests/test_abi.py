@@ -1,0 +1,102 @@
+"""The C ABI library: it loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU (CPU only: no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from channelwise_gated_delta_gb300 import _binding
+    from channelwise_gated_delta_gb300 import build as cbuild
+    cbuild.build()
+    return _binding.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDR_API\s+[\w\s\*]+?\b(gdr_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    syms = declared_symbols()
+    for s in ("gdr_forward", "gdr_forward_ex", "gdr_workspace_bytes", "gdr_device_check",
+              "gdr_status_string", "gdr_last_cuda_error", "gdr_version"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), "libgdr.so does not export %s" % s
+
+
+def test_internal_symbols_are_hidden(lib):
+    # only the C ABI is visible; kernels and launchers are not
+    assert not hasattr(lib, "_ZN3gdr13launch_decodeERKNS_7ProblemEP11CUstream_st")
+
+
+def test_status_strings_and_version(lib):
+    for st in range(9):
+        assert lib.gdr_status_string(st).decode().startswith("GDR_")
+    assert lib.gdr_version().decode().count(".") == 2
+
+
+FAKE = 1 << 40  # 16-byte aligned host address that is never dereferenced
+
+
+def call(lib, B=1, T=4, HK=1, HV=2, dk=32, dv=32, chunk=16, dtype=1, ptrs=None, ws=None,
+         ws_bytes=0, flags=0):
+    step = 1 << 30
+    p = dict(q=FAKE, k=FAKE + step, v=FAKE + 2 * step, g=FAKE + 3 * step, beta=FAKE + 4 * step,
+             h0=FAKE + 5 * step, out=FAKE + 6 * step, ht=FAKE + 7 * step)
+    if ptrs:
+        p.update(ptrs)
+    args = [ctypes.c_void_p(p[n]) if p[n] is not None else None
+            for n in ("q", "k", "v", "g", "beta", "h0", "out", "ht")]
+    return lib.gdr_forward_ex(*args, B, T, HK, HV, dk, dv, chunk, None, dtype,
+                              None if ws is None else ctypes.c_void_p(ws), ws_bytes, flags)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(HK=2, HV=3), 2),                 # HV % HK != 0
+    (dict(B=-1), 2),
+    (dict(T=-3), 2),
+    (dict(HK=0), 2),
+    (dict(dk=48), 3),                      # unsupported head dim
+    (dict(dv=256), 3),
+    (dict(chunk=128), 3),
+    (dict(dtype=7), 3),
+    (dict(ptrs=dict(q=None)), 1),
+    (dict(ptrs=dict(out=None)), 1),
+    (dict(ptrs=dict(g=FAKE + (3 << 30) + 4)), 4),     # misaligned
+    (dict(ptrs=dict(out=FAKE + 16)), 8),               # out overlaps q
+    (dict(ptrs=dict(ht=FAKE + (1 << 30))), 8),         # ht overlaps k
+    (dict(ptrs=dict(ht=FAKE + (5 << 30) + 16)), 8),    # ht partially overlaps h0
+    (dict(T=40), 5),                                   # prefill needs a workspace, none given
+])
+def test_bad_arguments_rejected_before_launch(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_workspace_sizes(lib):
+    # decode needs none; the CUDA-core prefill needs one record per chunk
+    assert lib.gdr_workspace_bytes(64, 1, 16, 32, 128, 128, 64, 1, 0) == 0
+    small = lib.gdr_workspace_bytes(1, 40, 1, 2, 32, 32, 16, 0, 0)
+    assert small > 0
+    assert lib.gdr_workspace_bytes(1, 1, 1, 2, 32, 32, 16, 0, 1) > 0   # forced chunked at T=1
+    assert lib.gdr_workspace_bytes(1, 40, 2, 3, 32, 32, 16, 0, 0) == 0  # invalid shape
+    # a workspace one byte short is rejected
+    assert call(lib, T=40, dtype=0, ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5
+    # misaligned workspace
+    assert call(lib, T=40, dtype=0, ws=FAKE + (9 << 30) + 16, ws_bytes=small) == 4
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from channelwise_gated_delta_gb300 import _binding
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.load_library(str(tmp_path / "missing.so"))
