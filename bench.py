@@ -52,7 +52,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--workload", choices=["all", "prefill", "decode"], default="all",
+                    help="prefill: the headline only; decode: only the decode measurement "
+                         "(printed as its own line, for profiling the decode kernel)")
     return ap.parse_args()
 
 
@@ -402,9 +404,18 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
     hbm_peak, _, peak_kind = load_peaks()
 
+    if args.workload == "decode":
+        dec = bench_decode(args, ws, rank, dev, hbm_peak, peak_kind)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC + " [decode only]", "decode": dec}), flush=True)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     pre = bench_prefill(args, ws, rank, dev)
     w = pre["w"]
-    dec = None if args.no_decode else bench_decode(args, ws, rank, dev, hbm_peak, peak_kind)
+    dec = None if args.workload == "prefill" else bench_decode(args, ws, rank, dev, hbm_peak,
+                                                               peak_kind)
 
     bytes_launch, per_token = prefill_bytes_per_launch(w)
     trace = pre["trace"]

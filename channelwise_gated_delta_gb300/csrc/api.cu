@@ -52,9 +52,12 @@ gdr_status validate(const void *q, const void *k, const void *v, const float *g,
     if (BT > (1LL << 40) || (long long)B * HV > (1LL << 30)) return GDR_ERR_SHAPE;
     const bool work = BT > 0;
     if (work && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_NULL;
-    const void *ptrs[] = {q, k, v, g, beta, h0, out, ht};
+    // 16-byte alignment for everything read or written in vectors or bulk
+    // copies; beta is only ever read one element at a time
+    const void *ptrs[] = {q, k, v, g, h0, out, ht};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    if (beta && ((uintptr_t)beta & 3u) != 0) return GDR_ERR_ALIGN;
 
     const size_t es = qkv_dtype == GDR_BF16 ? 2 : 4;
     const Range rq = range_of(q, (size_t)BT * HK * dk * es);

@@ -22,7 +22,8 @@
  * reads key/query head hv / G (contiguous groups).
  *
  * Memory and layouts.  Every pointer is DEVICE memory owned by the caller,
- * 16-byte aligned, densely packed row-major with the last index fastest:
+ * 16-byte aligned (beta: 4-byte aligned), densely packed row-major with the
+ * last index fastest:
  *     q, k   [B][T][HK][dk]   dtype qkv_dtype
  *     v      [B][T][HV][dv]   dtype qkv_dtype
  *     g      [B][T][HV][dk]   float32, natural-log decay (<= 0 expected, not checked)
@@ -65,7 +66,7 @@ typedef enum gdr_status {
     GDR_ERR_NULL = 1,        /* a required pointer is NULL */
     GDR_ERR_SHAPE = 2,       /* negative size, HV % HK != 0, or a size that overflows */
     GDR_ERR_UNSUPPORTED = 3, /* dk, dv, chunk or dtype outside the supported set */
-    GDR_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    GDR_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned (beta: 4-byte) */
     GDR_ERR_WORKSPACE = 5,   /* caller workspace NULL or smaller than gdr_workspace_bytes */
     GDR_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
     GDR_ERR_TIMEOUT = 7,     /* a kernel gave up on a bounded wait (see gdr_device_check) */

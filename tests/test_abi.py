@@ -74,6 +74,7 @@ def call(lib, B=1, T=4, HK=1, HV=2, dk=32, dv=32, chunk=16, dtype=1, ptrs=None, 
     (dict(ptrs=dict(q=None)), 1),
     (dict(ptrs=dict(out=None)), 1),
     (dict(ptrs=dict(g=FAKE + (3 << 30) + 4)), 4),     # misaligned
+    (dict(ptrs=dict(beta=FAKE + (4 << 30) + 2)), 4),  # beta needs 4-byte alignment
     (dict(ptrs=dict(out=FAKE + 16)), 8),               # out overlaps q
     (dict(ptrs=dict(ht=FAKE + (1 << 30))), 8),         # ht overlaps k
     (dict(ptrs=dict(ht=FAKE + (5 << 30) + 16)), 8),    # ht partially overlaps h0

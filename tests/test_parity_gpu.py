@@ -154,7 +154,7 @@ def test_resume_matches_single_call():
     d = draw(1, 100, 1, 2, 64, 64, dtype=torch.float32, seed=12)
     c = to_cuda(d)
     o_all, h_all = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=32)
-    sl = lambda x, a, b: x[:, a:b].contiguous()
+    sl = lambda x, a, b: x[:, a:b].clone()  # fresh, aligned allocations
     oa, ha = gdr_forward(*(sl(c[n], 0, 37) for n in ("q", "k", "v", "g", "beta")), c["h0"], chunk=32)
     ob, hb = gdr_forward(*(sl(c[n], 37, 100) for n in ("q", "k", "v", "g", "beta")), ha, chunk=32)
     ref_o, ref_h = run_oracle(d)
