@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
                 4: "GDR_ERR_ALIGN", 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA",
                 7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_ALIAS"}
 
-EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_device_check",
+EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_forward_chunked_noalloc",
+            "gdr_device_check",
             "gdr_trace_enable", "gdr_trace_read", "gdr_status_string", "gdr_last_cuda_error",
             "gdr_version")
 
@@ -55,6 +56,8 @@ def load_library(path=LIB_PATH):
     lib.gdr_forward_ex.restype = i
     lib.gdr_forward.argtypes = fwd
     lib.gdr_forward.restype = i
+    lib.gdr_forward_chunked_noalloc.argtypes = fwd
+    lib.gdr_forward_chunked_noalloc.restype = i
     lib.gdr_device_check.argtypes = [vp]
     lib.gdr_device_check.restype = i
     lib.gdr_status_string.argtypes = [i]

@@ -153,6 +153,13 @@ const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_pr
 }  // namespace
 
 namespace gdr {
+// Lets other translation units of the library report a CUDA failure through
+// gdr_last_cuda_error().
+int record_cuda_error(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return (int)e;
+}
+
 void trace_begin(int kernel, cudaStream_t stream) {
     (void)kernel;
     std::lock_guard<std::mutex> lock(g_trace_mutex);

@@ -115,6 +115,43 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
                                void *stream, int qkv_dtype);
 
 /*
+ * Size in bytes of the fixed device scratch array behind
+ * gdr_forward_chunked_noalloc (64 MiB, held on every device that loads the
+ * library until the process exits).
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * The chunked CUDA-core prefill (the same kernels and results as
+ * gdr_forward_ex with GDR_FLAG_FORCE_CHUNKED | GDR_FLAG_FORCE_GENERIC) with
+ * its workspace taken from a fixed array inside the library instead of being
+ * allocated or passed in.  Nothing in the pages corresponds to it: it exists
+ * for callers that cannot allocate device memory -- a runtime whose memory
+ * planner owns every device byte and gives operators only their inputs and
+ * outputs, a serving loop that must never pay cudaMalloc's device-wide
+ * synchronisation, or a plugin whose host process lets only its own caching
+ * allocator own device memory.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Arguments, layouts and errors are those of gdr_forward (T == 1 is run
+ * through the chunked path too).  A problem whose workspace
+ * (gdr_workspace_bytes with those two flags) exceeds
+ * GDR_NOALLOC_SCRATCH_BYTES is rejected with GDR_ERR_WORKSPACE before
+ * anything is enqueued.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches
+ * it; make that first call before any stream capture.  All calls on a device
+ * share the one array and it keeps the last call's contents (each call writes
+ * every scratch word it reads, so nothing needs clearing): calls whose work
+ * can overlap on the GPU -- different streams, or different host threads --
+ * race on it and must be serialised by the caller.
+ */
+GDR_API gdr_status gdr_forward_chunked_noalloc(const void *q, const void *k, const void *v,
+                                               const float *g, const float *beta,
+                                               const float *h0, void *out, float *ht, int B,
+                                               int T, int HK, int HV, int dk, int dv, int chunk,
+                                               void *stream, int qkv_dtype);
+
+/*
  * Waits for `stream`, then reads and clears the library's device error word
  * on the current device.  Returns GDR_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, GDR_ERR_CUDA if the stream reported an
