@@ -80,14 +80,43 @@ gdr_status validate(const void *q, const void *k, const void *v, const float *g,
     return GDR_OK;
 }
 
-enum class Route { Nothing, EmptySequence, Decode, GenericPrefill };
+enum class Route { Nothing, EmptySequence, Decode, GenericPrefill, TensorCorePrefill };
 
 Route choose(const gdr::Problem &p, unsigned flags) {
     if (p.B == 0) return Route::Nothing;
     if (p.T == 0) return Route::EmptySequence;
     if (p.T == 1 && !(flags & GDR_FLAG_FORCE_CHUNKED)) return Route::Decode;
+    if (gdr::tc_prefill_supported(p) && !(flags & GDR_FLAG_FORCE_GENERIC))
+        return Route::TensorCorePrefill;
     return Route::GenericPrefill;
 }
+
+std::mutex g_err_mutex;
+std::vector<int *> g_err_addr;
+
+}  // namespace
+
+namespace gdr {
+// Device address of g_gdr_device_error on the current device (looked up once
+// per device).
+cudaError_t device_error_word(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if ((int)g_err_addr.size() <= dev) g_err_addr.resize(dev + 1, nullptr);
+    if (!g_err_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_gdr_device_error);
+        if (e != cudaSuccess) return e;
+        g_err_addr[dev] = static_cast<int *>(p);
+    }
+    *out = g_err_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace gdr
+
+namespace {
 
 size_t route_workspace(const gdr::Problem &p, Route r) {
     return r == Route::GenericPrefill ? gdr::generic_prefill_workspace_bytes(p) : 0;
@@ -112,6 +141,12 @@ gdr_status run(const gdr::Problem &p, Route r, void *ws, cudaStream_t stream) {
         case Route::GenericPrefill:
             e = gdr::launch_generic_prefill(p, ws, stream);
             break;
+        case Route::TensorCorePrefill: {
+            int *err = nullptr;
+            e = gdr::device_error_word(&err);
+            if (e == cudaSuccess) e = gdr::launch_tc_prefill(p, err, stream);
+            break;
+        }
     }
     return e == cudaSuccess ? GDR_OK : cuda_fail(e);
 }

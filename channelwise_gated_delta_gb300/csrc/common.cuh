@@ -77,6 +77,12 @@ struct Problem {
 };
 
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream);
+bool tc_prefill_supported(const Problem &p);
+// api.cu: device address of the library's error word on the current device,
+// and a setter for gdr_last_cuda_error().
+cudaError_t device_error_word(int **out);
+int record_cuda_error(cudaError_t e);
+cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream);
 size_t generic_prefill_workspace_bytes(const Problem &p);
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream);
 }  // namespace gdr

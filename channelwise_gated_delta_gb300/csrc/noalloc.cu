@@ -24,10 +24,6 @@
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GDR_NOALLOC_SCRATCH_BYTES];
 
-namespace gdr {
-int record_cuda_error(cudaError_t e);  // api.cu: remembers e for gdr_last_cuda_error()
-}
-
 namespace {
 
 std::mutex g_noalloc_mutex;

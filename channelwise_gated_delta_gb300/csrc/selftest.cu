@@ -1,0 +1,97 @@
+// selftest.cu -- gdr_selftest_umma: one tensor-core GEMM through the same
+// shared-memory layouts, descriptors, MMA issue and TMEM read-back the
+// prefill kernel uses, so a layout or descriptor fault can be told apart from
+// an algebra fault.  D[128 x N] = A[128 x 64] * B[N x 64]^T, bf16 in, f32 out.
+#include "common.cuh"
+#include "gdr.h"
+#include "sm100_ptx.cuh"
+
+namespace gdr {
+namespace {
+
+using namespace sm100;
+
+constexpr int kM = 128, kK = 64;
+
+__global__ void __launch_bounds__(128, 1)
+    gdr_selftest_umma_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ B,
+                             float *__restrict__ D, int N, int a_mn, int b_mn, int *dev_error) {
+    __shared__ __align__(1024) unsigned char sa[kM * kK * 2];
+    __shared__ __align__(1024) unsigned char sb[128 * kK * 2];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t slot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) tmem_alloc(&slot, 128);
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    // A: element (m, k) -> K-major (row m) or MN-major (k, mn = m) layout
+    for (int idx = tid; idx < kM * kK; idx += 128) {
+        const int m = idx / kK, k = idx % kK;
+        const uint32_t off = a_mn ? mnmajor_off(k, m, kK) : kmajor_off(m, k, kK);
+        *reinterpret_cast<__nv_bfloat16 *>(sa + off) = A[idx];
+    }
+    for (int idx = tid; idx < N * kK; idx += 128) {
+        const int n = idx / kK, k = idx % kK;
+        const uint32_t off = b_mn ? mnmajor_off(k, n, kK) : kmajor_off(n, k, kK);
+        *reinterpret_cast<__nv_bfloat16 *>(sb + off) = B[idx];
+    }
+    fence_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = slot;
+    if (tid == 0) {
+        const uint32_t idesc = idesc_bf16(kM, N, a_mn != 0, b_mn != 0, false);
+        for (int ks = 0; ks < kK / 16; ++ks) {
+            const uint64_t ad = smem_desc(smem_u32(sa) + ks * 256, 128, kK * 16);
+            const uint64_t bd = smem_desc(smem_u32(sb) + ks * 256, 128, kK * 16);
+            mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar);
+    }
+    const bool ok = mbar_wait_bounded(&bar, 0, 2000000000ull);
+    const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    tc_fence_after_sync();
+    if (all_ok) {
+        const int row = 32 * warp + lane;
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            float d[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + c0, d);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) D[row * N + c0 + u] = d[u];
+        }
+    } else if (tid == 0) {
+        atomicOr(dev_error, 1);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N,
+                                                const void *A, const void *B, float *D,
+                                                void *stream) {
+    if (!A || !B || !D) return GDR_ERR_NULL;
+    if (N != 64 && N != 128) return GDR_ERR_UNSUPPORTED;
+    int *err = nullptr;
+    cudaError_t e = gdr::device_error_word(&err);
+    if (e == cudaSuccess) {
+        gdr::gdr_selftest_umma_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, N,
+            a_mn_major != 0, b_mn_major != 0, err);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        gdr::record_cuda_error(e);
+        return GDR_ERR_CUDA;
+    }
+    return GDR_OK;
+}

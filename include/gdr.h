@@ -171,6 +171,18 @@ GDR_API gdr_status gdr_device_check(void *stream);
 GDR_API gdr_status gdr_trace_enable(int on);
 GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, double *total_ms);
 
+/*
+ * Diagnostic: one tensor-core GEMM through the shared-memory operand layouts,
+ * descriptors and TMEM read-back of the tensor-core prefill.
+ * D[128 x N] = A[128 x 64] * B[N x 64]^T with A, B row-major bf16 and D
+ * row-major float32 (device pointers), N in {64, 128}; a_mn_major /
+ * b_mn_major select the MN-major instead of the K-major shared-memory layout
+ * for that operand.  Enqueued on `stream`; a timed-out wait is reported by
+ * gdr_device_check.
+ */
+GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N, const void *A,
+                                     const void *B, float *D, void *stream);
+
 /* Human-readable name of a gdr_status value (static string, never NULL). */
 GDR_API const char *gdr_status_string(int status);
 
