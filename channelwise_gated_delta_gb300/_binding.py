@@ -189,7 +189,7 @@ def gdr_selftest_umma(A, B, a_mn_major=False, b_mn_major=False, stream=None):
     D = torch.empty(A.shape[0], N, dtype=torch.float32, device=A.device)
     if stream is None:
         stream = torch.cuda.current_stream(A.device)
-    st = lib.gdr_selftest_umma(1 if a_mn_major else 0, 1 if b_mn_major else 0, N, _ptr(A),
+    st = lib.gdr_selftest_umma(int(a_mn_major), int(b_mn_major), N, _ptr(A),
                                _ptr(B), _ptr(D), ctypes.c_void_p(stream.cuda_stream))
     _check(lib, st)
     return D

@@ -26,15 +26,21 @@ __global__ void __launch_bounds__(128, 1)
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
-    // A: element (m, k) -> K-major (row m) or MN-major (k, mn = m) layout
+    // Layout modes: 0 = K-major (row m or n), 1 = MN-major, 2 = a K-major tile
+    // of the transpose (rows k, K extent M or N) read back through an MN-major
+    // descriptor with LBO and SBO swapped in role.
     for (int idx = tid; idx < kM * kK; idx += 128) {
         const int m = idx / kK, k = idx % kK;
-        const uint32_t off = a_mn ? mnmajor_off(k, m, kK) : kmajor_off(m, k, kK);
+        const uint32_t off = a_mn == 2   ? kmajor_off(k, m, kM)
+                             : a_mn == 1 ? mnmajor_off(k, m, kK)
+                                         : kmajor_off(m, k, kK);
         *reinterpret_cast<__nv_bfloat16 *>(sa + off) = A[idx];
     }
     for (int idx = tid; idx < N * kK; idx += 128) {
         const int n = idx / kK, k = idx % kK;
-        const uint32_t off = b_mn ? mnmajor_off(k, n, kK) : kmajor_off(n, k, kK);
+        const uint32_t off = b_mn == 2   ? kmajor_off(k, n, N)
+                             : b_mn == 1 ? mnmajor_off(k, n, kK)
+                                         : kmajor_off(n, k, kK);
         *reinterpret_cast<__nv_bfloat16 *>(sb + off) = B[idx];
     }
     fence_async_smem();
@@ -44,9 +50,12 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t tmem = slot;
     if (tid == 0) {
         const uint32_t idesc = idesc_bf16(kM, N, a_mn != 0, b_mn != 0, false);
+        // K-direction / MN-direction core-matrix strides of each operand
+        const uint32_t a_lbo = a_mn == 2 ? kM * 16 : 128, a_sbo = a_mn == 2 ? 128 : kK * 16;
+        const uint32_t b_lbo = b_mn == 2 ? N * 16 : 128, b_sbo = b_mn == 2 ? 128 : kK * 16;
         for (int ks = 0; ks < kK / 16; ++ks) {
-            const uint64_t ad = smem_desc(smem_u32(sa) + ks * 256, 128, kK * 16);
-            const uint64_t bd = smem_desc(smem_u32(sb) + ks * 256, 128, kK * 16);
+            const uint64_t ad = smem_desc(smem_u32(sa) + ks * 2 * a_lbo, a_lbo, a_sbo);
+            const uint64_t bd = smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
             mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
         }
         mma_commit(&bar);
@@ -81,12 +90,14 @@ extern "C" GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, 
                                                 void *stream) {
     if (!A || !B || !D) return GDR_ERR_NULL;
     if (N != 64 && N != 128) return GDR_ERR_UNSUPPORTED;
+    if (a_mn_major < 0 || a_mn_major > 2 || b_mn_major < 0 || b_mn_major > 2)
+        return GDR_ERR_UNSUPPORTED;
     int *err = nullptr;
     cudaError_t e = gdr::device_error_word(&err);
     if (e == cudaSuccess) {
         gdr::gdr_selftest_umma_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
             static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, N,
-            a_mn_major != 0, b_mn_major != 0, err);
+            a_mn_major, b_mn_major, err);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {

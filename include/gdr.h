@@ -175,9 +175,11 @@ GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, d
  * Diagnostic: one tensor-core GEMM through the shared-memory operand layouts,
  * descriptors and TMEM read-back of the tensor-core prefill.
  * D[128 x N] = A[128 x 64] * B[N x 64]^T with A, B row-major bf16 and D
- * row-major float32 (device pointers), N in {64, 128}; a_mn_major /
- * b_mn_major select the MN-major instead of the K-major shared-memory layout
- * for that operand.  Enqueued on `stream`; a timed-out wait is reported by
+ * row-major float32 (device pointers), N in {64, 128}.  a_mn_major /
+ * b_mn_major pick the shared-memory layout of that operand: 0 K-major,
+ * 1 MN-major, 2 a K-major tile of the transposed operand read through an
+ * MN-major descriptor (the way the prefill reuses one tile for both
+ * orientations).  Enqueued on `stream`; a timed-out wait is reported by
  * gdr_device_check.
  */
 GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N, const void *A,
