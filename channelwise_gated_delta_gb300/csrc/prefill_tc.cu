@@ -45,10 +45,16 @@
 // core-matrix layout (sm100_ptx.cuh); each of Lk, Lq and R is stored once
 // and read both K-major and, through an MN-major descriptor with the two
 // core-matrix strides exchanged, transposed.  Accumulators are float32 in
-// TMEM.  The next chunk's inputs are fetched with cp.async while the current
-// chunk's solve and state products run.  The 64 x 64 inverse runs in
-// float32: diagonal blocks by a right-looking sweep per column, off-diagonal
-// blocks by tf32 mma.sync 16 x 16 products.
+// TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
+// swizzled boxes; rows past the end of the sequence are zero-filled by the
+// copy engine), the next chunk's copies in flight while the current chunk's
+// solve and state products run; v lands directly in the swizzled MN-major
+// layout the tensor core reads.  The 64 x 64 inverse runs in float32:
+// diagonal 16 x 16 blocks by a right-looking sweep (four threads per
+// column), off-diagonal blocks one block column per warp with tf32 mma.sync.
+#include <cuda.h>
+#include <mutex>
+
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -61,13 +67,13 @@ constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
 constexpr int kThreads = 256;
 constexpr float kRangeNats = 80.f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per MMA batch
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
-// ---- shared memory map (bytes)
-constexpr uint32_t kRawK = 0;                 // bf16 [64][128], 16-byte chunks XOR-swizzled by row
-constexpr uint32_t kRawQ = kRawK + 16384;     // same for q
-constexpr uint32_t kOpV = kRawQ + 16384;      // V as MN-major A (k = s, mn = j), K extent 64
-constexpr uint32_t kG = kOpV + 16384;         // f32 [64][128], 16-byte chunks XOR-swizzled by row
+// ---- shared memory map (bytes from a 1024-byte aligned base)
+constexpr uint32_t kRawK = 0;                 // k: 2 TMA boxes [64 rows][64 bf16], 128B-swizzled
+constexpr uint32_t kRawQ = kRawK + 16384;     // q: same
+constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
+constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
 constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lk, 64-127 Lq
 constexpr uint32_t kOpR = kOpL + 32768;       // [64][128] K-major: R
 constexpr uint32_t kAT = kOpR + 16384;        // 32 KB: f32 A and T (64x64 each), later S'^T
@@ -85,12 +91,19 @@ constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (double-buffered)
 constexpr uint32_t kEGm = kBeta + 512;        // f32 [128] exp(G_m)
 constexpr uint32_t kCL = kEGm + 512;          // f32 [128] exp(G_last - G_m)
 constexpr uint32_t kGamL = kCL + 512;         // f32 [128] exp(G_last)
-constexpr uint32_t kGm = kGamL + 512;         // f32 [128] G_m
-constexpr uint32_t kTot = kGm + 512;          // f32 [128] prefix-sum carry
-constexpr uint32_t kBar = kTot + 512;         // mbarrier (8 B)
-constexpr uint32_t kTmemSlot = kBar + 8;      // u32
-constexpr uint32_t kSmemBytes = kTmemSlot + 8;
+constexpr uint32_t kGm = kGamL + 512;         // f32 [128] G_m (raw reference row)
+constexpr uint32_t kGl = kGm + 512;           // f32 [128] G_last
+constexpr uint32_t kTot = kGl + 512;          // f32 [128] prefix-sum carry
+constexpr uint32_t kBarMma = kTot + 512;      // mbarrier: MMA batches
+constexpr uint32_t kBarKQG = kBarMma + 8;     // mbarrier: k, q, g tiles
+constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
+constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
+constexpr uint32_t kAbort = kTmemSlot + 4;    // i32 sticky abort flag
+constexpr uint32_t kSmemUsed = kAbort + 4;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack for the 1024-byte base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kBytesKQG = 16384 + 16384 + 32768;
+constexpr uint32_t kBytesV = 16384;
 
 // ---- TMEM columns (float32 accumulators, lane = M row)
 constexpr uint32_t kTmGram = 0;     // [128 x 64]: rows 0-63 Lk R^T, 64-127 Lq R^T
@@ -103,13 +116,13 @@ constexpr uint32_t kTmemCols = 512;
 // 64 x 64 f32 tiles (A, T) with an XOR swizzle: rows and columns both walk
 // conflict-free
 __device__ __forceinline__ int sq_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
-// raw bf16 [64][128]: element offset of (r, i)
-__device__ __forceinline__ int rawkq_idx(int r, int i) {
-    return r * 128 + ((((i >> 3) ^ (r & 7))) << 3) + (i & 7);
+// byte offset of bf16 element (r, i) of a k or q tile (two 64-channel boxes)
+__device__ __forceinline__ uint32_t kq_off(int r, int i) {
+    return (uint32_t)((i >> 6) * 8192 + r * 128 + ((((i & 63) >> 3) ^ (r & 7)) << 4) + (i & 7) * 2);
 }
-// G f32 [64][128]: element offset of (r, i)
-__device__ __forceinline__ int g_idx(int r, int i) {
-    return r * 128 + ((((i >> 2) ^ (r & 7))) << 2) + (i & 3);
+// byte offset of f32 element (r, i) of the g tile (four 32-channel boxes)
+__device__ __forceinline__ uint32_t g_off(int r, int i) {
+    return (uint32_t)((i >> 5) * 8192 + r * 128 + ((((i & 31) >> 2) ^ (r & 7)) << 4) + (i & 3) * 4);
 }
 
 __device__ __forceinline__ uint4 pack_bf16x8(const float *x) {
@@ -134,6 +147,10 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 u, float *x) {
         x[2 * e + 1] = f.y;
     }
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 
 // Issues the K-steps of one GEMM, D (+)= A * B^T, each K-step of 16
 // advancing the operand start addresses by two core matrices along K.
@@ -148,13 +165,12 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_addr, uint32_t 
     }
 }
 
-// Waits for the CTA's MMA batch; false (uniform across the CTA) on timeout.
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase) {
-    const bool ok = mbar_wait_bounded(bar, phase, kWaitLimitNs);
-    phase ^= 1u;
-    const int any_fail = __syncthreads_or(ok ? 0 : 1);
-    tc_fence_after_sync();
-    return any_fail == 0;
+// Bounded wait on an mbarrier phase.  A timeout sets the CTA's sticky abort
+// flag; later waits then return at once, and the chunk loop ends at its next
+// barrier, so a stuck copy or MMA can never hang the kernel.
+__device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (*abort_flag) return;
+    if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) *abort_flag = 1;
 }
 
 // ---- tf32 mma.sync for the 16 x 16 block products of the inverse
@@ -172,67 +188,37 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Issues the cp.async copies of one chunk's k, q, g rows (rows >= L zeroed).
-__device__ __forceinline__ void load_kqg(unsigned char *smem, const __nv_bfloat16 *k,
-                                         const __nv_bfloat16 *q, const float *g, int b, int T,
-                                         int t0, int L, int HK, int HV, int hk, int hv, int tid) {
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+struct TileMaps {
+    CUtensorMap k, q, g, v;
+};
+
+// One elected thread: the k, q and g boxes of one chunk (tokens t0 .. t0+63).
+__device__ __forceinline__ void issue_kqg(unsigned char *sm, const TileMaps &tm, uint64_t *bar,
+                                          int b, int t0, int hk, int hv) {
+    mbar_arrive_expect_tx(bar, kBytesKQG);
+    tma_load_4d(sm + kRawK, &tm.k, 0, hk, t0, b, bar);
+    tma_load_4d(sm + kRawK + 8192, &tm.k, 64, hk, t0, b, bar);
+    tma_load_4d(sm + kRawQ, &tm.q, 0, hk, t0, b, bar);
+    tma_load_4d(sm + kRawQ + 8192, &tm.q, 64, hk, t0, b, bar);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int id = tid + kThreads * it;  // 0..1023
-        const int r = id >> 4, cc = id & 15;
-        const int pc = cc ^ (r & 7);
-        unsigned char *dk_ = smem + kRawK + r * 256 + pc * 16;
-        unsigned char *dq_ = smem + kRawQ + r * 256 + pc * 16;
-        if (r < L) {
-            const size_t tk = ((size_t)b * T + t0 + r) * HK + hk;
-            cp_async16(dk_, k + tk * kD + cc * 8);
-            cp_async16(dq_, q + tk * kD + cc * 8);
-        } else {
-            *reinterpret_cast<uint4 *>(dk_) = zero4;
-            *reinterpret_cast<uint4 *>(dq_) = zero4;
-        }
-    }
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int id = tid + kThreads * it;  // 0..2047
-        const int r = id >> 5, cc = id & 31;
-        unsigned char *dg = smem + kG + r * 512 + ((cc ^ (r & 7)) * 16);
-        if (r < L)
-            cp_async16(dg, g + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 4);
-        else
-            *reinterpret_cast<uint4 *>(dg) = zero4;
-    }
+    for (int x = 0; x < 4; ++x) tma_load_4d(sm + kG + 8192 * x, &tm.g, 32 * x, hv, t0, b, bar);
 }
-__device__ __forceinline__ void load_v(unsigned char *smem, const __nv_bfloat16 *v, int b, int T,
-                                       int t0, int L, int HV, int hv, int tid) {
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int id = tid + kThreads * it;
-        const int r = id >> 4, cc = id & 15;
-        unsigned char *dv_ = smem + kOpV + mnmajor_off(r, cc * 8, kC);
-        if (r < L)
-            cp_async16(dv_, v + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8);
-        else
-            *reinterpret_cast<uint4 *>(dv_) = zero4;
-    }
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait0() {
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, uint64_t *bar, int b,
+                                        int t0, int hv) {
+    mbar_arrive_expect_tx(bar, kBytesV);
+    tma_load_4d(sm + kOpV, &tm.v, 0, hv, t0, b, bar);
+    tma_load_4d(sm + kOpV + 8192, &tm.v, 64, hv, t0, b, bar);
 }
 
 template <bool HAS_H0, bool STORE_HT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdr_prefill_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                          const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-                          const float *__restrict__ beta, const float *h0,
-                          __nv_bfloat16 *__restrict__ out, float *ht, int T, int HK, int HV,
-                          int *dev_error) {
-    extern __shared__ __align__(1024) unsigned char smem[];
+    gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const float *__restrict__ beta,
+                          const float *h0, __nv_bfloat16 *__restrict__ out, float *ht, int T,
+                          int HK, int HV, int *dev_error) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
+    unsigned char *smem =
+        smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wq = warp & 3;        // TMEM lane quarter of this warp
@@ -246,30 +232,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sCL = reinterpret_cast<float *>(smem + kCL);
     float *sGamL = reinterpret_cast<float *>(smem + kGamL);
     float *sGm = reinterpret_cast<float *>(smem + kGm);
+    float *sGl = reinterpret_cast<float *>(smem + kGl);
     float *sTot = reinterpret_cast<float *>(smem + kTot);
-    float *sG = reinterpret_cast<float *>(smem + kG);
     float *sA = reinterpret_cast<float *>(smem + kA32);
     float *sT = reinterpret_cast<float *>(smem + kT32);
     float *sX = reinterpret_cast<float *>(smem + kX32);
-    const __nv_bfloat16 *rawk = reinterpret_cast<const __nv_bfloat16 *>(smem + kRawK);
-    const __nv_bfloat16 *rawq = reinterpret_cast<const __nv_bfloat16 *>(smem + kRawQ);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBar);
+    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(smem + kBarMma);
+    uint64_t *bar_kqg = reinterpret_cast<uint64_t *>(smem + kBarKQG);
+    uint64_t *bar_v = reinterpret_cast<uint64_t *>(smem + kBarV);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kAbort);
+    auto gval = [&](int r, int i) -> float {
+        return *reinterpret_cast<const float *>(smem + kG + g_off(r, i));
+    };
+    auto kval = [&](uint32_t base, int r, int i) -> float {
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + base + kq_off(r, i)));
+    };
 
+    const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_kqg, 1);
+        mbar_init(bar_v, 1);
+        *abort_flag = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&tm.k);
+        tma_prefetch_desc(&tm.q);
+        tma_prefetch_desc(&tm.g);
+        tma_prefetch_desc(&tm.v);
     }
-    const int NC = (T + kC - 1) / kC;
-    // first chunk's inputs
+    __syncthreads();
+    if (tid == 0) {  // first chunk's inputs
+        issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv);
+        issue_v(smem, tm, bar_v, b, 0, hv);
+    }
     {
-        const int L0 = min(kC, T);
-        load_kqg(smem, k, q, g, b, T, 0, L0, HK, HV, hk, hv, tid);
-        load_v(smem, v, b, T, 0, L0, HV, hv, tid);
-        cp_async_commit();
         float *sb0 = reinterpret_cast<float *>(smem + kBeta);
+        const int L0 = min(kC, T);
         if (tid < kC) sb0[tid] = tid < L0 ? beta[((size_t)b * T + tid) * HV + hv] : 0.f;
+    }
+    // T' is lower triangular: its strictly-upper 16 x 16 blocks stay zero
+    for (int idx = tid; idx < 64 * 8; idx += kThreads) {
+        const int r = idx >> 3, s0 = (idx & 7) * 8;
+        if ((s0 >> 4) > (r >> 4))
+            *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
     // state: S[64*ih + u][j], u = 0..63
     float S[64];
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
-    uint32_t phase = 0;
-    bool aborted = false;
+    uint32_t mma_phase = 0;
+    int issued_kqg = 1, issued_v = 1;  // loads issued so far (thread 0's view is authoritative)
 
     for (int c = 0; c < NC; ++c) {
         const int t0 = c * kC;
@@ -291,17 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *sbeta = reinterpret_cast<const float *>(smem + kBeta + 256 * (c & 1));
         const bool has_next = c + 1 < NC;
         const int t0n = t0 + kC;
-        const int Ln = has_next ? min(kC, T - t0n) : 0;
 
-        cp_async_wait0();
+        wait_bar(bar_kqg, (uint32_t)(c & 1), abort_flag);
         __syncthreads();
+        if (*abort_flag) break;
 
         // ---------------- per-channel prefix sums of g (two halves of 32 rows)
         {
             const int i = tid & 127, hh = tid >> 7;
             float x[32];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) x[r] = sG[g_idx(32 * hh + r, i)];
+            for (int r = 0; r < 32; ++r) x[r] = gval(32 * hh + r, i);
 #pragma unroll
             for (int r = 1; r < 32; ++r) x[r] += x[r - 1];
             if (hh == 0) sTot[i] = x[31];
@@ -312,27 +319,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < 32; ++r) x[r] += carry;
             }
 #pragma unroll
-            for (int r = 0; r < 32; ++r) sG[g_idx(32 * hh + r, i)] = x[r];
+            for (int r = 0; r < 32; ++r)
+                *reinterpret_cast<float *>(smem + kG + g_off(32 * hh + r, i)) = x[r];
         }
         __syncthreads();
+        // reference-row and last-row values, then the range check
         int bad = 0;
         if (tid < kD) {
-            const int i = tid;
-            const float g0 = sG[g_idx(0, i)], gm = sG[g_idx(m, i)], gl = sG[g_idx(L - 1, i)];
-            bad = (g0 - gm > kRangeNats) || (gm - gl > kRangeNats);
-            sGm[i] = gm;
-            sGamL[i] = __expf(gl);
+            const float gm = gval(m, tid), gl = gval(L - 1, tid);
+            sGm[tid] = gm;
+            sGl[tid] = gl;
+            bad = (gval(0, tid) - gm > kRangeNats) || (gm - gl > kRangeNats);
         }
         const bool slow = __syncthreads_or(bad) != 0;
         if (tid < kD) {
             // the fallback factorises around the chunk start (G_m = 0) and
             // stores R with the full decay to the chunk end (scale 1)
-            const float gm = slow ? 0.f : sGm[tid];
-            sGm[tid] = gm;
+            const float gm = slow ? 0.f : sGm[tid], gl = sGl[tid];
             sEGm[tid] = slow ? 1.f : __expf(gm);
-            sCL[tid] = slow ? 1.f : __expf(sG[g_idx(L - 1, tid)] - gm);
+            sCL[tid] = slow ? 1.f : __expf(gl - gm);
+            sGamL[tid] = __expf(gl);
         }
-        __syncthreads();
 
         // ---------------- operands Lk, Lq, R (bf16, K-major core-matrix tiles)
 #pragma unroll 2
@@ -342,29 +349,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = ((id >> 7) << 3) | r8;
             const int c8 = (id >> 3) & 15;
             const int ch = c8 * 8;
-            float kv[8], qv[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + r * 256 + ((c8 ^ r8) << 4)), kv);
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + r * 256 + ((c8 ^ r8) << 4)), qv);
-            const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + r * 512 + (((2 * c8) ^ r8) << 4));
-            const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + r * 512 + (((2 * c8 + 1) ^ r8) << 4));
-            const float4 m_lo = *reinterpret_cast<const float4 *>(sGm + ch);
-            const float4 m_hi = *reinterpret_cast<const float4 *>(sGm + ch + 4);
-            const float d[8] = {g_lo.x - m_lo.x, g_lo.y - m_lo.y, g_lo.z - m_lo.z, g_lo.w - m_lo.w,
-                                g_hi.x - m_hi.x, g_hi.y - m_hi.y, g_hi.z - m_hi.z, g_hi.w - m_hi.w};
+            float kv[8], qv[8], gv[8], gm[8];
+            const uint32_t kqo = (uint32_t)((c8 >> 3) * 8192 + r * 128 + (((c8 & 7) ^ r8) << 4));
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kqo), kv);
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kqo), qv);
+            const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
+            const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
+            const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
+            gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
+            gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
+            if (!slow) {
+                const float4 m_lo = *reinterpret_cast<const float4 *>(sGm + ch);
+                const float4 m_hi = *reinterpret_cast<const float4 *>(sGm + ch + 4);
+                gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
+                gm[4] = m_hi.x; gm[5] = m_hi.y; gm[6] = m_hi.z; gm[7] = m_hi.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gm[e] = 0.f;
+            }
             float lk[8], lq[8], rk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float el = __expf(d[e]);
+                const float d = gv[e] - gm[e];
+                const float el = __expf(d);
                 lk[e] = kv[e] * el;
                 lq[e] = qv[e] * el;
-            }
-            if (!slow) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) rk[e] = kv[e] * __expf(-d[e]);
-            } else {
-                // G_m = 0 here, so d = G; R = exp(G_L - G) K directly (factor <= 1)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) rk[e] = kv[e] * __expf(sG[g_idx(L - 1, ch + e)] - d[e]);
+                // fallback: R = exp(G_L - G) K directly (factor <= 1)
+                rk[e] = kv[e] * __expf(slow ? sGl[ch + e] - gv[e] : -d);
             }
             *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
             *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lq);
@@ -373,16 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         __syncthreads();
 
-        // ---------------- MMA batch 1: gram [Lk; Lq] R^T
+        // ---------------- MMA batch 1: gram [Lk; Lq] R^T, then A (f32) and P (bf16)
         if (!slow) {
             if (tid == 0) {
                 tc_fence_after_sync();
                 gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
                      idesc_bf16(128, 64, false, false, false), kD / 16, false);
-                mma_commit(bar);
+                mma_commit(bar_mma);
             }
-            if (!wait_mma(bar, phase)) { aborted = true; break; }
-            // A (f32, beta-folded, strictly lower) and P (bf16, causal)
+            wait_bar(bar_mma, mma_phase, abort_flag);
+            mma_phase ^= 1u;
+            tc_fence_after_sync();
             float dd[32];
             tmem_ld32(tl + kTmGram + 32 * ih, dd);
             const int row = 32 * wq + lane;
@@ -414,10 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float a = 0.f, p = 0.f;
                 if (s <= r && r < L) {
                     for (int i = 0; i < kD; ++i) {
-                        const float e = __expf(sG[g_idx(r, i)] - sG[g_idx(s, i)]);
-                        const float kse = __bfloat162float(rawk[rawkq_idx(s, i)]) * e;
-                        a = fmaf(__bfloat162float(rawk[rawkq_idx(r, i)]), kse, a);
-                        p = fmaf(__bfloat162float(rawq[rawkq_idx(r, i)]), kse, p);
+                        const float e = __expf(gval(r, i) - gval(s, i));
+                        const float kse = kval(kRawK, s, i) * e;
+                        a = fmaf(kval(kRawK, r, i), kse, a);
+                        p = fmaf(kval(kRawQ, r, i), kse, p);
                     }
                 }
                 sA[sq_idx(r, s)] = (s < r) ? sbeta[r] * a : 0.f;
@@ -429,121 +441,127 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // prefetch the next chunk's k, q, g (their buffers are free now)
         if (has_next) {
-            load_kqg(smem, k, q, g, b, T, t0n, Ln, HK, HV, hk, hv, tid);
-            cp_async_commit();
+            if (tid == 0) {
+                issue_kqg(smem, tm, bar_kqg, b, t0n, hk, hv);
+                ++issued_kqg;
+            }
             float *sbn = reinterpret_cast<float *>(smem + kBeta + 256 * ((c + 1) & 1));
+            const int Ln = min(kC, T - t0n);
             if (tid < kC) sbn[tid] = tid < Ln ? beta[((size_t)b * T + t0n + tid) * HV + hv] : 0.f;
         }
 
-        // ---------------- T = (I + A)^-1, diagonal 16 x 16 blocks (right-looking)
-        if (tid < 64) {
-            const int I = tid >> 4, jj = tid & 15;
-            float x[16];
+        // ---------------- T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking,
+        // four threads per column (thread p owns the rows r = p mod 4)
+        {
+            const int I = tid >> 6, jj = (tid >> 2) & 15, p = tid & 3;
+            float x[4];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = (r == jj) ? 1.f : 0.f;
+            for (int q4 = 0; q4 < 4; ++q4) x[q4] = (4 * q4 + p == jj) ? 1.f : 0.f;
 #pragma unroll
             for (int s = 0; s < 15; ++s) {
+                const float xs = __shfl_sync(0xffffffffu, x[s >> 2], (lane & ~3) | (s & 3));
 #pragma unroll
-                for (int r = s + 1; r < 16; ++r)
-                    x[r] = fmaf(-sA[sq_idx(16 * I + r, 16 * I + s)], x[s], x[r]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int r = 4 * q4 + p;
+                    if (r > s) x[q4] = fmaf(-sA[sq_idx(16 * I + r, 16 * I + s)], xs, x[q4]);
+                }
             }
+            __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
+            const float bj = sbeta[16 * I + jj];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[sq_idx(16 * I + r, 16 * I + jj)] = x[r];
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int r = 16 * I + 4 * q4 + p;
+                sT[sq_idx(r, 16 * I + jj)] = x[q4];
+                opt[kmajor_off(r, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x[q4] * bj);
+            }
         }
         __syncthreads();
-        // ---------------- off-diagonal blocks, level by level: T_IJ = -T_II sum_M A_IM T_MJ
-        {
+        // ---------------- off-diagonal blocks: warp J walks block column J,
+        // T_IJ = -T_II sum_{M=J}^{I-1} A_IM T_MJ for I = J+1 .. 3
+        if (warp < 3) {
+            const int J = warp;
             const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll 1
-            for (int dlev = 1; dlev < 4; ++dlev) {
-                if (warp < 4 - dlev) {
-                    const int J = warp, I = J + dlev;
-                    float xc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int M = J; M < I; ++M) {
-#pragma unroll
-                        for (int kh = 0; kh < 2; ++kh) {
-                            const int kc = 16 * M + 8 * kh + tq;
-                            uint32_t a[4];
-                            a[0] = to_tf32(sA[sq_idx(16 * I + gq, kc)]);
-                            a[1] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc)]);
-                            a[2] = to_tf32(sA[sq_idx(16 * I + gq, kc + 4)]);
-                            a[3] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc + 4)]);
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const int n = 16 * J + 8 * nt + gq;
-                                mma_tf32(xc[nt], a, to_tf32(sT[sq_idx(kc, n)]),
-                                         to_tf32(sT[sq_idx(kc + 4, n)]));
-                            }
-                        }
-                    }
-                    float *xs = sX + warp * 256;  // X as f32 [16][16]
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        xs[gq * 16 + 8 * nt + 2 * tq] = xc[nt][0];
-                        xs[gq * 16 + 8 * nt + 2 * tq + 1] = xc[nt][1];
-                        xs[(gq + 8) * 16 + 8 * nt + 2 * tq] = xc[nt][2];
-                        xs[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = xc[nt][3];
-                    }
-                    __syncwarp();
-                    float yc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float *xs = sX + warp * 256;  // X as f32 [16][16]
+            for (int I = J + 1; I < 4; ++I) {
+                float xc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int M = J; M < I; ++M) {
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
-                        const int kc = 16 * I + 8 * kh + tq;
+                        const int kc = 16 * M + 8 * kh + tq;
                         uint32_t a[4];
-                        a[0] = to_tf32(sT[sq_idx(16 * I + gq, kc)]);
-                        a[1] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc)]);
-                        a[2] = to_tf32(sT[sq_idx(16 * I + gq, kc + 4)]);
-                        a[3] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc + 4)]);
+                        a[0] = to_tf32(sA[sq_idx(16 * I + gq, kc)]);
+                        a[1] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc)]);
+                        a[2] = to_tf32(sA[sq_idx(16 * I + gq, kc + 4)]);
+                        a[3] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc + 4)]);
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
-                            const int kx = 8 * kh + tq, n = 8 * nt + gq;
-                            mma_tf32(yc[nt], a, to_tf32(xs[kx * 16 + n]), to_tf32(xs[(kx + 4) * 16 + n]));
+                            const int n = 16 * J + 8 * nt + gq;
+                            mma_tf32(xc[nt], a, to_tf32(sT[sq_idx(kc, n)]),
+                                     to_tf32(sT[sq_idx(kc + 4, n)]));
                         }
                     }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    xs[gq * 16 + 8 * nt + 2 * tq] = xc[nt][0];
+                    xs[gq * 16 + 8 * nt + 2 * tq + 1] = xc[nt][1];
+                    xs[(gq + 8) * 16 + 8 * nt + 2 * tq] = xc[nt][2];
+                    xs[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = xc[nt][3];
+                }
+                __syncwarp();
+                float yc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kh = 0; kh < 2; ++kh) {
+                    const int kc = 16 * I + 8 * kh + tq;
+                    uint32_t a[4];
+                    a[0] = to_tf32(sT[sq_idx(16 * I + gq, kc)]);
+                    a[1] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc)]);
+                    a[2] = to_tf32(sT[sq_idx(16 * I + gq, kc + 4)]);
+                    a[3] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc + 4)]);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        const int col = 16 * J + 8 * nt + 2 * tq;
-                        sT[sq_idx(16 * I + gq, col)] = -yc[nt][0];
-                        sT[sq_idx(16 * I + gq, col + 1)] = -yc[nt][1];
-                        sT[sq_idx(16 * I + gq + 8, col)] = -yc[nt][2];
-                        sT[sq_idx(16 * I + gq + 8, col + 1)] = -yc[nt][3];
+                        const int kx = 8 * kh + tq, n = 8 * nt + gq;
+                        mma_tf32(yc[nt], a, to_tf32(xs[kx * 16 + n]), to_tf32(xs[(kx + 4) * 16 + n]));
                     }
                 }
-                __syncthreads();
-            }
-        }
-        // T' = T diag(beta) as bf16 (zero above the diagonal)
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int id = tid + kThreads * it;  // 0..511
-            const int r = id & 63, s0 = (id >> 6) * 8;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = s0 + e;
-                x[e] = (s <= r) ? sT[sq_idx(r, s)] * sbeta[s] : 0.f;
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * J + 8 * nt + 2 * tq;
+                    const float b0 = sbeta[col], b1 = sbeta[col + 1];
+                    sT[sq_idx(16 * I + gq, col)] = -yc[nt][0];
+                    sT[sq_idx(16 * I + gq, col + 1)] = -yc[nt][1];
+                    sT[sq_idx(16 * I + gq + 8, col)] = -yc[nt][2];
+                    sT[sq_idx(16 * I + gq + 8, col + 1)] = -yc[nt][3];
+                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
+                        pack_bf16x2(-yc[nt][0] * b0, -yc[nt][1] * b1);
+                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
+                        pack_bf16x2(-yc[nt][2] * b0, -yc[nt][3] * b1);
+                }
+                __syncwarp();
             }
-            *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = pack_bf16x8(x);
         }
         fence_async_smem();
         __syncthreads();
 
         // ---------------- MMA batch 2: (T'Lk)^T = Lk^T T'^T,  U^T = V^T T'^T
+        wait_bar(bar_v, (uint32_t)(c & 1), abort_flag);
         if (tid == 0) {
             tc_fence_after_sync();
             // Lk read transposed: MN-major (k = s, mn = i), K-direction stride 2048, MN 128
             gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
                  idesc_bf16(128, 64, true, false, false), kC / 16, false);
-            gemm(tmem + kTmUT, sbase + kOpV, 128, kC * 16, sbase + kOpT, 128, kC * 16,
-                 idesc_bf16(128, 64, true, false, false), kC / 16, false);
-            mma_commit(bar);
+            // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
+            const uint32_t vid = idesc_bf16(128, 64, true, false, false);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
+                         smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid, ks > 0 ? 1u : 0u);
+            mma_commit(bar_mma);
         }
-        if (!wait_mma(bar, phase)) { aborted = true; break; }
-        // prefetch the next chunk's v (its buffer is free now)
-        if (has_next) {
-            load_v(smem, v, b, T, t0n, Ln, HV, hv, tid);
-            cp_async_commit();
-        }
+        wait_bar(bar_mma, mma_phase, abort_flag);
+        mma_phase ^= 1u;
+        tc_fence_after_sync();
+        // all threads are past the batch-2 wait once this barrier completes:
+        // v's buffer is free for the next chunk's copy
         {
             float dd[32];
             tmem_ld32(tl + kTmWkT + 32 * ih, dd);  // row i = this lane, columns r
@@ -568,14 +586,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---------------- MMA batch 3: U^T -= S'^T (T'Lk)^T,  O^T = S'^T Lq^T
         if (tid == 0) {
+            if (has_next) {  // batch 2 is done, so v's buffer is free
+                issue_v(smem, tm, bar_v, b, t0n, hv);
+                ++issued_v;
+            }
             tc_fence_after_sync();
             gemm(tmem + kTmUT, sbase + kOpST, 128, kD * 16, sbase + kOpWK, 128, kD * 16,
                  idesc_bf16(128, 64, false, true, true), kD / 16, true);
             gemm(tmem + kTmOT, sbase + kOpST, 128, kD * 16, sbase + kOpL + 16384, 128, kD * 16,
                  idesc_bf16(128, 64, false, false, false), kD / 16, false);
-            mma_commit(bar);
+            mma_commit(bar_mma);
         }
-        if (!wait_mma(bar, phase)) { aborted = true; break; }
+        wait_bar(bar_mma, mma_phase, abort_flag);
+        mma_phase ^= 1u;
+        tc_fence_after_sync();
         {
             float dd[32];
             tmem_ld32(tl + kTmUT + 32 * ih, dd);
@@ -595,9 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                  idesc_bf16(128, 64, false, false, false), kC / 16, true);
             gemm(tmem + kTmDS, sbase + kOpUT, 128, kC * 16, sbase + kOpR, kD * 16, 128,
                  idesc_bf16(128, 128, false, true, false), kC / 16, false);
-            mma_commit(bar);
+            mma_commit(bar_mma);
         }
-        if (!wait_mma(bar, phase)) { aborted = true; break; }
+        wait_bar(bar_mma, mma_phase, abort_flag);
+        mma_phase ^= 1u;
+        tc_fence_after_sync();
         {
             float dd[32];
             tmem_ld32(tl + kTmDS + 64 * ih, dd);
@@ -631,10 +657,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    cp_async_wait0();
-    if (aborted) {
-        if (tid == 0) atomicOr(dev_error, 1);
-    } else if (STORE_HT) {
+    __syncthreads();
+    const bool aborted = *abort_flag != 0;
+    if (tid == 0 && aborted) {
+        // never leave with copies in flight: wait (bounded) for the last copy
+        // issued on each barrier; its phases complete in order
+        atomicOr(dev_error, 1);
+        mbar_wait_bounded(bar_kqg, (uint32_t)((issued_kqg - 1) & 1), kWaitLimitNs);
+        mbar_wait_bounded(bar_v, (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
+    }
+    if (!aborted && STORE_HT) {
 #pragma unroll
         for (int u = 0; u < 64; ++u) ht[((size_t)head * kD + 64 * ih + u) * kD + j] = S[u];
     }
@@ -646,6 +678,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---- host side: TMA tensor maps, encoded per call through the driver entry point
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(cudaError_t *err) {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static cudaError_t status = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                  cudaEnableDefault, &q);
+        if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    *err = status;
+    return fn;
+}
+
+// [B][T][H][128] tensor of `esize`-byte elements; boxes of `box_inner`
+// elements x 64 tokens, 128-byte swizzled, zero fill outside the tensor.
+bool encode_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
+                int esize, int B, int T, int H, int box_inner) {
+    const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)128 * esize, (cuuint64_t)H * 128 * esize,
+                                   (cuuint64_t)T * H * 128 * esize};
+    const cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 64, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_prefill_supported(const Problem &p) {
@@ -655,17 +723,23 @@ bool tc_prefill_supported(const Problem &p) {
 cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.HV;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+    cudaError_t e = cudaSuccess;
+    EncodeTiledFn fn = encode_fn(&e);
+    if (e != cudaSuccess) return e;
+    TileMaps tm;
+    if (!encode_map(fn, &tm.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
+        !encode_map(fn, &tm.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
+        !encode_map(fn, &tm.g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.HV, 32) ||
+        !encode_map(fn, &tm.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 64))
+        return cudaErrorInvalidValue;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
     auto run = [&](auto kernel) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSmemBytes);
+        if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
-        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(q, k, v, p.g, p.beta, p.h0, out,
-                                                                  p.ht, p.T, p.HK, p.HV, dev_error);
+        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, p.beta, p.h0, out, p.ht,
+                                                                  p.T, p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };

@@ -31,14 +31,16 @@ __global__ void __launch_bounds__(128, 1)
     // descriptor with LBO and SBO swapped in role.
     for (int idx = tid; idx < kM * kK; idx += 128) {
         const int m = idx / kK, k = idx % kK;
-        const uint32_t off = a_mn == 2   ? kmajor_off(k, m, kM)
+        const uint32_t off = a_mn == 3   ? sw128_mnmajor_off(k, m, kK)
+                             : a_mn == 2 ? kmajor_off(k, m, kM)
                              : a_mn == 1 ? mnmajor_off(k, m, kK)
                                          : kmajor_off(m, k, kK);
         *reinterpret_cast<__nv_bfloat16 *>(sa + off) = A[idx];
     }
     for (int idx = tid; idx < N * kK; idx += 128) {
         const int n = idx / kK, k = idx % kK;
-        const uint32_t off = b_mn == 2   ? kmajor_off(k, n, N)
+        const uint32_t off = b_mn == 3   ? sw128_mnmajor_off(k, n, kK)
+                             : b_mn == 2 ? kmajor_off(k, n, N)
                              : b_mn == 1 ? mnmajor_off(k, n, kK)
                                          : kmajor_off(n, k, kK);
         *reinterpret_cast<__nv_bfloat16 *>(sb + off) = B[idx];
@@ -54,8 +56,13 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t a_lbo = a_mn == 2 ? kM * 16 : 128, a_sbo = a_mn == 2 ? 128 : kK * 16;
         const uint32_t b_lbo = b_mn == 2 ? N * 16 : 128, b_sbo = b_mn == 2 ? 128 : kK * 16;
         for (int ks = 0; ks < kK / 16; ++ks) {
-            const uint64_t ad = smem_desc(smem_u32(sa) + ks * 2 * a_lbo, a_lbo, a_sbo);
-            const uint64_t bd = smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
+            // swizzled MN-major: 64-element blocks of kK rows (LBO), 8-row atoms (SBO)
+            const uint64_t ad =
+                a_mn == 3 ? smem_desc_sw128(smem_u32(sa) + ks * 2048, kK * 128, 1024)
+                          : smem_desc(smem_u32(sa) + ks * 2 * a_lbo, a_lbo, a_sbo);
+            const uint64_t bd =
+                b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
+                          : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
             mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
         }
         mma_commit(&bar);
@@ -90,7 +97,7 @@ extern "C" GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, 
                                                 void *stream) {
     if (!A || !B || !D) return GDR_ERR_NULL;
     if (N != 64 && N != 128) return GDR_ERR_UNSUPPORTED;
-    if (a_mn_major < 0 || a_mn_major > 2 || b_mn_major < 0 || b_mn_major > 2)
+    if (a_mn_major < 0 || a_mn_major > 3 || b_mn_major < 0 || b_mn_major > 3)
         return GDR_ERR_UNSUPPORTED;
     int *err = nullptr;
     cudaError_t e = gdr::device_error_word(&err);

@@ -45,6 +45,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)1u << 46;
     return d;
 }
+// Same with the 128-byte swizzle (layout type 2): rows of 128 bytes in atoms
+// of 8 rows (1024 bytes, 1024-byte aligned), the 16-byte chunk index XORed
+// with the row index within the atom -- the layout a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_128B writes.  For an MN-major operand: 64 contiguous
+// M/N elements per 128-byte row, one K index per row; SBO = 1024 (next 8 K
+// rows), LBO = stride between 64-element M/N blocks.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo) | ((uint64_t)2u << 61);
+}
+// Byte offset of element (k, mn) in an MN-major 128-byte-swizzled bf16 tile
+// made of 64-element M/N blocks of `k_extent` rows each.
+__device__ __forceinline__ uint32_t sw128_mnmajor_off(int k, int mn, int k_extent) {
+    return (uint32_t)((mn >> 6) * (k_extent * 128) + k * 128 +
+                      ((((mn & 63) >> 3) ^ (k & 7)) << 4) + (mn & 7) * 2);
+}
 
 // Instruction descriptor for kind::f16 with bf16 A and B, f32 accumulator:
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
@@ -154,6 +169,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// ---- TMA: one box of a 4-D tensor map into shared memory, completion
+// counted in bytes on the mbarrier.  Coordinates are element indices,
+// innermost first; rows outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, int c0, int c1,
+                                            int c2, int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
 // ---- cp.async (16-byte global -> shared copies)

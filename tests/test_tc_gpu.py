@@ -13,8 +13,8 @@ from tests.test_parity_gpu import check, run_gpu, run_oracle
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("a_mn", [0, 1, 2])
-@pytest.mark.parametrize("b_mn", [0, 1, 2])
+@pytest.mark.parametrize("a_mn", [0, 1, 2, 3])
+@pytest.mark.parametrize("b_mn", [0, 1, 2, 3])
 @pytest.mark.parametrize("N", [64, 128])
 def test_umma_gemm_layouts(a_mn, b_mn, N):
     """One tcgen05 GEMM per operand layout: bf16 products summed in f32 are
