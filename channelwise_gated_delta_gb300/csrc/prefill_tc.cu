@@ -36,9 +36,9 @@
 // factors <= 1) and computes A and P with exact pairwise decays on CUDA
 // cores, so the result is right for any g <= 0.
 //
-// GB300 mapping.  One CTA (8 warps) per (batch, value head) walks that head's
-// chunks in order; the float32 state never leaves registers (thread = one
-// value column j, 64 of the 128 key rows).  State products are computed
+// GB300 mapping.  One CTA (16 warps) per (batch, value head) walks that
+// head's chunks in order; the float32 state never leaves registers (thread =
+// one value column j, 32 of the 128 key rows).  State products are computed
 // transposed so that M = dv = 128 fills the MMA:
 //   U^T = (T'V)^T - S'^T (T'Lk)^T,  O^T = S'^T Lq^T + U^T P^T,  dS^T = U^T R.
 // Operands are bf16 tiles in shared memory in the interleaved (no-swizzle)
@@ -50,8 +50,9 @@
 // copy engine), the next chunk's copies in flight while the current chunk's
 // solve and state products run; v lands directly in the swizzled MN-major
 // layout the tensor core reads.  The 64 x 64 inverse runs in float32:
-// diagonal 16 x 16 blocks by a right-looking sweep (four threads per
-// column), off-diagonal blocks one block column per warp with tf32 mma.sync.
+// diagonal 16 x 16 blocks by a right-looking sweep (eight threads per
+// column), off-diagonal blocks by a 32 x 32 block recursion whose 16 x 16
+// products run on tf32 mma.sync, two or four warps per level.
 #include <cuda.h>
 #include <mutex>
 
@@ -65,7 +66,7 @@ using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps
 constexpr float kRangeNats = 80.f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -85,7 +86,7 @@ constexpr uint32_t kOpP = kOpT + 8192;        // P as K-major B [64 r][64 s]
 constexpr uint32_t kOpWK = kOpP + 8192;       // (T'Lk) as MN-major B (k = i, mn = r), K extent 128
 constexpr uint32_t kStage = kOpWK;            //   later: bf16 O [64][128] staging for the stores
 constexpr uint32_t kOpUT = kOpWK + 16384;     // U^T as K-major A [128 j][64 r]
-constexpr uint32_t kX32 = kOpUT;              //   earlier: f32 [3][16][16] solve scratch
+constexpr uint32_t kX32 = kOpUT;              //   earlier: f32 [4][16][16] solve scratch
 constexpr uint32_t kSmall = kOpUT + 16384;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (double-buffered)
 constexpr uint32_t kEGm = kBeta + 512;        // f32 [128] exp(G_m)
@@ -93,8 +94,8 @@ constexpr uint32_t kCL = kEGm + 512;          // f32 [128] exp(G_last - G_m)
 constexpr uint32_t kGamL = kCL + 512;         // f32 [128] exp(G_last)
 constexpr uint32_t kGm = kGamL + 512;         // f32 [128] G_m (raw reference row)
 constexpr uint32_t kGl = kGm + 512;           // f32 [128] G_last
-constexpr uint32_t kTot = kGl + 512;          // f32 [128] prefix-sum carry
-constexpr uint32_t kBarMma = kTot + 512;      // mbarrier: MMA batches
+constexpr uint32_t kTot = kGl + 512;          // f32 [3][128] prefix-sum carries
+constexpr uint32_t kBarMma = kTot + 1536;     // mbarrier: MMA batches
 constexpr uint32_t kBarKQG = kBarMma + 8;     // mbarrier: k, q, g tiles
 constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
 constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
@@ -210,6 +211,36 @@ __device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, u
     tma_load_4d(sm + kOpV + 8192, &tm.v, 64, hv, t0, b, bar);
 }
 
+// One warp: acc (16 x 16, two m16n8 C tiles) += X * Y for 16 x 16 f32 blocks,
+// in tf32.  X and Y are read through index functors (row, col) -> float.
+template <typename FX, typename FY>
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], FX X, FY Y, int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh) {
+        const int kc = 8 * kh + tq;
+        uint32_t a[4];
+        a[0] = to_tf32(X(gq, kc));
+        a[1] = to_tf32(X(gq + 8, kc));
+        a[2] = to_tf32(X(gq, kc + 4));
+        a[3] = to_tf32(X(gq + 8, kc + 4));
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            mma_tf32(acc[nt], a, to_tf32(Y(kc, 8 * nt + gq)), to_tf32(Y(kc + 4, 8 * nt + gq)));
+    }
+}
+// C tiles of one warp's 16 x 16 result -> f32 [16][16] scratch
+__device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        xs[gq * 16 + 8 * nt + 2 * tq] = acc[nt][0];
+        xs[gq * 16 + 8 * nt + 2 * tq + 1] = acc[nt][1];
+        xs[(gq + 8) * 16 + 8 * nt + 2 * tq] = acc[nt][2];
+        xs[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = acc[nt][3];
+    }
+}
+
 template <bool HAS_H0, bool STORE_HT>
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const float *__restrict__ beta,
@@ -222,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wq = warp & 3;        // TMEM lane quarter of this warp
-    const int ih = warp >> 2;       // which half of the key channels / tokens this warp takes
+    const int iq = warp >> 2;       // which quarter of the key channels / tokens this warp takes
     const int head = blockIdx.x;    // b * HV + hv
     const int hv = head % HV, b = head / HV;
     const int hk = hv / (HV / HK);
@@ -248,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto kval = [&](uint32_t base, int r, int i) -> float {
         return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + base + kq_off(r, i)));
     };
+    // 16 x 16 block (I, J) of the swizzled 64 x 64 tiles as index functors
+    auto blkA = [&](int I, int J) { return [=](int r, int c) { return sA[sq_idx(16 * I + r, 16 * J + c)]; }; };
+    auto blkT = [&](int I, int J) { return [=](int r, int c) { return sT[sq_idx(16 * I + r, 16 * J + c)]; }; };
+    auto blkX = [&](int n) { const float *x = sX + 256 * n; return [=](int r, int c) { return x[r * 16 + c]; }; };
 
     const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -278,11 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((s0 >> 4) > (r >> 4))
             *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
-    // state: S[64*ih + u][j], u = 0..63
-    float S[64];
+    // state: S[32*iq + u][j], u = 0..31
+    float S[32];
 #pragma unroll
-    for (int u = 0; u < 64; ++u)
-        S[u] = HAS_H0 ? h0[((size_t)head * kD + 64 * ih + u) * kD + j] : 0.f;
+    for (int u = 0; u < 32; ++u)
+        S[u] = HAS_H0 ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -298,29 +333,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *sbeta = reinterpret_cast<const float *>(smem + kBeta + 256 * (c & 1));
         const bool has_next = c + 1 < NC;
         const int t0n = t0 + kC;
+        // the next chunk's beta: loaded now, stored at the end of the chunk
+        float beta_next = 0.f;
+        if (has_next && tid < kC && t0n + tid < T)
+            beta_next = beta[((size_t)b * T + t0n + tid) * HV + hv];
 
         wait_bar(bar_kqg, (uint32_t)(c & 1), abort_flag);
         __syncthreads();
         if (*abort_flag) break;
 
-        // ---------------- per-channel prefix sums of g (two halves of 32 rows)
+        // ---------------- per-channel prefix sums of g (four quarters of 16 rows)
         {
-            const int i = tid & 127, hh = tid >> 7;
-            float x[32];
+            const int i = tid & 127, qq = tid >> 7;
+            float x[16];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) x[r] = gval(32 * hh + r, i);
+            for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i);
 #pragma unroll
-            for (int r = 1; r < 32; ++r) x[r] += x[r - 1];
-            if (hh == 0) sTot[i] = x[31];
+            for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
+            if (qq < 3) sTot[qq * 128 + i] = x[15];
             __syncthreads();
-            if (hh == 1) {
-                const float carry = sTot[i];
+            float carry = 0.f;
+            for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
 #pragma unroll
-                for (int r = 0; r < 32; ++r) x[r] += carry;
-            }
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-                *reinterpret_cast<float *>(smem + kG + g_off(32 * hh + r, i)) = x[r];
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = x[r] + carry;
         }
         __syncthreads();
         // reference-row and last-row values, then the range check
@@ -342,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---------------- operands Lk, Lq, R (bf16, K-major core-matrix tiles)
-#pragma unroll 2
-        for (int it = 0; it < 4; ++it) {
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
             const int id = tid + kThreads * it;  // 0..1023
             const int r8 = id & 7;
             const int r = ((id >> 7) << 3) | r8;
@@ -395,27 +431,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar(bar_mma, mma_phase, abort_flag);
             mma_phase ^= 1u;
             tc_fence_after_sync();
-            float dd[32];
-            tmem_ld32(tl + kTmGram + 32 * ih, dd);
+            float dd[16];
+            tmem_ld16(tl + kTmGram + 16 * iq, dd);
             const int row = 32 * wq + lane;
             if (row < kC) {
                 const int r = row;
                 const float br = sbeta[r];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int s = 32 * ih + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int s = 16 * iq + u;
                     sA[sq_idx(r, s)] = (s < r && r < L) ? br * dd[u] : 0.f;
                 }
             } else {
                 const int r = row - kC;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int s = 32 * ih + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int s = 16 * iq + u;
                     dd[u] = (s <= r && r < L) ? dd[u] : 0.f;
                 }
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, 32 * ih + 8 * q8, kC)) =
+                for (int q8 = 0; q8 < 2; ++q8)
+                    *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
                         pack_bf16x8(&dd[8 * q8]);
             }
         } else {
@@ -440,105 +476,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
 
         // prefetch the next chunk's k, q, g (their buffers are free now)
-        if (has_next) {
-            if (tid == 0) {
-                issue_kqg(smem, tm, bar_kqg, b, t0n, hk, hv);
-                ++issued_kqg;
-            }
-            float *sbn = reinterpret_cast<float *>(smem + kBeta + 256 * ((c + 1) & 1));
-            const int Ln = min(kC, T - t0n);
-            if (tid < kC) sbn[tid] = tid < Ln ? beta[((size_t)b * T + t0n + tid) * HV + hv] : 0.f;
+        if (has_next && tid == 0) {
+            issue_kqg(smem, tm, bar_kqg, b, t0n, hk, hv);
+            ++issued_kqg;
         }
 
         // ---------------- T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking,
-        // four threads per column (thread p owns the rows r = p mod 4)
+        // eight threads per column (thread p owns the rows r = p and p + 8)
         {
-            const int I = tid >> 6, jj = (tid >> 2) & 15, p = tid & 3;
-            float x[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) x[q4] = (4 * q4 + p == jj) ? 1.f : 0.f;
+            const int I = tid >> 7, jj = (tid >> 3) & 15, p = tid & 7;
+            float x0 = (p == jj) ? 1.f : 0.f, x1 = (p + 8 == jj) ? 1.f : 0.f;
 #pragma unroll
             for (int s = 0; s < 15; ++s) {
-                const float xs = __shfl_sync(0xffffffffu, x[s >> 2], (lane & ~3) | (s & 3));
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int r = 4 * q4 + p;
-                    if (r > s) x[q4] = fmaf(-sA[sq_idx(16 * I + r, 16 * I + s)], xs, x[q4]);
-                }
+                const float xs = __shfl_sync(0xffffffffu, s < 8 ? x0 : x1, (lane & ~7) | (s & 7));
+                if (p > s) x0 = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s)], xs, x0);
+                if (p + 8 > s) x1 = fmaf(-sA[sq_idx(16 * I + p + 8, 16 * I + s)], xs, x1);
             }
             __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
             const float bj = sbeta[16 * I + jj];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int r = 16 * I + 4 * q4 + p;
-                sT[sq_idx(r, 16 * I + jj)] = x[q4];
-                opt[kmajor_off(r, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x[q4] * bj);
-            }
+            sT[sq_idx(16 * I + p, 16 * I + jj)] = x0;
+            sT[sq_idx(16 * I + p + 8, 16 * I + jj)] = x1;
+            opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
+            opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
         }
         __syncthreads();
-        // ---------------- off-diagonal blocks: warp J walks block column J,
-        // T_IJ = -T_II sum_{M=J}^{I-1} A_IM T_MJ for I = J+1 .. 3
-        if (warp < 3) {
-            const int J = warp;
+        // ---------------- off-diagonal blocks by 32 x 32 block recursion:
+        //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
+        //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
+        auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
             const int gq = lane >> 2, tq = lane & 3;
-            float *xs = sX + warp * 256;  // X as f32 [16][16]
-            for (int I = J + 1; I < 4; ++I) {
-                float xc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                for (int M = J; M < I; ++M) {
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh) {
-                        const int kc = 16 * M + 8 * kh + tq;
-                        uint32_t a[4];
-                        a[0] = to_tf32(sA[sq_idx(16 * I + gq, kc)]);
-                        a[1] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc)]);
-                        a[2] = to_tf32(sA[sq_idx(16 * I + gq, kc + 4)]);
-                        a[3] = to_tf32(sA[sq_idx(16 * I + gq + 8, kc + 4)]);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const int n = 16 * J + 8 * nt + gq;
-                            mma_tf32(xc[nt], a, to_tf32(sT[sq_idx(kc, n)]),
-                                     to_tf32(sT[sq_idx(kc + 4, n)]));
-                        }
-                    }
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    xs[gq * 16 + 8 * nt + 2 * tq] = xc[nt][0];
-                    xs[gq * 16 + 8 * nt + 2 * tq + 1] = xc[nt][1];
-                    xs[(gq + 8) * 16 + 8 * nt + 2 * tq] = xc[nt][2];
-                    xs[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = xc[nt][3];
-                }
-                __syncwarp();
-                float yc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int kh = 0; kh < 2; ++kh) {
-                    const int kc = 16 * I + 8 * kh + tq;
-                    uint32_t a[4];
-                    a[0] = to_tf32(sT[sq_idx(16 * I + gq, kc)]);
-                    a[1] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc)]);
-                    a[2] = to_tf32(sT[sq_idx(16 * I + gq, kc + 4)]);
-                    a[3] = to_tf32(sT[sq_idx(16 * I + gq + 8, kc + 4)]);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int kx = 8 * kh + tq, n = 8 * nt + gq;
-                        mma_tf32(yc[nt], a, to_tf32(xs[kx * 16 + n]), to_tf32(xs[(kx + 4) * 16 + n]));
-                    }
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * J + 8 * nt + 2 * tq;
-                    const float b0 = sbeta[col], b1 = sbeta[col + 1];
-                    sT[sq_idx(16 * I + gq, col)] = -yc[nt][0];
-                    sT[sq_idx(16 * I + gq, col + 1)] = -yc[nt][1];
-                    sT[sq_idx(16 * I + gq + 8, col)] = -yc[nt][2];
-                    sT[sq_idx(16 * I + gq + 8, col + 1)] = -yc[nt][3];
-                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
-                        pack_bf16x2(-yc[nt][0] * b0, -yc[nt][1] * b1);
-                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
-                        pack_bf16x2(-yc[nt][2] * b0, -yc[nt][3] * b1);
-                }
-                __syncwarp();
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = 16 * J + 8 * nt + 2 * tq;
+                const float b0 = sbeta[col], b1 = sbeta[col + 1];
+                sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
+                sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
+                sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
+                sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
+                *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
+                    pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
+                *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
+                    pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
             }
+        };
+        if (warp < 2) {  // level 1: blocks (1,0) and (3,2)
+            const int I = 2 * warp + 1, J = 2 * warp;
+            float acc[2][4] = {};
+            blk_mma(acc, blkA(I, J), blkT(J, J), lane);
+            blk_store(sX + 256 * warp, acc, lane);
+            __syncwarp();
+            float y[2][4] = {};
+            blk_mma(y, blkT(I, I), blkX(warp), lane);
+            emit(I, J, y);
+        }
+        __syncthreads();
+        if (warp < 4) {  // level 2, X = [A_20 A_21; A_30 A_31] T1
+            const int I = 2 + (warp >> 1), J = warp & 1;
+            float acc[2][4] = {};
+            if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
+            blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
+            blk_store(sX + 256 * warp, acc, lane);  // X_IJ at slot 2 (I - 2) + J
+        }
+        __syncthreads();
+        if (warp < 4) {  // level 2, T_IJ = -T2 X
+            const int I = 2 + (warp >> 1), J = warp & 1;
+            float acc[2][4] = {};
+            blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
+            if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
+            emit(I, J, acc);
         }
         fence_async_smem();
         __syncthreads();
@@ -560,24 +565,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_bar(bar_mma, mma_phase, abort_flag);
         mma_phase ^= 1u;
         tc_fence_after_sync();
-        // all threads are past the batch-2 wait once this barrier completes:
-        // v's buffer is free for the next chunk's copy
         {
-            float dd[32];
-            tmem_ld32(tl + kTmWkT + 32 * ih, dd);  // row i = this lane, columns r
+            float dd[16];
+            tmem_ld16(tl + kTmWkT + 16 * iq, dd);  // row i = this lane, columns r
             const int i = 32 * wq + lane;
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 32 * ih + 8 * q8, kD)) =
+            for (int q8 = 0; q8 < 2; ++q8)
+                *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 16 * iq + 8 * q8, kD)) =
                     pack_bf16x8(&dd[8 * q8]);
         }
         // S'^T = (diag(exp(G_m)) S)^T as the A operand (bf16)
 #pragma unroll
-        for (int u8 = 0; u8 < 8; ++u8) {
+        for (int u8 = 0; u8 < 4; ++u8) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = S[8 * u8 + e] * sEGm[64 * ih + 8 * u8 + e];
-            *reinterpret_cast<uint4 *>(smem + kOpST + kmajor_off(j, 64 * ih + 8 * u8, kD)) =
+            for (int e = 0; e < 8; ++e) x[e] = S[8 * u8 + e] * sEGm[32 * iq + 8 * u8 + e];
+            *reinterpret_cast<uint4 *>(smem + kOpST + kmajor_off(j, 32 * iq + 8 * u8, kD)) =
                 pack_bf16x8(x);
         }
         fence_async_smem();
@@ -601,11 +604,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_phase ^= 1u;
         tc_fence_after_sync();
         {
-            float dd[32];
-            tmem_ld32(tl + kTmUT + 32 * ih, dd);
+            float dd[16];
+            tmem_ld16(tl + kTmUT + 16 * iq, dd);
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(smem + kOpUT + kmajor_off(j, 32 * ih + 8 * q8, kC)) =
+            for (int q8 = 0; q8 < 2; ++q8)
+                *reinterpret_cast<uint4 *>(smem + kOpUT + kmajor_off(j, 16 * iq + 8 * q8, kC)) =
                     pack_bf16x8(&dd[8 * q8]);
         }
         fence_async_smem();
@@ -626,29 +629,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         {
             float dd[32];
-            tmem_ld32(tl + kTmDS + 64 * ih, dd);
+            tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                const int i = 64 * ih + u;
+                const int i = 32 * iq + u;
                 S[u] = fmaf(sGamL[i], S[u], sCL[i] * dd[u]);
             }
-            tmem_ld32(tl + kTmDS + 64 * ih + 32, dd);
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = 64 * ih + 32 + u;
-                S[32 + u] = fmaf(sGamL[i], S[32 + u], sCL[i] * dd[u]);
-            }
             // O^T -> bf16 O [r][j] staging
-            tmem_ld32(tl + kTmOT + 32 * ih, dd);
+            float oo[16];
+            tmem_ld16(tl + kTmOT + 16 * iq, oo);
             __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) stg[(32 * ih + u) * kD + j] = __float2bfloat16_rn(dd[u]);
+            for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
+        }
+        if (has_next && tid < kC) {
+            float *sbn = reinterpret_cast<float *>(smem + kBeta + 256 * ((c + 1) & 1));
+            sbn[tid] = beta_next;
         }
         tc_fence_before_sync();
         __syncthreads();
         // coalesced 16-byte stores of the chunk's output rows
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < 2; ++it) {
             const int id = tid + kThreads * it;  // 0..1023
             const int r = id >> 4, cc = id & 15;
             if (r < L)
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!aborted && STORE_HT) {
 #pragma unroll
-        for (int u = 0; u < 64; ++u) ht[((size_t)head * kD + 64 * ih + u) * kD + j] = S[u];
+        for (int u = 0; u < 32; ++u) ht[((size_t)head * kD + 32 * iq + u) * kD + j] = S[u];
     }
     tc_fence_before_sync();
     __syncthreads();
