@@ -88,11 +88,11 @@ constexpr uint32_t kStage = kOpWK;            //   later: bf16 O [64][128] stagi
 constexpr uint32_t kOpUT = kOpWK + 16384;     // U^T as K-major A [128 j][64 r]
 constexpr uint32_t kX32 = kOpUT;              //   earlier: f32 [4][16][16] solve scratch
 constexpr uint32_t kSmall = kOpUT + 16384;
-constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (double-buffered)
-constexpr uint32_t kEGm = kBeta + 512;        // f32 [128] exp(G_m)
-constexpr uint32_t kCL = kEGm + 512;          // f32 [128] exp(G_last - G_m)
-constexpr uint32_t kGamL = kCL + 512;         // f32 [128] exp(G_last)
-constexpr uint32_t kGm = kGamL + 512;         // f32 [128] G_m (raw reference row)
+constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
+constexpr uint32_t kEGm = kBeta + 512;        // f32 [2][128] exp(G_m) (by chunk parity)
+constexpr uint32_t kCL = kEGm + 1024;         // f32 [2][128] exp(G_last - G_m)
+constexpr uint32_t kGamL = kCL + 1024;        // f32 [2][128] exp(G_last)
+constexpr uint32_t kGm = kGamL + 1024;        // f32 [128] G_m (raw reference row)
 constexpr uint32_t kGl = kGm + 512;           // f32 [128] G_last
 constexpr uint32_t kTot = kGl + 512;          // f32 [3][128] prefix-sum carries
 constexpr uint32_t kBarMma = kTot + 1536;     // mbarrier: MMA batches
@@ -193,16 +193,18 @@ struct TileMaps {
     CUtensorMap k, q, g, v;
 };
 
-// One elected thread: the k, q and g boxes of one chunk (tokens t0 .. t0+63).
+// Lanes 0-7 of one warp: the k, q and g boxes of one chunk (tokens t0 ..
+// t0+63), one box per lane, after lane 0 has announced the byte count.
 __device__ __forceinline__ void issue_kqg(unsigned char *sm, const TileMaps &tm, uint64_t *bar,
-                                          int b, int t0, int hk, int hv) {
-    mbar_arrive_expect_tx(bar, kBytesKQG);
-    tma_load_4d(sm + kRawK, &tm.k, 0, hk, t0, b, bar);
-    tma_load_4d(sm + kRawK + 8192, &tm.k, 64, hk, t0, b, bar);
-    tma_load_4d(sm + kRawQ, &tm.q, 0, hk, t0, b, bar);
-    tma_load_4d(sm + kRawQ + 8192, &tm.q, 64, hk, t0, b, bar);
-#pragma unroll
-    for (int x = 0; x < 4; ++x) tma_load_4d(sm + kG + 8192 * x, &tm.g, 32 * x, hv, t0, b, bar);
+                                          int b, int t0, int hk, int hv, int lane) {
+    if (lane == 0) mbar_arrive_expect_tx(bar, kBytesKQG);
+    __syncwarp();
+    if (lane < 2)
+        tma_load_4d(sm + kRawK + 8192 * lane, &tm.k, 64 * lane, hk, t0, b, bar);
+    else if (lane < 4)
+        tma_load_4d(sm + kRawQ + 8192 * (lane - 2), &tm.q, 64 * (lane - 2), hk, t0, b, bar);
+    else if (lane < 8)
+        tma_load_4d(sm + kG + 8192 * (lane - 4), &tm.g, 32 * (lane - 4), hv, t0, b, bar);
 }
 __device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, uint64_t *bar, int b,
                                         int t0, int hv) {
@@ -259,9 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = hv / (HV / HK);
     const int j = 32 * wq + lane;   // this thread's value column (TMEM lane)
 
-    float *sEGm = reinterpret_cast<float *>(smem + kEGm);
-    float *sCL = reinterpret_cast<float *>(smem + kCL);
-    float *sGamL = reinterpret_cast<float *>(smem + kGamL);
     float *sGm = reinterpret_cast<float *>(smem + kGm);
     float *sGl = reinterpret_cast<float *>(smem + kGl);
     float *sTot = reinterpret_cast<float *>(smem + kTot);
@@ -279,10 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto kval = [&](uint32_t base, int r, int i) -> float {
         return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + base + kq_off(r, i)));
     };
+    // per-chunk vectors, double-buffered by chunk parity
+    auto vec = [&](uint32_t base, int parity) {
+        return reinterpret_cast<float *>(smem + base + 512 * parity);
+    };
     // 16 x 16 block (I, J) of the swizzled 64 x 64 tiles as index functors
     auto blkA = [&](int I, int J) { return [=](int r, int c) { return sA[sq_idx(16 * I + r, 16 * J + c)]; }; };
     auto blkT = [&](int I, int J) { return [=](int r, int c) { return sT[sq_idx(16 * I + r, 16 * J + c)]; }; };
     auto blkX = [&](int n) { const float *x = sX + 256 * n; return [=](int r, int c) { return x[r * 16 + c]; }; };
+    auto mma_wait = [&](uint32_t &phase) {
+        wait_bar(bar_mma, phase, abort_flag);
+        phase ^= 1u;
+        tc_fence_after_sync();
+    };
 
     const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -298,15 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm.v);
     }
     __syncthreads();
-    if (tid == 0) {  // first chunk's inputs
-        issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv);
-        issue_v(smem, tm, bar_v, b, 0, hv);
+    if (warp == 0) {  // first chunk's inputs
+        issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv, lane);
+        if (lane == 0) issue_v(smem, tm, bar_v, b, 0, hv);
     }
-    {
-        float *sb0 = reinterpret_cast<float *>(smem + kBeta);
-        const int L0 = min(kC, T);
-        if (tid < kC) sb0[tid] = tid < L0 ? beta[((size_t)b * T + tid) * HV + hv] : 0.f;
-    }
+    if (tid < kC)  // beta buffers: [2][64] floats by chunk parity
+        reinterpret_cast<float *>(smem + kBeta)[tid] =
+            tid < min(kC, T) ? beta[((size_t)b * T + tid) * HV + hv] : 0.f;
     // T' is lower triangular: its strictly-upper 16 x 16 blocks stay zero
     for (int idx = tid; idx < 64 * 8; idx += kThreads) {
         const int r = idx >> 3, s0 = (idx & 7) * 8;
@@ -324,338 +330,368 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
     uint32_t mma_phase = 0;
-    int issued_kqg = 1, issued_v = 1;  // loads issued so far (thread 0's view is authoritative)
+    int issued_kqg = 1, issued_v = 1;  // loads issued so far (thread 0's count is used)
 
-    for (int c = 0; c < NC; ++c) {
-        const int t0 = c * kC;
-        const int L = min(kC, T - t0);
-        const int m = (L - 1) / 2;  // reference row of the factorisation
-        const float *sbeta = reinterpret_cast<const float *>(smem + kBeta + 256 * (c & 1));
-        const bool has_next = c + 1 < NC;
-        const int t0n = t0 + kC;
-        // the next chunk's beta: loaded now, stored at the end of the chunk
-        float beta_next = 0.f;
-        if (has_next && tid < kC && t0n + tid < T)
-            beta_next = beta[((size_t)b * T + t0n + tid) * HV + hv];
+    // Software pipeline: iteration c finishes the state products of chunk c
+    // (scan) and prepares chunk c + 1 (prep), so each wait for a tensor-core
+    // batch of one has the other's CUDA-core work in front of it.
+    //   1 prep: prefix sums, scales          (scan's batch 3 in flight)
+    //   2 scan: U^T read-back, issue batch 4
+    //   3 prep: operand tiles, issue gram    (scan's batch 4 in flight)
+    //   4 scan: dS and O read-back, outputs  (prep's gram in flight)
+    //   5 prep: A and P, inverse, issue batch 2
+    //   6 prep: S'^T, (T'Lk)^T read-back, issue the next scan's batch 3
+    for (int c = -1; c < NC; ++c) {
+        const bool has_scan = c >= 0;
+        const bool has_prep = c + 1 < NC;
+        const int cn = c + 1;                          // chunk being prepared
+        const int t0 = c * kC, L = has_scan ? min(kC, T - t0) : 0;
+        const int t0n = cn * kC, Ln = has_prep ? min(kC, T - t0n) : 0;
+        const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
+        const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
+        const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
+        float beta_n2 = 0.f;                           // beta of chunk cn + 1, stored in step 6
+        if (has_next2 && tid < kC && t0n + kC + tid < T)
+            beta_n2 = beta[((size_t)b * T + t0n + kC + tid) * HV + hv];
 
-        wait_bar(bar_kqg, (uint32_t)(c & 1), abort_flag);
+        // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
+        bool slow = false;
+        if (has_prep) wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
         __syncthreads();
         if (*abort_flag) break;
-
-        // ---------------- per-channel prefix sums of g (four quarters of 16 rows)
-        {
-            const int i = tid & 127, qq = tid >> 7;
-            float x[16];
+        if (has_prep) {
+            {
+                const int i = tid & 127, qq = tid >> 7;
+                float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i);
+                for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i);
 #pragma unroll
-            for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
-            if (qq < 3) sTot[qq * 128 + i] = x[15];
+                for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
+                if (qq < 3) sTot[qq * 128 + i] = x[15];
+                __syncthreads();
+                float carry = 0.f;
+                for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = x[r] + carry;
+            }
             __syncthreads();
-            float carry = 0.f;
-            for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = x[r] + carry;
-        }
-        __syncthreads();
-        // reference-row and last-row values, then the range check
-        int bad = 0;
-        if (tid < kD) {
-            const float gm = gval(m, tid), gl = gval(L - 1, tid);
-            sGm[tid] = gm;
-            sGl[tid] = gl;
-            bad = (gval(0, tid) - gm > kRangeNats) || (gm - gl > kRangeNats);
-        }
-        const bool slow = __syncthreads_or(bad) != 0;
-        if (tid < kD) {
-            // the fallback factorises around the chunk start (G_m = 0) and
-            // stores R with the full decay to the chunk end (scale 1)
-            const float gm = slow ? 0.f : sGm[tid], gl = sGl[tid];
-            sEGm[tid] = slow ? 1.f : __expf(gm);
-            sCL[tid] = slow ? 1.f : __expf(gl - gm);
-            sGamL[tid] = __expf(gl);
+            // reference-row and last-row values, then the range check
+            int bad = 0;
+            if (tid < kD) {
+                const float gm = gval(mref, tid), gl = gval(Ln - 1, tid);
+                sGm[tid] = gm;
+                sGl[tid] = gl;
+                bad = (gval(0, tid) - gm > kRangeNats) || (gm - gl > kRangeNats);
+            }
+            slow = __syncthreads_or(bad) != 0;
+            if (tid < kD) {
+                // the fallback factorises around the chunk start (G_m = 0) and
+                // stores R with the full decay to the chunk end (scale 1)
+                const float gm = slow ? 0.f : sGm[tid], gl = sGl[tid];
+                vec(kEGm, pn)[tid] = slow ? 1.f : __expf(gm);
+                vec(kCL, pn)[tid] = slow ? 1.f : __expf(gl - gm);
+                vec(kGamL, pn)[tid] = __expf(gl);
+            }
         }
 
-        // ---------------- operands Lk, Lq, R (bf16, K-major core-matrix tiles)
+        // ---------------- 2 scan: U^T read-back, then batch 4 (O^T += U^T P^T, dS^T = U^T R)
+        if (has_scan) {
+            mma_wait(mma_phase);  // batch 3 of chunk c
+            {
+                float dd[16];
+                tmem_ld16(tl + kTmUT + 16 * iq, dd);
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int id = tid + kThreads * it;  // 0..1023
-            const int r8 = id & 7;
-            const int r = ((id >> 7) << 3) | r8;
-            const int c8 = (id >> 3) & 15;
-            const int ch = c8 * 8;
-            float kv[8], qv[8], gv[8], gm[8];
-            const uint32_t kqo = (uint32_t)((c8 >> 3) * 8192 + r * 128 + (((c8 & 7) ^ r8) << 4));
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kqo), kv);
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kqo), qv);
-            const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
-            const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
-            const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
-            gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
-            gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
-            if (!slow) {
-                const float4 m_lo = *reinterpret_cast<const float4 *>(sGm + ch);
-                const float4 m_hi = *reinterpret_cast<const float4 *>(sGm + ch + 4);
-                gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
-                gm[4] = m_hi.x; gm[5] = m_hi.y; gm[6] = m_hi.z; gm[7] = m_hi.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) gm[e] = 0.f;
+                for (int q8 = 0; q8 < 2; ++q8)
+                    *reinterpret_cast<uint4 *>(smem + kOpUT + kmajor_off(j, 16 * iq + 8 * q8, kC)) =
+                        pack_bf16x8(&dd[8 * q8]);
             }
-            float lk[8], lq[8], rk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float d = gv[e] - gm[e];
-                const float el = __expf(d);
-                lk[e] = kv[e] * el;
-                lq[e] = qv[e] * el;
-                // fallback: R = exp(G_L - G) K directly (factor <= 1)
-                rk[e] = kv[e] * __expf(slow ? sGl[ch + e] - gv[e] : -d);
-            }
-            *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
-            *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lq);
-            *reinterpret_cast<uint4 *>(smem + kOpR + kmajor_off(r, ch, kD)) = pack_bf16x8(rk);
-        }
-        fence_async_smem();
-        __syncthreads();
-
-        // ---------------- MMA batch 1: gram [Lk; Lq] R^T, then A (f32) and P (bf16)
-        if (!slow) {
+            fence_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
             if (tid == 0) {
                 tc_fence_after_sync();
-                gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
+                gemm(tmem + kTmOT, sbase + kOpUT, 128, kC * 16, sbase + kOpP, 128, kC * 16,
+                     idesc_bf16(128, 64, false, false, false), kC / 16, true);
+                gemm(tmem + kTmDS, sbase + kOpUT, 128, kC * 16, sbase + kOpR, kD * 16, 128,
+                     idesc_bf16(128, 128, false, true, false), kC / 16, false);
+                mma_commit(bar_mma);
+            }
+        }
+
+        // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
+        if (has_prep) {
+            float rkeep[2][8];
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int id = tid + kThreads * it;  // 0..1023
+                const int r8 = id & 7;
+                const int r = ((id >> 7) << 3) | r8;
+                const int c8 = (id >> 3) & 15;
+                const int ch = c8 * 8;
+                float kv[8], qv[8], gv[8], gm[8];
+                const uint32_t kqo = (uint32_t)((c8 >> 3) * 8192 + r * 128 + (((c8 & 7) ^ r8) << 4));
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kqo), kv);
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kqo), qv);
+                const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
+                const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
+                const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
+                gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
+                gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
+                if (!slow) {
+                    const float4 m_lo = *reinterpret_cast<const float4 *>(sGm + ch);
+                    const float4 m_hi = *reinterpret_cast<const float4 *>(sGm + ch + 4);
+                    gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
+                    gm[4] = m_hi.x; gm[5] = m_hi.y; gm[6] = m_hi.z; gm[7] = m_hi.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gm[e] = 0.f;
+                }
+                float lk[8], lq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = gv[e] - gm[e];
+                    const float el = __expf(d);
+                    lk[e] = kv[e] * el;
+                    lq[e] = qv[e] * el;
+                    // fallback: R = exp(G_L - G) K directly (factor <= 1)
+                    rkeep[it][e] = kv[e] * __expf(slow ? sGl[ch + e] - gv[e] : -d);
+                }
+                // Lk and Lq are not read by the scan's batch 4: write them now
+                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
+                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lq);
+            }
+            if (has_scan) mma_wait(mma_phase);  // batch 4 of chunk c has finished reading R
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int id = tid + kThreads * it;
+                const int r = ((id >> 7) << 3) | (id & 7);
+                const int ch = ((id >> 3) & 15) * 8;
+                *reinterpret_cast<uint4 *>(smem + kOpR + kmajor_off(r, ch, kD)) = pack_bf16x8(rkeep[it]);
+            }
+            fence_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            if (!slow) {
+                if (tid == 0) {
+                    tc_fence_after_sync();
+                    gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
+                         idesc_bf16(128, 64, false, false, false), kD / 16, false);
+                    mma_commit(bar_mma);
+                }
+                // the raw k, q, g tiles are consumed: fetch the next chunk's
+                if (has_next2 && warp == 0) issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                if (has_next2 && tid == 0) ++issued_kqg;
+            }
+        } else if (has_scan) {
+            mma_wait(mma_phase);  // batch 4 of the last chunk
+        }
+
+        // ---------------- 4 scan: dS^T and O^T read-back, state update, outputs
+        if (has_scan) {
+            {
+                const float *cl = vec(kCL, ps), *gam = vec(kGamL, ps);
+                float dd[32];
+                tmem_ld32(tl + kTmDS + 32 * iq, dd);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int i = 32 * iq + u;
+                    S[u] = fmaf(gam[i], S[u], cl[i] * dd[u]);
+                }
+                // O^T -> bf16 O [r][j] staging
+                float oo[16];
+                tmem_ld16(tl + kTmOT + 16 * iq, oo);
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
+            }
+            tc_fence_before_sync();
+            __syncthreads();
+            // coalesced 16-byte stores of the chunk's output rows
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int id = tid + kThreads * it;  // 0..1023
+                const int r = id >> 4, cc = id & 15;
+                if (r < L)
+                    *reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8) =
+                        *reinterpret_cast<const uint4 *>(smem + kStage + r * 256 + cc * 16);
+            }
+        }
+
+        // ---------------- 5 prep: A (f32) and P (bf16), the inverse, batch 2
+        if (has_prep) {
+            const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
+            if (!slow) {
+                mma_wait(mma_phase);  // gram of chunk cn
+                float dd[16];
+                tmem_ld16(tl + kTmGram + 16 * iq, dd);
+                const int row = 32 * wq + lane;
+                if (row < kC) {
+                    const int r = row;
+                    const float br = bvec[r];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int s = 16 * iq + u;
+                        sA[sq_idx(r, s)] = (s < r && r < Ln) ? br * dd[u] : 0.f;
+                    }
+                } else {
+                    const int r = row - kC;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int s = 16 * iq + u;
+                        dd[u] = (s <= r && r < Ln) ? dd[u] : 0.f;
+                    }
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8)
+                        *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
+                            pack_bf16x8(&dd[8 * q8]);
+                }
+            } else {
+                // exact pairwise decays on CUDA cores (every exponent <= 0)
+                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
+                for (int idx = tid; idx < kC * kC; idx += kThreads) {
+                    const int r = idx >> 6, s = idx & 63;
+                    float a = 0.f, p = 0.f;
+                    if (s <= r && r < Ln) {
+                        for (int i = 0; i < kD; ++i) {
+                            const float e = __expf(gval(r, i) - gval(s, i));
+                            const float kse = kval(kRawK, s, i) * e;
+                            a = fmaf(kval(kRawK, r, i), kse, a);
+                            p = fmaf(kval(kRawQ, r, i), kse, p);
+                        }
+                    }
+                    sA[sq_idx(r, s)] = (s < r) ? bvec[r] * a : 0.f;
+                    op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
+                }
+            }
+            tc_fence_before_sync();
+            __syncthreads();
+            if (slow && has_next2) {  // raw tiles were read until now on this path
+                if (warp == 0) issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                if (tid == 0) ++issued_kqg;
+            }
+
+            // T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking, eight
+            // threads per column (thread p owns the rows r = p and p + 8)
+            {
+                const int I = tid >> 7, jj = (tid >> 3) & 15, p = tid & 7;
+                float x0 = (p == jj) ? 1.f : 0.f, x1 = (p + 8 == jj) ? 1.f : 0.f;
+#pragma unroll
+                for (int s = 0; s < 15; ++s) {
+                    const float xs = __shfl_sync(0xffffffffu, s < 8 ? x0 : x1, (lane & ~7) | (s & 7));
+                    if (p > s) x0 = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s)], xs, x0);
+                    if (p + 8 > s) x1 = fmaf(-sA[sq_idx(16 * I + p + 8, 16 * I + s)], xs, x1);
+                }
+                __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
+                const float bj = bvec[16 * I + jj];
+                sT[sq_idx(16 * I + p, 16 * I + jj)] = x0;
+                sT[sq_idx(16 * I + p + 8, 16 * I + jj)] = x1;
+                opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
+                opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
+            }
+            __syncthreads();
+            // off-diagonal blocks by 32 x 32 block recursion:
+            //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
+            //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
+            auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
+                const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * J + 8 * nt + 2 * tq;
+                    const float b0 = bvec[col], b1 = bvec[col + 1];
+                    sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
+                    sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
+                    sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
+                    sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
+                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
+                        pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
+                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
+                        pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
+                }
+            };
+            if (warp < 2) {  // level 1: blocks (1,0) and (3,2)
+                const int I = 2 * warp + 1, J = 2 * warp;
+                float acc[2][4] = {};
+                blk_mma(acc, blkA(I, J), blkT(J, J), lane);
+                blk_store(sX + 256 * warp, acc, lane);
+                __syncwarp();
+                float y[2][4] = {};
+                blk_mma(y, blkT(I, I), blkX(warp), lane);
+                emit(I, J, y);
+            }
+            __syncthreads();
+            if (warp < 4) {  // level 2, X = [A_20 A_21; A_30 A_31] T1
+                const int I = 2 + (warp >> 1), J = warp & 1;
+                float acc[2][4] = {};
+                if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
+                blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
+                blk_store(sX + 256 * warp, acc, lane);  // X_IJ at slot 2 (I - 2) + J
+            }
+            __syncthreads();
+            if (warp < 4) {  // level 2, T_IJ = -T2 X
+                const int I = 2 + (warp >> 1), J = warp & 1;
+                float acc[2][4] = {};
+                blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
+                if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
+                emit(I, J, acc);
+            }
+            fence_async_smem();
+            __syncthreads();
+            wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
+            if (tid == 0) {
+                tc_fence_after_sync();
+                // (T'Lk)^T: Lk read transposed, MN-major (k = s, mn = i): K stride 2048, MN 128
+                gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
+                     idesc_bf16(128, 64, true, false, false), kC / 16, false);
+                // (T'V)^T: V 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
+                const uint32_t vid = idesc_bf16(128, 64, true, false, false);
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
+                             smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid, ks > 0 ? 1u : 0u);
+                mma_commit(bar_mma);
+            }
+        }
+
+        // ---------------- 6 prep: S'^T, (T'Lk)^T read-back, the next scan's batch 3
+        if (has_prep) {
+            // S'^T = (diag(exp(G_m)) S)^T as the A operand (bf16); S now holds chunk cn's start
+            const float *egm = vec(kEGm, pn);
+#pragma unroll
+            for (int u8 = 0; u8 < 4; ++u8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = S[8 * u8 + e] * egm[32 * iq + 8 * u8 + e];
+                *reinterpret_cast<uint4 *>(smem + kOpST + kmajor_off(j, 32 * iq + 8 * u8, kD)) =
+                    pack_bf16x8(x);
+            }
+            mma_wait(mma_phase);  // batch 2 of chunk cn
+            {
+                float dd[16];
+                tmem_ld16(tl + kTmWkT + 16 * iq, dd);  // row i = this lane, columns r
+                const int i = 32 * wq + lane;
+#pragma unroll
+                for (int q8 = 0; q8 < 2; ++q8)
+                    *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 16 * iq + 8 * q8, kD)) =
+                        pack_bf16x8(&dd[8 * q8]);
+            }
+            if (has_next2 && tid < kC)
+                reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1))[tid] = beta_n2;
+            fence_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                if (has_next2) {  // batch 2 is done, so v's buffer is free
+                    issue_v(smem, tm, bar_v, b, t0n + kC, hv);
+                    ++issued_v;
+                }
+                tc_fence_after_sync();
+                // U^T -= S'^T (T'Lk)^T  and  O^T = S'^T Lq^T
+                gemm(tmem + kTmUT, sbase + kOpST, 128, kD * 16, sbase + kOpWK, 128, kD * 16,
+                     idesc_bf16(128, 64, false, true, true), kD / 16, true);
+                gemm(tmem + kTmOT, sbase + kOpST, 128, kD * 16, sbase + kOpL + 16384, 128, kD * 16,
                      idesc_bf16(128, 64, false, false, false), kD / 16, false);
                 mma_commit(bar_mma);
             }
-            wait_bar(bar_mma, mma_phase, abort_flag);
-            mma_phase ^= 1u;
-            tc_fence_after_sync();
-            float dd[16];
-            tmem_ld16(tl + kTmGram + 16 * iq, dd);
-            const int row = 32 * wq + lane;
-            if (row < kC) {
-                const int r = row;
-                const float br = sbeta[r];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int s = 16 * iq + u;
-                    sA[sq_idx(r, s)] = (s < r && r < L) ? br * dd[u] : 0.f;
-                }
-            } else {
-                const int r = row - kC;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int s = 16 * iq + u;
-                    dd[u] = (s <= r && r < L) ? dd[u] : 0.f;
-                }
-#pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
-                        pack_bf16x8(&dd[8 * q8]);
-            }
-        } else {
-            // exact pairwise decays on CUDA cores (every exponent <= 0)
-            __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
-            for (int idx = tid; idx < kC * kC; idx += kThreads) {
-                const int r = idx >> 6, s = idx & 63;
-                float a = 0.f, p = 0.f;
-                if (s <= r && r < L) {
-                    for (int i = 0; i < kD; ++i) {
-                        const float e = __expf(gval(r, i) - gval(s, i));
-                        const float kse = kval(kRawK, s, i) * e;
-                        a = fmaf(kval(kRawK, r, i), kse, a);
-                        p = fmaf(kval(kRawQ, r, i), kse, p);
-                    }
-                }
-                sA[sq_idx(r, s)] = (s < r) ? sbeta[r] * a : 0.f;
-                op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
-            }
-        }
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // prefetch the next chunk's k, q, g (their buffers are free now)
-        if (has_next && tid == 0) {
-            issue_kqg(smem, tm, bar_kqg, b, t0n, hk, hv);
-            ++issued_kqg;
-        }
-
-        // ---------------- T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking,
-        // eight threads per column (thread p owns the rows r = p and p + 8)
-        {
-            const int I = tid >> 7, jj = (tid >> 3) & 15, p = tid & 7;
-            float x0 = (p == jj) ? 1.f : 0.f, x1 = (p + 8 == jj) ? 1.f : 0.f;
-#pragma unroll
-            for (int s = 0; s < 15; ++s) {
-                const float xs = __shfl_sync(0xffffffffu, s < 8 ? x0 : x1, (lane & ~7) | (s & 7));
-                if (p > s) x0 = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s)], xs, x0);
-                if (p + 8 > s) x1 = fmaf(-sA[sq_idx(16 * I + p + 8, 16 * I + s)], xs, x1);
-            }
-            __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
-            const float bj = sbeta[16 * I + jj];
-            sT[sq_idx(16 * I + p, 16 * I + jj)] = x0;
-            sT[sq_idx(16 * I + p + 8, 16 * I + jj)] = x1;
-            opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
-            opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
-        }
-        __syncthreads();
-        // ---------------- off-diagonal blocks by 32 x 32 block recursion:
-        //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
-        //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
-        auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
-            const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = 16 * J + 8 * nt + 2 * tq;
-                const float b0 = sbeta[col], b1 = sbeta[col + 1];
-                sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
-                sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
-                sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
-                sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
-                *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
-                    pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
-                *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
-                    pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
-            }
-        };
-        if (warp < 2) {  // level 1: blocks (1,0) and (3,2)
-            const int I = 2 * warp + 1, J = 2 * warp;
-            float acc[2][4] = {};
-            blk_mma(acc, blkA(I, J), blkT(J, J), lane);
-            blk_store(sX + 256 * warp, acc, lane);
-            __syncwarp();
-            float y[2][4] = {};
-            blk_mma(y, blkT(I, I), blkX(warp), lane);
-            emit(I, J, y);
-        }
-        __syncthreads();
-        if (warp < 4) {  // level 2, X = [A_20 A_21; A_30 A_31] T1
-            const int I = 2 + (warp >> 1), J = warp & 1;
-            float acc[2][4] = {};
-            if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
-            blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
-            blk_store(sX + 256 * warp, acc, lane);  // X_IJ at slot 2 (I - 2) + J
-        }
-        __syncthreads();
-        if (warp < 4) {  // level 2, T_IJ = -T2 X
-            const int I = 2 + (warp >> 1), J = warp & 1;
-            float acc[2][4] = {};
-            blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
-            if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
-            emit(I, J, acc);
-        }
-        fence_async_smem();
-        __syncthreads();
-
-        // ---------------- MMA batch 2: (T'Lk)^T = Lk^T T'^T,  U^T = V^T T'^T
-        wait_bar(bar_v, (uint32_t)(c & 1), abort_flag);
-        if (tid == 0) {
-            tc_fence_after_sync();
-            // Lk read transposed: MN-major (k = s, mn = i), K-direction stride 2048, MN 128
-            gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
-                 idesc_bf16(128, 64, true, false, false), kC / 16, false);
-            // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
-            const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
-                         smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid, ks > 0 ? 1u : 0u);
-            mma_commit(bar_mma);
-        }
-        wait_bar(bar_mma, mma_phase, abort_flag);
-        mma_phase ^= 1u;
-        tc_fence_after_sync();
-        {
-            float dd[16];
-            tmem_ld16(tl + kTmWkT + 16 * iq, dd);  // row i = this lane, columns r
-            const int i = 32 * wq + lane;
-#pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8)
-                *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 16 * iq + 8 * q8, kD)) =
-                    pack_bf16x8(&dd[8 * q8]);
-        }
-        // S'^T = (diag(exp(G_m)) S)^T as the A operand (bf16)
-#pragma unroll
-        for (int u8 = 0; u8 < 4; ++u8) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = S[8 * u8 + e] * sEGm[32 * iq + 8 * u8 + e];
-            *reinterpret_cast<uint4 *>(smem + kOpST + kmajor_off(j, 32 * iq + 8 * u8, kD)) =
-                pack_bf16x8(x);
-        }
-        fence_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // ---------------- MMA batch 3: U^T -= S'^T (T'Lk)^T,  O^T = S'^T Lq^T
-        if (tid == 0) {
-            if (has_next) {  // batch 2 is done, so v's buffer is free
-                issue_v(smem, tm, bar_v, b, t0n, hv);
-                ++issued_v;
-            }
-            tc_fence_after_sync();
-            gemm(tmem + kTmUT, sbase + kOpST, 128, kD * 16, sbase + kOpWK, 128, kD * 16,
-                 idesc_bf16(128, 64, false, true, true), kD / 16, true);
-            gemm(tmem + kTmOT, sbase + kOpST, 128, kD * 16, sbase + kOpL + 16384, 128, kD * 16,
-                 idesc_bf16(128, 64, false, false, false), kD / 16, false);
-            mma_commit(bar_mma);
-        }
-        wait_bar(bar_mma, mma_phase, abort_flag);
-        mma_phase ^= 1u;
-        tc_fence_after_sync();
-        {
-            float dd[16];
-            tmem_ld16(tl + kTmUT + 16 * iq, dd);
-#pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8)
-                *reinterpret_cast<uint4 *>(smem + kOpUT + kmajor_off(j, 16 * iq + 8 * q8, kC)) =
-                    pack_bf16x8(&dd[8 * q8]);
-        }
-        fence_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // ---------------- MMA batch 4: O^T += U^T P^T,  dS^T = U^T R (R read MN-major)
-        if (tid == 0) {
-            tc_fence_after_sync();
-            gemm(tmem + kTmOT, sbase + kOpUT, 128, kC * 16, sbase + kOpP, 128, kC * 16,
-                 idesc_bf16(128, 64, false, false, false), kC / 16, true);
-            gemm(tmem + kTmDS, sbase + kOpUT, 128, kC * 16, sbase + kOpR, kD * 16, 128,
-                 idesc_bf16(128, 128, false, true, false), kC / 16, false);
-            mma_commit(bar_mma);
-        }
-        wait_bar(bar_mma, mma_phase, abort_flag);
-        mma_phase ^= 1u;
-        tc_fence_after_sync();
-        {
-            float dd[32];
-            tmem_ld32(tl + kTmDS + 32 * iq, dd);
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = 32 * iq + u;
-                S[u] = fmaf(sGamL[i], S[u], sCL[i] * dd[u]);
-            }
-            // O^T -> bf16 O [r][j] staging
-            float oo[16];
-            tmem_ld16(tl + kTmOT + 16 * iq, oo);
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
-        }
-        if (has_next && tid < kC) {
-            float *sbn = reinterpret_cast<float *>(smem + kBeta + 256 * ((c + 1) & 1));
-            sbn[tid] = beta_next;
-        }
-        tc_fence_before_sync();
-        __syncthreads();
-        // coalesced 16-byte stores of the chunk's output rows
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int id = tid + kThreads * it;  // 0..1023
-            const int r = id >> 4, cc = id & 15;
-            if (r < L)
-                *reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8) =
-                    *reinterpret_cast<const uint4 *>(smem + kStage + r * 256 + cc * 16);
         }
     }
 
