@@ -41,11 +41,12 @@
 // one value column j, 32 of the 128 key rows).  State products are computed
 // transposed so that M = dv = 128 fills the MMA:
 //   U^T = (T'V)^T - S'^T (T'Lk)^T,  O^T = S'^T Lq^T + U^T P^T,  dS^T = U^T R.
-// Operands are bf16 tiles in shared memory in the interleaved (no-swizzle)
+// The per-chunk tiles are bf16 in shared memory in the interleaved (no-swizzle)
 // core-matrix layout (sm100_ptx.cuh); each of Lk, Lq and R is stored once
 // and read both K-major and, through an MN-major descriptor with the two
-// core-matrix strides exchanged, transposed.  Accumulators are float32 in
-// TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
+// core-matrix strides exchanged, transposed.  The two state-dependent A
+// operands, S'^T and U^T, are written as bf16 straight into tensor memory
+// and read from there by the MMA.  Accumulators are float32 in TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
 // swizzled boxes; rows past the end of the sequence are zero-filled by the
 // copy engine), the next chunk's copies in flight while the current chunk's
 // solve and state products run; v lands directly in the swizzled MN-major
@@ -77,17 +78,15 @@ constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizz
 constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
 constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lk, 64-127 Lq
 constexpr uint32_t kOpR = kOpL + 32768;       // [64][128] K-major: R
-constexpr uint32_t kAT = kOpR + 16384;        // 32 KB: f32 A and T (64x64 each), later S'^T
+constexpr uint32_t kAT = kOpR + 16384;        // 32 KB: f32 A and T (64x64 each)
 constexpr uint32_t kA32 = kAT;
 constexpr uint32_t kT32 = kAT + 16384;
-constexpr uint32_t kOpST = kAT;               //   S'^T as K-major A [128 j][128 i]
 constexpr uint32_t kOpT = kAT + 32768;        // T' as K-major B [64 r][64 s]
 constexpr uint32_t kOpP = kOpT + 8192;        // P as K-major B [64 r][64 s]
-constexpr uint32_t kOpWK = kOpP + 8192;       // (T'Lk) as MN-major B (k = i, mn = r), K extent 128
+constexpr uint32_t kOpWK = kOpP + 8192;       // -(T'Lk) as MN-major B (k = i, mn = r), K extent 128
 constexpr uint32_t kStage = kOpWK;            //   later: bf16 O [64][128] staging for the stores
-constexpr uint32_t kOpUT = kOpWK + 16384;     // U^T as K-major A [128 j][64 r]
-constexpr uint32_t kX32 = kOpUT;              //   earlier: f32 [4][16][16] solve scratch
-constexpr uint32_t kSmall = kOpUT + 16384;
+constexpr uint32_t kX32 = kOpWK + 16384;      // f32 [4][16][16] solve scratch
+constexpr uint32_t kSmall = kX32 + 4096;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
 constexpr uint32_t kEGm = kBeta + 512;        // f32 [2][128] exp(G_m) (by chunk parity)
 constexpr uint32_t kCL = kEGm + 1024;         // f32 [2][128] exp(G_last - G_m)
@@ -112,6 +111,8 @@ constexpr uint32_t kTmWkT = 64;     // [128 i x 64 r]  (T' Lk)^T
 constexpr uint32_t kTmUT = 128;     // [128 j x 64 r]
 constexpr uint32_t kTmOT = 192;     // [128 j x 64 r]
 constexpr uint32_t kTmDS = 256;     // [128 j x 128 i]
+constexpr uint32_t kTmSTb = 384;    // S'^T as bf16 A operand: [128 j x 128 i], 2 per column
+constexpr uint32_t kTmUTb = 448;    // U^T as bf16 A operand: [128 j x 64 r], 2 per column
 constexpr uint32_t kTmemCols = 512;
 
 // 64 x 64 f32 tiles (A, T) with an XOR swizzle: rows and columns both walk
@@ -401,20 +402,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 float dd[16];
                 tmem_ld16(tl + kTmUT + 16 * iq, dd);
+                uint32_t w[8];
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    *reinterpret_cast<uint4 *>(smem + kOpUT + kmajor_off(j, 16 * iq + 8 * q8, kC)) =
-                        pack_bf16x8(&dd[8 * q8]);
+                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
+                tmem_st8(tl + kTmUTb + 8 * iq, w);
+                tmem_st_wait();
             }
-            fence_async_smem();
             tc_fence_before_sync();
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after_sync();
-                gemm(tmem + kTmOT, sbase + kOpUT, 128, kC * 16, sbase + kOpP, 128, kC * 16,
-                     idesc_bf16(128, 64, false, false, false), kC / 16, true);
-                gemm(tmem + kTmDS, sbase + kOpUT, 128, kC * 16, sbase + kOpR, kD * 16, 128,
-                     idesc_bf16(128, 128, false, true, false), kC / 16, false);
+                const uint32_t io = idesc_bf16(128, 64, false, false, false);
+                const uint32_t ids = idesc_bf16(128, 128, false, true, false);
+                for (int ks = 0; ks < kC / 16; ++ks) {  // A = U^T (bf16) in TMEM, 8 columns per K step
+                    mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
+                                smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
+                    mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
+                                smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids, ks > 0 ? 1u : 0u);
+                }
                 mma_commit(bar_mma);
             }
         }
@@ -490,13 +495,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- 4 scan: dS^T and O^T read-back, state update, outputs
         if (has_scan) {
             {
-                const float *cl = vec(kCL, ps), *gam = vec(kGamL, ps);
+                const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
+                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kGamL, ps) + 32 * iq);
                 float dd[32];
                 tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int i = 32 * iq + u;
-                    S[u] = fmaf(gam[i], S[u], cl[i] * dd[u]);
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 cl = cl4[u4], gm = gam4[u4];
+                    S[4 * u4 + 0] = fmaf(gm.x, S[4 * u4 + 0], cl.x * dd[4 * u4 + 0]);
+                    S[4 * u4 + 1] = fmaf(gm.y, S[4 * u4 + 1], cl.y * dd[4 * u4 + 1]);
+                    S[4 * u4 + 2] = fmaf(gm.z, S[4 * u4 + 2], cl.z * dd[4 * u4 + 2]);
+                    S[4 * u4 + 3] = fmaf(gm.w, S[4 * u4 + 3], cl.w * dd[4 * u4 + 3]);
                 }
                 // O^T -> bf16 O [r][j] staging
                 float oo[16];
@@ -516,6 +525,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8) =
                         *reinterpret_cast<const uint4 *>(smem + kStage + r * 256 + cc * 16);
             }
+        }
+
+        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
+        // in TMEM (S now holds that chunk's starting state); batch 3 of chunk
+        // c, its previous reader, finished in step 2
+        if (has_prep) {
+            const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
+            uint32_t w[16];
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 e = egm4[u4];
+                w[2 * u4] = pack_bf16x2(S[4 * u4] * e.x, S[4 * u4 + 1] * e.y);
+                w[2 * u4 + 1] = pack_bf16x2(S[4 * u4 + 2] * e.z, S[4 * u4 + 3] * e.w);
+            }
+            tmem_st16(tl + kTmSTb + 16 * iq, w);
+            tmem_st_wait();
         }
 
         // ---------------- 5 prep: A (f32) and P (bf16), the inverse, batch 2
@@ -652,22 +677,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // ---------------- 6 prep: S'^T, (T'Lk)^T read-back, the next scan's batch 3
+        // ---------------- 6 prep: -(T'Lk)^T read-back, the next scan's batch 3
         if (has_prep) {
-            // S'^T = (diag(exp(G_m)) S)^T as the A operand (bf16); S now holds chunk cn's start
-            const float *egm = vec(kEGm, pn);
-#pragma unroll
-            for (int u8 = 0; u8 < 4; ++u8) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = S[8 * u8 + e] * egm[32 * iq + 8 * u8 + e];
-                *reinterpret_cast<uint4 *>(smem + kOpST + kmajor_off(j, 32 * iq + 8 * u8, kD)) =
-                    pack_bf16x8(x);
-            }
             mma_wait(mma_phase);  // batch 2 of chunk cn
             {
                 float dd[16];
                 tmem_ld16(tl + kTmWkT + 16 * iq, dd);  // row i = this lane, columns r
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dd[e] = -dd[e];
                 const int i = 32 * wq + lane;
 #pragma unroll
                 for (int q8 = 0; q8 < 2; ++q8)
@@ -685,11 +702,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++issued_v;
                 }
                 tc_fence_after_sync();
-                // U^T -= S'^T (T'Lk)^T  and  O^T = S'^T Lq^T
-                gemm(tmem + kTmUT, sbase + kOpST, 128, kD * 16, sbase + kOpWK, 128, kD * 16,
-                     idesc_bf16(128, 64, false, true, true), kD / 16, true);
-                gemm(tmem + kTmOT, sbase + kOpST, 128, kD * 16, sbase + kOpL + 16384, 128, kD * 16,
-                     idesc_bf16(128, 64, false, false, false), kD / 16, false);
+                // U^T += S'^T (-(T'Lk))^T  and  O^T = S'^T Lq^T, A = S'^T (bf16) in TMEM
+                const uint32_t iu = idesc_bf16(128, 64, false, true, false);
+                const uint32_t io = idesc_bf16(128, 64, false, false, false);
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
+                                smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
+                    mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
+                                smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16), io,
+                                ks > 0 ? 1u : 0u);
+                }
                 mma_commit(bar_mma);
             }
         }

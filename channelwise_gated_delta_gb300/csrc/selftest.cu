@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t slot;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp == 0) tmem_alloc(&slot, 128);
+    if (warp == 0) tmem_alloc(&slot, 256);
     if (tid == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
@@ -50,12 +50,39 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = slot;
+    if (a_mn == 4) {
+        // A in tensor memory: row m in lane m, (A[m][2c], A[m][2c+1]) packed in column 128 + c
+        const int m = 32 * warp + lane;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                __nv_bfloat162 pr;
+                pr.x = A[m * kK + 32 * h + 2 * c];
+                pr.y = A[m * kK + 32 * h + 2 * c + 1];
+                w[c] = *reinterpret_cast<uint32_t *>(&pr);
+            }
+            tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + 128 + 16 * h, w);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+    }
     if (tid == 0) {
         const uint32_t idesc = idesc_bf16(kM, N, a_mn != 0, b_mn != 0, false);
         // K-direction / MN-direction core-matrix strides of each operand
         const uint32_t a_lbo = a_mn == 2 ? kM * 16 : 128, a_sbo = a_mn == 2 ? 128 : kK * 16;
         const uint32_t b_lbo = b_mn == 2 ? N * 16 : 128, b_sbo = b_mn == 2 ? 128 : kK * 16;
-        for (int ks = 0; ks < kK / 16; ++ks) {
+        for (int ks = 0; ks < kK / 16 && a_mn == 4; ++ks) {
+            const uint64_t bd =
+                b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
+                          : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
+            mma_bf16_ts(tmem, tmem + 128 + 8 * ks, bd, idesc_bf16(kM, N, false, b_mn != 0, false),
+                        ks > 0 ? 1u : 0u);
+        }
+        for (int ks = 0; ks < kK / 16 && a_mn != 4; ++ks) {
             // swizzled MN-major: 64-element blocks of kK rows (LBO), 8-row atoms (SBO)
             const uint64_t ad =
                 a_mn == 3 ? smem_desc_sw128(smem_u32(sa) + ks * 2048, kK * 128, 1024)
@@ -85,7 +112,7 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -97,7 +124,7 @@ extern "C" GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, 
                                                 void *stream) {
     if (!A || !B || !D) return GDR_ERR_NULL;
     if (N != 64 && N != 128) return GDR_ERR_UNSUPPORTED;
-    if (a_mn_major < 0 || a_mn_major > 3 || b_mn_major < 0 || b_mn_major > 3)
+    if (a_mn_major < 0 || a_mn_major > 4 || b_mn_major < 0 || b_mn_major > 3)
         return GDR_ERR_UNSUPPORTED;
     int *err = nullptr;
     cudaError_t e = gdr::device_error_word(&err);

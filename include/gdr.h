@@ -180,8 +180,9 @@ GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, d
  * 1 MN-major, 2 a K-major tile of the transposed operand read through an
  * MN-major descriptor (the way the prefill reuses one tile for both
  * orientations), 3 MN-major with the 128-byte swizzle that TMA tensor loads
- * produce.  Enqueued on `stream`; a timed-out wait is reported by
- * gdr_device_check.
+ * produce; a_mn_major = 4 places A in tensor memory instead (row m in lane
+ * m, two consecutive-K bf16 values per 32-bit column).  Enqueued on
+ * `stream`; a timed-out wait is reported by gdr_device_check.
  */
 GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N, const void *A,
                                      const void *B, float *D, void *stream);

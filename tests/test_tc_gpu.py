@@ -13,7 +13,7 @@ from tests.test_parity_gpu import check, run_gpu, run_oracle
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("a_mn", [0, 1, 2, 3])
+@pytest.mark.parametrize("a_mn", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("b_mn", [0, 1, 2, 3])
 @pytest.mark.parametrize("N", [64, 128])
 def test_umma_gemm_layouts(a_mn, b_mn, N):
