@@ -28,6 +28,8 @@
 //   A = tril(diag(beta) Lk R^T),  P = tril(Lq R^T),
 //   (exp(G) * K) S = Lk S',  (exp(G) * Q) S = Lq S',
 //   (exp(G_L - G) * K)^T U = diag(exp(G_L - G_m)) R^T U.
+// (In the kernel G is kept in log2 units, G * log2(e), so that every decay
+// factor is a single ex2.)
 // While every channel decays by at most 80 nats between the chunk's first
 // token and m and between m and its last token, all factors are finite and
 // the products are exact to rounding.  A chunk outside that range (decay
@@ -68,7 +70,8 @@ using namespace sm100;
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
 constexpr int kThreads = 512;  // 16 warps
-constexpr float kRangeNats = 80.f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = tid & 127, qq = tid >> 7;
                 float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i);
+                for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i) * kLog2e;  // log2 units
 #pragma unroll
                 for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
@@ -383,16 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float gm = gval(mref, tid), gl = gval(Ln - 1, tid);
                 sGm[tid] = gm;
                 sGl[tid] = gl;
-                bad = (gval(0, tid) - gm > kRangeNats) || (gm - gl > kRangeNats);
+                bad = (gval(0, tid) - gm > kRangeLog2) || (gm - gl > kRangeLog2);
             }
             slow = __syncthreads_or(bad) != 0;
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
                 const float gm = slow ? 0.f : sGm[tid], gl = sGl[tid];
-                vec(kEGm, pn)[tid] = slow ? 1.f : __expf(gm);
-                vec(kCL, pn)[tid] = slow ? 1.f : __expf(gl - gm);
-                vec(kGamL, pn)[tid] = __expf(gl);
+                vec(kEGm, pn)[tid] = slow ? 1.f : fast_exp2(gm);
+                vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
+                vec(kGamL, pn)[tid] = fast_exp2(gl);
             }
         }
 
@@ -456,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float d = gv[e] - gm[e];
-                    const float el = __expf(d);
+                    const float el = fast_exp2(d);
                     lk[e] = kv[e] * el;
                     lq[e] = qv[e] * el;
                     // fallback: R = exp(G_L - G) K directly (factor <= 1)
-                    rkeep[it][e] = kv[e] * __expf(slow ? sGl[ch + e] - gv[e] : -d);
+                    rkeep[it][e] = kv[e] * fast_exp2(slow ? sGl[ch + e] - gv[e] : -d);
                 }
                 // Lk and Lq are not read by the scan's batch 4: write them now
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float a = 0.f, p = 0.f;
                     if (s <= r && r < Ln) {
                         for (int i = 0; i < kD; ++i) {
-                            const float e = __expf(gval(r, i) - gval(s, i));
+                            const float e = fast_exp2(gval(r, i) - gval(s, i));
                             const float kse = kval(kRawK, s, i) * e;
                             a = fmaf(kval(kRawK, r, i), kse, a);
                             p = fmaf(kval(kRawQ, r, i), kse, p);

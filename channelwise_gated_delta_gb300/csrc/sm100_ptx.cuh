@@ -202,6 +202,20 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity
         : "memory");
     return ok;
 }
+// Same, but the thread may sleep in hardware up to `hint_ns` nanoseconds
+// waiting for the phase instead of returning at once.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                        uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok;
+}
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -214,9 +228,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        // sleep in the barrier (up to 100 us per try) rather than spin on it
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+// ex2.approx: 2^x (relative error about 2^-22 on normal results)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
