@@ -69,7 +69,10 @@ using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
-constexpr int kThreads = 512;  // 16 warps
+constexpr int kCompute = 512;               // 16 compute warps
+constexpr int kThreads = kCompute + 32;     // + one warp that issues MMAs and TMA copies
+constexpr int kBarCompute = 1;              // named barrier: compute warps only
+constexpr int kBarH1 = 2, kBarH2 = 3, kBarH3 = 4, kBarH4 = 5;  // compute -> issuer handoffs
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -102,7 +105,8 @@ constexpr uint32_t kBarKQG = kBarMma + 8;     // mbarrier: k, q, g tiles
 constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
 constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
 constexpr uint32_t kAbort = kTmemSlot + 4;    // i32 sticky abort flag
-constexpr uint32_t kSmemUsed = kAbort + 4;
+constexpr uint32_t kSlowFlag = kAbort + 4;    // i32: the prepared chunk takes the exact path
+constexpr uint32_t kSmemUsed = kSlowFlag + 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack for the 1024-byte base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kBytesKQG = 16384 + 16384 + 32768;
@@ -258,8 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool issuer_warp = tid >= kCompute;
     const int wq = warp & 3;        // TMEM lane quarter of this warp
-    const int iq = warp >> 2;       // which quarter of the key channels / tokens this warp takes
+    const int iq = (warp >> 2) & 3; // which quarter of the key channels / tokens this warp takes
     const int head = blockIdx.x;    // b * HV + hv
     const int hv = head % HV, b = head / HV;
     const int hk = hv / (HV / HK);
@@ -276,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_v = reinterpret_cast<uint64_t *>(smem + kBarV);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kAbort);
+    volatile int *slow_flag = reinterpret_cast<volatile int *>(smem + kSlowFlag);
     auto gval = [&](int r, int i) -> float {
         return *reinterpret_cast<const float *>(smem + kG + g_off(r, i));
     };
@@ -295,10 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         phase ^= 1u;
         tc_fence_after_sync();
     };
+    auto csync = [&]() { named_sync(kBarCompute, kCompute); };
+    // compute warps hand a finished operand set to the issuer warp and go on
+    auto handoff = [&](int id) {
+        fence_async_smem();
+        tc_fence_before_sync();
+        named_arrive(id, kThreads);
+    };
 
     const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
-    if (tid == 0) {
+    if (tid == kCompute) {
         mbar_init(bar_mma, 1);
         mbar_init(bar_kqg, 1);
         mbar_init(bar_v, 1);
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm.v);
     }
     __syncthreads();
-    if (warp == 0) {  // first chunk's inputs
+    if (issuer_warp) {  // first chunk's inputs
         issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv, lane);
         if (lane == 0) issue_v(smem, tm, bar_v, b, 0, hv);
     }
@@ -323,28 +336,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((s0 >> 4) > (r >> 4))
             *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
-    // state: S[32*iq + u][j], u = 0..31
+    // state: S[32*iq + u][j], u = 0..31 (compute warps)
     float S[32];
 #pragma unroll
     for (int u = 0; u < 32; ++u)
-        S[u] = HAS_H0 ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
+        S[u] = (HAS_H0 && !issuer_warp) ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
     uint32_t mma_phase = 0;
-    int issued_kqg = 1, issued_v = 1;  // loads issued so far (thread 0's count is used)
+    int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer lane 0's count is used)
 
     // Software pipeline: iteration c finishes the state products of chunk c
     // (scan) and prepares chunk c + 1 (prep), so each wait for a tensor-core
-    // batch of one has the other's CUDA-core work in front of it.
+    // batch of one has the other's CUDA-core work in front of it.  One warp
+    // issues every MMA and TMA copy; the compute warps hand operands over
+    // with named-barrier arrivals and never wait for the issue itself.
     //   1 prep: prefix sums, scales          (scan's batch 3 in flight)
-    //   2 scan: U^T read-back, issue batch 4
-    //   3 prep: operand tiles, issue gram    (scan's batch 4 in flight)
-    //   4 scan: dS and O read-back, outputs  (prep's gram in flight)
-    //   5 prep: A and P, inverse, issue batch 2
-    //   6 prep: S'^T, (T'Lk)^T read-back, issue the next scan's batch 3
+    //   2 scan: U^T read-back   -> H1: batch 4
+    //   3 prep: operand tiles   -> H2: gram, next k/q/g copies
+    //   4 scan: dS and O read-back, outputs; S'^T for the prepared chunk
+    //   5 prep: A and P, inverse -> H3: batch 2
+    //   6 prep: (T'Lk)^T read-back -> H4: next v copy, the next scan's batch 3
     for (int c = -1; c < NC; ++c) {
         const bool has_scan = c >= 0;
         const bool has_prep = c + 1 < NC;
@@ -354,16 +369,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
         const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
         const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
-        float beta_n2 = 0.f;                           // beta of chunk cn + 1, stored in step 6
+
+        __syncthreads();
+        if (*abort_flag) break;
+
+        if (issuer_warp) {
+            // ============ issuer warp: one lane issues, the warp follows the handoffs
+            const uint32_t io = idesc_bf16(128, 64, false, false, false);
+            if (has_scan) {
+                named_sync(kBarH1, kThreads);
+                if (lane == 0) {  // batch 4: O^T += U^T P^T, dS^T = U^T R, A = U^T in TMEM
+                    tc_fence_after_sync();
+                    const uint32_t ids = idesc_bf16(128, 128, false, true, false);
+                    for (int ks = 0; ks < kC / 16; ++ks) {
+                        mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
+                                    smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
+                        mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
+                                    smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids,
+                                    ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_mma);
+                }
+            }
+            if (has_prep) {
+                named_sync(kBarH2, kThreads);
+                const bool slow = *slow_flag != 0;
+                if (!slow) {
+                    if (lane == 0) {  // gram [Lk; Lq] R^T
+                        tc_fence_after_sync();
+                        gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
+                             io, kD / 16, false);
+                        mma_commit(bar_mma);
+                    }
+                    // the raw k, q, g tiles are consumed: fetch the next chunk's
+                    if (has_next2) {
+                        issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                        ++issued_kqg;
+                    }
+                }
+                named_sync(kBarH3, kThreads);
+                if (slow && has_next2) {  // the exact path read the raw tiles until now
+                    issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                    ++issued_kqg;
+                }
+                if (lane == 0) {  // batch 2: (T'Lk)^T and (T'V)^T
+                    wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
+                    tc_fence_after_sync();
+                    // Lk read transposed: MN-major (k = s, mn = i), K stride 2048, MN 128
+                    gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
+                         idesc_bf16(128, 64, true, false, false), kC / 16, false);
+                    // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
+                    const uint32_t vid = idesc_bf16(128, 64, true, false, false);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
+                                 smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
+                                 ks > 0 ? 1u : 0u);
+                    mma_commit(bar_mma);
+                }
+                named_sync(kBarH4, kThreads);
+                if (lane == 0) {
+                    if (has_next2) {  // batch 2 is done, so v's buffer is free
+                        issue_v(smem, tm, bar_v, b, t0n + kC, hv);
+                        ++issued_v;
+                    }
+                    tc_fence_after_sync();
+                    // U^T += S'^T (-(T'Lk))^T  and  O^T = S'^T Lq^T, A = S'^T (bf16) in TMEM
+                    const uint32_t iu = idesc_bf16(128, 64, false, true, false);
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
+                                    smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
+                        mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
+                                    smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16), io,
+                                    ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_mma);
+                }
+            }
+            continue;
+        }
+
+        // ============ compute warps
+        float beta_n2 = 0.f;  // beta of chunk cn + 1, stored in step 6
         if (has_next2 && tid < kC && t0n + kC + tid < T)
             beta_n2 = beta[((size_t)b * T + t0n + kC + tid) * HV + hv];
 
         // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
         bool slow = false;
-        if (has_prep) wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
-        __syncthreads();
-        if (*abort_flag) break;
         if (has_prep) {
+            wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
+            csync();
             {
                 const int i = tid & 127, qq = tid >> 7;
                 float x[16];
@@ -372,14 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
-                __syncthreads();
+                csync();
                 float carry = 0.f;
                 for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
                     *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = x[r] + carry;
             }
-            __syncthreads();
+            csync();
             // reference-row and last-row values, then the range check
             int bad = 0;
             if (tid < kD) {
@@ -388,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sGl[tid] = gl;
                 bad = (gval(0, tid) - gm > kRangeLog2) || (gm - gl > kRangeLog2);
             }
-            slow = __syncthreads_or(bad) != 0;
+            slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
+            if (tid == 0) *slow_flag = slow ? 1 : 0;  // read by the issuer after H2
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
@@ -399,32 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // ---------------- 2 scan: U^T read-back, then batch 4 (O^T += U^T P^T, dS^T = U^T R)
+        // ---------------- 2 scan: U^T read-back as the bf16 A operand of batch 4
         if (has_scan) {
             mma_wait(mma_phase);  // batch 3 of chunk c
-            {
-                float dd[16];
-                tmem_ld16(tl + kTmUT + 16 * iq, dd);
-                uint32_t w[8];
+            float dd[16];
+            tmem_ld16(tl + kTmUT + 16 * iq, dd);
+            uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
-                tmem_st8(tl + kTmUTb + 8 * iq, w);
-                tmem_st_wait();
-            }
-            tc_fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after_sync();
-                const uint32_t io = idesc_bf16(128, 64, false, false, false);
-                const uint32_t ids = idesc_bf16(128, 128, false, true, false);
-                for (int ks = 0; ks < kC / 16; ++ks) {  // A = U^T (bf16) in TMEM, 8 columns per K step
-                    mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
-                                smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
-                    mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
-                                smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(bar_mma);
-            }
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
+            tmem_st8(tl + kTmUTb + 8 * iq, w);
+            tmem_st_wait();
+            handoff(kBarH1);
         }
 
         // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
@@ -432,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float rkeep[2][8];
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
-                const int id = tid + kThreads * it;  // 0..1023
+                const int id = tid + kCompute * it;  // 0..1023
                 const int r8 = id & 7;
                 const int r = ((id >> 7) << 3) | r8;
                 const int c8 = (id >> 3) & 15;
@@ -472,25 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (has_scan) mma_wait(mma_phase);  // batch 4 of chunk c has finished reading R
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
-                const int id = tid + kThreads * it;
+                const int id = tid + kCompute * it;
                 const int r = ((id >> 7) << 3) | (id & 7);
                 const int ch = ((id >> 3) & 15) * 8;
                 *reinterpret_cast<uint4 *>(smem + kOpR + kmajor_off(r, ch, kD)) = pack_bf16x8(rkeep[it]);
             }
-            fence_async_smem();
-            tc_fence_before_sync();
-            __syncthreads();
-            if (!slow) {
-                if (tid == 0) {
-                    tc_fence_after_sync();
-                    gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
-                         idesc_bf16(128, 64, false, false, false), kD / 16, false);
-                    mma_commit(bar_mma);
-                }
-                // the raw k, q, g tiles are consumed: fetch the next chunk's
-                if (has_next2 && warp == 0) issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
-                if (has_next2 && tid == 0) ++issued_kqg;
-            }
+            handoff(kBarH2);
         } else if (has_scan) {
             mma_wait(mma_phase);  // batch 4 of the last chunk
         }
@@ -518,18 +585,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
             }
             tc_fence_before_sync();
-            __syncthreads();
+            csync();
             // coalesced 16-byte stores of the chunk's output rows
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
-                const int id = tid + kThreads * it;  // 0..1023
+                const int id = tid + kCompute * it;  // 0..1023
                 const int r = id >> 4, cc = id & 15;
                 if (r < L)
                     *reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8) =
                         *reinterpret_cast<const uint4 *>(smem + kStage + r * 256 + cc * 16);
             }
         }
-
         // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
         // in TMEM (S now holds that chunk's starting state); batch 3 of chunk
         // c, its previous reader, finished in step 2
@@ -546,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
         }
 
-        // ---------------- 5 prep: A (f32) and P (bf16), the inverse, batch 2
+        // ---------------- 5 prep: A (f32) and P (bf16), the inverse
         if (has_prep) {
             const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
             if (!slow) {
@@ -577,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // exact pairwise decays on CUDA cores (every exponent <= 0)
                 __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
-                for (int idx = tid; idx < kC * kC; idx += kThreads) {
+                for (int idx = tid; idx < kC * kC; idx += kCompute) {
                     const int r = idx >> 6, s = idx & 63;
                     float a = 0.f, p = 0.f;
                     if (s <= r && r < Ln) {
@@ -593,11 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before_sync();
-            __syncthreads();
-            if (slow && has_next2) {  // raw tiles were read until now on this path
-                if (warp == 0) issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
-                if (tid == 0) ++issued_kqg;
-            }
+            csync();
 
             // T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking, eight
             // threads per column (thread p owns the rows r = p and p + 8)
@@ -617,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
                 opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
             }
-            __syncthreads();
+            csync();
             // off-diagonal blocks by 32 x 32 block recursion:
             //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
             //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
@@ -647,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 blk_mma(y, blkT(I, I), blkX(warp), lane);
                 emit(I, J, y);
             }
-            __syncthreads();
+            csync();
             if (warp < 4) {  // level 2, X = [A_20 A_21; A_30 A_31] T1
                 const int I = 2 + (warp >> 1), J = warp & 1;
                 float acc[2][4] = {};
@@ -655,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
                 blk_store(sX + 256 * warp, acc, lane);  // X_IJ at slot 2 (I - 2) + J
             }
-            __syncthreads();
+            csync();
             if (warp < 4) {  // level 2, T_IJ = -T2 X
                 const int I = 2 + (warp >> 1), J = warp & 1;
                 float acc[2][4] = {};
@@ -663,24 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
                 emit(I, J, acc);
             }
-            fence_async_smem();
-            __syncthreads();
-            wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
-            if (tid == 0) {
-                tc_fence_after_sync();
-                // (T'Lk)^T: Lk read transposed, MN-major (k = s, mn = i): K stride 2048, MN 128
-                gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
-                     idesc_bf16(128, 64, true, false, false), kC / 16, false);
-                // (T'V)^T: V 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
-                const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-                for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
-                             smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid, ks > 0 ? 1u : 0u);
-                mma_commit(bar_mma);
-            }
+            handoff(kBarH3);  // T' (and S'^T in TMEM) are complete: batch 2
         }
 
-        // ---------------- 6 prep: -(T'Lk)^T read-back, the next scan's batch 3
+        // ---------------- 6 prep: -(T'Lk)^T read-back -> the next scan's batch 3
         if (has_prep) {
             mma_wait(mma_phase);  // batch 2 of chunk cn
             {
@@ -696,40 +744,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (has_next2 && tid < kC)
                 reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1))[tid] = beta_n2;
-            fence_async_smem();
-            tc_fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                if (has_next2) {  // batch 2 is done, so v's buffer is free
-                    issue_v(smem, tm, bar_v, b, t0n + kC, hv);
-                    ++issued_v;
-                }
-                tc_fence_after_sync();
-                // U^T += S'^T (-(T'Lk))^T  and  O^T = S'^T Lq^T, A = S'^T (bf16) in TMEM
-                const uint32_t iu = idesc_bf16(128, 64, false, true, false);
-                const uint32_t io = idesc_bf16(128, 64, false, false, false);
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
-                                smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
-                    mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
-                                smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16), io,
-                                ks > 0 ? 1u : 0u);
-                }
-                mma_commit(bar_mma);
-            }
+            handoff(kBarH4);
         }
     }
 
     __syncthreads();
     const bool aborted = *abort_flag != 0;
-    if (tid == 0 && aborted) {
+    if (tid == kCompute && aborted) {
         // never leave with copies in flight: wait (bounded) for the last copy
         // issued on each barrier; its phases complete in order
         atomicOr(dev_error, 1);
         mbar_wait_bounded(bar_kqg, (uint32_t)((issued_kqg - 1) & 1), kWaitLimitNs);
         mbar_wait_bounded(bar_v, (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
     }
-    if (!aborted && STORE_HT) {
+    if (!aborted && STORE_HT && !issuer_warp) {
 #pragma unroll
         for (int u = 0; u < 32; ++u) ht[((size_t)head * kD + 32 * iq + u) * kD + j] = S[u];
     }

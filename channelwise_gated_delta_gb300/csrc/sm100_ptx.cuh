@@ -262,6 +262,27 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---- named barriers (id 0 is __syncthreads)
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// bar.sync that also ORs a predicate over the participating threads
+__device__ __forceinline__ int named_sync_or(int id, int nthreads, int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 q, %2, 0;\n\t"
+        "bar.red.or.pred p, %0, %1, q;\n\t"
+        "selp.s32 %3, 1, 0, p;\n\t}"
+        : "+r"(id), "+r"(nthreads), "+r"(pred), "=r"(r)
+        :
+        : "memory");
+    return r;
+}
+
 // ---- cp.async (16-byte global -> shared copies)
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
