@@ -41,7 +41,10 @@ DECODE = "decode_b64"
 # DRAM bytes (read + write) per launch from an ncu capture, keyed by kernel,
 # with the sha256 of the source file the capture was taken from: a kernel
 # whose source has changed since reports traffic null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # decode B64: one launch, --set full capture (136.3 MB read + 73.9 MB written)
+    "gdr_decode_kernel": {"bytes": 210_200_000, "sha": "1b350c7a4ac6f3e0"},
+}
 
 
 def parse_args():
@@ -135,7 +138,7 @@ def src_sha(name):
 
 
 KERNEL_SOURCE = {"gdr_decode_kernel": "decode.cu", "gdr_chunk_prep": "prefill_generic.cu",
-                 "gdr_chunk_scan": "prefill_generic.cu"}
+                 "gdr_chunk_scan": "prefill_generic.cu", "gdr_prefill_fused": "prefill_tc.cu"}
 
 
 def traffic_for(kernel):
@@ -175,10 +178,12 @@ def roofline(kernel, launches, total_ms, bytes_per_launch, peak, peak_kind):
 
 
 def max_over_ranks(x, ws):
+    """Largest value of x over all ranks (timing: the slowest rank counts)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -320,64 +325,61 @@ def bench_decode(args, ws, rank, dev, peak, peak_kind):
 
 
 # ----------------------------------------------------------------- CPU oracle
-def oracle_sample(w, heads, T, threads=None, seed=7):
-    """Times the fp64 oracle on `heads` value heads x T tokens of workload w's
-    distributions.  Returns (seconds, head_tokens, cores)."""
+def oracle_batch_element(w, seed, threads=None, T=None):
+    """Times the fp64 oracle on one batch element of workload w (all HV value
+    heads, T tokens, w's distributions).  Returns (seconds, head_tokens, cores)."""
     import oracle
     from channelwise_gated_delta_gb300.inputs import draw, to_f64
-    HK = max(1, heads // max(1, w.HV // w.HK))
-    HV = HK * (w.HV // w.HK)
-    d = draw(1, T, HK, HV, w.dk, w.dv, dtype=w.dtype, h0=w.h0, seed=seed, g_mu=w.g_mu,
+    T = T or w.T
+    d = draw(1, T, w.HK, w.HV, w.dk, w.dv, dtype=w.dtype, h0=w.h0, seed=seed, g_mu=w.g_mu,
              g_sigma=w.g_sigma, beta_mu=w.beta_mu, beta_sigma=w.beta_sigma)
     arrs = [to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")]
     h0 = to_f64(d["h0"])
+    del d
     cores = threads or oracle.default_threads()
     t = time.perf_counter()
     oracle.recurrence(*arrs, h0, threads=cores)
     dt = time.perf_counter() - t
-    return dt, HV * T, min(cores, HV)
+    return dt, w.HV * T, min(cores, w.HV)
 
 
 def cpu_baseline(w):
+    """The oracle over the whole workload, one batch element at a time."""
     import oracle
     cores = oracle.default_threads()
-    heads = max(2, 2 * cores)
-    T = 4096
-    dt, head_tokens, used = oracle_sample(w, heads, T, threads=cores)
-    # aim for ~10 s of CPU work: grow the sample once if the first was short
-    if dt < 3.0:
-        T2 = min(w.T, int(T * min(8.0, 10.0 / max(dt, 1e-3))))
-        dt, head_tokens, used = oracle_sample(w, heads, T2, threads=cores)
-        T = T2
-    tok_s = head_tokens / dt / w.HV
+    total_s, head_tokens, used = 0.0, 0, 1
+    for bi in range(w.B):
+        dt, ht_, used = oracle_batch_element(w, seed=7 + bi, threads=cores)
+        total_s += dt
+        head_tokens += ht_
+    tok_s = head_tokens / total_s / w.HV
     return {"value": round(tok_s, 2), "unit": "tokens/s", "cores": used, "kind": "oracle",
-            "sample": "%d value heads x %d tokens of the %s distributions (fp64 recurrence, "
-                      "%.1f s)" % (head_tokens // T, T, w.name, dt)}
+            "sample": "the full workload: %d batch elements x %d value heads x %d tokens, fp64 "
+                      "recurrence, %.1f s of oracle time" % (w.B, w.HV, w.T, total_s)}
 
 
 def run_reference(args):
-    """Reference arm: the fp64 oracle on the host cores, same metric and unit."""
+    """Reference arm: the fp64 oracle on the host cores, same metric and unit.
+    Each step is one batch element of the workload (all value heads, all tokens)."""
     from channelwise_gated_delta_gb300.inputs import WORKLOADS
     import oracle
     w = WORKLOADS[PREFILL]
     cores = oracle.default_threads()
-    heads = max(2, cores)
-    T = w.T
-    for _ in range(args.warmup):
-        oracle_sample(w, heads, 64, threads=cores)
-    total_s, total_ht = 0.0, 0
+    for i in range(args.warmup):
+        oracle_batch_element(w, seed=50 + i, threads=cores, T=64)
+    total_s, total_ht, used = 0.0, 0, 1
     for i in range(args.steps):
-        dt, ht_, used = oracle_sample(w, heads, T, threads=cores, seed=100 + i)
+        dt, ht_, used = oracle_batch_element(w, seed=100 + i, threads=cores)
         total_s += dt
         total_ht += ht_
     tok_s = total_ht / total_s / w.HV
-    sample = "%d value heads x %d tokens per step of the %s distributions" % (
-        total_ht // (T * args.steps), T, w.name)
+    sample = "one batch element per step (%d value heads x %d tokens) of the %s workload" % (
+        w.HV, w.T, w.name)
     line = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 3), "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * total_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name + " (sampled)", "B": w.B, "T": w.T, "HK": w.HK,
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "HK": w.HK,
                        "HV": w.HV, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
             "cpu_baseline": {"value": round(tok_s, 3), "unit": "tokens/s", "cores": used,
                              "kind": "oracle", "sample": sample},
