@@ -198,7 +198,7 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 }
 
 struct TileMaps {
-    CUtensorMap k, q, g, v;
+    CUtensorMap k, q, g, v, o;
 };
 
 // Lanes 0-7 of one warp: the k, q and g boxes of one chunk (tokens t0 ..
@@ -254,8 +254,7 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
 template <bool HAS_H0, bool STORE_HT>
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const float *__restrict__ beta,
-                          const float *h0, __nv_bfloat16 *__restrict__ out, float *ht, int T,
-                          int HK, int HV, int *dev_error) {
+                          const float *h0, float *ht, int T, int HK, int HV, int *dev_error) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
     unsigned char *smem =
@@ -321,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm.q);
         tma_prefetch_desc(&tm.g);
         tma_prefetch_desc(&tm.v);
+        tma_prefetch_desc(&tm.o);
     }
     __syncthreads();
     if (issuer_warp) {  // first chunk's inputs
@@ -370,15 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
         const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
 
-        __syncthreads();
-        if (*abort_flag) break;
-
+        // No block-wide barrier per chunk: the issuer warp meets the compute
+        // warps only at the four handoffs, so the compute warps start the next
+        // chunk while the issuer is still feeding the previous batch.  After
+        // a timed-out wait (sticky abort flag) every thread still runs every
+        // iteration and every barrier, but waits return at once and nothing
+        // new is issued.
         if (issuer_warp) {
             // ============ issuer warp: one lane issues, the warp follows the handoffs
             const uint32_t io = idesc_bf16(128, 64, false, false, false);
             if (has_scan) {
                 named_sync(kBarH1, kThreads);
-                if (lane == 0) {  // batch 4: O^T += U^T P^T, dS^T = U^T R, A = U^T in TMEM
+                if (lane == 0 && !*abort_flag) {  // batch 4: O^T += U^T P^T, dS^T = U^T R, A = U^T in TMEM
                     tc_fence_after_sync();
                     const uint32_t ids = idesc_bf16(128, 128, false, true, false);
                     for (int ks = 0; ks < kC / 16; ++ks) {
@@ -394,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (has_prep) {
                 named_sync(kBarH2, kThreads);
                 const bool slow = *slow_flag != 0;
-                if (!slow) {
+                const bool live = !*abort_flag;  // one warp-wide read: uniform
+                if (!slow && live) {
                     if (lane == 0) {  // gram [Lk; Lq] R^T
                         tc_fence_after_sync();
                         gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
@@ -408,11 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 named_sync(kBarH3, kThreads);
-                if (slow && has_next2) {  // the exact path read the raw tiles until now
+                if (slow && has_next2 && live) {  // the exact path read the raw tiles until now
                     issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
                     ++issued_kqg;
                 }
-                if (lane == 0) {  // batch 2: (T'Lk)^T and (T'V)^T
+                if (lane == 0 && live) {  // batch 2: (T'Lk)^T and (T'V)^T
                     wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
                     tc_fence_after_sync();
                     // Lk read transposed: MN-major (k = s, mn = i), K stride 2048, MN 128
@@ -427,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar_mma);
                 }
                 named_sync(kBarH4, kThreads);
-                if (lane == 0) {
+                if (lane == 0 && live) {
                     if (has_next2) {  // batch 2 is done, so v's buffer is free
                         issue_v(smem, tm, bar_v, b, t0n + kC, hv);
                         ++issued_v;
@@ -584,16 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
             }
+            fence_async_smem();
             tc_fence_before_sync();
             csync();
-            // coalesced 16-byte stores of the chunk's output rows
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int id = tid + kCompute * it;  // 0..1023
-                const int r = id >> 4, cc = id & 15;
-                if (r < L)
-                    *reinterpret_cast<uint4 *>(out + (((size_t)b * T + t0 + r) * HV + hv) * kD + cc * 8) =
-                        *reinterpret_cast<const uint4 *>(smem + kStage + r * 256 + cc * 16);
+            // one TMA store of the chunk's [64 x 128] output box; rows past
+            // the end of the sequence fall outside the tensor and are dropped
+            if (tid == 0 && !*abort_flag) {
+                tma_store_4d(&tm.o, smem + kStage, 0, hv, t0, b);
+                bulk_commit_group();
             }
         }
         // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
@@ -614,6 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---------------- 5 prep: A (f32) and P (bf16), the inverse
         if (has_prep) {
+            // the staging box is rewritten in step 6: the store must have read
+            // it (ordered before those writes by the barriers below)
+            if (tid == 0) bulk_wait_read_all();
             const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
             if (!slow) {
                 mma_wait(mma_phase);  // gram of chunk cn
@@ -748,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (tid == 0) bulk_wait_all();
     __syncthreads();
     const bool aborted = *abort_flag != 0;
     if (tid == kCompute && aborted) {
@@ -794,14 +800,15 @@ EncodeTiledFn encode_fn(cudaError_t *err) {
 // [B][T][H][128] tensor of `esize`-byte elements; boxes of `box_inner`
 // elements x 64 tokens, 128-byte swizzled, zero fill outside the tensor.
 bool encode_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
-                int esize, int B, int T, int H, int box_inner) {
+                int esize, int B, int T, int H, int box_inner,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)128 * esize, (cuuint64_t)H * 128 * esize,
                                    (cuuint64_t)T * H * 128 * esize};
     const cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 64, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -821,16 +828,18 @@ cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t str
     if (!encode_map(fn, &tm.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
         !encode_map(fn, &tm.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
         !encode_map(fn, &tm.g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.HV, 32) ||
-        !encode_map(fn, &tm.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 64))
+        !encode_map(fn, &tm.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 64) ||
+        // output: one unswizzled [64 tokens][128 channels] box per chunk
+        !encode_map(fn, &tm.o, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
     auto run = [&](auto kernel) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
-        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, p.beta, p.h0, out, p.ht,
-                                                                  p.T, p.HK, p.HV, dev_error);
+        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, p.beta, p.h0, p.ht, p.T,
+                                                                  p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };

@@ -258,6 +258,27 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, in
         "r"(smem_u32(bar))
         : "memory");
 }
+// Tiled TMA store of a shared-memory box to a 4-D tensor (bulk async group);
+// rows outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, const void *smem_src, int c0, int c1,
+                                             int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// waits until the issuing thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// waits until the issuing thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
