@@ -69,10 +69,14 @@ using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
-constexpr int kCompute = 512;               // 16 compute warps
-constexpr int kThreads = kCompute + 32;     // + one warp that issues MMAs and TMA copies
-constexpr int kBarCompute = 1;              // named barrier: compute warps only
-constexpr int kBarH1 = 2, kBarH2 = 3, kBarH3 = 4, kBarH4 = 5;  // compute -> issuer handoffs
+constexpr int kCompute = 512;               // 16 state warps
+constexpr int kThreads = kCompute + 128;    // + 4 auxiliary warps: 2 issuers, 2 solvers
+constexpr int kHand = kCompute + 64;        // state warps + issuer warps
+constexpr int kBarCompute = 1;              // named barrier: state warps only
+constexpr int kBarH1 = 2, kBarH2 = 3, kBarH4 = 4;  // state -> issuer handoffs (kHand threads)
+constexpr int kBarS4 = 5;                   // state -> issuer: chunk outputs and S' done (kHand)
+constexpr int kBarDiag = 6;                 // state -> auxiliary: A and diagonal inverses done (all)
+constexpr int kBarAux = 7;                  // auxiliary warps only
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -261,7 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool issuer_warp = tid >= kCompute;
+    // Warps 0-15 own the state and do the per-chunk CUDA-core work; warps
+    // 16-19 are auxiliary.  Warps 16 and 17 issue the MMAs, splitting each
+    // batch between independent accumulators (lane 0 of each), and warp 16
+    // the TMA copies; all four run the off-diagonal levels of the triangular
+    // inverse while the state warps read back the previous chunk's state
+    // and outputs.
+    const bool aux = tid >= kCompute;
+    const int aw = warp - kCompute / 32;  // auxiliary warp index 0..3
+    const bool issuer_warp = aux && aw < 2;
+    const bool issuer_a = aux && aw == 0;
     const int wq = warp & 3;        // TMEM lane quarter of this warp
     const int iq = (warp >> 2) & 3; // which quarter of the key channels / tokens this warp takes
     const int head = blockIdx.x;    // b * HV + hv
@@ -301,17 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
     };
     auto csync = [&]() { named_sync(kBarCompute, kCompute); };
-    // compute warps hand a finished operand set to the issuer warp and go on
-    auto handoff = [&](int id) {
+    // state warps hand a finished operand set over and go on
+    auto handoff = [&](int id, int count) {
         fence_async_smem();
         tc_fence_before_sync();
-        named_arrive(id, kThreads);
+        named_arrive(id, count);
     };
 
     const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == kCompute) {
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_mma, 2);  // one arrival per issuing thread per batch
         mbar_init(bar_kqg, 1);
         mbar_init(bar_v, 1);
         *abort_flag = 0;
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm.o);
     }
     __syncthreads();
-    if (issuer_warp) {  // first chunk's inputs
+    if (issuer_a) {  // first chunk's inputs
         issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv, lane);
         if (lane == 0) issue_v(smem, tm, bar_v, b, 0, hv);
     }
@@ -340,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float S[32];
 #pragma unroll
     for (int u = 0; u < 32; ++u)
-        S[u] = (HAS_H0 && !issuer_warp) ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
+        S[u] = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -351,14 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Software pipeline: iteration c finishes the state products of chunk c
     // (scan) and prepares chunk c + 1 (prep), so each wait for a tensor-core
-    // batch of one has the other's CUDA-core work in front of it.  One warp
-    // issues every MMA and TMA copy; the compute warps hand operands over
-    // with named-barrier arrivals and never wait for the issue itself.
+    // batch of one has the other's CUDA-core work in front of it.  The
+    // issuer warps issue every MMA and TMA copy; the state warps hand
+    // operands over with named-barrier arrivals and never wait for the issue.
     //   1 prep: prefix sums, scales          (scan's batch 3 in flight)
     //   2 scan: U^T read-back   -> H1: batch 4
     //   3 prep: operand tiles   -> H2: gram, next k/q/g copies
-    //   4 scan: dS and O read-back, outputs; S'^T for the prepared chunk
-    //   5 prep: A and P, inverse -> H3: batch 2
+    //   5 prep: A and P, diagonal inverses -> the auxiliary warps: off-diagonal levels
+    //   4 scan: state and O read-back, outputs; S'^T for the prepared chunk
+    //                           -> S4 (with the levels done): batch 2
     //   6 prep: (T'Lk)^T read-back -> H4: next v copy, the next scan's batch 3
     for (int c = -1; c < NC; ++c) {
         const bool has_scan = c >= 0;
@@ -369,93 +383,160 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
         const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
         const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
+        (void)L;
 
-        // No block-wide barrier per chunk: the issuer warp meets the compute
-        // warps only at the four handoffs, so the compute warps start the next
-        // chunk while the issuer is still feeding the previous batch.  After
-        // a timed-out wait (sticky abort flag) every thread still runs every
-        // iteration and every barrier, but waits return at once and nothing
-        // new is issued.
-        if (issuer_warp) {
-            // ============ issuer warp: one lane issues, the warp follows the handoffs
+        // No block-wide barrier per chunk: the groups meet only at named
+        // barriers.  After a timed-out wait (sticky abort flag) every thread
+        // still runs every iteration and every barrier, but waits return at
+        // once and nothing new is issued.
+        if (aux) {
+            // ============ auxiliary warps
             const uint32_t io = idesc_bf16(128, 64, false, false, false);
-            if (has_scan) {
-                named_sync(kBarH1, kThreads);
-                if (lane == 0 && !*abort_flag) {  // batch 4: O^T += U^T P^T, dS^T = U^T R, A = U^T in TMEM
+            if (has_scan && issuer_warp) {
+                named_sync(kBarH1, kHand);
+                if (lane == 0 && !*abort_flag) {  // batch 4, A = U^T (bf16) in TMEM
                     tc_fence_after_sync();
-                    const uint32_t ids = idesc_bf16(128, 128, false, true, false);
-                    for (int ks = 0; ks < kC / 16; ++ks) {
-                        mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
-                                    smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
-                        mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
-                                    smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids,
-                                    ks > 0 ? 1u : 0u);
+                    if (issuer_a) {  // O^T += U^T P^T
+                        for (int ks = 0; ks < kC / 16; ++ks)
+                            mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
+                                        smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
+                    } else {  // dS^T = U^T R (R read transposed)
+                        const uint32_t ids = idesc_bf16(128, 128, false, true, false);
+                        for (int ks = 0; ks < kC / 16; ++ks)
+                            mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
+                                        smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids,
+                                        ks > 0 ? 1u : 0u);
                     }
                     mma_commit(bar_mma);
                 }
             }
             if (has_prep) {
-                named_sync(kBarH2, kThreads);
-                const bool slow = *slow_flag != 0;
-                const bool live = !*abort_flag;  // one warp-wide read: uniform
-                if (!slow && live) {
-                    if (lane == 0) {  // gram [Lk; Lq] R^T
-                        tc_fence_after_sync();
-                        gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128, kD * 16,
-                             io, kD / 16, false);
-                        mma_commit(bar_mma);
-                    }
-                    // the raw k, q, g tiles are consumed: fetch the next chunk's
-                    if (has_next2) {
-                        issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
-                        ++issued_kqg;
+                bool slow = false, live = true;
+                if (issuer_warp) {
+                    named_sync(kBarH2, kHand);
+                    slow = *slow_flag != 0;
+                    live = !*abort_flag;  // one warp-wide read: uniform
+                    if (!slow && live) {
+                        if (lane == 0) {  // gram [Lk; Lq] R^T: one accumulator, thread A alone
+                            if (issuer_a) {
+                                tc_fence_after_sync();
+                                gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128,
+                                     kD * 16, io, kD / 16, false);
+                                mma_commit(bar_mma);
+                            } else {
+                                mbar_arrive(bar_mma);
+                            }
+                        }
+                        // the raw k, q, g tiles are consumed: fetch the next chunk's
+                        if (issuer_a && has_next2) {
+                            issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                            ++issued_kqg;
+                        }
                     }
                 }
-                named_sync(kBarH3, kThreads);
-                if (slow && has_next2 && live) {  // the exact path read the raw tiles until now
+                named_sync(kBarDiag, kThreads);  // A and the diagonal inverses are done
+                if (issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until now
                     issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
                     ++issued_kqg;
                 }
-                if (lane == 0 && live) {  // batch 2: (T'Lk)^T and (T'V)^T
-                    wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
-                    tc_fence_after_sync();
-                    // Lk read transposed: MN-major (k = s, mn = i), K stride 2048, MN 128
-                    gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
-                         idesc_bf16(128, 64, true, false, false), kC / 16, false);
-                    // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
-                    const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-                    for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
-                                 smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
-                                 ks > 0 ? 1u : 0u);
-                    mma_commit(bar_mma);
+                const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
+                auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
+                    const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 16 * J + 8 * nt + 2 * tq;
+                        const float b0 = bvec[col], b1 = bvec[col + 1];
+                        sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
+                        sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
+                        sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
+                        sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
+                        *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
+                            pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
+                        *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
+                            pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
+                    }
+                };
+                if (aw < 2) {  // level 1: blocks (1,0) and (3,2)
+                    const int I = 2 * aw + 1, J = 2 * aw;
+                    float acc[2][4] = {};
+                    blk_mma(acc, blkA(I, J), blkT(J, J), lane);
+                    blk_store(sX + 256 * aw, acc, lane);
+                    __syncwarp();
+                    float y[2][4] = {};
+                    blk_mma(y, blkT(I, I), blkX(aw), lane);
+                    emit(I, J, y);
                 }
-                named_sync(kBarH4, kThreads);
-                if (lane == 0 && live) {
-                    if (has_next2) {  // batch 2 is done, so v's buffer is free
-                        issue_v(smem, tm, bar_v, b, t0n + kC, hv);
-                        ++issued_v;
+                named_sync(kBarAux, kThreads - kCompute);
+                {  // level 2, X = [A_20 A_21; A_30 A_31] T1
+                    const int I = 2 + (aw >> 1), J = aw & 1;
+                    float acc[2][4] = {};
+                    if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
+                    blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
+                    blk_store(sX + 256 * aw, acc, lane);  // X_IJ at slot 2 (I - 2) + J
+                }
+                named_sync(kBarAux, kThreads - kCompute);
+                {  // level 2, T_IJ = -T2 X
+                    const int I = 2 + (aw >> 1), J = aw & 1;
+                    float acc[2][4] = {};
+                    blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
+                    if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
+                    emit(I, J, acc);
+                }
+                fence_async_smem();  // T' is read by the tensor core
+                named_sync(kBarAux, kThreads - kCompute);
+                if (issuer_warp) {
+                    named_sync(kBarS4, kHand);  // S' in TMEM, the staging box read
+                    if (lane == 0 && live) {  // batch 2
+                        if (issuer_a) {  // (T'Lk)^T; Lk read transposed: MN-major (k = s, mn = i)
+                            tc_fence_after_sync();
+                            gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
+                                 idesc_bf16(128, 64, true, false, false), kC / 16, false);
+                        } else {  // (T'V)^T; V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart)
+                            wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
+                            tc_fence_after_sync();
+                            const uint32_t vid = idesc_bf16(128, 64, true, false, false);
+                            for (int ks = 0; ks < kC / 16; ++ks)
+                                mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
+                                         smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
+                                         ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar_mma);
                     }
-                    tc_fence_after_sync();
-                    // U^T += S'^T (-(T'Lk))^T  and  O^T = S'^T Lq^T, A = S'^T (bf16) in TMEM
-                    const uint32_t iu = idesc_bf16(128, 64, false, true, false);
-                    for (int ks = 0; ks < kD / 16; ++ks) {
-                        mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
-                                    smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
-                        mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
-                                    smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16), io,
-                                    ks > 0 ? 1u : 0u);
+                    named_sync(kBarH4, kHand);
+                    if (lane == 0 && live) {  // batch 3, A = S'^T (bf16) in TMEM
+                        if (issuer_a && has_next2) {  // batch 2 is done, so v's buffer is free
+                            issue_v(smem, tm, bar_v, b, t0n + kC, hv);
+                            ++issued_v;
+                        }
+                        tc_fence_after_sync();
+                        if (issuer_a) {  // U^T += S'^T (-(T'Lk))^T
+                            const uint32_t iu = idesc_bf16(128, 64, false, true, false);
+                            for (int ks = 0; ks < kD / 16; ++ks)
+                                mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
+                                            smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
+                        } else {  // O^T = S'^T Lq^T
+                            for (int ks = 0; ks < kD / 16; ++ks)
+                                mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
+                                            smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16),
+                                            io, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar_mma);
                     }
-                    mma_commit(bar_mma);
                 }
             }
             continue;
         }
 
-        // ============ compute warps
-        float beta_n2 = 0.f;  // beta of chunk cn + 1, stored in step 6
-        if (has_next2 && tid < kC && t0n + kC + tid < T)
-            beta_n2 = beta[((size_t)b * T + t0n + kC + tid) * HV + hv];
+        // ============ state warps
+        // beta of chunk cn + 1 straight into its buffer (read from step 5 of
+        // the next iteration on; the wait is in step 6)
+        if (has_next2 && tid < kC) {
+            float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
+            if (t0n + kC + tid < T)
+                cp_async4(dst, beta + ((size_t)b * T + t0n + kC + tid) * HV + hv);
+            else
+                *dst = 0.f;
+        }
 
         // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
         bool slow = false;
@@ -508,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
             tmem_st8(tl + kTmUTb + 8 * iq, w);
             tmem_st_wait();
-            handoff(kBarH1);
+            handoff(kBarH1, kHand);
         }
 
         // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
@@ -561,64 +642,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ch = ((id >> 3) & 15) * 8;
                 *reinterpret_cast<uint4 *>(smem + kOpR + kmajor_off(r, ch, kD)) = pack_bf16x8(rkeep[it]);
             }
-            handoff(kBarH2);
+            handoff(kBarH2, kHand);
         } else if (has_scan) {
             mma_wait(mma_phase);  // batch 4 of the last chunk
         }
 
-        // ---------------- 4 scan: dS^T and O^T read-back, state update, outputs
-        if (has_scan) {
-            {
-                const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
-                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kGamL, ps) + 32 * iq);
-                float dd[32];
-                tmem_ld32(tl + kTmDS + 32 * iq, dd);
-#pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 cl = cl4[u4], gm = gam4[u4];
-                    S[4 * u4 + 0] = fmaf(gm.x, S[4 * u4 + 0], cl.x * dd[4 * u4 + 0]);
-                    S[4 * u4 + 1] = fmaf(gm.y, S[4 * u4 + 1], cl.y * dd[4 * u4 + 1]);
-                    S[4 * u4 + 2] = fmaf(gm.z, S[4 * u4 + 2], cl.z * dd[4 * u4 + 2]);
-                    S[4 * u4 + 3] = fmaf(gm.w, S[4 * u4 + 3], cl.w * dd[4 * u4 + 3]);
-                }
-                // O^T -> bf16 O [r][j] staging
-                float oo[16];
-                tmem_ld16(tl + kTmOT + 16 * iq, oo);
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
-            }
-            fence_async_smem();
-            tc_fence_before_sync();
-            csync();
-            // one TMA store of the chunk's [64 x 128] output box; rows past
-            // the end of the sequence fall outside the tensor and are dropped
-            if (tid == 0 && !*abort_flag) {
-                tma_store_4d(&tm.o, smem + kStage, 0, hv, t0, b);
-                bulk_commit_group();
-            }
-        }
-        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
-        // in TMEM (S now holds that chunk's starting state); batch 3 of chunk
-        // c, its previous reader, finished in step 2
+        // ---------------- 5 prep: A (f32) and P (bf16), diagonal inverses
         if (has_prep) {
-            const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
-            uint32_t w[16];
-#pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4) {
-                const float4 e = egm4[u4];
-                w[2 * u4] = pack_bf16x2(S[4 * u4] * e.x, S[4 * u4 + 1] * e.y);
-                w[2 * u4 + 1] = pack_bf16x2(S[4 * u4 + 2] * e.z, S[4 * u4 + 3] * e.w);
-            }
-            tmem_st16(tl + kTmSTb + 16 * iq, w);
-            tmem_st_wait();
-        }
-
-        // ---------------- 5 prep: A (f32) and P (bf16), the inverse
-        if (has_prep) {
-            // the staging box is rewritten in step 6: the store must have read
-            // it (ordered before those writes by the barriers below)
-            if (tid == 0) bulk_wait_read_all();
             const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
             if (!slow) {
                 mma_wait(mma_phase);  // gram of chunk cn
@@ -684,53 +714,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
                 opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
             }
-            csync();
-            // off-diagonal blocks by 32 x 32 block recursion:
-            //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
-            //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
-            auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
-                const int gq = lane >> 2, tq = lane & 3;
+            handoff(kBarDiag, kThreads);  // the auxiliary warps take the off-diagonal levels
+        }
+
+        // ---------------- 4 scan: dS^T and O^T read-back, state update, outputs
+        if (has_scan) {
+            {
+                const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
+                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kGamL, ps) + 32 * iq);
+                float dd[32];
+                tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * J + 8 * nt + 2 * tq;
-                    const float b0 = bvec[col], b1 = bvec[col + 1];
-                    sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
-                    sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
-                    sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
-                    sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
-                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
-                        pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
-                    *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
-                        pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 cl = cl4[u4], gm = gam4[u4];
+                    S[4 * u4 + 0] = fmaf(gm.x, S[4 * u4 + 0], cl.x * dd[4 * u4 + 0]);
+                    S[4 * u4 + 1] = fmaf(gm.y, S[4 * u4 + 1], cl.y * dd[4 * u4 + 1]);
+                    S[4 * u4 + 2] = fmaf(gm.z, S[4 * u4 + 2], cl.z * dd[4 * u4 + 2]);
+                    S[4 * u4 + 3] = fmaf(gm.w, S[4 * u4 + 3], cl.w * dd[4 * u4 + 3]);
                 }
-            };
-            if (warp < 2) {  // level 1: blocks (1,0) and (3,2)
-                const int I = 2 * warp + 1, J = 2 * warp;
-                float acc[2][4] = {};
-                blk_mma(acc, blkA(I, J), blkT(J, J), lane);
-                blk_store(sX + 256 * warp, acc, lane);
-                __syncwarp();
-                float y[2][4] = {};
-                blk_mma(y, blkT(I, I), blkX(warp), lane);
-                emit(I, J, y);
+                // O^T -> bf16 O [r][j] staging
+                float oo[16];
+                tmem_ld16(tl + kTmOT + 16 * iq, oo);
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
             }
+            fence_async_smem();
+            tc_fence_before_sync();
             csync();
-            if (warp < 4) {  // level 2, X = [A_20 A_21; A_30 A_31] T1
-                const int I = 2 + (warp >> 1), J = warp & 1;
-                float acc[2][4] = {};
-                if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
-                blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
-                blk_store(sX + 256 * warp, acc, lane);  // X_IJ at slot 2 (I - 2) + J
+            // one TMA store of the chunk's [64 x 128] output box; rows past
+            // the end of the sequence fall outside the tensor and are dropped
+            if (tid == 0 && !*abort_flag) {
+                tma_store_4d(&tm.o, smem + kStage, 0, hv, t0, b);
+                bulk_commit_group();
             }
-            csync();
-            if (warp < 4) {  // level 2, T_IJ = -T2 X
-                const int I = 2 + (warp >> 1), J = warp & 1;
-                float acc[2][4] = {};
-                blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
-                if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
-                emit(I, J, acc);
+        }
+        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
+        // in TMEM (S now holds that chunk's starting state); batch 3 of chunk
+        // c, its previous reader, finished in step 2.  Then the issuers may
+        // start batch 2, which also allows the staging box to be rewritten
+        // (with W), so the output store must have read it first.
+        if (has_prep) {
+            const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
+            uint32_t w[16];
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 e = egm4[u4];
+                w[2 * u4] = pack_bf16x2(S[4 * u4] * e.x, S[4 * u4 + 1] * e.y);
+                w[2 * u4 + 1] = pack_bf16x2(S[4 * u4 + 2] * e.z, S[4 * u4 + 3] * e.w);
             }
-            handoff(kBarH3);  // T' (and S'^T in TMEM) are complete: batch 2
+            tmem_st16(tl + kTmSTb + 16 * iq, w);
+            tmem_st_wait();
+            if (tid == 0) bulk_wait_read_all();
+            handoff(kBarS4, kHand);
         }
 
         // ---------------- 6 prep: -(T'Lk)^T read-back -> the next scan's batch 3
@@ -747,9 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 16 * iq + 8 * q8, kD)) =
                         pack_bf16x8(&dd[8 * q8]);
             }
-            if (has_next2 && tid < kC)
-                reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1))[tid] = beta_n2;
-            handoff(kBarH4);
+            if (has_next2 && tid < kC) cp_async_wait_all();  // beta of chunk cn + 1
+            handoff(kBarH4, kHand);
         }
     }
 
@@ -763,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(bar_kqg, (uint32_t)((issued_kqg - 1) & 1), kWaitLimitNs);
         mbar_wait_bounded(bar_v, (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
     }
-    if (!aborted && STORE_HT && !issuer_warp) {
+    if (!aborted && STORE_HT && !aux) {
 #pragma unroll
         for (int u = 0; u < 32; ++u) ht[((size_t)head * kD + 32 * iq + u) * kD + j] = S[u];
     }
