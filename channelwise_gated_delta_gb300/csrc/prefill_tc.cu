@@ -38,24 +38,27 @@
 // factors <= 1) and computes A and P with exact pairwise decays on CUDA
 // cores, so the result is right for any g <= 0.
 //
-// GB300 mapping.  One CTA (16 warps) per (batch, value head) walks that
-// head's chunks in order; the float32 state never leaves registers (thread =
-// one value column j, 32 of the 128 key rows).  State products are computed
-// transposed so that M = dv = 128 fills the MMA:
-//   U^T = (T'V)^T - S'^T (T'Lk)^T,  O^T = S'^T Lq^T + U^T P^T,  dS^T = U^T R.
+// GB300 mapping.  One CTA (16 state warps + 4 auxiliary warps) per (batch,
+// value head) walks that head's chunks in order; the float32 state never
+// leaves registers (thread = one value column j, 32 of the 128 key rows).
+// State products are computed transposed so that M = dv = 128 fills the MMA,
+// and T' is applied after the state product so that the inverse of the next
+// chunk is off the path from one chunk's state to the next:
+//   Z^T = S'^T Lk^T,  U^T = (V^T - Z^T) T'^T,  O^T = S'^T Lq^T + U^T P^T,
+//   dS^T = U^T R.
 // The per-chunk tiles are bf16 in shared memory in the interleaved (no-swizzle)
-// core-matrix layout (sm100_ptx.cuh); each of Lk, Lq and R is stored once
-// and read both K-major and, through an MN-major descriptor with the two
-// core-matrix strides exchanged, transposed.  The two state-dependent A
-// operands, S'^T and U^T, are written as bf16 straight into tensor memory
-// and read from there by the MMA.  Accumulators are float32 in TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
+// core-matrix layout (sm100_ptx.cuh); R is stored once and read both K-major
+// and, through an MN-major descriptor with the two core-matrix strides
+// exchanged, transposed.  The state-dependent A operands S'^T, -Z^T and U^T
+// are written as bf16 straight into tensor memory and read from there by the
+// MMA.  Accumulators are float32 in TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
 // swizzled boxes; rows past the end of the sequence are zero-filled by the
 // copy engine), the next chunk's copies in flight while the current chunk's
 // solve and state products run; v lands directly in the swizzled MN-major
 // layout the tensor core reads.  The 64 x 64 inverse runs in float32:
-// diagonal 16 x 16 blocks by a right-looking sweep (eight threads per
-// column), off-diagonal blocks by a 32 x 32 block recursion whose 16 x 16
-// products run on tf32 mma.sync, two or four warps per level.
+// diagonal 16 x 16 blocks by a right-looking sweep (one thread per column),
+// off-diagonal blocks by a 32 x 32 block recursion whose 16 x 16 products run
+// on tf32 mma.sync, on the four auxiliary warps.
 #include <cuda.h>
 #include <mutex>
 
@@ -73,10 +76,10 @@ constexpr int kCompute = 512;               // 16 state warps
 constexpr int kThreads = kCompute + 128;    // + 4 auxiliary warps: 2 issuers, 2 solvers
 constexpr int kHand = kCompute + 64;        // state warps + issuer warps
 constexpr int kBarCompute = 1;              // named barrier: state warps only
-constexpr int kBarH1 = 2, kBarH2 = 3, kBarH4 = 4;  // state -> issuer handoffs (kHand threads)
-constexpr int kBarS4 = 5;                   // state -> issuer: chunk outputs and S' done (kHand)
-constexpr int kBarDiag = 6;                 // state -> auxiliary: A and diagonal inverses done (all)
-constexpr int kBarAux = 7;                  // auxiliary warps only
+constexpr int kBarH1 = 2, kBarH2 = 3, kBarH4 = 4, kBarHZ = 5;  // state -> issuer handoffs (kHand threads)
+constexpr int kBarDiag = 6;                 // state -> solvers: A, P read back (kCompute + 64)
+constexpr int kBarAux = 7;                  // solver warps only (64)
+constexpr int kBarSolve = 8;                // solvers -> issuers: T' complete (128)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -87,25 +90,25 @@ constexpr uint32_t kRawQ = kRawK + 16384;     // q: same
 constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
 constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
 constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lk, 64-127 Lq
-constexpr uint32_t kOpR = kOpL + 32768;       // [64][128] K-major: R
-constexpr uint32_t kAT = kOpR + 16384;        // 32 KB: f32 A and T (64x64 each)
+constexpr uint32_t kOpR = kOpL + 32768;       // [2][64][128] K-major: R (by chunk parity)
+constexpr uint32_t kAT = kOpR + 32768;        // 32 KB: f32 A and T (64x64 each)
 constexpr uint32_t kA32 = kAT;
 constexpr uint32_t kT32 = kAT + 16384;
 constexpr uint32_t kOpT = kAT + 32768;        // T' as K-major B [64 r][64 s]
-constexpr uint32_t kOpP = kOpT + 8192;        // P as K-major B [64 r][64 s]
-constexpr uint32_t kOpWK = kOpP + 8192;       // -(T'Lk) as MN-major B (k = i, mn = r), K extent 128
-constexpr uint32_t kStage = kOpWK;            //   later: bf16 O [64][128] staging for the stores
-constexpr uint32_t kX32 = kOpWK + 16384;      // f32 [4][16][16] solve scratch
+constexpr uint32_t kOpP = kOpT + 8192;        // [2] P as K-major B [64 r][64 s] (by chunk parity)
+constexpr uint32_t kStage = kOpP + 16384;     // bf16 O [64][128] staging for the output store
+constexpr uint32_t kX32 = kStage + 16384;     // f32 [4][16][16] solve scratch
 constexpr uint32_t kSmall = kX32 + 4096;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
 constexpr uint32_t kEGm = kBeta + 512;        // f32 [2][128] exp(G_m) (by chunk parity)
 constexpr uint32_t kCL = kEGm + 1024;         // f32 [2][128] exp(G_last - G_m)
 constexpr uint32_t kGamL = kCL + 1024;        // f32 [2][128] exp(G_last)
-constexpr uint32_t kGm = kGamL + 1024;        // f32 [128] G_m (raw reference row)
-constexpr uint32_t kGl = kGm + 512;           // f32 [128] G_last
-constexpr uint32_t kTot = kGl + 512;          // f32 [3][128] prefix-sum carries
-constexpr uint32_t kBarMma = kTot + 1536;     // mbarrier: MMA batches
-constexpr uint32_t kBarKQG = kBarMma + 8;     // mbarrier: k, q, g tiles
+constexpr uint32_t kTot = kGamL + 1024;       // f32 [3][128] prefix-sum carries, then G_m and G_last
+constexpr uint32_t kBarA = kTot + 1536;       // mbarriers: MMA batches a, b, g, 4
+constexpr uint32_t kBarB = kBarA + 8;
+constexpr uint32_t kBarG = kBarB + 8;
+constexpr uint32_t kBar4 = kBarG + 8;
+constexpr uint32_t kBarKQG = kBar4 + 8;       // mbarrier: k, q, g tiles
 constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
 constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
 constexpr uint32_t kAbort = kTmemSlot + 4;    // i32 sticky abort flag
@@ -118,12 +121,13 @@ constexpr uint32_t kBytesV = 16384;
 
 // ---- TMEM columns (float32 accumulators, lane = M row)
 constexpr uint32_t kTmGram = 0;     // [128 x 64]: rows 0-63 Lk R^T, 64-127 Lq R^T
-constexpr uint32_t kTmWkT = 64;     // [128 i x 64 r]  (T' Lk)^T
+constexpr uint32_t kTmZT = 64;      // [128 j x 64 r]  Z^T = (Lk S')^T
 constexpr uint32_t kTmUT = 128;     // [128 j x 64 r]
 constexpr uint32_t kTmOT = 192;     // [128 j x 64 r]
 constexpr uint32_t kTmDS = 256;     // [128 j x 128 i]
 constexpr uint32_t kTmSTb = 384;    // S'^T as bf16 A operand: [128 j x 128 i], 2 per column
 constexpr uint32_t kTmUTb = 448;    // U^T as bf16 A operand: [128 j x 64 r], 2 per column
+constexpr uint32_t kTmZTb = 480;    // -Z^T as bf16 A operand: [128 j x 64 r], 2 per column
 constexpr uint32_t kTmemCols = 512;
 
 // 64 x 64 f32 tiles (A, T) with an XOR swizzle: rows and columns both walk
@@ -265,16 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // Warps 0-15 own the state and do the per-chunk CUDA-core work; warps
-    // 16-19 are auxiliary.  Warps 16 and 17 issue the MMAs, splitting each
-    // batch between independent accumulators (lane 0 of each), and warp 16
-    // the TMA copies; all four run the off-diagonal levels of the triangular
-    // inverse while the state warps read back the previous chunk's state
-    // and outputs.
+    // Warps 0-15 own the state and do the per-chunk element-wise work; warps
+    // 16-19 are auxiliary.  Warps 16 and 17 issue the MMAs (lane 0 of each,
+    // on independent accumulators) and warp 16 the TMA copies; warps 18 and
+    // 19 invert I + A for the next chunk while the state warps run the
+    // current chunk's state products.
     const bool aux = tid >= kCompute;
     const int aw = warp - kCompute / 32;  // auxiliary warp index 0..3
     const bool issuer_warp = aux && aw < 2;
     const bool issuer_a = aux && aw == 0;
+    const int sw = aw - 2;                // solver warp index 0..1
     const int wq = warp & 3;        // TMEM lane quarter of this warp
     const int iq = (warp >> 2) & 3; // which quarter of the key channels / tokens this warp takes
     const int head = blockIdx.x;    // b * HV + hv
@@ -282,13 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = hv / (HV / HK);
     const int j = 32 * wq + lane;   // this thread's value column (TMEM lane)
 
-    float *sGm = reinterpret_cast<float *>(smem + kGm);
-    float *sGl = reinterpret_cast<float *>(smem + kGl);
     float *sTot = reinterpret_cast<float *>(smem + kTot);
+    float *sGm = reinterpret_cast<float *>(smem + kTot);        // after the prefix sums
+    float *sGl = reinterpret_cast<float *>(smem + kTot + 512);  //   reuse the carries' space
     float *sA = reinterpret_cast<float *>(smem + kA32);
     float *sT = reinterpret_cast<float *>(smem + kT32);
     float *sX = reinterpret_cast<float *>(smem + kX32);
-    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(smem + kBarMma);
+    uint64_t *bar_a = reinterpret_cast<uint64_t *>(smem + kBarA);
+    uint64_t *bar_b = reinterpret_cast<uint64_t *>(smem + kBarB);
+    uint64_t *bar_g = reinterpret_cast<uint64_t *>(smem + kBarG);
+    uint64_t *bar_4 = reinterpret_cast<uint64_t *>(smem + kBar4);
     uint64_t *bar_kqg = reinterpret_cast<uint64_t *>(smem + kBarKQG);
     uint64_t *bar_v = reinterpret_cast<uint64_t *>(smem + kBarV);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemSlot);
@@ -308,23 +315,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto blkA = [&](int I, int J) { return [=](int r, int c) { return sA[sq_idx(16 * I + r, 16 * J + c)]; }; };
     auto blkT = [&](int I, int J) { return [=](int r, int c) { return sT[sq_idx(16 * I + r, 16 * J + c)]; }; };
     auto blkX = [&](int n) { const float *x = sX + 256 * n; return [=](int r, int c) { return x[r * 16 + c]; }; };
-    auto mma_wait = [&](uint32_t &phase) {
-        wait_bar(bar_mma, phase, abort_flag);
+    auto wait_on = [&](uint64_t *bar, uint32_t &phase) {
+        wait_bar(bar, phase, abort_flag);
         phase ^= 1u;
         tc_fence_after_sync();
     };
     auto csync = [&]() { named_sync(kBarCompute, kCompute); };
-    // state warps hand a finished operand set over and go on
+    // State warps hand a finished operand set over and go on.  In normal
+    // operation the mbarrier waits on each batch keep the state warps from
+    // lapping the auxiliary warps on these arrive-only barriers; after a
+    // timeout those waits return at once, so every handoff then blocks.
     auto handoff = [&](int id, int count) {
         fence_async_smem();
         tc_fence_before_sync();
-        named_arrive(id, count);
+        if (*abort_flag)
+            named_sync(id, count);
+        else
+            named_arrive(id, count);
     };
 
     const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == kCompute) {
-        mbar_init(bar_mma, 2);  // one arrival per issuing thread per batch
+        mbar_init(bar_a, 2);  // both issuers commit batch a
+        mbar_init(bar_b, 1);
+        mbar_init(bar_g, 1);
+        mbar_init(bar_4, 2);  // both issuers commit batch 4
         mbar_init(bar_kqg, 1);
         mbar_init(bar_v, 1);
         *abort_flag = 0;
@@ -349,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((s0 >> 4) > (r >> 4))
             *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
-    // state: S[32*iq + u][j], u = 0..31 (compute warps)
+    // state: S[32*iq + u][j], u = 0..31 (state warps)
     float S[32];
 #pragma unroll
     for (int u = 0; u < 32; ++u)
@@ -359,73 +375,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
-    uint32_t mma_phase = 0;
+    uint32_t ph_a = 0, ph_b = 0, ph_g = 0, ph_4 = 0;
     int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer lane 0's count is used)
 
-    // Software pipeline: iteration c finishes the state products of chunk c
-    // (scan) and prepares chunk c + 1 (prep), so each wait for a tensor-core
-    // batch of one has the other's CUDA-core work in front of it.  The
-    // issuer warps issue every MMA and TMA copy; the state warps hand
-    // operands over with named-barrier arrivals and never wait for the issue.
-    //   1 prep: prefix sums, scales          (scan's batch 3 in flight)
-    //   2 scan: U^T read-back   -> H1: batch 4
-    //   3 prep: operand tiles   -> H2: gram, next k/q/g copies
-    //   5 prep: A and P, diagonal inverses -> the auxiliary warps: off-diagonal levels
-    //   4 scan: state and O read-back, outputs; S'^T for the prepared chunk
-    //                           -> S4 (with the levels done): batch 2
-    //   6 prep: (T'Lk)^T read-back -> H4: next v copy, the next scan's batch 3
+    // Two-stage pipeline: iteration c runs the state products of chunk c
+    // (scan) and prepares chunk c + 1 (prep).  U = T'(V - Lk S') is formed as
+    // Z = Lk S' first and T' applied afterwards, so the inverse of chunk c+1
+    // is not on the path from one chunk's state to the next: the auxiliary
+    // warps compute it while the state warps read back chunk c.
+    //   state warps                                     MMA batch issued after the handoff
+    //   1 prep: prefix sums, scales of chunk c+1
+    //   2 scan: -Z^T read-back (bf16, TMEM)         HZ:  b: U^T = V^T T'^T - Z^T T'^T
+    //   3 prep: Lk, Lq, R tiles                     H2:  g: gram [Lk; Lq] R^T, next k/q/g copies
+    //   4 scan: U^T read-back (bf16, TMEM)          H1:  4: O^T += U^T P^T, dS^T = U^T R; next v copy
+    //   5 prep: A and P read-back                   DIAG: the auxiliary warps invert I + A
+    //   6 scan: state and O read-back, O store; S'^T of chunk c+1
+    //                                               H4:  a: [Z^T | O^T] = S'^T [Lk; Lq]^T
     for (int c = -1; c < NC; ++c) {
         const bool has_scan = c >= 0;
         const bool has_prep = c + 1 < NC;
         const int cn = c + 1;                          // chunk being prepared
-        const int t0 = c * kC, L = has_scan ? min(kC, T - t0) : 0;
+        const int t0 = c * kC;
         const int t0n = cn * kC, Ln = has_prep ? min(kC, T - t0n) : 0;
         const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
         const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
         const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
-        (void)L;
 
         // No block-wide barrier per chunk: the groups meet only at named
-        // barriers.  After a timed-out wait (sticky abort flag) every thread
-        // still runs every iteration and every barrier, but waits return at
-        // once and nothing new is issued.
+        // barriers and mbarriers.  After a timed-out wait (sticky abort flag)
+        // every thread still runs every iteration and every barrier, but
+        // waits return at once and nothing new is issued.
         if (aux) {
             // ============ auxiliary warps
             const uint32_t io = idesc_bf16(128, 64, false, false, false);
-            if (has_scan && issuer_warp) {
-                named_sync(kBarH1, kHand);
-                if (lane == 0 && !*abort_flag) {  // batch 4, A = U^T (bf16) in TMEM
-                    tc_fence_after_sync();
-                    if (issuer_a) {  // O^T += U^T P^T
-                        for (int ks = 0; ks < kC / 16; ++ks)
-                            mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
-                                        smem_desc(sbase + kOpP + ks * 256, 128, kC * 16), io, 1u);
-                    } else {  // dS^T = U^T R (R read transposed)
-                        const uint32_t ids = idesc_bf16(128, 128, false, true, false);
-                        for (int ks = 0; ks < kC / 16; ++ks)
-                            mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
-                                        smem_desc(sbase + kOpR + ks * 4096, kD * 16, 128), ids,
-                                        ks > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar_mma);
-                }
-            }
-            if (has_prep) {
+            if (issuer_warp) {
                 bool slow = false, live = true;
-                if (issuer_warp) {
+                if (has_scan) {
+                    named_sync(kBarHZ, kHand);
+                    named_sync(kBarSolve, 128);  // T' of chunk c is complete
+                    if (issuer_a && lane == 0 && !*abort_flag) {
+                        // b: U^T = V^T T'^T + (-Z^T) T'^T, one accumulator
+                        wait_bar(bar_v, (uint32_t)(c & 1), abort_flag);
+                        tc_fence_after_sync();
+                        // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
+                        const uint32_t vid = idesc_bf16(128, 64, true, false, false);
+                        for (int ks = 0; ks < kC / 16; ++ks)
+                            mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
+                                     smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
+                                     ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < kC / 16; ++ks)
+                            mma_bf16_ts(tmem + kTmUT, tmem + kTmZTb + 8 * ks,
+                                        smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), io, 1u);
+                        mma_commit(bar_b);
+                    }
+                }
+                if (has_prep) {
                     named_sync(kBarH2, kHand);
                     slow = *slow_flag != 0;
                     live = !*abort_flag;  // one warp-wide read: uniform
                     if (!slow && live) {
-                        if (lane == 0) {  // gram [Lk; Lq] R^T: one accumulator, thread A alone
-                            if (issuer_a) {
-                                tc_fence_after_sync();
-                                gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR, 128,
-                                     kD * 16, io, kD / 16, false);
-                                mma_commit(bar_mma);
-                            } else {
-                                mbar_arrive(bar_mma);
-                            }
+                        if (issuer_a && lane == 0) {  // g: gram [Lk; Lq] R^T
+                            tc_fence_after_sync();
+                            gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR + pn * 16384, 128,
+                                 kD * 16, io, kD / 16, false);
+                            mma_commit(bar_g);
                         }
                         // the raw k, q, g tiles are consumed: fetch the next chunk's
                         if (issuer_a && has_next2) {
@@ -434,12 +447,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                named_sync(kBarDiag, kThreads);  // A and the diagonal inverses are done
-                if (issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until now
-                    issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
-                    ++issued_kqg;
+                if (has_scan) {
+                    named_sync(kBarH1, kHand);
+                    if (lane == 0 && !*abort_flag) {  // 4, A = U^T (bf16) in TMEM
+                        tc_fence_after_sync();
+                        if (issuer_a) {  // O^T += U^T P^T
+                            for (int ks = 0; ks < kC / 16; ++ks)
+                                mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
+                                            smem_desc(sbase + kOpP + ps * 8192 + ks * 256, 128, kC * 16),
+                                            io, 1u);
+                        } else {  // dS^T = U^T R (R read transposed)
+                            const uint32_t ids = idesc_bf16(128, 128, false, true, false);
+                            for (int ks = 0; ks < kC / 16; ++ks)
+                                mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
+                                            smem_desc(sbase + kOpR + ps * 16384 + ks * 4096, kD * 16, 128),
+                                            ids, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar_4);
+                        // batch b of chunk c has completed (the state warps waited
+                        // for it): v's buffer takes the prepared chunk's
+                        if (issuer_a && has_prep) {
+                            issue_v(smem, tm, bar_v, b, t0n, hv);
+                            ++issued_v;
+                        }
+                    }
                 }
+                if (has_prep) {
+                    named_sync(kBarH4, kHand);
+                    if (issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
+                        issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                        ++issued_kqg;
+                    }
+                    if (lane == 0 && !*abort_flag) {
+                        // a: Z^T = S'^T Lk^T (thread A) and O^T = S'^T Lq^T (thread B), A = S'^T in TMEM
+                        tc_fence_after_sync();
+                        const uint32_t dst = issuer_a ? kTmZT : kTmOT;
+                        const uint32_t rows = issuer_a ? 0u : 16384u;  // Lk rows 0-63, Lq rows 64-127
+                        for (int ks = 0; ks < kD / 16; ++ks)
+                            mma_bf16_ts(tmem + dst, tmem + kTmSTb + 8 * ks,
+                                        smem_desc(sbase + kOpL + rows + ks * 256, 128, kD * 16), io,
+                                        ks > 0 ? 1u : 0u);
+                        mma_commit(bar_a);
+                    }
+                }
+            } else if (has_prep) {
+                // ---- solver warps: T' of chunk cn
+                named_sync(kBarDiag, kCompute + 64);  // A and P of chunk cn are read back
                 const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
+                // diagonal 16 x 16 blocks of T = (I + A)^-1: one thread per
+                // column (block I = t / 16, column jj = t % 16), right-looking;
+                // the column of A read at each step is the same for the 16
+                // threads of a block (broadcast loads)
+                {
+                    const int t = tid - kCompute - 64, I = t >> 4, jj = t & 15;
+                    float x[16];
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) x[p] = (p == jj) ? 1.f : 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < 15; ++s2) {
+#pragma unroll
+                        for (int p = s2 + 1; p < 16; ++p)
+                            x[p] = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s2)], x[s2], x[p]);
+                    }
+                    __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
+                    const float bj = bvec[16 * I + jj];
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        sT[sq_idx(16 * I + p, 16 * I + jj)] = x[p];
+                        opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x[p] * bj);
+                    }
+                }
+                named_sync(kBarAux, 64);
+                // off-diagonal blocks by 32 x 32 block recursion:
+                //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
+                //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
                 auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
                     const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
@@ -456,87 +537,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
                     }
                 };
-                if (aw < 2) {  // level 1: blocks (1,0) and (3,2)
-                    const int I = 2 * aw + 1, J = 2 * aw;
+                {  // level 1: block (1,0) on solver 0, (3,2) on solver 1
+                    const int I = 2 * sw + 1, J = 2 * sw;
                     float acc[2][4] = {};
                     blk_mma(acc, blkA(I, J), blkT(J, J), lane);
-                    blk_store(sX + 256 * aw, acc, lane);
+                    blk_store(sX + 256 * sw, acc, lane);
                     __syncwarp();
                     float y[2][4] = {};
-                    blk_mma(y, blkT(I, I), blkX(aw), lane);
+                    blk_mma(y, blkT(I, I), blkX(sw), lane);
                     emit(I, J, y);
                 }
-                named_sync(kBarAux, kThreads - kCompute);
-                {  // level 2, X = [A_20 A_21; A_30 A_31] T1
-                    const int I = 2 + (aw >> 1), J = aw & 1;
-                    float acc[2][4] = {};
-                    if (J == 0) blk_mma(acc, blkA(I, 0), blkT(0, 0), lane);
-                    blk_mma(acc, blkA(I, 1), blkT(1, J), lane);
-                    blk_store(sX + 256 * aw, acc, lane);  // X_IJ at slot 2 (I - 2) + J
+                named_sync(kBarAux, 64);
+                {  // level 2, row I = 2 + sw of X = [A_20 A_21; A_30 A_31] T1 (slots 2 (I - 2) + J)
+                    const int I = 2 + sw;
+                    float x0[2][4] = {}, x1[2][4] = {};
+                    blk_mma(x0, blkA(I, 0), blkT(0, 0), lane);
+                    blk_mma(x0, blkA(I, 1), blkT(1, 0), lane);
+                    blk_mma(x1, blkA(I, 1), blkT(1, 1), lane);
+                    blk_store(sX + 256 * (2 * sw), x0, lane);
+                    blk_store(sX + 256 * (2 * sw + 1), x1, lane);
                 }
-                named_sync(kBarAux, kThreads - kCompute);
-                {  // level 2, T_IJ = -T2 X
-                    const int I = 2 + (aw >> 1), J = aw & 1;
-                    float acc[2][4] = {};
-                    blk_mma(acc, blkT(I, 2), blkX(J), lane);  // T_I2 X_2J
-                    if (I == 3) blk_mma(acc, blkT(3, 3), blkX(2 + J), lane);
-                    emit(I, J, acc);
+                named_sync(kBarAux, 64);
+                {  // level 2, column J = sw of T_lo = -T2 X
+                    const int J = sw;
+                    float t2[2][4] = {}, t3[2][4] = {};
+                    blk_mma(t2, blkT(2, 2), blkX(J), lane);      // T_22 X_2J
+                    blk_mma(t3, blkT(3, 2), blkX(J), lane);      // T_32 X_2J
+                    blk_mma(t3, blkT(3, 3), blkX(2 + J), lane);  // + T_33 X_3J
+                    emit(2, J, t2);
+                    emit(3, J, t3);
                 }
                 fence_async_smem();  // T' is read by the tensor core
-                named_sync(kBarAux, kThreads - kCompute);
-                if (issuer_warp) {
-                    named_sync(kBarS4, kHand);  // S' in TMEM, the staging box read
-                    if (lane == 0 && live) {  // batch 2
-                        if (issuer_a) {  // (T'Lk)^T; Lk read transposed: MN-major (k = s, mn = i)
-                            tc_fence_after_sync();
-                            gemm(tmem + kTmWkT, sbase + kOpL, kD * 16, 128, sbase + kOpT, 128, kC * 16,
-                                 idesc_bf16(128, 64, true, false, false), kC / 16, false);
-                        } else {  // (T'V)^T; V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart)
-                            wait_bar(bar_v, (uint32_t)(cn & 1), abort_flag);
-                            tc_fence_after_sync();
-                            const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-                            for (int ks = 0; ks < kC / 16; ++ks)
-                                mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
-                                         smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
-                                         ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar_mma);
-                    }
-                    named_sync(kBarH4, kHand);
-                    if (lane == 0 && live) {  // batch 3, A = S'^T (bf16) in TMEM
-                        if (issuer_a && has_next2) {  // batch 2 is done, so v's buffer is free
-                            issue_v(smem, tm, bar_v, b, t0n + kC, hv);
-                            ++issued_v;
-                        }
-                        tc_fence_after_sync();
-                        if (issuer_a) {  // U^T += S'^T (-(T'Lk))^T
-                            const uint32_t iu = idesc_bf16(128, 64, false, true, false);
-                            for (int ks = 0; ks < kD / 16; ++ks)
-                                mma_bf16_ts(tmem + kTmUT, tmem + kTmSTb + 8 * ks,
-                                            smem_desc(sbase + kOpWK + ks * 256, 128, kD * 16), iu, 1u);
-                        } else {  // O^T = S'^T Lq^T
-                            for (int ks = 0; ks < kD / 16; ++ks)
-                                mma_bf16_ts(tmem + kTmOT, tmem + kTmSTb + 8 * ks,
-                                            smem_desc(sbase + kOpL + 16384 + ks * 256, 128, kD * 16),
-                                            io, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar_mma);
-                    }
-                }
+                if (*abort_flag)
+                    named_sync(kBarSolve, 128);
+                else
+                    named_arrive(kBarSolve, 128);
             }
             continue;
         }
 
         // ============ state warps
         // beta of chunk cn + 1 straight into its buffer (read from step 5 of
-        // the next iteration on; the wait is in step 6)
-        if (has_next2 && tid < kC) {
-            float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
-            if (t0n + kC + tid < T)
-                cp_async4(dst, beta + ((size_t)b * T + t0n + kC + tid) * HV + hv);
-            else
-                *dst = 0.f;
-        }
+        // the next iteration on; the wait is at the end of step 6).  The
+        // buffer last held chunk c's beta, which the auxiliary warps read
+        // while inverting for chunk c: it is refilled only once batch b of
+        // chunk c, issued after that inverse, has completed (step 4).
+        auto prefetch_beta = [&]() {
+            if (has_next2 && tid < kC) {
+                float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
+                if (t0n + kC + tid < T)
+                    cp_async4(dst, beta + ((size_t)b * T + t0n + kC + tid) * HV + hv);
+                else
+                    *dst = 0.f;
+            }
+        };
+        if (!has_scan) prefetch_beta();
+        // the staging box is rewritten in step 6: the previous chunk's output
+        // store must have read it (ordered by the barriers of step 1)
+        if (tid == 0) bulk_wait_read_all();
 
         // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
         bool slow = false;
@@ -568,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bad = (gval(0, tid) - gm > kRangeLog2) || (gm - gl > kRangeLog2);
             }
             slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
-            if (tid == 0) *slow_flag = slow ? 1 : 0;  // read by the issuer after H2
+            if (tid == 0) *slow_flag = slow ? 1 : 0;  // read by the issuers after H2
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
@@ -578,23 +636,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vec(kGamL, pn)[tid] = fast_exp2(gl);
             }
         }
+        if (!has_prep) csync();  // orders thread 0's staging-box wait before step 6
 
-        // ---------------- 2 scan: U^T read-back as the bf16 A operand of batch 4
+        // ---------------- 2 scan: -Z^T read-back as the bf16 A operand of batch b
         if (has_scan) {
-            mma_wait(mma_phase);  // batch 3 of chunk c
+            wait_on(bar_a, ph_a);  // batch a of chunk c
             float dd[16];
-            tmem_ld16(tl + kTmUT + 16 * iq, dd);
+            tmem_ld16(tl + kTmZT + 16 * iq, dd);
             uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
-            tmem_st8(tl + kTmUTb + 8 * iq, w);
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(-dd[2 * e], -dd[2 * e + 1]);
+            tmem_st8(tl + kTmZTb + 8 * iq, w);
             tmem_st_wait();
-            handoff(kBarH1, kHand);
+            handoff(kBarHZ, kHand);
         }
 
         // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
         if (has_prep) {
-            float rkeep[2][8];
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int id = tid + kCompute * it;  // 0..1023
@@ -620,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) gm[e] = 0.f;
                 }
-                float lk[8], lq[8];
+                float lk[8], lq[8], rr[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float d = gv[e] - gm[e];
@@ -628,30 +686,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lk[e] = kv[e] * el;
                     lq[e] = qv[e] * el;
                     // fallback: R = exp(G_L - G) K directly (factor <= 1)
-                    rkeep[it][e] = kv[e] * fast_exp2(slow ? sGl[ch + e] - gv[e] : -d);
+                    rr[e] = kv[e] * fast_exp2(slow ? sGl[ch + e] - gv[e] : -d);
                 }
-                // Lk and Lq are not read by the scan's batch 4: write them now
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lq);
-            }
-            if (has_scan) mma_wait(mma_phase);  // batch 4 of chunk c has finished reading R
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int id = tid + kCompute * it;
-                const int r = ((id >> 7) << 3) | (id & 7);
-                const int ch = ((id >> 3) & 15) * 8;
-                *reinterpret_cast<uint4 *>(smem + kOpR + kmajor_off(r, ch, kD)) = pack_bf16x8(rkeep[it]);
+                *reinterpret_cast<uint4 *>(smem + kOpR + pn * 16384 + kmajor_off(r, ch, kD)) =
+                    pack_bf16x8(rr);
             }
             handoff(kBarH2, kHand);
-        } else if (has_scan) {
-            mma_wait(mma_phase);  // batch 4 of the last chunk
         }
 
-        // ---------------- 5 prep: A (f32) and P (bf16), diagonal inverses
+        // ---------------- 4 scan: U^T read-back as the bf16 A operand of batch 4
+        if (has_scan) {
+            wait_on(bar_b, ph_b);  // batch b of chunk c
+            prefetch_beta();
+            float dd[16];
+            tmem_ld16(tl + kTmUT + 16 * iq, dd);
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
+            tmem_st8(tl + kTmUTb + 8 * iq, w);
+            tmem_st_wait();
+            handoff(kBarH1, kHand);
+        }
+
+        // ---------------- 5 prep: A (f32) and P (bf16) of chunk cn
         if (has_prep) {
             const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
+            unsigned char *pbuf = smem + kOpP + pn * 8192;
             if (!slow) {
-                mma_wait(mma_phase);  // gram of chunk cn
+                wait_on(bar_g, ph_g);  // gram of chunk cn
                 float dd[16];
                 tmem_ld16(tl + kTmGram + 16 * iq, dd);
                 const int row = 32 * wq + lane;
@@ -672,12 +736,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8)
-                        *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
+                        *reinterpret_cast<uint4 *>(pbuf + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
                             pack_bf16x8(&dd[8 * q8]);
                 }
             } else {
                 // exact pairwise decays on CUDA cores (every exponent <= 0)
-                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
+                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(pbuf);
                 for (int idx = tid; idx < kC * kC; idx += kCompute) {
                     const int r = idx >> 6, s = idx & 63;
                     float a = 0.f, p = 0.f;
@@ -693,32 +757,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
                 }
             }
-            tc_fence_before_sync();
-            csync();
-
-            // T = (I + A)^-1: diagonal 16 x 16 blocks, right-looking, eight
-            // threads per column (thread p owns the rows r = p and p + 8)
-            {
-                const int I = tid >> 7, jj = (tid >> 3) & 15, p = tid & 7;
-                float x0 = (p == jj) ? 1.f : 0.f, x1 = (p + 8 == jj) ? 1.f : 0.f;
-#pragma unroll
-                for (int s = 0; s < 15; ++s) {
-                    const float xs = __shfl_sync(0xffffffffu, s < 8 ? x0 : x1, (lane & ~7) | (s & 7));
-                    if (p > s) x0 = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s)], xs, x0);
-                    if (p + 8 > s) x1 = fmaf(-sA[sq_idx(16 * I + p + 8, 16 * I + s)], xs, x1);
-                }
-                __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
-                const float bj = bvec[16 * I + jj];
-                sT[sq_idx(16 * I + p, 16 * I + jj)] = x0;
-                sT[sq_idx(16 * I + p + 8, 16 * I + jj)] = x1;
-                opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x0 * bj);
-                opt[kmajor_off(16 * I + p + 8, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x1 * bj);
-            }
-            handoff(kBarDiag, kThreads);  // the auxiliary warps take the off-diagonal levels
+            handoff(kBarDiag, kCompute + 64);  // the solver warps invert I + A
         }
 
-        // ---------------- 4 scan: dS^T and O^T read-back, state update, outputs
+        // ---------------- 6 scan: state and O^T read-back, outputs
         if (has_scan) {
+            wait_on(bar_4, ph_4);  // batch 4 of chunk c
             {
                 const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
                 const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kGamL, ps) + 32 * iq);
@@ -749,11 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_commit_group();
             }
         }
-        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as a bf16 A operand
-        // in TMEM (S now holds that chunk's starting state); batch 3 of chunk
-        // c, its previous reader, finished in step 2.  Then the issuers may
-        // start batch 2, which also allows the staging box to be rewritten
-        // (with W), so the output store must have read it first.
+        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as the bf16 A
+        // operand of batch a (S now holds that chunk's starting state; the
+        // previous batch a was waited for in step 2)
         if (has_prep) {
             const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
             uint32_t w[16];
@@ -765,24 +807,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st16(tl + kTmSTb + 16 * iq, w);
             tmem_st_wait();
-            if (tid == 0) bulk_wait_read_all();
-            handoff(kBarS4, kHand);
-        }
-
-        // ---------------- 6 prep: -(T'Lk)^T read-back -> the next scan's batch 3
-        if (has_prep) {
-            mma_wait(mma_phase);  // batch 2 of chunk cn
-            {
-                float dd[16];
-                tmem_ld16(tl + kTmWkT + 16 * iq, dd);  // row i = this lane, columns r
-#pragma unroll
-                for (int e = 0; e < 16; ++e) dd[e] = -dd[e];
-                const int i = 32 * wq + lane;
-#pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    *reinterpret_cast<uint4 *>(smem + kOpWK + mnmajor_off(i, 16 * iq + 8 * q8, kD)) =
-                        pack_bf16x8(&dd[8 * q8]);
-            }
             if (has_next2 && tid < kC) cp_async_wait_all();  // beta of chunk cn + 1
             handoff(kBarH4, kHand);
         }
