@@ -89,7 +89,7 @@ constexpr uint32_t kRawK = 0;                 // k: 2 TMA boxes [64 rows][64 bf1
 constexpr uint32_t kRawQ = kRawK + 16384;     // q: same
 constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
 constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
-constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lk, 64-127 Lq
+constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lq, 64-127 Lk
 constexpr uint32_t kOpR = kOpL + 32768;       // [2][64][128] K-major: R (by chunk parity)
 constexpr uint32_t kAT = kOpR + 32768;        // 32 KB: f32 A and T (64x64 each)
 constexpr uint32_t kA32 = kAT;
@@ -112,15 +112,15 @@ constexpr uint32_t kBarKQG = kBar4 + 8;       // mbarrier: k, q, g tiles
 constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
 constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
 constexpr uint32_t kAbort = kTmemSlot + 4;    // i32 sticky abort flag
-constexpr uint32_t kSlowFlag = kAbort + 4;    // i32: the prepared chunk takes the exact path
-constexpr uint32_t kSmemUsed = kSlowFlag + 4;
+constexpr uint32_t kSlowFlag = kAbort + 4;    // i32 [2] (by chunk parity): the chunk takes the exact path
+constexpr uint32_t kSmemUsed = kSlowFlag + 8;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack for the 1024-byte base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kBytesKQG = 16384 + 16384 + 32768;
 constexpr uint32_t kBytesV = 16384;
 
 // ---- TMEM columns (float32 accumulators, lane = M row)
-constexpr uint32_t kTmGram = 0;     // [128 x 64]: rows 0-63 Lk R^T, 64-127 Lq R^T
+constexpr uint32_t kTmGram = 0;     // [128 x 64]: rows 0-63 Lq R^T (P), 64-127 Lk R^T (A)
 constexpr uint32_t kTmZT = 64;      // [128 j x 64 r]  Z^T = (Lk S')^T
 constexpr uint32_t kTmUT = 128;     // [128 j x 64 r]
 constexpr uint32_t kTmOT = 192;     // [128 j x 64 r]
@@ -133,6 +133,12 @@ constexpr uint32_t kTmemCols = 512;
 // 64 x 64 f32 tiles (A, T) with an XOR swizzle: rows and columns both walk
 // conflict-free
 __device__ __forceinline__ int sq_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
+// In the swizzled tile the 16 entries of row r inside diagonal block I = r / 16
+// occupy one aligned group of 16 floats, at r * 64 + 32 * (I / 2).  The
+// diagonal blocks of A are only read by the diagonal inverses, so they are
+// stored transposed there: A[16 I + p][16 I + q] at row 16 I + q, slot p, and
+// column q of a block is one contiguous run of 16 floats.
+__device__ __forceinline__ int diagT_idx(int I, int q, int p) { return (16 * I + q) * 64 + 32 * (I >> 1) + p; }
 // byte offset of bf16 element (r, i) of a k or q tile (two 64-channel boxes)
 __device__ __forceinline__ uint32_t kq_off(int r, int i) {
     return (uint32_t)((i >> 6) * 8192 + r * 128 + ((((i & 63) >> 3) ^ (r & 7)) << 4) + (i & 7) * 2);
@@ -376,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
     uint32_t ph_a = 0, ph_b = 0, ph_g = 0, ph_4 = 0;
+    uint32_t ph_gs = 0;  // the solver warps' count of gram completions
     int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer lane 0's count is used)
 
     // Two-stage pipeline: iteration c runs the state products of chunk c
@@ -431,10 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (has_prep) {
                     named_sync(kBarH2, kHand);
-                    slow = *slow_flag != 0;
+                    slow = slow_flag[pn] != 0;
                     live = !*abort_flag;  // one warp-wide read: uniform
                     if (!slow && live) {
-                        if (issuer_a && lane == 0) {  // g: gram [Lk; Lq] R^T
+                        if (issuer_a && lane == 0) {  // g: gram [Lq; Lk] R^T
                             tc_fence_after_sync();
                             gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR + pn * 16384, 128,
                                  kD * 16, io, kD / 16, false);
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // a: Z^T = S'^T Lk^T (thread A) and O^T = S'^T Lq^T (thread B), A = S'^T in TMEM
                         tc_fence_after_sync();
                         const uint32_t dst = issuer_a ? kTmZT : kTmOT;
-                        const uint32_t rows = issuer_a ? 0u : 16384u;  // Lk rows 0-63, Lq rows 64-127
+                        const uint32_t rows = issuer_a ? 16384u : 0u;  // Lq rows 0-63, Lk rows 64-127
                         for (int ks = 0; ks < kD / 16; ++ks)
                             mma_bf16_ts(tmem + dst, tmem + kTmSTb + 8 * ks,
                                         smem_desc(sbase + kOpL + rows + ks * 256, 128, kD * 16), io,
@@ -492,12 +499,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (has_prep) {
                 // ---- solver warps: T' of chunk cn
-                named_sync(kBarDiag, kCompute + 64);  // A and P of chunk cn are read back
+                named_sync(kBarDiag, kCompute + 64);  // chunk cn's tiles are in, or A (exact path)
                 const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
+                if (slow_flag[pn] == 0) {
+                    // A = beta-scaled strictly lower part of gram rows 64-127
+                    wait_on(bar_g, ph_gs);  // gram of chunk cn
+                    const int r = 32 * sw + lane;
+                    const float br = bvec[r];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float dd[16];
+                        tmem_ld16(tl + kTmGram + 16 * g, dd);
+                        const bool diag = g == (r >> 4);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int s = 16 * g + u;
+                            const float a = (s < r && r < Ln) ? br * dd[u] : 0.f;
+                            if (diag)
+                                sA[diagT_idx(g, u, r & 15)] = a;
+                            else
+                                sA[sq_idx(r, s)] = a;
+                        }
+                    }
+                    named_sync(kBarAux, 64);
+                }
                 // diagonal 16 x 16 blocks of T = (I + A)^-1: one thread per
                 // column (block I = t / 16, column jj = t % 16), right-looking;
-                // the column of A read at each step is the same for the 16
-                // threads of a block (broadcast loads)
+                // column s2 of A's block is one contiguous run of 16 floats,
+                // the same for the 16 threads of a block (broadcast loads)
                 {
                     const int t = tid - kCompute - 64, I = t >> 4, jj = t & 15;
                     float x[16];
@@ -505,9 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int p = 0; p < 16; ++p) x[p] = (p == jj) ? 1.f : 0.f;
 #pragma unroll
                     for (int s2 = 0; s2 < 15; ++s2) {
+                        const float4 *col = reinterpret_cast<const float4 *>(sA + diagT_idx(I, s2, 0));
 #pragma unroll
-                        for (int p = s2 + 1; p < 16; ++p)
-                            x[p] = fmaf(-sA[sq_idx(16 * I + p, 16 * I + s2)], x[s2], x[p]);
+                        for (int g4 = (s2 + 1) >> 2; g4 < 4; ++g4) {
+                            const float4 a = col[g4];
+                            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (4 * g4 + e > s2) x[4 * g4 + e] = fmaf(-av[e], x[s2], x[4 * g4 + e]);
+                        }
                     }
                     __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
                     const float bj = bvec[16 * I + jj];
@@ -592,14 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         if (!has_scan) prefetch_beta();
-        // the staging box is rewritten in step 6: the previous chunk's output
-        // store must have read it (ordered by the barriers of step 1)
-        if (tid == 0) bulk_wait_read_all();
-
         // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
         bool slow = false;
         if (has_prep) {
             wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
+            // the staging box is rewritten in step 6: the previous chunk's
+            // output store must have read it (ordered by the barrier below)
+            if (tid == 0) bulk_wait_read_all();
             csync();
             {
                 const int i = tid & 127, qq = tid >> 7;
@@ -626,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bad = (gval(0, tid) - gm > kRangeLog2) || (gm - gl > kRangeLog2);
             }
             slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
-            if (tid == 0) *slow_flag = slow ? 1 : 0;  // read by the issuers after H2
+            if (tid == 0) slow_flag[pn] = slow ? 1 : 0;  // read by the issuers and the solvers
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
@@ -636,7 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vec(kGamL, pn)[tid] = fast_exp2(gl);
             }
         }
-        if (!has_prep) csync();  // orders thread 0's staging-box wait before step 6
+        if (!has_prep) {  // orders thread 0's staging-box wait before step 6
+            if (tid == 0) bulk_wait_read_all();
+            csync();
+        }
 
         // ---------------- 2 scan: -Z^T read-back as the bf16 A operand of batch b
         if (has_scan) {
@@ -688,8 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // fallback: R = exp(G_L - G) K directly (factor <= 1)
                     rr[e] = kv[e] * fast_exp2(slow ? sGl[ch + e] - gv[e] : -d);
                 }
-                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lk);
-                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lq);
+                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
+                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lk);
                 *reinterpret_cast<uint4 *>(smem + kOpR + pn * 16384 + kmajor_off(r, ch, kD)) =
                     pack_bf16x8(rr);
             }
@@ -715,20 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
             unsigned char *pbuf = smem + kOpP + pn * 8192;
             if (!slow) {
-                wait_on(bar_g, ph_g);  // gram of chunk cn
-                float dd[16];
-                tmem_ld16(tl + kTmGram + 16 * iq, dd);
-                const int row = 32 * wq + lane;
-                if (row < kC) {
-                    const int r = row;
-                    const float br = bvec[r];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int s = 16 * iq + u;
-                        sA[sq_idx(r, s)] = (s < r && r < Ln) ? br * dd[u] : 0.f;
-                    }
-                } else {
-                    const int r = row - kC;
+                // the solver warps read A themselves (gram rows 64-127)
+                handoff(kBarDiag, kCompute + 64);
+                if (wq < 2) {  // P rows: gram rows 0-63
+                    wait_on(bar_g, ph_g);  // gram of chunk cn
+                    float dd[16];
+                    tmem_ld16(tl + kTmGram + 16 * iq, dd);
+                    const int r = 32 * wq + lane;
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int s = 16 * iq + u;
@@ -738,6 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q8 = 0; q8 < 2; ++q8)
                         *reinterpret_cast<uint4 *>(pbuf + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
                             pack_bf16x8(&dd[8 * q8]);
+                } else {
+                    ph_g ^= 1u;  // this gram completion is not needed here
                 }
             } else {
                 // exact pairwise decays on CUDA cores (every exponent <= 0)
@@ -753,11 +785,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p = fmaf(kval(kRawQ, r, i), kse, p);
                         }
                     }
-                    sA[sq_idx(r, s)] = (s < r) ? bvec[r] * a : 0.f;
+                    const float av = (s < r) ? bvec[r] * a : 0.f;
+                    if ((r >> 4) == (s >> 4))
+                        sA[diagT_idx(r >> 4, s & 15, r & 15)] = av;
+                    else
+                        sA[sq_idx(r, s)] = av;
                     op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
                 }
+                handoff(kBarDiag, kCompute + 64);  // the solver warps invert I + A
             }
-            handoff(kBarDiag, kCompute + 64);  // the solver warps invert I + A
         }
 
         // ---------------- 6 scan: state and O^T read-back, outputs
