@@ -371,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((s0 >> 4) > (r >> 4))
             *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
-    // state: S[32*iq + u][j], u = 0..31 (state warps)
-    float S[32];
+    // state: S[32*iq + 2h + e][j] in S2[h].x / .y (state warps), pairs for packed fp32
+    float2 S2[16];
 #pragma unroll
-    for (int u = 0; u < 32; ++u)
-        S[u] = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + u) * kD + j] : 0.f;
+    for (int h = 0; h < 16; ++h) {
+        S2[h].x = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + 2 * h) * kD + j] : 0.f;
+        S2[h].y = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + 2 * h + 1) * kD + j] : 0.f;
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -716,14 +718,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 8; ++e) gm[e] = 0.f;
                 }
                 float lk[8], lq[8], rr[8];
+                if (!slow) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d = gv[e] - gm[e];
-                    const float el = fast_exp2(d);
-                    lk[e] = kv[e] * el;
-                    lq[e] = qv[e] * el;
-                    // fallback: R = exp(G_L - G) K directly (factor <= 1)
-                    rr[e] = kv[e] * fast_exp2(slow ? sGl[ch + e] - gv[e] : -d);
+                    for (int e = 0; e < 8; e += 2) {  // packed fp32 pairs
+                        const float2 d = __fadd2_rn(make_float2(gv[e], gv[e + 1]),
+                                                    make_float2(-gm[e], -gm[e + 1]));
+                        const float2 el = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        const float2 er = make_float2(fast_exp2(-d.x), fast_exp2(-d.y));
+                        const float2 kk = make_float2(kv[e], kv[e + 1]);
+                        const float2 a = __fmul2_rn(kk, el);
+                        const float2 bq = __fmul2_rn(make_float2(qv[e], qv[e + 1]), el);
+                        const float2 cr = __fmul2_rn(kk, er);
+                        lk[e] = a.x; lk[e + 1] = a.y;
+                        lq[e] = bq.x; lq[e + 1] = bq.y;
+                        rr[e] = cr.x; rr[e + 1] = cr.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float el = fast_exp2(gv[e]);
+                        lk[e] = kv[e] * el;
+                        lq[e] = qv[e] * el;
+                        // R = exp(G_L - G) K directly (factor <= 1)
+                        rr[e] = kv[e] * fast_exp2(sGl[ch + e] - gv[e]);
+                    }
                 }
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lk);
@@ -805,12 +823,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float dd[32];
                 tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
+                for (int u4 = 0; u4 < 8; ++u4) {  // S = exp(G_L) S + cL dS, packed fp32 pairs
                     const float4 cl = cl4[u4], gm = gam4[u4];
-                    S[4 * u4 + 0] = fmaf(gm.x, S[4 * u4 + 0], cl.x * dd[4 * u4 + 0]);
-                    S[4 * u4 + 1] = fmaf(gm.y, S[4 * u4 + 1], cl.y * dd[4 * u4 + 1]);
-                    S[4 * u4 + 2] = fmaf(gm.z, S[4 * u4 + 2], cl.z * dd[4 * u4 + 2]);
-                    S[4 * u4 + 3] = fmaf(gm.w, S[4 * u4 + 3], cl.w * dd[4 * u4 + 3]);
+                    S2[2 * u4] = __ffma2_rn(make_float2(gm.x, gm.y), S2[2 * u4],
+                                            __fmul2_rn(make_float2(cl.x, cl.y),
+                                                       make_float2(dd[4 * u4], dd[4 * u4 + 1])));
+                    S2[2 * u4 + 1] = __ffma2_rn(make_float2(gm.z, gm.w), S2[2 * u4 + 1],
+                                                __fmul2_rn(make_float2(cl.z, cl.w),
+                                                           make_float2(dd[4 * u4 + 2], dd[4 * u4 + 3])));
                 }
                 // O^T -> bf16 O [r][j] staging
                 float oo[16];
@@ -838,8 +858,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u4 = 0; u4 < 8; ++u4) {
                 const float4 e = egm4[u4];
-                w[2 * u4] = pack_bf16x2(S[4 * u4] * e.x, S[4 * u4 + 1] * e.y);
-                w[2 * u4 + 1] = pack_bf16x2(S[4 * u4 + 2] * e.z, S[4 * u4 + 3] * e.w);
+                const float2 a = __fmul2_rn(S2[2 * u4], make_float2(e.x, e.y));
+                const float2 c2 = __fmul2_rn(S2[2 * u4 + 1], make_float2(e.z, e.w));
+                w[2 * u4] = pack_bf16x2(a.x, a.y);
+                w[2 * u4 + 1] = pack_bf16x2(c2.x, c2.y);
             }
             tmem_st16(tl + kTmSTb + 16 * iq, w);
             tmem_st_wait();
@@ -860,7 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!aborted && STORE_HT && !aux) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) ht[((size_t)head * kD + 32 * iq + u) * kD + j] = S[u];
+        for (int h = 0; h < 16; ++h) {
+            ht[((size_t)head * kD + 32 * iq + 2 * h) * kD + j] = S2[h].x;
+            ht[((size_t)head * kD + 32 * iq + 2 * h + 1) * kD + j] = S2[h].y;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
