@@ -177,15 +177,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // Issues the K-steps of one GEMM, D (+)= A * B^T, each K-step of 16
 // advancing the operand start addresses by two core matrices along K.
-__device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_addr, uint32_t a_lbo,
-                                     uint32_t a_sbo, uint32_t b_addr, uint32_t b_lbo,
-                                     uint32_t b_sbo, uint32_t idesc, int k_steps,
-                                     bool accumulate_first) {
-    for (int ks = 0; ks < k_steps; ++ks) {
-        const uint64_t ad = smem_desc(a_addr + ks * 2 * a_lbo, a_lbo, a_sbo);
-        const uint64_t bd = smem_desc(b_addr + ks * 2 * b_lbo, b_lbo, b_sbo);
-        mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate_first) ? 1u : 0u);
-    }
+// Issues K_STEPS MMAs D (+)= A * B^T with shared-memory operands.  The
+// descriptors are built once; each K-step advances the start-address field
+// (address / 16, bits 0-13) by a fixed number of bytes, which never carries
+// out of the field for addresses inside shared memory.
+template <int K_STEPS>
+__device__ __forceinline__ void gemm_ss(uint32_t d_tmem, uint64_t a_desc, uint32_t a_step,
+                                        uint64_t b_desc, uint32_t b_step, uint32_t idesc,
+                                        bool accumulate_first) {
+#pragma unroll
+    for (int ks = 0; ks < K_STEPS; ++ks)
+        mma_bf16(d_tmem, a_desc + (uint64_t)((ks * a_step) >> 4),
+                 b_desc + (uint64_t)((ks * b_step) >> 4), idesc,
+                 (ks > 0 || accumulate_first) ? 1u : 0u);
+}
+// Same with the A operand in tensor memory (bf16 packed two per column,
+// eight columns per K-step of 16).
+template <int K_STEPS>
+__device__ __forceinline__ void gemm_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t b_step, uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+    for (int ks = 0; ks < K_STEPS; ++ks)
+        mma_bf16_ts(d_tmem, a_tmem + 8 * ks, b_desc + (uint64_t)((ks * b_step) >> 4), idesc,
+                    (ks > 0 || accumulate_first) ? 1u : 0u);
 }
 
 // Bounded wait on an mbarrier phase.  A timeout sets the CTA's sticky abort
@@ -428,13 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after_sync();
                         // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
                         const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-                        for (int ks = 0; ks < kC / 16; ++ks)
-                            mma_bf16(tmem + kTmUT, smem_desc_sw128(sbase + kOpV + ks * 2048, 8192, 1024),
-                                     smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), vid,
-                                     ks > 0 ? 1u : 0u);
-                        for (int ks = 0; ks < kC / 16; ++ks)
-                            mma_bf16_ts(tmem + kTmUT, tmem + kTmZTb + 8 * ks,
-                                        smem_desc(sbase + kOpT + ks * 256, 128, kC * 16), io, 1u);
+                        const uint64_t tdesc = smem_desc(sbase + kOpT, 128, kC * 16);
+                        gemm_ss<kC / 16>(tmem + kTmUT, smem_desc_sw128(sbase + kOpV, 8192, 1024), 2048,
+                                         tdesc, 256, vid, false);
+                        gemm_ts<kC / 16>(tmem + kTmUT, tmem + kTmZTb, tdesc, 256, io, true);
                         mma_commit(bar_b);
                     }
                 }
@@ -445,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!slow && live) {
                         if (issuer_a && lane == 0) {  // g: gram [Lq; Lk] R^T
                             tc_fence_after_sync();
-                            gemm(tmem + kTmGram, sbase + kOpL, 128, kD * 16, sbase + kOpR + pn * 16384, 128,
-                                 kD * 16, io, kD / 16, false);
+                            gemm_ss<kD / 16>(tmem + kTmGram, smem_desc(sbase + kOpL, 128, kD * 16), 256,
+                                             smem_desc(sbase + kOpR + pn * 16384, 128, kD * 16), 256,
+                                             io, false);
                             mma_commit(bar_g);
                         }
                         // the raw k, q, g tiles are consumed: fetch the next chunk's
@@ -461,16 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0 && !*abort_flag) {  // 4, A = U^T (bf16) in TMEM
                         tc_fence_after_sync();
                         if (issuer_a) {  // O^T += U^T P^T
-                            for (int ks = 0; ks < kC / 16; ++ks)
-                                mma_bf16_ts(tmem + kTmOT, tmem + kTmUTb + 8 * ks,
-                                            smem_desc(sbase + kOpP + ps * 8192 + ks * 256, 128, kC * 16),
-                                            io, 1u);
+                            gemm_ts<kC / 16>(tmem + kTmOT, tmem + kTmUTb,
+                                             smem_desc(sbase + kOpP + ps * 8192, 128, kC * 16), 256,
+                                             io, true);
                         } else {  // dS^T = U^T R (R read transposed)
                             const uint32_t ids = idesc_bf16(128, 128, false, true, false);
-                            for (int ks = 0; ks < kC / 16; ++ks)
-                                mma_bf16_ts(tmem + kTmDS, tmem + kTmUTb + 8 * ks,
-                                            smem_desc(sbase + kOpR + ps * 16384 + ks * 4096, kD * 16, 128),
-                                            ids, ks > 0 ? 1u : 0u);
+                            gemm_ts<kC / 16>(tmem + kTmDS, tmem + kTmUTb,
+                                             smem_desc(sbase + kOpR + ps * 16384, kD * 16, 128), 4096,
+                                             ids, false);
                         }
                         mma_commit(bar_4);
                         // batch b of chunk c has completed (the state warps waited
@@ -492,10 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after_sync();
                         const uint32_t dst = issuer_a ? kTmZT : kTmOT;
                         const uint32_t rows = issuer_a ? 16384u : 0u;  // Lq rows 0-63, Lk rows 64-127
-                        for (int ks = 0; ks < kD / 16; ++ks)
-                            mma_bf16_ts(tmem + dst, tmem + kTmSTb + 8 * ks,
-                                        smem_desc(sbase + kOpL + rows + ks * 256, 128, kD * 16), io,
-                                        ks > 0 ? 1u : 0u);
+                        gemm_ts<kD / 16>(tmem + dst, tmem + kTmSTb,
+                                         smem_desc(sbase + kOpL + rows, 128, kD * 16), 256, io, false);
                         mma_commit(bar_a);
                     }
                 }
