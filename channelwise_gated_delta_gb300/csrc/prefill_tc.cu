@@ -211,11 +211,10 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, volatil
 }
 
 // ---- tf32 mma.sync for the 16 x 16 block products of the inverse
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// The f32 bit pattern is passed as is: the tf32 MMA reads the sign, the
+// exponent and the top 10 mantissa bits (truncation; the result feeds a bf16
+// operand, whose rounding is coarser).
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
