@@ -211,10 +211,6 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, volatil
 }
 
 // ---- tf32 mma.sync for the 16 x 16 block products of the inverse
-// The f32 bit pattern is passed as is: the tf32 MMA reads the sign, the
-// exponent and the top 10 mantissa bits (truncation; the result feeds a bf16
-// operand, whose rounding is coarser).
-__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
@@ -248,22 +244,55 @@ __device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, u
     tma_load_4d(sm + kOpV + 8192, &tm.v, 64, hv, t0, b, bar);
 }
 
-// One warp: acc (16 x 16, two m16n8 C tiles) += X * Y for 16 x 16 f32 blocks,
-// in tf32.  X and Y are read through index functors (row, col) -> float.
-template <typename FX, typename FY>
-__device__ __forceinline__ void blk_mma(float (&acc)[2][4], FX X, FY Y, int lane) {
+// Block (I, J) of a swizzled 64 x 64 f32 tile: with R = 16 I + r, element
+// (r, c) sits at R * 64 + 16 (J ^ (I & 1)) + (c ^ r) -- the row's 16 block
+// entries form one aligned group, permuted by r.  swz_block returns the
+// group base of row 0; the per-lane offsets below add the rest.
+__device__ __forceinline__ const float *swz_block(const float *tile, int I, int J) {
+    return tile + I * 1024 + 16 * (J ^ (I & 1));
+}
+struct FragOffsets {  // per-lane offsets of the m16n8k8 tf32 fragments in a swizzled block
+    int a0, a1;       // A: row gq, columns tq / tq + 4
+    int b0, b1;       // B: rows tq / tq + 4, column gq
+    int x0, x1;       // the same for a plain [16][16] block (row stride 16)
+};
+__device__ __forceinline__ FragOffsets frag_offsets(int lane) {
     const int gq = lane >> 2, tq = lane & 3;
+    FragOffsets f;
+    f.a0 = gq * 64 + (tq ^ gq);
+    f.a1 = gq * 64 + ((tq + 4) ^ gq);
+    f.b0 = tq * 64 + (tq ^ gq);
+    f.b1 = (tq + 4) * 64 + ((tq + 4) ^ gq);
+    f.x0 = tq * 16 + gq;
+    f.x1 = (tq + 4) * 16 + gq;
+    return f;
+}
+// acc += X * Y for 16 x 16 blocks on tf32 mma.sync (one warp); X a swizzled
+// block, Y a swizzled block (SWZ_Y) or a plain [16][16] scratch block.
+template <bool SWZ_Y>
+__device__ __forceinline__ void blk_mma2(float (&acc)[2][4], const float *X, const float *Y,
+                                         const FragOffsets &f) {
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
-        const int kc = 8 * kh + tq;
         uint32_t a[4];
-        a[0] = to_tf32(X(gq, kc));
-        a[1] = to_tf32(X(gq + 8, kc));
-        a[2] = to_tf32(X(gq, kc + 4));
-        a[3] = to_tf32(X(gq + 8, kc + 4));
+        // rows gq and gq + 8 (+512), columns 8 kh + tq and 8 kh + tq + 4;
+        // row gq + 8 flips bit 3 of the permuted column
+        a[0] = __float_as_uint(X[f.a0 + 8 * kh]);
+        a[1] = __float_as_uint(X[f.a0 + 512 + 8 * (kh ^ 1)]);
+        a[2] = __float_as_uint(X[f.a1 + 8 * kh]);
+        a[3] = __float_as_uint(X[f.a1 + 512 + 8 * (kh ^ 1)]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-            mma_tf32(acc[nt], a, to_tf32(Y(kc, 8 * nt + gq)), to_tf32(Y(kc + 4, 8 * nt + gq)));
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            if (SWZ_Y) {  // rows 8 kh + tq (+4), column 8 nt + gq
+                b0 = __float_as_uint(Y[f.b0 + 512 * kh + 8 * (nt ^ kh)]);
+                b1 = __float_as_uint(Y[f.b1 + 512 * kh + 8 * (nt ^ kh)]);
+            } else {
+                b0 = __float_as_uint(Y[f.x0 + 128 * kh + 8 * nt]);
+                b1 = __float_as_uint(Y[f.x1 + 128 * kh + 8 * nt]);
+            }
+            mma_tf32(acc[nt], a, b0, b1);
+        }
     }
 }
 // C tiles of one warp's 16 x 16 result -> f32 [16][16] scratch
@@ -330,10 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto vec = [&](uint32_t base, int parity) {
         return reinterpret_cast<float *>(smem + base + 512 * parity);
     };
-    // 16 x 16 block (I, J) of the swizzled 64 x 64 tiles as index functors
-    auto blkA = [&](int I, int J) { return [=](int r, int c) { return sA[sq_idx(16 * I + r, 16 * J + c)]; }; };
-    auto blkT = [&](int I, int J) { return [=](int r, int c) { return sT[sq_idx(16 * I + r, 16 * J + c)]; }; };
-    auto blkX = [&](int n) { const float *x = sX + 256 * n; return [=](int r, int c) { return x[r * 16 + c]; }; };
     auto wait_on = [&](uint64_t *bar, uint32_t &phase) {
         wait_bar(bar, phase, abort_flag);
         phase ^= 1u;
@@ -565,39 +590,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // off-diagonal blocks by 32 x 32 block recursion:
                 //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
                 //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
+                const FragOffsets fo = frag_offsets(lane);
                 auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
                     const int gq = lane >> 2, tq = lane & 3;
+                    float *trow = sT + I * 1024 + 16 * (J ^ (I & 1)) + gq * 64;
+                    const int u0 = (2 * tq) ^ gq, u1 = (2 * tq + 1) ^ gq;
+                    unsigned char *prow = smem + kOpT + 2 * I * 1024 + gq * 16 + 4 * tq;
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        const int col = 16 * J + 8 * nt + 2 * tq;
-                        const float b0 = bvec[col], b1 = bvec[col + 1];
-                        sT[sq_idx(16 * I + gq, col)] = -acc[nt][0];
-                        sT[sq_idx(16 * I + gq, col + 1)] = -acc[nt][1];
-                        sT[sq_idx(16 * I + gq + 8, col)] = -acc[nt][2];
-                        sT[sq_idx(16 * I + gq + 8, col + 1)] = -acc[nt][3];
-                        *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq, col, kC)) =
-                            pack_bf16x2(-acc[nt][0] * b0, -acc[nt][1] * b1);
-                        *reinterpret_cast<uint32_t *>(smem + kOpT + kmajor_off(16 * I + gq + 8, col, kC)) =
-                            pack_bf16x2(-acc[nt][2] * b0, -acc[nt][3] * b1);
+                        const float2 bb = *reinterpret_cast<const float2 *>(bvec + 16 * J + 8 * nt + 2 * tq);
+                        trow[8 * nt + u0] = -acc[nt][0];
+                        trow[8 * nt + u1] = -acc[nt][1];
+                        trow[512 + 8 * (nt ^ 1) + u0] = -acc[nt][2];
+                        trow[512 + 8 * (nt ^ 1) + u1] = -acc[nt][3];
+                        // T' = T diag(beta), bf16, K-major [64 r][64 s]: (2 J + nt) * 128 + row offsets
+                        *reinterpret_cast<uint32_t *>(prow + (2 * J + nt) * 128) =
+                            pack_bf16x2(-acc[nt][0] * bb.x, -acc[nt][1] * bb.y);
+                        *reinterpret_cast<uint32_t *>(prow + 1024 + (2 * J + nt) * 128) =
+                            pack_bf16x2(-acc[nt][2] * bb.x, -acc[nt][3] * bb.y);
                     }
                 };
                 {  // level 1: block (1,0) on solver 0, (3,2) on solver 1
                     const int I = 2 * sw + 1, J = 2 * sw;
                     float acc[2][4] = {};
-                    blk_mma(acc, blkA(I, J), blkT(J, J), lane);
+                    blk_mma2<true>(acc, swz_block(sA, I, J), swz_block(sT, J, J), fo);
                     blk_store(sX + 256 * sw, acc, lane);
                     __syncwarp();
                     float y[2][4] = {};
-                    blk_mma(y, blkT(I, I), blkX(sw), lane);
+                    blk_mma2<false>(y, swz_block(sT, I, I), sX + 256 * sw, fo);
                     emit(I, J, y);
                 }
                 named_sync(kBarAux, 64);
                 {  // level 2, row I = 2 + sw of X = [A_20 A_21; A_30 A_31] T1 (slots 2 (I - 2) + J)
                     const int I = 2 + sw;
                     float x0[2][4] = {}, x1[2][4] = {};
-                    blk_mma(x0, blkA(I, 0), blkT(0, 0), lane);
-                    blk_mma(x0, blkA(I, 1), blkT(1, 0), lane);
-                    blk_mma(x1, blkA(I, 1), blkT(1, 1), lane);
+                    blk_mma2<true>(x0, swz_block(sA, I, 0), swz_block(sT, 0, 0), fo);
+                    blk_mma2<true>(x0, swz_block(sA, I, 1), swz_block(sT, 1, 0), fo);
+                    blk_mma2<true>(x1, swz_block(sA, I, 1), swz_block(sT, 1, 1), fo);
                     blk_store(sX + 256 * (2 * sw), x0, lane);
                     blk_store(sX + 256 * (2 * sw + 1), x1, lane);
                 }
@@ -605,9 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {  // level 2, column J = sw of T_lo = -T2 X
                     const int J = sw;
                     float t2[2][4] = {}, t3[2][4] = {};
-                    blk_mma(t2, blkT(2, 2), blkX(J), lane);      // T_22 X_2J
-                    blk_mma(t3, blkT(3, 2), blkX(J), lane);      // T_32 X_2J
-                    blk_mma(t3, blkT(3, 3), blkX(2 + J), lane);  // + T_33 X_3J
+                    blk_mma2<false>(t2, swz_block(sT, 2, 2), sX + 256 * J, fo);        // T_22 X_2J
+                    blk_mma2<false>(t3, swz_block(sT, 3, 2), sX + 256 * J, fo);        // T_32 X_2J
+                    blk_mma2<false>(t3, swz_block(sT, 3, 3), sX + 256 * (2 + J), fo);  // + T_33 X_3J
                     emit(2, J, t2);
                     emit(3, J, t3);
                 }
