@@ -581,9 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
                     const float bj = bvec[16 * I + jj];
 #pragma unroll
-                    for (int p = 0; p < 16; ++p) {
+                    for (int p = 0; p < 16; p += 2) {
                         sT[sq_idx(16 * I + p, 16 * I + jj)] = x[p];
-                        opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = __float2bfloat16_rn(x[p] * bj);
+                        sT[sq_idx(16 * I + p + 1, 16 * I + jj)] = x[p + 1];
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(x[p] * bj, x[p + 1] * bj);
+                        opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = h.x;
+                        opt[kmajor_off(16 * I + p + 1, 16 * I + jj, kC) >> 1] = h.y;
                     }
                 }
                 named_sync(kBarAux, 64);
@@ -873,7 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16(tl + kTmOT + 16 * iq, oo);
                 __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) stg[(16 * iq + u) * kD + j] = __float2bfloat16_rn(oo[u]);
+                for (int u = 0; u < 16; u += 2) {  // converted in pairs, stored per row
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(oo[u], oo[u + 1]);
+                    stg[(16 * iq + u) * kD + j] = h.x;
+                    stg[(16 * iq + u + 1) * kD + j] = h.y;
+                }
             }
             fence_async_smem();
             tc_fence_before_sync();
