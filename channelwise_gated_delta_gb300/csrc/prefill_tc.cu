@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // Warps 0-15 own the state and do the per-chunk element-wise work; warps
     // 16-19 are auxiliary.  Warps 16 and 17 issue the MMAs (lane 0 of each,
-    // on independent accumulators) and warp 16 the TMA copies; warps 18 and
+    // on independent accumulators) and warp 17 the TMA loads; warps 18 and
     // 19 invert I + A for the next chunk while the state warps run the
     // current chunk's state products.
     const bool aux = tid >= kCompute;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm.o);
     }
     __syncthreads();
-    if (issuer_a) {  // first chunk's inputs
+    if (issuer_warp && !issuer_a) {  // first chunk's inputs (warp B issues every TMA load)
         issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv, lane);
         if (lane == 0) issue_v(smem, tm, bar_v, b, 0, hv);
     }
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
     uint32_t ph_a = 0, ph_b = 0, ph_g = 0, ph_4 = 0;
     uint32_t ph_gs = 0;  // the solver warps' count of gram completions
-    int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer lane 0's count is used)
+    int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer warp B, lane 0's count is used)
 
     // Two-stage pipeline: iteration c runs the state products of chunk c
     // (scan) and prepares chunk c + 1 (prep).  U = T'(V - Lk S') is formed as
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_commit(bar_g);
                         }
                         // the raw k, q, g tiles are consumed: fetch the next chunk's
-                        if (issuer_a && has_next2) {
+                        if (!issuer_a && has_next2) {
                             issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
                             ++issued_kqg;
                         }
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(bar_4);
                         // batch b of chunk c has completed (the state warps waited
                         // for it): v's buffer takes the prepared chunk's
-                        if (issuer_a && has_prep) {
+                        if (!issuer_a && has_prep) {
                             issue_v(smem, tm, bar_v, b, t0n, hv);
                             ++issued_v;
                         }
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (has_prep) {
                     named_sync(kBarH4, kHand);
-                    if (issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
+                    if (!issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
                         issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
                         ++issued_kqg;
                     }
@@ -916,10 +916,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) bulk_wait_all();
     __syncthreads();
     const bool aborted = *abort_flag != 0;
-    if (tid == kCompute && aborted) {
+    if (tid == kCompute && aborted) atomicOr(dev_error, 1);
+    if (tid == kCompute + 32 && aborted) {
         // never leave with copies in flight: wait (bounded) for the last copy
         // issued on each barrier; its phases complete in order
-        atomicOr(dev_error, 1);
         mbar_wait_bounded(bar_kqg, (uint32_t)((issued_kqg - 1) & 1), kWaitLimitNs);
         mbar_wait_bounded(bar_v, (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
     }
