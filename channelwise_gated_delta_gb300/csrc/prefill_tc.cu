@@ -96,7 +96,7 @@ constexpr uint32_t kA32 = kAT;
 constexpr uint32_t kT32 = kAT + 16384;
 constexpr uint32_t kOpT = kAT + 32768;        // T' as K-major B [64 r][64 s]
 constexpr uint32_t kOpP = kOpT + 8192;        // [2] P as K-major B [64 r][64 s] (by chunk parity)
-constexpr uint32_t kStage = kOpP + 16384;     // bf16 O [64][128] staging for the output store
+constexpr uint32_t kStage = kOpP + 16384;     // bf16 O staging: per state warp one [16 r][32 j] box
 constexpr uint32_t kX32 = kStage + 16384;     // f32 [4][16][16] solve scratch
 constexpr uint32_t kSmall = kX32 + 4096;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
@@ -672,15 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool slow = false;
         if (has_prep) {
             wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
-            // the staging box is rewritten in step 6: the previous chunk's
-            // output store must have read it (ordered by the barrier below)
-            if (tid == 0) bulk_wait_read_all();
-            csync();
             {
                 const int i = tid & 127, qq = tid >> 7;
                 float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = gval(16 * qq + r, i) * kLog2e;  // log2 units
+                for (int r = 0; r < 16; r += 2) {  // log2 units
+                    const float2 v = __fmul2_rn(make_float2(gval(16 * qq + r, i), gval(16 * qq + r + 1, i)),
+                                                make_float2(kLog2e, kLog2e));
+                    x[r] = v.x;
+                    x[r + 1] = v.y;
+                }
 #pragma unroll
                 for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
@@ -688,8 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float carry = 0.f;
                 for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
 #pragma unroll
-                for (int r = 0; r < 16; ++r)
-                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = x[r] + carry;
+                for (int r = 0; r < 16; r += 2) {
+                    const float2 v = __fadd2_rn(make_float2(x[r], x[r + 1]), make_float2(carry, carry));
+                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = v.x;
+                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r + 1, i)) = v.y;
+                }
             }
             csync();
             // reference-row and last-row values, then the range check
@@ -710,10 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
                 vec(kGamL, pn)[tid] = fast_exp2(gl);
             }
-        }
-        if (!has_prep) {  // orders thread 0's staging-box wait before step 6
-            if (tid == 0) bulk_wait_read_all();
-            csync();
         }
 
         // ---------------- 2 scan: -Z^T read-back as the bf16 A operand of batch b
@@ -871,25 +871,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 __fmul2_rn(make_float2(cl.z, cl.w),
                                                            make_float2(dd[4 * u4 + 2], dd[4 * u4 + 3])));
                 }
-                // O^T -> bf16 O [r][j] staging
+                // O^T -> this warp's bf16 O box [16 r][32 j] (rows 16 iq .., columns 32 wq ..)
                 float oo[16];
                 tmem_ld16(tl + kTmOT + 16 * iq, oo);
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage);
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage + 1024 * warp);
+                // the previous chunk's store from this box must have read it
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
 #pragma unroll
                 for (int u = 0; u < 16; u += 2) {  // converted in pairs, stored per row
                     const __nv_bfloat162 h = __floats2bfloat162_rn(oo[u], oo[u + 1]);
-                    stg[(16 * iq + u) * kD + j] = h.x;
-                    stg[(16 * iq + u + 1) * kD + j] = h.y;
+                    stg[u * 32 + lane] = h.x;
+                    stg[(u + 1) * 32 + lane] = h.y;
                 }
-            }
-            fence_async_smem();
-            tc_fence_before_sync();
-            csync();
-            // one TMA store of the chunk's [64 x 128] output box; rows past
-            // the end of the sequence fall outside the tensor and are dropped
-            if (tid == 0 && !*abort_flag) {
-                tma_store_4d(&tm.o, smem + kStage, 0, hv, t0, b);
-                bulk_commit_group();
+                fence_async_smem();
+                __syncwarp();
+                // one TMA store per warp; rows past the end of the sequence
+                // fall outside the tensor and are dropped
+                if (lane == 0 && !*abort_flag) {
+                    tma_store_4d(&tm.o, stg, 32 * wq, hv, t0 + 16 * iq, b);
+                    bulk_commit_group();
+                }
             }
         }
         // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as the bf16 A
@@ -913,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (tid == 0) bulk_wait_all();
+    if (!aux && lane == 0) bulk_wait_all();
     __syncthreads();
     const bool aborted = *abort_flag != 0;
     if (tid == kCompute && aborted) atomicOr(dev_error, 1);
@@ -964,11 +966,11 @@ EncodeTiledFn encode_fn(cudaError_t *err) {
 // elements x 64 tokens, 128-byte swizzled, zero fill outside the tensor.
 bool encode_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
                 int esize, int B, int T, int H, int box_inner,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int box_rows = 64) {
     const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)128 * esize, (cuuint64_t)H * 128 * esize,
                                    (cuuint64_t)T * H * 128 * esize};
-    const cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 64, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
@@ -992,9 +994,9 @@ cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t str
         !encode_map(fn, &tm.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
         !encode_map(fn, &tm.g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.HV, 32) ||
         !encode_map(fn, &tm.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 64) ||
-        // output: one unswizzled [64 tokens][128 channels] box per chunk
-        !encode_map(fn, &tm.o, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 128,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
+        // output: unswizzled [16 tokens][32 channels] boxes, one per state warp
+        !encode_map(fn, &tm.o, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 32,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, 16))
         return cudaErrorInvalidValue;
     auto run = [&](auto kernel) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
