@@ -335,8 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = 32 * wq + lane;   // this thread's value column (TMEM lane)
 
     float *sTot = reinterpret_cast<float *>(smem + kTot);
-    float *sGm = reinterpret_cast<float *>(smem + kTot);        // after the prefix sums
-    float *sGl = reinterpret_cast<float *>(smem + kTot + 512);  //   reuse the carries' space
     float *sA = reinterpret_cast<float *>(smem + kA32);
     float *sT = reinterpret_cast<float *>(smem + kT32);
     float *sX = reinterpret_cast<float *>(smem + kX32);
@@ -685,7 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
-                csync();
+                // Range check, conservatively per 16-row quarter: the spans it
+                // guards (rows 1..m and m+1..L-1, at most 32 rows) cover at
+                // most three quarters, so no quarter decaying by more than a
+                // third of the range keeps every factor within exp(+-80).
+                const int bad = -x[15] > kRangeLog2 * (1.f / 3.f);
+                slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
                 float carry = 0.f;
                 for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
 #pragma unroll
@@ -695,21 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r + 1, i)) = v.y;
                 }
             }
-            csync();
-            // reference-row and last-row values, then the range check
-            int bad = 0;
-            if (tid < kD) {
-                const float gm = gval(mref, tid), gl = gval(Ln - 1, tid);
-                sGm[tid] = gm;
-                sGl[tid] = gl;
-                bad = (gval(0, tid) - gm > kRangeLog2) || (gm - gl > kRangeLog2);
-            }
-            slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
             if (tid == 0) slow_flag[pn] = slow ? 1 : 0;  // read by the issuers and the solvers
+            csync();
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
-                const float gm = slow ? 0.f : sGm[tid], gl = sGl[tid];
+                const float gm = slow ? 0.f : gval(mref, tid), gl = gval(Ln - 1, tid);
                 vec(kEGm, pn)[tid] = slow ? 1.f : fast_exp2(gm);
                 vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
                 vec(kGamL, pn)[tid] = fast_exp2(gl);
@@ -748,8 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
                 gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
                 if (!slow) {
-                    const float4 m_lo = *reinterpret_cast<const float4 *>(sGm + ch);
-                    const float4 m_hi = *reinterpret_cast<const float4 *>(sGm + ch + 4);
+                    // G at the reference row, from the G tile
+                    const float4 m_lo = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch));
+                    const float4 m_hi = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch + 4));
                     gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
                     gm[4] = m_hi.x; gm[5] = m_hi.y; gm[6] = m_hi.z; gm[7] = m_hi.w;
                 } else {
@@ -779,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lk[e] = kv[e] * el;
                         lq[e] = qv[e] * el;
                         // R = exp(G_L - G) K directly (factor <= 1)
-                        rr[e] = kv[e] * fast_exp2(sGl[ch + e] - gv[e]);
+                        rr[e] = kv[e] * fast_exp2(gval(Ln - 1, ch + e) - gv[e]);
                     }
                 }
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
