@@ -367,8 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // operation the mbarrier waits on each batch keep the state warps from
     // lapping the auxiliary warps on these arrive-only barriers; after a
     // timeout those waits return at once, so every handoff then blocks.
-    auto handoff = [&](int id, int count) {
-        fence_async_smem();
+    // The proxy fence is needed only after shared-memory writes that the
+    // tensor core or a TMA copy reads (smem_operands); TMEM writes need only
+    // the tcgen05 fence.
+    auto handoff = [&](int id, int count, bool smem_operands) {
+        if (smem_operands) fence_async_smem();
         tc_fence_before_sync();
         if (*abort_flag)
             named_sync(id, count);
@@ -720,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(-dd[2 * e], -dd[2 * e + 1]);
             tmem_st8(tl + kTmZTb + 8 * iq, w);
             tmem_st_wait();
-            handoff(kBarHZ, kHand);
+            handoff(kBarHZ, kHand, false);
         }
 
         // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(smem + kOpR + pn * 16384 + kmajor_off(r, ch, kD)) =
                     pack_bf16x8(rr);
             }
-            handoff(kBarH2, kHand);
+            handoff(kBarH2, kHand, true);
         }
 
         // ---------------- 4 scan: U^T read-back as the bf16 A operand of batch 4
@@ -796,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
             tmem_st8(tl + kTmUTb + 8 * iq, w);
             tmem_st_wait();
-            handoff(kBarH1, kHand);
+            handoff(kBarH1, kHand, false);
         }
 
         // ---------------- 5 prep: A (f32) and P (bf16) of chunk cn
@@ -805,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char *pbuf = smem + kOpP + pn * 8192;
             if (!slow) {
                 // the solver warps read A themselves (gram rows 64-127)
-                handoff(kBarDiag, kCompute + 64);
+                handoff(kBarDiag, kCompute + 64, true);
                 if (wq < 2) {  // P rows: gram rows 0-63
                     wait_on(bar_g, ph_g);  // gram of chunk cn
                     float dd[16];
@@ -844,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sA[sq_idx(r, s)] = av;
                     op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
                 }
-                handoff(kBarDiag, kCompute + 64);  // the solver warps invert I + A
+                handoff(kBarDiag, kCompute + 64, true);  // the solver warps invert I + A
             }
         }
 
@@ -906,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tl + kTmSTb + 16 * iq, w);
             tmem_st_wait();
             if (has_next2 && tid < kC) cp_async_wait_all();  // beta of chunk cn + 1
-            handoff(kBarH4, kHand);
+            handoff(kBarH4, kHand, false);
         }
     }
 
