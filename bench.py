@@ -45,7 +45,7 @@ NCU_TRAFFIC = {
     # decode B64: one launch, --set full capture (136.3 MB read + 73.9 MB written)
     "gdr_decode_kernel": {"bytes": 210_200_000, "sha": "1b350c7a4ac6f3e0"},
     # prefill_t16k: one launch, --set full capture (2.165 GB read + 0.521 GB written)
-    "gdr_prefill_fused": {"bytes": 2_686_260_000, "sha": "2df958bc651a0548"},
+    "gdr_prefill_fused": {"bytes": 2_686_400_000, "sha": "24de0c0ac4504926"},
 }
 
 
