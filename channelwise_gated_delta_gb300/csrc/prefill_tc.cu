@@ -538,26 +538,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
                 if (slow_flag[pn] == 0) {
                     // A = beta-scaled strictly lower part of gram rows 64-127
+                    // (blocks above the diagonal are never read: not written)
                     wait_on(bar_g, ph_gs);  // gram of chunk cn
-                    const int r = 32 * sw + lane;
+                    const int r = 32 * sw + lane, rb = r >> 4;
                     const float br = bvec[r];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
+                        if (sw == 0 && g >= 2) break;  // rows 0-31: column blocks 0-1 only
                         float dd[16];
                         tmem_ld16(tl + kTmGram + 16 * g, dd);
-                        const bool diag = g == (r >> 4);
+                        if (g == rb) {  // diagonal block, stored transposed
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            const int s = 16 * g + u;
-                            const float a = (s < r && r < Ln) ? br * dd[u] : 0.f;
-                            if (diag)
-                                sA[diagT_idx(g, u, r & 15)] = a;
-                            else
-                                sA[sq_idx(r, s)] = a;
+                            for (int u = 0; u < 16; ++u)
+                                sA[diagT_idx(g, u, r & 15)] = (16 * g + u < r && r < Ln) ? br * dd[u] : 0.f;
+                        } else if (g < rb) {
+#pragma unroll
+                            for (int u = 0; u < 16; ++u)
+                                sA[sq_idx(r, 16 * g + u)] = r < Ln ? br * dd[u] : 0.f;
                         }
                     }
-                    named_sync(kBarAux, 64);
                 }
+                // Each solver warp's diagonal blocks and level-1 block use only
+                // the rows it read itself (or, on the exact path, rows written
+                // before the DIAG barrier): a warp barrier suffices until level 2.
+                __syncwarp();
                 // diagonal 16 x 16 blocks of T = (I + A)^-1: one thread per
                 // column (block I = t / 16, column jj = t % 16), right-looking;
                 // column s2 of A's block is one contiguous run of 16 floats,
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         opt[kmajor_off(16 * I + p + 1, 16 * I + jj, kC) >> 1] = h.y;
                     }
                 }
-                named_sync(kBarAux, 64);
+                __syncwarp();
                 // off-diagonal blocks by 32 x 32 block recursion:
                 //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
                 //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
