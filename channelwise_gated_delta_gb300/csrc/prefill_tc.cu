@@ -102,8 +102,8 @@ constexpr uint32_t kSmall = kX32 + 4096;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
 constexpr uint32_t kEGm = kBeta + 512;        // f32 [2][128] exp(G_m) (by chunk parity)
 constexpr uint32_t kCL = kEGm + 1024;         // f32 [2][128] exp(G_last - G_m)
-constexpr uint32_t kGamL = kCL + 1024;        // f32 [2][128] exp(G_last)
-constexpr uint32_t kTot = kGamL + 1024;       // f32 [3][128] prefix-sum carries, then G_m and G_last
+constexpr uint32_t kRho = kCL + 1024;         // f32 [2][128] exp(G_last) / exp(G_m) (by chunk parity)
+constexpr uint32_t kTot = kRho + 1024;        // f32 [3][128] prefix-sum carries
 constexpr uint32_t kBarA = kTot + 1536;       // mbarriers: MMA batches a, b, g, 4
 constexpr uint32_t kBarB = kBarA + 8;
 constexpr uint32_t kBarG = kBarB + 8;
@@ -711,10 +711,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
                 const float gm = slow ? 0.f : gval(mref, tid), gl = gval(Ln - 1, tid);
-                vec(kEGm, pn)[tid] = slow ? 1.f : fast_exp2(gm);
+                const float egm = slow ? 1.f : fast_exp2(gm);
+                vec(kEGm, pn)[tid] = egm;
                 vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
-                vec(kGamL, pn)[tid] = fast_exp2(gl);
+                vec(kRho, pn)[tid] = fast_exp2(gl - gm);  // exp(G_L) / exp(G_m)
+                if (has_scan) {
+                    // The state registers hold S' = exp(G_m) S of the chunk being
+                    // scanned; the update to the next chunk's S' is
+                    //   S'_{c+1} = [exp(G_m') rho] S'_c + [exp(G_m') cL] dS
+                    // (G_m' the next chunk's reference row), written over
+                    // chunk c's rho and cL, which nothing else reads
+                    vec(kRho, ps)[tid] *= egm;
+                    vec(kCL, ps)[tid] *= egm;
+                }
             }
+            csync();  // the vectors are read by every state warp in step 6
         }
 
         // ---------------- 2 scan: -Z^T read-back as the bf16 A operand of batch b
@@ -859,12 +870,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_scan) {
             wait_on(bar_4, ph_4);  // batch 4 of chunk c
             {
+                // S' <- alpha S' + delta dS (the next chunk's S', or after the
+                // last chunk S itself: there the factors are rho and cL)
                 const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
-                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kGamL, ps) + 32 * iq);
+                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kRho, ps) + 32 * iq);
                 float dd[32];
                 tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {  // S = exp(G_L) S + cL dS, packed fp32 pairs
+                for (int u4 = 0; u4 < 8; ++u4) {  // packed fp32 pairs
                     const float4 cl = cl4[u4], gm = gam4[u4];
                     S2[2 * u4] = __ffma2_rn(make_float2(gm.x, gm.y), S2[2 * u4],
                                             __fmul2_rn(make_float2(cl.x, cl.y),
@@ -897,19 +910,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as the bf16 A
-        // operand of batch a (S now holds that chunk's starting state; the
-        // previous batch a was waited for in step 2)
+        // operand of batch a (the registers hold S' already, except for the
+        // first chunk, whose h0 is scaled here; the previous batch a was
+        // waited for in step 2)
         if (has_prep) {
-            const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
+            if (!has_scan) {
+                const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 e = egm4[u4];
+                    S2[2 * u4] = __fmul2_rn(S2[2 * u4], make_float2(e.x, e.y));
+                    S2[2 * u4 + 1] = __fmul2_rn(S2[2 * u4 + 1], make_float2(e.z, e.w));
+                }
+            }
             uint32_t w[16];
 #pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4) {
-                const float4 e = egm4[u4];
-                const float2 a = __fmul2_rn(S2[2 * u4], make_float2(e.x, e.y));
-                const float2 c2 = __fmul2_rn(S2[2 * u4 + 1], make_float2(e.z, e.w));
-                w[2 * u4] = pack_bf16x2(a.x, a.y);
-                w[2 * u4 + 1] = pack_bf16x2(c2.x, c2.y);
-            }
+            for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(S2[h].x, S2[h].y);
             tmem_st16(tl + kTmSTb + 16 * iq, w);
             tmem_st_wait();
             if (has_next2 && tid < kC) cp_async_wait_all();  // beta of chunk cn + 1
