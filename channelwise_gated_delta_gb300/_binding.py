@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
                 7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_ALIAS"}
 
 EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_forward_chunked_noalloc",
-            "gdr_device_check",
+            "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_device_check",
             "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma", "gdr_status_string",
             "gdr_last_cuda_error", "gdr_version")
 
@@ -58,6 +58,11 @@ def load_library(path=LIB_PATH):
     lib.gdr_forward.restype = i
     lib.gdr_forward_chunked_noalloc.argtypes = fwd
     lib.gdr_forward_chunked_noalloc.restype = i
+    ip = ctypes.POINTER(i)
+    lib.gdr_varlen_workspace_bytes.argtypes = [ip, i, i, i, i, i, i, i, u]
+    lib.gdr_varlen_workspace_bytes.restype = sz
+    lib.gdr_forward_varlen.argtypes = [vp] * 8 + [ip] + [i] * 6 + [vp, i, vp, sz, u]
+    lib.gdr_forward_varlen.restype = i
     lib.gdr_device_check.argtypes = [vp]
     lib.gdr_device_check.restype = i
     lib.gdr_status_string.argtypes = [i]
@@ -152,6 +157,82 @@ def gdr_forward(q, k, v, g, beta, h0=None, out=None, ht=None, chunk=64, stream=N
                             ctypes.c_void_p(stream.cuda_stream), code, ws_ptr, ws_bytes, flags)
     _check(lib, st)
     return out, ht
+
+
+def _cu_array(cu_seqlens):
+    """cu_seqlens (a sequence of ints or a CPU integer tensor) as a ctypes int32 array."""
+    if isinstance(cu_seqlens, torch.Tensor):
+        if cu_seqlens.device.type != "cpu":
+            raise ValueError("cu_seqlens must be host memory (a CPU tensor or a list)")
+        cu_seqlens = cu_seqlens.tolist()
+    vals = [int(x) for x in cu_seqlens]
+    if not vals:
+        raise ValueError("cu_seqlens needs at least one entry")
+    return (ctypes.c_int * len(vals))(*vals), len(vals) - 1
+
+
+def gdr_varlen_workspace_bytes(cu_seqlens, HK, HV, dk, dv, chunk=64, dtype=torch.bfloat16, flags=0):
+    lib = load_library()
+    cu, n = _cu_array(cu_seqlens)
+    return int(lib.gdr_varlen_workspace_bytes(cu, n, HK, HV, dk, dv, chunk, _dtype_code(dtype),
+                                              flags))
+
+
+def gdr_forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, out=None, ht=None, chunk=64,
+                       stream=None, workspace=None, flags=0, store_ht=True):
+    """Packed variable-length batch: N sequences stored back to back.
+
+    q, k [total, HK, dk]; v [total, HV, dv]; g [total, HV, dk] f32; beta [total, HV]
+    f32 (a leading batch dim of 1 is accepted and kept on ``out``); cu_seqlens
+    host ints [N + 1]; h0 / ht [N, HV, dk, dv] f32.  Returns (out, ht).
+    """
+    lib = load_library()
+    cu, n = _cu_array(cu_seqlens)
+    lead = q.dim() == 4
+    if lead:
+        if q.shape[0] != 1:
+            raise ValueError("a packed batch has a leading dim of 1")
+        q, k, v, g, beta = q[0], k[0], v[0], g[0], beta[0]
+    total, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("out", out), ("ht", ht)):
+        if t is None:
+            continue
+        if t.device != dev or dev.type != "cuda":
+            raise ValueError("%s must be a CUDA tensor on %s" % (name, dev))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if cu[n] != total:
+        raise ValueError("cu_seqlens[-1] (%d) != number of token rows (%d)" % (cu[n], total))
+    if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k must match q in shape and dtype; v must match q in dtype")
+    if v.shape[0] != total or tuple(g.shape) != (total, HV, dk) or tuple(beta.shape) != (total, HV):
+        raise ValueError("inconsistent shapes")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if h0 is not None and (tuple(h0.shape) != (n, HV, dk, dv) or h0.dtype != torch.float32):
+        raise ValueError("h0 must be float32 [N, HV, dk, dv]")
+    if out is None:
+        out = torch.empty(total, HV, dv, dtype=q.dtype, device=dev)
+    elif out.dim() == 4:
+        out = out[0]
+    if ht is None and store_ht:
+        ht = torch.empty(n, HV, dk, dv, dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    need = int(lib.gdr_varlen_workspace_bytes(cu, n, HK, HV, dk, dv, chunk, code, flags))
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
+    st = lib.gdr_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                _ptr(out), _ptr(ht), cu, n, HK, HV, dk, dv, chunk,
+                                ctypes.c_void_p(stream.cuda_stream), code, ws_ptr, ws_bytes, flags)
+    _check(lib, st)
+    return (out.unsqueeze(0) if lead else out), ht
 
 
 def gdr_device_check(stream=None):

@@ -3,6 +3,7 @@
 // chunked hot loops for autovectorization", pytorch/executorch PR #21021,
 // second commit summary: T == 1 runs the two-pass token recurrence, T != 1
 // the chunkwise WY/UT form), workspace management and launches.
+#include <algorithm>
 #include <mutex>
 #include <stdint.h>
 #include <string.h>
@@ -38,18 +39,18 @@ bool overlap(Range a, Range b) {
     return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
 }
 
-// Validates shapes and pointers; fills `p`. Does not look at the workspace.
-gdr_status validate(const void *q, const void *k, const void *v, const float *g,
-                    const float *beta, const float *h0, void *out, float *ht, int B, int T,
-                    int HK, int HV, int dk, int dv, int chunk, int qkv_dtype, gdr::Problem *p) {
-    if (B < 0 || T < 0 || HK <= 0 || HV <= 0) return GDR_ERR_SHAPE;
+// Validates pointers for BT token rows and NS state slots (alignment,
+// overlap); the shape checks common to every entry point.
+gdr_status validate_rows(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, const float *h0, void *out, float *ht, long long BT,
+                         long long NS, int HK, int HV, int dk, int dv, int chunk, int qkv_dtype) {
+    if (HK <= 0 || HV <= 0) return GDR_ERR_SHAPE;
     if (HV % HK != 0) return GDR_ERR_SHAPE;
     if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
     if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk))
         return GDR_ERR_UNSUPPORTED;
     // every element count must fit comfortably in 63 bits, and grids in 31
-    const long long BT = (long long)B * T;
-    if (BT > (1LL << 40) || (long long)B * HV > (1LL << 30)) return GDR_ERR_SHAPE;
+    if (BT > (1LL << 40) || NS * HV > (1LL << 30)) return GDR_ERR_SHAPE;
     const bool work = BT > 0;
     if (work && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_NULL;
     // 16-byte alignment for everything read or written in vectors or bulk
@@ -65,16 +66,27 @@ gdr_status validate(const void *q, const void *k, const void *v, const float *g,
     const Range rv = range_of(v, (size_t)BT * HV * dv * es);
     const Range rg = range_of(g, (size_t)BT * HV * dk * 4);
     const Range rb = range_of(beta, (size_t)BT * HV * 4);
-    const Range rs0 = h0 ? range_of(h0, (size_t)B * HV * dk * dv * 4) : Range{0, 0};
+    const Range rs0 = h0 ? range_of(h0, (size_t)NS * HV * dk * dv * 4) : Range{0, 0};
     const Range ro = work ? range_of(out, (size_t)BT * HV * dv * es) : Range{0, 0};
-    const Range rst = ht ? range_of(ht, (size_t)B * HV * dk * dv * 4) : Range{0, 0};
+    const Range rst = ht ? range_of(ht, (size_t)NS * HV * dk * dv * 4) : Range{0, 0};
     const Range ins[] = {rq, rk, rv, rg, rb};
     for (const Range &r : ins) {
         if (overlap(ro, r) || overlap(rst, r)) return GDR_ERR_ALIAS;
     }
     if (overlap(ro, rs0) || overlap(ro, rst)) return GDR_ERR_ALIAS;
     if (h0 && ht && h0 != ht && overlap(rs0, rst)) return GDR_ERR_ALIAS;
+    return GDR_OK;
+}
 
+// Validates shapes and pointers of a dense [B, T] batch; fills `p`. Does not
+// look at the workspace.
+gdr_status validate(const void *q, const void *k, const void *v, const float *g,
+                    const float *beta, const float *h0, void *out, float *ht, int B, int T,
+                    int HK, int HV, int dk, int dv, int chunk, int qkv_dtype, gdr::Problem *p) {
+    if (B < 0 || T < 0) return GDR_ERR_SHAPE;
+    const gdr_status st = validate_rows(q, k, v, g, beta, h0, out, ht, (long long)B * T, B, HK,
+                                        HV, dk, dv, chunk, qkv_dtype);
+    if (st != GDR_OK) return st;
     *p = gdr::Problem{q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
                       qkv_dtype == GDR_BF16 ? 1 : 0};
     return GDR_OK;
@@ -149,6 +161,92 @@ gdr_status run(const gdr::Problem &p, Route r, void *ws, cudaStream_t stream) {
         }
     }
     return e == cudaSuccess ? GDR_OK : cuda_fail(e);
+}
+
+// ---- packed variable-length batches
+//
+// Workspace: the batch's tables (copied in from the host by one
+// cudaMemcpyAsync), then the chunk records of the CUDA-core prefill.  Each
+// part starts on a 256-byte boundary.
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct VarlenPlan {
+    std::vector<int2> rows;      // single-token sequences: {token row, slot}
+    std::vector<int4> tc_seqs;   // tensor-core prefill: {first row, length, slot, 0}
+    std::vector<int4> gen_seqs;  // CUDA-core prefill: {first row, length, slot, first chunk}
+    std::vector<int2> chunks;    // CUDA-core prefill: {first row, length} per chunk
+    std::vector<int> empty;      // slots of zero-length sequences
+    size_t off_rows = 0, off_tc = 0, off_maps = 0, off_gen = 0, off_chunks = 0;
+    size_t table_bytes = 0, record_off = 0, total_bytes = 0;
+};
+
+// Checks cu_seqlens (cu[0] = 0, non-decreasing, cu[N] < 2^31) and assigns
+// every sequence its route.  `p` carries the shapes; its pointers may be null.
+gdr_status check_cu_seqlens(const int *cu, int N) {
+    if (N < 0) return GDR_ERR_SHAPE;
+    if (N > 0 && !cu) return GDR_ERR_NULL;
+    if (N > 0 && cu[0] != 0) return GDR_ERR_SHAPE;
+    for (int n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return GDR_ERR_SHAPE;
+    return GDR_OK;
+}
+
+gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned flags,
+                       VarlenPlan *plan) {
+    const gdr_status st = check_cu_seqlens(cu, N);
+    if (st != GDR_OK) return st;
+    gdr::Problem one = p;  // a sequence of length L, for routing
+    one.B = 1;
+    long long nch = 0;
+    for (int n = 0; n < N; ++n) {
+        const int L = cu[n + 1] - cu[n];
+        one.T = L;
+        switch (choose(one, flags)) {
+            case Route::Nothing:
+                break;
+            case Route::EmptySequence:
+                plan->empty.push_back(n);
+                break;
+            case Route::Decode:
+                plan->rows.push_back(make_int2(cu[n], n));
+                break;
+            case Route::TensorCorePrefill:
+                plan->tc_seqs.push_back(make_int4(cu[n], L, n, 0));
+                break;
+            case Route::GenericPrefill:
+                plan->gen_seqs.push_back(make_int4(cu[n], L, n, 0));
+                nch += (L + p.chunk - 1) / p.chunk;
+                break;
+        }
+    }
+    if (nch * p.HV > 0x7fffffffLL) return GDR_ERR_SHAPE;
+    // longest first: a sequence's CTAs run its chunks in order, so the long
+    // ones start at once and the short ones fill in behind them
+    auto longer = [](const int4 &a, const int4 &b) { return a.y > b.y; };
+    std::stable_sort(plan->tc_seqs.begin(), plan->tc_seqs.end(), longer);
+    std::stable_sort(plan->gen_seqs.begin(), plan->gen_seqs.end(), longer);
+    for (int4 &sd : plan->gen_seqs) {
+        sd.w = (int)plan->chunks.size();
+        for (int t = 0; t < sd.y; t += p.chunk)
+            plan->chunks.push_back(make_int2(sd.x + t, std::min(p.chunk, sd.y - t)));
+    }
+    size_t off = 0;
+    plan->off_rows = off;
+    off = align256(off + plan->rows.size() * sizeof(int2));
+    plan->off_tc = off;
+    off = align256(off + plan->tc_seqs.size() * sizeof(int4));
+    plan->off_maps = off;
+    off = align256(off + plan->tc_seqs.size() * gdr::tc_seq_maps_bytes());
+    plan->off_gen = off;
+    off = align256(off + plan->gen_seqs.size() * sizeof(int4));
+    plan->off_chunks = off;
+    off = align256(off + plan->chunks.size() * sizeof(int2));
+    plan->table_bytes = off;
+    plan->record_off = off;
+    const bool any = !plan->rows.empty() || !plan->tc_seqs.empty() || !plan->gen_seqs.empty();
+    plan->total_bytes =
+        any ? off + gdr::generic_varlen_record_bytes(p, (long long)plan->chunks.size()) : 0;
+    return GDR_OK;
 }
 
 // Library-owned workspace, one per device.
@@ -316,6 +414,102 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
         ws = w.ptr;
     }
     return run(p, r, ws, static_cast<cudaStream_t>(stream));
+}
+
+GDR_API size_t gdr_varlen_workspace_bytes(const int *cu_seqlens, int N, int HK, int HV, int dk,
+                                          int dv, int chunk, int qkv_dtype, unsigned flags) {
+    if (HK <= 0 || HV <= 0 || HV % HK != 0) return 0;
+    if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk)) return 0;
+    const gdr::Problem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         N, 0, HK, HV, dk, dv, chunk, qkv_dtype == GDR_BF16 ? 1 : 0};
+    VarlenPlan plan;
+    if (plan_varlen(cu_seqlens, N, p, flags, &plan) != GDR_OK) return 0;
+    return plan.total_bytes;
+}
+
+GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, const float *h0, void *out, float *ht,
+                                      const int *cu_seqlens, int N, int HK, int HV, int dk, int dv,
+                                      int chunk, void *stream, int qkv_dtype, void *workspace,
+                                      size_t workspace_bytes, unsigned flags) {
+    gdr_status st = check_cu_seqlens(cu_seqlens, N);
+    if (st != GDR_OK) return st;
+    const long long total = N > 0 ? cu_seqlens[N] : 0;
+    st = validate_rows(q, k, v, g, beta, h0, out, ht, total, N, HK, HV, dk, dv, chunk,
+                                  qkv_dtype);
+    if (st != GDR_OK) return st;
+    const gdr::Problem base{q, k, v, g, beta, h0, out, ht, N, 0, HK, HV, dk, dv, chunk,
+                            qkv_dtype == GDR_BF16 ? 1 : 0};
+    VarlenPlan plan;
+    st = plan_varlen(cu_seqlens, N, base, flags, &plan);
+    if (st != GDR_OK) return st;
+    if (plan.total_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.total_bytes) return GDR_ERR_WORKSPACE;
+        if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaError_t e = cudaSuccess;
+
+    // tables, staged on the host and copied in one piece
+    if (plan.table_bytes > 0) {
+        std::vector<unsigned char> host(plan.table_bytes, 0);
+        if (!plan.rows.empty())
+            memcpy(host.data() + plan.off_rows, plan.rows.data(), plan.rows.size() * sizeof(int2));
+        if (!plan.tc_seqs.empty())
+            memcpy(host.data() + plan.off_tc, plan.tc_seqs.data(), plan.tc_seqs.size() * sizeof(int4));
+        for (size_t i = 0; i < plan.tc_seqs.size(); ++i) {
+            e = gdr::tc_encode_seq_maps(base, (size_t)plan.tc_seqs[i].x, plan.tc_seqs[i].y,
+                                        host.data() + plan.off_maps + i * gdr::tc_seq_maps_bytes());
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        if (!plan.gen_seqs.empty())
+            memcpy(host.data() + plan.off_gen, plan.gen_seqs.data(), plan.gen_seqs.size() * sizeof(int4));
+        if (!plan.chunks.empty())
+            memcpy(host.data() + plan.off_chunks, plan.chunks.data(), plan.chunks.size() * sizeof(int2));
+        // pageable source: the call returns once the bytes have been taken
+        e = cudaMemcpyAsync(ws, host.data(), plan.table_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    // zero-length sequences: the final state is the initial one
+    if (ht && h0 != ht) {
+        const size_t bytes = (size_t)HV * dk * dv * sizeof(float);
+        for (int n : plan.empty) {
+            float *dst = ht + (size_t)n * HV * dk * dv;
+            e = h0 ? cudaMemcpyAsync(dst, h0 + (size_t)n * HV * dk * dv, bytes,
+                                     cudaMemcpyDeviceToDevice, s)
+                   : cudaMemsetAsync(dst, 0, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    if (!plan.rows.empty()) {
+        gdr::Problem p = base;
+        p.B = (int)plan.rows.size();
+        p.T = 1;
+        e = gdr::launch_decode_rows(p, reinterpret_cast<const int2 *>(ws + plan.off_rows), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!plan.tc_seqs.empty()) {
+        int *err = nullptr;
+        e = gdr::device_error_word(&err);
+        if (e != cudaSuccess) return cuda_fail(e);
+        gdr::Problem p = base;
+        p.B = (int)plan.tc_seqs.size();
+        e = gdr::launch_tc_prefill_varlen(p, ws + plan.off_maps,
+                                          reinterpret_cast<const int4 *>(ws + plan.off_tc), p.B,
+                                          err, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!plan.gen_seqs.empty()) {
+        gdr::Problem p = base;
+        p.B = (int)plan.gen_seqs.size();
+        e = gdr::launch_generic_prefill_varlen(
+            p, ws + plan.record_off, reinterpret_cast<const int2 *>(ws + plan.off_chunks),
+            (int)plan.chunks.size(), reinterpret_cast<const int4 *>(ws + plan.off_gen), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GDR_OK;
 }
 
 GDR_API gdr_status gdr_device_check(void *stream) {

@@ -85,4 +85,22 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream);
 size_t generic_prefill_workspace_bytes(const Problem &p);
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream);
+
+// Packed variable-length batches (p.B = number of entries in the table, the
+// pointers those of the packed tensors).
+// Decode of single tokens: rows[b] = {token row, state slot}.
+cudaError_t launch_decode_rows(const Problem &p, const int2 *rows, cudaStream_t stream);
+// Tensor-core prefill: seqs[s] = {first token row, length, state slot, -};
+// seq_maps: one tensor-map set per sequence (tc_seq_maps_bytes() each,
+// 64-byte aligned, in device memory), filled on the host by tc_encode_seq_maps.
+size_t tc_seq_maps_bytes();
+cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst);
+cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, const int4 *seqs,
+                                     int nseq, int *dev_error, cudaStream_t stream);
+// CUDA-core chunked prefill: chunks[i] = {first token row, length} of every
+// sequence's chunks, seqs[s] = {first token row, length, state slot, index
+// of its first chunk}; records: generic_varlen_record_bytes(p, nchunks).
+size_t generic_varlen_record_bytes(const Problem &p, long long nchunks);
+cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
+                                          int nchunks, const int4 *seqs, cudaStream_t stream);
 }  // namespace gdr

@@ -66,12 +66,12 @@ __device__ __forceinline__ float4 block_column_sum(float4 part, float (*red)[kDe
     return tot;
 }
 
-template <typename Tin, int DK, bool HAS_H0, bool STORE_HT>
+template <typename Tin, int DK, bool HAS_H0, bool STORE_HT, bool ROWS>
 __global__ void __launch_bounds__(2 * DK)
     gdr_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                       const Tin *__restrict__ v, const float *__restrict__ g,
                       const float *__restrict__ beta, const float *h0, Tin *__restrict__ out,
-                      float *ht, int HK, int HV, int dv) {
+                      float *ht, const int2 *__restrict__ rows, int HK, int HV, int dv) {
     constexpr int NT = 2 * DK;
     constexpr int NW = NT / 32;
     constexpr int RG = DK / 4;  // row groups; each thread holds 4 rows
@@ -87,10 +87,20 @@ __global__ void __launch_bounds__(2 * DK)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = tid & 7, rg = tid >> 3;
     const int col = tile * kDecodeBV + 4 * cq;
-    const size_t head = (size_t)head_idx;
+    // token row and state slot of this batch element: both b, or for one
+    // token of a packed variable-length batch, taken from `rows`
+    int trow = b;
+    size_t head = (size_t)head_idx;  // token-major: q/k/v/g/beta/out
+    size_t shead = head;             // state-major: h0/ht
+    if (ROWS) {
+        const int2 r = rows[b];
+        trow = r.x;
+        head = (size_t)r.x * HV + hv;
+        shead = (size_t)r.y * HV + hv;
+    }
 
-    const Tin *kp = k + ((size_t)b * HK + hk) * DK;
-    const Tin *qp = q + ((size_t)b * HK + hk) * DK;
+    const Tin *kp = k + ((size_t)trow * HK + hk) * DK;
+    const Tin *qp = q + ((size_t)trow * HK + hk) * DK;
     const float *gp = g + head * DK;
     const float bt = beta[head];
     const float4 vv = load4(v + head * dv + col);
@@ -102,7 +112,7 @@ __global__ void __launch_bounds__(2 * DK)
     for (int m = 0; m < 4; ++m) {
         const int r = rg + RG * m;
         if (HAS_H0) {
-            s[m] = ldg_stream4(h0 + (head * DK + r) * dv + col);
+            s[m] = ldg_stream4(h0 + (shead * DK + r) * dv + col);
         } else {
             s[m] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -130,14 +140,14 @@ __global__ void __launch_bounds__(2 * DK)
     for (int m = 0; m < 4; ++m) {
         s[m] = f4_fma(kr[m], u, s[m]);
         oacc = f4_fma(qr[m], s[m], oacc);
-        if (STORE_HT) stg_stream4(ht + (head * DK + rg + RG * m) * dv + col, s[m]);
+        if (STORE_HT) stg_stream4(ht + (shead * DK + rg + RG * m) * dv + col, s[m]);
     }
     const float4 o = block_column_sum<NW>(oacc, red2, warp, lane, cq);
     if (tid < 8) store4(out + head * dv + col, o);
 }
 
-template <typename Tin, int DK>
-cudaError_t launch_decode_t(const Problem &p, cudaStream_t stream) {
+template <typename Tin, int DK, bool ROWS>
+cudaError_t launch_decode_t(const Problem &p, const int2 *rows, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.HV * (p.dv / kDecodeBV);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)blocks), block(2 * DK);
@@ -146,27 +156,27 @@ cudaError_t launch_decode_t(const Problem &p, cudaStream_t stream) {
     Tin *out = static_cast<Tin *>(p.out);
     trace_begin(kKernDecode, stream);
     if (p.h0 && p.ht)
-        gdr_decode_kernel<Tin, DK, true, true><<<grid, block, 0, stream>>>(
-            q, k, v, p.g, p.beta, p.h0, out, p.ht, p.HK, p.HV, p.dv);
+        gdr_decode_kernel<Tin, DK, true, true, ROWS><<<grid, block, 0, stream>>>(
+            q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else if (p.h0)
-        gdr_decode_kernel<Tin, DK, true, false><<<grid, block, 0, stream>>>(
-            q, k, v, p.g, p.beta, p.h0, out, p.ht, p.HK, p.HV, p.dv);
+        gdr_decode_kernel<Tin, DK, true, false, ROWS><<<grid, block, 0, stream>>>(
+            q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else if (p.ht)
-        gdr_decode_kernel<Tin, DK, false, true><<<grid, block, 0, stream>>>(
-            q, k, v, p.g, p.beta, p.h0, out, p.ht, p.HK, p.HV, p.dv);
+        gdr_decode_kernel<Tin, DK, false, true, ROWS><<<grid, block, 0, stream>>>(
+            q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else
-        gdr_decode_kernel<Tin, DK, false, false><<<grid, block, 0, stream>>>(
-            q, k, v, p.g, p.beta, p.h0, out, p.ht, p.HK, p.HV, p.dv);
+        gdr_decode_kernel<Tin, DK, false, false, ROWS><<<grid, block, 0, stream>>>(
+            q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     trace_end(kKernDecode, stream);
     return cudaGetLastError();
 }
 
-template <typename Tin>
-cudaError_t launch_decode_dt(const Problem &p, cudaStream_t stream) {
+template <typename Tin, bool ROWS>
+cudaError_t launch_decode_dt(const Problem &p, const int2 *rows, cudaStream_t stream) {
     switch (p.dk) {
-        case 32: return launch_decode_t<Tin, 32>(p, stream);
-        case 64: return launch_decode_t<Tin, 64>(p, stream);
-        case 128: return launch_decode_t<Tin, 128>(p, stream);
+        case 32: return launch_decode_t<Tin, 32, ROWS>(p, rows, stream);
+        case 64: return launch_decode_t<Tin, 64, ROWS>(p, rows, stream);
+        case 128: return launch_decode_t<Tin, 128, ROWS>(p, rows, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -174,7 +184,13 @@ cudaError_t launch_decode_dt(const Problem &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream) {
-    return p.bf16 ? launch_decode_dt<__nv_bfloat16>(p, stream) : launch_decode_dt<float>(p, stream);
+    return p.bf16 ? launch_decode_dt<__nv_bfloat16, false>(p, nullptr, stream)
+                  : launch_decode_dt<float, false>(p, nullptr, stream);
+}
+
+cudaError_t launch_decode_rows(const Problem &p, const int2 *rows, cudaStream_t stream) {
+    return p.bf16 ? launch_decode_dt<__nv_bfloat16, true>(p, rows, stream)
+                  : launch_decode_dt<float, true>(p, rows, stream);
 }
 
 }  // namespace gdr

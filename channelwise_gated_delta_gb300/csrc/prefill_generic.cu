@@ -58,8 +58,9 @@ template <typename Tin>
 __global__ void __launch_bounds__(kPrepThreads)
     gdr_chunk_prep(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ g,
-                   const float *__restrict__ beta, float *__restrict__ ws, int T, int HK, int HV,
-                   int dk, int dv, int C, int NC) {
+                   const float *__restrict__ beta, float *__restrict__ ws,
+                   const int2 *__restrict__ chunks, int T, int HK, int HV, int dk, int dv, int C,
+                   int NC) {
     extern __shared__ float smem[];
     const int ldk = dk + 1;  // padded rows: threads walking s hit distinct banks
     const int ldw = dk + dv;
@@ -70,32 +71,49 @@ __global__ void __launch_bounds__(kPrepThreads)
     float *Ws = As + C * C;         // [C][dk + dv]
     float *bs = Ws + C * ldw;       // [C]
 
-    const int c = blockIdx.x % NC;
-    const int head_idx = blockIdx.x / NC;
-    const int hv = head_idx % HV, b = head_idx / HV;
+    // The chunk: its first token row in the [rows][H][d] view of the inputs,
+    // its length, and its record.  Dense batches: CTA (b, hv, c), record
+    // (b, hv, c).  Packed variable-length batches: CTA (chunk, hv) over the
+    // table of every sequence's chunks {first row, length}, record (chunk, hv).
+    int hv, L;
+    size_t tr0, rec_idx;
+    if (chunks) {
+        const int ci = blockIdx.x / HV;
+        hv = blockIdx.x % HV;
+        const int2 e = chunks[ci];
+        tr0 = (size_t)e.x;
+        L = e.y;
+        rec_idx = (size_t)ci * HV + hv;
+    } else {
+        const int c = blockIdx.x % NC;
+        const int head_idx = blockIdx.x / NC;
+        hv = head_idx % HV;
+        const int b = head_idx / HV;
+        tr0 = (size_t)b * T + (size_t)c * C;
+        L = min(C, T - c * C);
+        rec_idx = (size_t)head_idx * NC + c;
+    }
     const int hk = hv / (HV / HK);
-    const int t0 = c * C;
-    const int L = min(C, T - t0);
     const int tid = threadIdx.x;
     const ChunkLayout lay{C, dk, dv};
-    float *rec = ws + ((size_t)head_idx * NC + c) * lay.floats();
+    float *rec = ws + rec_idx * lay.floats();
 
     // Load the chunk (rows >= L are zero; a zero gate keeps G flat there).
     for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
         const int r = idx / dk, i = idx % dk;
         float kv = 0.f, qv = 0.f, gv = 0.f;
         if (r < L) {
-            const size_t tk = ((size_t)b * T + t0 + r) * HK + hk;
+            const size_t tk = (tr0 + r) * HK + hk;
             kv = to_f32(k[tk * dk + i]);
             qv = to_f32(q[tk * dk + i]);
-            gv = g[(((size_t)b * T + t0 + r) * HV + hv) * dk + i];
+            gv = g[((tr0 + r) * HV + hv) * dk + i];
         }
         Ks[r * ldk + i] = kv;
         Qs[r * ldk + i] = qv;
         Gs[r * ldk + i] = gv;
     }
     for (int r = tid; r < C; r += kPrepThreads)
-        bs[r] = r < L ? beta[((size_t)b * T + t0 + r) * HV + hv] : 0.f;
+        bs[r] = r < L ? beta[(tr0 + r) * HV + hv] : 0.f;
     __syncthreads();
 
     // Per-channel inclusive prefix sum of the log-decay.
@@ -134,7 +152,7 @@ __global__ void __launch_bounds__(kPrepThreads)
             if (col < dk) {
                 x = bs[r] * Ks[r * ldk + col] * expf(Gs[r * ldk + col]);
             } else {
-                const size_t tv = ((size_t)b * T + t0 + r) * HV + hv;
+                const size_t tv = (tr0 + r) * HV + hv;
                 x = bs[r] * to_f32(v[tv * dv + (col - dk)]);
             }
         }
@@ -173,7 +191,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 template <typename Tin>
 __global__ void __launch_bounds__(kScanThreads)
     gdr_chunk_scan(const float *__restrict__ ws, const float *h0, Tin *__restrict__ out,
-                   float *ht, int T, int HV, int dk, int dv, int C, int NC) {
+                   float *ht, const int4 *__restrict__ seqs, int T_dense, int HV, int dk, int dv,
+                   int C, int NC_dense) {
     extern __shared__ float smem[];
     const int ldk = dk + 1;
     const int ldc = C + 1;
@@ -188,8 +207,24 @@ __global__ void __launch_bounds__(kScanThreads)
 
     const int ntile = dv / kScanBV;
     const int tile = blockIdx.x % ntile;
-    const int head_idx = blockIdx.x / ntile;
-    const int hv = head_idx % HV, b = head_idx / HV;
+    const int hv = (blockIdx.x / ntile) % HV;
+    const int b = blockIdx.x / ntile / HV;
+    // The sequence: first token row, length, state slot, and where its chunk
+    // records start and how far apart they are (dense: b's own rows, slot b,
+    // records (b, hv, c); packed: {first row, length, slot, first chunk}
+    // from the table, records (chunk, hv)).
+    size_t tok0 = (size_t)b * T_dense, rec0 = ((size_t)b * HV + hv) * NC_dense, rec_step = 1;
+    int T = T_dense, slot = b;
+    if (seqs) {
+        const int4 sd = seqs[b];
+        tok0 = (size_t)sd.x;
+        T = sd.y;
+        slot = sd.z;
+        rec0 = (size_t)sd.w * HV + hv;
+        rec_step = HV;
+    }
+    const int NC = (T + C - 1) / C;
+    const size_t head_idx = (size_t)slot * HV + hv;  // state slot
     const int j0 = tile * kScanBV;
     const int tid = threadIdx.x;
     const int jj = tid % kScanBV;        // column within the tile
@@ -198,11 +233,11 @@ __global__ void __launch_bounds__(kScanThreads)
 
     for (int idx = tid; idx < dk * kScanBV; idx += kScanThreads) {
         const int i = idx / kScanBV, j = idx % kScanBV;
-        Ss[idx] = h0 ? h0[((size_t)head_idx * dk + i) * dv + j0 + j] : 0.f;
+        Ss[idx] = h0 ? h0[(head_idx * dk + i) * dv + j0 + j] : 0.f;
     }
 
     for (int c = 0; c < NC; ++c) {
-        const float *rec = ws + ((size_t)head_idx * NC + c) * lay.floats();
+        const float *rec = ws + (rec0 + (size_t)c * rec_step) * lay.floats();
         const int t0 = c * C;
         const int L = min(C, T - t0);
         for (int idx = tid; idx < C * dk; idx += kScanThreads) {
@@ -236,7 +271,7 @@ __global__ void __launch_bounds__(kScanThreads)
             for (int i = 0; i < dk; ++i) acc = fmaf(qrow[i], Ss[i * kScanBV + jj], acc);
             const float *prow = Ps + r * ldc;
             for (int s = 0; s <= r; ++s) acc = fmaf(prow[s], Us[s * kScanBV + jj], acc);
-            out[(((size_t)b * T + t0 + r) * HV + hv) * dv + j0 + jj] = from_f32<Tin>(acc);
+            out[((tok0 + t0 + r) * HV + hv) * dv + j0 + jj] = from_f32<Tin>(acc);
         }
 
         // S = diag(gam) S0 + Kh^T U   (new values kept in registers until
@@ -257,7 +292,7 @@ __global__ void __launch_bounds__(kScanThreads)
     if (ht) {
         for (int idx = tid; idx < dk * kScanBV; idx += kScanThreads) {
             const int i = idx / kScanBV, j = idx % kScanBV;
-            ht[((size_t)head_idx * dk + i) * dv + j0 + j] = Ss[idx];
+            ht[(head_idx * dk + i) * dv + j0 + j] = Ss[idx];
         }
     }
 }
@@ -270,12 +305,15 @@ size_t scan_smem_bytes(int dk, int C) {
                             (size_t)2 * C * kScanBV + dk);
 }
 
+// Dense batches: chunks == seqs == nullptr, B x T from p.  Packed batches:
+// nchunks chunk records and p.B sequence records.
 template <typename Tin>
-cudaError_t launch_generic_t(const Problem &p, void *workspace, cudaStream_t stream) {
+cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chunks, int nchunks,
+                             const int4 *seqs, cudaStream_t stream) {
     const int C = p.chunk;
     const int NC = (p.T + C - 1) / C;
     float *ws = static_cast<float *>(workspace);
-    const long long prep_blocks = (long long)p.B * p.HV * NC;
+    const long long prep_blocks = chunks ? (long long)nchunks * p.HV : (long long)p.B * p.HV * NC;
     const long long scan_blocks = (long long)p.B * p.HV * (p.dv / kScanBV);
     if (prep_blocks > 0x7fffffffLL || scan_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const size_t sp = prep_smem_bytes(p.dk, p.dv, C);
@@ -288,13 +326,13 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, cudaStream_t str
     trace_begin(kKernChunkPrep, stream);
     gdr_chunk_prep<Tin><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
         static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
-        static_cast<const Tin *>(p.v), p.g, p.beta, ws, p.T, p.HK, p.HV, p.dk, p.dv, C, NC);
+        static_cast<const Tin *>(p.v), p.g, p.beta, ws, chunks, p.T, p.HK, p.HV, p.dk, p.dv, C, NC);
     trace_end(kKernChunkPrep, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     trace_begin(kKernChunkScan, stream);
     gdr_chunk_scan<Tin><<<(unsigned)scan_blocks, kScanThreads, ss, stream>>>(
-        ws, p.h0, static_cast<Tin *>(p.out), p.ht, p.T, p.HV, p.dk, p.dv, C, NC);
+        ws, p.h0, static_cast<Tin *>(p.out), p.ht, seqs, p.T, p.HV, p.dk, p.dv, C, NC);
     trace_end(kKernChunkScan, stream);
     return cudaGetLastError();
 }
@@ -308,8 +346,19 @@ size_t generic_prefill_workspace_bytes(const Problem &p) {
 }
 
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream) {
-    return p.bf16 ? launch_generic_t<__nv_bfloat16>(p, workspace, stream)
-                  : launch_generic_t<float>(p, workspace, stream);
+    return p.bf16 ? launch_generic_t<__nv_bfloat16>(p, workspace, nullptr, 0, nullptr, stream)
+                  : launch_generic_t<float>(p, workspace, nullptr, 0, nullptr, stream);
+}
+
+size_t generic_varlen_record_bytes(const Problem &p, long long nchunks) {
+    const ChunkLayout lay{p.chunk, p.dk, p.dv};
+    return sizeof(float) * lay.floats() * (size_t)nchunks * p.HV;
+}
+
+cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
+                                          int nchunks, const int4 *seqs, cudaStream_t stream) {
+    return p.bf16 ? launch_generic_t<__nv_bfloat16>(p, records, chunks, nchunks, seqs, stream)
+                  : launch_generic_t<float>(p, records, chunks, nchunks, seqs, stream);
 }
 
 }  // namespace gdr

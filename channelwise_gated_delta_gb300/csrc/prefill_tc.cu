@@ -61,6 +61,7 @@
 // on tf32 mma.sync, on the four auxiliary warps.
 #include <cuda.h>
 #include <mutex>
+#include <string.h>
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -307,10 +308,14 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
     }
 }
 
-template <bool HAS_H0, bool STORE_HT>
+// Packed variable-length batches: one record per sequence, {first token row
+// in the packed tensors, length, state slot}; the sequence's tensor maps sit
+// at the same index of a TileMaps array in global memory.
+template <bool HAS_H0, bool STORE_HT, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const float *__restrict__ beta,
-                          const float *h0, float *ht, int T, int HK, int HV, int *dev_error) {
+    gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const TileMaps *seq_maps,
+                          const int4 *seqs, const float *__restrict__ beta, const float *h0,
+                          float *ht, int T_dense, int HK, int HV, int *dev_error) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
     unsigned char *smem =
@@ -329,9 +334,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = aw - 2;                // solver warp index 0..1
     const int wq = warp & 3;        // TMEM lane quarter of this warp
     const int iq = (warp >> 2) & 3; // which quarter of the key channels / tokens this warp takes
-    const int head = blockIdx.x;    // b * HV + hv
-    const int hv = head % HV, b = head / HV;
+    const int head = blockIdx.x;    // b * HV + hv (b: the sequence's index)
+    const int hv = head % HV;
+    int b = head / HV;              // batch coordinate of the tensor maps
     const int hk = hv / (HV / HK);
+    int T = T_dense;
+    size_t tok0 = (size_t)b * T;    // the sequence's first token row
+    size_t shead = head;            // state slot * HV + hv
+    const TileMaps *mp = &tm;
+    if (VARLEN) {
+        const int4 sd = seqs[b];
+        tok0 = (size_t)sd.x;
+        T = sd.y;
+        shead = (size_t)sd.z * HV + hv;
+        mp = seq_maps + b;
+        b = 0;  // each sequence's maps describe a [1][T][H][128] tensor
+        // the maps were written to global memory before the launch: order
+        // those writes before this thread's tensor-map reads
+        fence_tensormap_acquire(&mp->k);
+        fence_tensormap_acquire(&mp->q);
+        fence_tensormap_acquire(&mp->g);
+        fence_tensormap_acquire(&mp->v);
+        fence_tensormap_acquire(&mp->o);
+    }
+    const TileMaps &m = *mp;
     const int j = 32 * wq + lane;   // this thread's value column (TMEM lane)
 
     float *sTot = reinterpret_cast<float *>(smem + kTot);
@@ -390,20 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_v, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm.k);
-        tma_prefetch_desc(&tm.q);
-        tma_prefetch_desc(&tm.g);
-        tma_prefetch_desc(&tm.v);
-        tma_prefetch_desc(&tm.o);
+        tma_prefetch_desc(&m.k);
+        tma_prefetch_desc(&m.q);
+        tma_prefetch_desc(&m.g);
+        tma_prefetch_desc(&m.v);
+        tma_prefetch_desc(&m.o);
     }
     __syncthreads();
     if (issuer_warp && !issuer_a) {  // first chunk's inputs (warp B issues every TMA load)
-        issue_kqg(smem, tm, bar_kqg, b, 0, hk, hv, lane);
-        if (lane == 0) issue_v(smem, tm, bar_v, b, 0, hv);
+        issue_kqg(smem, m, bar_kqg, b, 0, hk, hv, lane);
+        if (lane == 0) issue_v(smem, m, bar_v, b, 0, hv);
     }
     if (tid < kC)  // beta buffers: [2][64] floats by chunk parity
         reinterpret_cast<float *>(smem + kBeta)[tid] =
-            tid < min(kC, T) ? beta[((size_t)b * T + tid) * HV + hv] : 0.f;
+            tid < min(kC, T) ? beta[(tok0 + tid) * HV + hv] : 0.f;
     // T' is lower triangular: its strictly-upper 16 x 16 blocks stay zero
     for (int idx = tid; idx < 64 * 8; idx += kThreads) {
         const int r = idx >> 3, s0 = (idx & 7) * 8;
@@ -414,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 S2[16];
 #pragma unroll
     for (int h = 0; h < 16; ++h) {
-        S2[h].x = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + 2 * h) * kD + j] : 0.f;
-        S2[h].y = (HAS_H0 && !aux) ? h0[((size_t)head * kD + 32 * iq + 2 * h + 1) * kD + j] : 0.f;
+        S2[h].x = (HAS_H0 && !aux) ? h0[(shead * kD + 32 * iq + 2 * h) * kD + j] : 0.f;
+        S2[h].y = (HAS_H0 && !aux) ? h0[(shead * kD + 32 * iq + 2 * h + 1) * kD + j] : 0.f;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -488,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         // the raw k, q, g tiles are consumed: fetch the next chunk's
                         if (!issuer_a && has_next2) {
-                            issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                            issue_kqg(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
                             ++issued_kqg;
                         }
                     }
@@ -511,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // batch b of chunk c has completed (the state warps waited
                         // for it): v's buffer takes the prepared chunk's
                         if (!issuer_a && has_prep) {
-                            issue_v(smem, tm, bar_v, b, t0n, hv);
+                            issue_v(smem, m, bar_v, b, t0n, hv);
                             ++issued_v;
                         }
                     }
@@ -519,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (has_prep) {
                     named_sync(kBarH4, kHand);
                     if (!issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
-                        issue_kqg(smem, tm, bar_kqg, b, t0n + kC, hk, hv, lane);
+                        issue_kqg(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
                         ++issued_kqg;
                     }
                     if (lane == 0 && !*abort_flag) {
@@ -667,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (has_next2 && tid < kC) {
                 float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
                 if (t0n + kC + tid < T)
-                    cp_async4(dst, beta + ((size_t)b * T + t0n + kC + tid) * HV + hv);
+                    cp_async4(dst, beta + (tok0 + t0n + kC + tid) * HV + hv);
                 else
                     *dst = 0.f;
             }
@@ -904,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // one TMA store per warp; rows past the end of the sequence
                 // fall outside the tensor and are dropped
                 if (lane == 0 && !*abort_flag) {
-                    tma_store_4d(&tm.o, stg, 32 * wq, hv, t0 + 16 * iq, b);
+                    tma_store_4d(&m.o, stg, 32 * wq, hv, t0 + 16 * iq, b);
                     bulk_commit_group();
                 }
             }
@@ -946,8 +972,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!aborted && STORE_HT && !aux) {
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-            ht[((size_t)head * kD + 32 * iq + 2 * h) * kD + j] = S2[h].x;
-            ht[((size_t)head * kD + 32 * iq + 2 * h + 1) * kD + j] = S2[h].y;
+            ht[(shead * kD + 32 * iq + 2 * h) * kD + j] = S2[h].x;
+            ht[(shead * kD + 32 * iq + 2 * h + 1) * kD + j] = S2[h].y;
         }
     }
     tc_fence_before_sync();
@@ -1001,35 +1027,74 @@ bool tc_prefill_supported(const Problem &p) {
     return p.bf16 && p.dk == kD && p.dv == kD && p.chunk == kC;
 }
 
-cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream) {
-    const long long blocks = (long long)p.B * p.HV;
+namespace {
+
+// The five tensor maps of a [B][T][H][128] problem whose token 0 of batch 0
+// sits at row `tok0` of the packed tensors.
+bool encode_maps(EncodeTiledFn fn, TileMaps *tm, const Problem &p, size_t tok0, int B, int T) {
+    const char *q = static_cast<const char *>(p.q) + tok0 * p.HK * kD * 2;
+    const char *k = static_cast<const char *>(p.k) + tok0 * p.HK * kD * 2;
+    const char *v = static_cast<const char *>(p.v) + tok0 * p.HV * kD * 2;
+    const char *g = reinterpret_cast<const char *>(p.g) + tok0 * p.HV * kD * 4;
+    const char *o = static_cast<const char *>(p.out) + tok0 * p.HV * kD * 2;
+    return encode_map(fn, &tm->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
+           encode_map(fn, &tm->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
+           encode_map(fn, &tm->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, p.HV, 32) &&
+           encode_map(fn, &tm->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 64) &&
+           // output: unswizzled [16 tokens][32 channels] boxes, one per state warp
+           encode_map(fn, &tm->o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, 16);
+}
+
+template <bool VARLEN>
+cudaError_t launch_tc(const Problem &p, const TileMaps &tm, const TileMaps *seq_maps,
+                      const int4 *seqs, long long blocks, int *dev_error, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaSuccess;
-    EncodeTiledFn fn = encode_fn(&e);
-    if (e != cudaSuccess) return e;
-    TileMaps tm;
-    if (!encode_map(fn, &tm.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
-        !encode_map(fn, &tm.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HK, 64) ||
-        !encode_map(fn, &tm.g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.HV, 32) ||
-        !encode_map(fn, &tm.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 64) ||
-        // output: unswizzled [16 tokens][32 channels] boxes, one per state warp
-        !encode_map(fn, &tm.o, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.HV, 32,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, 16))
-        return cudaErrorInvalidValue;
     auto run = [&](auto kernel) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
-        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, p.beta, p.h0, p.ht, p.T,
-                                                                  p.HK, p.HV, dev_error);
+        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, seq_maps, seqs, p.beta, p.h0,
+                                                                  p.ht, p.T, p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };
-    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true>);
-    if (p.h0) return run(gdr_prefill_tc_kernel<true, false>);
-    if (p.ht) return run(gdr_prefill_tc_kernel<false, true>);
-    return run(gdr_prefill_tc_kernel<false, false>);
+    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN>);
+    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN>);
+    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN>);
+    return run(gdr_prefill_tc_kernel<false, false, VARLEN>);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    EncodeTiledFn fn = encode_fn(&e);
+    if (e != cudaSuccess) return e;
+    TileMaps tm;
+    if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
+    return launch_tc<false>(p, tm, nullptr, nullptr, (long long)p.B * p.HV, dev_error, stream);
+}
+
+size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
+
+cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst) {
+    cudaError_t e = cudaSuccess;
+    EncodeTiledFn fn = encode_fn(&e);
+    if (e != cudaSuccess) return e;
+    TileMaps tm;
+    if (!encode_maps(fn, &tm, p, tok0, 1, L)) return cudaErrorInvalidValue;
+    memcpy(dst, &tm, sizeof(TileMaps));
+    return cudaSuccess;
+}
+
+cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, const int4 *seqs,
+                                     int nseq, int *dev_error, cudaStream_t stream) {
+    TileMaps unused;
+    memset(&unused, 0, sizeof(unused));
+    return launch_tc<true>(p, unused, static_cast<const TileMaps *>(seq_maps), seqs,
+                           (long long)nseq * p.HV, dev_error, stream);
 }
 
 }  // namespace gdr

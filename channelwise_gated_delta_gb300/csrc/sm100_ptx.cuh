@@ -282,6 +282,14 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Acquire side of the tensor-map proxy fence: a tensor map that sits in
+// global memory (written by a copy before the launch) is read by TMA only
+// after this, in the thread that issues the copies.
+__device__ __forceinline__ void fence_tensormap_acquire(const void *tmap) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap))
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

@@ -97,6 +97,21 @@ def draw_workload(w: Workload, seed=0, device="cpu"):
     return [draw(1, L, w.HK, w.HV, w.dk, w.dv, generator=gen, **kw) for L in w.lengths]
 
 
+def pack(seqs):
+    """Packs per-sequence problems (B=1 each, as draw_workload returns for a
+    ragged workload) back to back: q/k/v/g/beta gain a leading dim of 1 over
+    all tokens, h0 stacks to [N, HV, dk, dv] (None if the sequences have
+    none).  Returns (packed dict, cu_seqlens list of N + 1 ints)."""
+    cu = [0]
+    for d in seqs:
+        cu.append(cu[-1] + d["q"].shape[1])
+    packed = {n: torch.cat([d[n] for d in seqs], dim=1).contiguous()
+              for n in ("q", "k", "v", "g", "beta")}
+    packed["h0"] = (None if seqs[0]["h0"] is None
+                    else torch.cat([d["h0"] for d in seqs], dim=0).contiguous())
+    return packed, cu
+
+
 def to_f64(x):
     """Exact float64 numpy copy of a tensor (bf16 and f32 values are exact in f64)."""
     if x is None:

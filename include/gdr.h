@@ -152,6 +152,47 @@ GDR_API gdr_status gdr_forward_chunked_noalloc(const void *q, const void *k, con
                                                void *stream, int qkv_dtype);
 
 /*
+ * Packed variable-length batches.  The same page's second commit summary
+ * treats every sequence of a batch independently, routes a sequence of one
+ * token to the single-token recurrence and runs a ragged last chunk through
+ * the chunkwise path; this entry runs N such sequences of different lengths
+ * stored back to back, with one launch per route for the whole batch.
+ *
+ *   cu_seqlens  HOST int32 [N + 1]: cu_seqlens[0] == 0, non-decreasing;
+ *               sequence n is token rows cu_seqlens[n] .. cu_seqlens[n+1]-1.
+ *               Read during the call only.
+ *   q, k        [total][HK][dk]   (total = cu_seqlens[N]), dtype qkv_dtype
+ *   v, out      [total][HV][dv]   dtype qkv_dtype
+ *   g           [total][HV][dk]   float32
+ *   beta        [total][HV]       float32
+ *   h0, ht      [N][HV][dk][dv]   float32, slot n = sequence n; NULL as in
+ *               gdr_forward (ht == h0 updates in place)
+ *
+ * Sequence n starts from h0[n] (zeros if NULL) and leaves its final state in
+ * ht[n]; a zero-length sequence copies h0[n] (or zeros) to ht[n].  Each
+ * sequence takes the route gdr_forward_ex would give it as a B = 1 call
+ * with the same flags: length 1 the single-token kernel, longer ones the
+ * tensor-core prefill (bf16, dk = dv = 128, chunk 64) or else the CUDA-core
+ * chunked prefill; the outputs equal those of N such calls bit for bit.
+ * Enqueued on `stream`: one host-to-device copy of the batch's tables (from
+ * pageable host memory: the call returns once the bytes have been taken, so
+ * it cannot be captured in a CUDA graph), one copy or memset per zero-length
+ * sequence, then at most four kernel launches.
+ *
+ * `workspace`: device memory of at least gdr_varlen_workspace_bytes(...)
+ * bytes, 256-byte aligned, untouched by anything else until the stream has
+ * passed this call.  Allocates nothing.  Errors: GDR_ERR_SHAPE for a
+ * cu_seqlens that breaks the rules above; the rest as gdr_forward_ex.
+ */
+GDR_API size_t gdr_varlen_workspace_bytes(const int *cu_seqlens, int N, int HK, int HV, int dk,
+                                          int dv, int chunk, int qkv_dtype, unsigned flags);
+GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, const float *h0, void *out, float *ht,
+                                      const int *cu_seqlens, int N, int HK, int HV, int dk, int dv,
+                                      int chunk, void *stream, int qkv_dtype, void *workspace,
+                                      size_t workspace_bytes, unsigned flags);
+
+/*
  * Waits for `stream`, then reads and clears the library's device error word
  * on the current device.  Returns GDR_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, GDR_ERR_CUDA if the stream reported an

@@ -101,3 +101,56 @@ def test_binding_fails_loudly_without_library(tmp_path):
     from channelwise_gated_delta_gb300 import _binding
     with pytest.raises(RuntimeError, match="not built"):
         _binding.load_library(str(tmp_path / "missing.so"))
+
+
+def cu_array(vals):
+    return (ctypes.c_int * len(vals))(*vals)
+
+
+def call_varlen(lib, cu, N=None, HK=1, HV=2, dk=32, dv=32, chunk=16, dtype=0, ptrs=None, ws=None,
+                ws_bytes=0, flags=0):
+    step = 1 << 30
+    p = dict(q=FAKE, k=FAKE + step, v=FAKE + 2 * step, g=FAKE + 3 * step, beta=FAKE + 4 * step,
+             h0=FAKE + 5 * step, out=FAKE + 6 * step, ht=FAKE + 7 * step)
+    if ptrs:
+        p.update(ptrs)
+    args = [ctypes.c_void_p(p[n]) if p[n] is not None else None
+            for n in ("q", "k", "v", "g", "beta", "h0", "out", "ht")]
+    n = len(cu) - 1 if N is None else N
+    arr = None if cu is None else cu_array(cu)
+    return lib.gdr_forward_varlen(*args, arr, n, HK, HV, dk, dv, chunk, None, dtype,
+                                  None if ws is None else ctypes.c_void_p(ws), ws_bytes, flags)
+
+
+@pytest.mark.parametrize("cu,kw,status", [
+    ([1, 4, 8], {}, 2),             # cu_seqlens[0] != 0
+    ([0, 5, 4], {}, 2),             # decreasing offsets
+    ([0, 4], dict(N=-1), 2),        # negative count
+    (None, dict(N=2), 1),           # no offsets
+    ([0, 4, 8], dict(HK=2, HV=3), 2),
+    ([0, 4, 8], dict(dk=48), 3),
+    ([0, 4, 8], dict(ptrs=dict(q=None)), 1),
+    ([0, 4, 8], dict(ptrs=dict(out=FAKE + 16)), 8),     # out overlaps q
+    ([0, 4, 8], dict(ptrs=dict(ht=FAKE + (5 << 30) + 16)), 8),
+    ([0, 4, 8], {}, 5),             # needs a workspace, none given
+])
+def test_varlen_bad_arguments_rejected_before_launch(lib, cu, kw, status):
+    assert call_varlen(lib, cu, **kw) == status
+
+
+def test_varlen_workspace_sizes(lib):
+    ws = lambda cu, **kw: lib.gdr_varlen_workspace_bytes(
+        cu_array(cu), len(cu) - 1, kw.get("HK", 1), kw.get("HV", 2), kw.get("dk", 32),
+        kw.get("dv", 32), kw.get("chunk", 16), kw.get("dtype", 0), kw.get("flags", 0))
+    assert ws([0]) == 0                     # no sequences
+    assert ws([0, 0, 0]) == 0               # only empty ones: nothing to stage
+    one = ws([0, 1])                        # one single-token sequence: its table row
+    assert 0 < one <= 512
+    small = ws([0, 40])
+    more = ws([0, 40, 80])                  # twice the chunk records
+    assert small > one and more > small
+    assert ws([0, 40, 80], HK=2, HV=3) == 0  # invalid shape
+    assert ws([1, 40]) == 0                  # invalid offsets
+    # a workspace one byte short, or misaligned, is rejected
+    assert call_varlen(lib, [0, 40], ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5
+    assert call_varlen(lib, [0, 40], ws=FAKE + (9 << 30) + 16, ws_bytes=small) == 4
