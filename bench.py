@@ -43,9 +43,9 @@ DECODE = "decode_b64"
 # whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
     # decode B64: one launch, --set full capture (136.3 MB read + 73.9 MB written)
-    "gdr_decode_kernel": {"bytes": 210_200_000, "sha": "1b350c7a4ac6f3e0"},
+    "gdr_decode_kernel": {"bytes": 210_200_000, "sha": "cf654d30f50c579a"},
     # prefill_t16k: one launch, --set full capture (2.165 GB read + 0.521 GB written)
-    "gdr_prefill_fused": {"bytes": 2_686_400_000, "sha": "24de0c0ac4504926"},
+    "gdr_prefill_fused": {"bytes": 2_686_400_000, "sha": "9d539aeeff021d9c"},
 }
 
 
