@@ -112,6 +112,34 @@ def pack(seqs):
     return packed, cu
 
 
+def draw_parents(B, T, kind="random", seed=0, branching=3):
+    """Parent arrays [B, T] (int32, parent[b, t] in [-1, t-1], -1 = a root) of
+    draft-token trees, parents before children:
+      "chain"   parent t-1 (a plain sequence);
+      "star"    every token a root (T independent single-token steps);
+      "random"  each token's parent uniform over the earlier tokens, or a
+                root with probability 1/(t+1);
+      "beam"    breadth-first tree, each node with up to `branching` children
+                (the usual shape of a speculative-decoding draft tree)."""
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    par = torch.empty(B, T, dtype=torch.int32)
+    for b in range(B):
+        for t in range(T):
+            if kind == "chain":
+                p = t - 1
+            elif kind == "star":
+                p = -1
+            elif kind == "beam":
+                p = (t - 1) // branching if t > 0 else -1
+            elif kind == "random":
+                p = int(torch.randint(-1, t, (1,), generator=gen)) if t > 0 else -1
+            else:
+                raise ValueError(kind)
+            par[b, t] = p
+    return par
+
+
 def to_f64(x):
     """Exact float64 numpy copy of a tensor (bf16 and f32 values are exact in f64)."""
     if x is None:

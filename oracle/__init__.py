@@ -21,6 +21,16 @@ Two routines, both in float64:
     recurrence over a chunk; it exists to pin the recurrence (the two must
     agree to rounding for every chunk size) and is never the parity target.
 
+``tree_recurrence`` / ``tree_wy``
+    Tree verification, the workload of the page "Support TreeUpdateSolve
+    kernel" (trymirai/uzu PR #576): the tokens form a tree of draft tokens
+    (parents before children) and the tree's ancestor relation takes the
+    place of the causal order.  ``tree_recurrence`` is the definition: each
+    token's output is the last output of the token recurrence run along its
+    root path.  ``tree_wy`` is the same WY/UT algebra as ``chunked_wy`` with
+    the ancestor mask and path prefix sums, over the whole tree at once; it
+    exists to pin the form the GPU computes.
+
 Array layouts (numpy, C-contiguous):
     q, k [B, T, HK, dk]; v [B, T, HV, dv]; g [B, T, HV, dk]; beta [B, T, HV];
     h0 [B, HV, dk, dv] or None.  Returns (o [B, T, HV, dv], ht [B, HV, dk, dv]).
@@ -162,3 +172,104 @@ def chunked_wy(q, k, v, g, beta, h0=None, chunk=64):
                 S = np.exp(G[-1])[:, None] * S + Kh.T @ U
             ht[b, hv] = S
     return out, ht
+
+
+def _check_parent(parent, B, T):
+    parent = np.asarray(parent, dtype=np.int64).reshape(B, T)
+    for b in range(B):
+        for t in range(T):
+            assert -1 <= parent[b, t] < t, "parents must precede their children"
+    return parent
+
+
+def _path(parent_b, t):
+    """Root-to-t token indices (ancestors first, t last)."""
+    path = []
+    while t >= 0:
+        path.append(t)
+        t = parent_b[t]
+    return path[::-1]
+
+
+def tree_recurrence(q, k, v, g, beta, h0, parent, threads=None):
+    """Tree verification by definition: o[b, t] is the output of the last
+    token when the token recurrence runs over the root path of t (its
+    ancestors from the root down, then t), starting from h0[b] (zeros if
+    None).  parent [B, T] ints, parent[b, t] in [-1, t-1], -1 for a token
+    whose parent is the state h0.  Returns o [B, T, HV, dv].
+
+    All paths of a tree run as one batch of `recurrence`: a path shorter than
+    the deepest is padded at its front with tokens of zero decay (g = 0) and
+    beta = 0, which leave the state unchanged exactly (multiplied by
+    exp(0) = 1 and added beta * ... = 0), and their outputs are discarded."""
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    parent = _check_parent(parent, B, T)
+    out = np.zeros((B, T, HV, dv))
+    for b in range(B):
+        if T == 0:
+            continue
+        paths = [_path(parent[b], t) for t in range(T)]
+        depth = max(len(p) for p in paths)
+        qp = np.zeros((T, depth, HK, dk))
+        kp = np.zeros((T, depth, HK, dk))
+        vp = np.zeros((T, depth, HV, dv))
+        gp = np.zeros((T, depth, HV, dk))
+        bp = np.zeros((T, depth, HV))
+        for t, p in enumerate(paths):
+            off = depth - len(p)
+            qp[t, off:] = q[b, p]
+            kp[t, off:] = k[b, p]
+            vp[t, off:] = v[b, p]
+            gp[t, off:] = g[b, p]
+            bp[t, off:] = beta[b, p]
+        hp = None if h0 is None else np.repeat(_f64(h0)[b:b + 1], T, axis=0)
+        o, _ = recurrence(qp, kp, vp, gp, bp, hp, threads=threads)
+        out[b] = o[:, -1]
+    return out
+
+
+def tree_wy(q, k, v, g, beta, h0, parent):
+    """The WY/UT form of tree verification, one solve over the whole tree.
+
+    Per (b, hv), with anc(r) the strict ancestors of token r:
+      G_r     = sum of g over the root path of r (inclusive), per channel
+      A[r,s]  = beta_r * sum_i k_ri k_si exp(G_ri - G_si)      (s in anc(r))
+      P[r,s]  = sum_i q_ri k_si exp(G_ri - G_si)                (s in anc(r) or s = r)
+      Kt = exp(G) * k,  Qt = exp(G) * q
+      (I + A) U = diag(beta) (V - Kt S0)     (unit lower triangular: parents first)
+      O = Qt S0 + P U
+    Returns o [B, T, HV, dv]."""
+    from scipy.linalg import solve_triangular
+
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    group = HV // HK
+    parent = _check_parent(parent, B, T)
+    out = np.zeros((B, T, HV, dv))
+    for b in range(B):
+        anc = np.zeros((T, T))
+        for r in range(T):
+            for s in _path(parent[b], r)[:-1]:
+                anc[r, s] = 1.0
+        path_or_self = anc + np.eye(T)
+        for hv in range(HV):
+            hk = hv // group
+            S = np.zeros((dk, dv)) if h0 is None else _f64(h0)[b, hv]
+            K, Q, V = k[b, :, hk], q[b, :, hk], v[b, :, hv]
+            bet = beta[b, :, hv]
+            G = np.zeros((T, dk))
+            for r in range(T):
+                G[r] = g[b, r, hv] + (G[parent[b, r]] if parent[b, r] >= 0 else 0.0)
+            D = np.where(path_or_self[:, :, None] > 0, G[:, None, :] - G[None, :, :], -np.inf)
+            E = np.exp(D)
+            A = bet[:, None] * np.einsum("ri,si,rsi->rs", K, K, E) * anc
+            P = np.einsum("ri,si,rsi->rs", Q, K, E) * path_or_self
+            Kt = np.exp(G) * K
+            Qt = np.exp(G) * Q
+            rhs = bet[:, None] * (V - Kt @ S)
+            U = solve_triangular(np.eye(T) + A, rhs, lower=True, unit_diagonal=True)
+            out[b, :, hv] = Qt @ S + P @ U
+    return out
