@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
                 7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_ALIAS"}
 
 EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_forward_chunked_noalloc",
-            "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_device_check",
+            "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_tree_workspace_bytes",
+            "gdr_forward_tree", "gdr_device_check",
             "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma", "gdr_status_string",
             "gdr_last_cuda_error", "gdr_version")
 
@@ -63,6 +64,10 @@ def load_library(path=LIB_PATH):
     lib.gdr_varlen_workspace_bytes.restype = sz
     lib.gdr_forward_varlen.argtypes = [vp] * 8 + [ip] + [i] * 6 + [vp, i, vp, sz, u]
     lib.gdr_forward_varlen.restype = i
+    lib.gdr_tree_workspace_bytes.argtypes = [i] * 7
+    lib.gdr_tree_workspace_bytes.restype = sz
+    lib.gdr_forward_tree.argtypes = [vp] * 7 + [ip] + [i] * 6 + [vp, i, vp, sz]
+    lib.gdr_forward_tree.restype = i
     lib.gdr_device_check.argtypes = [vp]
     lib.gdr_device_check.restype = i
     lib.gdr_status_string.argtypes = [i]
@@ -233,6 +238,58 @@ def gdr_forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, out=None, ht=None,
                                 ctypes.c_void_p(stream.cuda_stream), code, ws_ptr, ws_bytes, flags)
     _check(lib, st)
     return (out.unsqueeze(0) if lead else out), ht
+
+
+def gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, dtype=torch.bfloat16):
+    lib = load_library()
+    return int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, _dtype_code(dtype)))
+
+
+def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, workspace=None):
+    """Tree verification: each batch element's T <= 64 tokens form a draft
+    tree given by ``parent`` (host ints [B, T], parent[b, t] in [-1, t-1]);
+    every token's output is that of the recurrence run along its root path
+    from h0[b].  Tensors as in gdr_forward.  Returns out [B, T, HV, dv]."""
+    lib = load_library()
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("out", out)):
+        if t is None:
+            continue
+        if t.device != dev or dev.type != "cuda":
+            raise ValueError("%s must be a CUDA tensor on %s" % (name, dev))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k must match q in shape and dtype; v must match q in dtype")
+    if tuple(v.shape[:2]) != (B, T) or tuple(g.shape) != (B, T, HV, dk) or \
+            tuple(beta.shape) != (B, T, HV):
+        raise ValueError("inconsistent shapes")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if h0 is not None and (tuple(h0.shape) != (B, HV, dk, dv) or h0.dtype != torch.float32):
+        raise ValueError("h0 must be float32 [B, HV, dk, dv]")
+    par = torch.as_tensor(parent, dtype=torch.int32, device="cpu").contiguous()
+    if tuple(par.shape) != (B, T):
+        raise ValueError("parent must be [B, T]")
+    par_c = par.numpy().ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+    if out is None:
+        out = torch.empty(B, T, HV, dv, dtype=q.dtype, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    need = int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, code))
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
+    st = lib.gdr_forward_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(out),
+                              par_c, B, T, HK, HV, dk, dv, ctypes.c_void_p(stream.cuda_stream), code,
+                              ws_ptr, ws_bytes)
+    _check(lib, st)
+    return out
 
 
 def gdr_device_check(stream=None):

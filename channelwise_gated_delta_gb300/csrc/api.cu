@@ -311,6 +311,18 @@ void trace_end(int kernel, cudaStream_t stream) {
 }
 }  // namespace gdr
 
+namespace {
+// Trees run as one chunk of the CUDA-core kernels: the smallest supported
+// chunk that holds T tokens (0 when T is too large).
+int tree_chunk(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 0; }
+
+size_t tree_layout(const gdr::Problem &p, size_t *record_off) {
+    const size_t table = align256((size_t)p.B * p.T * sizeof(int));
+    *record_off = table;
+    return table + gdr::generic_tree_record_bytes(p);
+}
+}  // namespace
+
 extern "C" {
 
 GDR_API gdr_status gdr_trace_enable(int on) {
@@ -510,6 +522,50 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return GDR_OK;
+}
+
+GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
+                                        int qkv_dtype) {
+    if (B < 0 || T < 0 || HK <= 0 || HV <= 0 || HV % HK != 0) return 0;
+    if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
+    if (!supported_dim(dk) || !supported_dim(dv) || !tree_chunk(T)) return 0;
+    if ((long long)B * T == 0) return 0;
+    const gdr::Problem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         B, T, HK, HV, dk, dv, tree_chunk(T), qkv_dtype == GDR_BF16 ? 1 : 0};
+    size_t off = 0;
+    return tree_layout(p, &off);
+}
+
+GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *h0, void *out,
+                                    const int *parent, int B, int T, int HK, int HV, int dk,
+                                    int dv, void *stream, int qkv_dtype, void *workspace,
+                                    size_t workspace_bytes) {
+    if (B < 0 || T < 0) return GDR_ERR_SHAPE;
+    if (T > 64) return GDR_ERR_UNSUPPORTED;
+    const int chunk = tree_chunk(T > 0 ? T : 1);
+    gdr::Problem p;
+    gdr_status st = validate(q, k, v, g, beta, h0, out, nullptr, B, T, HK, HV, dk, dv, chunk,
+                             qkv_dtype, &p);
+    if (st != GDR_OK) return st;
+    if ((long long)B * T == 0) return GDR_OK;
+    if (!parent) return GDR_ERR_NULL;
+    for (long long bt = 0; bt < (long long)B * T; ++bt) {
+        const int t = (int)(bt % T);
+        if (parent[bt] < -1 || parent[bt] >= t) return GDR_ERR_SHAPE;
+    }
+    size_t record_off = 0;
+    const size_t need = tree_layout(p, &record_off);
+    if (!workspace || workspace_bytes < need) return GDR_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    // the parents, from pageable host memory: taken before the call returns
+    cudaError_t e = cudaMemcpyAsync(ws, parent, (size_t)B * T * sizeof(int),
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = gdr::launch_generic_tree(p, ws + record_off, reinterpret_cast<const int *>(ws), s);
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e);
 }
 
 GDR_API gdr_status gdr_device_check(void *stream) {

@@ -103,4 +103,9 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
 size_t generic_varlen_record_bytes(const Problem &p, long long nchunks);
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
                                           int nchunks, const int4 *seqs, cudaStream_t stream);
+// Tree verification on CUDA cores: p.B trees of p.T <= p.chunk tokens each,
+// parents [B][T] (device); records: generic_tree_record_bytes(p).
+size_t generic_tree_record_bytes(const Problem &p);
+cudaError_t launch_generic_tree(const Problem &p, void *records, const int *parents,
+                                cudaStream_t stream);
 }  // namespace gdr

@@ -54,13 +54,18 @@ struct ChunkLayout {
     }
 };
 
-template <typename Tin>
+// TREE: the T <= C tokens of each (b, hv) are a draft-token tree given by
+// parents[b][t] (-1 for a root, else an earlier token), solved as one chunk:
+// prefix sums run along root paths and the ancestor relation replaces the
+// causal order in A and P (page "Support TreeUpdateSolve kernel",
+// trymirai/uzu PR #576).  No state carry is prepared.
+template <typename Tin, bool TREE>
 __global__ void __launch_bounds__(kPrepThreads)
     gdr_chunk_prep(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ g,
                    const float *__restrict__ beta, float *__restrict__ ws,
-                   const int2 *__restrict__ chunks, int T, int HK, int HV, int dk, int dv, int C,
-                   int NC) {
+                   const int2 *__restrict__ chunks, const int *__restrict__ parents, int T,
+                   int HK, int HV, int dk, int dv, int C, int NC) {
     extern __shared__ float smem[];
     const int ldk = dk + 1;  // padded rows: threads walking s hit distinct banks
     const int ldw = dk + dv;
@@ -70,6 +75,9 @@ __global__ void __launch_bounds__(kPrepThreads)
     float *As = Gs + C * ldk;       // [C][C]
     float *Ws = As + C * C;         // [C][dk + dv]
     float *bs = Ws + C * ldw;       // [C]
+    int *par = reinterpret_cast<int *>(bs + C);                          // [C] (TREE)
+    unsigned long long *anc = reinterpret_cast<unsigned long long *>(
+        reinterpret_cast<uintptr_t>(par + C + 1) & ~(uintptr_t)7);     // [C] (TREE)
 
     // The chunk: its first token row in the [rows][H][d] view of the inputs,
     // its length, and its record.  Dense batches: CTA (b, hv, c), record
@@ -114,14 +122,35 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     for (int r = tid; r < C; r += kPrepThreads)
         bs[r] = r < L ? beta[(tr0 + r) * HV + hv] : 0.f;
+    if (TREE) {
+        const int b = blockIdx.x / NC / HV;
+        for (int r = tid; r < C; r += kPrepThreads) par[r] = r < L ? parents[(size_t)b * T + r] : -1;
+    }
     __syncthreads();
 
-    // Per-channel inclusive prefix sum of the log-decay.
-    for (int i = tid; i < dk; i += kPrepThreads) {
-        float run = 0.f;
-        for (int r = 0; r < C; ++r) {
-            run += Gs[r * ldk + i];
-            Gs[r * ldk + i] = run;
+    if (TREE) {
+        // Ancestor sets as bit masks (parents precede their children), and
+        // the prefix sums of the log-decay along each token's root path.
+        if (tid == 0) {
+            for (int r = 0; r < C; ++r) {
+                const int p = par[r];
+                anc[r] = p < 0 ? 0ull : (anc[p] | (1ull << p));
+            }
+        }
+        for (int i = tid; i < dk; i += kPrepThreads) {
+            for (int r = 0; r < C; ++r) {
+                const int p = par[r];
+                Gs[r * ldk + i] += p < 0 ? 0.f : Gs[p * ldk + i];
+            }
+        }
+    } else {
+        // Per-channel inclusive prefix sum of the log-decay.
+        for (int i = tid; i < dk; i += kPrepThreads) {
+            float run = 0.f;
+            for (int r = 0; r < C; ++r) {
+                run += Gs[r * ldk + i];
+                Gs[r * ldk + i] = run;
+            }
         }
     }
     __syncthreads();
@@ -130,8 +159,11 @@ __global__ void __launch_bounds__(kPrepThreads)
     float *Pg = rec + lay.p();
     for (int idx = tid; idx < C * C; idx += kPrepThreads) {
         const int r = idx / C, s = idx % C;
+        // s is an earlier token r depends on: s <= r, or in a tree s == r or
+        // an ancestor of r
+        const bool below = TREE ? (s < r && ((anc[r] >> s) & 1ull)) : s < r;
         float a = 0.f, pp = 0.f;
-        if (s <= r && r < L) {
+        if ((below || s == r) && r < L) {
             const float *kr = Ks + r * ldk, *ks = Ks + s * ldk, *qr = Qs + r * ldk;
             const float *gr = Gs + r * ldk, *gs = Gs + s * ldk;
             for (int i = 0; i < dk; ++i) {
@@ -141,7 +173,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                 pp = fmaf(qr[i], kse, pp);
             }
         }
-        As[r * C + s] = (s < r) ? bs[r] * a : 0.f;
+        As[r * C + s] = below ? bs[r] * a : 0.f;
         Pg[idx] = pp;
     }
     // Right-hand sides of the WY solve: diag(beta) [exp(G) * K | V].
@@ -172,23 +204,26 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     __syncthreads();
 
-    // Scan operands: Wk, Wv, Qt = exp(G) Q, Kh = exp(G_L - G) K, gam = exp(G_L).
+    // Scan operands: Wk, Wv, Qt = exp(G) Q, Kh = exp(G_L - G) K, gam = exp(G_L)
+    // (a tree has no last token to carry the state to: no Kh, gam).
     const float *gl = Gs + (L - 1) * ldk;
     for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
         const int r = idx / dk, i = idx % dk;
         const float gri = Gs[r * ldk + i];
         rec[lay.wk() + idx] = Ws[r * ldw + i];
         rec[lay.qt() + idx] = Qs[r * ldk + i] * expf(gri);
-        rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(gl[i] - gri) : 0.f;
+        if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(gl[i] - gri) : 0.f;
     }
     for (int idx = tid; idx < C * dv; idx += kPrepThreads) {
         const int r = idx / dv, j = idx % dv;
         rec[lay.wv() + idx] = Ws[r * ldw + dk + j];
     }
-    for (int i = tid; i < dk; i += kPrepThreads) rec[lay.gam() + i] = expf(gl[i]);
+    if (!TREE)
+        for (int i = tid; i < dk; i += kPrepThreads) rec[lay.gam() + i] = expf(gl[i]);
 }
 
-template <typename Tin>
+// TREE: one chunk (the tree), outputs only: no state update, no ht.
+template <typename Tin, bool TREE>
 __global__ void __launch_bounds__(kScanThreads)
     gdr_chunk_scan(const float *__restrict__ ws, const float *h0, Tin *__restrict__ out,
                    float *ht, const int4 *__restrict__ seqs, int T_dense, int HV, int dk, int dv,
@@ -244,7 +279,7 @@ __global__ void __launch_bounds__(kScanThreads)
             const int r = idx / dk, i = idx % dk;
             Wk[r * ldk + i] = rec[lay.wk() + idx];
             Qt[r * ldk + i] = rec[lay.qt() + idx];
-            Kh[r * ldk + i] = rec[lay.kh() + idx];
+            if (!TREE) Kh[r * ldk + i] = rec[lay.kh() + idx];
         }
         for (int idx = tid; idx < C * C; idx += kScanThreads)
             Ps[(idx / C) * ldc + idx % C] = rec[lay.p() + idx];
@@ -252,7 +287,8 @@ __global__ void __launch_bounds__(kScanThreads)
             const int r = idx / kScanBV, j = idx % kScanBV;
             Wv[idx] = rec[lay.wv() + (size_t)r * dv + j0 + j];
         }
-        for (int i = tid; i < dk; i += kScanThreads) gam[i] = rec[lay.gam() + i];
+        if (!TREE)
+            for (int i = tid; i < dk; i += kScanThreads) gam[i] = rec[lay.gam() + i];
         __syncthreads();
 
         // U = Wv - Wk S0
@@ -274,6 +310,7 @@ __global__ void __launch_bounds__(kScanThreads)
             out[((tok0 + t0 + r) * HV + hv) * dv + j0 + jj] = from_f32<Tin>(acc);
         }
 
+        if (TREE) break;  // one chunk; no state to carry
         // S = diag(gam) S0 + Kh^T U   (new values kept in registers until
         // every thread is done reading S0)
         float snew[128 / (kScanThreads / kScanBV)];
@@ -289,7 +326,7 @@ __global__ void __launch_bounds__(kScanThreads)
         __syncthreads();
     }
 
-    if (ht) {
+    if (!TREE && ht) {
         for (int idx = tid; idx < dk * kScanBV; idx += kScanThreads) {
             const int i = idx / kScanBV, j = idx % kScanBV;
             ht[(head_idx * dk + i) * dv + j0 + j] = Ss[idx];
@@ -298,7 +335,9 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 size_t prep_smem_bytes(int dk, int dv, int C) {
-    return sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * C + (size_t)C * (dk + dv) + C);
+    // floats, then (trees) C parent indices and C 8-byte ancestor masks
+    return sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * C + (size_t)C * (dk + dv) + C) +
+           sizeof(int) * (C + 2) + sizeof(unsigned long long) * C;
 }
 size_t scan_smem_bytes(int dk, int C) {
     return sizeof(float) * ((size_t)dk * kScanBV + (size_t)3 * C * (dk + 1) + (size_t)C * (C + 1) +
@@ -306,10 +345,11 @@ size_t scan_smem_bytes(int dk, int C) {
 }
 
 // Dense batches: chunks == seqs == nullptr, B x T from p.  Packed batches:
-// nchunks chunk records and p.B sequence records.
-template <typename Tin>
+// nchunks chunk records and p.B sequence records.  Trees (TREE): p.T <=
+// p.chunk tokens per batch element, parents [B][T] on the device.
+template <typename Tin, bool TREE>
 cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chunks, int nchunks,
-                             const int4 *seqs, cudaStream_t stream) {
+                             const int4 *seqs, const int *parents, cudaStream_t stream) {
     const int C = p.chunk;
     const int NC = (p.T + C - 1) / C;
     float *ws = static_cast<float *>(workspace);
@@ -319,19 +359,22 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chun
     const size_t sp = prep_smem_bytes(p.dk, p.dv, C);
     const size_t ss = scan_smem_bytes(p.dk, C);
     cudaError_t e;
-    e = cudaFuncSetAttribute(gdr_chunk_prep<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    e = cudaFuncSetAttribute(gdr_chunk_prep<Tin, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sp);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gdr_chunk_scan<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    e = cudaFuncSetAttribute(gdr_chunk_scan<Tin, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ss);
     if (e != cudaSuccess) return e;
     trace_begin(kKernChunkPrep, stream);
-    gdr_chunk_prep<Tin><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
+    gdr_chunk_prep<Tin, TREE><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
         static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
-        static_cast<const Tin *>(p.v), p.g, p.beta, ws, chunks, p.T, p.HK, p.HV, p.dk, p.dv, C, NC);
+        static_cast<const Tin *>(p.v), p.g, p.beta, ws, chunks, parents, p.T, p.HK, p.HV, p.dk,
+        p.dv, C, NC);
     trace_end(kKernChunkPrep, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     trace_begin(kKernChunkScan, stream);
-    gdr_chunk_scan<Tin><<<(unsigned)scan_blocks, kScanThreads, ss, stream>>>(
+    gdr_chunk_scan<Tin, TREE><<<(unsigned)scan_blocks, kScanThreads, ss, stream>>>(
         ws, p.h0, static_cast<Tin *>(p.out), p.ht, seqs, p.T, p.HV, p.dk, p.dv, C, NC);
     trace_end(kKernChunkScan, stream);
     return cudaGetLastError();
@@ -346,8 +389,10 @@ size_t generic_prefill_workspace_bytes(const Problem &p) {
 }
 
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream) {
-    return p.bf16 ? launch_generic_t<__nv_bfloat16>(p, workspace, nullptr, 0, nullptr, stream)
-                  : launch_generic_t<float>(p, workspace, nullptr, 0, nullptr, stream);
+    return p.bf16 ? launch_generic_t<__nv_bfloat16, false>(p, workspace, nullptr, 0, nullptr,
+                                                           nullptr, stream)
+                  : launch_generic_t<float, false>(p, workspace, nullptr, 0, nullptr, nullptr,
+                                                   stream);
 }
 
 size_t generic_varlen_record_bytes(const Problem &p, long long nchunks) {
@@ -357,8 +402,23 @@ size_t generic_varlen_record_bytes(const Problem &p, long long nchunks) {
 
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
                                           int nchunks, const int4 *seqs, cudaStream_t stream) {
-    return p.bf16 ? launch_generic_t<__nv_bfloat16>(p, records, chunks, nchunks, seqs, stream)
-                  : launch_generic_t<float>(p, records, chunks, nchunks, seqs, stream);
+    return p.bf16 ? launch_generic_t<__nv_bfloat16, false>(p, records, chunks, nchunks, seqs,
+                                                           nullptr, stream)
+                  : launch_generic_t<float, false>(p, records, chunks, nchunks, seqs, nullptr,
+                                                   stream);
+}
+
+size_t generic_tree_record_bytes(const Problem &p) {
+    const ChunkLayout lay{p.chunk, p.dk, p.dv};
+    return sizeof(float) * lay.floats() * (size_t)p.B * p.HV;
+}
+
+cudaError_t launch_generic_tree(const Problem &p, void *records, const int *parents,
+                                cudaStream_t stream) {
+    return p.bf16 ? launch_generic_t<__nv_bfloat16, true>(p, records, nullptr, 0, nullptr,
+                                                          parents, stream)
+                  : launch_generic_t<float, true>(p, records, nullptr, 0, nullptr, parents,
+                                                  stream);
 }
 
 }  // namespace gdr

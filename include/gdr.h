@@ -193,6 +193,38 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
                                       size_t workspace_bytes, unsigned flags);
 
 /*
+ * Tree verification (page "Support TreeUpdateSolve kernel", trymirai/uzu PR
+ * #576): each batch element's T tokens are a tree of draft tokens, and each
+ * token sees the state reached by running the recurrence along its own root
+ * path -- its ancestors from the root down, then itself -- starting from
+ * h0[b] (zeros if NULL).  out[b][t] is that run's output for token t.
+ *
+ *   parent  HOST int32 [B][T]: parent[b][t] in [-1, t-1] (parents precede
+ *           their children; -1: the token follows h0 directly).  Read during
+ *           the call only.
+ *   q, k, v, g, beta, h0, out: layouts as in gdr_forward, T <= 64.
+ *
+ * There is no final-state output: a tree has one state per leaf.  To commit
+ * an accepted path, run gdr_forward (or gdr_forward_varlen) on its tokens
+ * from the same h0.  Runs the CUDA-core chunked kernels with the whole tree
+ * as one chunk (float32 arithmetic, both dtypes): path prefix sums of g and
+ * the ancestor relation in place of the causal order.  `workspace`: device
+ * memory of gdr_tree_workspace_bytes(...) bytes, 256-byte aligned,
+ * untouched until the stream has passed the call.  Enqueues one
+ * host-to-device copy of the parents (pageable: the call returns once they
+ * have been taken) and two kernel launches.  Errors: GDR_ERR_UNSUPPORTED for
+ * T > 64, GDR_ERR_SHAPE for a parent outside [-1, t-1], the rest as
+ * gdr_forward_ex.  B == 0 or T == 0 does nothing.
+ */
+GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
+                                        int qkv_dtype);
+GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *h0, void *out,
+                                    const int *parent, int B, int T, int HK, int HV, int dk,
+                                    int dv, void *stream, int qkv_dtype, void *workspace,
+                                    size_t workspace_bytes);
+
+/*
  * Waits for `stream`, then reads and clears the library's device error word
  * on the current device.  Returns GDR_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, GDR_ERR_CUDA if the stream reported an

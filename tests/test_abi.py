@@ -154,3 +154,31 @@ def test_varlen_workspace_sizes(lib):
     # a workspace one byte short, or misaligned, is rejected
     assert call_varlen(lib, [0, 40], ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5
     assert call_varlen(lib, [0, 40], ws=FAKE + (9 << 30) + 16, ws_bytes=small) == 4
+
+
+def call_tree(lib, parent, B=1, T=4, HK=1, HV=2, dk=32, dv=32, dtype=0, ws=None, ws_bytes=0):
+    step = 1 << 30
+    args = [ctypes.c_void_p(FAKE + n * step) for n in range(7)]
+    arr = None if parent is None else cu_array(parent)
+    return lib.gdr_forward_tree(*args, arr, B, T, HK, HV, dk, dv, None, dtype,
+                                None if ws is None else ctypes.c_void_p(ws), ws_bytes)
+
+
+@pytest.mark.parametrize("parent,kw,status", [
+    ([-1, 0, 0, 1], dict(T=65), 3),         # more than 64 tokens
+    ([-1, 0, 3, 1], {}, 2),                  # parent after its child
+    ([-1, -2, 0, 1], {}, 2),                 # parent below -1
+    (None, {}, 1),                           # no parents
+    ([-1, 0, 0, 1], dict(dk=48), 3),
+    ([-1, 0, 0, 1], {}, 5),                  # needs a workspace
+])
+def test_tree_bad_arguments_rejected_before_launch(lib, parent, kw, status):
+    assert call_tree(lib, parent, **kw) == status
+
+
+def test_tree_workspace_sizes(lib):
+    assert lib.gdr_tree_workspace_bytes(1, 0, 1, 2, 32, 32, 0) == 0
+    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0) == 0
+    small = lib.gdr_tree_workspace_bytes(1, 16, 1, 2, 32, 32, 0)
+    assert 0 < small < lib.gdr_tree_workspace_bytes(1, 17, 1, 2, 32, 32, 0)
+    assert call_tree(lib, [-1, 0, 0, 1], ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5

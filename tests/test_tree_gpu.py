@@ -1,0 +1,89 @@
+"""GPU parity of tree verification (gdr_forward_tree) against the oracle's
+definition: each token's output is the recurrence run along its root path."""
+import pytest
+import torch
+
+import oracle
+from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE_GENERIC,
+                                           GdrError, gdr_device_check, gdr_forward,
+                                           gdr_forward_tree)
+from channelwise_gated_delta_gb300.inputs import draw, draw_parents, to_f64
+from tests.parity_util import assert_close, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def run_tree(d, parent):
+    c = to_cuda(d)
+    out = gdr_forward_tree(c["q"], c["k"], c["v"], c["g"], c["beta"], parent, h0=c["h0"])
+    gdr_device_check()
+    return out
+
+
+def check(d, parent):
+    ref = oracle.tree_recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                 to_f64(d["h0"]), parent.numpy())
+    assert_close("o", run_tree(d, parent), ref, d["q"].dtype)
+
+
+@pytest.mark.parametrize("kind", ["random", "beam", "star", "chain"])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 33, 64])
+def test_tree_shapes(kind, T):
+    d = draw(2, T, 2, 4, 64, 64, dtype=torch.float32, seed=T)
+    check(d, draw_parents(2, T, kind, seed=T))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+def test_tree_dims_and_dtypes(dtype, dk, dv):
+    d = draw(2, 40, 1, 2, dk, dv, dtype=dtype, seed=dk + dv)
+    check(d, draw_parents(2, 40, "random", seed=dk))
+
+
+def test_tree_no_initial_state_grouped_heads():
+    d = draw(3, 24, 2, 6, 64, 64, dtype=torch.float32, h0=False, seed=11)
+    check(d, draw_parents(3, 24, "beam", seed=11, branching=2))
+
+
+def test_tree_verify_shape():
+    """A draft-tree verify step at model shapes: 8 trees of 64 tokens,
+    HK = 16, HV = 32, dk = dv = 128, bf16, with an initial state."""
+    d = draw(8, 64, 16, 32, 128, 128, dtype=torch.bfloat16, seed=12)
+    check(d, draw_parents(8, 64, "beam", seed=12, branching=4))
+
+
+def test_tree_slow_decay_beta_near_one():
+    """The conditioning stress recipe (beta near 1, slow decay) on a deep tree."""
+    d = draw(2, 64, 1, 2, 128, 128, dtype=torch.float32, seed=13, g_mu=-3.0, beta_mu=2.0,
+             beta_sigma=0.5)
+    check(d, draw_parents(2, 64, "random", seed=13))
+
+
+@pytest.mark.parametrize("T,chunk", [(16, 16), (30, 32), (64, 64)])
+def test_chain_tree_equals_chunked_sequence_bitwise(T, chunk):
+    """A chain is a sequence: same kernels, same arithmetic, same bits as the
+    CUDA-core chunked route over one chunk."""
+    d = draw(2, T, 1, 2, 64, 64, dtype=torch.float32, seed=14)
+    c = to_cuda(d)
+    tree = gdr_forward_tree(c["q"], c["k"], c["v"], c["g"], c["beta"],
+                            draw_parents(2, T, "chain"), h0=c["h0"])
+    seq, _ = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=chunk,
+                         flags=GDR_FLAG_FORCE_CHUNKED | GDR_FLAG_FORCE_GENERIC)
+    gdr_device_check()
+    assert torch.equal(tree, seq)
+
+
+def test_bad_trees_rejected():
+    d = to_cuda(draw(1, 4, 1, 1, 32, 32, seed=15))
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"])
+    with pytest.raises(GdrError) as e:
+        gdr_forward_tree(*args, [[-1, 0, 2, 0]], h0=d["h0"])   # parent not before child
+    assert e.value.status == 2
+    with pytest.raises(GdrError) as e:
+        gdr_forward_tree(*args, [[-1, 0, -2, 0]], h0=d["h0"])  # below -1
+    assert e.value.status == 2
+    big = to_cuda(draw(1, 65, 1, 1, 32, 32, seed=16))
+    with pytest.raises(GdrError) as e:
+        gdr_forward_tree(big["q"], big["k"], big["v"], big["g"], big["beta"],
+                         draw_parents(1, 65, "chain"))
+    assert e.value.status == 3
