@@ -64,9 +64,9 @@ def load_library(path=LIB_PATH):
     lib.gdr_varlen_workspace_bytes.restype = sz
     lib.gdr_forward_varlen.argtypes = [vp] * 8 + [ip] + [i] * 6 + [vp, i, vp, sz, u]
     lib.gdr_forward_varlen.restype = i
-    lib.gdr_tree_workspace_bytes.argtypes = [i] * 7
+    lib.gdr_tree_workspace_bytes.argtypes = [i] * 7 + [u]
     lib.gdr_tree_workspace_bytes.restype = sz
-    lib.gdr_forward_tree.argtypes = [vp] * 7 + [ip] + [i] * 6 + [vp, i, vp, sz]
+    lib.gdr_forward_tree.argtypes = [vp] * 7 + [ip] + [i] * 6 + [vp, i, vp, sz, u]
     lib.gdr_forward_tree.restype = i
     lib.gdr_device_check.argtypes = [vp]
     lib.gdr_device_check.restype = i
@@ -240,12 +240,13 @@ def gdr_forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, out=None, ht=None,
     return (out.unsqueeze(0) if lead else out), ht
 
 
-def gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, dtype=torch.bfloat16):
+def gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, dtype=torch.bfloat16, flags=0):
     lib = load_library()
-    return int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, _dtype_code(dtype)))
+    return int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, _dtype_code(dtype), flags))
 
 
-def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, workspace=None):
+def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, workspace=None,
+                     flags=0):
     """Tree verification: each batch element's T <= 64 tokens form a draft
     tree given by ``parent`` (host ints [B, T], parent[b, t] in [-1, t-1]);
     every token's output is that of the recurrence run along its root path
@@ -280,14 +281,14 @@ def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, w
         out = torch.empty(B, T, HV, dv, dtype=q.dtype, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    need = int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, code))
+    need = int(lib.gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, code, flags))
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = _ptr(workspace) if need > 0 else None
     ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
     st = lib.gdr_forward_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(out),
                               par_c, B, T, HK, HV, dk, dv, ctypes.c_void_p(stream.cuda_stream), code,
-                              ws_ptr, ws_bytes)
+                              ws_ptr, ws_bytes, flags)
     _check(lib, st)
     return out
 

@@ -316,10 +316,17 @@ namespace {
 // chunk that holds T tokens (0 when T is too large).
 int tree_chunk(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 0; }
 
-size_t tree_layout(const gdr::Problem &p, size_t *record_off) {
+bool tree_on_tensor_cores(const gdr::Problem &p, unsigned flags) {
+    gdr::Problem c = p;
+    c.chunk = 64;
+    return gdr::tc_prefill_supported(c) && !(flags & GDR_FLAG_FORCE_GENERIC);
+}
+
+// Workspace: the parents, then (CUDA-core route) the per-tree records.
+size_t tree_layout(const gdr::Problem &p, unsigned flags, size_t *record_off) {
     const size_t table = align256((size_t)p.B * p.T * sizeof(int));
     *record_off = table;
-    return table + gdr::generic_tree_record_bytes(p);
+    return table + (tree_on_tensor_cores(p, flags) ? 0 : gdr::generic_tree_record_bytes(p));
 }
 }  // namespace
 
@@ -525,7 +532,7 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
 }
 
 GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
-                                        int qkv_dtype) {
+                                        int qkv_dtype, unsigned flags) {
     if (B < 0 || T < 0 || HK <= 0 || HV <= 0 || HV % HK != 0) return 0;
     if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
     if (!supported_dim(dk) || !supported_dim(dv) || !tree_chunk(T)) return 0;
@@ -533,14 +540,14 @@ GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, in
     const gdr::Problem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                          B, T, HK, HV, dk, dv, tree_chunk(T), qkv_dtype == GDR_BF16 ? 1 : 0};
     size_t off = 0;
-    return tree_layout(p, &off);
+    return tree_layout(p, flags, &off);
 }
 
 GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v, const float *g,
                                     const float *beta, const float *h0, void *out,
                                     const int *parent, int B, int T, int HK, int HV, int dk,
                                     int dv, void *stream, int qkv_dtype, void *workspace,
-                                    size_t workspace_bytes) {
+                                    size_t workspace_bytes, unsigned flags) {
     if (B < 0 || T < 0) return GDR_ERR_SHAPE;
     if (T > 64) return GDR_ERR_UNSUPPORTED;
     const int chunk = tree_chunk(T > 0 ? T : 1);
@@ -555,7 +562,7 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
         if (parent[bt] < -1 || parent[bt] >= t) return GDR_ERR_SHAPE;
     }
     size_t record_off = 0;
-    const size_t need = tree_layout(p, &record_off);
+    const size_t need = tree_layout(p, flags, &record_off);
     if (!workspace || workspace_bytes < need) return GDR_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -564,7 +571,18 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
     cudaError_t e = cudaMemcpyAsync(ws, parent, (size_t)B * T * sizeof(int),
                                     cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = gdr::launch_generic_tree(p, ws + record_off, reinterpret_cast<const int *>(ws), s);
+    const int *par_dev = reinterpret_cast<const int *>(ws);
+    if (tree_on_tensor_cores(p, flags)) {
+        int *err = nullptr;
+        e = gdr::device_error_word(&err);
+        if (e == cudaSuccess) {
+            gdr::Problem tc = p;
+            tc.chunk = 64;
+            e = gdr::launch_tc_tree(tc, par_dev, err, s);
+        }
+    } else {
+        e = gdr::launch_generic_tree(p, ws + record_off, par_dev, s);
+    }
     return e == cudaSuccess ? GDR_OK : cuda_fail(e);
 }
 

@@ -106,6 +106,10 @@ cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const
 // Tree verification on CUDA cores: p.B trees of p.T <= p.chunk tokens each,
 // parents [B][T] (device); records: generic_tree_record_bytes(p).
 size_t generic_tree_record_bytes(const Problem &p);
+// Tree verification on the tensor cores (tc_prefill_supported, T <= 64):
+// parents [B][T] on the device.
+cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
+                           cudaStream_t stream);
 cudaError_t launch_generic_tree(const Problem &p, void *records, const int *parents,
                                 cudaStream_t stream);
 }  // namespace gdr

@@ -98,6 +98,10 @@ constexpr uint32_t kT32 = kAT + 16384;
 constexpr uint32_t kOpT = kAT + 32768;        // T' as K-major B [64 r][64 s]
 constexpr uint32_t kOpP = kOpT + 8192;        // [2] P as K-major B [64 r][64 s] (by chunk parity)
 constexpr uint32_t kStage = kOpP + 16384;     // bf16 O staging: per state warp one [16 r][32 j] box
+// Trees are one chunk, so the parity-1 P buffer is free: ancestor masks
+// (u64 [64]) and parents (i32 [64]) of the tree
+constexpr uint32_t kTreeAnc = kOpP + 8192;
+constexpr uint32_t kTreePar = kTreeAnc + 512;
 constexpr uint32_t kX32 = kStage + 16384;     // f32 [4][16][16] solve scratch
 constexpr uint32_t kSmall = kX32 + 4096;
 constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
@@ -311,11 +315,17 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
 // Packed variable-length batches: one record per sequence, {first token row
 // in the packed tensors, length, state slot}; the sequence's tensor maps sit
 // at the same index of a TileMaps array in global memory.
-template <bool HAS_H0, bool STORE_HT, bool VARLEN>
+// TREE: each batch element's T <= 64 tokens are a draft-token tree, parents
+// [B][T] (-1 for a root), run as one chunk with no state carry (page "Support
+// TreeUpdateSolve kernel", trymirai/uzu PR #576): the prefix sums of g run
+// along root paths, the decay reference is the tree's start (G_m = 0), and
+// the ancestor relation replaces the causal order in A and P.
+template <bool HAS_H0, bool STORE_HT, bool VARLEN, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const TileMaps *seq_maps,
-                          const int4 *seqs, const float *__restrict__ beta, const float *h0,
-                          float *ht, int T_dense, int HK, int HV, int *dev_error) {
+                          const int4 *seqs, const int *parents, const float *__restrict__ beta,
+                          const float *h0, float *ht, int T_dense, int HK, int HV,
+                          int *dev_error) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
     unsigned char *smem =
@@ -430,6 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kC)  // beta buffers: [2][64] floats by chunk parity
         reinterpret_cast<float *>(smem + kBeta)[tid] =
             tid < min(kC, T) ? beta[(tok0 + tid) * HV + hv] : 0.f;
+    const unsigned long long *tree_anc = reinterpret_cast<const unsigned long long *>(smem + kTreeAnc);
+    if (TREE && tid < kC)  // the tree's parents (rows past T: roots)
+        reinterpret_cast<int *>(smem + kTreePar)[tid] = tid < T ? parents[(size_t)b * T + tid] : -1;
+    // s is a token r depends on: an earlier one (sequence) or an ancestor (tree)
+    auto dep = [&](int r, int s) -> bool {
+        return TREE ? ((tree_anc[r] >> s) & 1ull) != 0 : s < r;
+    };
     // T' is lower triangular: its strictly-upper 16 x 16 blocks stay zero
     for (int idx = tid; idx < 64 * 8; idx += kThreads) {
         const int r = idx >> 3, s0 = (idx & 7) * 8;
@@ -446,6 +463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    if (TREE && tid < kC) {
+        // each token's ancestor set as a bit mask, by a walk up its root path
+        // (parents precede their children: at most 63 steps; the bounds keep
+        // the walk inside the table whatever it holds)
+        const int *par = reinterpret_cast<const int *>(smem + kTreePar);
+        unsigned long long a = 0ull;
+        int u = par[tid];
+        for (int step = 0; step < kC && u >= 0 && u < tid; ++step) {
+            a |= 1ull << u;
+            u = par[u];
+        }
+        reinterpret_cast<unsigned long long *>(smem + kTreeAnc)[tid] = a;
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
     uint32_t ph_a = 0, ph_b = 0, ph_g = 0, ph_4 = 0;
@@ -576,11 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (g == rb) {  // diagonal block, stored transposed
 #pragma unroll
                             for (int u = 0; u < 16; ++u)
-                                sA[diagT_idx(g, u, r & 15)] = (16 * g + u < r && r < Ln) ? br * dd[u] : 0.f;
+                                sA[diagT_idx(g, u, r & 15)] = (dep(r, 16 * g + u) && r < Ln) ? br * dd[u] : 0.f;
                         } else if (g < rb) {
 #pragma unroll
                             for (int u = 0; u < 16; ++u)
-                                sA[sq_idx(r, 16 * g + u)] = r < Ln ? br * dd[u] : 0.f;
+                                sA[sq_idx(r, 16 * g + u)] =
+                                    (r < Ln && (!TREE || dep(r, 16 * g + u))) ? br * dd[u] : 0.f;
                         }
                     }
                 }
@@ -703,7 +734,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool slow = false;
         if (has_prep) {
             wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
-            {
+            if (TREE) {
+                // log2 units in place, then prefix sums along root paths: one
+                // thread per channel walks the rows in order (parents first)
+                {
+                    const int i = tid & 127, qq = tid >> 7;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        float *gp = reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i));
+                        *gp *= kLog2e;
+                    }
+                }
+                csync();
+                float gmin = 0.f;
+                if (tid < kD) {
+                    const int *par = reinterpret_cast<const int *>(smem + kTreePar);
+                    for (int r = 0; r < kC; ++r) {
+                        const int p = par[r];
+                        float *gp = reinterpret_cast<float *>(smem + kG + g_off(r, tid));
+                        const float x = *gp + (p >= 0 && p < r ? gval(p, tid) : 0.f);
+                        *gp = x;
+                        gmin = fminf(gmin, x);
+                    }
+                }
+                // the factors exp(G) <= 1 and exp(-G) stay finite while no
+                // path decays by more than the range
+                slow = named_sync_or(kBarCompute, kCompute, -gmin > kRangeLog2) != 0;
+            } else {
                 const int i = tid & 127, qq = tid >> 7;
                 float x[16];
 #pragma unroll
@@ -736,8 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
-                const float gm = slow ? 0.f : gval(mref, tid), gl = gval(Ln - 1, tid);
-                const float egm = slow ? 1.f : fast_exp2(gm);
+                const float gm = (slow || TREE) ? 0.f : gval(mref, tid), gl = gval(Ln - 1, tid);
+                const float egm = (slow || TREE) ? 1.f : fast_exp2(gm);
                 vec(kEGm, pn)[tid] = egm;
                 vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
                 vec(kRho, pn)[tid] = fast_exp2(gl - gm);  // exp(G_L) / exp(G_m)
@@ -785,8 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
                 gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
                 gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
-                if (!slow) {
-                    // G at the reference row, from the G tile
+                if (!slow && !TREE) {
+                    // G at the reference row, from the G tile (a tree's
+                    // reference is its start, G_m = 0)
                     const float4 m_lo = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch));
                     const float4 m_hi = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch + 4));
                     gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
@@ -817,8 +875,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float el = fast_exp2(gv[e]);
                         lk[e] = kv[e] * el;
                         lq[e] = qv[e] * el;
-                        // R = exp(G_L - G) K directly (factor <= 1)
-                        rr[e] = kv[e] * fast_exp2(gval(Ln - 1, ch + e) - gv[e]);
+                        // R = exp(G_L - G) K directly (factor <= 1); a tree
+                        // carries no state, and its R is not read
+                        rr[e] = TREE ? 0.f : kv[e] * fast_exp2(gval(Ln - 1, ch + e) - gv[e]);
                     }
                 }
                 *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
@@ -858,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int s = 16 * iq + u;
-                        dd[u] = (s <= r && r < Ln) ? dd[u] : 0.f;
+                        dd[u] = ((s == r || dep(r, s)) && r < Ln) ? dd[u] : 0.f;
                     }
 #pragma unroll
                     for (int q8 = 0; q8 < 2; ++q8)
@@ -873,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int idx = tid; idx < kC * kC; idx += kCompute) {
                     const int r = idx >> 6, s = idx & 63;
                     float a = 0.f, p = 0.f;
-                    if (s <= r && r < Ln) {
+                    if ((s == r || dep(r, s)) && r < Ln) {
                         for (int i = 0; i < kD; ++i) {
                             const float e = fast_exp2(gval(r, i) - gval(s, i));
                             const float kse = kval(kRawK, s, i) * e;
@@ -881,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p = fmaf(kval(kRawQ, r, i), kse, p);
                         }
                     }
-                    const float av = (s < r) ? bvec[r] * a : 0.f;
+                    const float av = dep(r, s) ? bvec[r] * a : 0.f;
                     if ((r >> 4) == (s >> 4))
                         sA[diagT_idx(r >> 4, s & 15, r & 15)] = av;
                     else
@@ -897,13 +956,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_on(bar_4, ph_4);  // batch 4 of chunk c
             {
                 // S' <- alpha S' + delta dS (the next chunk's S', or after the
-                // last chunk S itself: there the factors are rho and cL)
+                // last chunk S itself: there the factors are rho and cL; a
+                // tree carries no state)
                 const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
                 const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kRho, ps) + 32 * iq);
                 float dd[32];
-                tmem_ld32(tl + kTmDS + 32 * iq, dd);
+                if (!TREE) tmem_ld32(tl + kTmDS + 32 * iq, dd);
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {  // packed fp32 pairs
+                for (int u4 = 0; u4 < 8 && !TREE; ++u4) {  // packed fp32 pairs
                     const float4 cl = cl4[u4], gm = gam4[u4];
                     S2[2 * u4] = __ffma2_rn(make_float2(gm.x, gm.y), S2[2 * u4],
                                             __fmul2_rn(make_float2(cl.x, cl.y),
@@ -1046,24 +1106,28 @@ bool encode_maps(EncodeTiledFn fn, TileMaps *tm, const Problem &p, size_t tok0, 
                       CU_TENSOR_MAP_SWIZZLE_NONE, 16);
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool TREE>
 cudaError_t launch_tc(const Problem &p, const TileMaps &tm, const TileMaps *seq_maps,
-                      const int4 *seqs, long long blocks, int *dev_error, cudaStream_t stream) {
+                      const int4 *seqs, const int *parents, long long blocks, int *dev_error,
+                      cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     auto run = [&](auto kernel) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
-        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tm, seq_maps, seqs, p.beta, p.h0,
-                                                                  p.ht, p.T, p.HK, p.HV, dev_error);
+        kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(
+            tm, seq_maps, seqs, parents, p.beta, p.h0, p.ht, p.T, p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };
-    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN>);
-    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN>);
-    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN>);
-    return run(gdr_prefill_tc_kernel<false, false, VARLEN>);
+    if (TREE)  // outputs only
+        return p.h0 ? run(gdr_prefill_tc_kernel<true, false, false, true>)
+                    : run(gdr_prefill_tc_kernel<false, false, false, true>);
+    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN, false>);
+    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN, false>);
+    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN, false>);
+    return run(gdr_prefill_tc_kernel<false, false, VARLEN, false>);
 }
 
 }  // namespace
@@ -1074,7 +1138,8 @@ cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t str
     if (e != cudaSuccess) return e;
     TileMaps tm;
     if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
-    return launch_tc<false>(p, tm, nullptr, nullptr, (long long)p.B * p.HV, dev_error, stream);
+    return launch_tc<false, false>(p, tm, nullptr, nullptr, nullptr, (long long)p.B * p.HV,
+                                   dev_error, stream);
 }
 
 size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
@@ -1093,8 +1158,22 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
                                      int nseq, int *dev_error, cudaStream_t stream) {
     TileMaps unused;
     memset(&unused, 0, sizeof(unused));
-    return launch_tc<true>(p, unused, static_cast<const TileMaps *>(seq_maps), seqs,
-                           (long long)nseq * p.HV, dev_error, stream);
+    return launch_tc<true, false>(p, unused, static_cast<const TileMaps *>(seq_maps), seqs,
+                                  nullptr, (long long)nseq * p.HV, dev_error, stream);
+}
+
+cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
+                           cudaStream_t stream) {
+    if (p.T > kC) return cudaErrorInvalidValue;
+    cudaError_t e = cudaSuccess;
+    EncodeTiledFn fn = encode_fn(&e);
+    if (e != cudaSuccess) return e;
+    TileMaps tm;
+    if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
+    Problem outputs_only = p;
+    outputs_only.ht = nullptr;
+    return launch_tc<false, true>(outputs_only, tm, nullptr, nullptr, parents,
+                                  (long long)p.B * p.HV, dev_error, stream);
 }
 
 }  // namespace gdr

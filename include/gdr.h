@@ -206,23 +206,25 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
  *
  * There is no final-state output: a tree has one state per leaf.  To commit
  * an accepted path, run gdr_forward (or gdr_forward_varlen) on its tokens
- * from the same h0.  Runs the CUDA-core chunked kernels with the whole tree
- * as one chunk (float32 arithmetic, both dtypes): path prefix sums of g and
- * the ancestor relation in place of the causal order.  `workspace`: device
- * memory of gdr_tree_workspace_bytes(...) bytes, 256-byte aligned,
- * untouched until the stream has passed the call.  Enqueues one
- * host-to-device copy of the parents (pageable: the call returns once they
- * have been taken) and two kernel launches.  Errors: GDR_ERR_UNSUPPORTED for
- * T > 64, GDR_ERR_SHAPE for a parent outside [-1, t-1], the rest as
- * gdr_forward_ex.  B == 0 or T == 0 does nothing.
+ * from the same h0.  The whole tree is one chunk of the chunked prefill: path
+ * prefix sums of g and the ancestor relation in place of the causal order.
+ * bf16 q/k/v with dk = dv = 128 run on the tensor-core prefill kernel (one
+ * launch), everything else -- or any call with GDR_FLAG_FORCE_GENERIC in
+ * `flags` -- on the CUDA-core chunk kernels (two launches, float32
+ * throughout).  `workspace`: device memory of gdr_tree_workspace_bytes(...)
+ * bytes (same flags), 256-byte aligned, untouched until the stream has
+ * passed the call.  Also enqueues one host-to-device copy of the parents
+ * (pageable: the call returns once they have been taken).  Errors:
+ * GDR_ERR_UNSUPPORTED for T > 64, GDR_ERR_SHAPE for a parent outside
+ * [-1, t-1], the rest as gdr_forward_ex.  B == 0 or T == 0 does nothing.
  */
 GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
-                                        int qkv_dtype);
+                                        int qkv_dtype, unsigned flags);
 GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v, const float *g,
                                     const float *beta, const float *h0, void *out,
                                     const int *parent, int B, int T, int HK, int HV, int dk,
                                     int dv, void *stream, int qkv_dtype, void *workspace,
-                                    size_t workspace_bytes);
+                                    size_t workspace_bytes, unsigned flags);
 
 /*
  * Waits for `stream`, then reads and clears the library's device error word

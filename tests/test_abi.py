@@ -161,7 +161,7 @@ def call_tree(lib, parent, B=1, T=4, HK=1, HV=2, dk=32, dv=32, dtype=0, ws=None,
     args = [ctypes.c_void_p(FAKE + n * step) for n in range(7)]
     arr = None if parent is None else cu_array(parent)
     return lib.gdr_forward_tree(*args, arr, B, T, HK, HV, dk, dv, None, dtype,
-                                None if ws is None else ctypes.c_void_p(ws), ws_bytes)
+                                None if ws is None else ctypes.c_void_p(ws), ws_bytes, 0)
 
 
 @pytest.mark.parametrize("parent,kw,status", [
@@ -177,8 +177,11 @@ def test_tree_bad_arguments_rejected_before_launch(lib, parent, kw, status):
 
 
 def test_tree_workspace_sizes(lib):
-    assert lib.gdr_tree_workspace_bytes(1, 0, 1, 2, 32, 32, 0) == 0
-    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0) == 0
-    small = lib.gdr_tree_workspace_bytes(1, 16, 1, 2, 32, 32, 0)
-    assert 0 < small < lib.gdr_tree_workspace_bytes(1, 17, 1, 2, 32, 32, 0)
+    assert lib.gdr_tree_workspace_bytes(1, 0, 1, 2, 32, 32, 0, 0) == 0
+    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0, 0) == 0
+    small = lib.gdr_tree_workspace_bytes(1, 16, 1, 2, 32, 32, 0, 0)
+    assert 0 < small < lib.gdr_tree_workspace_bytes(1, 17, 1, 2, 32, 32, 0, 0)
+    # tensor-core route (bf16, d = 128): the parents only
+    assert lib.gdr_tree_workspace_bytes(2, 64, 1, 2, 128, 128, 1, 0) == 512
+    assert lib.gdr_tree_workspace_bytes(2, 64, 1, 2, 128, 128, 1, 2) > 512  # forced CUDA cores
     assert call_tree(lib, [-1, 0, 0, 1], ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5

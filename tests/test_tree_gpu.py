@@ -13,17 +13,47 @@ from tests.parity_util import assert_close, to_cuda
 pytestmark = pytest.mark.gpu
 
 
-def run_tree(d, parent):
+def run_tree(d, parent, flags=0):
     c = to_cuda(d)
-    out = gdr_forward_tree(c["q"], c["k"], c["v"], c["g"], c["beta"], parent, h0=c["h0"])
+    out = gdr_forward_tree(c["q"], c["k"], c["v"], c["g"], c["beta"], parent, h0=c["h0"],
+                           flags=flags)
     gdr_device_check()
     return out
 
 
-def check(d, parent):
+def check(d, parent, flags=0):
     ref = oracle.tree_recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
                                  to_f64(d["h0"]), parent.numpy())
-    assert_close("o", run_tree(d, parent), ref, d["q"].dtype)
+    assert_close("o", run_tree(d, parent, flags), ref, d["q"].dtype)
+
+
+# --------------------------- tensor-core route (bf16, dk = dv = 128)
+@pytest.mark.parametrize("kind", ["random", "beam", "star", "chain"])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 33, 64])
+def test_tc_tree_shapes(kind, T):
+    d = draw(2, T, 2, 4, 128, 128, dtype=torch.bfloat16, seed=100 + T)
+    check(d, draw_parents(2, T, kind, seed=T))
+
+
+def test_tc_tree_no_initial_state():
+    d = draw(3, 48, 1, 2, 128, 128, dtype=torch.bfloat16, h0=False, seed=101)
+    check(d, draw_parents(3, 48, "random", seed=101))
+
+
+@pytest.mark.parametrize("kind", ["chain", "random"])
+def test_tc_tree_strong_decay(kind):
+    """|g| ~ 3 per token: a 64-deep chain decays by ~190 nats (the exact
+    path), a random tree's shallow paths stay in range (the fast path)."""
+    d = draw(2, 64, 1, 2, 128, 128, dtype=torch.bfloat16, seed=102, g_mu=3.0)
+    check(d, draw_parents(2, 64, kind, seed=102))
+
+
+def test_tc_and_cuda_core_routes_agree():
+    d = draw(4, 64, 2, 4, 128, 128, dtype=torch.bfloat16, seed=103)
+    par = draw_parents(4, 64, "beam", seed=103, branching=3)
+    tc = run_tree(d, par).float()
+    cc = run_tree(d, par, flags=GDR_FLAG_FORCE_GENERIC).float()
+    assert (tc - cc).abs().max().item() <= 2e-2 * cc.abs().max().item()
 
 
 @pytest.mark.parametrize("kind", ["random", "beam", "star", "chain"])
