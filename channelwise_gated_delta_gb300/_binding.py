@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
 
 EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_forward_chunked_noalloc",
             "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_tree_workspace_bytes",
-            "gdr_forward_tree", "gdr_device_check",
+            "gdr_forward_tree", "gdr_host_staging_bytes", "gdr_forward_host", "gdr_device_check",
             "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma", "gdr_status_string",
             "gdr_last_cuda_error", "gdr_version")
 
@@ -68,6 +68,10 @@ def load_library(path=LIB_PATH):
     lib.gdr_tree_workspace_bytes.restype = sz
     lib.gdr_forward_tree.argtypes = [vp] * 7 + [ip] + [i] * 6 + [vp, i, vp, sz, u]
     lib.gdr_forward_tree.restype = i
+    lib.gdr_host_staging_bytes.argtypes = [i] * 8
+    lib.gdr_host_staging_bytes.restype = sz
+    lib.gdr_forward_host.argtypes = fwd + [vp, sz]
+    lib.gdr_forward_host.restype = i
     lib.gdr_device_check.argtypes = [vp]
     lib.gdr_device_check.restype = i
     lib.gdr_status_string.argtypes = [i]
@@ -291,6 +295,56 @@ def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, w
                               ws_ptr, ws_bytes, flags)
     _check(lib, st)
     return out
+
+
+def gdr_host_staging_bytes(B, T, HK, HV, dk, dv, chunk=64, dtype=torch.bfloat16):
+    lib = load_library()
+    return int(lib.gdr_host_staging_bytes(B, T, HK, HV, dk, dv, chunk, _dtype_code(dtype)))
+
+
+def gdr_forward_host(q, k, v, g, beta, h0, out, ht, chunk=64, stream=None, staging=None,
+                     device=None):
+    """The forward pass on HOST tensors (CPU, pinned for overlap): copies in,
+    computes and copies out through the library, batch elements pipelined
+    through two device slots.  Shapes as in gdr_forward; ``out`` and ``ht``
+    (may be None, or ``ht is h0``) are host tensors written by the call,
+    complete once ``stream`` (default: the current stream of ``device``)
+    reaches the call's end.  Returns (out, ht)."""
+    lib = load_library()
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("out", out), ("ht", ht)):
+        if t is None:
+            continue
+        if t.device.type != "cpu":
+            raise ValueError("%s must be a host tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != q.dtype:
+        raise ValueError("k, v and out must match q in dtype (and k in shape)")
+    if tuple(v.shape[:2]) != (B, T) or tuple(g.shape) != (B, T, HV, dk) or \
+            tuple(beta.shape) != (B, T, HV) or tuple(out.shape) != (B, T, HV, dv):
+        raise ValueError("inconsistent shapes")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    for name, t in (("h0", h0), ("ht", ht)):
+        if t is not None and (tuple(t.shape) != (B, HV, dk, dv) or t.dtype != torch.float32):
+            raise ValueError("%s must be float32 [B, HV, dk, dv]" % name)
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    need = int(lib.gdr_host_staging_bytes(B, T, HK, HV, dk, dv, chunk, code))
+    if need > 0 and (staging is None or staging.numel() * staging.element_size() < need):
+        staging = torch.empty(need, dtype=torch.uint8, device=dev)
+    st_ptr = _ptr(staging) if need > 0 else None
+    st_bytes = staging.numel() * staging.element_size() if need > 0 else 0
+    st = lib.gdr_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                              _ptr(out), _ptr(ht), B, T, HK, HV, dk, dv, chunk,
+                              ctypes.c_void_p(stream.cuda_stream), code, st_ptr, st_bytes)
+    _check(lib, st)
+    return out, ht
 
 
 def gdr_device_check(stream=None):

@@ -152,6 +152,31 @@ GDR_API gdr_status gdr_forward_chunked_noalloc(const void *q, const void *k, con
                                                void *stream, int qkv_dtype);
 
 /*
+ * The forward pass on HOST buffers.  Arguments and layouts are those of
+ * gdr_forward, except that q, k, v, g, beta, h0, out and ht are host memory
+ * (page-locked for the copies to run asynchronously; pageable memory works
+ * but each copy then waits for the host).  Nothing in the pages corresponds
+ * to it: it is the input/output path of a caller whose tensors live on the
+ * host.  The batch streams through two device slots in `staging` (device
+ * memory of gdr_host_staging_bytes(...) bytes, 256-byte aligned): while
+ * batch element b computes on `stream`, element b + 1 is copied in and
+ * element b - 1 copied out on two library-owned streams, so the copies in
+ * both directions overlap the compute.  Ordered after earlier work on
+ * `stream`; later work on `stream` starts after the last copy out.  Results
+ * equal those of gdr_forward on the same values bit for bit.  Calls from
+ * several host threads are serialised while they enqueue.  Errors as
+ * gdr_forward_ex (GDR_ERR_WORKSPACE for a short staging buffer); a failure
+ * after the first copy leaves the outputs partly written.
+ */
+GDR_API size_t gdr_host_staging_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                      int qkv_dtype);
+GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *h0, void *out, float *ht,
+                                    int B, int T, int HK, int HV, int dk, int dv, int chunk,
+                                    void *stream, int qkv_dtype, void *staging,
+                                    size_t staging_bytes);
+
+/*
  * Packed variable-length batches.  The same page's second commit summary
  * treats every sequence of a batch independently, routes a sequence of one
  * token to the single-token recurrence and runs a ragged last chunk through

@@ -185,3 +185,18 @@ def test_tree_workspace_sizes(lib):
     assert lib.gdr_tree_workspace_bytes(2, 64, 1, 2, 128, 128, 1, 0) == 512
     assert lib.gdr_tree_workspace_bytes(2, 64, 1, 2, 128, 128, 1, 2) > 512  # forced CUDA cores
     assert call_tree(lib, [-1, 0, 0, 1], ws=FAKE + (9 << 30), ws_bytes=small - 1) == 5
+
+
+def test_host_entry_rejections(lib):
+    assert lib.gdr_host_staging_bytes(0, 10, 1, 2, 32, 32, 16, 0) == 0
+    assert lib.gdr_host_staging_bytes(2, 10, 2, 3, 32, 32, 16, 0) == 0
+    one = lib.gdr_host_staging_bytes(1, 10, 1, 2, 32, 32, 16, 0)
+    assert 0 < one and lib.gdr_host_staging_bytes(5, 10, 1, 2, 32, 32, 16, 0) == 2 * one
+    step = 1 << 30
+    ptrs = [ctypes.c_void_p(FAKE + n * step) for n in range(8)]
+    args = lambda **kw: [kw.get("B", 2), 10, 1, 2, kw.get("dk", 32), 32, 16, None, 0]
+    assert lib.gdr_forward_host(*ptrs, *args(), None, 0) == 5             # no staging
+    assert lib.gdr_forward_host(*ptrs, *args(dk=48), None, 0) == 3
+    assert lib.gdr_forward_host(*ptrs, *args(B=-1), None, 0) == 2
+    assert lib.gdr_forward_host(*ptrs, *args(), ctypes.c_void_p(FAKE + (9 << 30) + 16),
+                                2 * one) == 4                              # misaligned
