@@ -31,6 +31,15 @@ Two routines, both in float64:
     the ancestor mask and path prefix sums, over the whole tree at once; it
     exists to pin the form the GPU computes.
 
+``scalar_gate_recurrence`` / ``scalar_gate_wy``
+    The scalar-gate variant (one log-decay per token and value head, the
+    same for every key channel), the case in which the review thread of
+    "Support TreeUpdateSolve kernel" weighs a per-key-head gram against a
+    per-value-head one.  The definition is the recurrence with g broadcast
+    over the key channels; ``scalar_gate_wy`` is the chunked form with the
+    decay factored out of the dot products, so that one gram K K^T per key
+    head serves all of its value heads.
+
 Array layouts (numpy, C-contiguous):
     q, k [B, T, HK, dk]; v [B, T, HV, dv]; g [B, T, HV, dk]; beta [B, T, HV];
     h0 [B, HV, dk, dv] or None.  Returns (o [B, T, HV, dv], ht [B, HV, dk, dv]).
@@ -273,3 +282,60 @@ def tree_wy(q, k, v, g, beta, h0, parent):
             U = solve_triangular(np.eye(T) + A, rhs, lower=True, unit_diagonal=True)
             out[b, :, hv] = Qt @ S + P @ U
     return out
+
+
+def scalar_gate_recurrence(q, k, v, g, beta, h0=None, threads=None):
+    """Scalar-gate forward by definition: g [B, T, HV] (one log-decay per
+    token and value head) applied to every key channel, i.e. the recurrence
+    with g repeated over dk.  Returns (o, ht)."""
+    g = _f64(g)
+    dk = np.asarray(q).shape[3]
+    return recurrence(q, k, v, np.repeat(g[..., None], dk, axis=3), beta, h0, threads=threads)
+
+
+def scalar_gate_wy(q, k, v, g, beta, h0=None, chunk=64):
+    """Scalar-gate chunked form with the gram per key head.
+
+    Per chunk of L tokens, with G the inclusive prefix of the scalar g of a
+    value head and Gamma[r, s] = exp(G_r - G_s) (s <= r):
+      KK = K K^T and QK = Q K^T, once per KEY head (shared by its G value heads)
+      A = diag(beta) (KK * Gamma), strictly lower;  P = QK * Gamma, lower
+      (I + A) U = diag(beta) (V - exp(G) K S0)
+      O = exp(G) Q S0 + P U
+      S_next = exp(G_L) S0 + (exp(G_L - G) K)^T U
+    Returns (o [B, T, HV, dv], ht [B, HV, dk, dv])."""
+    from scipy.linalg import solve_triangular
+
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    group = HV // HK
+    out = np.zeros((B, T, HV, dv))
+    ht = np.zeros((B, HV, dk, dv))
+    for b in range(B):
+        S = {hv: (np.zeros((dk, dv)) if h0 is None else _f64(h0)[b, hv].copy())
+             for hv in range(HV)}
+        for t0 in range(0, T, chunk):
+            t1 = min(T, t0 + chunk)
+            L = t1 - t0
+            for hk in range(HK):
+                K = k[b, t0:t1, hk]
+                Q = q[b, t0:t1, hk]
+                KK = K @ K.T            # the key-head gram, shared below
+                QK = Q @ K.T
+                for hv in range(hk * group, (hk + 1) * group):
+                    G = np.cumsum(g[b, t0:t1, hv])                      # [L]
+                    diff = G[:, None] - G[None, :]
+                    Gamma = np.exp(np.where(np.tril(np.ones((L, L))) > 0, diff, -np.inf))
+                    bet = beta[b, t0:t1, hv]
+                    A = bet[:, None] * KK * Gamma * np.tril(np.ones((L, L)), -1)
+                    P = QK * Gamma
+                    V = v[b, t0:t1, hv]
+                    eG = np.exp(G)[:, None]
+                    rhs = bet[:, None] * (V - (eG * K) @ S[hv])
+                    U = solve_triangular(np.eye(L) + A, rhs, lower=True, unit_diagonal=True)
+                    out[b, t0:t1, hv] = (eG * Q) @ S[hv] + P @ U
+                    S[hv] = np.exp(G[-1]) * S[hv] + (np.exp(G[-1] - G)[:, None] * K).T @ U
+        for hv in range(HV):
+            ht[b, hv] = S[hv]
+    return out, ht
