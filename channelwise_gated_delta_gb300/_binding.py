@@ -19,6 +19,7 @@ GDR_F32 = 0
 GDR_BF16 = 1
 GDR_FLAG_FORCE_CHUNKED = 1
 GDR_FLAG_FORCE_GENERIC = 2
+GDR_FLAG_SCALAR_GATE = 4
 
 STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_UNSUPPORTED",
                 4: "GDR_ERR_ALIGN", 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA",
@@ -143,8 +144,11 @@ def gdr_forward(q, k, v, g, beta, h0=None, out=None, ht=None, chunk=64, stream=N
             raise ValueError("%s must be contiguous" % name)
     if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k must match q in shape and dtype; v must match q in dtype")
-    if tuple(v.shape[:2]) != (B, T) or tuple(g.shape) != (B, T, HV, dk) or \
-            tuple(beta.shape) != (B, T, HV):
+    if tuple(g.shape) == (B, T, HV):   # a scalar gate: one log-decay per token and head
+        flags |= GDR_FLAG_SCALAR_GATE
+    elif tuple(g.shape) != (B, T, HV, dk):
+        raise ValueError("g must be [B, T, HV, dk] (channelwise) or [B, T, HV] (scalar gate)")
+    if tuple(v.shape[:2]) != (B, T) or tuple(beta.shape) != (B, T, HV):
         raise ValueError("inconsistent shapes")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
@@ -218,7 +222,11 @@ def gdr_forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, out=None, ht=None,
         raise ValueError("cu_seqlens[-1] (%d) != number of token rows (%d)" % (cu[n], total))
     if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k must match q in shape and dtype; v must match q in dtype")
-    if v.shape[0] != total or tuple(g.shape) != (total, HV, dk) or tuple(beta.shape) != (total, HV):
+    if tuple(g.shape) == (total, HV):   # a scalar gate
+        flags |= GDR_FLAG_SCALAR_GATE
+    elif tuple(g.shape) != (total, HV, dk):
+        raise ValueError("g must be [total, HV, dk] (channelwise) or [total, HV] (scalar gate)")
+    if v.shape[0] != total or tuple(beta.shape) != (total, HV):
         raise ValueError("inconsistent shapes")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
@@ -270,8 +278,11 @@ def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, w
             raise ValueError("%s must be contiguous" % name)
     if k.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k must match q in shape and dtype; v must match q in dtype")
-    if tuple(v.shape[:2]) != (B, T) or tuple(g.shape) != (B, T, HV, dk) or \
-            tuple(beta.shape) != (B, T, HV):
+    if tuple(g.shape) == (B, T, HV):   # a scalar gate
+        flags |= GDR_FLAG_SCALAR_GATE
+    elif tuple(g.shape) != (B, T, HV, dk):
+        raise ValueError("g must be [B, T, HV, dk] (channelwise) or [B, T, HV] (scalar gate)")
+    if tuple(v.shape[:2]) != (B, T) or tuple(beta.shape) != (B, T, HV):
         raise ValueError("inconsistent shapes")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")

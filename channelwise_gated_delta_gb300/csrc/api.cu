@@ -43,7 +43,8 @@ bool overlap(Range a, Range b) {
 // overlap); the shape checks common to every entry point.
 gdr_status validate_rows(const void *q, const void *k, const void *v, const float *g,
                          const float *beta, const float *h0, void *out, float *ht, long long BT,
-                         long long NS, int HK, int HV, int dk, int dv, int chunk, int qkv_dtype) {
+                         long long NS, int HK, int HV, int dk, int dv, int chunk, int qkv_dtype,
+                         bool g_scalar) {
     if (HK <= 0 || HV <= 0) return GDR_ERR_SHAPE;
     if (HV % HK != 0) return GDR_ERR_SHAPE;
     if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
@@ -64,7 +65,7 @@ gdr_status validate_rows(const void *q, const void *k, const void *v, const floa
     const Range rq = range_of(q, (size_t)BT * HK * dk * es);
     const Range rk = range_of(k, (size_t)BT * HK * dk * es);
     const Range rv = range_of(v, (size_t)BT * HV * dv * es);
-    const Range rg = range_of(g, (size_t)BT * HV * dk * 4);
+    const Range rg = range_of(g, (size_t)BT * HV * (g_scalar ? 1 : dk) * 4);
     const Range rb = range_of(beta, (size_t)BT * HV * 4);
     const Range rs0 = h0 ? range_of(h0, (size_t)NS * HV * dk * dv * 4) : Range{0, 0};
     const Range ro = work ? range_of(out, (size_t)BT * HV * dv * es) : Range{0, 0};
@@ -82,13 +83,15 @@ gdr_status validate_rows(const void *q, const void *k, const void *v, const floa
 // look at the workspace.
 gdr_status validate(const void *q, const void *k, const void *v, const float *g,
                     const float *beta, const float *h0, void *out, float *ht, int B, int T,
-                    int HK, int HV, int dk, int dv, int chunk, int qkv_dtype, gdr::Problem *p) {
+                    int HK, int HV, int dk, int dv, int chunk, int qkv_dtype, gdr::Problem *p,
+                    unsigned flags = 0) {
     if (B < 0 || T < 0) return GDR_ERR_SHAPE;
+    const bool gs = (flags & GDR_FLAG_SCALAR_GATE) != 0;
     const gdr_status st = validate_rows(q, k, v, g, beta, h0, out, ht, (long long)B * T, B, HK,
-                                        HV, dk, dv, chunk, qkv_dtype);
+                                        HV, dk, dv, chunk, qkv_dtype, gs);
     if (st != GDR_OK) return st;
     *p = gdr::Problem{q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
-                      qkv_dtype == GDR_BF16 ? 1 : 0};
+                      qkv_dtype == GDR_BF16 ? 1 : 0, gs ? 1 : 0};
     return GDR_OK;
 }
 
@@ -319,7 +322,8 @@ int tree_chunk(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 0; }
 bool tree_on_tensor_cores(const gdr::Problem &p, unsigned flags) {
     gdr::Problem c = p;
     c.chunk = 64;
-    return gdr::tc_prefill_supported(c) && !(flags & GDR_FLAG_FORCE_GENERIC);
+    return gdr::tc_prefill_supported(c) && !(flags & GDR_FLAG_FORCE_GENERIC) &&
+           !(flags & GDR_FLAG_SCALAR_GATE);
 }
 
 // Workspace: the parents, then (CUDA-core route) the per-tree records.
@@ -388,7 +392,7 @@ GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, c
                                   size_t workspace_bytes, unsigned flags) {
     gdr::Problem p;
     gdr_status st = validate(q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
-                             qkv_dtype, &p);
+                             qkv_dtype, &p, flags);
     if (st != GDR_OK) return st;
     const Route r = choose(p, flags);
     const size_t need = route_workspace(p, r);
@@ -455,11 +459,12 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
     gdr_status st = check_cu_seqlens(cu_seqlens, N);
     if (st != GDR_OK) return st;
     const long long total = N > 0 ? cu_seqlens[N] : 0;
+    const bool gs = (flags & GDR_FLAG_SCALAR_GATE) != 0;
     st = validate_rows(q, k, v, g, beta, h0, out, ht, total, N, HK, HV, dk, dv, chunk,
-                                  qkv_dtype);
+                                  qkv_dtype, gs);
     if (st != GDR_OK) return st;
     const gdr::Problem base{q, k, v, g, beta, h0, out, ht, N, 0, HK, HV, dk, dv, chunk,
-                            qkv_dtype == GDR_BF16 ? 1 : 0};
+                            qkv_dtype == GDR_BF16 ? 1 : 0, gs ? 1 : 0};
     VarlenPlan plan;
     st = plan_varlen(cu_seqlens, N, base, flags, &plan);
     if (st != GDR_OK) return st;
@@ -538,7 +543,8 @@ GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, in
     if (!supported_dim(dk) || !supported_dim(dv) || !tree_chunk(T)) return 0;
     if ((long long)B * T == 0) return 0;
     const gdr::Problem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                         B, T, HK, HV, dk, dv, tree_chunk(T), qkv_dtype == GDR_BF16 ? 1 : 0};
+                         B, T, HK, HV, dk, dv, tree_chunk(T), qkv_dtype == GDR_BF16 ? 1 : 0,
+                         (flags & GDR_FLAG_SCALAR_GATE) ? 1 : 0};
     size_t off = 0;
     return tree_layout(p, flags, &off);
 }
@@ -553,7 +559,7 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
     const int chunk = tree_chunk(T > 0 ? T : 1);
     gdr::Problem p;
     gdr_status st = validate(q, k, v, g, beta, h0, out, nullptr, B, T, HK, HV, dk, dv, chunk,
-                             qkv_dtype, &p);
+                             qkv_dtype, &p, flags);
     if (st != GDR_OK) return st;
     if ((long long)B * T == 0) return GDR_OK;
     if (!parent) return GDR_ERR_NULL;

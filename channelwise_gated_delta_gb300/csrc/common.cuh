@@ -73,7 +73,8 @@ struct Problem {
     void *out;
     float *ht;
     int B, T, HK, HV, dk, dv, chunk;
-    int bf16;  // 1: q/k/v/out are bfloat16, 0: float32
+    int bf16;      // 1: q/k/v/out are bfloat16, 0: float32
+    int g_scalar;  // 1: g is [rows][HV] (one log-decay per token and value head), 0: [rows][HV][dk]
 };
 
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream);

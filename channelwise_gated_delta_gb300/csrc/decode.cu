@@ -66,7 +66,8 @@ __device__ __forceinline__ float4 block_column_sum(float4 part, float (*red)[kDe
     return tot;
 }
 
-template <typename Tin, int DK, bool HAS_H0, bool STORE_HT, bool ROWS>
+// GS: a scalar gate, g[head] (one log-decay per token and value head).
+template <typename Tin, int DK, bool HAS_H0, bool STORE_HT, bool ROWS, bool GS>
 __global__ void __launch_bounds__(2 * DK)
     gdr_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                       const Tin *__restrict__ v, const float *__restrict__ g,
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(2 * DK)
 
     const Tin *kp = k + ((size_t)trow * HK + hk) * DK;
     const Tin *qp = q + ((size_t)trow * HK + hk) * DK;
-    const float *gp = g + head * DK;
+    const float *gp = g + head * (GS ? 1 : DK);
     const float bt = beta[head];
     const float4 vv = load4(v + head * dv + col);
 
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(2 * DK)
         }
         kr[m] = to_f32(kp[r]);
         qr[m] = to_f32(qp[r]);
-        const float gamma = expf(gp[r]);
+        const float gamma = expf(gp[GS ? 0 : r]);
         s[m].x *= gamma;
         s[m].y *= gamma;
         s[m].z *= gamma;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(2 * DK)
     if (tid < 8) store4(out + head * dv + col, o);
 }
 
-template <typename Tin, int DK, bool ROWS>
+template <typename Tin, int DK, bool ROWS, bool GS>
 cudaError_t launch_decode_t(const Problem &p, const int2 *rows, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.HV * (p.dv / kDecodeBV);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -156,29 +157,35 @@ cudaError_t launch_decode_t(const Problem &p, const int2 *rows, cudaStream_t str
     Tin *out = static_cast<Tin *>(p.out);
     trace_begin(kKernDecode, stream);
     if (p.h0 && p.ht)
-        gdr_decode_kernel<Tin, DK, true, true, ROWS><<<grid, block, 0, stream>>>(
+        gdr_decode_kernel<Tin, DK, true, true, ROWS, GS><<<grid, block, 0, stream>>>(
             q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else if (p.h0)
-        gdr_decode_kernel<Tin, DK, true, false, ROWS><<<grid, block, 0, stream>>>(
+        gdr_decode_kernel<Tin, DK, true, false, ROWS, GS><<<grid, block, 0, stream>>>(
             q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else if (p.ht)
-        gdr_decode_kernel<Tin, DK, false, true, ROWS><<<grid, block, 0, stream>>>(
+        gdr_decode_kernel<Tin, DK, false, true, ROWS, GS><<<grid, block, 0, stream>>>(
             q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     else
-        gdr_decode_kernel<Tin, DK, false, false, ROWS><<<grid, block, 0, stream>>>(
+        gdr_decode_kernel<Tin, DK, false, false, ROWS, GS><<<grid, block, 0, stream>>>(
             q, k, v, p.g, p.beta, p.h0, out, p.ht, rows, p.HK, p.HV, p.dv);
     trace_end(kKernDecode, stream);
     return cudaGetLastError();
 }
 
-template <typename Tin, bool ROWS>
-cudaError_t launch_decode_dt(const Problem &p, const int2 *rows, cudaStream_t stream) {
+template <typename Tin, bool ROWS, bool GS>
+cudaError_t launch_decode_d(const Problem &p, const int2 *rows, cudaStream_t stream) {
     switch (p.dk) {
-        case 32: return launch_decode_t<Tin, 32, ROWS>(p, rows, stream);
-        case 64: return launch_decode_t<Tin, 64, ROWS>(p, rows, stream);
-        case 128: return launch_decode_t<Tin, 128, ROWS>(p, rows, stream);
+        case 32: return launch_decode_t<Tin, 32, ROWS, GS>(p, rows, stream);
+        case 64: return launch_decode_t<Tin, 64, ROWS, GS>(p, rows, stream);
+        case 128: return launch_decode_t<Tin, 128, ROWS, GS>(p, rows, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <typename Tin, bool ROWS>
+cudaError_t launch_decode_dt(const Problem &p, const int2 *rows, cudaStream_t stream) {
+    return p.g_scalar ? launch_decode_d<Tin, ROWS, true>(p, rows, stream)
+                      : launch_decode_d<Tin, ROWS, false>(p, rows, stream);
 }
 
 }  // namespace

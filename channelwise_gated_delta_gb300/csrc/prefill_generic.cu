@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                    const Tin *__restrict__ v, const float *__restrict__ g,
                    const float *__restrict__ beta, float *__restrict__ ws,
                    const int2 *__restrict__ chunks, const int *__restrict__ parents, int T,
-                   int HK, int HV, int dk, int dv, int C, int NC) {
+                   int HK, int HV, int dk, int dv, int C, int NC, int g_scalar) {
     extern __shared__ float smem[];
     const int ldk = dk + 1;  // padded rows: threads walking s hit distinct banks
     const int ldw = dk + dv;
@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kPrepThreads)
             const size_t tk = (tr0 + r) * HK + hk;
             kv = to_f32(k[tk * dk + i]);
             qv = to_f32(q[tk * dk + i]);
-            gv = g[((tr0 + r) * HV + hv) * dk + i];
+            // a scalar gate has one log-decay per token and head
+            gv = g_scalar ? g[(tr0 + r) * HV + hv] : g[((tr0 + r) * HV + hv) * dk + i];
         }
         Ks[r * ldk + i] = kv;
         Qs[r * ldk + i] = qv;
@@ -369,7 +370,7 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chun
     gdr_chunk_prep<Tin, TREE><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
         static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
         static_cast<const Tin *>(p.v), p.g, p.beta, ws, chunks, parents, p.T, p.HK, p.HV, p.dk,
-        p.dv, C, NC);
+        p.dv, C, NC, p.g_scalar);
     trace_end(kKernChunkPrep, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -83,6 +83,7 @@ constexpr int kBarAux = 7;                  // solver warps only (64)
 constexpr int kBarSolve = 8;                // solvers -> issuers: T' complete (128)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
+constexpr float kQuarterLog2 = 21.f * kLog2e;  // per-quarter decay limit of the fast path
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
@@ -90,6 +91,7 @@ constexpr uint32_t kRawK = 0;                 // k: 2 TMA boxes [64 rows][64 bf1
 constexpr uint32_t kRawQ = kRawK + 16384;     // q: same
 constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
 constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
+                                              // (scalar gate: f32 [2][64] by chunk parity)
 constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lq, 64-127 Lk
 constexpr uint32_t kOpR = kOpL + 32768;       // [2][64][128] K-major: R (by chunk parity)
 constexpr uint32_t kAT = kOpR + 32768;        // 32 KB: f32 A and T (64x64 each)
@@ -230,16 +232,18 @@ struct TileMaps {
 };
 
 // Lanes 0-7 of one warp: the k, q and g boxes of one chunk (tokens t0 ..
-// t0+63), one box per lane, after lane 0 has announced the byte count.
+// t0+63), one box per lane, after lane 0 has announced the byte count.  A
+// scalar gate's g is not a tile: only k and q come by TMA.
+template <bool WITH_G>
 __device__ __forceinline__ void issue_kqg(unsigned char *sm, const TileMaps &tm, uint64_t *bar,
                                           int b, int t0, int hk, int hv, int lane) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, kBytesKQG);
+    if (lane == 0) mbar_arrive_expect_tx(bar, WITH_G ? kBytesKQG : kBytesKQG - 32768);
     __syncwarp();
     if (lane < 2)
         tma_load_4d(sm + kRawK + 8192 * lane, &tm.k, 64 * lane, hk, t0, b, bar);
     else if (lane < 4)
         tma_load_4d(sm + kRawQ + 8192 * (lane - 2), &tm.q, 64 * (lane - 2), hk, t0, b, bar);
-    else if (lane < 8)
+    else if (WITH_G && lane < 8)
         tma_load_4d(sm + kG + 8192 * (lane - 4), &tm.g, 32 * (lane - 4), hv, t0, b, bar);
 }
 __device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, uint64_t *bar, int b,
@@ -320,12 +324,15 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
 // TreeUpdateSolve kernel", trymirai/uzu PR #576): the prefix sums of g run
 // along root paths, the decay reference is the tree's start (G_m = 0), and
 // the ancestor relation replaces the causal order in A and P.
-template <bool HAS_H0, bool STORE_HT, bool VARLEN, bool TREE>
+// SCALAR_G: g is one log-decay per token and value head (gsc, [rows][HV]),
+// the same for every key channel; it is loaded like beta, its prefix sum is
+// one warp scan, and each row's decay factors are one exponential.
+template <bool HAS_H0, bool STORE_HT, bool VARLEN, bool TREE, bool SCALAR_G>
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const TileMaps *seq_maps,
                           const int4 *seqs, const int *parents, const float *__restrict__ beta,
-                          const float *h0, float *ht, int T_dense, int HK, int HV,
-                          int *dev_error) {
+                          const float *__restrict__ gsc, const float *h0, float *ht, int T_dense,
+                          int HK, int HV, int *dev_error) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
     unsigned char *smem =
@@ -383,7 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kAbort);
     volatile int *slow_flag = reinterpret_cast<volatile int *>(smem + kSlowFlag);
+    int g_par = 0;  // scalar gate: the parity of the chunk being prepared
     auto gval = [&](int r, int i) -> float {
+        if (SCALAR_G) return reinterpret_cast<const float *>(smem + kG)[64 * g_par + r];
         return *reinterpret_cast<const float *>(smem + kG + g_off(r, i));
     };
     auto kval = [&](uint32_t base, int r, int i) -> float {
@@ -428,18 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&m.k);
         tma_prefetch_desc(&m.q);
-        tma_prefetch_desc(&m.g);
+        if (!SCALAR_G) tma_prefetch_desc(&m.g);
         tma_prefetch_desc(&m.v);
         tma_prefetch_desc(&m.o);
     }
     __syncthreads();
     if (issuer_warp && !issuer_a) {  // first chunk's inputs (warp B issues every TMA load)
-        issue_kqg(smem, m, bar_kqg, b, 0, hk, hv, lane);
+        issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, 0, hk, hv, lane);
         if (lane == 0) issue_v(smem, m, bar_v, b, 0, hv);
     }
-    if (tid < kC)  // beta buffers: [2][64] floats by chunk parity
+    if (tid < kC) {  // beta (and a scalar gate's g) buffers: [2][64] floats by chunk parity
         reinterpret_cast<float *>(smem + kBeta)[tid] =
             tid < min(kC, T) ? beta[(tok0 + tid) * HV + hv] : 0.f;
+        if (SCALAR_G)
+            reinterpret_cast<float *>(smem + kG)[tid] =
+                tid < min(kC, T) ? gsc[(tok0 + tid) * HV + hv] : 0.f;
+    }
     const unsigned long long *tree_anc = reinterpret_cast<const unsigned long long *>(smem + kTreeAnc);
     if (TREE && tid < kC)  // the tree's parents (rows past T: roots)
         reinterpret_cast<int *>(smem + kTreePar)[tid] = tid < T ? parents[(size_t)b * T + tid] : -1;
@@ -503,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t0n = cn * kC, Ln = has_prep ? min(kC, T - t0n) : 0;
         const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
         const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
+        g_par = pn;
         const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
 
         // No block-wide barrier per chunk: the groups meet only at named
@@ -544,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         // the raw k, q, g tiles are consumed: fetch the next chunk's
                         if (!issuer_a && has_next2) {
-                            issue_kqg(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
+                            issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
                             ++issued_kqg;
                         }
                     }
@@ -575,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (has_prep) {
                     named_sync(kBarH4, kHand);
                     if (!issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
-                        issue_kqg(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
+                        issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
                         ++issued_kqg;
                     }
                     if (lane == 0 && !*abort_flag) {
@@ -723,10 +737,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto prefetch_beta = [&]() {
             if (has_next2 && tid < kC) {
                 float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
-                if (t0n + kC + tid < T)
+                float *gdst = reinterpret_cast<float *>(smem + kG + 256 * ((cn + 1) & 1)) + tid;
+                if (t0n + kC + tid < T) {
                     cp_async4(dst, beta + (tok0 + t0n + kC + tid) * HV + hv);
-                else
+                    if (SCALAR_G) cp_async4(gdst, gsc + (tok0 + t0n + kC + tid) * HV + hv);
+                } else {
                     *dst = 0.f;
+                    if (SCALAR_G) *gdst = 0.f;
+                }
             }
         };
         if (!has_scan) prefetch_beta();
@@ -734,7 +752,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool slow = false;
         if (has_prep) {
             wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
-            if (TREE) {
+            if (SCALAR_G) {
+                // one warp: inclusive prefix of the chunk's 64 log-decays (two
+                // per lane, log2 units), in place, and an exact range check
+                // on the two spans around the reference row (G is monotone)
+                int bad = 0;
+                if (warp == 0) {
+                    float *Gp = reinterpret_cast<float *>(smem + kG) + 64 * pn;
+                    const float a = Gp[2 * lane] * kLog2e, a2 = Gp[2 * lane + 1] * kLog2e;
+                    const float pair = a + a2;
+                    float x = pair;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    const float g_even = x - pair + a;
+                    Gp[2 * lane] = g_even;
+                    Gp[2 * lane + 1] = x;
+                    const float g0 = __shfl_sync(0xffffffffu, g_even, 0);
+                    const float gm_e = __shfl_sync(0xffffffffu, g_even, mref >> 1);
+                    const float gm_o = __shfl_sync(0xffffffffu, x, mref >> 1);
+                    const float gl_e = __shfl_sync(0xffffffffu, g_even, (Ln - 1) >> 1);
+                    const float gl_o = __shfl_sync(0xffffffffu, x, (Ln - 1) >> 1);
+                    const float gmv = (mref & 1) ? gm_o : gm_e;
+                    const float glv = ((Ln - 1) & 1) ? gl_o : gl_e;
+                    // each span within half the range: the folded carry factors
+                    // (one span of two neighbouring chunks each) stay above
+                    // exp(-80)
+                    bad = lane == 0 && (g0 - gmv > 0.5f * kRangeLog2 || gmv - glv > 0.5f * kRangeLog2);
+                }
+                slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
+            } else if (TREE) {
                 // log2 units in place, then prefix sums along root paths: one
                 // thread per channel walks the rows in order (parents first)
                 {
@@ -775,9 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
                 // Range check, conservatively per 16-row quarter: the spans it
                 // guards (rows 1..m and m+1..L-1, at most 32 rows) cover at
-                // most three quarters, so no quarter decaying by more than a
-                // third of the range keeps every factor within exp(+-80).
-                const int bad = -x[15] > kRangeLog2 * (1.f / 3.f);
+                // most three quarters, and two in a full chunk.  No quarter
+                // decaying by more than kQuarterLog2 keeps every factor
+                // within exp(+-63) and the folded carry factors of step 1
+                // (four quarters of two full chunks) above exp(-84), inside
+                // the normal float range.
+                const int bad = -x[15] > kQuarterLog2;
                 slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
                 float carry = 0.f;
                 for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
@@ -803,7 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // scanned; the update to the next chunk's S' is
                     //   S'_{c+1} = [exp(G_m') rho] S'_c + [exp(G_m') cL] dS
                     // (G_m' the next chunk's reference row), written over
-                    // chunk c's rho and cL, which nothing else reads
+                    // chunk c's rho and cL, which nothing else reads.  The
+                    // range checks keep both products above exp(-84): fast
+                    // chunks are full here (a ragged chunk is the last one),
+                    // so G_L - G_m spans two quarters of this chunk and G_m'
+                    // two of the next.
                     vec(kRho, ps)[tid] *= egm;
                     vec(kCL, ps)[tid] *= egm;
                 }
@@ -837,12 +893,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kqo = (uint32_t)((c8 >> 3) * 8192 + r * 128 + (((c8 & 7) ^ r8) << 4));
                 unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kqo), kv);
                 unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kqo), qv);
-                const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
-                const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
-                const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
-                gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
-                gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
-                if (!slow && !TREE) {
+                if (SCALAR_G) {
+                    const float gr = gval(r, 0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gv[e] = gr;
+                } else {
+                    const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
+                    const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
+                    const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
+                    gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
+                    gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
+                }
+                if (SCALAR_G && !slow) {
+                    const float gmr = gval(mref, 0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gm[e] = gmr;
+                } else if (!slow && !TREE) {
                     // G at the reference row, from the G tile (a tree's
                     // reference is its start, G_m = 0)
                     const float4 m_lo = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch));
@@ -854,7 +920,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 8; ++e) gm[e] = 0.f;
                 }
                 float lk[8], lq[8], rr[8];
-                if (!slow) {
+                if (!slow && SCALAR_G) {
+                    // one decay per row: two exponentials for the 8 channels
+                    const float d = gv[0] - gm[0];
+                    const float2 el = make_float2(fast_exp2(d), fast_exp2(d));
+                    const float2 er = make_float2(fast_exp2(-d), fast_exp2(-d));
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 kk = make_float2(kv[e], kv[e + 1]);
+                        const float2 a = __fmul2_rn(kk, el);
+                        const float2 bq = __fmul2_rn(make_float2(qv[e], qv[e + 1]), el);
+                        const float2 cr = __fmul2_rn(kk, er);
+                        lk[e] = a.x; lk[e + 1] = a.y;
+                        lq[e] = bq.x; lq[e + 1] = bq.y;
+                        rr[e] = cr.x; rr[e + 1] = cr.y;
+                    }
+                } else if (!slow) {
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {  // packed fp32 pairs
                         const float2 d = __fadd2_rn(make_float2(gv[e], gv[e + 1]),
@@ -1097,16 +1178,19 @@ bool encode_maps(EncodeTiledFn fn, TileMaps *tm, const Problem &p, size_t tok0, 
     const char *v = static_cast<const char *>(p.v) + tok0 * p.HV * kD * 2;
     const char *g = reinterpret_cast<const char *>(p.g) + tok0 * p.HV * kD * 4;
     const char *o = static_cast<const char *>(p.out) + tok0 * p.HV * kD * 2;
+    // a scalar gate's g is read without a tensor map
+    if (p.g_scalar) memset(&tm->g, 0, sizeof(tm->g));
     return encode_map(fn, &tm->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
            encode_map(fn, &tm->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
-           encode_map(fn, &tm->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, p.HV, 32) &&
+           (p.g_scalar ||
+            encode_map(fn, &tm->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, p.HV, 32)) &&
            encode_map(fn, &tm->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 64) &&
            // output: unswizzled [16 tokens][32 channels] boxes, one per state warp
            encode_map(fn, &tm->o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE, 16);
 }
 
-template <bool VARLEN, bool TREE>
+template <bool VARLEN, bool TREE, bool SCALAR_G>
 cudaError_t launch_tc(const Problem &p, const TileMaps &tm, const TileMaps *seq_maps,
                       const int4 *seqs, const int *parents, long long blocks, int *dev_error,
                       cudaStream_t stream) {
@@ -1117,17 +1201,17 @@ cudaError_t launch_tc(const Problem &p, const TileMaps &tm, const TileMaps *seq_
         if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
         kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(
-            tm, seq_maps, seqs, parents, p.beta, p.h0, p.ht, p.T, p.HK, p.HV, dev_error);
+            tm, seq_maps, seqs, parents, p.beta, p.g, p.h0, p.ht, p.T, p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };
     if (TREE)  // outputs only
-        return p.h0 ? run(gdr_prefill_tc_kernel<true, false, false, true>)
-                    : run(gdr_prefill_tc_kernel<false, false, false, true>);
-    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN, false>);
-    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN, false>);
-    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN, false>);
-    return run(gdr_prefill_tc_kernel<false, false, VARLEN, false>);
+        return p.h0 ? run(gdr_prefill_tc_kernel<true, false, false, true, false>)
+                    : run(gdr_prefill_tc_kernel<false, false, false, true, false>);
+    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN, false, SCALAR_G>);
+    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN, false, SCALAR_G>);
+    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN, false, SCALAR_G>);
+    return run(gdr_prefill_tc_kernel<false, false, VARLEN, false, SCALAR_G>);
 }
 
 }  // namespace
@@ -1138,8 +1222,10 @@ cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t str
     if (e != cudaSuccess) return e;
     TileMaps tm;
     if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
-    return launch_tc<false, false>(p, tm, nullptr, nullptr, nullptr, (long long)p.B * p.HV,
-                                   dev_error, stream);
+    return p.g_scalar ? launch_tc<false, false, true>(p, tm, nullptr, nullptr, nullptr,
+                                                      (long long)p.B * p.HV, dev_error, stream)
+                      : launch_tc<false, false, false>(p, tm, nullptr, nullptr, nullptr,
+                                                       (long long)p.B * p.HV, dev_error, stream);
 }
 
 size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
@@ -1158,8 +1244,11 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
                                      int nseq, int *dev_error, cudaStream_t stream) {
     TileMaps unused;
     memset(&unused, 0, sizeof(unused));
-    return launch_tc<true, false>(p, unused, static_cast<const TileMaps *>(seq_maps), seqs,
-                                  nullptr, (long long)nseq * p.HV, dev_error, stream);
+    const TileMaps *maps = static_cast<const TileMaps *>(seq_maps);
+    return p.g_scalar ? launch_tc<true, false, true>(p, unused, maps, seqs, nullptr,
+                                                     (long long)nseq * p.HV, dev_error, stream)
+                      : launch_tc<true, false, false>(p, unused, maps, seqs, nullptr,
+                                                      (long long)nseq * p.HV, dev_error, stream);
 }
 
 cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
@@ -1172,8 +1261,9 @@ cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
     if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
     Problem outputs_only = p;
     outputs_only.ht = nullptr;
-    return launch_tc<false, true>(outputs_only, tm, nullptr, nullptr, parents,
-                                  (long long)p.B * p.HV, dev_error, stream);
+    if (p.g_scalar) return cudaErrorInvalidValue;  // trees with a scalar gate: CUDA cores
+    return launch_tc<false, true, false>(outputs_only, tm, nullptr, nullptr, parents,
+                                         (long long)p.B * p.HV, dev_error, stream);
 }
 
 }  // namespace gdr

@@ -64,8 +64,11 @@ WORKLOADS = {
 
 
 def draw(B, T, HK, HV, dk, dv, dtype=torch.float32, h0=True, seed=0, g_mu=0.0, g_sigma=1.0,
-         beta_mu=0.0, beta_sigma=1.0, h0_scale=0.3, device="cpu", generator=None):
-    """Draws one problem.  Returns a dict q, k, v, g, beta, h0 (h0 may be None)."""
+         beta_mu=0.0, beta_sigma=1.0, h0_scale=0.3, device="cpu", generator=None,
+         scalar_gate=False):
+    """Draws one problem.  Returns a dict q, k, v, g, beta, h0 (h0 may be None).
+    g is [B, T, HV, dk], or [B, T, HV] (one log-decay per token and head) with
+    scalar_gate."""
     if generator is None:
         generator = torch.Generator(device=device)
         generator.manual_seed(seed)
@@ -73,7 +76,7 @@ def draw(B, T, HK, HV, dk, dv, dtype=torch.float32, h0=True, seed=0, g_mu=0.0, g
     q = torch.randn(B, T, HK, dk, **f32)
     k = torch.randn(B, T, HK, dk, **f32)
     v = torch.randn(B, T, HV, dv, **f32)
-    g_raw = torch.randn(B, T, HV, dk, **f32)
+    g_raw = torch.randn(*((B, T, HV) if scalar_gate else (B, T, HV, dk)), **f32)
     b_raw = torch.randn(B, T, HV, **f32)
     s0 = torch.randn(B, HV, dk, dv, **f32) if h0 else None
     q = torch.nn.functional.normalize(q, dim=-1)

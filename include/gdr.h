@@ -78,9 +78,20 @@ typedef enum gdr_dtype {
     GDR_BF16 = 1  /* q, k, v, out are bfloat16; g, beta, h0, ht stay float32 */
 } gdr_dtype;
 
-/* Flags for gdr_forward_ex (test and diagnosis use; 0 in normal calls). */
+/* Flags for gdr_forward_ex and the other entries that take them (0 in normal
+ * calls; the first two are for tests and diagnosis). */
 #define GDR_FLAG_FORCE_CHUNKED 1u /* run the chunked prefill even when T == 1 */
 #define GDR_FLAG_FORCE_GENERIC 2u /* use the CUDA-core prefill even where the tensor-core one applies */
+/*
+ * Scalar gate: g holds one log-decay per token and value head, [B][T][HV]
+ * float32 (varlen: [total][HV]), applied to every key channel -- the gated
+ * delta rule with a per-head decay, the case the review thread of "Support
+ * TreeUpdateSolve kernel" (trymirai/uzu PR #576) discusses for a per-key-head
+ * gram.  Accepted by gdr_forward_ex, gdr_workspace_bytes, gdr_forward_varlen,
+ * gdr_varlen_workspace_bytes, gdr_forward_tree and gdr_tree_workspace_bytes
+ * (trees with a scalar gate run on the CUDA-core route).
+ */
+#define GDR_FLAG_SCALAR_GATE 4u
 
 /*
  * Bytes of device workspace gdr_forward_ex needs for this call (0 when the
