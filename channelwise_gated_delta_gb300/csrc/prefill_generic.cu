@@ -54,6 +54,68 @@ struct ChunkLayout {
     }
 };
 
+// ---- 3xTF32 warp products: an f32 x is split exactly into a
+// tf32 head (x with its 13 low mantissa bits cleared) and the f32 rest
+// x - head; a product is head*head + head*rest + rest*head, the rest*rest
+// term (~2^-22 relative) dropped, and the tensor core reads the rest's top
+// 19 bits.  m16n8k8 fragments (g = lane / 4, t = lane % 4): A holds
+// (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B (t, g), (t + 4, g); the
+// accumulator (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = __float_as_uint(x) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32_acc(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The split A fragment of a 16 x 8 block at (m0, k0): element (row, col) at
+// A[row * lda + col] (or, TRANS_A, at A[col * lda + row]), times sign.
+template <bool TRANS_A>
+__device__ __forceinline__ void load_a3(uint32_t (&ah)[4], uint32_t (&al)[4], const float *A,
+                                        int lda, int m0, int k0, float sign, int g, int t) {
+    auto a_at = [&](int r, int c) {
+        return TRANS_A ? A[(k0 + c) * lda + m0 + r] : A[(m0 + r) * lda + k0 + c];
+    };
+    split_tf32(sign * a_at(g, t), ah[0], al[0]);
+    split_tf32(sign * a_at(g + 8, t), ah[1], al[1]);
+    split_tf32(sign * a_at(g, t + 4), ah[2], al[2]);
+    split_tf32(sign * a_at(g + 8, t + 4), ah[3], al[3]);
+}
+
+// acc (16 x 8) += A B for one k-step of 8 with a split A fragment; B element
+// (k, n) at B[k * ldb + n] (or, TRANS_B, at B[n * ldb + k]).
+template <bool TRANS_B>
+__device__ __forceinline__ void mma3_b(float (&acc)[4], const uint32_t (&ah)[4],
+                                       const uint32_t (&al)[4], const float *B, int ldb, int k0,
+                                       int n0, int g, int t) {
+    auto b_at = [&](int k, int n) {
+        return TRANS_B ? B[(n0 + n) * ldb + k0 + k] : B[(k0 + k) * ldb + n0 + n];
+    };
+    uint32_t bh0, bl0, bh1, bl1;
+    split_tf32(b_at(t, g), bh0, bl0);
+    split_tf32(b_at(t + 4, g), bh1, bl1);
+    mma_tf32_acc(acc, al, bh0, bh1);
+    mma_tf32_acc(acc, ah, bl0, bl1);
+    mma_tf32_acc(acc, ah, bh0, bh1);
+}
+
+// acc (16 x 8 tile) += sign * A[16 x 8] B[8 x 8] with the 3xTF32 split.
+template <bool TRANS_A>
+__device__ __forceinline__ void mma3_step(float (&acc)[4], const float *A, int lda, int m0, int k0,
+                                          const float *B, int ldb, int n0, float sign, int g,
+                                          int t) {
+    uint32_t ah[4], al[4];
+    load_a3<TRANS_A>(ah, al, A, lda, m0, k0, sign, g, t);
+    mma3_b<false>(acc, ah, al, B, ldb, k0, n0, g, t);
+}
+
 // TREE: the T <= C tokens of each (b, hv) are a draft-token tree given by
 // parents[b][t] (-1 for a root, else an earlier token), solved as one chunk:
 // prefix sums run along root paths and the ancestor relation replaces the
@@ -67,7 +129,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                    const int2 *__restrict__ chunks, const int *__restrict__ parents, int T,
                    int HK, int HV, int dk, int dv, int C, int NC, int g_scalar) {
     extern __shared__ float smem[];
-    const int ldk = dk + 1;  // padded rows: threads walking s hit distinct banks
+    const int ldk = dk + 4;  // padded rows: a warp's fragment loads hit distinct banks
     const int ldw = dk + dv;
     float *Ks = smem;               // [C][ldk]
     float *Qs = Ks + C * ldk;       // [C][ldk]
@@ -75,7 +137,11 @@ __global__ void __launch_bounds__(kPrepThreads)
     float *As = Gs + C * ldk;       // [C][C]
     float *Ws = As + C * C;         // [C][dk + dv]
     float *bs = Ws + C * ldw;       // [C]
-    int *par = reinterpret_cast<int *>(bs + C);                          // [C] (TREE)
+    float *gmv = bs + C;            // [dk] G at the reference row
+    float *egm = gmv + dk;          // [dk] exp(G_m)
+    float *clv = egm + dk;          // [dk] exp(G_L - G_m)
+    float *glv = clv + dk;          // [dk] G_L
+    int *par = reinterpret_cast<int *>(glv + dk);                        // [C] (TREE)
     unsigned long long *anc = reinterpret_cast<unsigned long long *>(
         reinterpret_cast<uintptr_t>(par + C + 1) & ~(uintptr_t)7);     // [C] (TREE)
 
@@ -156,34 +222,110 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     __syncthreads();
 
-    // Causal key/key (A, beta-folded, strictly lower) and query/key (P) terms.
+    // Reference-row factorisation (as in the tensor-core kernel): with m the
+    // middle row of the chunk (a tree: its start, G_m = 0),
+    //   A = tril(diag(beta) Lk R^T),  P = tril(Lq R^T),
+    //   Lk = K e^{G - G_m}, Lq = Q e^{G - G_m}, R = K e^{G_m - G},
+    // the decay leaves the dot products and A and P become 3xTF32 warp
+    // products.  Taken when every factor stays within e^{80} (the spans
+    // around m decay by at most 80 nats in every channel); otherwise A and P
+    // come from the exact pairwise decays below.
+    const int m = TREE ? -1 : (L - 1) / 2;
+    bool in_range = true;
+    if (tid < dk) {
+        const int i = tid;
+        const float gm = m < 0 ? 0.f : Gs[m * ldk + i];
+        const float gl = Gs[(L - 1) * ldk + i];
+        gmv[i] = gm;
+        glv[i] = gl;
+        egm[i] = expf(gm);
+        clv[i] = expf(gl - gm);
+        if (TREE) {
+            float gmin = 0.f;
+            for (int r = 0; r < L; ++r) gmin = fminf(gmin, Gs[r * ldk + i]);
+            in_range = -gmin <= 80.f;
+        } else {
+            in_range = Gs[i] - gm <= 80.f && gm - gl <= 80.f;
+        }
+    }
+    const bool fast = __syncthreads_and(in_range) != 0;
     float *Pg = rec + lay.p();
-    for (int idx = tid; idx < C * C; idx += kPrepThreads) {
-        const int r = idx / C, s = idx % C;
-        // s is an earlier token r depends on: s <= r, or in a tree s == r or
-        // an ancestor of r
-        const bool below = TREE ? (s < r && ((anc[r] >> s) & 1ull)) : s < r;
-        float a = 0.f, pp = 0.f;
-        if ((below || s == r) && r < L) {
-            const float *kr = Ks + r * ldk, *ks = Ks + s * ldk, *qr = Qs + r * ldk;
-            const float *gr = Gs + r * ldk, *gs = Gs + s * ldk;
-            for (int i = 0; i < dk; ++i) {
-                const float e = expf(gr[i] - gs[i]);
-                const float kse = ks[i] * e;
-                a = fmaf(kr[i], kse, a);
-                pp = fmaf(qr[i], kse, pp);
+    const int lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    if (fast) {
+        // in place: Gs <- Lk, Qs <- Lq, Ks <- R
+        for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
+            const int r = idx / dk, i = idx % dk;
+            const float d = Gs[r * ldk + i] - gmv[i];
+            const float up = expf(d), down = expf(-d);
+            const float kv = Ks[r * ldk + i];
+            Gs[r * ldk + i] = kv * up;
+            Qs[r * ldk + i] *= up;
+            Ks[r * ldk + i] = kv * down;
+        }
+        __syncthreads();
+        // warp w: row tile w / 2 of A (w even) or P (w odd), every column
+        // tile up to the diagonal block
+        const int mt = warp >> 1;
+        if (16 * mt < C) {
+            const bool is_p = warp & 1;
+            const float *Lx = is_p ? Qs : Gs;
+            const int m0 = 16 * mt, ntn = 2 * mt + 2;
+            float acc[8][4];
+#pragma unroll
+            for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            for (int k0 = 0; k0 < dk; k0 += 8) {
+                uint32_t ah[4], al[4];
+                load_a3<false>(ah, al, Lx, ldk, m0, k0, 1.f, g8, t4);
+#pragma unroll
+                for (int n = 0; n < 8; ++n)
+                    if (n < ntn) mma3_b<true>(acc[n], ah, al, Ks, ldk, k0, 8 * n, g8, t4);
+            }
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                if (n >= ntn) continue;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = m0 + g8 + 8 * (e >> 1), sc = 8 * n + 2 * t4 + (e & 1);
+                    const bool below = TREE ? (sc < r && ((anc[r] >> sc) & 1ull)) : sc < r;
+                    if (is_p)
+                        Pg[r * C + sc] = ((below || sc == r) && r < L) ? acc[n][e] : 0.f;
+                    else
+                        As[r * C + sc] = (below && r < L) ? bs[r] * acc[n][e] : 0.f;
+                }
             }
         }
-        As[r * C + s] = below ? bs[r] * a : 0.f;
-        Pg[idx] = pp;
+    } else {
+        // exact pairwise decays, every exponent <= 0
+        for (int idx = tid; idx < C * C; idx += kPrepThreads) {
+            const int r = idx / C, s = idx % C;
+            // s is an earlier token r depends on: s <= r, or in a tree s == r
+            // or an ancestor of r
+            const bool below = TREE ? (s < r && ((anc[r] >> s) & 1ull)) : s < r;
+            float a = 0.f, pp = 0.f;
+            if ((below || s == r) && r < L) {
+                const float *kr = Ks + r * ldk, *ks = Ks + s * ldk, *qr = Qs + r * ldk;
+                const float *gr = Gs + r * ldk, *gs = Gs + s * ldk;
+                for (int i = 0; i < dk; ++i) {
+                    const float e = expf(gr[i] - gs[i]);
+                    const float kse = ks[i] * e;
+                    a = fmaf(kr[i], kse, a);
+                    pp = fmaf(qr[i], kse, pp);
+                }
+            }
+            As[r * C + s] = below ? bs[r] * a : 0.f;
+            Pg[idx] = pp;
+        }
     }
-    // Right-hand sides of the WY solve: diag(beta) [exp(G) * K | V].
+    // Right-hand sides of the WY solve: diag(beta) [exp(G) * K | V]
+    // (exp(G) K = Lk exp(G_m) on the factored path).
     for (int idx = tid; idx < C * ldw; idx += kPrepThreads) {
         const int r = idx / ldw, col = idx % ldw;
         float x = 0.f;
         if (r < L) {
             if (col < dk) {
-                x = bs[r] * Ks[r * ldk + col] * expf(Gs[r * ldk + col]);
+                x = fast ? bs[r] * Gs[r * ldk + col] * egm[col]
+                         : bs[r] * Ks[r * ldk + col] * expf(Gs[r * ldk + col]);
             } else {
                 const size_t tv = (tr0 + r) * HV + hv;
                 x = bs[r] * to_f32(v[tv * dv + (col - dk)]);
@@ -206,39 +348,53 @@ __global__ void __launch_bounds__(kPrepThreads)
     __syncthreads();
 
     // Scan operands: Wk, Wv, Qt = exp(G) Q, Kh = exp(G_L - G) K, gam = exp(G_L)
-    // (a tree has no last token to carry the state to: no Kh, gam).
-    const float *gl = Gs + (L - 1) * ldk;
+    // (a tree has no last token to carry the state to: no Kh, gam).  On the
+    // factored path Qs holds Lq and Ks holds R: Qt = Lq exp(G_m) and
+    // Kh = R exp(G_L - G_m).
     for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
         const int r = idx / dk, i = idx % dk;
-        const float gri = Gs[r * ldk + i];
         rec[lay.wk() + idx] = Ws[r * ldw + i];
-        rec[lay.qt() + idx] = Qs[r * ldk + i] * expf(gri);
-        if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(gl[i] - gri) : 0.f;
+        if (fast) {
+            rec[lay.qt() + idx] = Qs[r * ldk + i] * egm[i];
+            if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * clv[i] : 0.f;
+        } else {
+            const float gri = Gs[r * ldk + i];
+            rec[lay.qt() + idx] = Qs[r * ldk + i] * expf(gri);
+            if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(glv[i] - gri) : 0.f;
+        }
     }
     for (int idx = tid; idx < C * dv; idx += kPrepThreads) {
         const int r = idx / dv, j = idx % dv;
         rec[lay.wv() + idx] = Ws[r * ldw + dk + j];
     }
     if (!TREE)
-        for (int i = tid; i < dk; i += kPrepThreads) rec[lay.gam() + i] = expf(gl[i]);
+        for (int i = tid; i < dk; i += kPrepThreads) rec[lay.gam() + i] = expf(glv[i]);
 }
 
 // TREE: one chunk (the tree), outputs only: no state update, no ht.
+//
+// Shared-memory rows are padded so that the fragment loads of a warp fall in
+// distinct banks: A operands by 4 floats (dk + 4, C + 4), B operands to 40
+// (32 columns + 8).  Per chunk, with 8 warps: U = Wv - Wk S (4 x 4 tiles,
+// warp w: row tile w / 2, column tiles 2 (w % 2) and +1), O = Qt S + P U
+// (same tiles), then S = diag(gam) S + Kh^T U (8 x 4 tiles, warp w: row
+// tile w, all four column tiles).
 template <typename Tin, bool TREE>
 __global__ void __launch_bounds__(kScanThreads)
     gdr_chunk_scan(const float *__restrict__ ws, const float *h0, Tin *__restrict__ out,
                    float *ht, const int4 *__restrict__ seqs, int T_dense, int HV, int dk, int dv,
                    int C, int NC_dense) {
     extern __shared__ float smem[];
-    const int ldk = dk + 1;
-    const int ldc = C + 1;
-    float *Ss = smem;                    // [dk][BV]   state tile
-    float *Wk = Ss + dk * kScanBV;       // [C][ldk]
-    float *Qt = Wk + C * ldk;            // [C][ldk]
-    float *Kh = Qt + C * ldk;            // [C][ldk]
-    float *Ps = Kh + C * ldk;            // [C][ldc]
-    float *Us = Ps + C * ldc;            // [C][BV]
-    float *Wv = Us + C * kScanBV;        // [C][BV]
+    constexpr int ldb = kScanBV + 8;     // B-operand rows (S, U)
+    const int lda = dk + 4;              // A-operand rows over dk (Wk, Qt, Kh)
+    const int ldp = C + 4;               // P rows
+    float *Ss = smem;                    // [dk][ldb]  state tile
+    float *Wk = Ss + dk * ldb;           // [C][lda]
+    float *Qt = Wk + C * lda;            // [C][lda]
+    float *Kh = Qt + C * lda;            // [C][lda]
+    float *Ps = Kh + C * lda;            // [C][ldp]
+    float *Us = Ps + C * ldp;            // [C][ldb]
+    float *Wv = Us + C * ldb;            // [C][BV]
     float *gam = Wv + C * kScanBV;       // [dk]
 
     const int ntile = dv / kScanBV;
@@ -262,87 +418,140 @@ __global__ void __launch_bounds__(kScanThreads)
     const int NC = (T + C - 1) / C;
     const size_t head_idx = (size_t)slot * HV + hv;  // state slot
     const int j0 = tile * kScanBV;
-    const int tid = threadIdx.x;
-    const int jj = tid % kScanBV;        // column within the tile
-    const int rr = tid / kScanBV;        // 0..7
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
     const ChunkLayout lay{C, dk, dv};
 
     for (int idx = tid; idx < dk * kScanBV; idx += kScanThreads) {
         const int i = idx / kScanBV, j = idx % kScanBV;
-        Ss[idx] = h0 ? h0[(head_idx * dk + i) * dv + j0 + j] : 0.f;
+        Ss[i * ldb + j] = h0 ? h0[(head_idx * dk + i) * dv + j0 + j] : 0.f;
     }
 
     for (int c = 0; c < NC; ++c) {
         const float *rec = ws + (rec0 + (size_t)c * rec_step) * lay.floats();
         const int t0 = c * C;
         const int L = min(C, T - t0);
-        for (int idx = tid; idx < C * dk; idx += kScanThreads) {
-            const int r = idx / dk, i = idx % dk;
-            Wk[r * ldk + i] = rec[lay.wk() + idx];
-            Qt[r * ldk + i] = rec[lay.qt() + idx];
-            if (!TREE) Kh[r * ldk + i] = rec[lay.kh() + idx];
+        // the chunk's record, 16 bytes at a time (every part starts on a
+        // multiple of 4 floats)
+        const int dk4 = dk / 4;
+        for (int idx = tid; idx < C * dk4; idx += kScanThreads) {
+            const int r = idx / dk4, i = 4 * (idx % dk4);
+            *reinterpret_cast<float4 *>(Wk + r * lda + i) =
+                *reinterpret_cast<const float4 *>(rec + lay.wk() + r * dk + i);
+            *reinterpret_cast<float4 *>(Qt + r * lda + i) =
+                *reinterpret_cast<const float4 *>(rec + lay.qt() + r * dk + i);
+            if (!TREE)
+                *reinterpret_cast<float4 *>(Kh + r * lda + i) =
+                    *reinterpret_cast<const float4 *>(rec + lay.kh() + r * dk + i);
         }
-        for (int idx = tid; idx < C * C; idx += kScanThreads)
-            Ps[(idx / C) * ldc + idx % C] = rec[lay.p() + idx];
-        for (int idx = tid; idx < C * kScanBV; idx += kScanThreads) {
-            const int r = idx / kScanBV, j = idx % kScanBV;
-            Wv[idx] = rec[lay.wv() + (size_t)r * dv + j0 + j];
+        for (int idx = tid; idx < C * C / 4; idx += kScanThreads) {
+            const int r = (4 * idx) / C, s4 = (4 * idx) % C;
+            *reinterpret_cast<float4 *>(Ps + r * ldp + s4) =
+                *reinterpret_cast<const float4 *>(rec + lay.p() + r * C + s4);
+        }
+        for (int idx = tid; idx < C * kScanBV / 4; idx += kScanThreads) {
+            const int r = (4 * idx) / kScanBV, j = (4 * idx) % kScanBV;
+            *reinterpret_cast<float4 *>(Wv + r * kScanBV + j) =
+                *reinterpret_cast<const float4 *>(rec + lay.wv() + (size_t)r * dv + j0 + j);
         }
         if (!TREE)
             for (int i = tid; i < dk; i += kScanThreads) gam[i] = rec[lay.gam() + i];
         __syncthreads();
 
-        // U = Wv - Wk S0
-        for (int r = rr; r < C; r += kScanThreads / kScanBV) {
-            float acc = Wv[r * kScanBV + jj];
-            const float *w = Wk + r * ldk;
-            for (int i = 0; i < dk; ++i) acc = fmaf(-w[i], Ss[i * kScanBV + jj], acc);
-            Us[r * kScanBV + jj] = acc;
+        // U = Wv - Wk S0 (rows past L are zero: Wk and Wv are)
+        const int um0 = 16 * (warp >> 1);
+        if (um0 < C) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = 8 * (2 * (warp & 1) + nt);
+                float acc[4] = {Wv[(um0 + g) * kScanBV + n0 + 2 * t],
+                                Wv[(um0 + g) * kScanBV + n0 + 2 * t + 1],
+                                Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t],
+                                Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t + 1]};
+                for (int k0 = 0; k0 < dk; k0 += 8)
+                    mma3_step<false>(acc, Wk, lda, um0, k0, Ss, ldb, n0, -1.f, g, t);
+                Us[(um0 + g) * ldb + n0 + 2 * t] = acc[0];
+                Us[(um0 + g) * ldb + n0 + 2 * t + 1] = acc[1];
+                Us[(um0 + g + 8) * ldb + n0 + 2 * t] = acc[2];
+                Us[(um0 + g + 8) * ldb + n0 + 2 * t + 1] = acc[3];
+            }
         }
         __syncthreads();
 
-        // O = Qt S0 + P U
-        for (int r = rr; r < L; r += kScanThreads / kScanBV) {
-            float acc = 0.f;
-            const float *qrow = Qt + r * ldk;
-            for (int i = 0; i < dk; ++i) acc = fmaf(qrow[i], Ss[i * kScanBV + jj], acc);
-            const float *prow = Ps + r * ldc;
-            for (int s = 0; s <= r; ++s) acc = fmaf(prow[s], Us[s * kScanBV + jj], acc);
-            out[((tok0 + t0 + r) * HV + hv) * dv + j0 + jj] = from_f32<Tin>(acc);
+        // O = Qt S0 + P U (P is zero above the diagonal and off a tree's
+        // ancestors), rows below L stored
+        if (um0 < C) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = 8 * (2 * (warp & 1) + nt);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k0 = 0; k0 < dk; k0 += 8)
+                    mma3_step<false>(acc, Qt, lda, um0, k0, Ss, ldb, n0, 1.f, g, t);
+                for (int k0 = 0; k0 < um0 + 16; k0 += 8)
+                    mma3_step<false>(acc, Ps, ldp, um0, k0, Us, ldb, n0, 1.f, g, t);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = um0 + g + 8 * h;
+                    if (r < L) {
+                        Tin *o = out + ((tok0 + t0 + r) * HV + hv) * dv + j0 + n0 + 2 * t;
+                        o[0] = from_f32<Tin>(acc[2 * h]);
+                        o[1] = from_f32<Tin>(acc[2 * h + 1]);
+                    }
+                }
+            }
         }
 
         if (TREE) break;  // one chunk; no state to carry
-        // S = diag(gam) S0 + Kh^T U   (new values kept in registers until
-        // every thread is done reading S0)
-        float snew[128 / (kScanThreads / kScanBV)];
-        int n = 0;
-        for (int i = rr; i < dk; i += kScanThreads / kScanBV, ++n) {
-            float acc = gam[i] * Ss[i * kScanBV + jj];
-            for (int r = 0; r < L; ++r) acc = fmaf(Kh[r * ldk + i], Us[r * kScanBV + jj], acc);
-            snew[n] = acc;
+        // S = diag(gam) S0 + Kh^T U (rows of Kh and U past L are zero), kept
+        // in registers until every warp is done reading S0
+        float sacc[8][4];
+        const int sm0 = 16 * warp;
+        const bool s_rows = sm0 < dk;
+        if (s_rows) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int n0 = 8 * nt;
+                const float ga = gam[sm0 + g], gb = gam[sm0 + g + 8];
+                sacc[nt][0] = ga * Ss[(sm0 + g) * ldb + n0 + 2 * t];
+                sacc[nt][1] = ga * Ss[(sm0 + g) * ldb + n0 + 2 * t + 1];
+                sacc[nt][2] = gb * Ss[(sm0 + g + 8) * ldb + n0 + 2 * t];
+                sacc[nt][3] = gb * Ss[(sm0 + g + 8) * ldb + n0 + 2 * t + 1];
+                for (int k0 = 0; k0 < L; k0 += 8)
+                    mma3_step<true>(sacc[nt], Kh, lda, sm0, k0, Us, ldb, n0, 1.f, g, t);
+            }
         }
         __syncthreads();
-        n = 0;
-        for (int i = rr; i < dk; i += kScanThreads / kScanBV, ++n) Ss[i * kScanBV + jj] = snew[n];
+        if (s_rows) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int n0 = 8 * nt;
+                Ss[(sm0 + g) * ldb + n0 + 2 * t] = sacc[nt][0];
+                Ss[(sm0 + g) * ldb + n0 + 2 * t + 1] = sacc[nt][1];
+                Ss[(sm0 + g + 8) * ldb + n0 + 2 * t] = sacc[nt][2];
+                Ss[(sm0 + g + 8) * ldb + n0 + 2 * t + 1] = sacc[nt][3];
+            }
+        }
         __syncthreads();
     }
 
     if (!TREE && ht) {
         for (int idx = tid; idx < dk * kScanBV; idx += kScanThreads) {
             const int i = idx / kScanBV, j = idx % kScanBV;
-            ht[(head_idx * dk + i) * dv + j0 + j] = Ss[idx];
+            ht[(head_idx * dk + i) * dv + j0 + j] = Ss[i * ldb + j];
         }
     }
 }
 
 size_t prep_smem_bytes(int dk, int dv, int C) {
     // floats, then (trees) C parent indices and C 8-byte ancestor masks
-    return sizeof(float) * ((size_t)3 * C * (dk + 1) + (size_t)C * C + (size_t)C * (dk + dv) + C) +
+    return sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * C + (size_t)C * (dk + dv) + C +
+                            (size_t)4 * dk) +
            sizeof(int) * (C + 2) + sizeof(unsigned long long) * C;
 }
 size_t scan_smem_bytes(int dk, int C) {
-    return sizeof(float) * ((size_t)dk * kScanBV + (size_t)3 * C * (dk + 1) + (size_t)C * (C + 1) +
-                            (size_t)2 * C * kScanBV + dk);
+    const size_t ldb = kScanBV + 8;
+    return sizeof(float) * ((size_t)dk * ldb + (size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
+                            (size_t)C * ldb + (size_t)C * kScanBV + dk);
 }
 
 // Dense batches: chunks == seqs == nullptr, B x T from p.  Packed batches:

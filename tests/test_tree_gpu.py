@@ -90,9 +90,10 @@ def test_tree_slow_decay_beta_near_one():
 
 
 @pytest.mark.parametrize("T,chunk", [(16, 16), (30, 32), (64, 64)])
-def test_chain_tree_equals_chunked_sequence_bitwise(T, chunk):
-    """A chain is a sequence: same kernels, same arithmetic, same bits as the
-    CUDA-core chunked route over one chunk."""
+def test_chain_tree_equals_chunked_sequence(T, chunk):
+    """A chain is a sequence: the tree route and the CUDA-core chunked route
+    over one chunk agree to float32 rounding (they factor the decay around
+    different reference rows: the tree's start and the chunk's middle)."""
     d = draw(2, T, 1, 2, 64, 64, dtype=torch.float32, seed=14)
     c = to_cuda(d)
     tree = gdr_forward_tree(c["q"], c["k"], c["v"], c["g"], c["beta"],
@@ -100,7 +101,7 @@ def test_chain_tree_equals_chunked_sequence_bitwise(T, chunk):
     seq, _ = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=chunk,
                          flags=GDR_FLAG_FORCE_CHUNKED | GDR_FLAG_FORCE_GENERIC)
     gdr_device_check()
-    assert torch.equal(tree, seq)
+    assert (tree - seq).abs().max().item() <= 1e-5 * seq.abs().max().item()
 
 
 def test_bad_trees_rejected():
