@@ -75,6 +75,18 @@ __device__ __forceinline__ void mma_tf32_acc(float (&c)[4], const uint32_t (&a)[
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
+// of this thread's copies.
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_copies() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // The split A fragment of a 16 x 8 block at (m0, k0): element (row, col) at
 // A[row * lda + col] (or, TRANS_A, at A[col * lda + row]), times sign.
 template <bool TRANS_A>
@@ -129,13 +141,13 @@ __global__ void __launch_bounds__(kPrepThreads)
                    const int2 *__restrict__ chunks, const int *__restrict__ parents, int T,
                    int HK, int HV, int dk, int dv, int C, int NC, int g_scalar) {
     extern __shared__ float smem[];
-    const int ldk = dk + 4;  // padded rows: a warp's fragment loads hit distinct banks
-    const int ldw = dk + dv;
+    // padded rows: a warp's fragment loads hit distinct banks
+    const int ldk = dk + 4, lda = C + 4, ldw = dk + dv + 8;
     float *Ks = smem;               // [C][ldk]
     float *Qs = Ks + C * ldk;       // [C][ldk]
     float *Gs = Qs + C * ldk;       // [C][ldk]
-    float *As = Gs + C * ldk;       // [C][C]
-    float *Ws = As + C * C;         // [C][dk + dv]
+    float *As = Gs + C * ldk;       // [C][lda]
+    float *Ws = As + C * lda;       // [C][ldw]: dk + dv columns used
     float *bs = Ws + C * ldw;       // [C]
     float *gmv = bs + C;            // [dk] G at the reference row
     float *egm = gmv + dk;          // [dk] exp(G_m)
@@ -172,20 +184,30 @@ __global__ void __launch_bounds__(kPrepThreads)
     const ChunkLayout lay{C, dk, dv};
     float *rec = ws + rec_idx * lay.floats();
 
-    // Load the chunk (rows >= L are zero; a zero gate keeps G flat there).
-    for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
-        const int r = idx / dk, i = idx % dk;
-        float kv = 0.f, qv = 0.f, gv = 0.f;
-        if (r < L) {
-            const size_t tk = (tr0 + r) * HK + hk;
-            kv = to_f32(k[tk * dk + i]);
-            qv = to_f32(q[tk * dk + i]);
-            // a scalar gate has one log-decay per token and head
-            gv = g_scalar ? g[(tr0 + r) * HV + hv] : g[((tr0 + r) * HV + hv) * dk + i];
+    // Load the chunk, four elements per access, several accesses in flight
+    // per thread (rows >= L are zero; a zero gate keeps G flat there).
+    {
+        const int dk4 = dk / 4;
+#pragma unroll 4
+        for (int idx = tid; idx < C * dk4; idx += kPrepThreads) {
+            const int r = idx / dk4, i = 4 * (idx % dk4);
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv, gv = kv;
+            if (r < L) {
+                const size_t tk = (tr0 + r) * HK + hk;
+                kv = load4(k + tk * dk + i);
+                qv = load4(q + tk * dk + i);
+                // a scalar gate has one log-decay per token and head
+                if (g_scalar) {
+                    const float x = g[(tr0 + r) * HV + hv];
+                    gv = make_float4(x, x, x, x);
+                } else {
+                    gv = load4(g + ((tr0 + r) * HV + hv) * dk + i);
+                }
+            }
+            *reinterpret_cast<float4 *>(Ks + r * ldk + i) = kv;
+            *reinterpret_cast<float4 *>(Qs + r * ldk + i) = qv;
+            *reinterpret_cast<float4 *>(Gs + r * ldk + i) = gv;
         }
-        Ks[r * ldk + i] = kv;
-        Qs[r * ldk + i] = qv;
-        Gs[r * ldk + i] = gv;
     }
     for (int r = tid; r < C; r += kPrepThreads)
         bs[r] = r < L ? beta[(tr0 + r) * HV + hv] : 0.f;
@@ -291,7 +313,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                     if (is_p)
                         Pg[r * C + sc] = ((below || sc == r) && r < L) ? acc[n][e] : 0.f;
                     else
-                        As[r * C + sc] = (below && r < L) ? bs[r] * acc[n][e] : 0.f;
+                        As[r * lda + sc] = (below && r < L) ? bs[r] * acc[n][e] : 0.f;
                 }
             }
         }
@@ -313,39 +335,76 @@ __global__ void __launch_bounds__(kPrepThreads)
                     pp = fmaf(qr[i], kse, pp);
                 }
             }
-            As[r * C + s] = below ? bs[r] * a : 0.f;
+            As[r * lda + s] = below ? bs[r] * a : 0.f;
             Pg[idx] = pp;
         }
     }
     // Right-hand sides of the WY solve: diag(beta) [exp(G) * K | V]
     // (exp(G) K = Lk exp(G_m) on the factored path).
-    for (int idx = tid; idx < C * ldw; idx += kPrepThreads) {
-        const int r = idx / ldw, col = idx % ldw;
+    const int nw = dk + dv;
+    for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
+        const int r = idx / dk, col = idx % dk;
         float x = 0.f;
-        if (r < L) {
-            if (col < dk) {
-                x = fast ? bs[r] * Gs[r * ldk + col] * egm[col]
-                         : bs[r] * Ks[r * ldk + col] * expf(Gs[r * ldk + col]);
-            } else {
-                const size_t tv = (tr0 + r) * HV + hv;
-                x = bs[r] * to_f32(v[tv * dv + (col - dk)]);
+        if (r < L)
+            x = fast ? bs[r] * Gs[r * ldk + col] * egm[col]
+                     : bs[r] * Ks[r * ldk + col] * expf(Gs[r * ldk + col]);
+        Ws[r * ldw + col] = x;
+    }
+    {
+        const int dv4 = dv / 4;
+#pragma unroll 4
+        for (int idx = tid; idx < C * dv4; idx += kPrepThreads) {
+            const int r = idx / dv4, j = 4 * (idx % dv4);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < L) {
+                x = load4(v + ((tr0 + r) * HV + hv) * dv + j);
+                const float br = bs[r];
+                x.x *= br; x.y *= br; x.z *= br; x.w *= br;
             }
+            *reinterpret_cast<float4 *>(Ws + r * ldw + dk + j) = x;
         }
-        Ws[idx] = x;
     }
     __syncthreads();
 
-    // (I + A) W = RHS by forward substitution; the columns are independent,
-    // so each thread owns whole columns and walks the rows in order.
-    for (int col = tid; col < ldw; col += kPrepThreads) {
-        for (int r = 1; r < L; ++r) {
-            float acc = Ws[r * ldw + col];
-            const float *ar = As + r * C;
-            for (int s = 0; s < r; ++s) acc = fmaf(-ar[s], Ws[s * ldw + col], acc);
-            Ws[r * ldw + col] = acc;
+    // (I + A) W = RHS, block by block of 16 rows: first the rows' update by
+    // the blocks already solved, W_I -= A_IJ W_J (J < I), as 3xTF32 warp
+    // products (warp w: column tiles 4w .. 4w + 3 of the dk + dv columns),
+    // then the unit-lower 16 x 16 diagonal block by forward substitution, one
+    // column per thread.  Rows past L have zero right-hand sides and zero
+    // rows of A, so their W stays zero.
+    for (int I = 0; 16 * I < L; ++I) {
+        const int r0 = 16 * I;
+        if (I > 0) {
+            for (int nt = 4 * warp; nt < 4 * warp + 4 && 8 * nt < nw; ++nt) {
+                const int n0 = 8 * nt;
+                float acc[4] = {Ws[(r0 + g8) * ldw + n0 + 2 * t4],
+                                Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1],
+                                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4],
+                                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1]};
+                for (int k0 = 0; k0 < r0; k0 += 8)
+                    mma3_step<false>(acc, As, lda, r0, k0, Ws, ldw, n0, -1.f, g8, t4);
+                Ws[(r0 + g8) * ldw + n0 + 2 * t4] = acc[0];
+                Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1] = acc[1];
+                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4] = acc[2];
+                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1] = acc[3];
+            }
+            __syncthreads();
         }
+        for (int col = tid; col < nw; col += kPrepThreads) {
+            float w[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) w[r] = Ws[(r0 + r) * ldw + col];
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                const float *ar = As + (r0 + r) * lda + r0;
+#pragma unroll
+                for (int q = 0; q < r; ++q) w[r] = fmaf(-ar[q], w[q], w[r]);
+            }
+#pragma unroll
+            for (int r = 1; r < 16; ++r) Ws[(r0 + r) * ldw + col] = w[r];
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
     // Scan operands: Wk, Wv, Qt = exp(G) Q, Kh = exp(G_L - G) K, gam = exp(G_L)
     // (a tree has no last token to carry the state to: no Kh, gam).  On the
@@ -363,9 +422,10 @@ __global__ void __launch_bounds__(kPrepThreads)
             if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(glv[i] - gri) : 0.f;
         }
     }
-    for (int idx = tid; idx < C * dv; idx += kPrepThreads) {
-        const int r = idx / dv, j = idx % dv;
-        rec[lay.wv() + idx] = Ws[r * ldw + dk + j];
+    for (int idx = tid; idx < C * dv / 4; idx += kPrepThreads) {
+        const int r = (4 * idx) / dv, j = (4 * idx) % dv;
+        *reinterpret_cast<float4 *>(rec + lay.wv() + r * dv + j) =
+            *reinterpret_cast<const float4 *>(Ws + r * ldw + dk + j);
     }
     if (!TREE)
         for (int i = tid; i < dk; i += kPrepThreads) rec[lay.gam() + i] = expf(glv[i]);
@@ -431,31 +491,26 @@ __global__ void __launch_bounds__(kScanThreads)
         const float *rec = ws + (rec0 + (size_t)c * rec_step) * lay.floats();
         const int t0 = c * C;
         const int L = min(C, T - t0);
-        // the chunk's record, 16 bytes at a time (every part starts on a
-        // multiple of 4 floats)
+        // the chunk's record, 16-byte asynchronous copies all in flight at
+        // once (every part starts on a multiple of 4 floats)
         const int dk4 = dk / 4;
         for (int idx = tid; idx < C * dk4; idx += kScanThreads) {
             const int r = idx / dk4, i = 4 * (idx % dk4);
-            *reinterpret_cast<float4 *>(Wk + r * lda + i) =
-                *reinterpret_cast<const float4 *>(rec + lay.wk() + r * dk + i);
-            *reinterpret_cast<float4 *>(Qt + r * lda + i) =
-                *reinterpret_cast<const float4 *>(rec + lay.qt() + r * dk + i);
-            if (!TREE)
-                *reinterpret_cast<float4 *>(Kh + r * lda + i) =
-                    *reinterpret_cast<const float4 *>(rec + lay.kh() + r * dk + i);
+            cp_async16(Wk + r * lda + i, rec + lay.wk() + r * dk + i);
+            cp_async16(Qt + r * lda + i, rec + lay.qt() + r * dk + i);
+            if (!TREE) cp_async16(Kh + r * lda + i, rec + lay.kh() + r * dk + i);
         }
         for (int idx = tid; idx < C * C / 4; idx += kScanThreads) {
             const int r = (4 * idx) / C, s4 = (4 * idx) % C;
-            *reinterpret_cast<float4 *>(Ps + r * ldp + s4) =
-                *reinterpret_cast<const float4 *>(rec + lay.p() + r * C + s4);
+            cp_async16(Ps + r * ldp + s4, rec + lay.p() + r * C + s4);
         }
         for (int idx = tid; idx < C * kScanBV / 4; idx += kScanThreads) {
             const int r = (4 * idx) / kScanBV, j = (4 * idx) % kScanBV;
-            *reinterpret_cast<float4 *>(Wv + r * kScanBV + j) =
-                *reinterpret_cast<const float4 *>(rec + lay.wv() + (size_t)r * dv + j0 + j);
+            cp_async16(Wv + r * kScanBV + j, rec + lay.wv() + (size_t)r * dv + j0 + j);
         }
         if (!TREE)
-            for (int i = tid; i < dk; i += kScanThreads) gam[i] = rec[lay.gam() + i];
+            for (int i = 4 * tid; i < dk; i += 4 * kScanThreads) cp_async16(gam + i, rec + lay.gam() + i);
+        cp_async_wait_all_copies();
         __syncthreads();
 
         // U = Wv - Wk S0 (rows past L are zero: Wk and Wv are)
@@ -544,8 +599,8 @@ __global__ void __launch_bounds__(kScanThreads)
 
 size_t prep_smem_bytes(int dk, int dv, int C) {
     // floats, then (trees) C parent indices and C 8-byte ancestor masks
-    return sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * C + (size_t)C * (dk + dv) + C +
-                            (size_t)4 * dk) +
+    return sizeof(float) * ((size_t)3 * C * (dk + 4) + (size_t)C * (C + 4) +
+                            (size_t)C * (dk + dv + 8) + C + (size_t)4 * dk) +
            sizeof(int) * (C + 2) + sizeof(unsigned long long) * C;
 }
 size_t scan_smem_bytes(int dk, int C) {
