@@ -83,7 +83,12 @@ constexpr int kBarAux = 7;                  // solver warps only (64)
 constexpr int kBarSolve = 8;                // solvers -> issuers: T' complete (128)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
-constexpr float kQuarterLog2 = 21.f * kLog2e;  // per-quarter decay limit of the fast path
+// Fast-path decay limits: a 16-row quarter within a third of the range keeps
+// the operand factors within exp(+-80); a half chunk (two quarters) within
+// 43 nats keeps the folded carry factors, which span the second half of one
+// chunk and the first half of the next, above exp(-86), in the normal range.
+constexpr float kQuarterLog2 = kRangeLog2 * (1.f / 3.f);
+constexpr float kHalfLog2 = 43.f * kLog2e;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
@@ -750,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!has_scan) prefetch_beta();
         // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
         bool slow = false;
+        int half_bad = 0;  // a half chunk decays by more than kHalfLog2 (channelwise)
         if (has_prep) {
             wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
             if (SCALAR_G) {
@@ -777,10 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float gl_o = __shfl_sync(0xffffffffu, x, (Ln - 1) >> 1);
                     const float gmv = (mref & 1) ? gm_o : gm_e;
                     const float glv = ((Ln - 1) & 1) ? gl_o : gl_e;
-                    // each span within half the range: the folded carry factors
-                    // (one span of two neighbouring chunks each) stay above
-                    // exp(-80)
-                    bad = lane == 0 && (g0 - gmv > 0.5f * kRangeLog2 || gmv - glv > 0.5f * kRangeLog2);
+                    // each span within kHalfLog2: the factors within exp(+-43),
+                    // the folded carry factors above exp(-86)
+                    bad = lane == 0 && (g0 - gmv > kHalfLog2 || gmv - glv > kHalfLog2);
                 }
                 slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
             } else if (TREE) {
@@ -824,13 +829,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (qq < 3) sTot[qq * 128 + i] = x[15];
                 // Range check, conservatively per 16-row quarter: the spans it
                 // guards (rows 1..m and m+1..L-1, at most 32 rows) cover at
-                // most three quarters, and two in a full chunk.  No quarter
-                // decaying by more than kQuarterLog2 keeps every factor
-                // within exp(+-63) and the folded carry factors of step 1
-                // (four quarters of two full chunks) above exp(-84), inside
-                // the normal float range.
+                // most three quarters.  The half-chunk check (quarters 0-1,
+                // 2-3, which contain the spans of a full chunk and the first
+                // span of any) is reduced in the next barrier.
                 const int bad = -x[15] > kQuarterLog2;
                 slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
+                if (qq & 1) half_bad = -(sTot[(qq - 1) * 128 + i] + x[15]) > kHalfLog2;
                 float carry = 0.f;
                 for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
 #pragma unroll
@@ -840,8 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r + 1, i)) = v.y;
                 }
             }
+            slow = (named_sync_or(kBarCompute, kCompute, half_bad) != 0) || slow;
             if (tid == 0) slow_flag[pn] = slow ? 1 : 0;  // read by the issuers and the solvers
-            csync();
             if (tid < kD) {
                 // the fallback factorises around the chunk start (G_m = 0) and
                 // stores R with the full decay to the chunk end (scale 1)
