@@ -168,16 +168,20 @@ GDR_API gdr_status gdr_forward_chunked_noalloc(const void *q, const void *k, con
  * (page-locked for the copies to run asynchronously; pageable memory works
  * but each copy then waits for the host).  Nothing in the pages corresponds
  * to it: it is the input/output path of a caller whose tensors live on the
- * host.  The batch streams through two device slots in `staging` (device
- * memory of gdr_host_staging_bytes(...) bytes, 256-byte aligned): while
- * batch element b computes on `stream`, element b + 1 is copied in and
- * element b - 1 copied out on two library-owned streams, so the copies in
- * both directions overlap the compute.  Ordered after earlier work on
- * `stream`; later work on `stream` starts after the last copy out.  Results
- * equal those of gdr_forward on the same values bit for bit.  Calls from
- * several host threads are serialised while they enqueue.  Errors as
- * gdr_forward_ex (GDR_ERR_WORKSPACE for a short staging buffer); a failure
- * after the first copy leaves the outputs partly written.
+ * host.  Each batch element is streamed in segments of whole chunks (2048
+ * tokens when T > 4096, else the whole sequence), each segment resuming from
+ * the state the previous one left in a device state buffer, through two
+ * device slots in `staging` (device memory of gdr_host_staging_bytes(...)
+ * bytes, 256-byte aligned): while one segment computes on `stream`, the next
+ * is copied in and the previous one copied out on two library-owned streams,
+ * so the copies in both directions overlap the compute.  Ordered after
+ * earlier work on `stream`; later work on `stream` starts after the last
+ * copy out.  Up to T = 4096 the results equal those of gdr_forward on the
+ * same values bit for bit; beyond, they differ by the rounding of the state
+ * handed from segment to segment.  Calls from several host threads are
+ * serialised while they enqueue.  Errors as gdr_forward_ex
+ * (GDR_ERR_WORKSPACE for a short staging buffer); a failure after the first
+ * copy leaves the outputs partly written.
  */
 GDR_API size_t gdr_host_staging_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
                                       int qkv_dtype);

@@ -86,3 +86,31 @@ def test_host_entry_back_to_back_calls():
         c = {n: t.cuda() for n, t in d.items()}
         out, ht = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=64)
         assert torch.equal(o, out.cpu()) and torch.equal(h, ht.cpu())
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_host_entry_segments_long_sequences(dtype, d):
+    """Sequences longer than two segments (4096 tokens) are streamed in
+    segments that resume from the state the previous one left: the result is
+    the recurrence's, to the route's tolerance, and within float32 rounding of
+    the unsegmented device call."""
+    import oracle
+    from channelwise_gated_delta_gb300.inputs import to_f64
+    from tests.parity_util import assert_close
+    d_ = draw(2, 4500, 1, 2, d, d, dtype=dtype, seed=11)
+    host = {n: pinned(d_[n]) for n in ("q", "k", "v", "g", "beta", "h0")}
+    out_h = torch.empty(2, 4500, 2, d, dtype=dtype).pin_memory()
+    ht_h = torch.empty(2, 2, d, d).pin_memory()
+    gdr_forward_host(host["q"], host["k"], host["v"], host["g"], host["beta"], host["h0"], out_h,
+                     ht_h, chunk=64)
+    torch.cuda.current_stream().synchronize()
+    gdr_device_check()
+    ref_o, ref_h = oracle.recurrence(*(to_f64(d_[n]) for n in ("q", "k", "v", "g", "beta")),
+                                     to_f64(d_["h0"]))
+    assert_close("o", out_h, ref_o, dtype)
+    assert_close("ht", ht_h, ref_h, dtype)
+    c = {n: t.cuda() for n, t in d_.items()}
+    out, ht = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=64)
+    tol = 1e-2 if dtype == torch.bfloat16 else 1e-5
+    assert (out_h.float() - out.cpu().float()).abs().max() <= tol * out.float().abs().max().cpu()
+    assert (ht_h - ht.cpu()).abs().max() <= tol * ht.abs().max().cpu()
