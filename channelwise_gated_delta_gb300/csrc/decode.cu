@@ -17,6 +17,7 @@
 // reduced with warp shuffles across the four row groups of a warp, then
 // across warps through shared memory.
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace gdr {
 namespace {
@@ -147,6 +148,200 @@ __global__ void __launch_bounds__(2 * DK)
     if (tid < 8) store4(out + head * dv + col, o);
 }
 
+// ---- dk = dv = 128: persistent, the 64 KB state of a head moved by bulk copies.
+//
+// One CTA per SM (256 threads) walks heads blockIdx.x, + gridDim.x, ...
+// through three shared-memory buffers: the state of head n + 2 and its k, q,
+// v rows are loading (one cp.async.bulk each, counted on the buffer's
+// mbarrier) while head n computes and the bulk store of head n - 1 drains.
+// Thread (j, h) owns column j and rows 64 h .. 64 h + 63: it keeps its 64
+// decayed entries in registers through the prediction, updates them, and
+// writes them back to the buffer for the output sum and the store.
+constexpr int kBulkD = 128;
+constexpr int kBulkThreads = 256;
+constexpr int kBulkBufs = 3;
+constexpr uint32_t kBulkStateBytes = kBulkD * kBulkD * 4;
+constexpr uint32_t kBulkVecBytes = 4 * kBulkD * 4;   // k, q, v, g rows (room for f32)
+constexpr uint32_t kBulkBufBytes = kBulkStateBytes + kBulkVecBytes;
+constexpr uint64_t kBulkWaitNs = 2000000000ull;  // 2 s
+
+template <typename Tin, bool HAS_H0, bool STORE_HT, bool ROWS, bool GS>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    gdr_decode_bulk_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                           const Tin *__restrict__ v, const float *__restrict__ g,
+                           const float *__restrict__ beta, const float *h0,
+                           Tin *__restrict__ out, float *ht, const int2 *__restrict__ rows, int HK,
+                           int HV, int nheads, int *dev_error) {
+    extern __shared__ float4 smem_f4[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(smem_f4);
+    float *red = reinterpret_cast<float *>(base + kBulkBufs * kBulkBufBytes);  // [2][128]
+    float *gam = red + 2 * kBulkD;                                               // exp(g) [128]
+    float *kf = gam + kBulkD;                                                    // k as f32 [128]
+    float *qf = kf + kBulkD;                                                     // q as f32 [128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qf + kBulkD);                 // [kBulkBufs]
+    const int tid = threadIdx.x, j = tid & (kBulkD - 1), half = tid >> 7;
+    constexpr uint32_t es = sizeof(Tin);
+
+    // token row, state slot and key head of the CTA's n-th head
+    auto head_of = [&](int n, size_t &head, size_t &shead, size_t &krow) {
+        const int head_idx = blockIdx.x + n * gridDim.x;
+        const int hv = head_idx % HV, b = head_idx / HV;
+        int trow = b;
+        head = (size_t)head_idx;
+        shead = head;
+        if (ROWS) {
+            const int2 r = rows[b];
+            trow = r.x;
+            head = (size_t)r.x * HV + hv;
+            shead = (size_t)r.y * HV + hv;
+        }
+        krow = (size_t)trow * HK + hv / (HV / HK);
+    };
+    auto buf = [&](int n) { return base + (n % kBulkBufs) * kBulkBufBytes; };
+    // thread 0: the loads of the CTA's n-th head into its buffer
+    auto issue = [&](int n) {
+        size_t head, shead, krow;
+        head_of(n, head, shead, krow);
+        unsigned char *bp = buf(n);
+        uint64_t *bar = bars + n % kBulkBufs;
+        const uint32_t bytes = (HAS_H0 ? kBulkStateBytes : 0u) + 3 * kBulkD * es +
+                               (GS ? 0u : kBulkD * 4u);
+        sm100::mbar_arrive_expect_tx(bar, bytes);
+        if (HAS_H0) sm100::bulk_load_1d(bp, h0 + shead * kBulkD * kBulkD, kBulkStateBytes, bar);
+        unsigned char *vp = bp + kBulkStateBytes;
+        sm100::bulk_load_1d(vp, k + krow * kBulkD, kBulkD * es, bar);
+        sm100::bulk_load_1d(vp + 512, q + krow * kBulkD, kBulkD * es, bar);
+        sm100::bulk_load_1d(vp + 1024, v + head * kBulkD, kBulkD * es, bar);
+        if (!GS) sm100::bulk_load_1d(vp + 1536, g + head * kBulkD, kBulkD * 4u, bar);
+    };
+    const int my = blockIdx.x < nheads ? (nheads - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (tid == 0) {
+        for (int i = 0; i < kBulkBufs; ++i) sm100::mbar_init(bars + i, 1);
+        sm100::fence_mbar_init();
+        for (int n = 0; n < kBulkBufs - 1 && n < my; ++n) issue(n);
+    }
+    __syncthreads();
+
+    // beta (and a scalar gate's g) of the next head are read one head ahead,
+    // so that their latency hides behind a head's work
+    float bt_next = 0.f, gs_next = 0.f;
+    if (my > 0) {
+        size_t head, shead, krow;
+        head_of(0, head, shead, krow);
+        bt_next = beta[head];
+        if (GS) gs_next = g[head];
+    }
+    int n = 0;
+    for (; n < my; ++n) {
+        if (tid == 0 && n + kBulkBufs - 1 < my) {
+            // the buffer of head n + 2 last held head n - 1: its store must
+            // have read it
+            sm100::bulk_wait_read_all();
+            issue(n + kBulkBufs - 1);
+        }
+        size_t head, shead, krow;
+        head_of(n, head, shead, krow);
+        const float bt = bt_next, gs = gs_next;
+        if (n + 1 < my) {
+            size_t h1, s1, k1;
+            head_of(n + 1, h1, s1, k1);
+            bt_next = beta[h1];
+            if (GS) gs_next = g[h1];
+        }
+        const bool ok = __syncthreads_and(
+            sm100::mbar_wait_bounded(bars + n % kBulkBufs, (uint32_t)((n / kBulkBufs) & 1),
+                                     kBulkWaitNs)) != 0;
+        if (!ok) {
+            if (tid == 0) atomicOr(dev_error, 1);
+            break;
+        }
+        float *S = reinterpret_cast<float *>(buf(n));
+        const Tin *kv = reinterpret_cast<const Tin *>(buf(n) + kBulkStateBytes);
+        const Tin *qv = reinterpret_cast<const Tin *>(buf(n) + kBulkStateBytes + 512);
+        const Tin *vv = reinterpret_cast<const Tin *>(buf(n) + kBulkStateBytes + 1024);
+        // per row, once: the decay exp(g) and k, q as f32
+        if (tid < kBulkD) {
+            gam[tid] = expf(GS ? gs
+                               : reinterpret_cast<const float *>(buf(n) + kBulkStateBytes + 1536)[tid]);
+            kf[tid] = to_f32(kv[tid]);
+            qf[tid] = to_f32(qv[tid]);
+        }
+        __syncthreads();
+        // pass 1: decayed entries kept in registers, partial prediction
+        float s[64];
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            const int i = 64 * half + r;
+            const float x = HAS_H0 ? S[i * kBulkD + j] * gam[i] : 0.f;
+            s[r] = x;
+            acc = fmaf(kf[i], x, acc);
+        }
+        red[half * kBulkD + j] = acc;
+        __syncthreads();
+        const float u = bt * (to_f32(vv[j]) - (red[j] + red[kBulkD + j]));
+        __syncthreads();  // both halves have read red before it is reused
+        // pass 2: rank-one update, output partials, the tile back in the buffer
+        float o = 0.f;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            const int i = 64 * half + r;
+            const float x = fmaf(kf[i], u, s[r]);
+            o = fmaf(qf[i], x, o);
+            if (STORE_HT) S[i * kBulkD + j] = x;
+        }
+        red[half * kBulkD + j] = o;
+        if (STORE_HT) sm100::fence_async_smem();  // generic writes, before the bulk store reads
+        __syncthreads();
+        if (tid < kBulkD) out[head * kBulkD + tid] = from_f32<Tin>(red[tid] + red[kBulkD + tid]);
+        if (STORE_HT && tid == 0) {
+            sm100::bulk_store_1d(ht + shead * kBulkD * kBulkD, S, kBulkStateBytes);
+            sm100::bulk_commit_group();
+        }
+        __syncthreads();  // red is free again
+    }
+    if (tid == 0) {
+        sm100::bulk_wait_all();
+        // after a timeout at head n, never leave with loads in flight into
+        // this CTA: heads n .. n + 2 may have been issued
+        for (int m = n; m < my && m < n + kBulkBufs; ++m)
+            sm100::mbar_wait_bounded(bars + m % kBulkBufs, (uint32_t)((m / kBulkBufs) & 1),
+                                     kBulkWaitNs);
+    }
+}
+
+template <typename Tin, bool ROWS, bool GS>
+cudaError_t launch_decode_bulk(const Problem &p, const int2 *rows, cudaStream_t stream) {
+    const long long nheads = (long long)p.B * p.HV;
+    if (nheads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int grid = (int)(nheads < sms ? nheads : sms);
+    const size_t smem = kBulkBufs * kBulkBufBytes + 5 * kBulkD * sizeof(float) + 8 * kBulkBufs;
+    const Tin *q = static_cast<const Tin *>(p.q), *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    Tin *out = static_cast<Tin *>(p.out);
+    auto run = [&](auto kernel) -> cudaError_t {
+        cudaError_t err2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem);
+        if (err2 != cudaSuccess) return err2;
+        trace_begin(kKernDecode, stream);
+        kernel<<<grid, kBulkThreads, smem, stream>>>(q, k, v, p.g, p.beta, p.h0, out, p.ht, rows,
+                                                     p.HK, p.HV, (int)nheads, err);
+        trace_end(kKernDecode, stream);
+        return cudaGetLastError();
+    };
+    if (p.h0 && p.ht) return run(gdr_decode_bulk_kernel<Tin, true, true, ROWS, GS>);
+    if (p.h0) return run(gdr_decode_bulk_kernel<Tin, true, false, ROWS, GS>);
+    if (p.ht) return run(gdr_decode_bulk_kernel<Tin, false, true, ROWS, GS>);
+    return run(gdr_decode_bulk_kernel<Tin, false, false, ROWS, GS>);
+}
+
 template <typename Tin, int DK, bool ROWS, bool GS>
 cudaError_t launch_decode_t(const Problem &p, const int2 *rows, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.HV * (p.dv / kDecodeBV);
@@ -174,6 +369,7 @@ cudaError_t launch_decode_t(const Problem &p, const int2 *rows, cudaStream_t str
 
 template <typename Tin, bool ROWS, bool GS>
 cudaError_t launch_decode_d(const Problem &p, const int2 *rows, cudaStream_t stream) {
+    if (p.dk == kBulkD && p.dv == kBulkD) return launch_decode_bulk<Tin, ROWS, GS>(p, rows, stream);
     switch (p.dk) {
         case 32: return launch_decode_t<Tin, 32, ROWS, GS>(p, rows, stream);
         case 64: return launch_decode_t<Tin, 64, ROWS, GS>(p, rows, stream);
