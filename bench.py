@@ -42,8 +42,9 @@ DECODE = "decode_b64"
 # with the sha256 of the source file the capture was taken from: a kernel
 # whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
-    # decode B64: one launch, --set full capture (136.3 MB read + 74.1 MB written)
-    "gdr_decode_kernel": {"bytes": 210_429_000, "sha": "d3c4f4c4ffad7955"},
+    # decode B64: one launch of the persistent bulk-copy kernel, --set full
+    # capture (136.4 MB read + 74.2 MB written)
+    "gdr_decode_kernel": {"bytes": 210_509_000, "sha": "5f7ea947d98305b5"},
     # prefill_t16k: one launch, --set full capture (2.165 GB read + 0.521 GB written)
     "gdr_prefill_fused": {"bytes": 2_686_430_000, "sha": "a8e9ecbf981a3f54"},
 }
