@@ -364,6 +364,17 @@ def cpu_baseline(w):
                       "recurrence, %.1f s of oracle time" % (w.B, w.HV, w.T, total_s)}
 
 
+def prefill_config(w, ws):
+    """The workload the headline metric is quoted on (both arms report it)."""
+    return {"workload": "prefill B4 T16384 HK16 HV32 dk=dv=128 chunk64, bf16 q/k/v, f32 "
+                        "g/beta/state, beta=sigmoid(N(2,0.5)), g=-softplus(N(-3,1)), "
+                        "h0=0.3N(0,1)",
+            "B": w.B, "T": w.T, "HK": w.HK, "HV": w.HV, "dk": w.dk, "dv": w.dv,
+            "chunk": w.chunk, "l2": "inputs 2.7 GB > L2 (no flush); decode rotates 4 "
+                                    "state sets (537 MB)",
+            "parallelism": "replicas" if ws > 1 else "single"}
+
+
 def run_reference(args):
     """Reference arm: the fp64 oracle on the host cores, same metric and unit.
     Each step is one batch element of the workload (all value heads, all tokens)."""
@@ -385,8 +396,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * total_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "HK": w.HK,
-                       "HV": w.HV, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
+            "config": prefill_config(w, args.gpus),
             "cpu_baseline": {"value": round(tok_s, 3), "unit": "tokens/s", "cores": used,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(tok_s, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -433,13 +443,7 @@ def main():
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(pre["ms"] / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill B4 T16384 HK16 HV32 dk=dv=128 chunk64, bf16 q/k/v, f32 "
-                               "g/beta/state, beta=sigmoid(N(2,0.5)), g=-softplus(N(-3,1)), "
-                               "h0=0.3N(0,1)",
-                   "B": w.B, "T": w.T, "HK": w.HK, "HV": w.HV, "dk": w.dk, "dv": w.dv,
-                   "chunk": w.chunk, "l2": "inputs 2.7 GB > L2 (no flush); decode rotates 4 "
-                                           "state sets (537 MB)",
-                   "parallelism": "replicas" if ws > 1 else "single"},
+        "config": prefill_config(w, ws),
         "roofline": roofline(dom[0], dom[1][0], dom[1][1], bytes_launch, hbm_peak, peak_kind),
         "kernels": {k: {"launches": v[0], "ms_total": round(v[1], 3)} for k, v in trace.items()},
         "gpu_launches": sum(v[0] for v in trace.values()),
