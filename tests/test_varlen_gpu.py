@@ -139,3 +139,42 @@ def test_bad_cu_seqlens_rejected():
     with pytest.raises(ValueError):  # last offset != number of rows
         gdr_forward_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], [0, 4, 9], h0=c["h0"],
                            chunk=16)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_many_sequences_random_lengths(dtype, d):
+    """257 sequences of random lengths 0..70 (tables of hundreds of entries,
+    many single-token rows): bit for bit the per-sequence calls, and the
+    oracle on a sample of sequences."""
+    gen = torch.Generator()
+    gen.manual_seed(20)
+    lengths = [int(x) for x in torch.randint(0, 71, (257,), generator=gen)]
+    lengths[3] = 1
+    lengths[4] = 0
+    seqs = draw_seqs(lengths, 1, 2, d, d, dtype, seed=21)
+    out, ht, cu = run_varlen(seqs, 64)
+    outs_1, hts_1 = run_each(seqs, 64)
+    for n in range(len(seqs)):
+        assert torch.equal(out[:, cu[n]:cu[n + 1]], outs_1[n]), n
+        assert torch.equal(ht[n:n + 1], hts_1[n]), n
+    for n in (0, 3, 4, 100, 256):
+        d_ = seqs[n]
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d_[x]) for x in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d_["h0"]))
+        assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, dtype)
+        assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_all_single_tokens_equal_dense_decode(dtype):
+    """64 one-token sequences packed: the decode kernel through its row table
+    gives the dense decode's bits."""
+    d = draw(64, 1, 16, 32, 128, 128, dtype=dtype, seed=22)
+    c = to_cuda(d)
+    dense_o, dense_h = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"])
+    flat = lambda x: x.reshape(1, 64, *x.shape[2:]).contiguous()
+    out, ht = gdr_forward_varlen(flat(c["q"]), flat(c["k"]), flat(c["v"]), flat(c["g"]),
+                                 flat(c["beta"]), list(range(65)), h0=c["h0"])
+    gdr_device_check()
+    assert torch.equal(out.reshape(dense_o.shape), dense_o)
+    assert torch.equal(ht, dense_h)
