@@ -118,15 +118,37 @@ __device__ __forceinline__ void mma3_b(float (&acc)[4], const uint32_t (&ah)[4],
     mma_tf32_acc(acc, ah, bh0, bh1);
 }
 
-// acc (16 x 8 tile) += sign * A[16 x 8] B[8 x 8] with the 3xTF32 split.
-template <bool TRANS_A>
-__device__ __forceinline__ void mma3_step(float (&acc)[4], const float *A, int lda, int m0, int k0,
-                                          const float *B, int ldb, int n0, float sign, int g,
-                                          int t) {
-    uint32_t ah[4], al[4];
-    load_a3<TRANS_A>(ah, al, A, lda, m0, k0, sign, g, t);
-    mma3_b<false>(acc, ah, al, B, ldb, k0, n0, g, t);
+// NT adjacent 16 x 8 tiles of one row block: acc[n] += sign * A[m0.., 0..kend)
+// B[0..kend, nbase + 8 n ..].  k runs outermost, so the A fragment is split
+// once per k-step for all NT tiles, and the head*head products and the two
+// correction products go to separate accumulators: 2 NT independent chains
+// instead of one per tile.
+template <int NT, bool TRANS_A>
+__device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], const float *A, int lda, int m0,
+                                          int kend, const float *B, int ldb, int nbase,
+                                          float sign, int g, int t) {
+    float cor[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) cor[n][0] = cor[n][1] = cor[n][2] = cor[n][3] = 0.f;
+    for (int k0 = 0; k0 < kend; k0 += 8) {
+        uint32_t ah[4], al[4];
+        load_a3<TRANS_A>(ah, al, A, lda, m0, k0, sign, g, t);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(B[(k0 + t) * ldb + nbase + 8 * n + g], bh0, bl0);
+            split_tf32(B[(k0 + t + 4) * ldb + nbase + 8 * n + g], bh1, bl1);
+            mma_tf32_acc(cor[n], al, bh0, bh1);
+            mma_tf32_acc(cor[n], ah, bl0, bl1);
+            mma_tf32_acc(acc[n], ah, bh0, bh1);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] += cor[n][e];
 }
+
 
 // TREE: the T <= C tokens of each (b, hv) are a draft-token tree given by
 // parents[b][t] (-1 for a root, else an earlier token), solved as one chunk:
@@ -375,18 +397,28 @@ __global__ void __launch_bounds__(kPrepThreads)
     for (int I = 0; 16 * I < L; ++I) {
         const int r0 = 16 * I;
         if (I > 0) {
-            for (int nt = 4 * warp; nt < 4 * warp + 4 && 8 * nt < nw; ++nt) {
-                const int n0 = 8 * nt;
-                float acc[4] = {Ws[(r0 + g8) * ldw + n0 + 2 * t4],
-                                Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1],
-                                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4],
-                                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1]};
-                for (int k0 = 0; k0 < r0; k0 += 8)
-                    mma3_step<false>(acc, As, lda, r0, k0, Ws, ldw, n0, -1.f, g8, t4);
-                Ws[(r0 + g8) * ldw + n0 + 2 * t4] = acc[0];
-                Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1] = acc[1];
-                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4] = acc[2];
-                Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1] = acc[3];
+            // warp w: column tiles 4w .. 4w + 3 (all four exist whenever the
+            // first does: dk + dv is a multiple of 32)
+            const int nbase = 32 * warp;
+            if (nbase < nw) {
+                float acc[4][4];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int n0 = nbase + 8 * nt;
+                    acc[nt][0] = Ws[(r0 + g8) * ldw + n0 + 2 * t4];
+                    acc[nt][1] = Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1];
+                    acc[nt][2] = Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4];
+                    acc[nt][3] = Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1];
+                }
+                mma3_rows<4, false>(acc, As, lda, r0, r0, Ws, ldw, nbase, -1.f, g8, t4);
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int n0 = nbase + 8 * nt;
+                    Ws[(r0 + g8) * ldw + n0 + 2 * t4] = acc[nt][0];
+                    Ws[(r0 + g8) * ldw + n0 + 2 * t4 + 1] = acc[nt][1];
+                    Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4] = acc[nt][2];
+                    Ws[(r0 + g8 + 8) * ldw + n0 + 2 * t4 + 1] = acc[nt][3];
+                }
             }
             __syncthreads();
         }
@@ -514,21 +546,25 @@ __global__ void __launch_bounds__(kScanThreads)
         __syncthreads();
 
         // U = Wv - Wk S0 (rows past L are zero: Wk and Wv are)
-        const int um0 = 16 * (warp >> 1);
+        const int um0 = 16 * (warp >> 1), unb = 16 * (warp & 1);
         if (um0 < C) {
+            float acc[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const int n0 = 8 * (2 * (warp & 1) + nt);
-                float acc[4] = {Wv[(um0 + g) * kScanBV + n0 + 2 * t],
-                                Wv[(um0 + g) * kScanBV + n0 + 2 * t + 1],
-                                Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t],
-                                Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t + 1]};
-                for (int k0 = 0; k0 < dk; k0 += 8)
-                    mma3_step<false>(acc, Wk, lda, um0, k0, Ss, ldb, n0, -1.f, g, t);
-                Us[(um0 + g) * ldb + n0 + 2 * t] = acc[0];
-                Us[(um0 + g) * ldb + n0 + 2 * t + 1] = acc[1];
-                Us[(um0 + g + 8) * ldb + n0 + 2 * t] = acc[2];
-                Us[(um0 + g + 8) * ldb + n0 + 2 * t + 1] = acc[3];
+                const int n0 = unb + 8 * nt;
+                acc[nt][0] = Wv[(um0 + g) * kScanBV + n0 + 2 * t];
+                acc[nt][1] = Wv[(um0 + g) * kScanBV + n0 + 2 * t + 1];
+                acc[nt][2] = Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t];
+                acc[nt][3] = Wv[(um0 + g + 8) * kScanBV + n0 + 2 * t + 1];
+            }
+            mma3_rows<2, false>(acc, Wk, lda, um0, dk, Ss, ldb, unb, -1.f, g, t);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = unb + 8 * nt;
+                Us[(um0 + g) * ldb + n0 + 2 * t] = acc[nt][0];
+                Us[(um0 + g) * ldb + n0 + 2 * t + 1] = acc[nt][1];
+                Us[(um0 + g + 8) * ldb + n0 + 2 * t] = acc[nt][2];
+                Us[(um0 + g + 8) * ldb + n0 + 2 * t + 1] = acc[nt][3];
             }
         }
         __syncthreads();
@@ -536,21 +572,19 @@ __global__ void __launch_bounds__(kScanThreads)
         // O = Qt S0 + P U (P is zero above the diagonal and off a tree's
         // ancestors), rows below L stored
         if (um0 < C) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            mma3_rows<2, false>(acc, Qt, lda, um0, dk, Ss, ldb, unb, 1.f, g, t);
+            mma3_rows<2, false>(acc, Ps, ldp, um0, um0 + 16, Us, ldb, unb, 1.f, g, t);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const int n0 = 8 * (2 * (warp & 1) + nt);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int k0 = 0; k0 < dk; k0 += 8)
-                    mma3_step<false>(acc, Qt, lda, um0, k0, Ss, ldb, n0, 1.f, g, t);
-                for (int k0 = 0; k0 < um0 + 16; k0 += 8)
-                    mma3_step<false>(acc, Ps, ldp, um0, k0, Us, ldb, n0, 1.f, g, t);
+                const int n0 = unb + 8 * nt;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int r = um0 + g + 8 * h;
                     if (r < L) {
                         Tin *o = out + ((tok0 + t0 + r) * HV + hv) * dv + j0 + n0 + 2 * t;
-                        o[0] = from_f32<Tin>(acc[2 * h]);
-                        o[1] = from_f32<Tin>(acc[2 * h + 1]);
+                        o[0] = from_f32<Tin>(acc[nt][2 * h]);
+                        o[1] = from_f32<Tin>(acc[nt][2 * h + 1]);
                     }
                 }
             }
@@ -559,21 +593,20 @@ __global__ void __launch_bounds__(kScanThreads)
         if (TREE) break;  // one chunk; no state to carry
         // S = diag(gam) S0 + Kh^T U (rows of Kh and U past L are zero), kept
         // in registers until every warp is done reading S0
-        float sacc[8][4];
+        float sacc[4][4];
         const int sm0 = 16 * warp;
         const bool s_rows = sm0 < dk;
         if (s_rows) {
+            const float ga = gam[sm0 + g], gb = gam[sm0 + g + 8];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int n0 = 8 * nt;
-                const float ga = gam[sm0 + g], gb = gam[sm0 + g + 8];
                 sacc[nt][0] = ga * Ss[(sm0 + g) * ldb + n0 + 2 * t];
                 sacc[nt][1] = ga * Ss[(sm0 + g) * ldb + n0 + 2 * t + 1];
                 sacc[nt][2] = gb * Ss[(sm0 + g + 8) * ldb + n0 + 2 * t];
                 sacc[nt][3] = gb * Ss[(sm0 + g + 8) * ldb + n0 + 2 * t + 1];
-                for (int k0 = 0; k0 < L; k0 += 8)
-                    mma3_step<true>(sacc[nt], Kh, lda, sm0, k0, Us, ldb, n0, 1.f, g, t);
             }
+            mma3_rows<4, true>(sacc, Kh, lda, sm0, L, Us, ldb, 0, 1.f, g, t);
         }
         __syncthreads();
         if (s_rows) {
