@@ -40,6 +40,20 @@ Two routines, both in float64:
     decay factored out of the dot products, so that one gram K K^T per key
     head serves all of its value heads.
 
+``affine_map`` / ``segmented_forward``
+    The chunk-parallel state scan.  Over any run of tokens the recurrence is
+    an affine map of the state, S_end = M S_start + c, with M [dk, dk]
+    depending only on (k, g, beta) and c the end state from a zero start.
+    ``affine_map`` composes it token by token from the one-token map
+    S -> (I - beta k k^T) diag(exp g) S + beta k v^T (the unrolled update of
+    the first commit summary of the executorch page).  ``segmented_forward``
+    cuts the sequence into segments of whole chunks, takes the maps of the
+    middle segments, runs the first segment from h0, chains the maps to get
+    every segment's start state, and runs the other segments from those
+    starts: the order of work the GPU's segmented route follows.  The pages
+    only name the chunked pieces; this split of the serial carry is derived
+    from the algebra, and its result is the definition's.
+
 Array layouts (numpy, C-contiguous):
     q, k [B, T, HK, dk]; v [B, T, HV, dv]; g [B, T, HV, dk]; beta [B, T, HV];
     h0 [B, HV, dk, dv] or None.  Returns (o [B, T, HV, dv], ht [B, HV, dk, dv]).
@@ -338,4 +352,81 @@ def scalar_gate_wy(q, k, v, g, beta, h0=None, chunk=64):
                     S[hv] = np.exp(G[-1]) * S[hv] + (np.exp(G[-1] - G)[:, None] * K).T @ U
         for hv in range(HV):
             ht[b, hv] = S[hv]
+    return out, ht
+
+
+def segment_bounds(T, chunk, segments):
+    """Token ranges [t0, t1) of at most ``segments`` segments of whole chunks:
+    ceil(chunks / segments) chunks each, the last one shorter (and ragged
+    when T is not a multiple of the chunk).  No segment is empty."""
+    nch = -(-T // chunk)
+    if nch == 0:
+        return []
+    per = -(-nch // max(1, segments))
+    return [(c * chunk, min(T, (c + per) * chunk)) for c in range(0, nch, per)]
+
+
+def affine_map(k, v, g, beta, t0, t1):
+    """The map of tokens t0 .. t1-1 on the state of every (b, hv):
+    S_end = M S_start + c, M [B, HV, dk, dk], c [B, HV, dk, dv], composed
+    one token at a time: with a = exp(g_t) per key channel,
+      S -> (I - beta_t k_t k_t^T) diag(a) S + beta_t k_t v_t^T
+    (decay, then the delta update with the prediction (diag(a) S)^T k_t)."""
+    k, v, g, beta = (_f64(x) for x in (k, v, g, beta))
+    B, _, HK, dk = k.shape
+    HV, dv = v.shape[2], v.shape[3]
+    group = HV // HK
+    M = np.zeros((B, HV, dk, dk))
+    c = np.zeros((B, HV, dk, dv))
+    eye = np.eye(dk)
+    for b in range(B):
+        for hv in range(HV):
+            hk = hv // group
+            Mb, cb = eye.copy(), np.zeros((dk, dv))
+            for t in range(t0, t1):
+                kt = k[b, t, hk]
+                bt = beta[b, t, hv]
+                A = (eye - bt * np.outer(kt, kt)) * np.exp(g[b, t, hv])[None, :]
+                Mb = A @ Mb
+                cb = A @ cb + bt * np.outer(kt, v[b, t, hv])
+            M[b, hv], c[b, hv] = Mb, cb
+    return M, c
+
+
+def segmented_forward(q, k, v, g, beta, h0=None, segments=3, chunk=64):
+    """The chunk-parallel scan in the GPU's order of work; returns (o, ht).
+
+    With segments p = 0 .. P-1 (``segment_bounds``) and S_p the state at the
+    start of segment p:
+      1. (M_p, c_p) = affine_map over segment p, for p = 1 .. P-2
+      2. segment 0 runs from S_0 = h0 (or 0): its outputs and S_1
+      3. S_{p+1} = M_p S_p + c_p for p = 1 .. P-2
+      4. segment p >= 1 runs from S_p: its outputs (and, last, ht)
+    The runs are the token recurrence."""
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, HK, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    bounds = segment_bounds(T, chunk, segments)
+    start = np.zeros((B, HV, dk, dv)) if h0 is None else _f64(h0).copy()
+    if not bounds:
+        return np.zeros((B, 0, HV, dv)), start
+    maps = {p: affine_map(k, v, g, beta, *bounds[p]) for p in range(1, len(bounds) - 1)}
+    out = np.zeros((B, T, HV, dv))
+
+    def run(p, S):
+        t0, t1 = bounds[p]
+        sl = slice(t0, t1)
+        o, S_end = recurrence(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl], S)
+        out[:, sl] = o
+        return S_end
+
+    S = run(0, start)
+    starts = [S]
+    for p in range(1, len(bounds) - 1):
+        M, c = maps[p]
+        S = np.einsum("bhij,bhjv->bhiv", M, S) + c
+        starts.append(S)
+    ht = S if len(bounds) == 1 else None
+    for p in range(1, len(bounds)):
+        ht = run(p, starts[p - 1])
     return out, ht
