@@ -20,6 +20,15 @@ GDR_BF16 = 1
 GDR_FLAG_FORCE_CHUNKED = 1
 GDR_FLAG_FORCE_GENERIC = 2
 GDR_FLAG_SCALAR_GATE = 4
+GDR_FLAG_NO_SEGMENTS = 8
+
+
+def gdr_flag_segments(n):
+    """Flag bits that make the tensor-core route cut the state scan into at
+    most ``n`` segments (2 <= n <= 255), whatever the device."""
+    if not 2 <= n <= 255:
+        raise ValueError("segment count must be in 2 .. 255")
+    return (n & 0xFF) << 8
 
 STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_UNSUPPORTED",
                 4: "GDR_ERR_ALIGN", 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA",

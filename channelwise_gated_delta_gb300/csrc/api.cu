@@ -95,14 +95,26 @@ gdr_status validate(const void *q, const void *k, const void *v, const float *g,
     return GDR_OK;
 }
 
-enum class Route { Nothing, EmptySequence, Decode, GenericPrefill, TensorCorePrefill };
+enum class Route {
+    Nothing,
+    EmptySequence,
+    Decode,
+    GenericPrefill,
+    TensorCorePrefill,
+    SegmentedPrefill
+};
 
-Route choose(const gdr::Problem &p, unsigned flags) {
+// `segments`: whether the tensor-core route may split the state scan into
+// segments (dense batches only).
+Route choose(const gdr::Problem &p, unsigned flags, bool segments = false) {
     if (p.B == 0) return Route::Nothing;
     if (p.T == 0) return Route::EmptySequence;
     if (p.T == 1 && !(flags & GDR_FLAG_FORCE_CHUNKED)) return Route::Decode;
-    if (gdr::tc_prefill_supported(p) && !(flags & GDR_FLAG_FORCE_GENERIC))
+    if (gdr::tc_prefill_supported(p) && !(flags & GDR_FLAG_FORCE_GENERIC)) {
+        if (segments && (long long)p.B * p.T <= 0x7fffffffLL && gdr::segment_count(p, flags) >= 2)
+            return Route::SegmentedPrefill;
         return Route::TensorCorePrefill;
+    }
     return Route::GenericPrefill;
 }
 
@@ -133,11 +145,14 @@ cudaError_t device_error_word(int **out) {
 
 namespace {
 
-size_t route_workspace(const gdr::Problem &p, Route r) {
-    return r == Route::GenericPrefill ? gdr::generic_prefill_workspace_bytes(p) : 0;
+size_t route_workspace(const gdr::Problem &p, Route r, unsigned flags) {
+    if (r == Route::GenericPrefill) return gdr::generic_prefill_workspace_bytes(p);
+    if (r == Route::SegmentedPrefill)
+        return gdr::segmented_workspace_bytes(p, gdr::segment_count(p, flags));
+    return 0;
 }
 
-gdr_status run(const gdr::Problem &p, Route r, void *ws, cudaStream_t stream) {
+gdr_status run(const gdr::Problem &p, Route r, unsigned flags, void *ws, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
     switch (r) {
         case Route::Nothing:
@@ -160,6 +175,13 @@ gdr_status run(const gdr::Problem &p, Route r, void *ws, cudaStream_t stream) {
             int *err = nullptr;
             e = gdr::device_error_word(&err);
             if (e == cudaSuccess) e = gdr::launch_tc_prefill(p, err, stream);
+            break;
+        }
+        case Route::SegmentedPrefill: {
+            int *err = nullptr;
+            e = gdr::device_error_word(&err);
+            if (e == cudaSuccess)
+                e = gdr::launch_segmented_prefill(p, gdr::segment_count(p, flags), ws, err, stream);
             break;
         }
     }
@@ -214,6 +236,7 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
                 plan->rows.push_back(make_int2(cu[n], n));
                 break;
             case Route::TensorCorePrefill:
+            case Route::SegmentedPrefill:  // not chosen here
                 plan->tc_seqs.push_back(make_int4(cu[n], L, n, 0));
                 break;
             case Route::GenericPrefill:
@@ -284,7 +307,8 @@ cudaEvent_t take_event() {
 }
 
 const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_prep",
-                                              "gdr_chunk_scan", "gdr_prefill_fused"};
+                                              "gdr_chunk_scan",    "gdr_prefill_fused",
+                                              "gdr_segment_init",  "gdr_segment_combine"};
 
 }  // namespace
 
@@ -381,8 +405,9 @@ GDR_API size_t gdr_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
     if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
     if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(chunk)) return 0;
     p = gdr::Problem{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                     B, T, HK, HV, dk, dv, chunk, qkv_dtype == GDR_BF16 ? 1 : 0};
-    return route_workspace(p, choose(p, flags));
+                     B, T, HK, HV, dk, dv, chunk, qkv_dtype == GDR_BF16 ? 1 : 0,
+                     (flags & GDR_FLAG_SCALAR_GATE) ? 1 : 0};
+    return route_workspace(p, choose(p, flags, true), flags);
 }
 
 GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, const float *g,
@@ -394,13 +419,13 @@ GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, c
     gdr_status st = validate(q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
                              qkv_dtype, &p, flags);
     if (st != GDR_OK) return st;
-    const Route r = choose(p, flags);
-    const size_t need = route_workspace(p, r);
+    const Route r = choose(p, flags, true);
+    const size_t need = route_workspace(p, r, flags);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return GDR_ERR_WORKSPACE;
         if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGN;
     }
-    return run(p, r, workspace, static_cast<cudaStream_t>(stream));
+    return run(p, r, flags, workspace, static_cast<cudaStream_t>(stream));
 }
 
 GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, const float *g,
@@ -411,8 +436,8 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
     gdr_status st = validate(q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
                              qkv_dtype, &p);
     if (st != GDR_OK) return st;
-    const Route r = choose(p, 0u);
-    const size_t need = route_workspace(p, r);
+    const Route r = choose(p, 0u, true);
+    const size_t need = route_workspace(p, r, 0u);
     void *ws = nullptr;
     if (need > 0) {
         int dev = 0;
@@ -436,7 +461,7 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
         }
         ws = w.ptr;
     }
-    return run(p, r, ws, static_cast<cudaStream_t>(stream));
+    return run(p, r, 0u, ws, static_cast<cudaStream_t>(stream));
 }
 
 GDR_API size_t gdr_varlen_workspace_bytes(const int *cu_seqlens, int N, int HK, int HV, int dk,

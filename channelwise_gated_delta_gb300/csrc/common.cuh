@@ -62,7 +62,15 @@ __device__ __forceinline__ void stg_stream4(float *p, float4 x) {
 // Launchers implemented in the .cu files (host side, C++ linkage).
 namespace gdr {
 // Kernel identities for launch tracing (gdr_trace_enable / gdr_trace_read).
-enum KernelId { kKernDecode = 0, kKernChunkPrep = 1, kKernChunkScan = 2, kKernFused = 3, kNumKernels = 4 };
+enum KernelId {
+    kKernDecode = 0,
+    kKernChunkPrep = 1,
+    kKernChunkScan = 2,
+    kKernFused = 3,
+    kKernSegInit = 4,
+    kKernSegCombine = 5,
+    kNumKernels = 6
+};
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);
 void trace_end(int kernel, cudaStream_t stream);
@@ -94,8 +102,12 @@ cudaError_t launch_decode_rows(const Problem &p, const int2 *rows, cudaStream_t 
 // Tensor-core prefill: seqs[s] = {first token row, length, state slot, -};
 // seq_maps: one tensor-map set per sequence (tc_seq_maps_bytes() each,
 // 64-byte aligned, in device memory), filled on the host by tc_encode_seq_maps.
+// A non-null v_row (o_row) replaces the sequence's values (outputs) by a
+// one-row [1][HV][128] bf16 device tensor: the values read as zeros past its
+// row 0 (zero-filled loads), the outputs past row 0 are dropped.
 size_t tc_seq_maps_bytes();
-cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst);
+cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst,
+                               const void *v_row = nullptr, void *o_row = nullptr);
 cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, const int4 *seqs,
                                      int nseq, int *dev_error, cudaStream_t stream);
 // CUDA-core chunked prefill: chunks[i] = {first token row, length} of every
@@ -113,4 +125,12 @@ cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
                            cudaStream_t stream);
 cudaError_t launch_generic_tree(const Problem &p, void *records, const int *parents,
                                 cudaStream_t stream);
+
+// Chunk-parallel state scan on the tensor-core route (segments.cu): the
+// segment count chosen for `p` (0: not segmented) under `flags`, its
+// workspace, and the launches.
+int segment_count(const Problem &p, unsigned flags);
+size_t segmented_workspace_bytes(const Problem &p, int segments);
+cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
+                                     int *dev_error, cudaStream_t stream);
 }  // namespace gdr

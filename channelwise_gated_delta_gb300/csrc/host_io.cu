@@ -33,6 +33,11 @@ int segment_tokens(int T, int chunk) {
     return (kSegmentTokens / chunk) * chunk;
 }
 
+// The segmented state scan copies its tables from pageable host memory, which
+// may wait for the compute stream and so stall the copy pipeline; the host
+// entry is bound by its copies anyway.
+constexpr unsigned kSegFlags = GDR_FLAG_NO_SEGMENTS;
+
 // Per-slot layout: one segment's inputs, output and route workspace.
 struct SlotLayout {
     size_t q, k, v, g, beta, out, ws, bytes;  // offsets and slot size
@@ -47,7 +52,7 @@ SlotLayout slot_layout(int Ts, int HK, int HV, int dk, int dv, int chunk, int qk
     L.tv = (size_t)HV * dv * es;
     L.tg = (size_t)HV * dk * 4;
     L.tb = (size_t)HV * 4;
-    L.ws_b = gdr_workspace_bytes(1, Ts, HK, HV, dk, dv, chunk, qkv_dtype, 0);
+    L.ws_b = gdr_workspace_bytes(1, Ts, HK, HV, dk, dv, chunk, qkv_dtype, kSegFlags);
     size_t off = 0;
     auto put = [&](size_t n) {
         const size_t at = off;
@@ -231,7 +236,8 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
             const gdr_status st_fw = gdr_forward_ex(
                 sl + L.q, sl + L.k, sl + L.v, reinterpret_cast<const float *>(sl + L.g),
                 reinterpret_cast<const float *>(sl + L.beta), seg_h0, sl + L.out, state, 1, len,
-                HK, HV, dk, dv, chunk, cs, qkv_dtype, L.ws_b ? sl + L.ws : nullptr, L.ws_b, 0);
+                HK, HV, dk, dv, chunk, cs, qkv_dtype, L.ws_b ? sl + L.ws : nullptr, L.ws_b,
+                kSegFlags);
             if (st_fw != GDR_OK) return st_fw;
             if ((e = cudaEventRecord(io->computed[slot], cs)) != cudaSuccess) return fail(e);
             if ((e = cudaStreamWaitEvent(io->out, io->computed[slot], 0)) != cudaSuccess)

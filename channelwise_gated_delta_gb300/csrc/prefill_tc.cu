@@ -1234,12 +1234,20 @@ cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t str
 
 size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
 
-cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst) {
+cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst,
+                               const void *v_row, void *o_row) {
     cudaError_t e = cudaSuccess;
     EncodeTiledFn fn = encode_fn(&e);
     if (e != cudaSuccess) return e;
     TileMaps tm;
     if (!encode_maps(fn, &tm, p, tok0, 1, L)) return cudaErrorInvalidValue;
+    // one-row stand-ins: every load past row 0 reads the zero fill, every
+    // store past row 0 is dropped
+    if (v_row && !encode_map(fn, &tm.v, v_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV, 64))
+        return cudaErrorInvalidValue;
+    if (o_row && !encode_map(fn, &tm.o, o_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV, 32,
+                             CU_TENSOR_MAP_SWIZZLE_NONE, 16))
+        return cudaErrorInvalidValue;
     memcpy(dst, &tm, sizeof(TileMaps));
     return cudaSuccess;
 }

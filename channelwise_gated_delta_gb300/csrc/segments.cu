@@ -1,0 +1,362 @@
+// segments.cu -- the chunk-parallel state scan on the tensor-core prefill.
+//
+// The chunk-to-chunk state carry of the chunkwise form (page "Reorder
+// channelwise gated delta rule chunked hot loops for autovectorization",
+// pytorch/executorch PR #21021, second commit summary) is serial: one CTA
+// walks a head's chunks in order.  When batch x heads leaves most SMs idle,
+// the sequence is cut into P segments of whole chunks.  Over a segment the
+// recurrence is an affine map of the state, S_end = M S_start + c, with M
+// [dk][dk] depending on k, g and beta only: M is the end state of a run from
+// S_start = I with v = 0, c the end state of a run from S_start = 0.
+//
+//   wave A  (one launch, all concurrent)  segment 0 from h0 -> S_1;
+//           for p = 1 .. P-2: the runs that give M_p and c_p
+//   combine S_{p+1} = M_p S_p + c_p, p = 1 .. P-2 (gdr_segment_combine)
+//   wave B  (one launch) segment p = 1 .. P-1 from S_p: outputs, and ht
+//
+// Both waves are the packed-sequence tensor-core kernel: every run is one
+// "sequence" with its own tensor maps and state slot.  The map runs read
+// their values from a one-row zero tensor (every other row is the loads'
+// zero fill) and send their outputs to a one-row scratch tensor (every other
+// row falls outside it and is dropped), so they move no value or output
+// bytes.  The critical path is two segments instead of P.
+//
+// State slots, a group of 2P-3 per batch element b (each slot HV x [128][128]
+// f32): X_1, M_1, X_2, M_2, X_3, ..., M_{P-2}, X_{P-1} -- X_p at 2(p-1), M_p
+// at 2p-1.  gdr_segment_init fills X_1 = h0[b] (or 0), M_p = I and
+// X_{p+1} = 0; wave A leaves X_1 = S_1, M_p and X_{p+1} = c_p; the combine
+// turns X_{p+1} into S_{p+1} in place; wave B runs segment p in place on X_p,
+// which leaves the final state in X_{P-1}.
+#include <algorithm>
+#include <mutex>
+#include <string.h>
+#include <vector>
+
+#include "common.cuh"
+#include "gdr.h"
+
+namespace gdr {
+namespace {
+
+constexpr int kD = 128;   // dk = dv of the tensor-core route
+constexpr int kC = 64;    // its chunk
+constexpr size_t kSlotFloats = (size_t)kD * kD;
+// Shortest segment the automatic choice makes, in chunks: below this the
+// per-launch fill and the combine cost more than the shorter walk saves.
+constexpr int kMinSegmentChunks = 8;
+constexpr int kCombineThreads = 256;
+constexpr int kMtLd = kD + 4;  // transposed M rows, padded (16-byte aligned)
+constexpr size_t kCombineSmem = ((size_t)kD * kMtLd + (size_t)kD * 32) * sizeof(float);
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// SM count of the current device, looked up once per device; 0 if unknown.
+int sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, -1);
+    if (cache[dev] < 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+struct Segments {
+    int P = 0;        // number of segments
+    int per = 0;      // chunks per segment (the last may have fewer)
+    int group = 0;    // state slots per batch element, 2P - 3 (1 when P = 2)
+    int nA = 0, nB = 0;                // runs in wave A and wave B
+    size_t off_seqA = 0, off_mapA = 0, off_seqB = 0, off_mapB = 0;
+    size_t off_zero = 0, off_scratch = 0, off_state = 0, table_bytes = 0, total = 0;
+};
+
+Segments plan(const Problem &p, int P) {
+    Segments s;
+    const int nch = (p.T + kC - 1) / kC;
+    if (P < 2 || nch < 2) return s;
+    s.per = (nch + P - 1) / P;
+    s.P = (nch + s.per - 1) / s.per;
+    if (s.P < 2) {
+        s.P = 0;
+        return s;
+    }
+    s.group = 2 * s.P - 3;
+    s.nA = p.B * s.group;
+    s.nB = p.B * (s.P - 1);
+    const size_t maps = tc_seq_maps_bytes();
+    size_t off = 0;
+    s.off_seqA = off;
+    off = align256(off + (size_t)s.nA * sizeof(int4));
+    s.off_mapA = off;
+    off = align256(off + (size_t)s.nA * maps);
+    s.off_seqB = off;
+    off = align256(off + (size_t)s.nB * sizeof(int4));
+    s.off_mapB = off;
+    off = align256(off + (size_t)s.nB * maps);
+    s.table_bytes = off;
+    const size_t row = (size_t)p.HV * kD * 2;  // one bf16 token row of v / o
+    s.off_zero = off;
+    off = align256(off + row);
+    s.off_scratch = off;
+    off = align256(off + row);
+    s.off_state = off;
+    off += (size_t)s.nA * p.HV * kSlotFloats * sizeof(float);
+    s.total = off;
+    return s;
+}
+
+// Four blocks per (slot, head), 32 rows each: slot j of batch element b's
+// group is X_1 (j = 0: a copy of h0[b], or zeros), M_p (odd j: the
+// identity) or X_{p+1} (even j > 0: zeros).  [128][128] f32 row-major per
+// (slot, head).  Each thread's four loads are issued before its stores.
+// Block 0 also clears the one-row zero value tensor (zero_words 32-bit words).
+constexpr int kInitThreads = 256;
+constexpr int kInitPerThread = (int)(kSlotFloats / 4 / 4 / kInitThreads);  // float4s
+__global__ void __launch_bounds__(kInitThreads) gdr_segment_init(const float *__restrict__ h0,
+                                                                 float *__restrict__ state,
+                                                                 int HV, int group,
+                                                                 unsigned *__restrict__ zero_row,
+                                                                 int zero_words) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_words; i += kInitThreads) zero_row[i] = 0u;
+    const int sh = blockIdx.x >> 2, quarter = blockIdx.x & 3;  // sh = slot * HV + hv
+    const int slot = sh / HV, hv = sh % HV;
+    const int b = slot / group, j = slot % group;
+    const size_t first = (size_t)quarter * (kSlotFloats / 4 / 4);  // float4 index in the slot
+    float4 *dst = reinterpret_cast<float4 *>(state + (size_t)sh * kSlotFloats) + first;
+    const float4 *src = (j == 0 && h0)
+                            ? reinterpret_cast<const float4 *>(h0 + ((size_t)b * HV + hv) * kSlotFloats) + first
+                            : nullptr;
+    const bool ident = (j & 1) != 0;
+    float4 x[kInitPerThread];
+#pragma unroll
+    for (int u = 0; u < kInitPerThread; ++u) {
+        const int i = threadIdx.x + u * kInitThreads;
+        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (src) {
+            x[u] = src[i];
+        } else if (ident) {
+            const int e = (int)first + i;
+            const int r = e / (kD / 4), c0 = 4 * (e % (kD / 4));
+            if (r == c0) x[u].x = 1.f;
+            if (r == c0 + 1) x[u].y = 1.f;
+            if (r == c0 + 2) x[u].z = 1.f;
+            if (r == c0 + 3) x[u].w = 1.f;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kInitPerThread; ++u) dst[threadIdx.x + u * kInitThreads] = x[u];
+}
+
+// S_{p+1} = M_p S_p + c_p for p = 1 .. P-2, in place on the X slots.  One
+// CTA per (b, hv, 32-column slab of the state): the columns of the state are
+// independent, so the slab walks the whole chain alone, kept in shared
+// memory between steps.  M_p is staged transposed (Mt[k][r]) so that a
+// thread's four rows at one k are one float4; each thread owns a 4 x 4 tile
+// (rows 4 rg .., columns 4 cg .. of the slab).  f32 FMAs, k in order.
+__global__ void __launch_bounds__(kCombineThreads) gdr_segment_combine(float *__restrict__ state,
+                                                                       int HV, int P) {
+    extern __shared__ float smc[];
+    float *Mt = smc;                 // [128][kMtLd]
+    float *Xs = smc + kD * kMtLd;    // [128][32]
+    const int slab = blockIdx.x & 3, head = blockIdx.x >> 2;
+    const int hv = head % HV, b = head / HV;
+    const int group = 2 * P - 3;
+    auto slot = [&](int j) { return state + ((size_t)(b * group + j) * HV + hv) * kSlotFloats; };
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c0 = 32 * slab;
+    const int cg = lane & 7, rg = 4 * warp + (lane >> 3);
+
+    {
+        const float *x1 = slot(0);
+        float4 x[kD * 8 / kCombineThreads];
+#pragma unroll
+        for (int u = 0; u < kD * 8 / kCombineThreads; ++u) {
+            const int i = tid + u * kCombineThreads, r = i >> 3, qd = i & 7;
+            x[u] = *reinterpret_cast<const float4 *>(x1 + (size_t)r * kD + c0 + 4 * qd);
+        }
+#pragma unroll
+        for (int u = 0; u < kD * 8 / kCombineThreads; ++u) {
+            const int i = tid + u * kCombineThreads, r = i >> 3, qd = i & 7;
+            *reinterpret_cast<float4 *>(Xs + r * 32 + 4 * qd) = x[u];
+        }
+    }
+    for (int p = 1; p <= P - 2; ++p) {
+        const float *M = slot(2 * p - 1);
+        float *X = slot(2 * p);  // c_p in, S_{p+1} out
+        // this thread's c_p tile and M_p share, all loads in flight at once
+        float4 cv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            cv[i] = *reinterpret_cast<const float4 *>(X + (size_t)(4 * rg + i) * kD + c0 + 4 * cg);
+        constexpr int kMLoads = kD * (kD / 4) / kCombineThreads;
+        float4 m[kMLoads];
+#pragma unroll
+        for (int u = 0; u < kMLoads; ++u) {
+            // lanes take consecutive rows, so the transposed stores use all banks
+            const int i = tid + u * kCombineThreads;
+            const int r = (i & 31) + 32 * (i >> 10), kq = (i >> 5) & 31;
+            m[u] = *reinterpret_cast<const float4 *>(M + (size_t)r * kD + 4 * kq);
+        }
+        __syncthreads();  // Xs written; the previous step's reads of Mt done
+#pragma unroll
+        for (int u = 0; u < kMLoads; ++u) {
+            const int i = tid + u * kCombineThreads;
+            const int r = (i & 31) + 32 * (i >> 10), kq = (i >> 5) & 31;
+            Mt[(4 * kq + 0) * kMtLd + r] = m[u].x;
+            Mt[(4 * kq + 1) * kMtLd + r] = m[u].y;
+            Mt[(4 * kq + 2) * kMtLd + r] = m[u].z;
+            Mt[(4 * kq + 3) * kMtLd + r] = m[u].w;
+        }
+        __syncthreads();
+        float acc[4][4] = {};
+#pragma unroll 8
+        for (int k = 0; k < kD; ++k) {
+            const float4 m = *reinterpret_cast<const float4 *>(Mt + k * kMtLd + 4 * rg);
+            const float4 x = *reinterpret_cast<const float4 *>(Xs + k * 32 + 4 * cg);
+            const float mv[4] = {m.x, m.y, m.z, m.w}, xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(mv[i], xv[jj], acc[i][jj]);
+        }
+        __syncthreads();  // every read of Xs done before it is overwritten
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * rg + i;
+            float4 *dst = reinterpret_cast<float4 *>(X + (size_t)r * kD + c0 + 4 * cg);
+            const float4 c = cv[i];
+            const float4 y = make_float4(acc[i][0] + c.x, acc[i][1] + c.y, acc[i][2] + c.z,
+                                         acc[i][3] + c.w);
+            *dst = y;
+            *reinterpret_cast<float4 *>(Xs + r * 32 + 4 * cg) = y;
+        }
+    }
+}
+
+}  // namespace
+
+int segment_count(const Problem &p, unsigned flags) {
+    if (flags & GDR_FLAG_NO_SEGMENTS) return 0;
+    if (!tc_prefill_supported(p) || p.B <= 0 || p.T < 2) return 0;
+    const int nch = (p.T + kC - 1) / kC;
+    const int forced = (int)((flags >> 8) & 0xffu);
+    int P = forced;
+    if (!forced) {
+        // wave A runs B HV (2P - 3) CTAs, one per SM; take the largest P
+        // that keeps it to one wave, with segments of kMinSegmentChunks or more
+        const int sms = sm_count();
+        const long long units = (long long)p.B * p.HV;
+        if (sms <= 0 || units <= 0) return 0;
+        P = (int)((sms / units + 3) / 2);
+        P = std::min(P, nch / kMinSegmentChunks);
+        if (P < 3) return 0;  // two segments walk as long as one
+    }
+    const Segments s = plan(p, P);
+    if (s.P < 2 || (!forced && s.P < 3)) return 0;
+    return s.P;
+}
+
+size_t segmented_workspace_bytes(const Problem &p, int segments) {
+    return plan(p, segments).total;
+}
+
+cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
+                                     int *dev_error, cudaStream_t stream) {
+    const Segments s = plan(p, segments);
+    if (s.P != segments || s.total == 0) return cudaErrorInvalidValue;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const void *zero_row = ws + s.off_zero;  // cleared by gdr_segment_init
+    void *scratch_row = ws + s.off_scratch;
+    float *state = reinterpret_cast<float *>(ws + s.off_state);
+    const size_t maps = tc_seq_maps_bytes();
+    const int seg_len = s.per * kC;
+    auto seg_t0 = [&](int q) { return q * seg_len; };
+    auto seg_len_of = [&](int q) { return std::min(p.T, (q + 1) * seg_len) - q * seg_len; };
+
+    // tables: {first token row, length, state slot, 0} and the tensor maps
+    std::vector<unsigned char> host(s.table_bytes, 0);
+    int4 *seqA = reinterpret_cast<int4 *>(host.data() + s.off_seqA);
+    int4 *seqB = reinterpret_cast<int4 *>(host.data() + s.off_seqB);
+    cudaError_t e = cudaSuccess;
+    int a = 0, bb = 0;
+    for (int b = 0; b < p.B; ++b) {
+        const int base = b * s.group;
+        const size_t row0 = (size_t)b * p.T;
+        auto add = [&](int4 *tab, size_t off_map, int &n, int q, int slot_j, const void *v_row,
+                       void *o_row) {
+            const size_t tok0 = row0 + seg_t0(q);
+            tab[n] = make_int4((int)tok0, seg_len_of(q), base + slot_j, 0);
+            const cudaError_t r = tc_encode_seq_maps(p, tok0, seg_len_of(q),
+                                                     host.data() + off_map + (size_t)n * maps,
+                                                     v_row, o_row);
+            ++n;
+            return r;
+        };
+        e = add(seqA, s.off_mapA, a, 0, 0, nullptr, nullptr);
+        for (int q = 1; q <= s.P - 2 && e == cudaSuccess; ++q) {
+            e = add(seqA, s.off_mapA, a, q, 2 * q - 1, zero_row, scratch_row);  // M_q
+            if (e == cudaSuccess) e = add(seqA, s.off_mapA, a, q, 2 * q, nullptr, scratch_row);  // c_q
+        }
+        for (int q = 1; q <= s.P - 1 && e == cudaSuccess; ++q)
+            e = add(seqB, s.off_mapB, bb, q, 2 * (q - 1), nullptr, nullptr);
+        if (e != cudaSuccess) return e;
+    }
+    // pageable source: the call returns once the bytes have been taken
+    e = cudaMemcpyAsync(ws, host.data(), s.table_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+
+    trace_begin(kKernSegInit, stream);
+    gdr_segment_init<<<(unsigned)(4 * s.nA * p.HV), kInitThreads, 0, stream>>>(
+        p.h0, state, p.HV, s.group, reinterpret_cast<unsigned *>(ws + s.off_zero), p.HV * kD / 2);
+    trace_end(kKernSegInit, stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    Problem wave = p;
+    wave.h0 = state;
+    wave.ht = state;
+    wave.T = 0;
+    wave.B = s.nA;
+    e = launch_tc_prefill_varlen(wave, ws + s.off_mapA,
+                                 reinterpret_cast<const int4 *>(ws + s.off_seqA), s.nA, dev_error,
+                                 stream);
+    if (e != cudaSuccess) return e;
+    if (s.P >= 3) {
+        e = cudaFuncSetAttribute(gdr_segment_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kCombineSmem);
+        if (e != cudaSuccess) return e;
+        trace_begin(kKernSegCombine, stream);
+        gdr_segment_combine<<<(unsigned)(p.B * p.HV * (kD / 32)), kCombineThreads, kCombineSmem,
+                              stream>>>(state, p.HV, s.P);
+        trace_end(kKernSegCombine, stream);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    wave.B = s.nB;
+    e = launch_tc_prefill_varlen(wave, ws + s.off_mapB,
+                                 reinterpret_cast<const int4 *>(ws + s.off_seqB), s.nB, dev_error,
+                                 stream);
+    if (e != cudaSuccess) return e;
+    if (p.ht) {
+        // X_{P-1} of every batch element: one strided copy
+        const size_t head_bytes = (size_t)p.HV * kSlotFloats * sizeof(float);
+        e = cudaMemcpy2DAsync(p.ht, head_bytes, state + (size_t)2 * (s.P - 2) * p.HV * kSlotFloats,
+                              (size_t)s.group * head_bytes, head_bytes, p.B,
+                              cudaMemcpyDeviceToDevice, stream);
+    }
+    return e;
+}
+
+}  // namespace gdr

@@ -92,6 +92,36 @@ typedef enum gdr_dtype {
  * (trees with a scalar gate run on the CUDA-core route).
  */
 #define GDR_FLAG_SCALAR_GATE 4u
+/*
+ * Segmented state scan (gdr_forward, gdr_forward_ex, gdr_workspace_bytes; the
+ * tensor-core route only).  The chunk-to-chunk state carry is serial, one CTA
+ * per (batch, value head) walking its chunks in order, so a small batch x
+ * heads leaves most SMs idle.  The route then cuts the sequence into P
+ * segments of whole chunks.  Over a segment the recurrence is an affine map
+ * of the state, S_end = M S_start + c (M [dk][dk] from k, g and beta alone),
+ * which is how the chunk carry of the second commit summary of "Reorder
+ * channelwise gated delta rule chunked hot loops for autovectorization"
+ * (pytorch/executorch PR #21021) composes.  Segment 0 runs from h0 at the
+ * same time as the runs that give the middle segments' maps; the maps are
+ * chained to every segment's start state; the other segments then run from
+ * those starts.  The walk is two segments long instead of P.
+ *
+ * Chosen automatically when it pays: P is the largest value with
+ * B * HV * (2P - 3) CTAs fitting on the device's SMs at once and segments
+ * of at least 8 chunks; P >= 3 is needed.  The route needs workspace
+ * (gdr_workspace_bytes reports it): its tables, which are copied in from
+ * host memory like those of gdr_forward_varlen (pass GDR_FLAG_NO_SEGMENTS
+ * when capturing into a CUDA graph), and 2P - 3 f32 states per (batch,
+ * value head).  Results agree with the unsegmented route to within the
+ * tolerance of the route, not bit for bit (the states of later segments
+ * are reached through the maps).
+ *
+ * GDR_FLAG_NO_SEGMENTS: never segment.
+ * GDR_FLAG_SEGMENTS(n): segment into at most n pieces (2 <= n <= 255;
+ * fewer when the sequence has fewer chunks), whatever the device; for tests.
+ */
+#define GDR_FLAG_NO_SEGMENTS 8u
+#define GDR_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)
 
 /*
  * Bytes of device workspace gdr_forward_ex needs for this call (0 when the

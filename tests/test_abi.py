@@ -97,6 +97,37 @@ def test_workspace_sizes(lib):
     assert call(lib, T=40, dtype=0, ws=FAKE + (9 << 30) + 16, ws_bytes=small) == 4
 
 
+def test_segmented_scan_workspace(lib):
+    """Forced segments on the tensor-core route: 2P - 3 f32 states per
+    (batch, value head) plus small tables; none when segments are off, the
+    route is the CUDA-core one, or the sequence has fewer than two chunks."""
+    from channelwise_gated_delta_gb300 import GDR_FLAG_NO_SEGMENTS, gdr_flag_segments
+    state = 128 * 128 * 4
+    for B, T, HV, P, P_eff in [(1, 4096, 32, 3, 3), (2, 1000, 4, 5, 4), (1, 200, 2, 2, 2),
+                               (1, 4096, 2, 255, 64)]:
+        need = lib.gdr_workspace_bytes(B, T, HV // 2, HV, 128, 128, 64, 1, gdr_flag_segments(P))
+        states = B * (2 * P_eff - 3) * HV * state
+        assert states <= need < states + 64 * 1024 + B * (3 * P_eff) * 1024, (B, T, HV, P)
+    seg3 = gdr_flag_segments(3)
+    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 1,
+                                   seg3 | GDR_FLAG_NO_SEGMENTS) == 0
+    assert lib.gdr_workspace_bytes(1, 64, 1, 2, 128, 128, 64, 1, seg3) == 0   # one chunk
+    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, seg3) > 0  # chunk 32: CUDA cores
+    assert (lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, seg3)
+            == lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, 0))
+    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 0, seg3) == \
+        lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 0, 0)          # f32: CUDA cores
+    # no device here, so the automatic choice never segments
+    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 1, 0) == 0
+    # missing or short workspace: rejected before any launch
+    need = lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 1, seg3)
+    kw = dict(T=4096, HK=16, HV=32, dk=128, dv=128, chunk=64, dtype=1, flags=seg3)
+    assert call(lib, **kw) == 5
+    assert call(lib, ws=FAKE + (9 << 30), ws_bytes=need - 1, **kw) == 5
+    with pytest.raises(ValueError):
+        gdr_flag_segments(1)
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from channelwise_gated_delta_gb300 import _binding
     with pytest.raises(RuntimeError, match="not built"):

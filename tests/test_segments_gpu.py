@@ -1,0 +1,125 @@
+"""The segmented state scan of the tensor-core route on the GPU: parity with
+the fp64 oracle for forced segment counts (two to many, ragged last chunk,
+with and without h0, in place, scalar gate, strong decays), the first
+segment's rows bit for bit those of the unsegmented route, and the automatic
+choice on a small-batch long prefill."""
+import pytest
+import torch
+
+import oracle
+from channelwise_gated_delta_gb300 import (GDR_FLAG_NO_SEGMENTS, gdr_device_check, gdr_flag_segments,
+                                           gdr_forward, gdr_trace_enable, gdr_trace_read)
+from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw, draw_workload, to_f64
+from tests.parity_util import assert_close, to_cuda
+from tests.test_parity_gpu import run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def traced(fn):
+    gdr_trace_enable(True)
+    try:
+        res = fn()
+        gdr_device_check()
+        return res, gdr_trace_read()
+    finally:
+        gdr_trace_enable(False)
+
+
+def check_segmented(d, segments, inplace=False):
+    dtype = d["q"].dtype
+    ref_o, ref_h = run_oracle(d)
+    (out, ht), tr = traced(lambda: run_gpu(d, 64, flags=gdr_flag_segments(segments),
+                                           inplace=inplace))
+    assert_close("o", out, ref_o, dtype)
+    assert_close("ht", ht, ref_h, dtype)
+    assert "gdr_segment_init" in tr, tr
+    return out, ht
+
+
+@pytest.mark.parametrize("segments", [2, 3, 4, 6])
+@pytest.mark.parametrize("T", [129, 1000])
+def test_forced_segments_match_oracle(segments, T):
+    check_segmented(draw(1, T, 2, 4, 128, 128, dtype=torch.bfloat16, seed=400 + T + segments),
+                    segments)
+
+
+def test_batch_and_grouped_heads():
+    check_segmented(draw(3, 700, 1, 4, 128, 128, dtype=torch.bfloat16, seed=410), 4)
+
+
+def test_no_initial_state():
+    check_segmented(draw(2, 500, 2, 2, 128, 128, dtype=torch.bfloat16, h0=False, seed=411), 3)
+
+
+def test_in_place_state():
+    check_segmented(draw(1, 640, 2, 4, 128, 128, dtype=torch.bfloat16, seed=412), 5, inplace=True)
+
+
+def test_no_final_state():
+    d = draw(1, 400, 2, 4, 128, 128, dtype=torch.bfloat16, seed=413)
+    ref_o, _ = run_oracle(d)
+    c = to_cuda(d)
+    out, ht = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=64,
+                          flags=gdr_flag_segments(3), store_ht=False)
+    gdr_device_check()
+    assert ht is None
+    assert_close("o", out, ref_o, torch.bfloat16)
+
+
+def test_one_chunk_per_segment():
+    """More segments requested than chunks: every segment is one chunk."""
+    check_segmented(draw(1, 300, 1, 2, 128, 128, dtype=torch.bfloat16, seed=414), 200)
+
+
+def test_scalar_gate():
+    d = draw(1, 900, 2, 4, 128, 128, dtype=torch.bfloat16, seed=415, scalar_gate=True)
+    args = [to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")]
+    ref_o, ref_h = oracle.scalar_gate_recurrence(*args, to_f64(d["h0"]))
+    out, ht = run_gpu(d, 64, flags=gdr_flag_segments(4))
+    assert_close("o", out, ref_o, torch.bfloat16)
+    assert_close("ht", ht, ref_h, torch.bfloat16)
+
+
+@pytest.mark.parametrize("g_mu,beta_mu", [(-3.0, 2.0), (2.0, 0.0), (6.0, 0.0)])
+def test_decay_regimes(g_mu, beta_mu):
+    """Weak decay with strong updates (the long-prefill distribution), strong
+    decay, and decay strong enough for the kernel's exact pairwise path: the
+    maps M_p run from the identity through the same range handling."""
+    check_segmented(draw(1, 768, 2, 4, 128, 128, dtype=torch.bfloat16, seed=416, g_mu=g_mu,
+                         beta_mu=beta_mu, beta_sigma=0.5), 4)
+
+
+def test_first_segment_rows_are_the_unsegmented_bits():
+    """Segment 0 runs from h0 through the same kernel code as the plain route:
+    its rows (whole chunks) are bit for bit the plain route's."""
+    d = draw(2, 1000, 2, 4, 128, 128, dtype=torch.bfloat16, seed=417)
+    seg, _ = run_gpu(d, 64, flags=gdr_flag_segments(3))
+    plain, _ = run_gpu(d, 64, flags=GDR_FLAG_NO_SEGMENTS)
+    first = 64 * 6  # 16 chunks in 3 segments: 6 chunks each
+    assert torch.equal(seg[:, :first], plain[:, :first])
+
+
+def test_automatic_choice_on_a_small_batch_long_prefill():
+    """B = 1, 32 value heads, T = 4096 (64 chunks): the automatic choice
+    segments (32 CTAs would leave most SMs idle); oracle on a sample of heads."""
+    w = WORKLOADS["prefill_t4k"]
+    d = draw_workload(w)
+    (out, ht), tr = traced(lambda: run_gpu(d, w.chunk))
+    assert "gdr_segment_combine" in tr, tr
+    ref = oracle.recurrence_heads(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                  to_f64(d["h0"]), [(0, 0), (0, 13), (0, 31)])
+    for (b, hv), (ref_o, ref_h) in ref.items():
+        assert_close("o[%d,%d]" % (b, hv), out[b, :, hv], ref_o, d["q"].dtype)
+        assert_close("ht[%d,%d]" % (b, hv), ht[b, hv], ref_h, d["q"].dtype)
+    # and it agrees with the unsegmented route to within the same bound
+    plain_o, plain_h = run_gpu(d, w.chunk, flags=GDR_FLAG_NO_SEGMENTS)
+    assert_close("o vs plain", out, to_f64(plain_o), d["q"].dtype)
+    assert_close("ht vs plain", ht, to_f64(plain_h), d["q"].dtype)
+
+
+def test_large_batch_is_not_segmented():
+    """B x HV = 128 fills the device: the automatic choice keeps one walk."""
+    d = draw(4, 1024, 16, 32, 128, 128, dtype=torch.bfloat16, seed=418)
+    _, tr = traced(lambda: run_gpu(d, 64))
+    assert "gdr_segment_init" not in tr and "gdr_prefill_fused" in tr, tr
