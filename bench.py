@@ -58,9 +58,12 @@ def parse_args():
     ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--workload", choices=["all", "prefill", "decode", "prefill_t4k"],
+                    default="all",
                     help="prefill: the headline only; decode: only the decode measurement "
-                         "(printed as its own line, for profiling the decode kernel)")
+                         "(printed as its own line, for profiling the decode kernel); "
+                         "prefill_t4k: the B=1 T=4096 prefill alone (its own line), the "
+                         "small-batch case the segmented state scan serves")
     return ap.parse_args()
 
 
@@ -198,11 +201,11 @@ def barrier(ws):
 
 
 # ----------------------------------------------------------------- GPU arm
-def bench_prefill(args, ws, rank, dev):
+def bench_prefill(args, ws, rank, dev, name=PREFILL):
     from channelwise_gated_delta_gb300 import gdr_forward, gdr_trace_enable, gdr_trace_read
     from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw_workload
 
-    w = WORKLOADS[PREFILL]
+    w = WORKLOADS[name]
     d = draw_workload(w, seed=1000 + rank, device=dev)
     out = torch.empty(w.B, w.T, w.HV, w.dv, dtype=w.dtype, device=dev)
     ht = torch.empty(w.B, w.HV, w.dk, w.dv, dtype=torch.float32, device=dev)
@@ -405,6 +408,38 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind):
+    """prefill_t4k (B=1, 32 value heads): one line of its own.  The automatic
+    route cuts the state scan into segments here, so a step is several
+    launches (the segment waves, their state set-up and the map combine);
+    its roofline is the step's algorithmic bytes over the device time of
+    all of them."""
+    args.no_e2e = True
+    pre = bench_prefill(args, ws, rank, dev, name="prefill_t4k")
+    w = pre["w"]
+    bytes_step, per_token = prefill_bytes_per_launch(w)
+    trace = pre["trace"]
+    dev_ms = sum(v[1] for v in trace.values())
+    roof = roofline("step: " + " + ".join(sorted(trace)), args.steps, dev_ms, bytes_step,
+                    hbm_peak, peak_kind)
+    roof["algorithmic_bytes_per_token"] = per_token
+    line = {
+        "metric": "GDR prefill tokens/s [prefill_t4k]", "value": round(pre["tokens_per_s"], 1),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(pre["ms"] / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B1 T4096 HK16 HV32 dk=dv=128 chunk64, bf16 q/k/v, "
+                               "f32 g/beta, no h0, final state stored",
+                   "l2": "inputs 168 MB > 129 MB L2, streamed once per step"},
+        "roofline": roof,
+        "kernels": {k: {"launches": v[0], "ms_total": round(v[1], 3)} for k, v in trace.items()},
+        "gpu_launches": sum(v[0] for v in trace.values()),
+        "clocks": pre["clocks"],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -422,6 +457,12 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
     hbm_peak, _, peak_kind = load_peaks()
 
+    if args.workload == "prefill_t4k":
+        bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.workload == "decode":
         dec = bench_decode(args, ws, rank, dev, hbm_peak, peak_kind)
         if rank == 0:

@@ -7,6 +7,7 @@ import torch
 
 import oracle
 from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE_GENERIC,
+                                           GDR_FLAG_NO_SEGMENTS,
                                            GdrError, gdr_device_check, gdr_forward, gdr_forward_varlen,
                                            gdr_varlen_workspace_bytes)
 from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw, draw_workload, pack, to_f64
@@ -32,12 +33,13 @@ def run_varlen(seqs, chunk, flags=0, inplace=False, store_ht=True):
 
 
 def run_each(seqs, chunk, flags=0):
-    """One gdr_forward call per sequence; returns (outs, hts) lists."""
+    """One gdr_forward call per sequence, the state scan unsegmented (as in
+    the packed entry); returns (outs, hts) lists."""
     outs, hts = [], []
     for d in seqs:
         c = to_cuda(d)
         o, h = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], chunk=chunk,
-                           flags=flags)
+                           flags=flags | GDR_FLAG_NO_SEGMENTS)
         outs.append(o)
         hts.append(h)
     gdr_device_check()
