@@ -45,8 +45,8 @@ NCU_TRAFFIC = {
     # decode B64: one launch of the persistent bulk-copy kernel, --set full
     # capture (136.4 MB read + 74.2 MB written)
     "gdr_decode_kernel": {"bytes": 210_509_000, "sha": "5f7ea947d98305b5"},
-    # prefill_t16k: one launch, --set full capture (2.165 GB read + 0.521 GB written)
-    "gdr_prefill_fused": {"bytes": 2_686_430_000, "sha": "a8e9ecbf981a3f54"},
+    # prefill_t16k: one launch, DRAM counters (2.165 GB read + 0.521 GB written)
+    "gdr_prefill_fused": {"bytes": 2_685_396_000, "sha": "5b016de430e8fb57"},
 }
 
 
