@@ -34,7 +34,8 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
                 4: "GDR_ERR_ALIGN", 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA",
                 7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_ALIAS"}
 
-EXPORTED = ("gdr_workspace_bytes", "gdr_forward_ex", "gdr_forward", "gdr_forward_chunked_noalloc",
+EXPORTED = ("gdr_workspace_bytes", "gdr_set_workspace", "gdr_forward_ex", "gdr_forward",
+            "gdr_forward_chunked_noalloc",
             "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_tree_workspace_bytes",
             "gdr_forward_tree", "gdr_host_staging_bytes", "gdr_forward_host", "gdr_device_check",
             "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma", "gdr_status_string",
@@ -61,6 +62,8 @@ def load_library(path=LIB_PATH):
     lib = ctypes.CDLL(path)
     vp, sz, i, u = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint
     fwd = [vp] * 8 + [i] * 7 + [vp, i]
+    lib.gdr_set_workspace.argtypes = [vp, sz]
+    lib.gdr_set_workspace.restype = i
     lib.gdr_workspace_bytes.argtypes = [i] * 8 + [u]
     lib.gdr_workspace_bytes.restype = sz
     lib.gdr_forward_ex.argtypes = fwd + [vp, sz, u]
@@ -179,6 +182,28 @@ def gdr_forward(q, k, v, g, beta, h0=None, out=None, ht=None, chunk=64, stream=N
                             ctypes.c_void_p(stream.cuda_stream), code, ws_ptr, ws_bytes, flags)
     _check(lib, st)
     return out, ht
+
+
+_registered_ws = {}
+
+
+def gdr_set_workspace(workspace, device=None):
+    """Registers ``workspace`` (a CUDA uint8 tensor, 256-byte aligned, or None
+    to go back to the library's own) as the workspace of the C entry
+    ``gdr_forward`` on its device.  A reference is kept while registered."""
+    lib = load_library()
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        with torch.cuda.device(dev):
+            _check(lib, lib.gdr_set_workspace(None, 0))
+        _registered_ws.pop(dev.index, None)
+        return
+    if workspace.device.type != "cuda":
+        raise ValueError("the workspace must be a CUDA tensor")
+    with torch.cuda.device(workspace.device):
+        _check(lib, lib.gdr_set_workspace(_ptr(workspace),
+                                          workspace.numel() * workspace.element_size()))
+    _registered_ws[workspace.device.index] = workspace
 
 
 def _cu_array(cu_seqlens):

@@ -275,10 +275,13 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
     return GDR_OK;
 }
 
-// Library-owned workspace, one per device.
+// gdr_forward's workspace, one per device: the caller's (gdr_set_workspace)
+// when registered, else the library's own, grown on demand.
 struct OwnedWorkspace {
-    void *ptr = nullptr;
+    void *ptr = nullptr;   // library-owned
     size_t bytes = 0;
+    void *user = nullptr;  // caller-owned, registered
+    size_t user_bytes = 0;
 };
 std::mutex g_ws_mutex;
 std::vector<OwnedWorkspace> g_ws;
@@ -446,6 +449,10 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
         std::lock_guard<std::mutex> lock(g_ws_mutex);
         if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
         OwnedWorkspace &w = g_ws[dev];
+        if (w.user) {
+            if (w.user_bytes < need) return GDR_ERR_WORKSPACE;
+            return run(p, r, 0u, w.user, static_cast<cudaStream_t>(stream));
+        }
         if (w.bytes < need) {
             if (w.ptr) {
                 // the old buffer may still be in use by earlier launches
@@ -462,6 +469,19 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
         ws = w.ptr;
     }
     return run(p, r, 0u, ws, static_cast<cudaStream_t>(stream));
+}
+
+GDR_API gdr_status gdr_set_workspace(void *dev_ptr, size_t bytes) {
+    if (bytes > 0 && !dev_ptr) return GDR_ERR_NULL;
+    if (dev_ptr && ((uintptr_t)dev_ptr & 255u) != 0) return GDR_ERR_ALIGN;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
+    g_ws[dev].user = (dev_ptr && bytes > 0) ? dev_ptr : nullptr;
+    g_ws[dev].user_bytes = g_ws[dev].user ? bytes : 0;
+    return GDR_OK;
 }
 
 GDR_API size_t gdr_varlen_workspace_bytes(const int *cu_seqlens, int N, int HK, int HV, int dk,

@@ -156,6 +156,20 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
                                void *stream, int qkv_dtype);
 
 /*
+ * Registers a caller-owned device workspace for gdr_forward on the current
+ * device: from now on gdr_forward uses it instead of allocating, and a call
+ * that needs more than `bytes` returns GDR_ERR_WORKSPACE (size it with
+ * gdr_workspace_bytes for the largest call).  `dev_ptr` must be 256-byte
+ * aligned (GDR_ERR_ALIGN) and non-NULL when bytes > 0 (GDR_ERR_NULL); it
+ * stays the caller's, must outlive the work enqueued with it, and must not
+ * be used by anything else meanwhile.  dev_ptr = NULL (or bytes = 0) goes back
+ * to the library's own workspace.  The library's buffer, if one was
+ * allocated, is kept.  gdr_forward_ex and the other entries take their
+ * workspace per call and ignore this.
+ */
+GDR_API gdr_status gdr_set_workspace(void *dev_ptr, size_t bytes);
+
+/*
  * Size in bytes of the fixed device scratch array behind
  * gdr_forward_chunked_noalloc (64 MiB, held on every device that loads the
  * library until the process exits).

@@ -128,6 +128,12 @@ def test_segmented_scan_workspace(lib):
         gdr_flag_segments(1)
 
 
+def test_set_workspace_argument_checks(lib):
+    """gdr_set_workspace checks its arguments before it looks for a device."""
+    assert lib.gdr_set_workspace(None, 4096) == 1                  # GDR_ERR_NULL
+    assert lib.gdr_set_workspace(ctypes.c_void_p(FAKE + 16), 4096) == 4  # GDR_ERR_ALIGN
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from channelwise_gated_delta_gb300 import _binding
     with pytest.raises(RuntimeError, match="not built"):
