@@ -451,9 +451,8 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
         OwnedWorkspace &w = g_ws[dev];
         if (w.user) {
             if (w.user_bytes < need) return GDR_ERR_WORKSPACE;
-            return run(p, r, 0u, w.user, static_cast<cudaStream_t>(stream));
-        }
-        if (w.bytes < need) {
+            ws = w.user;
+        } else if (w.bytes < need) {
             if (w.ptr) {
                 // the old buffer may still be in use by earlier launches
                 e = cudaDeviceSynchronize();
@@ -466,7 +465,7 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
             if (e != cudaSuccess) return cuda_fail(e);
             w.bytes = need;
         }
-        ws = w.ptr;
+        if (!ws) ws = w.ptr;
     }
     return run(p, r, 0u, ws, static_cast<cudaStream_t>(stream));
 }
