@@ -46,7 +46,6 @@ constexpr size_t kSlotFloats = (size_t)kD * kD;
 constexpr int kMinSegmentChunks = 8;
 constexpr int kCombineThreads = 256;
 constexpr int kMtLd = kD + 4;  // transposed M rows, padded (16-byte aligned)
-constexpr size_t kCombineSmem = ((size_t)kD * kMtLd + (size_t)kD * 32) * sizeof(float);
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -160,46 +159,52 @@ __global__ void __launch_bounds__(kInitThreads) gdr_segment_init(const float *__
 }
 
 // S_{p+1} = M_p S_p + c_p for p = 1 .. P-2, in place on the X slots.  One
-// CTA per (b, hv, 32-column slab of the state): the columns of the state are
-// independent, so the slab walks the whole chain alone, kept in shared
+// CTA per (b, hv, SLAB-column slab of the state): the columns of the state
+// are independent, so the slab walks the whole chain alone, kept in shared
 // memory between steps.  M_p is staged transposed (Mt[k][r]) so that a
-// thread's four rows at one k are one float4; each thread owns a 4 x 4 tile
-// (rows 4 rg .., columns 4 cg .. of the slab).  f32 FMAs, k in order.
+// thread's R = SLAB / 8 rows at one k are one vector load; each thread owns
+// an R x 4 tile (rows R rg .., columns 4 cg .. of the slab).  f32 FMAs, k in
+// order.  SLAB = 16 (eight CTAs per head) when that many CTAs fit on the
+// SMs at once, else 32.
+template <int SLAB>
 __global__ void __launch_bounds__(kCombineThreads) gdr_segment_combine(float *__restrict__ state,
                                                                        int HV, int P) {
+    constexpr int R = SLAB / 8, CG = SLAB / 4, NS = kD / SLAB;
+    static_assert(R * 4 * kCombineThreads == kD * SLAB, "one R x 4 tile per thread");
     extern __shared__ float smc[];
     float *Mt = smc;                 // [128][kMtLd]
-    float *Xs = smc + kD * kMtLd;    // [128][32]
-    const int slab = blockIdx.x & 3, head = blockIdx.x >> 2;
+    float *Xs = smc + kD * kMtLd;    // [128][SLAB]
+    const int slab = blockIdx.x % NS, head = blockIdx.x / NS;
     const int hv = head % HV, b = head / HV;
     const int group = 2 * P - 3;
     auto slot = [&](int j) { return state + ((size_t)(b * group + j) * HV + hv) * kSlotFloats; };
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c0 = 32 * slab;
-    const int cg = lane & 7, rg = 4 * warp + (lane >> 3);
+    const int tid = threadIdx.x;
+    const int c0 = SLAB * slab;
+    const int cg = tid % CG, rg = tid / CG;
+    constexpr int kXLoads = kD * SLAB / 4 / kCombineThreads;
 
     {
         const float *x1 = slot(0);
-        float4 x[kD * 8 / kCombineThreads];
+        float4 x[kXLoads];
 #pragma unroll
-        for (int u = 0; u < kD * 8 / kCombineThreads; ++u) {
-            const int i = tid + u * kCombineThreads, r = i >> 3, qd = i & 7;
+        for (int u = 0; u < kXLoads; ++u) {
+            const int i = tid + u * kCombineThreads, r = i / CG, qd = i % CG;
             x[u] = *reinterpret_cast<const float4 *>(x1 + (size_t)r * kD + c0 + 4 * qd);
         }
 #pragma unroll
-        for (int u = 0; u < kD * 8 / kCombineThreads; ++u) {
-            const int i = tid + u * kCombineThreads, r = i >> 3, qd = i & 7;
-            *reinterpret_cast<float4 *>(Xs + r * 32 + 4 * qd) = x[u];
+        for (int u = 0; u < kXLoads; ++u) {
+            const int i = tid + u * kCombineThreads, r = i / CG, qd = i % CG;
+            *reinterpret_cast<float4 *>(Xs + r * SLAB + 4 * qd) = x[u];
         }
     }
     for (int p = 1; p <= P - 2; ++p) {
         const float *M = slot(2 * p - 1);
         float *X = slot(2 * p);  // c_p in, S_{p+1} out
         // this thread's c_p tile and M_p share, all loads in flight at once
-        float4 cv[4];
+        float4 cv[R];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            cv[i] = *reinterpret_cast<const float4 *>(X + (size_t)(4 * rg + i) * kD + c0 + 4 * cg);
+        for (int e = 0; e < R; ++e)
+            cv[e] = *reinterpret_cast<const float4 *>(X + (size_t)(R * rg + e) * kD + c0 + 4 * cg);
         constexpr int kMLoads = kD * (kD / 4) / kCombineThreads;
         float4 m[kMLoads];
 #pragma unroll
@@ -220,29 +225,39 @@ __global__ void __launch_bounds__(kCombineThreads) gdr_segment_combine(float *__
             Mt[(4 * kq + 3) * kMtLd + r] = m[u].w;
         }
         __syncthreads();
-        float acc[4][4] = {};
+        float acc[R][4] = {};
 #pragma unroll 8
         for (int k = 0; k < kD; ++k) {
-            const float4 m = *reinterpret_cast<const float4 *>(Mt + k * kMtLd + 4 * rg);
-            const float4 x = *reinterpret_cast<const float4 *>(Xs + k * 32 + 4 * cg);
-            const float mv[4] = {m.x, m.y, m.z, m.w}, xv[4] = {x.x, x.y, x.z, x.w};
+            float mv[R];
+            if constexpr (R == 4) {
+                const float4 mk = *reinterpret_cast<const float4 *>(Mt + k * kMtLd + R * rg);
+                mv[0] = mk.x, mv[1] = mk.y, mv[2] = mk.z, mv[3] = mk.w;
+            } else {
+                const float2 mk = *reinterpret_cast<const float2 *>(Mt + k * kMtLd + R * rg);
+                mv[0] = mk.x, mv[1] = mk.y;
+            }
+            const float4 x = *reinterpret_cast<const float4 *>(Xs + k * SLAB + 4 * cg);
+            const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int e = 0; e < R; ++e)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(mv[i], xv[jj], acc[i][jj]);
+                for (int jj = 0; jj < 4; ++jj) acc[e][jj] = fmaf(mv[e], xv[jj], acc[e][jj]);
         }
         __syncthreads();  // every read of Xs done before it is overwritten
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 4 * rg + i;
-            float4 *dst = reinterpret_cast<float4 *>(X + (size_t)r * kD + c0 + 4 * cg);
-            const float4 c = cv[i];
-            const float4 y = make_float4(acc[i][0] + c.x, acc[i][1] + c.y, acc[i][2] + c.z,
-                                         acc[i][3] + c.w);
-            *dst = y;
-            *reinterpret_cast<float4 *>(Xs + r * 32 + 4 * cg) = y;
+        for (int e = 0; e < R; ++e) {
+            const int r = R * rg + e;
+            const float4 c = cv[e];
+            const float4 y = make_float4(acc[e][0] + c.x, acc[e][1] + c.y, acc[e][2] + c.z,
+                                         acc[e][3] + c.w);
+            *reinterpret_cast<float4 *>(X + (size_t)r * kD + c0 + 4 * cg) = y;
+            *reinterpret_cast<float4 *>(Xs + r * SLAB + 4 * cg) = y;
         }
     }
+}
+
+constexpr size_t combine_smem(int slab) {
+    return ((size_t)kD * kMtLd + (size_t)kD * slab) * sizeof(float);
 }
 
 }  // namespace
@@ -334,14 +349,19 @@ cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *works
                                  stream);
     if (e != cudaSuccess) return e;
     if (s.P >= 3) {
-        e = cudaFuncSetAttribute(gdr_segment_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kCombineSmem);
-        if (e != cudaSuccess) return e;
-        trace_begin(kKernSegCombine, stream);
-        gdr_segment_combine<<<(unsigned)(p.B * p.HV * (kD / 32)), kCombineThreads, kCombineSmem,
-                              stream>>>(state, p.HV, s.P);
-        trace_end(kKernSegCombine, stream);
-        e = cudaGetLastError();
+        const int sms = sm_count();
+        const bool narrow = sms > 0 && (long long)p.B * p.HV * (kD / 16) <= sms;
+        auto combine = [&](auto kernel, int slab) -> cudaError_t {
+            cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)combine_smem(slab));
+            if (r != cudaSuccess) return r;
+            trace_begin(kKernSegCombine, stream);
+            kernel<<<(unsigned)(p.B * p.HV * (kD / slab)), kCombineThreads, combine_smem(slab),
+                     stream>>>(state, p.HV, s.P);
+            trace_end(kKernSegCombine, stream);
+            return cudaGetLastError();
+        };
+        e = narrow ? combine(gdr_segment_combine<16>, 16) : combine(gdr_segment_combine<32>, 32);
         if (e != cudaSuccess) return e;
     }
     wave.B = s.nB;
