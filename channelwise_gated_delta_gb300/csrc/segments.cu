@@ -16,10 +16,10 @@
 //
 // Both waves are the packed-sequence tensor-core kernel: every run is one
 // "sequence" with its own tensor maps and state slot.  The map runs read
-// their values from a one-row zero tensor (every other row is the loads'
-// zero fill) and send their outputs to a one-row scratch tensor (every other
-// row falls outside it and is dropped), so they move no value or output
-// bytes.  The critical path is two segments instead of P.
+// their values from a one-row zero tensor (each row past row 0 is the loads'
+// zero fill) and send their outputs to a one-row scratch tensor (each row
+// past row 0 falls outside it and is dropped), so they move no value or
+// output bytes.  The critical path is two segments instead of P.
 //
 // State slots, a group of 2P-3 per batch element b (each slot HV x [128][128]
 // f32): X_1, M_1, X_2, M_2, X_3, ..., M_{P-2}, X_{P-1} -- X_p at 2(p-1), M_p
