@@ -280,6 +280,8 @@ int segment_count(const Problem &p, unsigned flags) {
     }
     const Segments s = plan(p, P);
     if (s.P < 2 || (!forced && s.P < 3)) return 0;
+    // every grid (4 blocks per slot and head at most) and slot index in int
+    if ((long long)s.nA * p.HV * 4 > 0x7fffffffLL) return 0;
     return s.P;
 }
 
