@@ -174,12 +174,17 @@ def decode_bytes_per_launch(w):
     return state + small, state
 
 
+# GB300 HBM3e nominal bandwidth, reported beside the measured-peak fraction
+NOMINAL_HBM_GBS = 8000.0
+
+
 def roofline(kernel, launches, total_ms, bytes_per_launch, peak, peak_kind):
     avg_s = total_ms / 1e3 / max(launches, 1)
     achieved = bytes_per_launch / avg_s / 1e9
     return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel),
+            "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
             "avg_launch_us": round(avg_s * 1e6, 2), "launches": launches}
 
 
