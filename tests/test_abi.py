@@ -128,6 +128,25 @@ def test_segmented_scan_workspace(lib):
         gdr_flag_segments(1)
 
 
+@pytest.mark.parametrize("T", [65, 128, 129, 300, 1000, 4096, 4097])
+@pytest.mark.parametrize("P", [2, 3, 4, 5, 7, 16, 100])
+def test_segment_count_matches_oracle_bounds(lib, T, P):
+    """The library's segment plan (read back from its state slots: 2P-3 per
+    batch element and head) cuts a sequence into as many pieces as the
+    oracle's segment_bounds, which are written independently."""
+    import oracle
+    from channelwise_gated_delta_gb300 import gdr_flag_segments
+    B, HV = 2, 4
+    need = lib.gdr_workspace_bytes(B, T, 2, HV, 128, 128, 64, 1, gdr_flag_segments(P))
+    want = len(oracle.segment_bounds(T, 64, P))
+    if want < 2:
+        assert need == 0
+        return
+    state = B * HV * 128 * 128 * 4
+    slots = need // state              # the tables and two rows stay under one slot
+    assert slots == 2 * want - 3, (T, P, slots, want)
+
+
 def test_set_workspace_argument_checks(lib):
     """gdr_set_workspace checks its arguments before it looks for a device."""
     assert lib.gdr_set_workspace(None, 4096) == 1                  # GDR_ERR_NULL
