@@ -8,7 +8,7 @@ from ._binding import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE
                        GdrError, gdr_device_check, gdr_forward, gdr_forward_host,
                        gdr_forward_tree, gdr_host_staging_bytes,
                        gdr_forward_varlen, gdr_tree_workspace_bytes,
-                       gdr_selftest_umma, gdr_set_workspace,
+                       gdr_set_workspace,
                        gdr_trace_enable,
                        gdr_trace_read, gdr_version,
                        gdr_varlen_workspace_bytes, gdr_workspace_bytes, load_library)
@@ -16,7 +16,7 @@ from ._binding import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE
 __all__ = ["gdr_forward", "gdr_workspace_bytes", "gdr_forward_varlen", "gdr_varlen_workspace_bytes",
            "gdr_forward_tree", "gdr_tree_workspace_bytes", "gdr_forward_host",
            "gdr_host_staging_bytes", "gdr_device_check", "gdr_version", "gdr_set_workspace",
-           "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma",
+           "gdr_trace_enable", "gdr_trace_read",
            "load_library", "GdrError", "GDR_F32", "GDR_BF16", "GDR_FLAG_FORCE_CHUNKED",
            "GDR_FLAG_FORCE_GENERIC", "GDR_FLAG_SCALAR_GATE", "GDR_FLAG_NO_SEGMENTS",
            "gdr_flag_segments"]

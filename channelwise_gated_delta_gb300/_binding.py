@@ -38,7 +38,7 @@ EXPORTED = ("gdr_workspace_bytes", "gdr_set_workspace", "gdr_forward_ex", "gdr_f
             "gdr_forward_chunked_noalloc",
             "gdr_varlen_workspace_bytes", "gdr_forward_varlen", "gdr_tree_workspace_bytes",
             "gdr_forward_tree", "gdr_host_staging_bytes", "gdr_forward_host", "gdr_device_check",
-            "gdr_trace_enable", "gdr_trace_read", "gdr_selftest_umma", "gdr_status_string",
+            "gdr_trace_enable", "gdr_trace_read", "gdr_status_string",
             "gdr_last_cuda_error", "gdr_version")
 
 _lib = None
@@ -93,8 +93,6 @@ def load_library(path=LIB_PATH):
     lib.gdr_last_cuda_error.restype = i
     lib.gdr_version.argtypes = []
     lib.gdr_version.restype = ctypes.c_char_p
-    lib.gdr_selftest_umma.argtypes = [i, i, i, vp, vp, vp, vp]
-    lib.gdr_selftest_umma.restype = i
     lib.gdr_trace_enable.argtypes = [i]
     lib.gdr_trace_enable.restype = i
     lib.gdr_trace_read.argtypes = [i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i),
@@ -417,20 +415,6 @@ def gdr_trace_read():
     if got < 0:
         raise GdrError(6, "gdr_trace_read: a CUDA event query failed")
     return {names[i].decode(): (launches[i], total[i]) for i in range(got) if launches[i] > 0}
-
-
-def gdr_selftest_umma(A, B, a_mn_major=False, b_mn_major=False, stream=None):
-    """Diagnostic tensor-core GEMM: returns A[128, 64] @ B[N, 64]^T (f32) computed
-    through the shared-memory layouts and descriptors of the tensor-core prefill."""
-    lib = load_library()
-    N = B.shape[0]
-    D = torch.empty(A.shape[0], N, dtype=torch.float32, device=A.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(A.device)
-    st = lib.gdr_selftest_umma(int(a_mn_major), int(b_mn_major), N, _ptr(A),
-                               _ptr(B), _ptr(D), ctypes.c_void_p(stream.cuda_stream))
-    _check(lib, st)
-    return D
 
 
 def gdr_version():

@@ -311,7 +311,8 @@ cudaEvent_t take_event() {
 
 const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_prep",
                                               "gdr_chunk_scan",    "gdr_prefill_fused",
-                                              "gdr_segment_init",  "gdr_segment_combine"};
+                                              "gdr_segment_init",  "gdr_segment_combine",
+                                              "gdr_tree_tc"};
 
 }  // namespace
 

@@ -69,7 +69,8 @@ enum KernelId {
     kKernFused = 3,
     kKernSegInit = 4,
     kKernSegCombine = 5,
-    kNumKernels = 6
+    kKernTree = 6,
+    kNumKernels = 7
 };
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);

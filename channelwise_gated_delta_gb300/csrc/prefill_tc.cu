@@ -1,70 +1,70 @@
 // prefill_tc.cu -- chunkwise WY/UT prefill on the Blackwell tensor cores
-// (tcgen05 MMA, TMEM accumulators) for bf16 q/k/v with dk = dv = 128 and
-// chunks of 64 tokens, fused into one kernel.
+// (tcgen05 MMA, TMEM accumulators, TMA) for bf16 q/k/v with dk = dv = 128 and
+// chunks of 64 tokens: one warp-specialised CTA per (sequence, value head),
+// the float32 state resident in tensor memory.
 //
 // Method: page "Reorder channelwise gated delta rule chunked hot loops for
 // autovectorization" (pytorch/executorch PR #21021), second commit summary --
 // per chunk: per-channel log-decay prefix sums, the causal query/key terms,
-// the beta-folded unit-lower triangular transform, WY pseudo-keys and
-// pseudo-values, and the state carried to the next chunk, with a ragged last
-// chunk through the same code.  The triangular transform is a block forward
-// substitution (16 x 16 diagonal-block inverses, then the off-diagonal blocks
-// by small matrix products), the block-TRSM structure of trymirai/uzu PR #576
-// ("Support TreeUpdateSolve kernel", commit summary).
+// the beta-folded unit-lower triangular transform, WY pseudo-values, and the
+// state carried to the next chunk, with a ragged last chunk through the same
+// code.  The triangular transform is a block forward substitution (16 x 16
+// diagonal-block inverses, then the off-diagonal blocks by small matrix
+// products), the block-TRSM structure of trymirai/uzu PR #576 ("Support
+// TreeUpdateSolve kernel", commit summary).
 //
 // Algebra per chunk of L <= 64 tokens (r, s local token indices; S the state
 // at the chunk start; G the inclusive per-channel prefix sum of g):
 //   A[r,s] = beta_r sum_i k_ri k_si exp(G_ri - G_si)   (s < r)
 //   P[r,s] =        sum_i q_ri k_si exp(G_ri - G_si)   (s <= r)
 //   T'     = (I + A)^-1 diag(beta)
-//   U      = T' V - T' (exp(G) * K) S
+//   U      = T' (V - (exp(G) * K) S)
 //   O      = (exp(G) * Q) S + P U
 //   S     <- diag(exp(G_L)) S + (exp(G_L - G) * K)^T U
-//
-// Factoring around a reference row m of the chunk.  With
+// Factoring around a reference row m of the chunk, with
 //   Lk = K * exp(G - G_m),  Lq = Q * exp(G - G_m),  R = K * exp(G_m - G),
-//   S' = diag(exp(G_m)) S,
-// every product above is a product of these three tiles:
-//   A = tril(diag(beta) Lk R^T),  P = tril(Lq R^T),
-//   (exp(G) * K) S = Lk S',  (exp(G) * Q) S = Lq S',
-//   (exp(G_L - G) * K)^T U = diag(exp(G_L - G_m)) R^T U.
-// (In the kernel G is kept in log2 units, G * log2(e), so that every decay
-// factor is a single ex2.)
-// While every channel decays by at most 80 nats between the chunk's first
-// token and m and between m and its last token, all factors are finite and
-// the products are exact to rounding.  A chunk outside that range (decay
-// stronger than ~2.5 nats per token sustained over 32 tokens) uses m := the
-// chunk start instead (Lk = exp(G) K, Lq = exp(G) Q, R = exp(G_L - G) K, all
-// factors <= 1) and computes A and P with exact pairwise decays on CUDA
-// cores, so the result is right for any g <= 0.
+//   S' = diag(exp(G_m)) S:
+//   A = tril(diag(beta) Lk R^T),  P = tril(Lq R^T),  Z = Lk S',
+//   U = T' (V - Z),  O = Lq S' + P U,
+//   S'_next = diag(c) (S' + R^T U),  c = exp(G'_m + G_L - G_m)
+// (G'_m the next chunk's reference row; G is kept in log2 units so that every
+// factor is one ex2).  The same factor c multiplies both terms, so the state
+// update is an accumulation X += U^T R on the tensor core followed by one
+// column scaling, where X = S'^T is the state kept in TMEM.
+// While no 16-row quarter of the chunk decays by more than 80/3 nats and no
+// half by more than 43 nats in any channel, every factor lies within
+// exp(+-80) and c above exp(-86), in the normal float range.  A chunk outside
+// that range uses m := the chunk start (Lk = exp(G) K, Lq = exp(G) Q,
+// R = exp(G_L - G) K, all factors <= 1) with A and P from exact pairwise decays
+// on CUDA cores; its carry is X <- (exp(G_L) X + U^T R) c, the first factor
+// applied when X is written, so the result is right for any g <= 0.
 //
-// GB300 mapping.  One CTA (16 state warps + 4 auxiliary warps) per (batch,
-// value head) walks that head's chunks in order; the float32 state never
-// leaves registers (thread = one value column j, 32 of the 128 key rows).
-// State products are computed transposed so that M = dv = 128 fills the MMA,
-// and T' is applied after the state product so that the inverse of the next
-// chunk is off the path from one chunk's state to the next:
-//   Z^T = S'^T Lk^T,  U^T = (V^T - Z^T) T'^T,  O^T = S'^T Lq^T + U^T P^T,
-//   dS^T = U^T R.
-// The per-chunk tiles are bf16 in shared memory in the interleaved (no-swizzle)
-// core-matrix layout (sm100_ptx.cuh); R is stored once and read both K-major
-// and, through an MN-major descriptor with the two core-matrix strides
-// exchanged, transposed.  The state-dependent A operands S'^T, -Z^T and U^T
-// are written as bf16 straight into tensor memory and read from there by the
-// MMA.  Accumulators are float32 in TMEM.  Raw k, q, g and v tiles arrive by TMA tensor copies (128-byte
-// swizzled boxes; rows past the end of the sequence are zero-filled by the
-// copy engine), the next chunk's copies in flight while the current chunk's
-// solve and state products run; v lands directly in the swizzled MN-major
-// layout the tensor core reads.  The 64 x 64 inverse runs in float32:
-// diagonal 16 x 16 blocks by a right-looking sweep (one thread per column),
-// off-diagonal blocks by a 32 x 32 block recursion whose 16 x 16 products run
-// on tf32 mma.sync, on the four auxiliary warps.
+// GB300 mapping: one CTA of 20 warps per (sequence, value head) walks that
+// head's chunks in order.
+//   warps 0-7   chain warps: read back -Z, U and the state from TMEM between
+//               the state-dependent MMAs, scale the state by c, write the bf16
+//               operands S'^T, -Z^T and U^T back into TMEM, and store O.
+//   warps 8-15  prep warps: the prefix sums, range check and carry factors,
+//               the bf16 operand tiles Lq, Lk, R of the next chunk, the P
+//               read-back, and the exact pairwise path.
+//   warp 16     producer: TMA loads of k, q, g and v, and the gram
+//               [Lq; Lk] R^T of the chunk being prepared.
+//   warp 17     issues the state-dependent MMAs of the chunk being scanned:
+//               Z^T = S'^T Lk^T, O^T = S'^T Lq^T, U^T = (V^T - Z^T) T'^T,
+//               then X^T += U^T R and O^T += U^T P^T.
+//   warps 18-19 invert I + A for the chunk being prepared (its A rows are
+//               TMEM lanes 64-127, the lane quarters of these two warps).
+// Preparation of chunk c+1 starts as soon as chunk c's operand tiles have
+// been read by its O^T product, so the prefix sums, tiles, gram and inverse
+// of the next chunk overlap the state chain of the current one.  Every state
+// product is transposed so that M = dv = 128 fills the MMA; the state-side A
+// operands are bf16 in TMEM.  Every mbarrier wait is bounded.
 #include <cuda.h>
-#include <mutex>
 #include <string.h>
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.h"
 
 namespace gdr {
 namespace {
@@ -73,82 +73,92 @@ using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // dk = dv
-constexpr int kCompute = 512;               // 16 state warps
-constexpr int kThreads = kCompute + 128;    // + 4 auxiliary warps: 2 issuers, 2 solvers
-constexpr int kHand = kCompute + 64;        // state warps + issuer warps
-constexpr int kBarCompute = 1;              // named barrier: state warps only
-constexpr int kBarH1 = 2, kBarH2 = 3, kBarH4 = 4, kBarHZ = 5;  // state -> issuer handoffs (kHand threads)
-constexpr int kBarDiag = 6;                 // state -> solvers: A, P read back (kCompute + 64)
-constexpr int kBarAux = 7;                  // solver warps only (64)
-constexpr int kBarSolve = 8;                // solvers -> issuers: T' complete (128)
+constexpr int kWarps = 20;            // 5 per SM sub-partition: 96 registers a thread
+constexpr int kThreads = 32 * kWarps;
+constexpr int kWarpPrep0 = 8;        // warps 8-15
+constexpr int kWarpProducer = 16;    // TMA loads and the gram MMA
+constexpr int kWarpChainIssuer = 17;
+constexpr int kWarpSolver0 = 18;     // warps 18-19
+constexpr int kChainThreads = 256;
+constexpr int kPrepThreads = 256;
+constexpr int kHandThreads = kChainThreads + 32;  // chain warps + chain issuer warp
+// named barriers
+constexpr int kNbS = 1;      // chain -> issuer: X and S'^T of the next chunk written
+constexpr int kNbZb = 2;     // chain -> issuer: -Z^T written
+constexpr int kNbUb = 3;     // chain -> issuer: U^T written
+constexpr int kNbOfree = 4;  // chain -> issuer: O^T read
+constexpr int kNbPrep = 5;   // prep warps
+constexpr int kNbSolve = 6;  // solver warps
+
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRangeLog2 = 80.f * kLog2e;  // 80 nats, in the log2 units G is kept in
-// Fast-path decay limits: a 16-row quarter within a third of the range keeps
-// the operand factors within exp(+-80); a half chunk (two quarters) within
-// 43 nats keeps the folded carry factors, which span the second half of one
-// chunk and the first half of the next, above exp(-86), in the normal range.
-constexpr float kQuarterLog2 = kRangeLog2 * (1.f / 3.f);
+// Fast-path decay limits (log2 units): a 16-row quarter within a third of 80
+// nats keeps the operand factors within exp(+-80); a half chunk within 43
+// nats keeps the carry factor c, which spans the second half of one chunk and
+// the first half of the next, above exp(-86).
+constexpr float kQuarterLog2 = 80.f / 3.f * kLog2e;
 constexpr float kHalfLog2 = 43.f * kLog2e;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
-constexpr uint32_t kRawK = 0;                 // k: 2 TMA boxes [64 rows][64 bf16], 128B-swizzled
-constexpr uint32_t kRawQ = kRawK + 16384;     // q: same
-constexpr uint32_t kOpV = kRawQ + 16384;      // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
-constexpr uint32_t kG = kOpV + 16384;         // g: 4 boxes [64 rows][32 f32], 128B-swizzled
-                                              // (scalar gate: f32 [2][64] by chunk parity)
-constexpr uint32_t kOpL = kG + 32768;         // [128][128] K-major: rows 0-63 Lq, 64-127 Lk
-constexpr uint32_t kOpR = kOpL + 32768;       // [2][64][128] K-major: R (by chunk parity)
-constexpr uint32_t kAT = kOpR + 32768;        // 32 KB: f32 A and T (64x64 each)
-constexpr uint32_t kA32 = kAT;
-constexpr uint32_t kT32 = kAT + 16384;
-constexpr uint32_t kOpT = kAT + 32768;        // T' as K-major B [64 r][64 s]
-constexpr uint32_t kOpP = kOpT + 8192;        // [2] P as K-major B [64 r][64 s] (by chunk parity)
-constexpr uint32_t kStage = kOpP + 16384;     // bf16 O staging: per state warp one [16 r][32 j] box
-// Trees are one chunk, so the parity-1 P buffer is free: ancestor masks
-// (u64 [64]) and parents (i32 [64]) of the tree
-constexpr uint32_t kTreeAnc = kOpP + 8192;
-constexpr uint32_t kTreePar = kTreeAnc + 512;
-constexpr uint32_t kX32 = kStage + 16384;     // f32 [4][16][16] solve scratch
-constexpr uint32_t kSmall = kX32 + 4096;
-constexpr uint32_t kBeta = kSmall;            // f32 [2][64] (by chunk parity)
-constexpr uint32_t kEGm = kBeta + 512;        // f32 [2][128] exp(G_m) (by chunk parity)
-constexpr uint32_t kCL = kEGm + 1024;         // f32 [2][128] exp(G_last - G_m)
-constexpr uint32_t kRho = kCL + 1024;         // f32 [2][128] exp(G_last) / exp(G_m) (by chunk parity)
-constexpr uint32_t kTot = kRho + 1024;        // f32 [3][128] prefix-sum carries
-constexpr uint32_t kBarA = kTot + 1536;       // mbarriers: MMA batches a, b, g, 4
-constexpr uint32_t kBarB = kBarA + 8;
-constexpr uint32_t kBarG = kBarB + 8;
-constexpr uint32_t kBar4 = kBarG + 8;
-constexpr uint32_t kBarKQG = kBar4 + 8;       // mbarrier: k, q, g tiles
-constexpr uint32_t kBarV = kBarKQG + 8;       // mbarrier: v tile
-constexpr uint32_t kTmemSlot = kBarV + 8;     // u32
-constexpr uint32_t kAbort = kTmemSlot + 4;    // i32 sticky abort flag
-constexpr uint32_t kSlowFlag = kAbort + 4;    // i32 [2] (by chunk parity): the chunk takes the exact path
+constexpr uint32_t kRawK = 0;              // k: 2 TMA boxes [64 rows][64 bf16], 128B-swizzled
+constexpr uint32_t kRawQ = 16384;          // q: same
+constexpr uint32_t kG = 32768;             // g: 4 boxes [64 rows][32 f32], 128B-swizzled; then G
+constexpr uint32_t kOpV = 65536;           // v: 2 boxes [64 s][64 j] = swizzled MN-major A operand
+constexpr uint32_t kOpL = 81920;           // [128][128] K-major: rows 0-63 Lq, 64-127 Lk
+constexpr uint32_t kOpR = 114688;          // [2][64][128] K-major: R (by chunk parity)
+constexpr uint32_t kOpP = 147456;          // P as K-major B [64 r][64 s]
+constexpr uint32_t kOpT = 155648;          // T' as K-major B [64 r][64 s]
+constexpr uint32_t kA32 = 163840;          // f32 A (64 x 64, swizzled)
+constexpr uint32_t kT32 = 180224;          // f32 T
+constexpr uint32_t kX32 = 196608;          // f32 [4][16][16] solve scratch
+constexpr uint32_t kStage = 200704;        // bf16 O staging: per chain warp one [32 r][32 j] box
+constexpr uint32_t kTot = 217088;          // f32 [8][128] per-warp prefix totals
+constexpr uint32_t kGm = 221184;           // f32 [2][128] G at the reference row (by chunk parity)
+constexpr uint32_t kGL = kGm + 1024;       // f32 [2][128] G at the last row
+constexpr uint32_t kCv = kGL + 1024;       // f32 [2][128] carry factor c of the chunk scanned
+constexpr uint32_t kAv = kCv + 1024;       // f32 [2][128] pre-scale of the next chunk's X
+constexpr uint32_t kGsc = kAv + 1024;      // f32 [64] scalar gate: G of the chunk prepared
+constexpr uint32_t kBeta = kGsc + 256;     // f32 [64] beta of the chunk being inverted
+constexpr uint32_t kBars = kBeta + 256;    // mbarriers
+enum {
+    MB_RAW = 0,  // k, q, g tiles landed (TMA)
+    MB_V,        // v tile landed (TMA)
+    MB_TILES,    // operand tiles, carry factors, slow flag of a chunk written (prep)
+    MB_GRAM,     // gram complete, or the exact path's A and P written
+    MB_GFREE,    // gram read back and A consumed (solvers, P readers)
+    MB_TP,       // T' and P written (solvers, P readers)
+    MB_Z,        // Z^T product complete
+    MB_OPART,    // O^T = S'^T Lq^T complete: the Lq, Lk tiles are free
+    MB_U,        // U^T product complete: T' and v buffers free
+    MB_X,        // state and output accumulations complete
+    kNumBars
+};
+constexpr uint32_t kTmemSlot = kBars + 8 * kNumBars;
+constexpr uint32_t kAbort = kTmemSlot + 4;   // i32 sticky abort flag
+constexpr uint32_t kSlowFlag = kAbort + 4;   // i32 [2] (by chunk parity)
 constexpr uint32_t kSmemUsed = kSlowFlag + 8;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack for the 1024-byte base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kTot >= kStage + 16384, "layout");
 constexpr uint32_t kBytesKQG = 16384 + 16384 + 32768;
 constexpr uint32_t kBytesV = 16384;
 
 // ---- TMEM columns (float32 accumulators, lane = M row)
-constexpr uint32_t kTmGram = 0;     // [128 x 64]: rows 0-63 Lq R^T (P), 64-127 Lk R^T (A)
-constexpr uint32_t kTmZT = 64;      // [128 j x 64 r]  Z^T = (Lk S')^T
-constexpr uint32_t kTmUT = 128;     // [128 j x 64 r]
-constexpr uint32_t kTmOT = 192;     // [128 j x 64 r]
-constexpr uint32_t kTmDS = 256;     // [128 j x 128 i]
-constexpr uint32_t kTmSTb = 384;    // S'^T as bf16 A operand: [128 j x 128 i], 2 per column
-constexpr uint32_t kTmUTb = 448;    // U^T as bf16 A operand: [128 j x 64 r], 2 per column
-constexpr uint32_t kTmZTb = 480;    // -Z^T as bf16 A operand: [128 j x 64 r], 2 per column
+constexpr uint32_t kTmGram = 0;   // [128 x 64]: rows 0-63 Lq R^T (P), 64-127 Lk R^T (A)
+constexpr uint32_t kTmZ = 64;     // [128 j x 64 r]  Z^T
+constexpr uint32_t kTmU = 128;    // [128 j x 64 r]  U^T
+constexpr uint32_t kTmO = 192;    // [128 j x 64 r]  O^T
+constexpr uint32_t kTmX = 256;    // [128 j x 128 i] the state X = S'^T
+constexpr uint32_t kTmSb = 384;   // S'^T as bf16 A operand, 2 per column
+constexpr uint32_t kTmUb = 448;   // U^T as bf16 A operand
+constexpr uint32_t kTmZb = 480;   // -Z^T as bf16 A operand
 constexpr uint32_t kTmemCols = 512;
 
 // 64 x 64 f32 tiles (A, T) with an XOR swizzle: rows and columns both walk
 // conflict-free
 __device__ __forceinline__ int sq_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
-// In the swizzled tile the 16 entries of row r inside diagonal block I = r / 16
-// occupy one aligned group of 16 floats, at r * 64 + 32 * (I / 2).  The
-// diagonal blocks of A are only read by the diagonal inverses, so they are
-// stored transposed there: A[16 I + p][16 I + q] at row 16 I + q, slot p, and
+// The diagonal blocks of A are only read by the diagonal inverses, so they
+// are stored transposed: A[16 I + p][16 I + q] at row 16 I + q, slot p, and
 // column q of a block is one contiguous run of 16 floats.
 __device__ __forceinline__ int diagT_idx(int I, int q, int p) { return (16 * I + q) * 64 + 32 * (I >> 1) + p; }
 // byte offset of bf16 element (r, i) of a k or q tile (two 64-channel boxes)
@@ -186,13 +196,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
 
-// Issues the K-steps of one GEMM, D (+)= A * B^T, each K-step of 16
-// advancing the operand start addresses by two core matrices along K.
-// Issues K_STEPS MMAs D (+)= A * B^T with shared-memory operands.  The
-// descriptors are built once; each K-step advances the start-address field
-// (address / 16, bits 0-13) by a fixed number of bytes, which never carries
-// out of the field for addresses inside shared memory.
+// D (+)= A * B^T with shared-memory operands, K_STEPS steps of K = 16; each
+// step advances the descriptors' start-address field (address / 16) by a
+// fixed number of bytes, which never carries out of the field inside shared
+// memory.
 template <int K_STEPS>
 __device__ __forceinline__ void gemm_ss(uint32_t d_tmem, uint64_t a_desc, uint32_t a_step,
                                         uint64_t b_desc, uint32_t b_step, uint32_t idesc,
@@ -215,8 +226,8 @@ __device__ __forceinline__ void gemm_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 }
 
 // Bounded wait on an mbarrier phase.  A timeout sets the CTA's sticky abort
-// flag; later waits then return at once, and the chunk loop ends at its next
-// barrier, so a stuck copy or MMA can never hang the kernel.
+// flag; later waits then return at once, nothing new is issued, and every
+// group runs out its loop, so a stuck copy or MMA can never hang the kernel.
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (*abort_flag) return;
     if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) *abort_flag = 1;
@@ -231,37 +242,8 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-struct TileMaps {
-    CUtensorMap k, q, g, v, o;
-};
-
-// Lanes 0-7 of one warp: the k, q and g boxes of one chunk (tokens t0 ..
-// t0+63), one box per lane, after lane 0 has announced the byte count.  A
-// scalar gate's g is not a tile: only k and q come by TMA.
-template <bool WITH_G>
-__device__ __forceinline__ void issue_kqg(unsigned char *sm, const TileMaps &tm, uint64_t *bar,
-                                          int b, int t0, int hk, int hv, int lane) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, WITH_G ? kBytesKQG : kBytesKQG - 32768);
-    __syncwarp();
-    if (lane < 2)
-        tma_load_4d(sm + kRawK + 8192 * lane, &tm.k, 64 * lane, hk, t0, b, bar);
-    else if (lane < 4)
-        tma_load_4d(sm + kRawQ + 8192 * (lane - 2), &tm.q, 64 * (lane - 2), hk, t0, b, bar);
-    else if (WITH_G && lane < 8)
-        tma_load_4d(sm + kG + 8192 * (lane - 4), &tm.g, 32 * (lane - 4), hv, t0, b, bar);
-}
-__device__ __forceinline__ void issue_v(unsigned char *sm, const TileMaps &tm, uint64_t *bar, int b,
-                                        int t0, int hv) {
-    mbar_arrive_expect_tx(bar, kBytesV);
-    tma_load_4d(sm + kOpV, &tm.v, 0, hv, t0, b, bar);
-    tma_load_4d(sm + kOpV + 8192, &tm.v, 64, hv, t0, b, bar);
-}
-
 // Block (I, J) of a swizzled 64 x 64 f32 tile: with R = 16 I + r, element
-// (r, c) sits at R * 64 + 16 (J ^ (I & 1)) + (c ^ r) -- the row's 16 block
-// entries form one aligned group, permuted by r.  swz_block returns the
-// group base of row 0; the per-lane offsets below add the rest.
+// (r, c) sits at R * 64 + 16 (J ^ (I & 1)) + (c ^ r).
 __device__ __forceinline__ const float *swz_block(const float *tile, int I, int J) {
     return tile + I * 1024 + 16 * (J ^ (I & 1));
 }
@@ -289,8 +271,6 @@ __device__ __forceinline__ void blk_mma2(float (&acc)[2][4], const float *X, con
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
         uint32_t a[4];
-        // rows gq and gq + 8 (+512), columns 8 kh + tq and 8 kh + tq + 4;
-        // row gq + 8 flips bit 3 of the permuted column
         a[0] = __float_as_uint(X[f.a0 + 8 * kh]);
         a[1] = __float_as_uint(X[f.a0 + 512 + 8 * (kh ^ 1)]);
         a[2] = __float_as_uint(X[f.a1 + 8 * kh]);
@@ -298,7 +278,7 @@ __device__ __forceinline__ void blk_mma2(float (&acc)[2][4], const float *X, con
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;
-            if (SWZ_Y) {  // rows 8 kh + tq (+4), column 8 nt + gq
+            if (SWZ_Y) {
                 b0 = __float_as_uint(Y[f.b0 + 512 * kh + 8 * (nt ^ kh)]);
                 b1 = __float_as_uint(Y[f.b1 + 512 * kh + 8 * (nt ^ kh)]);
             } else {
@@ -309,7 +289,6 @@ __device__ __forceinline__ void blk_mma2(float (&acc)[2][4], const float *X, con
         }
     }
 }
-// C tiles of one warp's 16 x 16 result -> f32 [16][16] scratch
 __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], int lane) {
     const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
@@ -321,41 +300,25 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
     }
 }
 
-// Packed variable-length batches: one record per sequence, {first token row
-// in the packed tensors, length, state slot}; the sequence's tensor maps sit
-// at the same index of a TileMaps array in global memory.
-// TREE: each batch element's T <= 64 tokens are a draft-token tree, parents
-// [B][T] (-1 for a root), run as one chunk with no state carry (page "Support
-// TreeUpdateSolve kernel", trymirai/uzu PR #576): the prefix sums of g run
-// along root paths, the decay reference is the tree's start (G_m = 0), and
-// the ancestor relation replaces the causal order in A and P.
+struct TileMaps {
+    CUtensorMap k, q, g, v, o;
+};
+
+// Packed variable-length batches (VARLEN): one record per sequence, {first
+// token row in the packed tensors, length, state slot}; the sequence's tensor
+// maps sit at the same index of a TileMaps array in global memory.
 // SCALAR_G: g is one log-decay per token and value head (gsc, [rows][HV]),
-// the same for every key channel; it is loaded like beta, its prefix sum is
-// one warp scan, and each row's decay factors are one exponential.
-template <bool HAS_H0, bool STORE_HT, bool VARLEN, bool TREE, bool SCALAR_G>
+// the same for every key channel.
+template <bool HAS_H0, bool STORE_HT, bool VARLEN, bool SCALAR_G>
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_prefill_tc_kernel(const __grid_constant__ TileMaps tm, const TileMaps *seq_maps,
-                          const int4 *seqs, const int *parents, const float *__restrict__ beta,
+                          const int4 *seqs, const float *__restrict__ beta,
                           const float *__restrict__ gsc, const float *h0, float *ht, int T_dense,
                           int HK, int HV, int *dev_error) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte aligned base: the swizzled TMA boxes and descriptors need it
-    unsigned char *smem =
-        smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // Warps 0-15 own the state and do the per-chunk element-wise work; warps
-    // 16-19 are auxiliary.  Warps 16 and 17 issue the MMAs (lane 0 of each,
-    // on independent accumulators) and warp 17 the TMA loads; warps 18 and
-    // 19 invert I + A for the next chunk while the state warps run the
-    // current chunk's state products.
-    const bool aux = tid >= kCompute;
-    const int aw = warp - kCompute / 32;  // auxiliary warp index 0..3
-    const bool issuer_warp = aux && aw < 2;
-    const bool issuer_a = aux && aw == 0;
-    const int sw = aw - 2;                // solver warp index 0..1
-    const int wq = warp & 3;        // TMEM lane quarter of this warp
-    const int iq = (warp >> 2) & 3; // which quarter of the key channels / tokens this warp takes
     const int head = blockIdx.x;    // b * HV + hv (b: the sequence's index)
     const int hv = head % HV;
     int b = head / HV;              // batch coordinate of the tensor maps
@@ -371,407 +334,207 @@ __global__ void __launch_bounds__(kThreads, 1)
         shead = (size_t)sd.z * HV + hv;
         mp = seq_maps + b;
         b = 0;  // each sequence's maps describe a [1][T][H][128] tensor
-        // the maps were written to global memory before the launch: order
-        // those writes before this thread's tensor-map reads
-        fence_tensormap_acquire(&mp->k);
-        fence_tensormap_acquire(&mp->q);
-        fence_tensormap_acquire(&mp->g);
-        fence_tensormap_acquire(&mp->v);
-        fence_tensormap_acquire(&mp->o);
     }
     const TileMaps &m = *mp;
-    const int j = 32 * wq + lane;   // this thread's value column (TMEM lane)
+    const int NC = (T + kC - 1) / kC;
 
-    float *sTot = reinterpret_cast<float *>(smem + kTot);
-    float *sA = reinterpret_cast<float *>(smem + kA32);
-    float *sT = reinterpret_cast<float *>(smem + kT32);
-    float *sX = reinterpret_cast<float *>(smem + kX32);
-    uint64_t *bar_a = reinterpret_cast<uint64_t *>(smem + kBarA);
-    uint64_t *bar_b = reinterpret_cast<uint64_t *>(smem + kBarB);
-    uint64_t *bar_g = reinterpret_cast<uint64_t *>(smem + kBarG);
-    uint64_t *bar_4 = reinterpret_cast<uint64_t *>(smem + kBar4);
-    uint64_t *bar_kqg = reinterpret_cast<uint64_t *>(smem + kBarKQG);
-    uint64_t *bar_v = reinterpret_cast<uint64_t *>(smem + kBarV);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBars);
+    auto bar = [&](int i) { return bars + i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kAbort);
     volatile int *slow_flag = reinterpret_cast<volatile int *>(smem + kSlowFlag);
-    int g_par = 0;  // scalar gate: the parity of the chunk being prepared
-    auto gval = [&](int r, int i) -> float {
-        if (SCALAR_G) return reinterpret_cast<const float *>(smem + kG)[64 * g_par + r];
-        return *reinterpret_cast<const float *>(smem + kG + g_off(r, i));
-    };
-    auto kval = [&](uint32_t base, int r, int i) -> float {
-        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + base + kq_off(r, i)));
-    };
-    // per-chunk vectors, double-buffered by chunk parity
-    auto vec = [&](uint32_t base, int parity) {
-        return reinterpret_cast<float *>(smem + base + 512 * parity);
-    };
-    auto wait_on = [&](uint64_t *bar, uint32_t &phase) {
-        wait_bar(bar, phase, abort_flag);
-        phase ^= 1u;
-        tc_fence_after_sync();
-    };
-    auto csync = [&]() { named_sync(kBarCompute, kCompute); };
-    // State warps hand a finished operand set over and go on.  In normal
-    // operation the mbarrier waits on each batch keep the state warps from
-    // lapping the auxiliary warps on these arrive-only barriers; after a
-    // timeout those waits return at once, so every handoff then blocks.
-    // The proxy fence is needed only after shared-memory writes that the
-    // tensor core or a TMA copy reads (smem_operands); TMEM writes need only
-    // the tcgen05 fence.
-    auto handoff = [&](int id, int count, bool smem_operands) {
-        if (smem_operands) fence_async_smem();
-        tc_fence_before_sync();
-        if (*abort_flag)
-            named_sync(id, count);
-        else
-            named_arrive(id, count);
-    };
+    auto vec = [&](uint32_t base, int slot) { return reinterpret_cast<float *>(smem + base) + 128 * slot; };
+    auto wait = [&](int i, int chunk) { wait_bar(bar(i), (uint32_t)(chunk & 1), abort_flag); };
 
-    const int NC = (T + kC - 1) / kC;
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
-    if (tid == kCompute) {
-        mbar_init(bar_a, 2);  // both issuers commit batch a
-        mbar_init(bar_b, 1);
-        mbar_init(bar_g, 1);
-        mbar_init(bar_4, 2);  // both issuers commit batch 4
-        mbar_init(bar_kqg, 1);
-        mbar_init(bar_v, 1);
+    if (tid == 0) {
+        mbar_init(bar(MB_RAW), 1);
+        mbar_init(bar(MB_V), 1);
+        mbar_init(bar(MB_TILES), 1);
+        mbar_init(bar(MB_GRAM), 1);
+        mbar_init(bar(MB_GFREE), 1 + 4);  // one solver thread + the four P-reading warps
+        mbar_init(bar(MB_TP), 1 + 4);
+        mbar_init(bar(MB_Z), 1);
+        mbar_init(bar(MB_OPART), 1);
+        mbar_init(bar(MB_U), 1);
+        mbar_init(bar(MB_X), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&m.k);
-        tma_prefetch_desc(&m.q);
-        if (!SCALAR_G) tma_prefetch_desc(&m.g);
-        tma_prefetch_desc(&m.v);
-        tma_prefetch_desc(&m.o);
     }
-    __syncthreads();
-    if (issuer_warp && !issuer_a) {  // first chunk's inputs (warp B issues every TMA load)
-        issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, 0, hk, hv, lane);
-        if (lane == 0) issue_v(smem, m, bar_v, b, 0, hv);
-    }
-    if (tid < kC) {  // beta (and a scalar gate's g) buffers: [2][64] floats by chunk parity
-        reinterpret_cast<float *>(smem + kBeta)[tid] =
-            tid < min(kC, T) ? beta[(tok0 + tid) * HV + hv] : 0.f;
-        if (SCALAR_G)
-            reinterpret_cast<float *>(smem + kG)[tid] =
-                tid < min(kC, T) ? gsc[(tok0 + tid) * HV + hv] : 0.f;
-    }
-    const unsigned long long *tree_anc = reinterpret_cast<const unsigned long long *>(smem + kTreeAnc);
-    if (TREE && tid < kC)  // the tree's parents (rows past T: roots)
-        reinterpret_cast<int *>(smem + kTreePar)[tid] = tid < T ? parents[(size_t)b * T + tid] : -1;
-    // s is a token r depends on: an earlier one (sequence) or an ancestor (tree)
-    auto dep = [&](int r, int s) -> bool {
-        return TREE ? ((tree_anc[r] >> s) & 1ull) != 0 : s < r;
-    };
     // T' is lower triangular: its strictly-upper 16 x 16 blocks stay zero
     for (int idx = tid; idx < 64 * 8; idx += kThreads) {
         const int r = idx >> 3, s0 = (idx & 7) * 8;
         if ((s0 >> 4) > (r >> 4))
             *reinterpret_cast<uint4 *>(smem + kOpT + kmajor_off(r, s0, kC)) = make_uint4(0, 0, 0, 0);
     }
-    // state: S[32*iq + 2h + e][j] in S2[h].x / .y (state warps), pairs for packed fp32
-    float2 S2[16];
-#pragma unroll
-    for (int h = 0; h < 16; ++h) {
-        S2[h].x = (HAS_H0 && !aux) ? h0[(shead * kD + 32 * iq + 2 * h) * kD + j] : 0.f;
-        S2[h].y = (HAS_H0 && !aux) ? h0[(shead * kD + 32 * iq + 2 * h + 1) * kD + j] : 0.f;
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (TREE && tid < kC) {
-        // each token's ancestor set as a bit mask, by a walk up its root path
-        // (parents precede their children: at most 63 steps; the bounds keep
-        // the walk inside the table whatever it holds)
-        const int *par = reinterpret_cast<const int *>(smem + kTreePar);
-        unsigned long long a = 0ull;
-        int u = par[tid];
-        for (int step = 0; step < kC && u >= 0 && u < tid; ++step) {
-            a |= 1ull << u;
-            u = par[u];
-        }
-        reinterpret_cast<unsigned long long *>(smem + kTreeAnc)[tid] = a;
-    }
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);  // this warp's lane quarter
-    uint32_t ph_a = 0, ph_b = 0, ph_g = 0, ph_4 = 0;
-    uint32_t ph_gs = 0;  // the solver warps' count of gram completions
-    int issued_kqg = 1, issued_v = 1;  // loads issued so far (issuer warp B, lane 0's count is used)
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
+    const uint32_t io = idesc_bf16(128, 64, false, false, false);
+    int issued_raw = 0, issued_v = 0;  // producer: copies issued on MB_RAW, MB_V
 
-    // Two-stage pipeline: iteration c runs the state products of chunk c
-    // (scan) and prepares chunk c + 1 (prep).  U = T'(V - Lk S') is formed as
-    // Z = Lk S' first and T' applied afterwards, so the inverse of chunk c+1
-    // is not on the path from one chunk's state to the next: the auxiliary
-    // warps compute it while the state warps read back chunk c.
-    //   state warps                                     MMA batch issued after the handoff
-    //   1 prep: prefix sums, scales of chunk c+1
-    //   2 scan: -Z^T read-back (bf16, TMEM)         HZ:  b: U^T = V^T T'^T - Z^T T'^T
-    //   3 prep: Lk, Lq, R tiles                     H2:  g: gram [Lk; Lq] R^T, next k/q/g copies
-    //   4 scan: U^T read-back (bf16, TMEM)          H1:  4: O^T += U^T P^T, dS^T = U^T R; next v copy
-    //   5 prep: A and P read-back                   DIAG: the auxiliary warps invert I + A
-    //   6 scan: state and O read-back, O store; S'^T of chunk c+1
-    //                                               H4:  a: [Z^T | O^T] = S'^T [Lk; Lq]^T
-    for (int c = -1; c < NC; ++c) {
-        const bool has_scan = c >= 0;
-        const bool has_prep = c + 1 < NC;
-        const int cn = c + 1;                          // chunk being prepared
-        const int t0 = c * kC;
-        const int t0n = cn * kC, Ln = has_prep ? min(kC, T - t0n) : 0;
-        const int mref = (Ln - 1) / 2;                 // reference row of chunk cn
-        const int pn = cn & 1, ps = c & 1;             // buffer parities (prep, scan)
-        g_par = pn;
-        const bool has_next2 = cn + 1 < NC;            // a chunk after the prepared one
-
-        // No block-wide barrier per chunk: the groups meet only at named
-        // barriers and mbarriers.  After a timed-out wait (sticky abort flag)
-        // every thread still runs every iteration and every barrier, but
-        // waits return at once and nothing new is issued.
-        if (aux) {
-            // ============ auxiliary warps
-            const uint32_t io = idesc_bf16(128, 64, false, false, false);
-            if (issuer_warp) {
-                bool slow = false, live = true;
-                if (has_scan) {
-                    named_sync(kBarHZ, kHand);
-                    named_sync(kBarSolve, 128);  // T' of chunk c is complete
-                    if (issuer_a && lane == 0 && !*abort_flag) {
-                        // b: U^T = V^T T'^T + (-Z^T) T'^T, one accumulator
-                        wait_bar(bar_v, (uint32_t)(c & 1), abort_flag);
-                        tc_fence_after_sync();
-                        // V: 128B-swizzled MN-major (two 64-column blocks 8 KB apart, 8-row atoms)
-                        const uint32_t vid = idesc_bf16(128, 64, true, false, false);
-                        const uint64_t tdesc = smem_desc(sbase + kOpT, 128, kC * 16);
-                        gemm_ss<kC / 16>(tmem + kTmUT, smem_desc_sw128(sbase + kOpV, 8192, 1024), 2048,
-                                         tdesc, 256, vid, false);
-                        gemm_ts<kC / 16>(tmem + kTmUT, tmem + kTmZTb, tdesc, 256, io, true);
-                        mma_commit(bar_b);
-                    }
-                }
-                if (has_prep) {
-                    named_sync(kBarH2, kHand);
-                    slow = slow_flag[pn] != 0;
-                    live = !*abort_flag;  // one warp-wide read: uniform
-                    if (!slow && live) {
-                        if (issuer_a && lane == 0) {  // g: gram [Lq; Lk] R^T
-                            tc_fence_after_sync();
-                            gemm_ss<kD / 16>(tmem + kTmGram, smem_desc(sbase + kOpL, 128, kD * 16), 256,
-                                             smem_desc(sbase + kOpR + pn * 16384, 128, kD * 16), 256,
-                                             io, false);
-                            mma_commit(bar_g);
-                        }
-                        // the raw k, q, g tiles are consumed: fetch the next chunk's
-                        if (!issuer_a && has_next2) {
-                            issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
-                            ++issued_kqg;
-                        }
-                    }
-                }
-                if (has_scan) {
-                    named_sync(kBarH1, kHand);
-                    if (lane == 0 && !*abort_flag) {  // 4, A = U^T (bf16) in TMEM
-                        tc_fence_after_sync();
-                        if (issuer_a) {  // O^T += U^T P^T
-                            gemm_ts<kC / 16>(tmem + kTmOT, tmem + kTmUTb,
-                                             smem_desc(sbase + kOpP + ps * 8192, 128, kC * 16), 256,
-                                             io, true);
-                        } else {  // dS^T = U^T R (R read transposed)
-                            const uint32_t ids = idesc_bf16(128, 128, false, true, false);
-                            gemm_ts<kC / 16>(tmem + kTmDS, tmem + kTmUTb,
-                                             smem_desc(sbase + kOpR + ps * 16384, kD * 16, 128), 4096,
-                                             ids, false);
-                        }
-                        mma_commit(bar_4);
-                        // batch b of chunk c has completed (the state warps waited
-                        // for it): v's buffer takes the prepared chunk's
-                        if (!issuer_a && has_prep) {
-                            issue_v(smem, m, bar_v, b, t0n, hv);
-                            ++issued_v;
-                        }
-                    }
-                }
-                if (has_prep) {
-                    named_sync(kBarH4, kHand);
-                    if (!issuer_a && slow && has_next2 && live) {  // the exact path read the raw tiles until step 5
-                        issue_kqg<!SCALAR_G>(smem, m, bar_kqg, b, t0n + kC, hk, hv, lane);
-                        ++issued_kqg;
-                    }
-                    if (lane == 0 && !*abort_flag) {
-                        // a: Z^T = S'^T Lk^T (thread A) and O^T = S'^T Lq^T (thread B), A = S'^T in TMEM
-                        tc_fence_after_sync();
-                        const uint32_t dst = issuer_a ? kTmZT : kTmOT;
-                        const uint32_t rows = issuer_a ? 16384u : 0u;  // Lq rows 0-63, Lk rows 64-127
-                        gemm_ts<kD / 16>(tmem + dst, tmem + kTmSTb,
-                                         smem_desc(sbase + kOpL + rows, 128, kD * 16), 256, io, false);
-                        mma_commit(bar_a);
-                    }
-                }
-            } else if (has_prep) {
-                // ---- solver warps: T' of chunk cn
-                named_sync(kBarDiag, kCompute + 64);  // chunk cn's tiles are in, or A (exact path)
-                const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
-                if (slow_flag[pn] == 0) {
-                    // A = beta-scaled strictly lower part of gram rows 64-127
-                    // (blocks above the diagonal are never read: not written)
-                    wait_on(bar_g, ph_gs);  // gram of chunk cn
-                    const int r = 32 * sw + lane, rb = r >> 4;
-                    const float br = bvec[r];
+    if (warp < kWarpPrep0) {
+        // ================= chain warps: lane quarter wq, half hh of the state
+        // columns (i in [64 hh, 64 hh + 64)) and of the chunk rows (r in
+        // [32 hh, 32 hh + 32))
+        const int wq = warp & 3, hh = warp >> 2;
+        const int j = 32 * wq + lane;  // this thread's value column (TMEM lane)
+        if (VARLEN && lane == 0) fence_tensormap_acquire(&m.o);
+        __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage + 2048 * warp);
+        auto handoff = [&](int id) {
+            tc_fence_before_sync();
+            if (*abort_flag)
+                named_sync(id, kHandThreads);
+            else
+                named_arrive(id, kHandThreads);
+        };
+        // Writes the state columns i0 .. i0 + 31 from x (the accumulated
+        // X + U^T R, or h0): S' = x c is the bf16 operand of the next chunk and
+        // X = S' a the stored state; after the last chunk S' is the final state.
+        auto put_state = [&](int i0, float (&x)[32], int slot, bool last) {
+            const float *cv = vec(kCv, slot) + i0;
+            const float *av = vec(kAv, slot) + i0;
+            uint32_t wb[16];
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (sw == 0 && g >= 2) break;  // rows 0-31: column blocks 0-1 only
-                        float dd[16];
-                        tmem_ld16(tl + kTmGram + 16 * g, dd);
-                        if (g == rb) {  // diagonal block, stored transposed
-#pragma unroll
-                            for (int u = 0; u < 16; ++u)
-                                sA[diagT_idx(g, u, r & 15)] = (dep(r, 16 * g + u) && r < Ln) ? br * dd[u] : 0.f;
-                        } else if (g < rb) {
-#pragma unroll
-                            for (int u = 0; u < 16; ++u)
-                                sA[sq_idx(r, 16 * g + u)] =
-                                    (r < Ln && (!TREE || dep(r, 16 * g + u))) ? br * dd[u] : 0.f;
-                        }
-                    }
-                }
-                // Each solver warp's diagonal blocks and level-1 block use only
-                // the rows it read itself (or, on the exact path, rows written
-                // before the DIAG barrier): a warp barrier suffices until level 2.
-                __syncwarp();
-                // diagonal 16 x 16 blocks of T = (I + A)^-1: one thread per
-                // column (block I = t / 16, column jj = t % 16), right-looking;
-                // column s2 of A's block is one contiguous run of 16 floats,
-                // the same for the 16 threads of a block (broadcast loads)
-                {
-                    const int t = tid - kCompute - 64, I = t >> 4, jj = t & 15;
-                    float x[16];
-#pragma unroll
-                    for (int p = 0; p < 16; ++p) x[p] = (p == jj) ? 1.f : 0.f;
-#pragma unroll
-                    for (int s2 = 0; s2 < 15; ++s2) {
-                        const float4 *col = reinterpret_cast<const float4 *>(sA + diagT_idx(I, s2, 0));
-#pragma unroll
-                        for (int g4 = (s2 + 1) >> 2; g4 < 4; ++g4) {
-                            const float4 a = col[g4];
-                            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (4 * g4 + e > s2) x[4 * g4 + e] = fmaf(-av[e], x[s2], x[4 * g4 + e]);
-                        }
-                    }
-                    __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
-                    const float bj = bvec[16 * I + jj];
-#pragma unroll
-                    for (int p = 0; p < 16; p += 2) {
-                        sT[sq_idx(16 * I + p, 16 * I + jj)] = x[p];
-                        sT[sq_idx(16 * I + p + 1, 16 * I + jj)] = x[p + 1];
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(x[p] * bj, x[p + 1] * bj);
-                        opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = h.x;
-                        opt[kmajor_off(16 * I + p + 1, 16 * I + jj, kC) >> 1] = h.y;
-                    }
-                }
-                __syncwarp();
-                // off-diagonal blocks by 32 x 32 block recursion:
-                //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
-                //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
-                const FragOffsets fo = frag_offsets(lane);
-                auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
-                    const int gq = lane >> 2, tq = lane & 3;
-                    float *trow = sT + I * 1024 + 16 * (J ^ (I & 1)) + gq * 64;
-                    const int u0 = (2 * tq) ^ gq, u1 = (2 * tq + 1) ^ gq;
-                    unsigned char *prow = smem + kOpT + 2 * I * 1024 + gq * 16 + 4 * tq;
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const float2 bb = *reinterpret_cast<const float2 *>(bvec + 16 * J + 8 * nt + 2 * tq);
-                        trow[8 * nt + u0] = -acc[nt][0];
-                        trow[8 * nt + u1] = -acc[nt][1];
-                        trow[512 + 8 * (nt ^ 1) + u0] = -acc[nt][2];
-                        trow[512 + 8 * (nt ^ 1) + u1] = -acc[nt][3];
-                        // T' = T diag(beta), bf16, K-major [64 r][64 s]: (2 J + nt) * 128 + row offsets
-                        *reinterpret_cast<uint32_t *>(prow + (2 * J + nt) * 128) =
-                            pack_bf16x2(-acc[nt][0] * bb.x, -acc[nt][1] * bb.y);
-                        *reinterpret_cast<uint32_t *>(prow + 1024 + (2 * J + nt) * 128) =
-                            pack_bf16x2(-acc[nt][2] * bb.x, -acc[nt][3] * bb.y);
-                    }
-                };
-                {  // level 1: block (1,0) on solver 0, (3,2) on solver 1
-                    const int I = 2 * sw + 1, J = 2 * sw;
-                    float acc[2][4] = {};
-                    blk_mma2<true>(acc, swz_block(sA, I, J), swz_block(sT, J, J), fo);
-                    blk_store(sX + 256 * sw, acc, lane);
-                    __syncwarp();
-                    float y[2][4] = {};
-                    blk_mma2<false>(y, swz_block(sT, I, I), sX + 256 * sw, fo);
-                    emit(I, J, y);
-                }
-                named_sync(kBarAux, 64);
-                {  // level 2, row I = 2 + sw of X = [A_20 A_21; A_30 A_31] T1 (slots 2 (I - 2) + J)
-                    const int I = 2 + sw;
-                    float x0[2][4] = {}, x1[2][4] = {};
-                    blk_mma2<true>(x0, swz_block(sA, I, 0), swz_block(sT, 0, 0), fo);
-                    blk_mma2<true>(x0, swz_block(sA, I, 1), swz_block(sT, 1, 0), fo);
-                    blk_mma2<true>(x1, swz_block(sA, I, 1), swz_block(sT, 1, 1), fo);
-                    blk_store(sX + 256 * (2 * sw), x0, lane);
-                    blk_store(sX + 256 * (2 * sw + 1), x1, lane);
-                }
-                named_sync(kBarAux, 64);
-                {  // level 2, column J = sw of T_lo = -T2 X
-                    const int J = sw;
-                    float t2[2][4] = {}, t3[2][4] = {};
-                    blk_mma2<false>(t2, swz_block(sT, 2, 2), sX + 256 * J, fo);        // T_22 X_2J
-                    blk_mma2<false>(t3, swz_block(sT, 3, 2), sX + 256 * J, fo);        // T_32 X_2J
-                    blk_mma2<false>(t3, swz_block(sT, 3, 3), sX + 256 * (2 + J), fo);  // + T_33 X_3J
-                    emit(2, J, t2);
-                    emit(3, J, t3);
-                }
-                fence_async_smem();  // T' is read by the tensor core
-                if (*abort_flag)
-                    named_sync(kBarSolve, 128);
-                else
-                    named_arrive(kBarSolve, 128);
+            for (int u = 0; u < 32; u += 4) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(cv + u);
+                const float4 a4 = *reinterpret_cast<const float4 *>(av + u);
+                const float2 y0 = __fmul2_rn(make_float2(x[u], x[u + 1]), make_float2(c4.x, c4.y));
+                const float2 y1 = __fmul2_rn(make_float2(x[u + 2], x[u + 3]), make_float2(c4.z, c4.w));
+                wb[u / 2] = pack_bf16x2(y0.x, y0.y);
+                wb[u / 2 + 1] = pack_bf16x2(y1.x, y1.y);
+                const float2 z0 = __fmul2_rn(y0, make_float2(a4.x, a4.y));
+                const float2 z1 = __fmul2_rn(y1, make_float2(a4.z, a4.w));
+                x[u] = z0.x;
+                x[u + 1] = z0.y;
+                x[u + 2] = z1.x;
+                x[u + 3] = z1.y;
             }
-            continue;
-        }
-
-        // ============ state warps
-        // beta of chunk cn + 1 straight into its buffer (read from step 5 of
-        // the next iteration on; the wait is at the end of step 6).  The
-        // buffer last held chunk c's beta, which the auxiliary warps read
-        // while inverting for chunk c: it is refilled only once batch b of
-        // chunk c, issued after that inverse, has completed (step 4).
-        auto prefetch_beta = [&]() {
-            if (has_next2 && tid < kC) {
-                float *dst = reinterpret_cast<float *>(smem + kBeta + 256 * ((cn + 1) & 1)) + tid;
-                float *gdst = reinterpret_cast<float *>(smem + kG + 256 * ((cn + 1) & 1)) + tid;
-                if (t0n + kC + tid < T) {
-                    cp_async4(dst, beta + (tok0 + t0n + kC + tid) * HV + hv);
-                    if (SCALAR_G) cp_async4(gdst, gsc + (tok0 + t0n + kC + tid) * HV + hv);
-                } else {
-                    *dst = 0.f;
-                    if (SCALAR_G) *gdst = 0.f;
+            if (last) {  // the final factor's a is 1: x holds the final state
+                if (STORE_HT && !*abort_flag) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ht[(shead * kD + i0 + u) * kD + j] = x[u];
                 }
+            } else {
+                uint32_t wx[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) wx[u] = __float_as_uint(x[u]);
+                tmem_st32(tl + kTmX + i0, wx);
+                tmem_st16(tl + kTmSb + i0 / 2, wb);
             }
         };
-        if (!has_scan) prefetch_beta();
-        // ---------------- 1 prep: per-channel prefix sums of g (four quarters of 16 rows)
-        bool slow = false;
-        int half_bad = 0;  // a half chunk decays by more than kHalfLog2 (channelwise)
-        if (has_prep) {
-            wait_bar(bar_kqg, (uint32_t)(cn & 1), abort_flag);
+        // initial state: X = h0 c a with the factors of the first chunk
+        wait(MB_TILES, 0);
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            const int i0 = 64 * hh + 32 * p;
+            float x[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = HAS_H0 ? h0[(shead * kD + i0 + u) * kD + j] : 0.f;
+            put_state(i0, x, 1, false);
+        }
+        tmem_st_wait();
+        handoff(kNbS);
+#pragma unroll 1
+        for (int c = 0; c < NC; ++c) {
+            const bool last = c + 1 == NC;
+            // -Z^T as the bf16 A operand of the U product
+            wait(MB_Z, c);
+            tc_fence_after_sync();
+            {
+                float d[32];
+                tmem_ld32(tl + kTmZ + 32 * hh, d);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(-d[2 * e], -d[2 * e + 1]);
+                tmem_st16(tl + kTmZb + 16 * hh, w);
+                tmem_st_wait();
+            }
+            handoff(kNbZb);
+            // U^T as the bf16 A operand of the state and output products
+            wait(MB_U, c);
+            tc_fence_after_sync();
+            {
+                float d[32];
+                tmem_ld32(tl + kTmU + 32 * hh, d);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(d[2 * e], d[2 * e + 1]);
+                tmem_st16(tl + kTmUb + 16 * hh, w);
+                tmem_st_wait();
+            }
+            handoff(kNbUb);
+            // the state: X + U^T R scaled into the next chunk's frame
+            wait(MB_X, c);
+            tc_fence_after_sync();
+            if (!last) wait(MB_TILES, c + 1);  // the carry factors come with the next chunk's tiles
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                const int i0 = 64 * hh + 32 * p;
+                float x[32];
+                tmem_ld32(tl + kTmX + i0, x);
+                put_state(i0, x, c & 1, last);
+            }
+            if (!last) {
+                tmem_st_wait();
+                handoff(kNbS);
+            }
+            // O^T -> this warp's bf16 box [32 r][32 j] -> one TMA store
+            {
+                float o[32];
+                tmem_ld32(tl + kTmO + 32 * hh, o);
+                if (!last) handoff(kNbOfree);
+                if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 32; u += 2) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(o[u], o[u + 1]);
+                    stg[u * 32 + lane] = h.x;
+                    stg[(u + 1) * 32 + lane] = h.y;
+                }
+                fence_async_smem();
+                __syncwarp();
+                // rows past the end of the sequence fall outside the tensor and are dropped
+                if (lane == 0 && !*abort_flag) {
+                    tma_store_4d(&m.o, stg, 32 * wq, hv, c * kC + 32 * hh, b);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    } else if (warp < kWarpProducer) {
+        // ================= prep warps
+        const int pw = warp - kWarpPrep0;  // 0..7
+        const int pt = tid - 32 * kWarpPrep0;
+        const bool p_reader = (warp & 3) < 2;  // TMEM lanes 0-63: the P rows of the gram
+        float gs0 = 0.f, gs1 = 0.f;            // scalar gate: this lane's two log-decays of the chunk
+        auto load_gsc = [&](int t0) {
+            if (SCALAR_G && pw == 0) {
+                gs0 = t0 + 2 * lane < T ? gsc[(tok0 + t0 + 2 * lane) * HV + hv] : 0.f;
+                gs1 = t0 + 2 * lane + 1 < T ? gsc[(tok0 + t0 + 2 * lane + 1) * HV + hv] : 0.f;
+            }
+        };
+        load_gsc(0);
+#pragma unroll 1
+        for (int c = 0; c < NC; ++c) {
+            const int t0 = c * kC, L = min(kC, T - t0), mref = (L - 1) / 2;
+            const int par = c & 1;
+            if (c > 0) wait(MB_OPART, c - 1);  // Lq, Lk (and R of chunk c - 2) are free
+            wait(MB_RAW, c);
+            // ---------------- prefix sums (log2 units), range check, G_m and G_L
+            int bad = 0;
             if (SCALAR_G) {
-                // one warp: inclusive prefix of the chunk's 64 log-decays (two
-                // per lane, log2 units), in place, and an exact range check
-                // on the two spans around the reference row (G is monotone)
-                int bad = 0;
-                if (warp == 0) {
-                    float *Gp = reinterpret_cast<float *>(smem + kG) + 64 * pn;
-                    const float a = Gp[2 * lane] * kLog2e, a2 = Gp[2 * lane + 1] * kLog2e;
+                if (pw == 0) {
+                    float *Gp = reinterpret_cast<float *>(smem + kGsc);
+                    const float a = gs0 * kLog2e, a2 = gs1 * kLog2e;
                     const float pair = a + a2;
                     float x = pair;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, x, o);
-                        if (lane >= o) x += y;
+                        const float yv = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += yv;
                     }
                     const float g_even = x - pair + a;
                     Gp[2 * lane] = g_even;
@@ -779,347 +542,512 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float g0 = __shfl_sync(0xffffffffu, g_even, 0);
                     const float gm_e = __shfl_sync(0xffffffffu, g_even, mref >> 1);
                     const float gm_o = __shfl_sync(0xffffffffu, x, mref >> 1);
-                    const float gl_e = __shfl_sync(0xffffffffu, g_even, (Ln - 1) >> 1);
-                    const float gl_o = __shfl_sync(0xffffffffu, x, (Ln - 1) >> 1);
+                    const float gl_e = __shfl_sync(0xffffffffu, g_even, (L - 1) >> 1);
+                    const float gl_o = __shfl_sync(0xffffffffu, x, (L - 1) >> 1);
                     const float gmv = (mref & 1) ? gm_o : gm_e;
-                    const float glv = ((Ln - 1) & 1) ? gl_o : gl_e;
-                    // each span within kHalfLog2: the factors within exp(+-43),
-                    // the folded carry factors above exp(-86)
+                    const float glv = ((L - 1) & 1) ? gl_o : gl_e;
+                    // each span around the reference row within the half-chunk limit
                     bad = lane == 0 && (g0 - gmv > kHalfLog2 || gmv - glv > kHalfLog2);
+                    *reinterpret_cast<float4 *>(vec(kGm, par) + 4 * lane) = make_float4(gmv, gmv, gmv, gmv);
+                    *reinterpret_cast<float4 *>(vec(kGL, par) + 4 * lane) = make_float4(glv, glv, glv, glv);
+                    load_gsc(t0 + kC);  // the next chunk's log-decays
                 }
-                slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
-            } else if (TREE) {
-                // log2 units in place, then prefix sums along root paths: one
-                // thread per channel walks the rows in order (parents first)
+            } else {
+                // warp pw: rows 8 pw .. 8 pw + 7; lane: channels 4 lane .. 4 lane + 3
+                float4 x[8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const float4 v = *reinterpret_cast<const float4 *>(smem + kG + g_off(8 * pw + rr, 4 * lane));
+                    const float2 lo = __fmul2_rn(make_float2(v.x, v.y), make_float2(kLog2e, kLog2e));
+                    const float2 hi = __fmul2_rn(make_float2(v.z, v.w), make_float2(kLog2e, kLog2e));
+                    x[rr] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+#pragma unroll
+                for (int rr = 1; rr < 8; ++rr) {
+                    const float2 lo = __fadd2_rn(make_float2(x[rr].x, x[rr].y), make_float2(x[rr - 1].x, x[rr - 1].y));
+                    const float2 hi = __fadd2_rn(make_float2(x[rr].z, x[rr].w), make_float2(x[rr - 1].z, x[rr - 1].w));
+                    x[rr] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+                float4 *tot = reinterpret_cast<float4 *>(smem + kTot);
+                tot[32 * pw + lane] = x[7];
+                named_sync(kNbPrep, kPrepThreads);
+                // carry from the blocks above; quarter (blocks 2q, 2q+1) and
+                // half (blocks 4h .. 4h+3) decays, each checked once
+                float4 carry = make_float4(0.f, 0.f, 0.f, 0.f), half = carry;
+#pragma unroll
+                for (int w2 = 0; w2 < 7; ++w2) {
+                    if (w2 < pw) {
+                        const float4 t = tot[32 * w2 + lane];
+                        carry = make_float4(carry.x + t.x, carry.y + t.y, carry.z + t.z, carry.w + t.w);
+                        if ((w2 >> 2) == (pw >> 2))
+                            half = make_float4(half.x + t.x, half.y + t.y, half.z + t.z, half.w + t.w);
+                    }
+                }
+                const float4 own = x[7];
+                if (pw & 1) {
+                    const float4 t = tot[32 * (pw - 1) + lane];
+                    const float q0 = t.x + own.x, q1 = t.y + own.y, q2 = t.z + own.z, q3 = t.w + own.w;
+                    bad |= fminf(fminf(q0, q1), fminf(q2, q3)) < -kQuarterLog2;
+                }
+                if ((pw & 3) == 3) {
+                    const float h0v = half.x + own.x, h1v = half.y + own.y, h2v = half.z + own.z,
+                                h3v = half.w + own.w;
+                    bad |= fminf(fminf(h0v, h1v), fminf(h2v, h3v)) < -kHalfLog2;
+                }
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const float2 lo = __fadd2_rn(make_float2(x[rr].x, x[rr].y), make_float2(carry.x, carry.y));
+                    const float2 hi = __fadd2_rn(make_float2(x[rr].z, x[rr].w), make_float2(carry.z, carry.w));
+                    x[rr] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    *reinterpret_cast<float4 *>(smem + kG + g_off(8 * pw + rr, 4 * lane)) = x[rr];
+                    // G at the reference row and at the last row
+                    if (8 * pw + rr == mref) reinterpret_cast<float4 *>(vec(kGm, par))[lane] = x[rr];
+                    if (8 * pw + rr == L - 1) reinterpret_cast<float4 *>(vec(kGL, par))[lane] = x[rr];
+                }
+            }
+            const bool slow = named_sync_or(kNbPrep, kPrepThreads, bad) != 0;
+            // ---------------- carry factors: c of the previous chunk, a of this one;
+            // after the last chunk, the factor that leaves the final state
+            if (pt < kD) {
+                const int i = pt;
+                const float gm = slow ? 0.f : vec(kGm, par)[i], gl = vec(kGL, par)[i];
+                const float a_now = slow ? fast_exp2(gl) : 1.f;
+                if (c == 0) {
+                    vec(kCv, 1)[i] = fast_exp2(gm);
+                    vec(kAv, 1)[i] = a_now;
+                } else {
+                    const bool sp = slow_flag[par ^ 1] != 0;
+                    const float rel = sp ? 0.f : vec(kGL, par ^ 1)[i] - vec(kGm, par ^ 1)[i];
+                    vec(kCv, par ^ 1)[i] = fast_exp2(gm + rel);
+                    vec(kAv, par ^ 1)[i] = a_now;
+                }
+                if (c + 1 == NC) {
+                    vec(kCv, par)[i] = slow ? 1.f : fast_exp2(gl - gm);
+                    vec(kAv, par)[i] = 1.f;
+                }
+            }
+            // ---------------- operand tiles Lq, Lk, R (bf16, K-major core matrices)
+            {
+                // lane: channel group cg (8 channels) of four, row r8 of eight
+                const int cg = 4 * (pw & 3) + (lane >> 3), r8 = lane & 7, ch = 8 * cg;
+                float gm[8], gl[8];
                 {
-                    const int i = tid & 127, qq = tid >> 7;
+                    const float4 m0 = *reinterpret_cast<const float4 *>(vec(kGm, par) + ch);
+                    const float4 m1 = *reinterpret_cast<const float4 *>(vec(kGm, par) + ch + 4);
+                    const float4 l0 = *reinterpret_cast<const float4 *>(vec(kGL, par) + ch);
+                    const float4 l1 = *reinterpret_cast<const float4 *>(vec(kGL, par) + ch + 4);
+                    gm[0] = m0.x; gm[1] = m0.y; gm[2] = m0.z; gm[3] = m0.w;
+                    gm[4] = m1.x; gm[5] = m1.y; gm[6] = m1.z; gm[7] = m1.w;
+                    gl[0] = l0.x; gl[1] = l0.y; gl[2] = l0.z; gl[3] = l0.w;
+                    gl[4] = l1.x; gl[5] = l1.y; gl[6] = l1.z; gl[7] = l1.w;
+                }
+                unsigned char *rbuf = smem + kOpR + par * 16384;
+#pragma unroll 2
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int r = r8 + 8 * (4 * (pw >> 2) + kk);
+                    float kv[8], qv[8], gv[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kq_off(r, ch)), kv);
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kq_off(r, ch)), qv);
+                    if (SCALAR_G) {
+                        const float gr = reinterpret_cast<const float *>(smem + kGsc)[r];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        float *gp = reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i));
-                        *gp *= kLog2e;
+                        for (int e = 0; e < 8; ++e) gv[e] = gr;
+                    } else {
+                        const float4 g0 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, ch));
+                        const float4 g1 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, ch + 4));
+                        gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w;
+                        gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
                     }
-                }
-                csync();
-                float gmin = 0.f;
-                if (tid < kD) {
-                    const int *par = reinterpret_cast<const int *>(smem + kTreePar);
-                    for (int r = 0; r < kC; ++r) {
-                        const int p = par[r];
-                        float *gp = reinterpret_cast<float *>(smem + kG + g_off(r, tid));
-                        const float x = *gp + (p >= 0 && p < r ? gval(p, tid) : 0.f);
-                        *gp = x;
-                        gmin = fminf(gmin, x);
-                    }
-                }
-                // the factors exp(G) <= 1 and exp(-G) stay finite while no
-                // path decays by more than the range
-                slow = named_sync_or(kBarCompute, kCompute, -gmin > kRangeLog2) != 0;
-            } else {
-                const int i = tid & 127, qq = tid >> 7;
-                float x[16];
+                    float lk[8], lq[8], rv[8];
+                    if (!slow) {
+                        if (SCALAR_G) {  // one decay per row: two exponentials for 8 channels
+                            const float d = gv[0] - gm[0];
+                            const float el = fast_exp2(d), er = fast_exp2(-d);
 #pragma unroll
-                for (int r = 0; r < 16; r += 2) {  // log2 units
-                    const float2 v = __fmul2_rn(make_float2(gval(16 * qq + r, i), gval(16 * qq + r + 1, i)),
-                                                make_float2(kLog2e, kLog2e));
-                    x[r] = v.x;
-                    x[r + 1] = v.y;
-                }
+                            for (int e = 0; e < 8; ++e) {
+                                lk[e] = kv[e] * el;
+                                lq[e] = qv[e] * el;
+                                rv[e] = kv[e] * er;
+                            }
+                        } else {
 #pragma unroll
-                for (int r = 1; r < 16; ++r) x[r] += x[r - 1];
-                if (qq < 3) sTot[qq * 128 + i] = x[15];
-                // Range check, conservatively per 16-row quarter: the spans it
-                // guards (rows 1..m and m+1..L-1, at most 32 rows) cover at
-                // most three quarters.  The half-chunk check (quarters 0-1,
-                // 2-3, which contain the spans of a full chunk and the first
-                // span of any) is reduced in the next barrier.
-                const int bad = -x[15] > kQuarterLog2;
-                slow = named_sync_or(kBarCompute, kCompute, bad) != 0;
-                if (qq & 1) half_bad = -(sTot[(qq - 1) * 128 + i] + x[15]) > kHalfLog2;
-                float carry = 0.f;
-                for (int q2 = 0; q2 < qq; ++q2) carry += sTot[q2 * 128 + i];
+                            for (int e = 0; e < 8; e += 2) {  // packed fp32 pairs
+                                const float2 d = __fadd2_rn(make_float2(gv[e], gv[e + 1]),
+                                                            make_float2(-gm[e], -gm[e + 1]));
+                                const float2 el = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                                const float2 er = make_float2(fast_exp2(-d.x), fast_exp2(-d.y));
+                                const float2 kk2 = make_float2(kv[e], kv[e + 1]);
+                                const float2 a = __fmul2_rn(kk2, el);
+                                const float2 bq = __fmul2_rn(make_float2(qv[e], qv[e + 1]), el);
+                                const float2 cr = __fmul2_rn(kk2, er);
+                                lk[e] = a.x; lk[e + 1] = a.y;
+                                lq[e] = bq.x; lq[e + 1] = bq.y;
+                                rv[e] = cr.x; rv[e + 1] = cr.y;
+                            }
+                        }
+                    } else {
+                        // reference row = chunk start: every factor <= 1
 #pragma unroll
-                for (int r = 0; r < 16; r += 2) {
-                    const float2 v = __fadd2_rn(make_float2(x[r], x[r + 1]), make_float2(carry, carry));
-                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r, i)) = v.x;
-                    *reinterpret_cast<float *>(smem + kG + g_off(16 * qq + r + 1, i)) = v.y;
-                }
-            }
-            slow = (named_sync_or(kBarCompute, kCompute, half_bad) != 0) || slow;
-            if (tid == 0) slow_flag[pn] = slow ? 1 : 0;  // read by the issuers and the solvers
-            if (tid < kD) {
-                // the fallback factorises around the chunk start (G_m = 0) and
-                // stores R with the full decay to the chunk end (scale 1)
-                const float gm = (slow || TREE) ? 0.f : gval(mref, tid), gl = gval(Ln - 1, tid);
-                const float egm = (slow || TREE) ? 1.f : fast_exp2(gm);
-                vec(kEGm, pn)[tid] = egm;
-                vec(kCL, pn)[tid] = slow ? 1.f : fast_exp2(gl - gm);
-                vec(kRho, pn)[tid] = fast_exp2(gl - gm);  // exp(G_L) / exp(G_m)
-                if (has_scan) {
-                    // The state registers hold S' = exp(G_m) S of the chunk being
-                    // scanned; the update to the next chunk's S' is
-                    //   S'_{c+1} = [exp(G_m') rho] S'_c + [exp(G_m') cL] dS
-                    // (G_m' the next chunk's reference row), written over
-                    // chunk c's rho and cL, which nothing else reads.  The
-                    // range checks keep both products above exp(-84): fast
-                    // chunks are full here (a ragged chunk is the last one),
-                    // so G_L - G_m spans two quarters of this chunk and G_m'
-                    // two of the next.
-                    vec(kRho, ps)[tid] *= egm;
-                    vec(kCL, ps)[tid] *= egm;
-                }
-            }
-            csync();  // the vectors are read by every state warp in step 6
-        }
-
-        // ---------------- 2 scan: -Z^T read-back as the bf16 A operand of batch b
-        if (has_scan) {
-            wait_on(bar_a, ph_a);  // batch a of chunk c
-            float dd[16];
-            tmem_ld16(tl + kTmZT + 16 * iq, dd);
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(-dd[2 * e], -dd[2 * e + 1]);
-            tmem_st8(tl + kTmZTb + 8 * iq, w);
-            tmem_st_wait();
-            handoff(kBarHZ, kHand, false);
-        }
-
-        // ---------------- 3 prep: operand tiles Lk, Lq, R (bf16, K-major core matrices)
-        if (has_prep) {
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int id = tid + kCompute * it;  // 0..1023
-                const int r8 = id & 7;
-                const int r = ((id >> 7) << 3) | r8;
-                const int c8 = (id >> 3) & 15;
-                const int ch = c8 * 8;
-                float kv[8], qv[8], gv[8], gm[8];
-                const uint32_t kqo = (uint32_t)((c8 >> 3) * 8192 + r * 128 + (((c8 & 7) ^ r8) << 4));
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawK + kqo), kv);
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(smem + kRawQ + kqo), qv);
-                if (SCALAR_G) {
-                    const float gr = gval(r, 0);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[e] = gr;
-                } else {
-                    const uint32_t gbox = (uint32_t)((c8 >> 2) * 8192 + r * 128);
-                    const float4 g_lo = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8) & 7) ^ r8) << 4));
-                    const float4 g_hi = *reinterpret_cast<const float4 *>(smem + kG + gbox + ((((2 * c8 + 1) & 7) ^ r8) << 4));
-                    gv[0] = g_lo.x; gv[1] = g_lo.y; gv[2] = g_lo.z; gv[3] = g_lo.w;
-                    gv[4] = g_hi.x; gv[5] = g_hi.y; gv[6] = g_hi.z; gv[7] = g_hi.w;
-                }
-                if (SCALAR_G && !slow) {
-                    const float gmr = gval(mref, 0);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gm[e] = gmr;
-                } else if (!slow && !TREE) {
-                    // G at the reference row, from the G tile (a tree's
-                    // reference is its start, G_m = 0)
-                    const float4 m_lo = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch));
-                    const float4 m_hi = *reinterpret_cast<const float4 *>(smem + kG + g_off(mref, ch + 4));
-                    gm[0] = m_lo.x; gm[1] = m_lo.y; gm[2] = m_lo.z; gm[3] = m_lo.w;
-                    gm[4] = m_hi.x; gm[5] = m_hi.y; gm[6] = m_hi.z; gm[7] = m_hi.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gm[e] = 0.f;
-                }
-                float lk[8], lq[8], rr[8];
-                if (!slow && SCALAR_G) {
-                    // one decay per row: two exponentials for the 8 channels
-                    const float d = gv[0] - gm[0];
-                    const float2 el = make_float2(fast_exp2(d), fast_exp2(d));
-                    const float2 er = make_float2(fast_exp2(-d), fast_exp2(-d));
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const float2 kk = make_float2(kv[e], kv[e + 1]);
-                        const float2 a = __fmul2_rn(kk, el);
-                        const float2 bq = __fmul2_rn(make_float2(qv[e], qv[e + 1]), el);
-                        const float2 cr = __fmul2_rn(kk, er);
-                        lk[e] = a.x; lk[e + 1] = a.y;
-                        lq[e] = bq.x; lq[e + 1] = bq.y;
-                        rr[e] = cr.x; rr[e + 1] = cr.y;
-                    }
-                } else if (!slow) {
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {  // packed fp32 pairs
-                        const float2 d = __fadd2_rn(make_float2(gv[e], gv[e + 1]),
-                                                    make_float2(-gm[e], -gm[e + 1]));
-                        const float2 el = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                        const float2 er = make_float2(fast_exp2(-d.x), fast_exp2(-d.y));
-                        const float2 kk = make_float2(kv[e], kv[e + 1]);
-                        const float2 a = __fmul2_rn(kk, el);
-                        const float2 bq = __fmul2_rn(make_float2(qv[e], qv[e + 1]), el);
-                        const float2 cr = __fmul2_rn(kk, er);
-                        lk[e] = a.x; lk[e + 1] = a.y;
-                        lq[e] = bq.x; lq[e + 1] = bq.y;
-                        rr[e] = cr.x; rr[e + 1] = cr.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float el = fast_exp2(gv[e]);
-                        lk[e] = kv[e] * el;
-                        lq[e] = qv[e] * el;
-                        // R = exp(G_L - G) K directly (factor <= 1); a tree
-                        // carries no state, and its R is not read
-                        rr[e] = TREE ? 0.f : kv[e] * fast_exp2(gval(Ln - 1, ch + e) - gv[e]);
-                    }
-                }
-                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
-                *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lk);
-                *reinterpret_cast<uint4 *>(smem + kOpR + pn * 16384 + kmajor_off(r, ch, kD)) =
-                    pack_bf16x8(rr);
-            }
-            handoff(kBarH2, kHand, true);
-        }
-
-        // ---------------- 4 scan: U^T read-back as the bf16 A operand of batch 4
-        if (has_scan) {
-            wait_on(bar_b, ph_b);  // batch b of chunk c
-            prefetch_beta();
-            float dd[16];
-            tmem_ld16(tl + kTmUT + 16 * iq, dd);
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(dd[2 * e], dd[2 * e + 1]);
-            tmem_st8(tl + kTmUTb + 8 * iq, w);
-            tmem_st_wait();
-            handoff(kBarH1, kHand, false);
-        }
-
-        // ---------------- 5 prep: A (f32) and P (bf16) of chunk cn
-        if (has_prep) {
-            const float *bvec = reinterpret_cast<const float *>(smem + kBeta + 256 * pn);
-            unsigned char *pbuf = smem + kOpP + pn * 8192;
-            if (!slow) {
-                // the solver warps read A themselves (gram rows 64-127)
-                handoff(kBarDiag, kCompute + 64, true);
-                if (wq < 2) {  // P rows: gram rows 0-63
-                    wait_on(bar_g, ph_g);  // gram of chunk cn
-                    float dd[16];
-                    tmem_ld16(tl + kTmGram + 16 * iq, dd);
-                    const int r = 32 * wq + lane;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int s = 16 * iq + u;
-                        dd[u] = ((s == r || dep(r, s)) && r < Ln) ? dd[u] : 0.f;
-                    }
-#pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8)
-                        *reinterpret_cast<uint4 *>(pbuf + kmajor_off(r, 16 * iq + 8 * q8, kC)) =
-                            pack_bf16x8(&dd[8 * q8]);
-                } else {
-                    ph_g ^= 1u;  // this gram completion is not needed here
-                }
-            } else {
-                // exact pairwise decays on CUDA cores (every exponent <= 0)
-                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(pbuf);
-                for (int idx = tid; idx < kC * kC; idx += kCompute) {
-                    const int r = idx >> 6, s = idx & 63;
-                    float a = 0.f, p = 0.f;
-                    if ((s == r || dep(r, s)) && r < Ln) {
-                        for (int i = 0; i < kD; ++i) {
-                            const float e = fast_exp2(gval(r, i) - gval(s, i));
-                            const float kse = kval(kRawK, s, i) * e;
-                            a = fmaf(kval(kRawK, r, i), kse, a);
-                            p = fmaf(kval(kRawQ, r, i), kse, p);
+                        for (int e = 0; e < 8; ++e) {
+                            const float el = fast_exp2(gv[e]);
+                            lk[e] = kv[e] * el;
+                            lq[e] = qv[e] * el;
+                            rv[e] = kv[e] * fast_exp2(gl[e] - gv[e]);
                         }
                     }
-                    const float av = dep(r, s) ? bvec[r] * a : 0.f;
-                    if ((r >> 4) == (s >> 4))
-                        sA[diagT_idx(r >> 4, s & 15, r & 15)] = av;
-                    else
-                        sA[sq_idx(r, s)] = av;
-                    op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(p);
+                    *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(r, ch, kD)) = pack_bf16x8(lq);
+                    *reinterpret_cast<uint4 *>(smem + kOpL + kmajor_off(64 + r, ch, kD)) = pack_bf16x8(lk);
+                    *reinterpret_cast<uint4 *>(rbuf + kmajor_off(r, ch, kD)) = pack_bf16x8(rv);
                 }
-                handoff(kBarDiag, kCompute + 64, true);  // the solver warps invert I + A
+            }
+            if (slow) {
+                // ---------------- exact path: A (f32, beta-scaled) and P (bf16) from
+                // pairwise decays exp(G_r - G_s) <= 1 on CUDA cores; the solvers
+                // must be done with A, and the output product with P
+                if (c > 0) {
+                    wait(MB_GFREE, c - 1);
+                    wait(MB_X, c - 1);
+                }
+                float *sA = reinterpret_cast<float *>(smem + kA32);
+                for (int idx = pt; idx < 64 * 64 / 4; idx += kPrepThreads)
+                    reinterpret_cast<float4 *>(sA)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int idx = pt; idx < 64 * 64 * 2 / 16; idx += kPrepThreads)
+                    reinterpret_cast<uint4 *>(smem + kOpP)[idx] = make_uint4(0, 0, 0, 0);
+                named_sync(kNbPrep, kPrepThreads);
+                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
+                const float *gsv = reinterpret_cast<const float *>(smem + kGsc);
+                // warp pw: rows r = pw, pw + 8, ...; lanes over 4-channel groups
+#pragma unroll 1
+                for (int r = pw; r < L; r += 8) {
+                    const float br = beta[(tok0 + t0 + r) * HV + hv];
+                    float4 gr4;
+                    if (SCALAR_G) {
+                        gr4 = make_float4(gsv[r], gsv[r], gsv[r], gsv[r]);
+                    } else {
+                        gr4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, 4 * lane));
+                    }
+                    const uint2 kr2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(r, 4 * lane));
+                    const uint2 qr2 = *reinterpret_cast<const uint2 *>(smem + kRawQ + kq_off(r, 4 * lane));
+                    const float2 k01 = unpack_bf16x2(kr2.x), k23 = unpack_bf16x2(kr2.y);
+                    const float2 q01 = unpack_bf16x2(qr2.x), q23 = unpack_bf16x2(qr2.y);
+#pragma unroll 1
+                    for (int s = 0; s <= r; ++s) {
+                        float4 gs4;
+                        if (SCALAR_G) {
+                            gs4 = make_float4(gsv[s], gsv[s], gsv[s], gsv[s]);
+                        } else {
+                            gs4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(s, 4 * lane));
+                        }
+                        const uint2 ks2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(s, 4 * lane));
+                        const float2 s01 = unpack_bf16x2(ks2.x), s23 = unpack_bf16x2(ks2.y);
+                        const float e0 = fast_exp2(gr4.x - gs4.x), e1 = fast_exp2(gr4.y - gs4.y);
+                        const float e2 = fast_exp2(gr4.z - gs4.z), e3 = fast_exp2(gr4.w - gs4.w);
+                        const float k0 = s01.x * e0, k1 = s01.y * e1, k2 = s23.x * e2, k3 = s23.y * e3;
+                        float a = k01.x * k0 + k01.y * k1 + k23.x * k2 + k23.y * k3;
+                        float pv = q01.x * k0 + q01.y * k1 + q23.x * k2 + q23.y * k3;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            a += __shfl_xor_sync(0xffffffffu, a, o);
+                            pv += __shfl_xor_sync(0xffffffffu, pv, o);
+                        }
+                        if (lane == 0) {
+                            if (s < r) {
+                                if ((r >> 4) == (s >> 4))
+                                    sA[diagT_idx(r >> 4, s & 15, r & 15)] = br * a;
+                                else
+                                    sA[sq_idx(r, s)] = br * a;
+                            }
+                            op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(pv);
+                        }
+                    }
+                }
+            }
+            // the tiles (and on the exact path A and P) are read by the tensor core
+            fence_async_smem();
+            named_sync(kNbPrep, kPrepThreads);
+            if (pt == 0) {
+                slow_flag[par] = slow ? 1 : 0;
+                mbar_arrive(bar(MB_TILES));
+            }
+            // ---------------- P read-back (gram rows 0-63): lane quarter 0-1 warps
+            if (p_reader) {
+                wait(MB_GRAM, c);
+                if (!slow) {
+                    if (c > 0) wait(MB_X, c - 1);  // the output product has read the previous P
+                    tc_fence_after_sync();
+                    const int r = 32 * (warp & 3) + lane, s0 = 32 * (pw >> 2);
+                    float d[32];
+                    tmem_ld32(tl + kTmGram + s0, d);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) d[u] = (s0 + u <= r && r < L) ? d[u] : 0.f;
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(smem + kOpP + kmajor_off(r, s0 + 8 * q8, kC)) =
+                            pack_bf16x8(&d[8 * q8]);
+                    fence_async_smem();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(MB_TP));
+                    mbar_arrive(bar(MB_GFREE));
+                }
             }
         }
-
-        // ---------------- 6 scan: state and O^T read-back, outputs
-        if (has_scan) {
-            wait_on(bar_4, ph_4);  // batch 4 of chunk c
+    } else if (warp == kWarpChainIssuer) {
+        // ================= chain issuer
+        const uint32_t vid = idesc_bf16(128, 64, true, false, false);   // V: MN-major A
+        const uint32_t ids = idesc_bf16(128, 128, false, true, false);  // R^T: MN-major B
+        const uint64_t tdesc = smem_desc(sbase + kOpT, 128, kC * 16);
+#pragma unroll 1
+        for (int c = 0; c < NC; ++c) {
+            named_sync(kNbS, kHandThreads);  // X and S'^T of chunk c are in TMEM
+            if (lane == 0) {
+                wait(MB_TILES, c);
+                if (!*abort_flag) {  // Z^T = S'^T Lk^T
+                    tc_fence_after_sync();
+                    gemm_ts<kD / 16>(tmem + kTmZ, tmem + kTmSb,
+                                     smem_desc(sbase + kOpL + 16384, 128, kD * 16), 256, io, false);
+                    mma_commit(bar(MB_Z));
+                }
+            }
+            __syncwarp();
+            if (c > 0) named_sync(kNbOfree, kHandThreads);  // O^T of chunk c - 1 is read
+            if (lane == 0) {
+                if (!*abort_flag) {  // O^T = S'^T Lq^T
+                    tc_fence_after_sync();
+                    gemm_ts<kD / 16>(tmem + kTmO, tmem + kTmSb, smem_desc(sbase + kOpL, 128, kD * 16),
+                                     256, io, false);
+                    mma_commit(bar(MB_OPART));
+                }
+                wait(MB_TP, c);
+                wait(MB_V, c);
+                if (!*abort_flag) {  // U^T = V^T T'^T (V: 128B-swizzled MN-major)
+                    tc_fence_after_sync();
+                    gemm_ss<kC / 16>(tmem + kTmU, smem_desc_sw128(sbase + kOpV, 8192, 1024), 2048, tdesc,
+                                     256, vid, false);
+                }
+            }
+            __syncwarp();
+            named_sync(kNbZb, kHandThreads);
+            if (lane == 0 && !*abort_flag) {  // U^T += (-Z^T) T'^T
+                tc_fence_after_sync();
+                gemm_ts<kC / 16>(tmem + kTmU, tmem + kTmZb, tdesc, 256, io, true);
+                mma_commit(bar(MB_U));
+            }
+            __syncwarp();
+            named_sync(kNbUb, kHandThreads);
+            if (lane == 0 && !*abort_flag) {
+                tc_fence_after_sync();
+                // X^T += U^T R (R read transposed), O^T += U^T P^T
+                gemm_ts<kC / 16>(tmem + kTmX, tmem + kTmUb,
+                                 smem_desc(sbase + kOpR + (c & 1) * 16384, kD * 16, 128), 4096, ids, true);
+                gemm_ts<kC / 16>(tmem + kTmO, tmem + kTmUb, smem_desc(sbase + kOpP, 128, kC * 16), 256,
+                                 io, true);
+                mma_commit(bar(MB_X));
+            }
+            __syncwarp();
+        }
+    } else if (warp >= kWarpSolver0) {
+        // ================= solver warps: T' of each chunk; warp sw reads the A
+        // rows 32 sw .. 32 sw + 31 (TMEM lanes 64 + 32 sw ..)
+        const int sw = warp - kWarpSolver0;
+        const int st = tid - 32 * kWarpSolver0;  // 0..63
+        float *sA = reinterpret_cast<float *>(smem + kA32);
+        float *sT = reinterpret_cast<float *>(smem + kT32);
+        float *sX = reinterpret_cast<float *>(smem + kX32);
+        float *bvec = reinterpret_cast<float *>(smem + kBeta);
+        const FragOffsets fo = frag_offsets(lane);
+        float bnext = st < T ? beta[(tok0 + st) * HV + hv] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < NC; ++c) {
+            const int t0 = c * kC, L = min(kC, T - t0);
+            bvec[st] = bnext;
+            named_sync(kNbSolve, 64);
+            if (c + 1 < NC) bnext = t0 + kC + st < T ? beta[(tok0 + t0 + kC + st) * HV + hv] : 0.f;
+            wait(MB_GRAM, c);
+            if (slow_flag[c & 1] == 0) {
+                // A = beta-scaled strictly lower part of gram rows 64-127
+                tc_fence_after_sync();
+                const int r = 32 * sw + lane, rb = r >> 4;
+                const float br = bvec[r];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (sw == 0 && g >= 2) break;  // rows 0-31: column blocks 0-1 only
+                    float dd[16];
+                    tmem_ld16(tl + kTmGram + 16 * g, dd);
+                    if (g == rb) {  // diagonal block, stored transposed
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            sA[diagT_idx(g, u, r & 15)] = (16 * g + u < r && r < L) ? br * dd[u] : 0.f;
+                    } else if (g < rb) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) sA[sq_idx(r, 16 * g + u)] = r < L ? br * dd[u] : 0.f;
+                    }
+                }
+            }
+            if (c > 0) wait(MB_U, c - 1);  // the U product has read the previous T'
+            // Each solver warp's diagonal blocks and level-1 block use only the
+            // rows it wrote itself (or, on the exact path, rows written before
+            // the gram barrier): a warp barrier suffices until level 2.
+            __syncwarp();
             {
-                // S' <- alpha S' + delta dS (the next chunk's S', or after the
-                // last chunk S itself: there the factors are rho and cL; a
-                // tree carries no state)
-                const float4 *cl4 = reinterpret_cast<const float4 *>(vec(kCL, ps) + 32 * iq);
-                const float4 *gam4 = reinterpret_cast<const float4 *>(vec(kRho, ps) + 32 * iq);
-                float dd[32];
-                if (!TREE) tmem_ld32(tl + kTmDS + 32 * iq, dd);
+                // diagonal 16 x 16 blocks of T = (I + A)^-1: one thread per column
+                // (block I = st / 16, column jj = st % 16), right-looking
+                const int I = st >> 4, jj = st & 15;
+                float x[16];
 #pragma unroll
-                for (int u4 = 0; u4 < 8 && !TREE; ++u4) {  // packed fp32 pairs
-                    const float4 cl = cl4[u4], gm = gam4[u4];
-                    S2[2 * u4] = __ffma2_rn(make_float2(gm.x, gm.y), S2[2 * u4],
-                                            __fmul2_rn(make_float2(cl.x, cl.y),
-                                                       make_float2(dd[4 * u4], dd[4 * u4 + 1])));
-                    S2[2 * u4 + 1] = __ffma2_rn(make_float2(gm.z, gm.w), S2[2 * u4 + 1],
-                                                __fmul2_rn(make_float2(cl.z, cl.w),
-                                                           make_float2(dd[4 * u4 + 2], dd[4 * u4 + 3])));
-                }
-                // O^T -> this warp's bf16 O box [16 r][32 j] (rows 16 iq .., columns 32 wq ..)
-                float oo[16];
-                tmem_ld16(tl + kTmOT + 16 * iq, oo);
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + kStage + 1024 * warp);
-                // the previous chunk's store from this box must have read it
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
+                for (int p = 0; p < 16; ++p) x[p] = (p == jj) ? 1.f : 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; u += 2) {  // converted in pairs, stored per row
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(oo[u], oo[u + 1]);
-                    stg[u * 32 + lane] = h.x;
-                    stg[(u + 1) * 32 + lane] = h.y;
+                for (int s2 = 0; s2 < 15; ++s2) {
+                    const float4 *col = reinterpret_cast<const float4 *>(sA + diagT_idx(I, s2, 0));
+#pragma unroll
+                    for (int g4 = (s2 + 1) >> 2; g4 < 4; ++g4) {
+                        const float4 a = col[g4];
+                        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * g4 + e > s2) x[4 * g4 + e] = fmaf(-av[e], x[s2], x[4 * g4 + e]);
+                    }
                 }
-                fence_async_smem();
+                __nv_bfloat16 *opt = reinterpret_cast<__nv_bfloat16 *>(smem + kOpT);
+                const float bj = bvec[16 * I + jj];
+#pragma unroll
+                for (int p = 0; p < 16; p += 2) {
+                    sT[sq_idx(16 * I + p, 16 * I + jj)] = x[p];
+                    sT[sq_idx(16 * I + p + 1, 16 * I + jj)] = x[p + 1];
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(x[p] * bj, x[p + 1] * bj);
+                    opt[kmajor_off(16 * I + p, 16 * I + jj, kC) >> 1] = h.x;
+                    opt[kmajor_off(16 * I + p + 1, 16 * I + jj, kC) >> 1] = h.y;
+                }
+            }
+            __syncwarp();
+            // off-diagonal blocks by 32 x 32 block recursion:
+            //   T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22,
+            //   [T_20 T_21; T_30 T_31] = -[T_22 0; T_32 T_33] [A_20 A_21; A_30 A_31] [T_00 0; T_10 T_11]
+            auto emit = [&](int I, int J, const float (&acc)[2][4]) {  // T_IJ = -acc
+                const int gq = lane >> 2, tq = lane & 3;
+                float *trow = sT + I * 1024 + 16 * (J ^ (I & 1)) + gq * 64;
+                const int u0 = (2 * tq) ^ gq, u1 = (2 * tq + 1) ^ gq;
+                unsigned char *prow = smem + kOpT + 2 * I * 1024 + gq * 16 + 4 * tq;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float2 bb = *reinterpret_cast<const float2 *>(bvec + 16 * J + 8 * nt + 2 * tq);
+                    trow[8 * nt + u0] = -acc[nt][0];
+                    trow[8 * nt + u1] = -acc[nt][1];
+                    trow[512 + 8 * (nt ^ 1) + u0] = -acc[nt][2];
+                    trow[512 + 8 * (nt ^ 1) + u1] = -acc[nt][3];
+                    // T' = T diag(beta), bf16, K-major [64 r][64 s]
+                    *reinterpret_cast<uint32_t *>(prow + (2 * J + nt) * 128) =
+                        pack_bf16x2(-acc[nt][0] * bb.x, -acc[nt][1] * bb.y);
+                    *reinterpret_cast<uint32_t *>(prow + 1024 + (2 * J + nt) * 128) =
+                        pack_bf16x2(-acc[nt][2] * bb.x, -acc[nt][3] * bb.y);
+                }
+            };
+            {  // level 1: block (1,0) on solver 0, (3,2) on solver 1
+                const int I = 2 * sw + 1, J = 2 * sw;
+                float acc[2][4] = {};
+                blk_mma2<true>(acc, swz_block(sA, I, J), swz_block(sT, J, J), fo);
+                blk_store(sX + 256 * sw, acc, lane);
                 __syncwarp();
-                // one TMA store per warp; rows past the end of the sequence
-                // fall outside the tensor and are dropped
-                if (lane == 0 && !*abort_flag) {
-                    tma_store_4d(&m.o, stg, 32 * wq, hv, t0 + 16 * iq, b);
-                    bulk_commit_group();
+                float yv[2][4] = {};
+                blk_mma2<false>(yv, swz_block(sT, I, I), sX + 256 * sw, fo);
+                emit(I, J, yv);
+            }
+            named_sync(kNbSolve, 64);
+            {  // level 2, row I = 2 + sw of X = [A_20 A_21; A_30 A_31] T1
+                const int I = 2 + sw;
+                float x0[2][4] = {}, x1[2][4] = {};
+                blk_mma2<true>(x0, swz_block(sA, I, 0), swz_block(sT, 0, 0), fo);
+                blk_mma2<true>(x0, swz_block(sA, I, 1), swz_block(sT, 1, 0), fo);
+                blk_mma2<true>(x1, swz_block(sA, I, 1), swz_block(sT, 1, 1), fo);
+                blk_store(sX + 256 * (2 * sw), x0, lane);
+                blk_store(sX + 256 * (2 * sw + 1), x1, lane);
+            }
+            named_sync(kNbSolve, 64);
+            {  // level 2, column J = sw of T_lo = -T2 X
+                const int J = sw;
+                float t2[2][4] = {}, t3[2][4] = {};
+                blk_mma2<false>(t2, swz_block(sT, 2, 2), sX + 256 * J, fo);
+                blk_mma2<false>(t3, swz_block(sT, 3, 2), sX + 256 * J, fo);
+                blk_mma2<false>(t3, swz_block(sT, 3, 3), sX + 256 * (2 + J), fo);
+                emit(2, J, t2);
+                emit(3, J, t3);
+            }
+            fence_async_smem();  // T' is read by the tensor core
+            tc_fence_before_sync();
+            named_sync(kNbSolve, 64);
+            if (st == 0) {
+                mbar_arrive(bar(MB_TP));
+                mbar_arrive(bar(MB_GFREE));
+            }
+        }
+    } else {
+        // ================= producer (lane 0).  Per chunk c: once chunk c's
+        // tiles are built, the raw k, q, g copies of chunk c + 1 (their buffers
+        // are free) and the gram of chunk c (once the previous gram is read);
+        // then v of chunk c (once chunk c - 1's U product has read v).
+        if (lane == 0) {
+            if (VARLEN) {
+                // the maps were written to global memory before the launch
+                fence_tensormap_acquire(&m.k);
+                fence_tensormap_acquire(&m.q);
+                if (!SCALAR_G) fence_tensormap_acquire(&m.g);
+                fence_tensormap_acquire(&m.v);
+            }
+            tma_prefetch_desc(&m.k);
+            tma_prefetch_desc(&m.q);
+            if (!SCALAR_G) tma_prefetch_desc(&m.g);
+            tma_prefetch_desc(&m.v);
+            auto load_raw = [&](int t0) {
+                if (*abort_flag) return;
+                mbar_arrive_expect_tx(bar(MB_RAW), SCALAR_G ? kBytesKQG - 32768 : kBytesKQG);
+                tma_load_4d(smem + kRawK, &m.k, 0, hk, t0, b, bar(MB_RAW));
+                tma_load_4d(smem + kRawK + 8192, &m.k, 64, hk, t0, b, bar(MB_RAW));
+                tma_load_4d(smem + kRawQ, &m.q, 0, hk, t0, b, bar(MB_RAW));
+                tma_load_4d(smem + kRawQ + 8192, &m.q, 64, hk, t0, b, bar(MB_RAW));
+                if (!SCALAR_G) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        tma_load_4d(smem + kG + 8192 * q4, &m.g, 32 * q4, hv, t0, b, bar(MB_RAW));
+                }
+                ++issued_raw;
+            };
+            load_raw(0);
+#pragma unroll 1
+            for (int c = 0; c < NC; ++c) {
+                wait(MB_TILES, c);
+                if (c + 1 < NC) load_raw((c + 1) * kC);
+                if (c > 0) wait(MB_GFREE, c - 1);
+                if (slow_flag[c & 1] != 0) {
+                    mbar_arrive(bar(MB_GRAM));  // A and P came from the exact path
+                } else if (!*abort_flag) {
+                    tc_fence_after_sync();
+                    gemm_ss<kD / 16>(tmem + kTmGram, smem_desc(sbase + kOpL, 128, kD * 16), 256,
+                                     smem_desc(sbase + kOpR + (c & 1) * 16384, 128, kD * 16), 256, io,
+                                     false);
+                    mma_commit(bar(MB_GRAM));
+                }
+                if (c > 0) wait(MB_U, c - 1);
+                if (!*abort_flag) {
+                    mbar_arrive_expect_tx(bar(MB_V), kBytesV);
+                    tma_load_4d(smem + kOpV, &m.v, 0, hv, c * kC, b, bar(MB_V));
+                    tma_load_4d(smem + kOpV + 8192, &m.v, 64, hv, c * kC, b, bar(MB_V));
+                    ++issued_v;
                 }
             }
         }
-        // S'^T = (diag(exp(G_m)) S)^T of the prepared chunk as the bf16 A
-        // operand of batch a (the registers hold S' already, except for the
-        // first chunk, whose h0 is scaled here; the previous batch a was
-        // waited for in step 2)
-        if (has_prep) {
-            if (!has_scan) {
-                const float4 *egm4 = reinterpret_cast<const float4 *>(vec(kEGm, pn) + 32 * iq);
-#pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 e = egm4[u4];
-                    S2[2 * u4] = __fmul2_rn(S2[2 * u4], make_float2(e.x, e.y));
-                    S2[2 * u4 + 1] = __fmul2_rn(S2[2 * u4 + 1], make_float2(e.z, e.w));
-                }
-            }
-            uint32_t w[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(S2[h].x, S2[h].y);
-            tmem_st16(tl + kTmSTb + 16 * iq, w);
-            tmem_st_wait();
-            if (has_next2 && tid < kC) cp_async_wait_all();  // beta of chunk cn + 1
-            handoff(kBarH4, kHand, false);
-        }
+        __syncwarp();
     }
 
-    if (!aux && lane == 0) bulk_wait_all();
     __syncthreads();
     const bool aborted = *abort_flag != 0;
-    if (tid == kCompute && aborted) atomicOr(dev_error, 1);
-    if (tid == kCompute + 32 && aborted) {
+    if (tid == 0 && aborted) atomicOr(dev_error, 1);
+    if (warp == kWarpProducer && lane == 0 && aborted) {
         // never leave with copies in flight: wait (bounded) for the last copy
         // issued on each barrier; its phases complete in order
-        mbar_wait_bounded(bar_kqg, (uint32_t)((issued_kqg - 1) & 1), kWaitLimitNs);
-        mbar_wait_bounded(bar_v, (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
-    }
-    if (!aborted && STORE_HT && !aux) {
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            ht[(shead * kD + 32 * iq + 2 * h) * kD + j] = S2[h].x;
-            ht[(shead * kD + 32 * iq + 2 * h + 1) * kD + j] = S2[h].y;
-        }
+        if (issued_raw > 0) mbar_wait_bounded(bar(MB_RAW), (uint32_t)((issued_raw - 1) & 1), kWaitLimitNs);
+        if (issued_v > 0) mbar_wait_bounded(bar(MB_V), (uint32_t)((issued_v - 1) & 1), kWaitLimitNs);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1128,51 +1056,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
 }
-
-// ---- host side: TMA tensor maps, encoded per call through the driver entry point
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn(cudaError_t *err) {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    static cudaError_t status = cudaSuccess;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                                  cudaEnableDefault, &q);
-        if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
-        fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    *err = status;
-    return fn;
-}
-
-// [B][T][H][128] tensor of `esize`-byte elements; boxes of `box_inner`
-// elements x 64 tokens, 128-byte swizzled, zero fill outside the tensor.
-bool encode_map(EncodeTiledFn fn, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
-                int esize, int B, int T, int H, int box_inner,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int box_rows = 64) {
-    const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)128 * esize, (cuuint64_t)H * 128 * esize,
-                                   (cuuint64_t)T * H * 128 * esize};
-    const cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, (cuuint32_t)box_rows, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
-
-bool tc_prefill_supported(const Problem &p) {
-    return p.bf16 && p.dk == kD && p.dv == kD && p.chunk == kC;
-}
-
-namespace {
 
 // The five tensor maps of a [B][T][H][128] problem whose token 0 of batch 0
 // sits at row `tok0` of the packed tensors.
@@ -1184,52 +1067,53 @@ bool encode_maps(EncodeTiledFn fn, TileMaps *tm, const Problem &p, size_t tok0, 
     const char *o = static_cast<const char *>(p.out) + tok0 * p.HV * kD * 2;
     // a scalar gate's g is read without a tensor map
     if (p.g_scalar) memset(&tm->g, 0, sizeof(tm->g));
-    return encode_map(fn, &tm->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
-           encode_map(fn, &tm->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64) &&
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    return tma_encode_rows(fn, &tm->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64, sw, 64) &&
+           tma_encode_rows(fn, &tm->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HK, 64, sw, 64) &&
            (p.g_scalar ||
-            encode_map(fn, &tm->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, p.HV, 32)) &&
-           encode_map(fn, &tm->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 64) &&
-           // output: unswizzled [16 tokens][32 channels] boxes, one per state warp
-           encode_map(fn, &tm->o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 32,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, 16);
+            tma_encode_rows(fn, &tm->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, p.HV, 32, sw, 64)) &&
+           tma_encode_rows(fn, &tm->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 64, sw, 64) &&
+           // output: unswizzled [32 tokens][32 channels] boxes, one per chain warp
+           tma_encode_rows(fn, &tm->o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, T, p.HV, 32,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, 32);
 }
 
-template <bool VARLEN, bool TREE, bool SCALAR_G>
+template <bool VARLEN, bool SCALAR_G>
 cudaError_t launch_tc(const Problem &p, const TileMaps &tm, const TileMaps *seq_maps,
-                      const int4 *seqs, const int *parents, long long blocks, int *dev_error,
-                      cudaStream_t stream) {
+                      const int4 *seqs, long long blocks, int *dev_error, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
     auto run = [&](auto kernel) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         trace_begin(kKernFused, stream);
         kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(
-            tm, seq_maps, seqs, parents, p.beta, p.g, p.h0, p.ht, p.T, p.HK, p.HV, dev_error);
+            tm, seq_maps, seqs, p.beta, p.g, p.h0, p.ht, p.T, p.HK, p.HV, dev_error);
         trace_end(kKernFused, stream);
         return cudaGetLastError();
     };
-    if (TREE)  // outputs only
-        return p.h0 ? run(gdr_prefill_tc_kernel<true, false, false, true, false>)
-                    : run(gdr_prefill_tc_kernel<false, false, false, true, false>);
-    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN, false, SCALAR_G>);
-    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN, false, SCALAR_G>);
-    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN, false, SCALAR_G>);
-    return run(gdr_prefill_tc_kernel<false, false, VARLEN, false, SCALAR_G>);
+    if (p.h0 && p.ht) return run(gdr_prefill_tc_kernel<true, true, VARLEN, SCALAR_G>);
+    if (p.h0) return run(gdr_prefill_tc_kernel<true, false, VARLEN, SCALAR_G>);
+    if (p.ht) return run(gdr_prefill_tc_kernel<false, true, VARLEN, SCALAR_G>);
+    return run(gdr_prefill_tc_kernel<false, false, VARLEN, SCALAR_G>);
 }
 
 }  // namespace
 
+bool tc_prefill_supported(const Problem &p) {
+    return p.bf16 && p.dk == kD && p.dv == kD && p.chunk == kC;
+}
+
 cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
-    EncodeTiledFn fn = encode_fn(&e);
+    EncodeTiledFn fn = tma_encode_fn(&e);
     if (e != cudaSuccess) return e;
     TileMaps tm;
     if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
-    return p.g_scalar ? launch_tc<false, false, true>(p, tm, nullptr, nullptr, nullptr,
-                                                      (long long)p.B * p.HV, dev_error, stream)
-                      : launch_tc<false, false, false>(p, tm, nullptr, nullptr, nullptr,
-                                                       (long long)p.B * p.HV, dev_error, stream);
+    const long long blocks = (long long)p.B * p.HV;
+    return p.g_scalar ? launch_tc<false, true>(p, tm, nullptr, nullptr, blocks, dev_error, stream)
+                      : launch_tc<false, false>(p, tm, nullptr, nullptr, blocks, dev_error, stream);
 }
 
 size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
@@ -1237,16 +1121,17 @@ size_t tc_seq_maps_bytes() { return sizeof(TileMaps); }
 cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst,
                                const void *v_row, void *o_row) {
     cudaError_t e = cudaSuccess;
-    EncodeTiledFn fn = encode_fn(&e);
+    EncodeTiledFn fn = tma_encode_fn(&e);
     if (e != cudaSuccess) return e;
     TileMaps tm;
     if (!encode_maps(fn, &tm, p, tok0, 1, L)) return cudaErrorInvalidValue;
     // one-row stand-ins: every load past row 0 reads the zero fill, every
     // store past row 0 is dropped
-    if (v_row && !encode_map(fn, &tm.v, v_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV, 64))
+    if (v_row && !tma_encode_rows(fn, &tm.v, v_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV,
+                                  64, CU_TENSOR_MAP_SWIZZLE_128B, 64))
         return cudaErrorInvalidValue;
-    if (o_row && !encode_map(fn, &tm.o, o_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV, 32,
-                             CU_TENSOR_MAP_SWIZZLE_NONE, 16))
+    if (o_row && !tma_encode_rows(fn, &tm.o, o_row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, 1, p.HV,
+                                  32, CU_TENSOR_MAP_SWIZZLE_NONE, 32))
         return cudaErrorInvalidValue;
     memcpy(dst, &tm, sizeof(TileMaps));
     return cudaSuccess;
@@ -1257,25 +1142,9 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
     TileMaps unused;
     memset(&unused, 0, sizeof(unused));
     const TileMaps *maps = static_cast<const TileMaps *>(seq_maps);
-    return p.g_scalar ? launch_tc<true, false, true>(p, unused, maps, seqs, nullptr,
-                                                     (long long)nseq * p.HV, dev_error, stream)
-                      : launch_tc<true, false, false>(p, unused, maps, seqs, nullptr,
-                                                      (long long)nseq * p.HV, dev_error, stream);
-}
-
-cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
-                           cudaStream_t stream) {
-    if (p.T > kC) return cudaErrorInvalidValue;
-    cudaError_t e = cudaSuccess;
-    EncodeTiledFn fn = encode_fn(&e);
-    if (e != cudaSuccess) return e;
-    TileMaps tm;
-    if (!encode_maps(fn, &tm, p, 0, p.B, p.T)) return cudaErrorInvalidValue;
-    Problem outputs_only = p;
-    outputs_only.ht = nullptr;
-    if (p.g_scalar) return cudaErrorInvalidValue;  // trees with a scalar gate: CUDA cores
-    return launch_tc<false, true, false>(outputs_only, tm, nullptr, nullptr, parents,
-                                         (long long)p.B * p.HV, dev_error, stream);
+    return p.g_scalar
+               ? launch_tc<true, true>(p, unused, maps, seqs, (long long)nseq * p.HV, dev_error, stream)
+               : launch_tc<true, false>(p, unused, maps, seqs, (long long)nseq * p.HV, dev_error, stream);
 }
 
 }  // namespace gdr

@@ -61,6 +61,16 @@ __device__ __forceinline__ uint32_t sw128_mnmajor_off(int k, int mn, int k_exten
                       ((((mn & 63) >> 3) ^ (k & 7)) << 4) + (mn & 7) * 2);
 }
 
+// Byte offset of element (row, k) in a K-major 128-byte-swizzled bf16 tile
+// made of 64-element K blocks of `rows` rows each: a row's 64 elements fill
+// one 128-byte line whose 16-byte chunks are XORed with the row index within
+// its 8-row (1024-byte) atom -- the layout a TMA load of [rows][64] boxes with
+// CU_TENSOR_MAP_SWIZZLE_128B writes.
+__device__ __forceinline__ uint32_t sw128_kmajor_off(int row, int k, int rows) {
+    return (uint32_t)((k >> 6) * (rows * 128) + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) +
+                      (k & 7) * 2);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, f32 accumulator:
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 // (1 = bf16), 13 negate A, 15 A major (1 = MN-major), 16 B major,
@@ -123,6 +133,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {

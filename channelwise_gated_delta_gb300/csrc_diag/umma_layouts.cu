@@ -1,9 +1,12 @@
-// selftest.cu -- gdr_selftest_umma: one tensor-core GEMM through the same
-// shared-memory layouts, descriptors, MMA issue and TMEM read-back the
-// prefill kernel uses, so a layout or descriptor fault can be told apart from
-// an algebra fault.  D[128 x N] = A[128 x 64] * B[N x 64]^T, bf16 in, f32 out.
-#include "common.cuh"
-#include "gdr.h"
+// umma_layouts.cu -- test-only diagnostic library (libgdr_diag.so, not part
+// of the product library): one tensor-core GEMM through the shared-memory
+// operand layouts, descriptors, MMA issue and TMEM read-back that the
+// tensor-core kernels use, so that a layout or descriptor fault can be told
+// apart from an algebra fault.  D[128 x N] = A[128 x 64] * B[N x 64]^T, bf16
+// in, f32 out.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
 #include "sm100_ptx.cuh"
 
 namespace gdr {
@@ -28,10 +31,13 @@ __global__ void __launch_bounds__(128, 1)
     }
     // Layout modes: 0 = K-major (row m or n), 1 = MN-major, 2 = a K-major tile
     // of the transpose (rows k, K extent M or N) read back through an MN-major
-    // descriptor with LBO and SBO swapped in role.
+    // descriptor with LBO and SBO swapped in role, 3 = MN-major with the
+    // 128-byte swizzle, 5 = K-major with the 128-byte swizzle (rows of 64
+    // elements, 8-row atoms).
     for (int idx = tid; idx < kM * kK; idx += 128) {
         const int m = idx / kK, k = idx % kK;
-        const uint32_t off = a_mn == 3   ? sw128_mnmajor_off(k, m, kK)
+        const uint32_t off = a_mn == 5   ? sw128_kmajor_off(m, k, kM)
+                             : a_mn == 3 ? sw128_mnmajor_off(k, m, kK)
                              : a_mn == 2 ? kmajor_off(k, m, kM)
                              : a_mn == 1 ? mnmajor_off(k, m, kK)
                                          : kmajor_off(m, k, kK);
@@ -39,7 +45,8 @@ __global__ void __launch_bounds__(128, 1)
     }
     for (int idx = tid; idx < N * kK; idx += 128) {
         const int n = idx / kK, k = idx % kK;
-        const uint32_t off = b_mn == 3   ? sw128_mnmajor_off(k, n, kK)
+        const uint32_t off = b_mn == 5   ? sw128_kmajor_off(n, k, N)
+                             : b_mn == 3 ? sw128_mnmajor_off(k, n, kK)
                              : b_mn == 2 ? kmajor_off(k, n, N)
                              : b_mn == 1 ? mnmajor_off(k, n, kK)
                                          : kmajor_off(n, k, kK);
@@ -71,25 +78,32 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after_sync();
     }
     if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(kM, N, a_mn != 0, b_mn != 0, false);
+        const bool a_t = a_mn != 0 && a_mn != 5, b_t = b_mn != 0 && b_mn != 5;  // MN-major
+        const uint32_t idesc = idesc_bf16(kM, N, a_t, b_t, false);
         // K-direction / MN-direction core-matrix strides of each operand
         const uint32_t a_lbo = a_mn == 2 ? kM * 16 : 128, a_sbo = a_mn == 2 ? 128 : kK * 16;
         const uint32_t b_lbo = b_mn == 2 ? N * 16 : 128, b_sbo = b_mn == 2 ? 128 : kK * 16;
         for (int ks = 0; ks < kK / 16 && a_mn == 4; ++ks) {
             const uint64_t bd =
-                b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
-                          : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
-            mma_bf16_ts(tmem, tmem + 128 + 8 * ks, bd, idesc_bf16(kM, N, false, b_mn != 0, false),
+                b_mn == 5   ? smem_desc_sw128(smem_u32(sb) + ks * 32, 16, 1024)
+                : b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
+                            : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
+            mma_bf16_ts(tmem, tmem + 128 + 8 * ks, bd, idesc_bf16(kM, N, false, b_t, false),
                         ks > 0 ? 1u : 0u);
         }
         for (int ks = 0; ks < kK / 16 && a_mn != 4; ++ks) {
             // swizzled MN-major: 64-element blocks of kK rows (LBO), 8-row atoms (SBO)
+            // K-major swizzled: each K step of 16 elements advances the start
+            // address by 32 bytes inside the 128-byte row (the swizzle is applied
+            // to the absolute address); LBO is not used
             const uint64_t ad =
-                a_mn == 3 ? smem_desc_sw128(smem_u32(sa) + ks * 2048, kK * 128, 1024)
-                          : smem_desc(smem_u32(sa) + ks * 2 * a_lbo, a_lbo, a_sbo);
+                a_mn == 5   ? smem_desc_sw128(smem_u32(sa) + ks * 32, 16, 1024)
+                : a_mn == 3 ? smem_desc_sw128(smem_u32(sa) + ks * 2048, kK * 128, 1024)
+                            : smem_desc(smem_u32(sa) + ks * 2 * a_lbo, a_lbo, a_sbo);
             const uint64_t bd =
-                b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
-                          : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
+                b_mn == 5   ? smem_desc_sw128(smem_u32(sb) + ks * 32, 16, 1024)
+                : b_mn == 3 ? smem_desc_sw128(smem_u32(sb) + ks * 2048, kK * 128, 1024)
+                            : smem_desc(smem_u32(sb) + ks * 2 * b_lbo, b_lbo, b_sbo);
             mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
         }
         mma_commit(&bar);
@@ -119,24 +133,20 @@ __global__ void __launch_bounds__(128, 1)
 }  // namespace
 }  // namespace gdr
 
-extern "C" GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N,
-                                                const void *A, const void *B, float *D,
-                                                void *stream) {
-    if (!A || !B || !D) return GDR_ERR_NULL;
-    if (N != 64 && N != 128) return GDR_ERR_UNSUPPORTED;
-    if (a_mn_major < 0 || a_mn_major > 4 || b_mn_major < 0 || b_mn_major > 3)
-        return GDR_ERR_UNSUPPORTED;
-    int *err = nullptr;
-    cudaError_t e = gdr::device_error_word(&err);
-    if (e == cudaSuccess) {
-        gdr::gdr_selftest_umma_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-            static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, N,
-            a_mn_major, b_mn_major, err);
-        e = cudaGetLastError();
-    }
-    if (e != cudaSuccess) {
-        gdr::record_cuda_error(e);
-        return GDR_ERR_CUDA;
-    }
-    return GDR_OK;
+// D[128 x N] = A[128 x 64] * B[N x 64]^T (row-major bf16 in, row-major f32
+// out, device pointers), N in {64, 128}; a_mode (0-5) and b_mode (0-3, 5)
+// select the operand layouts listed in the kernel, a_mode 4 puts A in tensor
+// memory.  `err` is a device int that a timed-out wait sets to 1.  Returns 0,
+// or -1 for bad arguments, or the cudaError_t of the launch.
+extern "C" __attribute__((visibility("default"))) int gdr_diag_umma(int a_mode, int b_mode, int N,
+                                                                   const void *A, const void *B,
+                                                                   float *D, int *err,
+                                                                   void *stream) {
+    if (!A || !B || !D || !err) return -1;
+    if (N != 64 && N != 128) return -1;
+    if (a_mode < 0 || a_mode > 5 || b_mode < 0 || b_mode > 5 || b_mode == 4) return -1;
+    gdr::gdr_selftest_umma_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, N,
+        a_mode, b_mode, err);
+    return (int)cudaGetLastError();
 }

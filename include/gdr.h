@@ -330,22 +330,6 @@ GDR_API gdr_status gdr_device_check(void *stream);
 GDR_API gdr_status gdr_trace_enable(int on);
 GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, double *total_ms);
 
-/*
- * Diagnostic: one tensor-core GEMM through the shared-memory operand layouts,
- * descriptors and TMEM read-back of the tensor-core prefill.
- * D[128 x N] = A[128 x 64] * B[N x 64]^T with A, B row-major bf16 and D
- * row-major float32 (device pointers), N in {64, 128}.  a_mn_major /
- * b_mn_major pick the shared-memory layout of that operand: 0 K-major,
- * 1 MN-major, 2 a K-major tile of the transposed operand read through an
- * MN-major descriptor (the way the prefill reuses one tile for both
- * orientations), 3 MN-major with the 128-byte swizzle that TMA tensor loads
- * produce; a_mn_major = 4 places A in tensor memory instead (row m in lane
- * m, two consecutive-K bf16 values per 32-bit column).  Enqueued on
- * `stream`; a timed-out wait is reported by gdr_device_check.
- */
-GDR_API gdr_status gdr_selftest_umma(int a_mn_major, int b_mn_major, int N, const void *A,
-                                     const void *B, float *D, void *stream);
-
 /* Human-readable name of a gdr_status value (static string, never NULL). */
 GDR_API const char *gdr_status_string(int status);
 

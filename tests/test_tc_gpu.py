@@ -4,26 +4,26 @@ CUDA-core route, and the exact pairwise fallback for strong decay."""
 import pytest
 import torch
 
-from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_GENERIC, gdr_device_check,
-                                           gdr_selftest_umma)
+from channelwise_gated_delta_gb300 import GDR_FLAG_FORCE_GENERIC
 from channelwise_gated_delta_gb300.inputs import draw, to_f64
 from tests.parity_util import assert_close
 from tests.test_parity_gpu import check, run_gpu, run_oracle
+from tests.umma_diag import umma_gemm
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("a_mn", [0, 1, 2, 3, 4])
-@pytest.mark.parametrize("b_mn", [0, 1, 2, 3])
+@pytest.mark.parametrize("a_mn", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("b_mn", [0, 1, 2, 3, 5])
 @pytest.mark.parametrize("N", [64, 128])
 def test_umma_gemm_layouts(a_mn, b_mn, N):
-    """One tcgen05 GEMM per operand layout: bf16 products summed in f32 are
-    exact up to f32 rounding, so the result must match a f32 matmul closely."""
+    """One tcgen05 GEMM per operand layout (test-only diagnostic library):
+    bf16 products summed in f32 are exact up to f32 rounding, so the result
+    must match a f32 matmul closely."""
     g = torch.Generator(device="cpu").manual_seed(100 + N + 2 * a_mn + b_mn)
     A = torch.randn(128, 64, generator=g).to(torch.bfloat16).cuda()
     B = torch.randn(N, 64, generator=g).to(torch.bfloat16).cuda()
-    D = gdr_selftest_umma(A, B, a_mn_major=a_mn, b_mn_major=b_mn)
-    gdr_device_check()
+    D = umma_gemm(A, B, a_mn, b_mn)
     ref = A.double() @ B.double().T
     err = (D.double() - ref).abs().max().item()
     assert err <= 1e-4 * ref.abs().max().item(), err
