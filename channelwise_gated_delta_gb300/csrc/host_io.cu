@@ -77,6 +77,7 @@ struct DeviceIo {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t start = nullptr;
+    cudaEvent_t join_in = nullptr, join_out = nullptr;  // error paths: side streams -> caller
     cudaEvent_t in_ready[kSlots] = {}, computed[kSlots] = {}, out_done[kSlots] = {};
     cudaEvent_t state_done[kSlots] = {};
 };
@@ -94,6 +95,8 @@ cudaError_t device_io(DeviceIo **out) {
         e = cudaStreamCreateWithFlags(&io.in, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&io.out, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io.start, ef);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io.join_in, ef);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io.join_out, ef);
         for (int s = 0; s < kSlots && e == cudaSuccess; ++s) {
             e = cudaEventCreateWithFlags(&io.in_ready[s], ef);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io.computed[s], ef);
@@ -173,12 +176,33 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
         return GDR_ERR_CUDA;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    auto fail = [](cudaError_t err) {
+    // Once copies have been queued on the library's side streams, an error
+    // return must not leave them running behind the caller's back: they read
+    // and write the caller's host buffers and this call's staging.  The
+    // caller's stream is made to wait for both side streams (or, if that
+    // cannot be queued, the side streams are drained on the host) before the
+    // error is reported, so the caller may free or reuse its buffers once its
+    // own stream has completed.
+    bool queued = false;
+    auto join = [&]() {
+        if (!queued) return;
+        const bool ok = cudaEventRecord(io->join_in, io->in) == cudaSuccess &&
+                        cudaEventRecord(io->join_out, io->out) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, io->join_in, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(cs, io->join_out, 0) == cudaSuccess;
+        if (!ok) {
+            cudaStreamSynchronize(io->in);
+            cudaStreamSynchronize(io->out);
+        }
+    };
+    auto fail = [&](cudaError_t err) {
         gdr::record_cuda_error(err);
+        join();
         return GDR_ERR_CUDA;
     };
     // everything earlier on the caller's stream comes first
     if ((e = cudaEventRecord(io->start, cs)) != cudaSuccess) return fail(e);
+    queued = true;
     if ((e = cudaStreamWaitEvent(io->in, io->start, 0)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(io->out, io->start, 0)) != cudaSuccess) return fail(e);
 
@@ -238,7 +262,10 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
                 reinterpret_cast<const float *>(sl + L.beta), seg_h0, sl + L.out, state, 1, len,
                 HK, HV, dk, dv, chunk, cs, qkv_dtype, L.ws_b ? sl + L.ws : nullptr, L.ws_b,
                 kSegFlags);
-            if (st_fw != GDR_OK) return st_fw;
+            if (st_fw != GDR_OK) {
+                join();
+                return st_fw;
+            }
             if ((e = cudaEventRecord(io->computed[slot], cs)) != cudaSuccess) return fail(e);
             if ((e = cudaStreamWaitEvent(io->out, io->computed[slot], 0)) != cudaSuccess)
                 return fail(e);

@@ -150,3 +150,4 @@ extern "C" __attribute__((visibility("default"))) int gdr_diag_umma(int a_mode, 
         a_mode, b_mode, err);
     return (int)cudaGetLastError();
 }
+

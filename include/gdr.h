@@ -127,6 +127,9 @@ typedef enum gdr_dtype {
  * Bytes of device workspace gdr_forward_ex needs for this call (0 when the
  * chosen route needs none).  Returns 0 for arguments gdr_forward_ex would
  * reject.  Same shape arguments and flags as gdr_forward_ex.
+ * Passage: none in the pages; it sizes the scratch of the routes of
+ * gdr_forward_ex (the CUDA-core chunked prefill keeps per-chunk records, the
+ * segmented scan its tables and segment states).
  */
 GDR_API size_t gdr_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
                                    int qkv_dtype, unsigned flags);
@@ -136,6 +139,10 @@ GDR_API size_t gdr_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
  * memory of at least gdr_workspace_bytes(...) bytes (may be NULL when that is
  * 0), 256-byte aligned, not overlapping any other argument, and must not be
  * used by anything else until the enqueued work is done.  Allocates nothing.
+ * Passage: "Reorder channelwise gated delta rule chunked hot loops for
+ * autovectorization" (pytorch/executorch PR #21021), first commit summary
+ * (the two-pass token recurrence that T == 1 runs) and second commit summary
+ * (the routing by length and the chunkwise WY/UT form that T > 1 runs).
  */
 GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const float *h0, void *out, float *ht,
@@ -149,6 +156,16 @@ GDR_API gdr_status gdr_forward_ex(const void *q, const void *k, const void *v, c
  * (cudaMalloc synchronises the device, so a growing call is not
  * asynchronous).  Calls that share the library workspace must be ordered:
  * issue them on one stream per device, or use gdr_forward_ex.
+ * gdr_forward takes no flags, so a tensor-core prefill with a small batch x
+ * heads may take the segmented state scan (GDR_FLAG_NO_SEGMENTS below).  On
+ * that route the call copies its tables from pageable host memory, so it
+ * cannot be captured in a CUDA graph; whether it is taken depends on the
+ * device's SM count; and its results agree with the single walk within the
+ * route's tolerance, not bit for bit.  gdr_forward_ex with
+ * GDR_FLAG_NO_SEGMENTS is the deterministic, capturable alternative.
+ * Passage: as gdr_forward_ex; the argument list is that of the method's
+ * description (q, k, v, g, beta, h0, out, ht, B, T, HK, HV, dk, dv, chunk,
+ * stream) plus the q/k/v dtype.
  */
 GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, const float *g,
                                const float *beta, const float *h0, void *out, float *ht,
@@ -156,6 +173,7 @@ GDR_API gdr_status gdr_forward(const void *q, const void *k, const void *v, cons
                                void *stream, int qkv_dtype);
 
 /*
+ * Passage: none in the pages (memory management of gdr_forward).
  * Registers a caller-owned device workspace for gdr_forward on the current
  * device: from now on gdr_forward uses it instead of allocating, and a call
  * that needs more than `bytes` returns GDR_ERR_WORKSPACE (size it with
@@ -225,7 +243,9 @@ GDR_API gdr_status gdr_forward_chunked_noalloc(const void *q, const void *k, con
  * handed from segment to segment.  Calls from several host threads are
  * serialised while they enqueue.  Errors as gdr_forward_ex
  * (GDR_ERR_WORKSPACE for a short staging buffer); a failure after the first
- * copy leaves the outputs partly written.
+ * copy leaves the outputs partly written, and the call makes `stream` wait
+ * for the copies already queued on the library's streams before it returns
+ * the error, so the host buffers may be reused once `stream` has completed.
  */
 GDR_API size_t gdr_host_staging_bytes(int B, int T, int HK, int HV, int dk, int dv, int chunk,
                                       int qkv_dtype);
@@ -311,6 +331,7 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
                                     size_t workspace_bytes, unsigned flags);
 
 /*
+ * Passage: none in the pages (error reporting of the bounded waits).
  * Waits for `stream`, then reads and clears the library's device error word
  * on the current device.  Returns GDR_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, GDR_ERR_CUDA if the stream reported an
@@ -319,6 +340,7 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
 GDR_API gdr_status gdr_device_check(void *stream);
 
 /*
+ * Passage: none in the pages (measurement support).
  * Launch tracing.  While enabled (process-wide), every kernel launch made by
  * this library is bracketed by two CUDA events recorded on the launching
  * stream.  gdr_trace_read waits for the recorded events, writes per kernel
@@ -330,13 +352,15 @@ GDR_API gdr_status gdr_device_check(void *stream);
 GDR_API gdr_status gdr_trace_enable(int on);
 GDR_API int gdr_trace_read(int max_kernels, const char **names, int *launches, double *total_ms);
 
-/* Human-readable name of a gdr_status value (static string, never NULL). */
+/* Human-readable name of a gdr_status value (static string, never NULL).
+ * Passage: none in the pages. */
 GDR_API const char *gdr_status_string(int status);
 
-/* cudaError_t code of the last CUDA failure seen by this thread (0 if none). */
+/* cudaError_t code of the last CUDA failure seen by this thread (0 if none).
+ * Passage: none in the pages. */
 GDR_API int gdr_last_cuda_error(void);
 
-/* Library version string, e.g. "0.1.0" (static string). */
+/* Library version string, e.g. "0.1.0" (static string).  Passage: none in the pages. */
 GDR_API const char *gdr_version(void);
 
 #ifdef __cplusplus

@@ -4,10 +4,12 @@ array inside the library, for callers that cannot allocate device memory
 must avoid cudaMalloc's synchronisation, a plugin bound to its host's
 allocator).
 
-Its results must match the regular entry point, gdr_forward_ex, running the
-same chunked kernels with a workspace from torch's allocator, within the
-parity tolerance of the other tests.  Two calls in a row with different
-problems check that the shared scratch carries nothing over between calls.
+It runs the same chunked kernels with the same flags as the regular entry
+point, gdr_forward_ex with a workspace from torch's allocator, so its results
+must equal that entry point's bit for bit; both are also checked against the
+fp64 oracle.  The calls run a larger problem, then a smaller one, then the
+larger one again: a stale read of the shared scratch inside the smaller
+problem's footprint would see the larger problem's leftovers, not zeros.
 This file is collected last on purpose.
 """
 import ctypes
@@ -15,6 +17,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE_GENERIC,
                                            gdr_device_check, gdr_forward, load_library)
 from channelwise_gated_delta_gb300.inputs import draw, to_f64
@@ -43,22 +46,23 @@ def noalloc_call(lib, c, chunk):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_regular_entry_point_twice():
+def test_noalloc_matches_regular_entry_point_call_after_call():
     lib = load_library()
-    problems = [
-        (draw(2, 150, 2, 4, 64, 64, dtype=torch.float32, seed=21), 32),
-        (draw(1, 97, 16, 32, 128, 128, dtype=torch.bfloat16, seed=22), 64),
-    ]
+    large = (draw(1, 97, 16, 32, 128, 128, dtype=torch.bfloat16, seed=22), 64)
+    small = (draw(2, 150, 2, 4, 64, 64, dtype=torch.float32, seed=21), 32)
     flags = GDR_FLAG_FORCE_CHUNKED | GDR_FLAG_FORCE_GENERIC
-    for d, chunk in problems:
+    for d, chunk in (large, small, large):
         c = to_cuda(d)
         ref_o, ref_h = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"],
                                    chunk=chunk, flags=flags)
         gdr_device_check()
         out, ht = noalloc_call(lib, c, chunk)
-        dtype = d["q"].dtype
-        assert_close("o (no-alloc vs regular)", out, to_f64(ref_o), dtype)
-        assert_close("ht (no-alloc vs regular)", ht, to_f64(ref_h), dtype)
+        assert torch.equal(out, ref_o), "o differs from the regular entry point"
+        assert torch.equal(ht, ref_h), "ht differs from the regular entry point"
+        ro, rh = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                   to_f64(d["h0"]))
+        assert_close("o (no-alloc vs oracle)", out, ro, d["q"].dtype)
+        assert_close("ht (no-alloc vs oracle)", ht, rh, d["q"].dtype)
 
 
 def test_noalloc_rejects_oversized_problem():
