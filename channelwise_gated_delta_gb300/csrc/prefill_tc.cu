@@ -300,6 +300,123 @@ __device__ __forceinline__ void blk_store(float *xs, const float (&acc)[2][4], i
     }
 }
 
+// ---- exact path: the intra-chunk matrices A and P block by block
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Diagonal blocks about their middle row: every factor within exp(+-60)
+// (log2 units).
+constexpr float kDiagLog2 = 60.f * kLog2e;
+
+// One warp: rows r0 .. r0 + 15 of A and P against nt_n 8-column tiles from
+// column s0, on bf16 m16n8k16 mma.sync over the 128 key channels.  The
+// decay of a pair splits at reference row b,
+//   exp(G_r - G_s) = exp(G_r - G_b) exp(G_b - G_s),
+// the first factor scaling the row operands k_r and q_r and the second the
+// column operand k_s (both <= 1 when s < b <= r).  SCALAR_G: one decay per
+// row, applied to each product instead.  Writes every element of its blocks
+// (zeros above the diagonal and past row L); skip: zeros only.
+template <bool SCALAR_G>
+__device__ __forceinline__ void exact_block(const unsigned char *smem, float *sA, unsigned char *opP,
+                                            int r0, int s0, int nt_n, int b, bool diag, bool skip,
+                                            int L, float br0, float br1, int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+    float acc_a[4][4], acc_p[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc_a[nt][e] = acc_p[nt][e] = 0.f;
+    if (!skip) {
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+            const int chs[2] = {16 * ks + 2 * tq, 16 * ks + 2 * tq + 8};
+            float2 gb[2];
+            if (!SCALAR_G) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    gb[h] = *reinterpret_cast<const float2 *>(smem + kG + g_off(b, chs[h]));
+            }
+            // row operands: register (2 h + i) holds row r0 + gq + 8 i, channels chs[h]
+            uint32_t ak[4], aq[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = r0 + gq + 8 * i;
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(smem + kRawK + kq_off(r, chs[h]));
+                    const uint32_t qw = *reinterpret_cast<const uint32_t *>(smem + kRawQ + kq_off(r, chs[h]));
+                    if (SCALAR_G) {
+                        ak[2 * h + i] = kw;
+                        aq[2 * h + i] = qw;
+                    } else {
+                        const float2 g = *reinterpret_cast<const float2 *>(smem + kG + g_off(r, chs[h]));
+                        const float ex = fast_exp2(g.x - gb[h].x), ey = fast_exp2(g.y - gb[h].y);
+                        const float2 kf = unpack_bf16x2(kw), qf = unpack_bf16x2(qw);
+                        ak[2 * h + i] = pack_bf16x2(kf.x * ex, kf.y * ey);
+                        aq[2 * h + i] = pack_bf16x2(qf.x * ex, qf.y * ey);
+                    }
+                }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                if (nt < nt_n) {
+                    const int s = s0 + 8 * nt + gq;
+                    uint32_t bw[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t kw = *reinterpret_cast<const uint32_t *>(smem + kRawK + kq_off(s, chs[h]));
+                        if (SCALAR_G) {
+                            bw[h] = kw;
+                        } else {
+                            const float2 g = *reinterpret_cast<const float2 *>(smem + kG + g_off(s, chs[h]));
+                            const float2 kf = unpack_bf16x2(kw);
+                            bw[h] = pack_bf16x2(kf.x * fast_exp2(gb[h].x - g.x), kf.y * fast_exp2(gb[h].y - g.y));
+                        }
+                    }
+                    mma_bf16_16816(acc_a[nt], ak, bw[0], bw[1]);
+                    mma_bf16_16816(acc_p[nt], aq, bw[0], bw[1]);
+                }
+            }
+        }
+    }
+    const float *gsv = reinterpret_cast<const float *>(smem + kGsc);
+    const int I = r0 >> 4;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        if (nt >= nt_n) break;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = r0 + gq + 8 * i, s = s0 + 8 * nt + 2 * tq;
+            const float br = i ? br1 : br0;
+            float va[2], vp[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float a = acc_a[nt][2 * i + e], p = acc_p[nt][2 * i + e];
+                if (SCALAR_G && !skip) {
+                    const float f = fast_exp2(gsv[r] - gsv[s + e]);
+                    a *= f;
+                    p *= f;
+                }
+                const bool in = r < L && s + e <= r;
+                va[e] = (in && s + e < r) ? br * a : 0.f;
+                vp[e] = in ? p : 0.f;
+            }
+            if (diag) {
+                sA[diagT_idx(I, (s & 15), r & 15)] = va[0];
+                sA[diagT_idx(I, (s & 15) + 1, r & 15)] = va[1];
+            } else {
+                sA[sq_idx(r, s)] = va[0];
+                sA[sq_idx(r, s + 1)] = va[1];
+            }
+            *reinterpret_cast<uint32_t *>(opP + kmajor_off(r, s, kC)) = pack_bf16x2(vp[0], vp[1]);
+        }
+    }
+}
+
 struct TileMaps {
     CUtensorMap k, q, g, v, o;
 };
@@ -701,63 +818,85 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (slow) {
-                // ---------------- exact path: A (f32, beta-scaled) and P (bf16) from
-                // pairwise decays exp(G_r - G_s) <= 1 on CUDA cores; the solvers
-                // must be done with A, and the output product with P
+                // ---------------- exact path: A (f32, beta-scaled) and P (bf16) block by
+                // block, each decay split about a reference row inside the chunk; the
+                // solvers must be done with A, and the output product with P
                 if (c > 0) {
                     wait(MB_GFREE, c - 1);
                     wait(MB_X, c - 1);
                 }
                 float *sA = reinterpret_cast<float *>(smem + kA32);
-                for (int idx = pt; idx < 64 * 64 / 4; idx += kPrepThreads)
-                    reinterpret_cast<float4 *>(sA)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int idx = pt; idx < 64 * 64 * 2 / 16; idx += kPrepThreads)
-                    reinterpret_cast<uint4 *>(smem + kOpP)[idx] = make_uint4(0, 0, 0, 0);
-                named_sync(kNbPrep, kPrepThreads);
-                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
-                const float *gsv = reinterpret_cast<const float *>(smem + kGsc);
-                // warp pw: rows r = pw, pw + 8, ...; lanes over 4-channel groups
-#pragma unroll 1
-                for (int r = pw; r < L; r += 8) {
-                    const float br = beta[(tok0 + t0 + r) * HV + hv];
-                    float4 gr4;
-                    if (SCALAR_G) {
-                        gr4 = make_float4(gsv[r], gsv[r], gsv[r], gsv[r]);
-                    } else {
-                        gr4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, 4 * lane));
+                int *fallback = reinterpret_cast<int *>(smem + kTot);  // [4] diagonal blocks
+                // P above the diagonal blocks: zero
+                if (pt < 192) {
+                    const int u = pt >> 5, I = u < 3 ? 0 : (u < 5 ? 1 : 2);
+                    const int J = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3);
+                    *reinterpret_cast<uint4 *>(smem + kOpP +
+                                               kmajor_off(16 * I + ((pt & 31) >> 1), 16 * J + 8 * (pt & 1), kC)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                // warp pw: rows 32-47 and 48-63 against columns 0-31 (reference row 32),
+                // rows 16-31 against 0-15 (row 16), rows 48-63 against 32-47 (row 48),
+                // or diagonal block pw - 4 (its middle row)
+                const bool dg = pw >= 4;
+                const int r0 = dg ? 16 * (pw - 4) : (pw == 0 ? 32 : (pw == 2 ? 16 : 48));
+                const int s0 = dg ? r0 : (pw == 3 ? 32 : 0);
+                const int nt_n = pw < 2 ? 4 : 2;
+                int b = dg ? r0 + 8 : (pw < 2 ? 32 : r0);
+                bool skip = r0 >= L;
+                if (dg && !skip) {
+                    b = min(b, L - 1);
+                    if (!SCALAR_G) {
+                        // every factor of the block within range, else pairwise decays
+                        const float4 gb4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(b, 4 * lane));
+                        float dev = 0.f;
+#pragma unroll 4
+                        for (int r = r0; r < min(r0 + 16, L); ++r) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, 4 * lane));
+                            dev = fmaxf(dev, fmaxf(fmaxf(fabsf(g4.x - gb4.x), fabsf(g4.y - gb4.y)),
+                                                   fmaxf(fabsf(g4.z - gb4.z), fabsf(g4.w - gb4.w))));
+                        }
+                        skip = __any_sync(0xffffffffu, !(dev <= kDiagLog2)) != 0;
                     }
-                    const uint2 kr2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(r, 4 * lane));
-                    const uint2 qr2 = *reinterpret_cast<const uint2 *>(smem + kRawQ + kq_off(r, 4 * lane));
-                    const float2 k01 = unpack_bf16x2(kr2.x), k23 = unpack_bf16x2(kr2.y);
-                    const float2 q01 = unpack_bf16x2(qr2.x), q23 = unpack_bf16x2(qr2.y);
+                }
+                if (dg && lane == 0) fallback[pw - 4] = (skip && r0 < L) ? 1 : 0;
+                const size_t brow = tok0 + t0 + r0 + (lane >> 2);
+                const float br0 = r0 + (lane >> 2) < L ? beta[brow * HV + hv] : 0.f;
+                const float br1 = r0 + (lane >> 2) + 8 < L ? beta[(brow + 8) * HV + hv] : 0.f;
+                exact_block<SCALAR_G>(smem, sA, smem + kOpP, r0, s0, nt_n, b, dg, skip, L, br0, br1, lane);
+                named_sync(kNbPrep, kPrepThreads);
+                // diagonal blocks out of range: pairwise decays exp(G_r - G_s) <= 1,
+                // warp pw on rows pw and pw + 8 of the block, lanes over channels
+                __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(smem + kOpP);
 #pragma unroll 1
-                    for (int s = 0; s <= r; ++s) {
-                        float4 gs4;
-                        if (SCALAR_G) {
-                            gs4 = make_float4(gsv[s], gsv[s], gsv[s], gsv[s]);
-                        } else {
-                            gs4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(s, 4 * lane));
-                        }
-                        const uint2 ks2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(s, 4 * lane));
-                        const float2 s01 = unpack_bf16x2(ks2.x), s23 = unpack_bf16x2(ks2.y);
-                        const float e0 = fast_exp2(gr4.x - gs4.x), e1 = fast_exp2(gr4.y - gs4.y);
-                        const float e2 = fast_exp2(gr4.z - gs4.z), e3 = fast_exp2(gr4.w - gs4.w);
-                        const float k0 = s01.x * e0, k1 = s01.y * e1, k2 = s23.x * e2, k3 = s23.y * e3;
-                        float a = k01.x * k0 + k01.y * k1 + k23.x * k2 + k23.y * k3;
-                        float pv = q01.x * k0 + q01.y * k1 + q23.x * k2 + q23.y * k3;
+                for (int I = 0; I < 4; ++I) {
+                    if (!fallback[I]) continue;
+#pragma unroll 1
+                    for (int r = 16 * I + pw; r < min(16 * I + 16, L); r += 8) {
+                        const float br = beta[(tok0 + t0 + r) * HV + hv];
+                        const float4 gr4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(r, 4 * lane));
+                        const uint2 kr2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(r, 4 * lane));
+                        const uint2 qr2 = *reinterpret_cast<const uint2 *>(smem + kRawQ + kq_off(r, 4 * lane));
+                        const float2 k01 = unpack_bf16x2(kr2.x), k23 = unpack_bf16x2(kr2.y);
+                        const float2 q01 = unpack_bf16x2(qr2.x), q23 = unpack_bf16x2(qr2.y);
+#pragma unroll 1
+                        for (int s = 16 * I; s <= r; ++s) {
+                            const float4 gs4 = *reinterpret_cast<const float4 *>(smem + kG + g_off(s, 4 * lane));
+                            const uint2 ks2 = *reinterpret_cast<const uint2 *>(smem + kRawK + kq_off(s, 4 * lane));
+                            const float2 s01 = unpack_bf16x2(ks2.x), s23 = unpack_bf16x2(ks2.y);
+                            const float k0 = s01.x * fast_exp2(gr4.x - gs4.x), k1 = s01.y * fast_exp2(gr4.y - gs4.y);
+                            const float k2 = s23.x * fast_exp2(gr4.z - gs4.z), k3 = s23.y * fast_exp2(gr4.w - gs4.w);
+                            float a = k01.x * k0 + k01.y * k1 + k23.x * k2 + k23.y * k3;
+                            float pv = q01.x * k0 + q01.y * k1 + q23.x * k2 + q23.y * k3;
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            a += __shfl_xor_sync(0xffffffffu, a, o);
-                            pv += __shfl_xor_sync(0xffffffffu, pv, o);
-                        }
-                        if (lane == 0) {
-                            if (s < r) {
-                                if ((r >> 4) == (s >> 4))
-                                    sA[diagT_idx(r >> 4, s & 15, r & 15)] = br * a;
-                                else
-                                    sA[sq_idx(r, s)] = br * a;
+                            for (int o = 16; o > 0; o >>= 1) {
+                                a += __shfl_xor_sync(0xffffffffu, a, o);
+                                pv += __shfl_xor_sync(0xffffffffu, pv, o);
                             }
-                            op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(pv);
+                            if (lane == 0) {
+                                if (s < r) sA[diagT_idx(I, s & 15, r & 15)] = br * a;
+                                op[kmajor_off(r, s, kC) >> 1] = __float2bfloat16_rn(pv);
+                            }
                         }
                     }
                 }

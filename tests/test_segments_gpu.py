@@ -123,3 +123,70 @@ def test_large_batch_is_not_segmented():
     d = draw(4, 1024, 16, 32, 128, 128, dtype=torch.bfloat16, seed=418)
     _, tr = traced(lambda: run_gpu(d, 64))
     assert "gdr_segment_init" not in tr and "gdr_prefill_fused" in tr, tr
+
+
+def mixed_decay(B, T, HK, HV, pattern, seed, scalar_gate=False):
+    """A problem whose 64-row chunks follow `pattern`, one letter per chunk:
+      f  weak decay (about 0.05 nats a step): the fast path;
+      s  strong (about 6 nats a step): the exact path, its diagonal blocks
+         factored about their middle row;
+      x  steep (20 to 30 nats a step): diagonal blocks past the factor
+         range, pairwise decays;
+      c  weak, but one row drops by 100 nats in a few key channels (every
+         channel with a scalar gate): a cliff inside one block."""
+    d = draw(B, T, HK, HV, 128, 128, dtype=torch.bfloat16, seed=seed, g_mu=-3.0,
+             scalar_gate=scalar_gate)
+    gen = torch.Generator().manual_seed(seed + 1)
+    g = d["g"]
+    assert len(pattern) == (T + 63) // 64
+    for c, kind in enumerate(pattern):
+        rows = slice(64 * c, min(64 * c + 64, T))
+        shape = g[:, rows].shape
+        if kind == "s":
+            g[:, rows] = -torch.nn.functional.softplus(torch.randn(shape, generator=gen) * 0.5 + 6.0)
+        elif kind == "x":
+            g[:, rows] = -(20.0 + 10.0 * torch.rand(shape, generator=gen))
+        elif kind == "c":
+            r = min(64 * c + 37, T - 1)
+            if scalar_gate:
+                g[:, r] = -100.0
+            else:
+                g[:, r, :, :5] = -100.0
+        else:
+            assert kind == "f"
+    return d
+
+
+def assert_close_by_chunk(got, ref):
+    """The bf16 bound of each 64-row chunk of o on its own: a chunk of small
+    outputs is not hidden behind another's large ones."""
+    for t0 in range(0, ref.shape[1], 64):
+        assert_close("o rows %d+" % t0, got[:, t0:t0 + 64], ref[:, t0:t0 + 64], torch.bfloat16)
+
+
+MIXED = "fsfxsscfs" "fsxfcsx"  # 16 chunks, the last one 40 rows
+
+
+@pytest.mark.parametrize("segments", [0, 4, 5])
+def test_mixed_fast_and_exact_chunks_across_segments(segments):
+    """Fast and exact-path chunks side by side, at segment starts and ends
+    (4 segments: chunks 0-3 | 4-7 | 8-11 | 12-15; 5: a boundary inside the
+    run of exact chunks), including a ragged exact last chunk; 0 = one
+    unsegmented walk."""
+    d = mixed_decay(2, 1000, 2, 4, MIXED, seed=430 + segments)
+    ref_o, ref_h = run_oracle(d)
+    flags = gdr_flag_segments(segments) if segments else GDR_FLAG_NO_SEGMENTS
+    (out, ht), tr = traced(lambda: run_gpu(d, 64, flags=flags))
+    assert_close_by_chunk(out, ref_o)
+    assert_close("ht", ht, ref_h, torch.bfloat16)
+    assert ("gdr_segment_init" in tr) == bool(segments), tr
+
+
+def test_mixed_chunks_scalar_gate():
+    d = mixed_decay(1, 1000, 2, 4, MIXED, seed=440, scalar_gate=True)
+    args = [to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")]
+    ref_o, ref_h = oracle.scalar_gate_recurrence(*args, to_f64(d["h0"]))
+    for flags in (GDR_FLAG_NO_SEGMENTS, gdr_flag_segments(4)):
+        out, ht = run_gpu(d, 64, flags=flags)
+        assert_close_by_chunk(out, ref_o)
+        assert_close("ht", ht, ref_h, torch.bfloat16)
