@@ -21,6 +21,7 @@ GDR_FLAG_FORCE_CHUNKED = 1
 GDR_FLAG_FORCE_GENERIC = 2
 GDR_FLAG_SCALAR_GATE = 4
 GDR_FLAG_NO_SEGMENTS = 8
+GDR_FLAG_TREE_BLOCKED = 0x10000
 
 
 def gdr_flag_segments(n):
@@ -291,7 +292,7 @@ def gdr_tree_workspace_bytes(B, T, HK, HV, dk, dv, dtype=torch.bfloat16, flags=0
 
 def gdr_forward_tree(q, k, v, g, beta, parent, h0=None, out=None, stream=None, workspace=None,
                      flags=0):
-    """Tree verification: each batch element's T <= 64 tokens form a draft
+    """Tree verification: each batch element's T <= 512 tokens form a draft
     tree given by ``parent`` (host ints [B, T], parent[b, t] in [-1, t-1]);
     every token's output is that of the recurrence run along its root path
     from h0[b].  Tensors as in gdr_forward.  Returns out [B, T, HV, dv]."""
@@ -407,7 +408,7 @@ def gdr_trace_read():
     """Waits for the traced launches and returns {kernel name: (launches, total ms)}
     for every kernel kind launched since tracing was enabled (records are cleared)."""
     lib = load_library()
-    n = 8
+    n = 32
     names = (ctypes.c_char_p * n)()
     launches = (ctypes.c_int * n)()
     total = (ctypes.c_double * n)()

@@ -312,7 +312,8 @@ cudaEvent_t take_event() {
 const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_prep",
                                               "gdr_chunk_scan",    "gdr_prefill_fused",
                                               "gdr_segment_init",  "gdr_segment_combine",
-                                              "gdr_tree_tc"};
+                                              "gdr_tree_tc", "gdr_tree_path_kernel",
+                                              "gdr_tree_blocked_kernel"};
 
 }  // namespace
 
@@ -346,6 +347,7 @@ namespace {
 // Trees run as one chunk of the CUDA-core kernels: the smallest supported
 // chunk that holds T tokens (0 when T is too large).
 int tree_chunk(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 0; }
+constexpr int kTreeMaxTokens = 512;
 
 bool tree_on_tensor_cores(const gdr::Problem &p, unsigned flags) {
     gdr::Problem c = p;
@@ -354,10 +356,23 @@ bool tree_on_tensor_cores(const gdr::Problem &p, unsigned flags) {
            !(flags & GDR_FLAG_SCALAR_GATE);
 }
 
-// Workspace: the parents, then (CUDA-core route) the per-tree records.
+// Trees past one chunk, or any with GDR_FLAG_TREE_BLOCKED, take the blocked
+// solve.
+bool tree_blocked(const gdr::Problem &p, unsigned flags) {
+    return p.T > 64 || (flags & GDR_FLAG_TREE_BLOCKED);
+}
+// The Problem of a tree call: the chunk of the one-chunk routes (64 on the
+// blocked route, where it plays no part).
+int tree_problem_chunk(int T, unsigned flags) {
+    return (T > 64 || (flags & GDR_FLAG_TREE_BLOCKED)) ? 64 : tree_chunk(T > 0 ? T : 1);
+}
+
+// Workspace: the parents, then the route's own: the per-tree records (CUDA-core
+// route) or the ancestor masks and path sums (blocked route).
 size_t tree_layout(const gdr::Problem &p, unsigned flags, size_t *record_off) {
     const size_t table = align256((size_t)p.B * p.T * sizeof(int));
     *record_off = table;
+    if (tree_blocked(p, flags)) return table + gdr::tree_blocked_workspace_bytes(p);
     return table + (tree_on_tensor_cores(p, flags) ? 0 : gdr::generic_tree_record_bytes(p));
 }
 }  // namespace
@@ -585,11 +600,11 @@ GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, in
                                         int qkv_dtype, unsigned flags) {
     if (B < 0 || T < 0 || HK <= 0 || HV <= 0 || HV % HK != 0) return 0;
     if (qkv_dtype != GDR_F32 && qkv_dtype != GDR_BF16) return 0;
-    if (!supported_dim(dk) || !supported_dim(dv) || !tree_chunk(T)) return 0;
+    if (!supported_dim(dk) || !supported_dim(dv) || T > kTreeMaxTokens) return 0;
     if ((long long)B * T == 0) return 0;
     const gdr::Problem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                         B, T, HK, HV, dk, dv, tree_chunk(T), qkv_dtype == GDR_BF16 ? 1 : 0,
-                         (flags & GDR_FLAG_SCALAR_GATE) ? 1 : 0};
+                         B, T, HK, HV, dk, dv, tree_problem_chunk(T, flags),
+                         qkv_dtype == GDR_BF16 ? 1 : 0, (flags & GDR_FLAG_SCALAR_GATE) ? 1 : 0};
     size_t off = 0;
     return tree_layout(p, flags, &off);
 }
@@ -600,8 +615,8 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
                                     int dv, void *stream, int qkv_dtype, void *workspace,
                                     size_t workspace_bytes, unsigned flags) {
     if (B < 0 || T < 0) return GDR_ERR_SHAPE;
-    if (T > 64) return GDR_ERR_UNSUPPORTED;
-    const int chunk = tree_chunk(T > 0 ? T : 1);
+    if (T > kTreeMaxTokens) return GDR_ERR_UNSUPPORTED;
+    const int chunk = tree_problem_chunk(T, flags);
     gdr::Problem p;
     gdr_status st = validate(q, k, v, g, beta, h0, out, nullptr, B, T, HK, HV, dk, dv, chunk,
                              qkv_dtype, &p, flags);
@@ -623,7 +638,10 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
                                     cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
     const int *par_dev = reinterpret_cast<const int *>(ws);
-    if (tree_on_tensor_cores(p, flags)) {
+    if (tree_blocked(p, flags)) {
+        if (!gdr::tree_blocked_supported(p)) return GDR_ERR_UNSUPPORTED;
+        e = gdr::launch_tree_blocked(p, ws + record_off, par_dev, s);
+    } else if (tree_on_tensor_cores(p, flags)) {
         int *err = nullptr;
         e = gdr::device_error_word(&err);
         if (e == cudaSuccess) {

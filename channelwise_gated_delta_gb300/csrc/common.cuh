@@ -70,7 +70,9 @@ enum KernelId {
     kKernSegInit = 4,
     kKernSegCombine = 5,
     kKernTree = 6,
-    kNumKernels = 7
+    kKernTreePath = 7,
+    kKernTreeBlocked = 8,
+    kNumKernels = 9
 };
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);
@@ -125,6 +127,13 @@ size_t generic_tree_record_bytes(const Problem &p);
 cudaError_t launch_tc_tree(const Problem &p, const int *parents, int *dev_error,
                            cudaStream_t stream);
 cudaError_t launch_generic_tree(const Problem &p, void *records, const int *parents,
+                                cudaStream_t stream);
+// Tree verification of up to 512 tokens as one blocked unit-lower solve
+// (tree_blocked.cu): parents [B][T] on the device, workspace
+// tree_blocked_workspace_bytes(p), 256-byte aligned.
+bool tree_blocked_supported(const Problem &p);
+size_t tree_blocked_workspace_bytes(const Problem &p);
+cudaError_t launch_tree_blocked(const Problem &p, void *workspace, const int *parents,
                                 cudaStream_t stream);
 
 // Chunk-parallel state scan on the tensor-core route (segments.cu): the

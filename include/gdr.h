@@ -122,6 +122,9 @@ typedef enum gdr_dtype {
  */
 #define GDR_FLAG_NO_SEGMENTS 8u
 #define GDR_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)
+/* gdr_forward_tree: take the blocked solve (the route of trees past 64
+ * tokens) at any T. */
+#define GDR_FLAG_TREE_BLOCKED 0x10000u
 
 /*
  * Bytes of device workspace gdr_forward_ex needs for this call (0 when the
@@ -306,21 +309,25 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
  *   parent  HOST int32 [B][T]: parent[b][t] in [-1, t-1] (parents precede
  *           their children; -1: the token follows h0 directly).  Read during
  *           the call only.
- *   q, k, v, g, beta, h0, out: layouts as in gdr_forward, T <= 64.
+ *   q, k, v, g, beta, h0, out: layouts as in gdr_forward, T <= 512.
  *
  * There is no final-state output: a tree has one state per leaf.  To commit
  * an accepted path, run gdr_forward (or gdr_forward_varlen) on its tokens
- * from the same h0.  The whole tree is one chunk of the chunked prefill: path
- * prefix sums of g and the ancestor relation in place of the causal order.
- * bf16 q/k/v with dk = dv = 128 run on the tensor-core prefill kernel (one
- * launch), everything else -- or any call with GDR_FLAG_FORCE_GENERIC in
- * `flags` -- on the CUDA-core chunk kernels (two launches, float32
- * throughout).  `workspace`: device memory of gdr_tree_workspace_bytes(...)
- * bytes (same flags), 256-byte aligned, untouched until the stream has
- * passed the call.  Also enqueues one host-to-device copy of the parents
- * (pageable: the call returns once they have been taken).  Errors:
- * GDR_ERR_UNSUPPORTED for T > 64, GDR_ERR_SHAPE for a parent outside
- * [-1, t-1], the rest as gdr_forward_ex.  B == 0 or T == 0 does nothing.
+ * from the same h0.  A tree is one unit-lower system over its tokens: path
+ * prefix sums of g, and the ancestor relation in place of the causal order.
+ * Routes: T <= 64 with bf16 q/k/v and dk = dv = 128 runs as one chunk of the
+ * tensor-core prefill kernel (one launch); other T <= 64 calls, or any with
+ * GDR_FLAG_FORCE_GENERIC, as one chunk of the CUDA-core kernels (two
+ * launches, float32 throughout); T > 64, or any call with
+ * GDR_FLAG_TREE_BLOCKED, on the blocked solve (two launches: path sums and
+ * ancestor masks, then one CTA per tree, value head and dv part walking the
+ * 16-token blocks on bf16 mma.sync -- bf16 pairs hi + lo for f32 q/k/v).
+ * `workspace`: device memory of gdr_tree_workspace_bytes(...) bytes (same
+ * flags), 256-byte aligned, untouched until the stream has passed the call.
+ * Also enqueues one host-to-device copy of the parents (pageable: the call
+ * returns once they have been taken).  Errors: GDR_ERR_UNSUPPORTED for
+ * T > 512, GDR_ERR_SHAPE for a parent outside [-1, t-1], the rest as
+ * gdr_forward_ex.  B == 0 or T == 0 does nothing.
  */
 GDR_API size_t gdr_tree_workspace_bytes(int B, int T, int HK, int HV, int dk, int dv,
                                         int qkv_dtype, unsigned flags);

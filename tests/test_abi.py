@@ -221,7 +221,7 @@ def call_tree(lib, parent, B=1, T=4, HK=1, HV=2, dk=32, dv=32, dtype=0, ws=None,
 
 
 @pytest.mark.parametrize("parent,kw,status", [
-    ([-1, 0, 0, 1], dict(T=65), 3),         # more than 64 tokens
+    ([-1, 0, 0, 1], dict(T=513), 3),        # more than 512 tokens
     ([-1, 0, 3, 1], {}, 2),                  # parent after its child
     ([-1, -2, 0, 1], {}, 2),                 # parent below -1
     (None, {}, 1),                           # no parents
@@ -234,7 +234,13 @@ def test_tree_bad_arguments_rejected_before_launch(lib, parent, kw, status):
 
 def test_tree_workspace_sizes(lib):
     assert lib.gdr_tree_workspace_bytes(1, 0, 1, 2, 32, 32, 0, 0) == 0
-    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0, 0) == 0
+    assert lib.gdr_tree_workspace_bytes(1, 513, 1, 2, 32, 32, 0, 0) == 0
+    # past 64 tokens (or forced): the blocked solve, parents + ancestor masks + path sums
+    Tp = 96
+    blocked = 512 + 256 * ((Tp * (Tp // 32) * 4 + 255) // 256) + 256 * ((2 * Tp * 32 * 4 + 255) // 256)
+    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0, 0) == blocked
+    assert lib.gdr_tree_workspace_bytes(1, 64, 1, 2, 32, 32, 0, 0x10000) > 0
+    assert lib.gdr_tree_workspace_bytes(1, 512, 1, 2, 32, 32, 0, 0) > blocked
     small = lib.gdr_tree_workspace_bytes(1, 16, 1, 2, 32, 32, 0, 0)
     assert 0 < small < lib.gdr_tree_workspace_bytes(1, 17, 1, 2, 32, 32, 0, 0)
     # tensor-core route (bf16, d = 128): the parents only
