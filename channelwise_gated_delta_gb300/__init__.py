@@ -5,6 +5,7 @@ thin Python binding plus the seeded synthetic input generator.
 """
 from ._binding import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE_GENERIC,
                        GDR_FLAG_NO_SEGMENTS, GDR_FLAG_SCALAR_GATE, GDR_FLAG_TREE_BLOCKED,
+                       GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD,
                        gdr_flag_segments,
                        GdrError, gdr_device_check, gdr_forward, gdr_forward_host,
                        gdr_forward_tree, gdr_host_staging_bytes,
@@ -20,5 +21,5 @@ __all__ = ["gdr_forward", "gdr_workspace_bytes", "gdr_forward_varlen", "gdr_varl
            "gdr_trace_enable", "gdr_trace_read",
            "load_library", "GdrError", "GDR_F32", "GDR_BF16", "GDR_FLAG_FORCE_CHUNKED",
            "GDR_FLAG_FORCE_GENERIC", "GDR_FLAG_SCALAR_GATE", "GDR_FLAG_NO_SEGMENTS",
-           "GDR_FLAG_TREE_BLOCKED",
+           "GDR_FLAG_TREE_BLOCKED", "GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD",
            "gdr_flag_segments"]

@@ -22,6 +22,7 @@ GDR_FLAG_FORCE_GENERIC = 2
 GDR_FLAG_SCALAR_GATE = 4
 GDR_FLAG_NO_SEGMENTS = 8
 GDR_FLAG_TREE_BLOCKED = 0x10000
+GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD = 0x20000
 
 
 def gdr_flag_segments(n):

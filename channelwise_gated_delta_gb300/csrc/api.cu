@@ -312,8 +312,8 @@ cudaEvent_t take_event() {
 const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_prep",
                                               "gdr_chunk_scan",    "gdr_prefill_fused",
                                               "gdr_segment_init",  "gdr_segment_combine",
-                                              "gdr_tree_tc", "gdr_tree_path_kernel",
-                                              "gdr_tree_blocked_kernel"};
+                                              "gdr_tree_tc",       "gdr_tree_path_kernel",
+                                              "gdr_tree_gram_kernel", "gdr_tree_solve_kernel"};
 
 }  // namespace
 
@@ -640,7 +640,9 @@ GDR_API gdr_status gdr_forward_tree(const void *q, const void *k, const void *v,
     const int *par_dev = reinterpret_cast<const int *>(ws);
     if (tree_blocked(p, flags)) {
         if (!gdr::tree_blocked_supported(p)) return GDR_ERR_UNSUPPORTED;
-        e = gdr::launch_tree_blocked(p, ws + record_off, par_dev, s);
+        e = gdr::launch_tree_blocked(
+            p, ws + record_off, par_dev,
+            (flags & GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD) ? gdr::kTreeGramPerValueHead : 0u, s);
     } else if (tree_on_tensor_cores(p, flags)) {
         int *err = nullptr;
         e = gdr::device_error_word(&err);

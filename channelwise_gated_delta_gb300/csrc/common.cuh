@@ -71,8 +71,9 @@ enum KernelId {
     kKernSegCombine = 5,
     kKernTree = 6,
     kKernTreePath = 7,
-    kKernTreeBlocked = 8,
-    kNumKernels = 9
+    kKernTreeGram = 8,
+    kKernTreeSolve = 9,
+    kNumKernels = 10
 };
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);
@@ -130,11 +131,14 @@ cudaError_t launch_generic_tree(const Problem &p, void *records, const int *pare
                                 cudaStream_t stream);
 // Tree verification of up to 512 tokens as one blocked unit-lower solve
 // (tree_blocked.cu): parents [B][T] on the device, workspace
-// tree_blocked_workspace_bytes(p), 256-byte aligned.
+// tree_blocked_workspace_bytes(p), 256-byte aligned.  variant:
+// kTreeGramPerValueHead keeps a scalar gate's gram per value head (the
+// fused form) instead of once per key head.
+constexpr unsigned kTreeGramPerValueHead = 1u;
 bool tree_blocked_supported(const Problem &p);
 size_t tree_blocked_workspace_bytes(const Problem &p);
 cudaError_t launch_tree_blocked(const Problem &p, void *workspace, const int *parents,
-                                cudaStream_t stream);
+                                unsigned variant, cudaStream_t stream);
 
 // Chunk-parallel state scan on the tensor-core route (segments.cu): the
 // segment count chosen for `p` (0: not segmented) under `flags`, its

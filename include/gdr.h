@@ -125,6 +125,10 @@ typedef enum gdr_dtype {
 /* gdr_forward_tree: take the blocked solve (the route of trees past 64
  * tokens) at any T. */
 #define GDR_FLAG_TREE_BLOCKED 0x10000u
+/* gdr_forward_tree, blocked solve, scalar gate: build the gram once per value
+ * head (the fused form) instead of once per key head and share it across the
+ * key head's value heads (the default); for comparing the two. */
+#define GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD 0x20000u
 
 /*
  * Bytes of device workspace gdr_forward_ex needs for this call (0 when the
@@ -319,9 +323,13 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
  * tensor-core prefill kernel (one launch); other T <= 64 calls, or any with
  * GDR_FLAG_FORCE_GENERIC, as one chunk of the CUDA-core kernels (two
  * launches, float32 throughout); T > 64, or any call with
- * GDR_FLAG_TREE_BLOCKED, on the blocked solve (two launches: path sums and
- * ancestor masks, then one CTA per tree, value head and dv part walking the
- * 16-token blocks on bf16 mma.sync -- bf16 pairs hi + lo for f32 q/k/v).
+ * GDR_FLAG_TREE_BLOCKED, on the blocked solve (four launches: ancestor
+ * masks, path sums of g, the ancestor-masked grams of every 16 x 16 block
+ * pair in parallel, then one CTA per tree, value head and dv part
+ * substituting through the blocks in order; bf16 mma.sync, bf16 pairs
+ * hi + lo for f32 q/k/v).  With a scalar gate the gram is built once per key
+ * head and shared by its value heads (GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD:
+ * once per value head).
  * `workspace`: device memory of gdr_tree_workspace_bytes(...) bytes (same
  * flags), 256-byte aligned, untouched until the stream has passed the call.
  * Also enqueues one host-to-device copy of the parents (pageable: the call

@@ -235,12 +235,27 @@ def test_tree_bad_arguments_rejected_before_launch(lib, parent, kw, status):
 def test_tree_workspace_sizes(lib):
     assert lib.gdr_tree_workspace_bytes(1, 0, 1, 2, 32, 32, 0, 0) == 0
     assert lib.gdr_tree_workspace_bytes(1, 513, 1, 2, 32, 32, 0, 0) == 0
-    # past 64 tokens (or forced): the blocked solve, parents + ancestor masks + path sums
-    Tp = 96
-    blocked = 512 + 256 * ((Tp * (Tp // 32) * 4 + 255) // 256) + 256 * ((2 * Tp * 32 * 4 + 255) // 256)
-    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0, 0) == blocked
-    assert lib.gdr_tree_workspace_bytes(1, 64, 1, 2, 32, 32, 0, 0x10000) > 0
-    assert lib.gdr_tree_workspace_bytes(1, 512, 1, 2, 32, 32, 0, 0) > blocked
+    # past 64 tokens (or forced): the blocked solve -- parents, ancestor masks,
+    # path sums, block references, spread flags and column operands
+    # (channelwise gates), the block-pair fragments (bf16 pairs hi + lo for
+    # f32), their flags and the f32 diagonal blocks
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    def blocked(B, T, HV, dk, m, scalar=False):
+        Tp = 32 if T <= 32 else (T + 31) // 32 * 32
+        NB = (T + 15) // 16
+        NTRI = NB * (NB + 1) // 2
+        trees = B * HV
+        refs = 0 if scalar else (up(trees * NB * dk * 4) + up(trees * NB * (dk // 8) * 4)
+                                 + up(trees * Tp * (dk // 2) * m * 4))
+        return (up(B * T * 4) + up(B * Tp * (Tp // 32) * 4) + up(trees * Tp * (1 if scalar else dk) * 4)
+                + refs + up(trees * NTRI * 2 * m * 128 * 4) + up(trees * NTRI * 4)
+                + up(trees * NB * 256 * 4))
+    assert lib.gdr_tree_workspace_bytes(1, 65, 1, 2, 32, 32, 0, 0) == blocked(1, 65, 2, 32, 2)
+    assert lib.gdr_tree_workspace_bytes(3, 512, 2, 4, 128, 64, 1, 0) == blocked(3, 512, 4, 128, 1)
+    assert lib.gdr_tree_workspace_bytes(2, 64, 1, 2, 128, 128, 1, 0x10000) == blocked(2, 64, 2, 128, 1)
+    assert lib.gdr_tree_workspace_bytes(2, 300, 1, 2, 64, 64, 1, 4) == blocked(2, 300, 2, 64, 1, True)
     small = lib.gdr_tree_workspace_bytes(1, 16, 1, 2, 32, 32, 0, 0)
     assert 0 < small < lib.gdr_tree_workspace_bytes(1, 17, 1, 2, 32, 32, 0, 0)
     # tensor-core route (bf16, d = 128): the parents only

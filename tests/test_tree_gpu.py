@@ -6,7 +6,9 @@ import torch
 
 import oracle
 from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_CHUNKED, GDR_FLAG_FORCE_GENERIC,
-                                           GDR_FLAG_TREE_BLOCKED, GdrError, gdr_device_check,
+                                           GDR_FLAG_TREE_BLOCKED,
+                                           GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD, GdrError,
+                                           gdr_device_check,
                                            gdr_forward, gdr_forward_tree, gdr_trace_enable,
                                            gdr_trace_read)
 from channelwise_gated_delta_gb300.inputs import draw, draw_parents, to_f64
@@ -147,7 +149,7 @@ def check_blocked(d, kind, seed, flags=0, branching=3):
         tr = gdr_trace_read()
     finally:
         gdr_trace_enable(False)
-    assert "gdr_tree_blocked_kernel" in tr, tr
+    assert "gdr_tree_solve_kernel" in tr and "gdr_tree_gram_kernel" in tr, tr
     assert_close("o", out, oracle_tree(d, par, kind), d["q"].dtype)
     return out
 
@@ -172,8 +174,13 @@ def test_blocked_tree_f32_full_size():
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("kind", ["random", "chain"])
 def test_blocked_tree_scalar_gate(dtype, kind):
+    """The gram once per key head, shared by its two value heads (the
+    default), and once per value head: both at the oracle's bound, and the
+    same up to the order of float additions."""
     d = draw(2, 300, 2, 4, 128, 128, dtype=dtype, seed=220, scalar_gate=True)
-    check_blocked(d, kind, 220)
+    per_kh = check_blocked(d, kind, 220)
+    per_hv = check_blocked(d, kind, 220, flags=GDR_FLAG_TREE_GRAM_PER_VALUE_HEAD)
+    assert torch.equal(per_kh, per_hv)
 
 
 def test_blocked_tree_no_initial_state_grouped_heads():
