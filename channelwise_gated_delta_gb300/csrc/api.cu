@@ -169,7 +169,8 @@ gdr_status run(const gdr::Problem &p, Route r, unsigned flags, void *ws, cudaStr
             e = gdr::launch_decode(p, stream);
             break;
         case Route::GenericPrefill:
-            e = gdr::launch_generic_prefill(p, ws, stream);
+            e = gdr::launch_generic_prefill(
+                p, ws, stream, !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p));
             break;
         case Route::TensorCorePrefill: {
             int *err = nullptr;
@@ -313,7 +314,8 @@ const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_pr
                                               "gdr_chunk_scan",    "gdr_prefill_fused",
                                               "gdr_segment_init",  "gdr_segment_combine",
                                               "gdr_tree_tc",       "gdr_tree_path_kernel",
-                                              "gdr_tree_gram_kernel", "gdr_tree_solve_kernel"};
+                                              "gdr_tree_gram_kernel", "gdr_tree_solve_kernel",
+                                              "gdr_chunk_scan_tc"};
 
 }  // namespace
 
@@ -590,7 +592,8 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
         p.B = (int)plan.gen_seqs.size();
         e = gdr::launch_generic_prefill_varlen(
             p, ws + plan.record_off, reinterpret_cast<const int2 *>(ws + plan.off_chunks),
-            (int)plan.chunks.size(), reinterpret_cast<const int4 *>(ws + plan.off_gen), s);
+            (int)plan.chunks.size(), reinterpret_cast<const int4 *>(ws + plan.off_gen), s,
+            !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p));
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return GDR_OK;

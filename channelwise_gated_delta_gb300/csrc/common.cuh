@@ -73,7 +73,8 @@ enum KernelId {
     kKernTreePath = 7,
     kKernTreeGram = 8,
     kKernTreeSolve = 9,
-    kNumKernels = 10
+    kKernChunkScanTc = 10,
+    kNumKernels = 11
 };
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);
@@ -97,7 +98,10 @@ cudaError_t device_error_word(int **out);
 int record_cuda_error(cudaError_t e);
 cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream);
 size_t generic_prefill_workspace_bytes(const Problem &p);
-cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream);
+// tc_scan: the state scan on the tensor cores (launch_chunk_scan_tc) rather
+// than on CUDA cores; the prep writes its records for it.
+cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream,
+                                   bool tc_scan = false);
 
 // Packed variable-length batches (p.B = number of entries in the table, the
 // pointers those of the packed tensors).
@@ -119,7 +123,14 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
 // of its first chunk}; records: generic_varlen_record_bytes(p, nchunks).
 size_t generic_varlen_record_bytes(const Problem &p, long long nchunks);
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
-                                          int nchunks, const int4 *seqs, cudaStream_t stream);
+                                          int nchunks, const int4 *seqs, cudaStream_t stream,
+                                          bool tc_scan = false);
+// The state scan of the chunked prefill on the tensor cores (scan_tc.cu):
+// records in the tensor-core layout written by the prep kernel, rec_floats
+// floats each; dense batches (seqs == nullptr) or nseq packed sequences.
+bool scan_tc_supported(const Problem &p);
+cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t rec_floats,
+                                 const int4 *seqs, int nseq, cudaStream_t stream);
 // Tree verification on CUDA cores: p.B trees of p.T <= p.chunk tokens each,
 // parents [B][T] (device); records: generic_tree_record_bytes(p).
 size_t generic_tree_record_bytes(const Problem &p);

@@ -30,6 +30,7 @@
 //                   sequential over chunks: U, O and the state carry, with
 //                   the state tile resident in shared memory.
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace gdr {
 namespace {
@@ -155,7 +156,12 @@ __device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], const float *A, i
 // prefix sums run along root paths and the ancestor relation replaces the
 // causal order in A and P (page "Support TreeUpdateSolve kernel",
 // trymirai/uzu PR #576).  No state carry is prepared.
-template <typename Tin, bool TREE>
+// TCREC: the record's Wk, Qt, Kh and P as the tensor-core scan reads them
+// (scan_tc.cu): each f32 region of n values holds n bf16 "hi" values, then n
+// bf16 "lo" values (x - hi, rounded), in the K-major core-matrix order of a
+// [rows][k] tile (8 rows x 8 k per 128-byte core matrix); same offsets and
+// size as the f32 record.
+template <typename Tin, bool TREE, bool TCREC>
 __global__ void __launch_bounds__(kPrepThreads)
     gdr_chunk_prep(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ g,
@@ -442,16 +448,53 @@ __global__ void __launch_bounds__(kPrepThreads)
     // (a tree has no last token to carry the state to: no Kh, gam).  On the
     // factored path Qs holds Lq and Ks holds R: Qt = Lq exp(G_m) and
     // Kh = R exp(G_L - G_m).
+    // a value into a TC-layout region of a [rows][kext] tile: hi, then lo
+    auto put_tc = [&](size_t region, int row, int kk, int kext, int rows, float x) {
+        __nv_bfloat16 *base = reinterpret_cast<__nv_bfloat16 *>(rec + region);
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const uint32_t o = sm100::kmajor_off(row, kk, kext) / 2;
+        base[o] = h;
+        base[(size_t)rows * kext + o] = __float2bfloat16_rn(x - __bfloat162float(h));
+    };
     for (int idx = tid; idx < C * dk; idx += kPrepThreads) {
         const int r = idx / dk, i = idx % dk;
-        rec[lay.wk() + idx] = Ws[r * ldw + i];
+        float qt, kh = 0.f;
         if (fast) {
-            rec[lay.qt() + idx] = Qs[r * ldk + i] * egm[i];
-            if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * clv[i] : 0.f;
+            qt = Qs[r * ldk + i] * egm[i];
+            if (!TREE) kh = r < L ? Ks[r * ldk + i] * clv[i] : 0.f;
         } else {
             const float gri = Gs[r * ldk + i];
-            rec[lay.qt() + idx] = Qs[r * ldk + i] * expf(gri);
-            if (!TREE) rec[lay.kh() + idx] = r < L ? Ks[r * ldk + i] * expf(glv[i] - gri) : 0.f;
+            qt = Qs[r * ldk + i] * expf(gri);
+            if (!TREE) kh = r < L ? Ks[r * ldk + i] * expf(glv[i] - gri) : 0.f;
+        }
+        if (TCREC) {
+            put_tc(lay.wk(), r, i, dk, C, Ws[r * ldw + i]);
+            put_tc(lay.qt(), r, i, dk, C, qt);
+            put_tc(lay.kh(), r, i, dk, C, kh);
+        } else {
+            rec[lay.wk() + idx] = Ws[r * ldw + i];
+            rec[lay.qt() + idx] = qt;
+            if (!TREE) rec[lay.kh() + idx] = kh;
+        }
+    }
+    if (TCREC) {
+        // P, written above as f32 rows up to each row tile's diagonal block,
+        // into the same region in TC layout with zeros above the diagonal
+        // (the tensor-core products run over every column): every thread
+        // holds its values before any is overwritten
+        constexpr int kMaxPer = 64 * 64 / kPrepThreads;
+        float pv[kMaxPer];
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kMaxPer; ++m) {
+            const int idx = tid + kPrepThreads * m;
+            pv[m] = (idx < C * C && idx % C <= idx / C) ? Pg[idx] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kMaxPer; ++m) {
+            const int idx = tid + kPrepThreads * m;
+            if (idx < C * C) put_tc(lay.p(), idx / C, idx % C, C, C, pv[m]);
         }
     }
     for (int idx = tid; idx < C * dv / 4; idx += kPrepThreads) {
@@ -645,7 +688,7 @@ size_t scan_smem_bytes(int dk, int C) {
 // Dense batches: chunks == seqs == nullptr, B x T from p.  Packed batches:
 // nchunks chunk records and p.B sequence records.  Trees (TREE): p.T <=
 // p.chunk tokens per batch element, parents [B][T] on the device.
-template <typename Tin, bool TREE>
+template <typename Tin, bool TREE, bool TCREC = false>
 cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chunks, int nchunks,
                              const int4 *seqs, const int *parents, cudaStream_t stream) {
     const int C = p.chunk;
@@ -657,20 +700,24 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chun
     const size_t sp = prep_smem_bytes(p.dk, p.dv, C);
     const size_t ss = scan_smem_bytes(p.dk, C);
     cudaError_t e;
-    e = cudaFuncSetAttribute(gdr_chunk_prep<Tin, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sp);
+    e = cudaFuncSetAttribute(gdr_chunk_prep<Tin, TREE, TCREC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(gdr_chunk_scan<Tin, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ss);
     if (e != cudaSuccess) return e;
     trace_begin(kKernChunkPrep, stream);
-    gdr_chunk_prep<Tin, TREE><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
+    gdr_chunk_prep<Tin, TREE, TCREC><<<(unsigned)prep_blocks, kPrepThreads, sp, stream>>>(
         static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
         static_cast<const Tin *>(p.v), p.g, p.beta, ws, chunks, parents, p.T, p.HK, p.HV, p.dk,
         p.dv, C, NC, p.g_scalar);
     trace_end(kKernChunkPrep, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (TCREC) {
+        const ChunkLayout lay{C, p.dk, p.dv};
+        return launch_chunk_scan_tc(p, ws, lay.floats(), seqs, p.B, stream);
+    }
     trace_begin(kKernChunkScan, stream);
     gdr_chunk_scan<Tin, TREE><<<(unsigned)scan_blocks, kScanThreads, ss, stream>>>(
         ws, p.h0, static_cast<Tin *>(p.out), p.ht, seqs, p.T, p.HV, p.dk, p.dv, C, NC);
@@ -686,7 +733,13 @@ size_t generic_prefill_workspace_bytes(const Problem &p) {
     return sizeof(float) * lay.floats() * (size_t)p.B * p.HV * NC;
 }
 
-cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream) {
+cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream,
+                                   bool tc_scan) {
+    if (tc_scan)
+        return p.bf16 ? launch_generic_t<__nv_bfloat16, false, true>(p, workspace, nullptr, 0,
+                                                                     nullptr, nullptr, stream)
+                      : launch_generic_t<float, false, true>(p, workspace, nullptr, 0, nullptr,
+                                                             nullptr, stream);
     return p.bf16 ? launch_generic_t<__nv_bfloat16, false>(p, workspace, nullptr, 0, nullptr,
                                                            nullptr, stream)
                   : launch_generic_t<float, false>(p, workspace, nullptr, 0, nullptr, nullptr,
@@ -699,7 +752,13 @@ size_t generic_varlen_record_bytes(const Problem &p, long long nchunks) {
 }
 
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
-                                          int nchunks, const int4 *seqs, cudaStream_t stream) {
+                                          int nchunks, const int4 *seqs, cudaStream_t stream,
+                                          bool tc_scan) {
+    if (tc_scan)
+        return p.bf16 ? launch_generic_t<__nv_bfloat16, false, true>(p, records, chunks, nchunks,
+                                                                     seqs, nullptr, stream)
+                      : launch_generic_t<float, false, true>(p, records, chunks, nchunks, seqs,
+                                                             nullptr, stream);
     return p.bf16 ? launch_generic_t<__nv_bfloat16, false>(p, records, chunks, nchunks, seqs,
                                                            nullptr, stream)
                   : launch_generic_t<float, false>(p, records, chunks, nchunks, seqs, nullptr,
