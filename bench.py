@@ -45,8 +45,9 @@ NCU_TRAFFIC = {
     # decode B64: one launch of the persistent bulk-copy kernel, --set full
     # capture (136.4 MB read + 74.2 MB written)
     "gdr_decode_kernel": {"bytes": 210_509_000, "sha": "5f7ea947d98305b5"},
-    # prefill_t16k: one launch, DRAM counters (2.165 GB read + 0.521 GB written)
-    "gdr_prefill_fused": {"bytes": 2_685_396_000, "sha": "5b016de430e8fb57"},
+    # prefill_t16k: one launch of the warp-specialised kernel, DRAM counters
+    # (2.1654 GB read + 0.5211 GB written)
+    "gdr_prefill_fused": {"bytes": 2_686_545_408, "sha": "68aac477a65c49aa"},
 }
 
 
@@ -58,12 +59,18 @@ def parse_args():
     ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "prefill", "decode", "prefill_t4k"],
+    ap.add_argument("--workload", choices=["all", "prefill", "decode", "prefill_t4k", "tree",
+                                           "ragged_f32"],
                     default="all",
                     help="prefill: the headline only; decode: only the decode measurement "
                          "(printed as its own line, for profiling the decode kernel); "
                          "prefill_t4k: the B=1 T=4096 prefill alone (its own line), the "
-                         "small-batch case the segmented state scan serves")
+                         "small-batch case the segmented state scan serves; tree: tree "
+                         "verification of 8 beam trees of 512 draft tokens (its own line); "
+                         "ragged_f32: the ragged float32 batch through the packed entry "
+                         "(its own line)")
+    ap.add_argument("--no-segments", action="store_true",
+                    help="prefill workloads: one walk per head (GDR_FLAG_NO_SEGMENTS)")
     return ap.parse_args()
 
 
@@ -207,10 +214,12 @@ def barrier(ws):
 
 # ----------------------------------------------------------------- GPU arm
 def bench_prefill(args, ws, rank, dev, name=PREFILL):
-    from channelwise_gated_delta_gb300 import gdr_forward, gdr_trace_enable, gdr_trace_read
+    from channelwise_gated_delta_gb300 import (GDR_FLAG_NO_SEGMENTS, gdr_forward, gdr_trace_enable,
+                                               gdr_trace_read)
     from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw_workload
 
     w = WORKLOADS[name]
+    flags = GDR_FLAG_NO_SEGMENTS if args.no_segments else 0
     d = draw_workload(w, seed=1000 + rank, device=dev)
     out = torch.empty(w.B, w.T, w.HV, w.dv, dtype=w.dtype, device=dev)
     ht = torch.empty(w.B, w.HV, w.dk, w.dv, dtype=torch.float32, device=dev)
@@ -218,7 +227,7 @@ def bench_prefill(args, ws, rank, dev, name=PREFILL):
 
     def step():
         gdr_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=out, ht=ht,
-                    chunk=w.chunk, stream=stream)
+                    chunk=w.chunk, stream=stream, flags=flags)
 
     for _ in range(args.warmup):
         step()
@@ -445,6 +454,99 @@ def bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind):
         print(json.dumps(line), flush=True)
 
 
+def timed_steps(args, dev, step):
+    """W untimed steps, then K steps between CUDA events on the current
+    stream, with the library's launch trace and the SM clocks over them."""
+    from channelwise_gated_delta_gb300 import gdr_trace_enable, gdr_trace_read
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    gdr_trace_read()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    stream = torch.cuda.current_stream(dev)
+    gdr_trace_enable(True)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(False)
+    clk = clocks.stop()
+    return t0.elapsed_time(t1), gdr_trace_read(), clk
+
+
+def side_line(args, metric, workload, tokens, bytes_step, dtype, ms, trace, clk, hbm_peak,
+              peak_kind):
+    """One JSON line for a side workload: tokens/s over the timed steps, and
+    the step's algorithmic bytes over the device time of all its launches."""
+    dev_ms = sum(v[1] for v in trace.values())
+    roof = roofline("step: " + " + ".join(sorted(trace)), args.steps, dev_ms, bytes_step,
+                    hbm_peak, peak_kind)
+    return {
+        "metric": metric, "value": round(tokens * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {"workload": workload}, "roofline": roof,
+        "kernels": {k: {"launches": v[0], "ms_total": round(v[1], 3)} for k, v in trace.items()},
+        "gpu_launches": sum(v[0] for v in trace.values()), "clocks": clk,
+    }
+
+
+def bench_tree(args, dev, hbm_peak, peak_kind):
+    """Tree verification: 8 beam-shaped draft trees of 512 tokens (up to 4
+    children a node), HK=16, HV=32, dk=dv=128, bf16 q/k/v, with h0.  Bytes per
+    step: q, k per key head, v, g, beta and o per value head, h0 read once."""
+    from channelwise_gated_delta_gb300 import gdr_forward_tree
+    from channelwise_gated_delta_gb300.inputs import draw, draw_parents
+    B, T, HK, HV, d = 8, 512, 16, 32, 128
+    x = {k: (None if v is None else v.to(dev))
+         for k, v in draw(B, T, HK, HV, d, d, dtype=torch.bfloat16, seed=1).items()}
+    parent = draw_parents(B, T, "beam", seed=1, branching=4)
+    out = torch.empty(B, T, HV, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+
+    def step():
+        gdr_forward_tree(x["q"], x["k"], x["v"], x["g"], x["beta"], parent, h0=x["h0"], out=out,
+                         workspace=ws)
+
+    ms, trace, clk = timed_steps(args, dev, step)
+    per_token = 2 * HK * d * 2 + HV * d * 2 + HV * d * 4 + HV * 4 + HV * d * 2
+    bytes_step = B * T * per_token + B * HV * d * d * 4
+    return side_line(args, "GDR tree verification tokens/s [tree B8 T512 beam]",
+                     "tree verification B8 T512 (beam trees, up to 4 children) HK16 HV32 "
+                     "dk=dv=128, bf16 q/k/v, f32 g/beta/h0, blocked solve",
+                     B * T, bytes_step, "bf16", ms, trace, clk, hbm_peak, peak_kind)
+
+
+def bench_ragged_f32(args, dev, hbm_peak, peak_kind):
+    """The ragged float32 batch (lengths 1 .. 512, h0 given) through the
+    packed entry: the single token on the decode kernel, the rest on the
+    chunk prep and the tensor-core state scan."""
+    from channelwise_gated_delta_gb300 import gdr_forward_varlen
+    from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw_workload, pack
+    w = WORKLOADS["ragged_b8"]
+    packed, cu = pack(draw_workload(w, seed=1))
+    x = {k: (None if v is None else v.to(dev)) for k, v in packed.items()}
+    ws = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+    tokens = cu[-1]
+
+    def step():
+        gdr_forward_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, h0=x["h0"],
+                           chunk=w.chunk, workspace=ws)
+
+    ms, trace, clk = timed_steps(args, dev, step)
+    per_token = 2 * w.HK * w.dk * 4 + w.HV * w.dv * 4 + w.HV * w.dk * 4 + w.HV * 4 + w.HV * w.dv * 4
+    bytes_step = tokens * per_token + 2 * (len(cu) - 1) * w.HV * w.dk * w.dv * 4
+    return side_line(args, "GDR prefill tokens/s [ragged_b8 f32]",
+                     "ragged batch, lengths 1 33 49 64 97 128 256 512, HK16 HV32 dk=dv=128 "
+                     "chunk64, f32 q/k/v/g/beta/state, h0 given, packed entry",
+                     tokens, bytes_step, "f32", ms, trace, clk, hbm_peak, peak_kind)
+
+
 # ----------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -462,6 +564,14 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
     hbm_peak, _, peak_kind = load_peaks()
 
+    if args.workload in ("tree", "ragged_f32"):
+        if rank == 0:
+            fn = bench_tree if args.workload == "tree" else bench_ragged_f32
+            print(json.dumps(fn(args, dev, hbm_peak, peak_kind)), flush=True)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.workload == "prefill_t4k":
         bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind)
         if ws > 1:
