@@ -35,9 +35,11 @@
 // half by more than 43 nats in any channel, every factor lies within
 // exp(+-80) and c above exp(-86), in the normal float range.  A chunk outside
 // that range uses m := the chunk start (Lk = exp(G) K, Lq = exp(G) Q,
-// R = exp(G_L - G) K, all factors <= 1) with A and P from exact pairwise decays
-// on CUDA cores; its carry is X <- (exp(G_L) X + U^T R) c, the first factor
-// applied when X is written, so the result is right for any g <= 0.
+// R = exp(G_L - G) K, all factors <= 1) with A and P built 16 x 16 block by
+// block on bf16 mma.sync, each block's decays split about a row inside it
+// (exact_block below; pairwise decays for a diagonal block past that
+// range); its carry is X <- (exp(G_L) X + U^T R) c, the first factor applied
+// when X is written, so the result is right for any g <= 0.
 //
 // GB300 mapping: one CTA of 20 warps per (sequence, value head) walks that
 // head's chunks in order.
@@ -46,7 +48,7 @@
 //               operands S'^T, -Z^T and U^T back into TMEM, and store O.
 //   warps 8-15  prep warps: the prefix sums, range check and carry factors,
 //               the bf16 operand tiles Lq, Lk, R of the next chunk, the P
-//               read-back, and the exact pairwise path.
+//               read-back, and the exact path's A and P blocks.
 //   warp 16     producer: TMA loads of k, q, g and v, and the gram
 //               [Lq; Lk] R^T of the chunk being prepared.
 //   warp 17     issues the state-dependent MMAs of the chunk being scanned:
