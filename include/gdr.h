@@ -81,7 +81,9 @@ typedef enum gdr_dtype {
 /* Flags for gdr_forward_ex and the other entries that take them (0 in normal
  * calls; the first two are for tests and diagnosis). */
 #define GDR_FLAG_FORCE_CHUNKED 1u /* run the chunked prefill even when T == 1 */
-#define GDR_FLAG_FORCE_GENERIC 2u /* use the CUDA-core prefill even where the tensor-core one applies */
+/* the chunked prefill on CUDA cores throughout (chunk prep and state scan),
+ * even where the fused tensor-core kernel or the tensor-core state scan applies */
+#define GDR_FLAG_FORCE_GENERIC 2u
 /*
  * Scalar gate: g holds one log-decay per token and value head, [B][T][HV]
  * float32 (varlen: [total][HV]), applied to every key channel -- the gated
@@ -89,7 +91,8 @@ typedef enum gdr_dtype {
  * TreeUpdateSolve kernel" (trymirai/uzu PR #576) discusses for a per-key-head
  * gram.  Accepted by gdr_forward_ex, gdr_workspace_bytes, gdr_forward_varlen,
  * gdr_varlen_workspace_bytes, gdr_forward_tree and gdr_tree_workspace_bytes
- * (trees with a scalar gate run on the CUDA-core route).
+ * (trees of up to 64 tokens with a scalar gate run as one CUDA-core chunk,
+ * longer ones on the blocked solve).
  */
 #define GDR_FLAG_SCALAR_GATE 4u
 /*
@@ -283,8 +286,10 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
  * ht[n]; a zero-length sequence copies h0[n] (or zeros) to ht[n].  Each
  * sequence takes the route gdr_forward_ex would give it as a B = 1 call
  * with the same flags: length 1 the single-token kernel, longer ones the
- * tensor-core prefill (bf16, dk = dv = 128, chunk 64) or else the CUDA-core
- * chunked prefill; the outputs equal those of N such calls bit for bit.
+ * tensor-core prefill (bf16, dk = dv = 128, chunk 64) or else the chunked
+ * prefill (chunk prep, then the state scan on the tensor cores unless
+ * GDR_FLAG_FORCE_GENERIC); the outputs equal those of N such calls bit for
+ * bit.
  * Enqueued on `stream`: one host-to-device copy of the batch's tables (from
  * pageable host memory: the call returns once the bytes have been taken, so
  * it cannot be captured in a CUDA graph), one copy or memset per zero-length
