@@ -56,9 +56,10 @@
 //               then X^T += U^T R and O^T += U^T P^T.
 //   warps 18-19 invert I + A for the chunk being prepared (its A rows are
 //               TMEM lanes 64-127, the lane quarters of these two warps).
-// Preparation of chunk c+1 starts as soon as chunk c's operand tiles have
-// been read by its O^T product, so the prefix sums, tiles, gram and inverse
-// of the next chunk overlap the state chain of the current one.  Every state
+// Preparation of chunk c+1 starts with its prefix sums and carry factors as
+// soon as its k, q, g tiles land, and writes its operand tiles once chunk c's
+// O^T product has read theirs, so the prefix sums, tiles, gram and inverse of
+// the next chunk overlap the state chain of the current one.  Every state
 // product is transposed so that M = dv = 128 fills the MMA; the state-side A
 // operands are bf16 in TMEM.  Every mbarrier wait is bounded.
 #include <cuda.h>
@@ -640,7 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < NC; ++c) {
             const int t0 = c * kC, L = min(kC, T - t0), mref = (L - 1) / 2;
             const int par = c & 1;
-            if (c > 0) wait(MB_OPART, c - 1);  // Lq, Lk (and R of chunk c - 2) are free
             wait(MB_RAW, c);
             // ---------------- prefix sums (log2 units), range check, G_m and G_L
             int bad = 0;
@@ -740,10 +740,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     vec(kCv, par ^ 1)[i] = fast_exp2(gm + rel);
                     vec(kAv, par ^ 1)[i] = a_now;
                 }
-                if (c + 1 == NC) {
-                    vec(kCv, par)[i] = slow ? 1.f : fast_exp2(gl - gm);
-                    vec(kAv, par)[i] = 1.f;
-                }
+            }
+            // the prefix sums and carry factors above touch nothing the chain still
+            // reads; from here on the Lq, Lk tiles, R of chunk c - 2 and the carry
+            // slot of chunk c - 2 are rewritten, all free once chunk c - 1's O^T
+            // product (issued after chunk c - 2's state went back to TMEM) is done
+            if (c > 0) wait(MB_OPART, c - 1);
+            if (c + 1 == NC && pt < kD) {
+                const float gm = slow ? 0.f : vec(kGm, par)[pt], gl = vec(kGL, par)[pt];
+                vec(kCv, par)[pt] = slow ? 1.f : fast_exp2(gl - gm);
+                vec(kAv, par)[pt] = 1.f;
             }
             // ---------------- operand tiles Lq, Lk, R (bf16, K-major core matrices)
             {
