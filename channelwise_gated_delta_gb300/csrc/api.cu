@@ -202,8 +202,10 @@ struct VarlenPlan {
     std::vector<int4> gen_seqs;  // CUDA-core prefill: {first row, length, slot, first chunk}
     std::vector<int2> chunks;    // CUDA-core prefill: {first row, length} per chunk
     std::vector<int> empty;      // slots of zero-length sequences
+    std::vector<gdr::SegSeq> seg_seqs;  // tensor-core prefill cut into seg_P segments
+    int seg_P = 0;
     size_t off_rows = 0, off_tc = 0, off_maps = 0, off_gen = 0, off_chunks = 0;
-    size_t table_bytes = 0, record_off = 0, total_bytes = 0;
+    size_t table_bytes = 0, record_off = 0, off_seg = 0, total_bytes = 0;
 };
 
 // Checks cu_seqlens (cu[0] = 0, non-decreasing, cu[N] < 2^31) and assigns
@@ -252,6 +254,26 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
     auto longer = [](const int4 &a, const int4 &b) { return a.y > b.y; };
     std::stable_sort(plan->tc_seqs.begin(), plan->tc_seqs.end(), longer);
     std::stable_sort(plan->gen_seqs.begin(), plan->gen_seqs.end(), longer);
+    // long tensor-core sequences on an otherwise idle device: cut into
+    // segments (the chunk-parallel state scan); the others walk whole
+    if (!plan->tc_seqs.empty()) {
+        std::vector<int> lengths;
+        for (const int4 &sd : plan->tc_seqs) lengths.push_back(sd.y);
+        std::vector<char> cut;
+        const int P = gdr::varlen_segment_count(p, lengths.data(), (int)lengths.size(), flags, &cut);
+        if (P >= 2) {
+            std::vector<int4> walk;
+            for (size_t i = 0; i < plan->tc_seqs.size(); ++i) {
+                const int4 sd = plan->tc_seqs[i];
+                if (cut[i])
+                    plan->seg_seqs.push_back(gdr::SegSeq{(size_t)sd.x, sd.y, sd.z});
+                else
+                    walk.push_back(sd);
+            }
+            plan->tc_seqs.swap(walk);
+            plan->seg_P = P;
+        }
+    }
     for (int4 &sd : plan->gen_seqs) {
         sd.w = (int)plan->chunks.size();
         for (int t = 0; t < sd.y; t += p.chunk)
@@ -270,9 +292,15 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
     off = align256(off + plan->chunks.size() * sizeof(int2));
     plan->table_bytes = off;
     plan->record_off = off;
-    const bool any = !plan->rows.empty() || !plan->tc_seqs.empty() || !plan->gen_seqs.empty();
+    const bool any = !plan->rows.empty() || !plan->tc_seqs.empty() || !plan->gen_seqs.empty() ||
+                     !plan->seg_seqs.empty();
     plan->total_bytes =
         any ? off + gdr::generic_varlen_record_bytes(p, (long long)plan->chunks.size()) : 0;
+    if (!plan->seg_seqs.empty()) {
+        plan->off_seg = align256(plan->total_bytes);
+        plan->total_bytes = plan->off_seg + gdr::segmented_list_workspace_bytes(
+                                                p, (int)plan->seg_seqs.size(), plan->seg_P);
+    }
     return GDR_OK;
 }
 
@@ -585,6 +613,14 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
         e = gdr::launch_tc_prefill_varlen(p, ws + plan.off_maps,
                                           reinterpret_cast<const int4 *>(ws + plan.off_tc), p.B,
                                           err, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!plan.seg_seqs.empty()) {
+        int *err = nullptr;
+        e = gdr::device_error_word(&err);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = gdr::launch_segmented_list(base, plan.seg_seqs.data(), (int)plan.seg_seqs.size(),
+                                       plan.seg_P, ws + plan.off_seg, err, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (!plan.gen_seqs.empty()) {

@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <vector>
 #include <stdint.h>
 
 namespace gdr {
@@ -158,4 +159,30 @@ int segment_count(const Problem &p, unsigned flags);
 size_t segmented_workspace_bytes(const Problem &p, int segments);
 cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
                                      int *dev_error, cudaStream_t stream);
+// The segments a sequence of T tokens is cut into when P are asked for: P
+// segments of ceil(chunks / P) whole 64-token chunks, the last possibly
+// shorter, so fewer than P when the chunks do not spread that far; 0 when
+// fewer than two.
+inline int effective_segments(int T, int P) {
+    const int nch = (T + 63) / 64;
+    if (P < 2 || nch < 2) return 0;
+    const int per = (nch + P - 1) / P;
+    const int eff = (nch + per - 1) / per;
+    return eff >= 2 ? eff : 0;
+}
+// Packed batches: one sequence of a segmented launch (first token row,
+// length, index of its h0 / ht slot).
+struct SegSeq {
+    size_t row0;
+    int T;
+    int slot;
+};
+// The segment count for a packed batch whose tensor-core prefill sequences
+// have `lengths` (0: none cut); (*cut)[i] marks the sequences cut into that
+// many segments, the rest walk whole.
+int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+                         std::vector<char> *cut);
+size_t segmented_list_workspace_bytes(const Problem &p, int nseq, int P);
+cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq, int P,
+                                  void *workspace, int *dev_error, cudaStream_t stream);
 }  // namespace gdr

@@ -73,28 +73,28 @@ int sm_count() {
 
 struct Segments {
     int P = 0;        // number of segments
-    int per = 0;      // chunks per segment (the last may have fewer)
-    int group = 0;    // state slots per batch element, 2P - 3 (1 when P = 2)
+    int group = 0;    // state slots per sequence, 2P - 3 (1 when P = 2)
+    int nseq = 0;     // sequences
     int nA = 0, nB = 0;                // runs in wave A and wave B
-    size_t off_seqA = 0, off_mapA = 0, off_seqB = 0, off_mapB = 0;
+    size_t off_slots = 0, off_seqA = 0, off_mapA = 0, off_seqB = 0, off_mapB = 0;
     size_t off_zero = 0, off_scratch = 0, off_state = 0, table_bytes = 0, total = 0;
 };
 
-Segments plan(const Problem &p, int P) {
+// Workspace of nseq sequences cut into P segments each: the tables (the
+// sequences' h0 / ht slots, both waves' run records and tensor maps), the
+// zero value row, the scratch output row and 2P - 3 state slots per sequence.
+Segments plan_seqs(const Problem &p, int nseq, int P) {
     Segments s;
-    const int nch = (p.T + kC - 1) / kC;
-    if (P < 2 || nch < 2) return s;
-    s.per = (nch + P - 1) / P;
-    s.P = (nch + s.per - 1) / s.per;
-    if (s.P < 2) {
-        s.P = 0;
-        return s;
-    }
+    if (P < 2 || nseq <= 0) return s;
+    s.P = P;
+    s.nseq = nseq;
     s.group = 2 * s.P - 3;
-    s.nA = p.B * s.group;
-    s.nB = p.B * (s.P - 1);
+    s.nA = nseq * s.group;
+    s.nB = nseq * (s.P - 1);
     const size_t maps = tc_seq_maps_bytes();
     size_t off = 0;
+    s.off_slots = off;
+    off = align256(off + (size_t)nseq * sizeof(int));
     s.off_seqA = off;
     off = align256(off + (size_t)s.nA * sizeof(int4));
     s.off_mapA = off;
@@ -115,14 +115,21 @@ Segments plan(const Problem &p, int P) {
     return s;
 }
 
-// Four blocks per (slot, head), 32 rows each: slot j of batch element b's
-// group is X_1 (j = 0: a copy of h0[b], or zeros), M_p (odd j: the
+// A dense batch: every batch element is one sequence of p.T tokens.
+Segments plan(const Problem &p, int P) {
+    const int eff = effective_segments(p.T, P);
+    return eff >= 2 ? plan_seqs(p, p.B, eff) : Segments{};
+}
+
+// Four blocks per (slot, head), 32 rows each: slot j of sequence b's group
+// is X_1 (j = 0: a copy of h0[h0_slot[b]], or zeros), M_p (odd j: the
 // identity) or X_{p+1} (even j > 0: zeros).  [128][128] f32 row-major per
 // (slot, head).  Each thread's four loads are issued before its stores.
 // Block 0 also clears the one-row zero value tensor (zero_words 32-bit words).
 constexpr int kInitThreads = 256;
 constexpr int kInitPerThread = (int)(kSlotFloats / 4 / 4 / kInitThreads);  // float4s
 __global__ void __launch_bounds__(kInitThreads) gdr_segment_init(const float *__restrict__ h0,
+                                                                 const int *__restrict__ h0_slot,
                                                                  float *__restrict__ state,
                                                                  int HV, int group,
                                                                  unsigned *__restrict__ zero_row,
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(kInitThreads) gdr_segment_init(const float *__
     const size_t first = (size_t)quarter * (kSlotFloats / 4 / 4);  // float4 index in the slot
     float4 *dst = reinterpret_cast<float4 *>(state + (size_t)sh * kSlotFloats) + first;
     const float4 *src = (j == 0 && h0)
-                            ? reinterpret_cast<const float4 *>(h0 + ((size_t)b * HV + hv) * kSlotFloats) + first
+                            ? reinterpret_cast<const float4 *>(h0 + ((size_t)h0_slot[b] * HV + hv) * kSlotFloats) + first
                             : nullptr;
     const bool ident = (j & 1) != 0;
     float4 x[kInitPerThread];
@@ -289,31 +296,88 @@ size_t segmented_workspace_bytes(const Problem &p, int segments) {
     return plan(p, segments).total;
 }
 
-cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
-                                     int *dev_error, cudaStream_t stream) {
-    const Segments s = plan(p, segments);
-    if (s.P != segments || s.total == 0) return cudaErrorInvalidValue;
+int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+                         std::vector<char> *cut) {
+    cut->assign((size_t)std::max(n, 0), 0);
+    if ((flags & GDR_FLAG_NO_SEGMENTS) || n <= 0) return 0;
+    Problem one = p;
+    one.B = 1;
+    one.T = 2;
+    if (!tc_prefill_supported(one)) return 0;
+    auto select = [&](int P, int min_chunks) {
+        int m = 0;
+        for (int i = 0; i < n; ++i) {
+            const int nch = (lengths[i] + kC - 1) / kC;
+            (*cut)[i] = nch >= min_chunks && effective_segments(lengths[i], P) == P;
+            m += (*cut)[i];
+        }
+        return m;
+    };
+    const int forced = (int)((flags >> 8) & 0xffu);
+    int P = 0;
+    if (forced) {
+        P = forced;
+        if (select(P, 2) == 0) P = 0;
+    } else {
+        // every prefill sequence's CTAs and wave A's 2P - 3 runs per cut
+        // sequence in one wave on the SMs; the largest P from three up with
+        // segments of kMinSegmentChunks or more
+        const int sms = sm_count();
+        if (sms <= 0) return 0;
+        int longest = 0;
+        for (int i = 0; i < n; ++i) longest = std::max(longest, lengths[i]);
+        for (int q = ((longest + kC - 1) / kC) / kMinSegmentChunks; q >= 3 && !P; --q) {
+            const int m = select(q, q * kMinSegmentChunks);
+            if (m > 0 && (long long)p.HV * ((long long)(2 * q - 3) * m + (n - m)) <= sms) P = q;
+        }
+    }
+    if (P == 0) {
+        cut->assign((size_t)n, 0);
+        return 0;
+    }
+    long long m = 0;
+    for (char c : *cut) m += c;
+    if (m * (2 * P - 3) * p.HV * 4 > 0x7fffffffLL) {
+        cut->assign((size_t)n, 0);
+        return 0;
+    }
+    return P;
+}
+
+size_t segmented_list_workspace_bytes(const Problem &p, int nseq, int P) {
+    return plan_seqs(p, nseq, P).total;
+}
+
+cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq, int P,
+                                  void *workspace, int *dev_error, cudaStream_t stream) {
+    const Segments s = plan_seqs(p, nseq, P);
+    if (s.P != P || s.total == 0) return cudaErrorInvalidValue;
+    for (int i = 0; i < nseq; ++i)
+        if (effective_segments(seqs[i].T, P) != P) return cudaErrorInvalidValue;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     const void *zero_row = ws + s.off_zero;  // cleared by gdr_segment_init
     void *scratch_row = ws + s.off_scratch;
     float *state = reinterpret_cast<float *>(ws + s.off_state);
     const size_t maps = tc_seq_maps_bytes();
-    const int seg_len = s.per * kC;
-    auto seg_t0 = [&](int q) { return q * seg_len; };
-    auto seg_len_of = [&](int q) { return std::min(p.T, (q + 1) * seg_len) - q * seg_len; };
 
-    // tables: {first token row, length, state slot, 0} and the tensor maps
+    // tables: the sequences' h0 / ht slots; per run {first token row, length,
+    // state slot, 0} and its tensor maps
     std::vector<unsigned char> host(s.table_bytes, 0);
+    int *slots = reinterpret_cast<int *>(host.data() + s.off_slots);
     int4 *seqA = reinterpret_cast<int4 *>(host.data() + s.off_seqA);
     int4 *seqB = reinterpret_cast<int4 *>(host.data() + s.off_seqB);
     cudaError_t e = cudaSuccess;
     int a = 0, bb = 0;
-    for (int b = 0; b < p.B; ++b) {
+    for (int b = 0; b < nseq; ++b) {
+        const SegSeq &sq = seqs[b];
+        slots[b] = sq.slot;
         const int base = b * s.group;
-        const size_t row0 = (size_t)b * p.T;
+        const int seg_len = ((sq.T + kC - 1) / kC + P - 1) / P * kC;  // whole chunks
+        auto seg_t0 = [&](int q) { return q * seg_len; };
+        auto seg_len_of = [&](int q) { return std::min(sq.T, (q + 1) * seg_len) - q * seg_len; };
         auto add = [&](int4 *tab, size_t off_map, int &n, int q, int slot_j, const void *v_row,
                        void *o_row) {
-            const size_t tok0 = row0 + seg_t0(q);
+            const size_t tok0 = sq.row0 + seg_t0(q);
             tab[n] = make_int4((int)tok0, seg_len_of(q), base + slot_j, 0);
             const cudaError_t r = tc_encode_seq_maps(p, tok0, seg_len_of(q),
                                                      host.data() + off_map + (size_t)n * maps,
@@ -336,7 +400,8 @@ cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *works
 
     trace_begin(kKernSegInit, stream);
     gdr_segment_init<<<(unsigned)(4 * s.nA * p.HV), kInitThreads, 0, stream>>>(
-        p.h0, state, p.HV, s.group, reinterpret_cast<unsigned *>(ws + s.off_zero), p.HV * kD / 2);
+        p.h0, reinterpret_cast<const int *>(ws + s.off_slots), state, p.HV, s.group,
+        reinterpret_cast<unsigned *>(ws + s.off_zero), p.HV * kD / 2);
     trace_end(kKernSegInit, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -352,13 +417,13 @@ cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *works
     if (e != cudaSuccess) return e;
     if (s.P >= 3) {
         const int sms = sm_count();
-        const bool narrow = sms > 0 && (long long)p.B * p.HV * (kD / 16) <= sms;
+        const bool narrow = sms > 0 && (long long)nseq * p.HV * (kD / 16) <= sms;
         auto combine = [&](auto kernel, int slab) -> cudaError_t {
             cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)combine_smem(slab));
             if (r != cudaSuccess) return r;
             trace_begin(kKernSegCombine, stream);
-            kernel<<<(unsigned)(p.B * p.HV * (kD / slab)), kCombineThreads, combine_smem(slab),
+            kernel<<<(unsigned)(nseq * p.HV * (kD / slab)), kCombineThreads, combine_smem(slab),
                      stream>>>(state, p.HV, s.P);
             trace_end(kKernSegCombine, stream);
             return cudaGetLastError();
@@ -372,13 +437,32 @@ cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *works
                                  stream);
     if (e != cudaSuccess) return e;
     if (p.ht) {
-        // X_{P-1} of every batch element: one strided copy
+        // X_{P-1} of every sequence into its ht slot: one strided copy when the
+        // slots are the sequences' order, else one copy per sequence
         const size_t head_bytes = (size_t)p.HV * kSlotFloats * sizeof(float);
-        e = cudaMemcpy2DAsync(p.ht, head_bytes, state + (size_t)2 * (s.P - 2) * p.HV * kSlotFloats,
-                              (size_t)s.group * head_bytes, head_bytes, p.B,
-                              cudaMemcpyDeviceToDevice, stream);
+        const float *last = state + (size_t)2 * (s.P - 2) * p.HV * kSlotFloats;
+        bool in_order = true;
+        for (int b = 0; b < nseq; ++b) in_order = in_order && seqs[b].slot == b;
+        if (in_order) {
+            e = cudaMemcpy2DAsync(p.ht, head_bytes, last, (size_t)s.group * head_bytes, head_bytes,
+                                  nseq, cudaMemcpyDeviceToDevice, stream);
+        } else {
+            for (int b = 0; b < nseq && e == cudaSuccess; ++b)
+                e = cudaMemcpyAsync(p.ht + (size_t)seqs[b].slot * p.HV * kSlotFloats,
+                                    last + (size_t)b * s.group * p.HV * kSlotFloats, head_bytes,
+                                    cudaMemcpyDeviceToDevice, stream);
+        }
     }
     return e;
+}
+
+cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
+                                     int *dev_error, cudaStream_t stream) {
+    const Segments s = plan(p, segments);
+    if (s.P != segments || s.total == 0) return cudaErrorInvalidValue;
+    std::vector<SegSeq> seqs((size_t)p.B);
+    for (int b = 0; b < p.B; ++b) seqs[b] = SegSeq{(size_t)b * p.T, p.T, b};
+    return launch_segmented_list(p, seqs.data(), p.B, segments, workspace, dev_error, stream);
 }
 
 }  // namespace gdr

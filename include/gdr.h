@@ -288,12 +288,22 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
  * with the same flags: length 1 the single-token kernel, longer ones the
  * tensor-core prefill (bf16, dk = dv = 128, chunk 64) or else the chunked
  * prefill (chunk prep, then the state scan on the tensor cores unless
- * GDR_FLAG_FORCE_GENERIC); the outputs equal those of N such calls bit for
- * bit.
+ * GDR_FLAG_FORCE_GENERIC); the outputs equal those of N such calls with
+ * GDR_FLAG_NO_SEGMENTS bit for bit, except on the sequences cut below.
+ * Long tensor-core sequences may take the segmented state scan (see
+ * GDR_FLAG_SEGMENTS): automatically the largest P >= 3 for which HV CTAs
+ * per whole-walking prefill sequence plus HV (2P - 3) per cut one fit on
+ * the device's SMs at once, cutting the sequences of at least 8P chunks
+ * that spread over exactly P segments; GDR_FLAG_SEGMENTS(n) cuts every
+ * prefill sequence that spreads over exactly n; GDR_FLAG_NO_SEGMENTS none.
+ * A cut sequence agrees with the unsegmented result within the route's
+ * tolerance, not bit for bit.
  * Enqueued on `stream`: one host-to-device copy of the batch's tables (from
  * pageable host memory: the call returns once the bytes have been taken, so
  * it cannot be captured in a CUDA graph), one copy or memset per zero-length
- * sequence, then at most four kernel launches.
+ * sequence, then at most four kernel launches, plus those of the segmented
+ * scan (a second table copy, an initialisation, two prefill waves, the
+ * combine and one state copy per cut sequence) when sequences are cut.
  *
  * `workspace`: device memory of at least gdr_varlen_workspace_bytes(...)
  * bytes, 256-byte aligned, untouched by anything else until the stream has

@@ -194,6 +194,26 @@ def test_varlen_bad_arguments_rejected_before_launch(lib, cu, kw, status):
     assert call_varlen(lib, cu, **kw) == status
 
 
+def test_varlen_segmented_workspace(lib):
+    """A packed batch with forced segments: the sequences whose chunks spread
+    over the count get 2P - 3 f32 states per value head in the workspace (the
+    rest of the batch as before); on this machine (no device) the automatic
+    choice cuts nothing."""
+    from channelwise_gated_delta_gb300 import GDR_FLAG_NO_SEGMENTS, gdr_flag_segments
+    state = 128 * 128 * 4
+    ws = lambda cu, flags: lib.gdr_varlen_workspace_bytes(cu_array(cu), len(cu) - 1, 2, 4, 128,
+                                                          128, 64, 1, flags)
+    cu = [0, 1000, 1001, 1701, 1741]       # 1000 and 700 tokens cut, 1 decodes, 40 walks
+    base = ws(cu, 0)
+    assert base == ws(cu, GDR_FLAG_NO_SEGMENTS)
+    for P, ncut in [(3, 2), (2, 2)]:
+        extra = ws(cu, gdr_flag_segments(P)) - base
+        states = ncut * (2 * P - 3) * 4 * state
+        assert states <= extra < states + 64 * 1024, (P, extra)
+    assert ws(cu, gdr_flag_segments(5) | GDR_FLAG_NO_SEGMENTS) == base
+    assert ws([0, 40, 80], gdr_flag_segments(3)) == ws([0, 40, 80], 0)  # nothing spreads that far
+
+
 def test_varlen_workspace_sizes(lib):
     ws = lambda cu, **kw: lib.gdr_varlen_workspace_bytes(
         cu_array(cu), len(cu) - 1, kw.get("HK", 1), kw.get("HV", 2), kw.get("dk", 32),

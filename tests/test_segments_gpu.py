@@ -1,15 +1,17 @@
 """The segmented state scan of the tensor-core route on the GPU: parity with
 the fp64 oracle for forced segment counts (two to many, ragged last chunk,
 with and without h0, in place, scalar gate, strong decays), the first
-segment's rows bit for bit those of the unsegmented route, and the automatic
-choice on a small-batch long prefill."""
+segment's rows bit for bit those of the unsegmented route, the automatic
+choice on a small-batch long prefill, and packed batches whose long
+sequences are cut (automatically and forced) beside ones that walk whole."""
 import pytest
 import torch
 
 import oracle
 from channelwise_gated_delta_gb300 import (GDR_FLAG_NO_SEGMENTS, gdr_device_check, gdr_flag_segments,
-                                           gdr_forward, gdr_trace_enable, gdr_trace_read)
-from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw, draw_workload, to_f64
+                                           gdr_forward, gdr_forward_varlen, gdr_trace_enable,
+                                           gdr_trace_read)
+from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw, draw_workload, pack, to_f64
 from tests.parity_util import assert_close, to_cuda
 from tests.test_parity_gpu import run_gpu, run_oracle
 
@@ -190,3 +192,71 @@ def test_mixed_chunks_scalar_gate():
         out, ht = run_gpu(d, 64, flags=flags)
         assert_close_by_chunk(out, ref_o)
         assert_close("ht", ht, ref_h, torch.bfloat16)
+
+
+# ---- packed variable-length batches: long sequences cut into segments
+
+
+def run_packed(seqs, flags=0, inplace=False):
+    packed, cu = pack(seqs)
+    c = to_cuda(packed)
+    ht = c["h0"] if (inplace and c["h0"] is not None) else None
+    (out, ht), tr = traced(lambda: gdr_forward_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"],
+                                                      cu, h0=c["h0"], ht=ht, chunk=64,
+                                                      flags=flags))
+    return out, ht, cu, tr
+
+
+def check_packed(seqs, out, ht, cu):
+    for n, d in enumerate(seqs):
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d[x]) for x in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d["h0"]))
+        assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.bfloat16)
+        assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.bfloat16)
+
+
+def draw_packed(lengths, HK, HV, seed, **kw):
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    return [draw(1, L, HK, HV, 128, 128, dtype=torch.bfloat16, generator=gen, **kw)
+            for L in lengths]
+
+
+def test_packed_long_sequence_segmented_automatically():
+    """{4096, 1, 64} at the model's head shape: the 4096-token sequence is cut
+    (32 value heads leave most SMs idle), the 64-token one walks whole and
+    the single token decodes; every sequence against the oracle."""
+    props = torch.cuda.get_device_properties(0)
+    if props.multi_processor_count < 32 * 4:
+        pytest.skip("too few SMs for a three-segment wave beside the other sequence")
+    seqs = draw_packed((4096, 1, 64), 16, 32, seed=450)
+    out, ht, cu, tr = run_packed(seqs)
+    assert "gdr_segment_combine" in tr and "gdr_decode_kernel" in tr, tr
+    check_packed(seqs, out, ht, cu)
+    # the same batch with the scan unsegmented: the same results within the bound
+    out2, ht2, _, tr2 = run_packed(seqs, flags=GDR_FLAG_NO_SEGMENTS)
+    assert "gdr_segment_init" not in tr2, tr2
+    check_packed(seqs, out2, ht2, cu)
+
+
+@pytest.mark.parametrize("segments", [2, 3, 5])
+def test_packed_forced_segments_mixed_lengths(segments):
+    """The sequences whose chunks spread over the forced count are cut, in an
+    order their slots do not follow (longest first), beside ones that walk
+    whole and a decode token."""
+    lengths = (130, 1000, 40, 700, 1, 300)
+    seqs = draw_packed(lengths, 2, 4, seed=460 + segments)
+    out, ht, cu, tr = run_packed(seqs, flags=gdr_flag_segments(segments))
+    assert "gdr_segment_init" in tr, tr
+    check_packed(seqs, out, ht, cu)
+
+
+def test_packed_segments_in_place_and_without_h0():
+    seqs = draw_packed((900, 64, 650), 2, 4, seed=470)
+    out, ht, cu, tr = run_packed(seqs, flags=gdr_flag_segments(3), inplace=True)
+    assert "gdr_segment_init" in tr, tr
+    check_packed(seqs, out, ht, cu)
+    seqs = draw_packed((900, 650), 2, 4, seed=471, h0=False)
+    out, ht, cu, tr = run_packed(seqs, flags=gdr_flag_segments(4))
+    assert "gdr_segment_init" in tr, tr
+    check_packed(seqs, out, ht, cu)

@@ -123,10 +123,14 @@ def test_all_empty_and_none():
 
 
 def test_long_and_short_mix():
-    """A 4k sequence beside short ones: the long one's CTAs run first."""
+    """A 4k sequence beside short ones: walked whole, the long one's CTAs run
+    first (bit for bit the per-sequence calls); by default, with two value
+    heads leaving the SMs idle, it is cut into segments (within the bound)."""
     lengths = (3, 4096, 1, 300, 64)
-    check(draw_seqs(lengths, 1, 2, 128, 128, torch.bfloat16, seed=9, g_mu=-3.0, beta_mu=2.0,
-                    beta_sigma=0.5), 64)
+    seqs = draw_seqs(lengths, 1, 2, 128, 128, torch.bfloat16, seed=9, g_mu=-3.0, beta_mu=2.0,
+                     beta_sigma=0.5)
+    check(seqs, 64, flags=GDR_FLAG_NO_SEGMENTS)
+    check(seqs, 64, bitwise=False)
 
 
 def test_bad_cu_seqlens_rejected():
