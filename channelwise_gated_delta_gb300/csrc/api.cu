@@ -146,7 +146,8 @@ cudaError_t device_error_word(int **out) {
 namespace {
 
 size_t route_workspace(const gdr::Problem &p, Route r, unsigned flags) {
-    if (r == Route::GenericPrefill) return gdr::generic_prefill_workspace_bytes(p);
+    if (r == Route::GenericPrefill)
+        return gdr::generic_prefill_workspace_bytes(p, gdr::scan_segment_count(p, flags));
     if (r == Route::SegmentedPrefill)
         return gdr::segmented_workspace_bytes(p, gdr::segment_count(p, flags));
     return 0;
@@ -168,10 +169,12 @@ gdr_status run(const gdr::Problem &p, Route r, unsigned flags, void *ws, cudaStr
         case Route::Decode:
             e = gdr::launch_decode(p, stream);
             break;
-        case Route::GenericPrefill:
-            e = gdr::launch_generic_prefill(
-                p, ws, stream, !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p));
+        case Route::GenericPrefill: {
+            const bool tc = !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p);
+            e = gdr::launch_generic_prefill(p, ws, stream, tc,
+                                            tc ? gdr::scan_segment_count(p, flags) : 0);
             break;
+        }
         case Route::TensorCorePrefill: {
             int *err = nullptr;
             e = gdr::device_error_word(&err);
@@ -204,8 +207,10 @@ struct VarlenPlan {
     std::vector<int> empty;      // slots of zero-length sequences
     std::vector<gdr::SegSeq> seg_seqs;  // tensor-core prefill cut into seg_P segments
     int seg_P = 0;
+    std::vector<gdr::ScanSeq> scan_seqs;  // chunk-record prefill cut into scan_P segments
+    int scan_P = 0;
     size_t off_rows = 0, off_tc = 0, off_maps = 0, off_gen = 0, off_chunks = 0;
-    size_t table_bytes = 0, record_off = 0, off_seg = 0, total_bytes = 0;
+    size_t table_bytes = 0, record_off = 0, off_seg = 0, off_scan = 0, total_bytes = 0;
 };
 
 // Checks cu_seqlens (cu[0] = 0, non-decreasing, cu[N] < 2^31) and assigns
@@ -279,6 +284,28 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
         for (int t = 0; t < sd.y; t += p.chunk)
             plan->chunks.push_back(make_int2(sd.x + t, std::min(p.chunk, sd.y - t)));
     }
+    // the same for long sequences on the chunk-record route: every chunk's
+    // record is written at once, the cut ones' state scans run in segments
+    if (!plan->gen_seqs.empty()) {
+        std::vector<int> lengths;
+        for (const int4 &sd : plan->gen_seqs) lengths.push_back(sd.y);
+        std::vector<char> cut;
+        const int P =
+            gdr::scan_varlen_segment_count(p, lengths.data(), (int)lengths.size(), flags, &cut);
+        if (P >= 2) {
+            std::vector<int4> walk;
+            for (size_t i = 0; i < plan->gen_seqs.size(); ++i) {
+                const int4 sd = plan->gen_seqs[i];
+                if (cut[i])
+                    plan->scan_seqs.push_back(
+                        gdr::ScanSeq{sd.x, (long long)sd.w * p.HV, sd.y, sd.z, 1, p.HV});
+                else
+                    walk.push_back(sd);
+            }
+            plan->gen_seqs.swap(walk);
+            plan->scan_P = P;
+        }
+    }
     size_t off = 0;
     plan->off_rows = off;
     off = align256(off + plan->rows.size() * sizeof(int2));
@@ -293,13 +320,18 @@ gdr_status plan_varlen(const int *cu, int N, const gdr::Problem &p, unsigned fla
     plan->table_bytes = off;
     plan->record_off = off;
     const bool any = !plan->rows.empty() || !plan->tc_seqs.empty() || !plan->gen_seqs.empty() ||
-                     !plan->seg_seqs.empty();
+                     !plan->seg_seqs.empty() || !plan->scan_seqs.empty();
     plan->total_bytes =
         any ? off + gdr::generic_varlen_record_bytes(p, (long long)plan->chunks.size()) : 0;
     if (!plan->seg_seqs.empty()) {
         plan->off_seg = align256(plan->total_bytes);
         plan->total_bytes = plan->off_seg + gdr::segmented_list_workspace_bytes(
                                                 p, (int)plan->seg_seqs.size(), plan->seg_P);
+    }
+    if (!plan->scan_seqs.empty()) {
+        plan->off_scan = align256(plan->total_bytes);
+        plan->total_bytes = plan->off_scan + gdr::scan_segmented_bytes(
+                                                 p, (int)plan->scan_seqs.size(), plan->scan_P);
     }
     return GDR_OK;
 }
@@ -623,13 +655,14 @@ GDR_API gdr_status gdr_forward_varlen(const void *q, const void *k, const void *
                                        plan.seg_P, ws + plan.off_seg, err, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (!plan.gen_seqs.empty()) {
+    if (!plan.gen_seqs.empty() || !plan.scan_seqs.empty()) {
         gdr::Problem p = base;
         p.B = (int)plan.gen_seqs.size();
         e = gdr::launch_generic_prefill_varlen(
             p, ws + plan.record_off, reinterpret_cast<const int2 *>(ws + plan.off_chunks),
             (int)plan.chunks.size(), reinterpret_cast<const int4 *>(ws + plan.off_gen), s,
-            !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p));
+            !(flags & GDR_FLAG_FORCE_GENERIC) && gdr::scan_tc_supported(p),
+            plan.scan_seqs.data(), (int)plan.scan_seqs.size(), plan.scan_P, ws + plan.off_scan);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return GDR_OK;

@@ -100,9 +100,12 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_tc_prefill(const Problem &p, int *dev_error, cudaStream_t stream);
 size_t generic_prefill_workspace_bytes(const Problem &p);
 // tc_scan: the state scan on the tensor cores (launch_chunk_scan_tc) rather
-// than on CUDA cores; the prep writes its records for it.
+// than on CUDA cores; the prep writes its records for it.  segments >= 2
+// (tc_scan only): that scan cut into segments (scan_segment_count), with
+// the workspace generic_prefill_workspace_bytes(p, segments).
+size_t generic_prefill_workspace_bytes(const Problem &p, int segments);
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream,
-                                   bool tc_scan = false);
+                                   bool tc_scan = false, int segments = 0);
 
 // Packed variable-length batches (p.B = number of entries in the table, the
 // pointers those of the packed tensors).
@@ -123,15 +126,34 @@ cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, con
 // sequence's chunks, seqs[s] = {first token row, length, state slot, index
 // of its first chunk}; records: generic_varlen_record_bytes(p, nchunks).
 size_t generic_varlen_record_bytes(const Problem &p, long long nchunks);
+// tc_scan: also nseg sequences cut into seg_P segments (seg_seqs on the
+// host, records addressed as packed chunks), workspace seg_ws of
+// scan_segmented_bytes(p, nseg, seg_P); p.B counts the whole ones only.
+struct ScanSeq;
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
                                           int nchunks, const int4 *seqs, cudaStream_t stream,
-                                          bool tc_scan = false);
+                                          bool tc_scan = false, const ScanSeq *seg_seqs = nullptr,
+                                          int nseg = 0, int seg_P = 0, void *seg_ws = nullptr);
 // The state scan of the chunked prefill on the tensor cores (scan_tc.cu):
 // records in the tensor-core layout written by the prep kernel, rec_floats
 // floats each; dense batches (seqs == nullptr) or nseq packed sequences.
 bool scan_tc_supported(const Problem &p);
 cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t rec_floats,
                                  const int4 *seqs, int nseq, cudaStream_t stream);
+// One run of that scan in a segmented launch: tokens tok0 .. tok0 + T - 1,
+// whose chunk c of value head hv has its record at rec_base + hv * hv_stride
+// + c * c_stride; the state starts from slot `slot` of p.h0 and ends in slot
+// `slot` of p.ht.  kRunZeroValues: the values read as zero (the run from
+// the identity then ends in the segment's map M); kRunNoOutputs: the
+// outputs are dropped.
+struct ScanRun {
+    long long tok0, rec_base;
+    int T, slot, hv_stride, c_stride, flags, pad;
+};
+constexpr int kRunZeroValues = 1;
+constexpr int kRunNoOutputs = 2;
+cudaError_t launch_chunk_scan_runs(const Problem &p, const float *records, size_t rec_floats,
+                                   const ScanRun *runs, int nrun, cudaStream_t stream);
 // Tree verification on CUDA cores: p.B trees of p.T <= p.chunk tokens each,
 // parents [B][T] (device); records: generic_tree_record_bytes(p).
 size_t generic_tree_record_bytes(const Problem &p);
@@ -160,11 +182,12 @@ size_t segmented_workspace_bytes(const Problem &p, int segments);
 cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
                                      int *dev_error, cudaStream_t stream);
 // The segments a sequence of T tokens is cut into when P are asked for: P
-// segments of ceil(chunks / P) whole 64-token chunks, the last possibly
+// segments of ceil(chunks / P) whole chunks (64 tokens each unless `chunk`
+// says otherwise), the last possibly
 // shorter, so fewer than P when the chunks do not spread that far; 0 when
 // fewer than two.
-inline int effective_segments(int T, int P) {
-    const int nch = (T + 63) / 64;
+inline int effective_segments(int T, int P, int chunk = 64) {
+    const int nch = (T + chunk - 1) / chunk;
     if (P < 2 || nch < 2) return 0;
     const int per = (nch + P - 1) / P;
     const int eff = (nch + per - 1) / per;
@@ -185,4 +208,21 @@ int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned f
 size_t segmented_list_workspace_bytes(const Problem &p, int nseq, int P);
 cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq, int P,
                                   void *workspace, int *dev_error, cudaStream_t stream);
+// The same segmented scan on the route of chunk records (the CUDA-core prep,
+// then the tensor-core state scan; dk = dv = 128): the segment count for a
+// dense batch under `flags` (0: not segmented), and for packed sequences of
+// `lengths` with (*cut)[i] marking those cut; the workspace after the
+// records; the launches, given every sequence's first token row, length,
+// state slot and record addressing (rec_base: its chunk 0 of value head 0).
+struct ScanSeq {
+    long long tok0, rec_base;
+    int T, slot, hv_stride, c_stride;
+};
+int scan_segment_count(const Problem &p, unsigned flags);
+int scan_varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+                              std::vector<char> *cut);
+size_t scan_segmented_bytes(const Problem &p, int nseq, int P);
+cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t rec_floats,
+                                  const ScanSeq *seqs, int nseq, int P, void *workspace,
+                                  cudaStream_t stream);
 }  // namespace gdr

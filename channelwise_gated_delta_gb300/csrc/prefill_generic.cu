@@ -688,9 +688,19 @@ size_t scan_smem_bytes(int dk, int C) {
 // Dense batches: chunks == seqs == nullptr, B x T from p.  Packed batches:
 // nchunks chunk records and p.B sequence records.  Trees (TREE): p.T <=
 // p.chunk tokens per batch element, parents [B][T] on the device.
+// TCREC: a segmented scan (SegScan::P >= 2) runs `n` more sequences after
+// the p.B whole ones (none for a dense batch cut into segments).
+struct SegScan {
+    const ScanSeq *seqs = nullptr;
+    int n = 0, P = 0;
+    void *ws = nullptr;
+    bool whole = true;  // the p.B sequences of the batch walk whole
+};
+
 template <typename Tin, bool TREE, bool TCREC = false>
 cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chunks, int nchunks,
-                             const int4 *seqs, const int *parents, cudaStream_t stream) {
+                             const int4 *seqs, const int *parents, cudaStream_t stream,
+                             const SegScan &seg = SegScan{}) {
     const int C = p.chunk;
     const int NC = (p.T + C - 1) / C;
     float *ws = static_cast<float *>(workspace);
@@ -716,7 +726,13 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chun
     if (e != cudaSuccess) return e;
     if (TCREC) {
         const ChunkLayout lay{C, p.dk, p.dv};
-        return launch_chunk_scan_tc(p, ws, lay.floats(), seqs, p.B, stream);
+        if (seg.whole) {
+            e = launch_chunk_scan_tc(p, ws, lay.floats(), seqs, p.B, stream);
+            if (e != cudaSuccess) return e;
+        }
+        if (seg.P >= 2 && seg.n > 0)
+            e = launch_scan_segmented(p, ws, lay.floats(), seg.seqs, seg.n, seg.P, seg.ws, stream);
+        return e;
     }
     trace_begin(kKernChunkScan, stream);
     gdr_chunk_scan<Tin, TREE><<<(unsigned)scan_blocks, kScanThreads, ss, stream>>>(
@@ -733,8 +749,32 @@ size_t generic_prefill_workspace_bytes(const Problem &p) {
     return sizeof(float) * lay.floats() * (size_t)p.B * p.HV * NC;
 }
 
+size_t generic_prefill_workspace_bytes(const Problem &p, int segments) {
+    const size_t rec = generic_prefill_workspace_bytes(p);
+    if (segments < 2) return rec;
+    return ((rec + 255) & ~(size_t)255) + scan_segmented_bytes(p, p.B, segments);
+}
+
 cudaError_t launch_generic_prefill(const Problem &p, void *workspace, cudaStream_t stream,
-                                   bool tc_scan) {
+                                   bool tc_scan, int segments) {
+    if (tc_scan && segments >= 2) {
+        // every batch element cut into segments after the prep
+        const int NC = (p.T + p.chunk - 1) / p.chunk;
+        std::vector<ScanSeq> list((size_t)p.B);
+        for (int b = 0; b < p.B; ++b)
+            list[b] = ScanSeq{(long long)b * p.T, (long long)b * p.HV * NC, p.T, b, NC, 1};
+        SegScan seg;
+        seg.seqs = list.data();
+        seg.n = p.B;
+        seg.P = segments;
+        seg.ws = static_cast<unsigned char *>(workspace) +
+                 ((generic_prefill_workspace_bytes(p) + 255) & ~(size_t)255);
+        seg.whole = false;
+        return p.bf16 ? launch_generic_t<__nv_bfloat16, false, true>(p, workspace, nullptr, 0,
+                                                                     nullptr, nullptr, stream, seg)
+                      : launch_generic_t<float, false, true>(p, workspace, nullptr, 0, nullptr,
+                                                             nullptr, stream, seg);
+    }
     if (tc_scan)
         return p.bf16 ? launch_generic_t<__nv_bfloat16, false, true>(p, workspace, nullptr, 0,
                                                                      nullptr, nullptr, stream)
@@ -753,12 +793,20 @@ size_t generic_varlen_record_bytes(const Problem &p, long long nchunks) {
 
 cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const int2 *chunks,
                                           int nchunks, const int4 *seqs, cudaStream_t stream,
-                                          bool tc_scan) {
-    if (tc_scan)
+                                          bool tc_scan, const ScanSeq *seg_seqs, int nseg,
+                                          int seg_P, void *seg_ws) {
+    if (tc_scan) {
+        SegScan seg;
+        seg.seqs = seg_seqs;
+        seg.n = nseg;
+        seg.P = seg_P;
+        seg.ws = seg_ws;
+        seg.whole = p.B > 0;
         return p.bf16 ? launch_generic_t<__nv_bfloat16, false, true>(p, records, chunks, nchunks,
-                                                                     seqs, nullptr, stream)
+                                                                     seqs, nullptr, stream, seg)
                       : launch_generic_t<float, false, true>(p, records, chunks, nchunks, seqs,
-                                                             nullptr, stream);
+                                                             nullptr, stream, seg);
+    }
     return p.bf16 ? launch_generic_t<__nv_bfloat16, false>(p, records, chunks, nchunks, seqs,
                                                            nullptr, stream)
                   : launch_generic_t<float, false>(p, records, chunks, nchunks, seqs, nullptr,

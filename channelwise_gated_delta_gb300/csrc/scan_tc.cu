@@ -23,6 +23,12 @@
 // Qt, Kh and P straight in this form (gdr_chunk_prep with the TC layout), so
 // the scan moves them with bulk copies.
 //
+// A segmented scan (segments.cu) launches this kernel over a run table
+// instead: each run is a stretch of whole chunks with its own first record,
+// state slot and flags; a run that gives a segment's map M starts from the
+// identity and reads its values as zero (U = -Wk S), and the runs of the
+// first wave drop their outputs.
+//
 // Warps: 0-3 the chain (lane j = value column j: builds the bf16 state pair,
 // U = Wv - Z, reads O out, the final state), 4 the producer (one thread: bulk
 // copies of each chunk's operands), 5 the MMA issuer (one thread).  Wk and Kh
@@ -90,6 +96,7 @@ struct ScanTcArgs {
     void *out;          // [rows][HV][dv], float or bf16
     float *ht;          // [slots][HV][dk][dv] or null
     const int4 *seqs;   // packed batches: {first row, length, slot, first chunk}
+    const ScanRun *runs;  // runs of a segmented scan (instead of seqs), or null
     int *err;           // the library's error word
     int T_dense, HV, dk, dv, C, NC_dense;
     size_t rec_floats;
@@ -119,8 +126,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
     // batches {first row, length, slot, first chunk} with records (chunk, hv)
     const int hv = blockIdx.x % HV, b = blockIdx.x / HV;
     size_t tok0 = (size_t)b * a.T_dense, rec0 = ((size_t)b * HV + hv) * a.NC_dense, rec_step = 1;
-    int T = a.T_dense, sl = b;
-    if (a.seqs) {
+    int T = a.T_dense, sl = b, rflags = 0;
+    if (a.runs) {
+        const ScanRun r = a.runs[b];
+        tok0 = (size_t)r.tok0;
+        T = r.T;
+        sl = r.slot;
+        rec0 = (size_t)r.rec_base + (size_t)hv * r.hv_stride;
+        rec_step = (size_t)r.c_stride;
+        rflags = r.flags;
+    } else if (a.seqs) {
         const int4 sd = a.seqs[b];
         tok0 = (size_t)sd.x;
         T = sd.y;
@@ -278,6 +293,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         // ================= the chain: lane j = value column j
         const int j = tid;
         const bool jv = j < dv;
+        const bool vals = jv && !(rflags & kRunZeroValues);    // values read (else zero)
+        const bool outs = jv && !(rflags & kRunNoOutputs);     // outputs stored
         const uint32_t lo = (uint32_t)(32 * warp) << 16;
         const float *Wv = reinterpret_cast<const float *>(smem + kScWv);
         const float *gam = reinterpret_cast<const float *>(smem + kScGam);
@@ -325,8 +342,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     const int s = 16 * g + 2 * m;
-                    const float u0 = (jv ? Wv[s * dv + j] : 0.f) - z[2 * m];
-                    const float u1 = (jv ? Wv[(s + 1) * dv + j] : 0.f) - z[2 * m + 1];
+                    const float u0 = (vals ? Wv[s * dv + j] : 0.f) - z[2 * m];
+                    const float u1 = (vals ? Wv[(s + 1) * dv + j] : 0.f) - z[2 * m + 1];
                     sc_pack(u0, u1, h[m], l[m]);
                 }
                 tmem_st8(tmem + lo + kScTmUhi + 8 * g, h);
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     const int s = 16 * g + m;
-                    if (jv && s < L) out[((tok0 + t0 + s) * HV + hv) * dv + j] = from_f32<Tout>(o[m]);
+                    if (outs && s < L) out[((tok0 + t0 + s) * HV + hv) * dv + j] = from_f32<Tout>(o[m]);
                 }
             }
             tc_fence_before_sync();
@@ -380,17 +397,20 @@ bool scan_tc_supported(const Problem &p) {
            (p.chunk == 16 || p.chunk == 32 || p.chunk == 64);
 }
 
-cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t rec_floats,
-                                 const int4 *seqs, int nseq, cudaStream_t stream) {
+namespace {
+cudaError_t launch_scan(const Problem &p, const float *records, size_t rec_floats,
+                        const int4 *seqs, const ScanRun *runs, long long units,
+                        cudaStream_t stream) {
     int *err = nullptr;
     cudaError_t e = device_error_word(&err);
     if (e != cudaSuccess) return e;
     ScanTcArgs a;
-    a.ws = records; a.h0 = p.h0; a.out = p.out; a.ht = p.ht; a.seqs = seqs; a.err = err;
+    a.ws = records; a.h0 = p.h0; a.out = p.out; a.ht = p.ht; a.seqs = seqs; a.runs = runs;
+    a.err = err;
     a.T_dense = p.T; a.HV = p.HV; a.dk = p.dk; a.dv = p.dv; a.C = p.chunk;
     a.NC_dense = (p.T + p.chunk - 1) / p.chunk;
     a.rec_floats = rec_floats;
-    const long long ctas = (long long)(seqs ? nseq : p.B) * p.HV;
+    const long long ctas = units * p.HV;
     if (ctas == 0) return cudaSuccess;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     trace_begin(kKernChunkScanTc, stream);
@@ -408,6 +428,17 @@ cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t 
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     trace_end(kKernChunkScanTc, stream);
     return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t rec_floats,
+                                 const int4 *seqs, int nseq, cudaStream_t stream) {
+    return launch_scan(p, records, rec_floats, seqs, nullptr, seqs ? nseq : p.B, stream);
+}
+
+cudaError_t launch_chunk_scan_runs(const Problem &p, const float *records, size_t rec_floats,
+                                   const ScanRun *runs, int nrun, cudaStream_t stream) {
+    return launch_scan(p, records, rec_floats, nullptr, runs, nrun, stream);
 }
 
 }  // namespace gdr

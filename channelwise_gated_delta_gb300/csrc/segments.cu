@@ -267,48 +267,58 @@ constexpr size_t combine_smem(int slab) {
     return ((size_t)kD * kMtLd + (size_t)kD * slab) * sizeof(float);
 }
 
-}  // namespace
-
-int segment_count(const Problem &p, unsigned flags) {
-    if (flags & GDR_FLAG_NO_SEGMENTS) return 0;
-    if (!tc_prefill_supported(p) || p.B <= 0 || p.T < 2) return 0;
-    const int nch = (p.T + kC - 1) / kC;
-    const int forced = (int)((flags >> 8) & 0xffu);
-    int P = forced;
-    if (!forced) {
-        // wave A runs B HV (2P - 3) CTAs, one per SM; take the largest P
-        // that keeps it to one wave, with segments of kMinSegmentChunks or more
-        const int sms = sm_count();
-        const long long units = (long long)p.B * p.HV;
-        if (sms <= 0 || units <= 0) return 0;
-        P = (int)((sms / units + 3) / 2);
-        P = std::min(P, nch / kMinSegmentChunks);
-        if (P < 3) return 0;  // two segments walk as long as one
-    }
-    const Segments s = plan(p, P);
-    if (s.P < 2 || (!forced && s.P < 3)) return 0;
-    // every grid (4 blocks per slot and head at most) and slot index in int
-    if ((long long)s.nA * p.HV * 4 > 0x7fffffffLL) return 0;
-    return s.P;
+// The combine over nseq groups of 2P - 3 slots (nothing to chain when P = 2).
+cudaError_t launch_combine(const Problem &p, float *state, int nseq, int P, cudaStream_t stream) {
+    if (P < 3) return cudaSuccess;
+    const int sms = sm_count();
+    const bool narrow = sms > 0 && (long long)nseq * p.HV * (kD / 16) <= sms;
+    auto combine = [&](auto kernel, int slab) -> cudaError_t {
+        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)combine_smem(slab));
+        if (r != cudaSuccess) return r;
+        trace_begin(kKernSegCombine, stream);
+        kernel<<<(unsigned)(nseq * p.HV * (kD / slab)), kCombineThreads, combine_smem(slab),
+                 stream>>>(state, p.HV, P);
+        trace_end(kKernSegCombine, stream);
+        return cudaGetLastError();
+    };
+    return narrow ? combine(gdr_segment_combine<16>, 16) : combine(gdr_segment_combine<32>, 32);
 }
 
-size_t segmented_workspace_bytes(const Problem &p, int segments) {
-    return plan(p, segments).total;
+// X_{P-1} of every sequence into its ht slot (slots[b]): one strided copy
+// when the slots are the sequences' order, else one copy per sequence.
+cudaError_t copy_final_states(const Problem &p, const float *state, const std::vector<int> &slots,
+                              int P, cudaStream_t stream) {
+    if (!p.ht) return cudaSuccess;
+    const int nseq = (int)slots.size(), group = 2 * P - 3;
+    const size_t head_bytes = (size_t)p.HV * kSlotFloats * sizeof(float);
+    const float *last = state + (size_t)2 * (P - 2) * p.HV * kSlotFloats;
+    bool in_order = true;
+    for (int b = 0; b < nseq; ++b) in_order = in_order && slots[b] == b;
+    if (in_order)
+        return cudaMemcpy2DAsync(p.ht, head_bytes, last, (size_t)group * head_bytes, head_bytes,
+                                 nseq, cudaMemcpyDeviceToDevice, stream);
+    cudaError_t e = cudaSuccess;
+    for (int b = 0; b < nseq && e == cudaSuccess; ++b)
+        e = cudaMemcpyAsync(p.ht + (size_t)slots[b] * p.HV * kSlotFloats,
+                            last + (size_t)b * group * p.HV * kSlotFloats, head_bytes,
+                            cudaMemcpyDeviceToDevice, stream);
+    return e;
 }
 
-int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+// Which of n sequences of `lengths` (chunks of `chunk` tokens) to cut, and
+// into how many segments: forced (flags' segment count), every sequence that
+// spreads over exactly that many; automatic, the largest q >= 3 for which
+// every sequence's CTA and wave A's 2q - 3 runs per cut sequence fit on the
+// SMs in one wave, cutting the sequences of kMinSegmentChunks q chunks or
+// more that spread over exactly q.  0: none cut.
+int choose_list_segments(const Problem &p, const int *lengths, int n, unsigned flags, int chunk,
                          std::vector<char> *cut) {
-    cut->assign((size_t)std::max(n, 0), 0);
-    if ((flags & GDR_FLAG_NO_SEGMENTS) || n <= 0) return 0;
-    Problem one = p;
-    one.B = 1;
-    one.T = 2;
-    if (!tc_prefill_supported(one)) return 0;
     auto select = [&](int P, int min_chunks) {
         int m = 0;
         for (int i = 0; i < n; ++i) {
-            const int nch = (lengths[i] + kC - 1) / kC;
-            (*cut)[i] = nch >= min_chunks && effective_segments(lengths[i], P) == P;
+            const int nch = (lengths[i] + chunk - 1) / chunk;
+            (*cut)[i] = nch >= min_chunks && effective_segments(lengths[i], P, chunk) == P;
             m += (*cut)[i];
         }
         return m;
@@ -319,14 +329,11 @@ int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned f
         P = forced;
         if (select(P, 2) == 0) P = 0;
     } else {
-        // every prefill sequence's CTAs and wave A's 2P - 3 runs per cut
-        // sequence in one wave on the SMs; the largest P from three up with
-        // segments of kMinSegmentChunks or more
         const int sms = sm_count();
         if (sms <= 0) return 0;
         int longest = 0;
         for (int i = 0; i < n; ++i) longest = std::max(longest, lengths[i]);
-        for (int q = ((longest + kC - 1) / kC) / kMinSegmentChunks; q >= 3 && !P; --q) {
+        for (int q = ((longest + chunk - 1) / chunk) / kMinSegmentChunks; q >= 3 && !P; --q) {
             const int m = select(q, q * kMinSegmentChunks);
             if (m > 0 && (long long)p.HV * ((long long)(2 * q - 3) * m + (n - m)) <= sms) P = q;
         }
@@ -342,6 +349,52 @@ int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned f
         return 0;
     }
     return P;
+}
+
+// The dense-batch count: wave A runs B HV (2P - 3) CTAs, one per SM; the
+// largest P that keeps it to one wave, with segments of kMinSegmentChunks
+// chunks or more; forced counts as asked (fewer when the chunks do not
+// spread that far).
+int dense_segments(const Problem &p, unsigned flags, int chunk) {
+    const int nch = (p.T + chunk - 1) / chunk;
+    const int forced = (int)((flags >> 8) & 0xffu);
+    int P = forced;
+    if (!forced) {
+        const int sms = sm_count();
+        const long long units = (long long)p.B * p.HV;
+        if (sms <= 0 || units <= 0) return 0;
+        P = (int)((sms / units + 3) / 2);
+        P = std::min(P, nch / kMinSegmentChunks);
+        if (P < 3) return 0;  // two segments walk as long as one
+    }
+    const int eff = effective_segments(p.T, P, chunk);
+    if (eff < 2 || (!forced && eff < 3)) return 0;
+    // every grid (4 blocks per slot and head at most) and slot index in int
+    if ((long long)p.B * (2 * eff - 3) * p.HV * 4 > 0x7fffffffLL) return 0;
+    return eff;
+}
+
+}  // namespace
+
+int segment_count(const Problem &p, unsigned flags) {
+    if (flags & GDR_FLAG_NO_SEGMENTS) return 0;
+    if (!tc_prefill_supported(p) || p.B <= 0 || p.T < 2) return 0;
+    return dense_segments(p, flags, kC);
+}
+
+size_t segmented_workspace_bytes(const Problem &p, int segments) {
+    return plan(p, segments).total;
+}
+
+int varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+                         std::vector<char> *cut) {
+    cut->assign((size_t)std::max(n, 0), 0);
+    if ((flags & GDR_FLAG_NO_SEGMENTS) || n <= 0) return 0;
+    Problem one = p;
+    one.B = 1;
+    one.T = 2;
+    if (!tc_prefill_supported(one)) return 0;
+    return choose_list_segments(p, lengths, n, flags, kC, cut);
 }
 
 size_t segmented_list_workspace_bytes(const Problem &p, int nseq, int P) {
@@ -415,45 +468,16 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
                                  reinterpret_cast<const int4 *>(ws + s.off_seqA), s.nA, dev_error,
                                  stream);
     if (e != cudaSuccess) return e;
-    if (s.P >= 3) {
-        const int sms = sm_count();
-        const bool narrow = sms > 0 && (long long)nseq * p.HV * (kD / 16) <= sms;
-        auto combine = [&](auto kernel, int slab) -> cudaError_t {
-            cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)combine_smem(slab));
-            if (r != cudaSuccess) return r;
-            trace_begin(kKernSegCombine, stream);
-            kernel<<<(unsigned)(nseq * p.HV * (kD / slab)), kCombineThreads, combine_smem(slab),
-                     stream>>>(state, p.HV, s.P);
-            trace_end(kKernSegCombine, stream);
-            return cudaGetLastError();
-        };
-        e = narrow ? combine(gdr_segment_combine<16>, 16) : combine(gdr_segment_combine<32>, 32);
-        if (e != cudaSuccess) return e;
-    }
+    e = launch_combine(p, state, nseq, s.P, stream);
+    if (e != cudaSuccess) return e;
     wave.B = s.nB;
     e = launch_tc_prefill_varlen(wave, ws + s.off_mapB,
                                  reinterpret_cast<const int4 *>(ws + s.off_seqB), s.nB, dev_error,
                                  stream);
     if (e != cudaSuccess) return e;
-    if (p.ht) {
-        // X_{P-1} of every sequence into its ht slot: one strided copy when the
-        // slots are the sequences' order, else one copy per sequence
-        const size_t head_bytes = (size_t)p.HV * kSlotFloats * sizeof(float);
-        const float *last = state + (size_t)2 * (s.P - 2) * p.HV * kSlotFloats;
-        bool in_order = true;
-        for (int b = 0; b < nseq; ++b) in_order = in_order && seqs[b].slot == b;
-        if (in_order) {
-            e = cudaMemcpy2DAsync(p.ht, head_bytes, last, (size_t)s.group * head_bytes, head_bytes,
-                                  nseq, cudaMemcpyDeviceToDevice, stream);
-        } else {
-            for (int b = 0; b < nseq && e == cudaSuccess; ++b)
-                e = cudaMemcpyAsync(p.ht + (size_t)seqs[b].slot * p.HV * kSlotFloats,
-                                    last + (size_t)b * s.group * p.HV * kSlotFloats, head_bytes,
-                                    cudaMemcpyDeviceToDevice, stream);
-        }
-    }
-    return e;
+    std::vector<int> ht_slots((size_t)nseq);
+    for (int b = 0; b < nseq; ++b) ht_slots[b] = seqs[b].slot;
+    return copy_final_states(p, state, ht_slots, s.P, stream);
 }
 
 cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
@@ -463,6 +487,136 @@ cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *works
     std::vector<SegSeq> seqs((size_t)p.B);
     for (int b = 0; b < p.B; ++b) seqs[b] = SegSeq{(size_t)b * p.T, p.T, b};
     return launch_segmented_list(p, seqs.data(), p.B, segments, workspace, dev_error, stream);
+}
+
+
+// ---- the route of chunk records (CUDA-core prep, tensor-core state scan)
+//
+// Same waves, slots and combine as above; the runs are scan CTAs over the
+// records the prep kernel wrote for every chunk at once, so a run only
+// needs its first record, its length and its flags: a map run reads the
+// values as zero (kRunZeroValues) and, like a c run, drops its outputs
+// (kRunNoOutputs).  Segments are whole chunks of p.chunk tokens.
+
+namespace {
+
+struct ScanSegments {
+    int P = 0, group = 0, nseq = 0, nA = 0, nB = 0;
+    size_t off_slots = 0, off_runA = 0, off_runB = 0, table_bytes = 0, off_state = 0, total = 0;
+};
+
+ScanSegments plan_scan(const Problem &p, int nseq, int P) {
+    ScanSegments s;
+    if (P < 2 || nseq <= 0) return s;
+    s.P = P;
+    s.nseq = nseq;
+    s.group = 2 * P - 3;
+    s.nA = nseq * s.group;
+    s.nB = nseq * (P - 1);
+    size_t off = 0;
+    s.off_slots = off;
+    off = align256(off + (size_t)nseq * sizeof(int));
+    s.off_runA = off;
+    off = align256(off + (size_t)s.nA * sizeof(ScanRun));
+    s.off_runB = off;
+    off = align256(off + (size_t)s.nB * sizeof(ScanRun));
+    s.table_bytes = off;
+    s.off_state = off;
+    off += (size_t)s.nA * p.HV * kSlotFloats * sizeof(float);
+    s.total = off;
+    return s;
+}
+
+// dk = dv = 128 (the combine's state), the tensor-core scan, not forced
+// onto the CUDA-core kernels
+bool scan_segmentable(const Problem &p, unsigned flags) {
+    return !(flags & (GDR_FLAG_NO_SEGMENTS | GDR_FLAG_FORCE_GENERIC)) && p.dk == kD &&
+           p.dv == kD && scan_tc_supported(p);
+}
+
+}  // namespace
+
+int scan_segment_count(const Problem &p, unsigned flags) {
+    if (!scan_segmentable(p, flags) || p.B <= 0 || p.T < 2) return 0;
+    return dense_segments(p, flags, p.chunk);
+}
+
+int scan_varlen_segment_count(const Problem &p, const int *lengths, int n, unsigned flags,
+                              std::vector<char> *cut) {
+    cut->assign((size_t)std::max(n, 0), 0);
+    if (!scan_segmentable(p, flags) || n <= 0) return 0;
+    return choose_list_segments(p, lengths, n, flags, p.chunk, cut);
+}
+
+size_t scan_segmented_bytes(const Problem &p, int nseq, int P) {
+    return plan_scan(p, nseq, P).total;
+}
+
+cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t rec_floats,
+                                  const ScanSeq *seqs, int nseq, int P, void *workspace,
+                                  cudaStream_t stream) {
+    const ScanSegments s = plan_scan(p, nseq, P);
+    if (s.P != P || s.total == 0) return cudaErrorInvalidValue;
+    const int C = p.chunk;
+    for (int i = 0; i < nseq; ++i)
+        if (effective_segments(seqs[i].T, P, C) != P) return cudaErrorInvalidValue;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    float *state = reinterpret_cast<float *>(ws + s.off_state);
+
+    std::vector<unsigned char> host(s.table_bytes, 0);
+    int *slots = reinterpret_cast<int *>(host.data() + s.off_slots);
+    ScanRun *runA = reinterpret_cast<ScanRun *>(host.data() + s.off_runA);
+    ScanRun *runB = reinterpret_cast<ScanRun *>(host.data() + s.off_runB);
+    int a = 0, bb = 0;
+    for (int b = 0; b < nseq; ++b) {
+        const ScanSeq &sq = seqs[b];
+        slots[b] = sq.slot;
+        const int base = b * s.group;
+        const int per = ((sq.T + C - 1) / C + P - 1) / P;  // chunks per segment
+        auto run = [&](int q, int slot_j, int flags) {
+            const int c0 = q * per;
+            ScanRun r;
+            r.tok0 = sq.tok0 + (long long)c0 * C;
+            r.rec_base = sq.rec_base + (long long)c0 * sq.c_stride;
+            r.T = std::min(sq.T, (q + 1) * per * C) - c0 * C;
+            r.slot = base + slot_j;
+            r.hv_stride = sq.hv_stride;
+            r.c_stride = sq.c_stride;
+            r.flags = flags;
+            r.pad = 0;
+            return r;
+        };
+        runA[a++] = run(0, 0, 0);
+        for (int q = 1; q <= P - 2; ++q) {
+            runA[a++] = run(q, 2 * q - 1, kRunZeroValues | kRunNoOutputs);  // M_q
+            runA[a++] = run(q, 2 * q, kRunNoOutputs);                       // c_q
+        }
+        for (int q = 1; q <= P - 1; ++q) runB[bb++] = run(q, 2 * (q - 1), 0);
+    }
+    // pageable source: the call returns once the bytes have been taken
+    cudaError_t e = cudaMemcpyAsync(ws, host.data(), s.table_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+
+    trace_begin(kKernSegInit, stream);
+    gdr_segment_init<<<(unsigned)(4 * s.nA * p.HV), kInitThreads, 0, stream>>>(
+        p.h0, reinterpret_cast<const int *>(ws + s.off_slots), state, p.HV, s.group, nullptr, 0);
+    trace_end(kKernSegInit, stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    Problem wave = p;
+    wave.h0 = state;
+    wave.ht = state;
+    e = launch_chunk_scan_runs(wave, records, rec_floats,
+                               reinterpret_cast<const ScanRun *>(ws + s.off_runA), s.nA, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_combine(p, state, nseq, P, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_chunk_scan_runs(wave, records, rec_floats,
+                               reinterpret_cast<const ScanRun *>(ws + s.off_runB), s.nB, stream);
+    if (e != cudaSuccess) return e;
+    std::vector<int> sl((size_t)nseq);
+    for (int b = 0; b < nseq; ++b) sl[b] = seqs[b].slot;
+    return copy_final_states(p, state, sl, P, stream);
 }
 
 }  // namespace gdr

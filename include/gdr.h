@@ -97,9 +97,10 @@ typedef enum gdr_dtype {
 #define GDR_FLAG_SCALAR_GATE 4u
 /*
  * Segmented state scan (gdr_forward, gdr_forward_ex, gdr_workspace_bytes; the
- * tensor-core route only).  The chunk-to-chunk state carry is serial, one CTA
- * per (batch, value head) walking its chunks in order, so a small batch x
- * heads leaves most SMs idle.  The route then cuts the sequence into P
+ * tensor-core prefill, and the chunked prefill's state scan on the tensor
+ * cores when dk = dv = 128).  The chunk-to-chunk state carry is serial, one
+ * CTA per (batch, value head) walking its chunks in order, so a small batch
+ * x heads leaves most SMs idle.  The route then cuts the sequence into P
  * segments of whole chunks.  Over a segment the recurrence is an affine map
  * of the state, S_end = M S_start + c (M [dk][dk] from k, g and beta alone),
  * which is how the chunk carry of the second commit summary of "Reorder
@@ -118,6 +119,14 @@ typedef enum gdr_dtype {
  * value head).  Results agree with the unsegmented route to within the
  * tolerance of the route, not bit for bit (the states of later segments
  * are reached through the maps).
+ *
+ * On the chunked prefill (f32 q/k/v, or a chunk other than 64) every chunk's
+ * records are built at once as before and only the state scan is cut: its
+ * runs are scan CTAs over those records (the map runs read the values as
+ * zero), segments are whole chunks of the call's chunk length, and the
+ * launches are the prep, the set-up, the first scan wave, the combine and
+ * the second scan wave.  GDR_FLAG_FORCE_GENERIC (the CUDA-core scan) and
+ * dk or dv other than 128 never segment.
  *
  * GDR_FLAG_NO_SEGMENTS: never segment.
  * GDR_FLAG_SEGMENTS(n): segment into at most n pieces (2 <= n <= 255;
@@ -290,12 +299,14 @@ GDR_API gdr_status gdr_forward_host(const void *q, const void *k, const void *v,
  * prefill (chunk prep, then the state scan on the tensor cores unless
  * GDR_FLAG_FORCE_GENERIC); the outputs equal those of N such calls with
  * GDR_FLAG_NO_SEGMENTS bit for bit, except on the sequences cut below.
- * Long tensor-core sequences may take the segmented state scan (see
- * GDR_FLAG_SEGMENTS): automatically the largest P >= 3 for which HV CTAs
- * per whole-walking prefill sequence plus HV (2P - 3) per cut one fit on
- * the device's SMs at once, cutting the sequences of at least 8P chunks
- * that spread over exactly P segments; GDR_FLAG_SEGMENTS(n) cuts every
- * prefill sequence that spreads over exactly n; GDR_FLAG_NO_SEGMENTS none.
+ * Long prefill sequences may take the segmented state scan (see
+ * GDR_FLAG_SEGMENTS), those of the tensor-core prefill and those of the
+ * chunked prefill's tensor-core scan each chosen among their own kind:
+ * automatically the largest P >= 3 for which HV CTAs per whole-walking
+ * sequence plus HV (2P - 3) per cut one fit on the device's SMs at once,
+ * cutting the sequences of at least 8P chunks that spread over exactly P
+ * segments; GDR_FLAG_SEGMENTS(n) cuts every prefill sequence that spreads
+ * over exactly n; GDR_FLAG_NO_SEGMENTS none.
  * A cut sequence agrees with the unsegmented result within the route's
  * tolerance, not bit for bit.
  * Enqueued on `stream`: one host-to-device copy of the batch's tables (from

@@ -112,11 +112,6 @@ def test_segmented_scan_workspace(lib):
     assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 1,
                                    seg3 | GDR_FLAG_NO_SEGMENTS) == 0
     assert lib.gdr_workspace_bytes(1, 64, 1, 2, 128, 128, 64, 1, seg3) == 0   # one chunk
-    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, seg3) > 0  # chunk 32: CUDA cores
-    assert (lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, seg3)
-            == lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 32, 1, 0))
-    assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 0, seg3) == \
-        lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 0, 0)          # f32: CUDA cores
     # no device here, so the automatic choice never segments
     assert lib.gdr_workspace_bytes(1, 4096, 16, 32, 128, 128, 64, 1, 0) == 0
     # missing or short workspace: rejected before any launch
@@ -126,6 +121,52 @@ def test_segmented_scan_workspace(lib):
     assert call(lib, ws=FAKE + (9 << 30), ws_bytes=need - 1, **kw) == 5
     with pytest.raises(ValueError):
         gdr_flag_segments(1)
+
+
+def test_scan_route_segmented_workspace(lib):
+    """The chunk-record route (f32 q/k/v, or chunk 32): forced segments add
+    2P - 3 f32 states per (batch, value head) and small run tables after the
+    records; none with GDR_FLAG_NO_SEGMENTS, on the CUDA-core scan
+    (GDR_FLAG_FORCE_GENERIC), for dk != 128, or with one chunk."""
+    from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_GENERIC, GDR_FLAG_NO_SEGMENTS,
+                                               gdr_flag_segments)
+    state = 128 * 128 * 4
+    for B, T, HV, chunk, dt, P, P_eff in [(1, 4096, 32, 32, 1, 3, 3), (1, 4096, 32, 64, 0, 3, 3),
+                                          (2, 1000, 4, 64, 0, 5, 4), (1, 300, 2, 16, 0, 7, 7),
+                                          (1, 200, 2, 64, 0, 2, 2)]:
+        ws = lambda f: lib.gdr_workspace_bytes(B, T, HV // 2, HV, 128, 128, chunk, dt, f)
+        rec = ws(0 if P_eff < 3 else GDR_FLAG_NO_SEGMENTS)
+        assert rec > 0
+        extra = ws(gdr_flag_segments(P)) - ((rec + 255) // 256 * 256)
+        states = B * (2 * P_eff - 3) * HV * state
+        assert states < extra <= states + 3 * 256 + B * 3 * P_eff * 32, (B, T, HV, chunk, P)
+        assert ws(gdr_flag_segments(P) | GDR_FLAG_FORCE_GENERIC) == ws(GDR_FLAG_FORCE_GENERIC)
+    seg3 = gdr_flag_segments(3)
+    f32 = lambda dk, T, f: lib.gdr_workspace_bytes(1, T, 1, 2, dk, dk, 64, 0, f)
+    assert f32(64, 4096, seg3) == f32(64, 4096, 0)       # dk = 64: not segmented
+    assert f32(128, 64, seg3) == f32(128, 64, 0)         # one chunk
+    assert f32(128, 4096, seg3 | GDR_FLAG_NO_SEGMENTS) == f32(128, 4096, GDR_FLAG_NO_SEGMENTS)
+    # no device here, so the automatic choice never segments
+    assert f32(128, 4096, 0) == f32(128, 4096, GDR_FLAG_NO_SEGMENTS)
+
+
+def test_varlen_scan_route_segmented_workspace(lib):
+    """Packed f32 batches: the forced count cuts every chunk-record
+    sequence spread over exactly P segments, each with 2P - 3 states per value
+    head; decode tokens and shorter sequences are not cut."""
+    from channelwise_gated_delta_gb300 import GDR_FLAG_NO_SEGMENTS, gdr_flag_segments
+    HV, state = 4, 128 * 128 * 4
+    ws = lambda cu, f: lib.gdr_varlen_workspace_bytes(cu_array(cu), len(cu) - 1, 2, HV, 128,
+                                                      128, 64, 0, f)
+    cu = [0, 1000, 1001, 1701, 1741]   # 16 chunks, one token, 11 chunks, 1 chunk
+    base = ws(cu, GDR_FLAG_NO_SEGMENTS)
+    assert ws(cu, 0) == base
+    assert ws(cu, gdr_flag_segments(5)) == base   # 16 and 11 chunks both spread over 4
+    for P, cut in [(3, 2), (2, 2), (4, 2), (16, 1), (11, 1)]:
+        extra = ws(cu, gdr_flag_segments(P)) - (base + 255) // 256 * 256
+        states = cut * (2 * P - 3) * HV * state
+        assert states < extra <= states + 3 * 256 + cut * 3 * P * 32, (P, extra)
+    assert ws([0, 40, 80], gdr_flag_segments(3)) == ws([0, 40, 80], 0)
 
 
 @pytest.mark.parametrize("T", [65, 128, 129, 300, 1000, 4096, 4097])

@@ -2,14 +2,16 @@
 tcgen05 products in BF16x3, the state in tensor memory), the route of float32
 q/k/v and of the shapes the fused bf16 kernel does not take: parity with the
 fp64 oracle at the float32 bound, agreement with the CUDA-core scan
-(GDR_FLAG_FORCE_GENERIC), and the route actually taken."""
+(GDR_FLAG_FORCE_GENERIC), the route actually taken, and the same scan cut
+into segments (forced and automatic, dense and packed, with and without
+states, in place)."""
 import pytest
 import torch
 
 import oracle
 from channelwise_gated_delta_gb300 import (GDR_FLAG_FORCE_GENERIC, GDR_FLAG_NO_SEGMENTS,
-                                           gdr_device_check, gdr_forward, gdr_forward_varlen,
-                                           gdr_trace_enable, gdr_trace_read)
+                                           gdr_device_check, gdr_flag_segments, gdr_forward,
+                                           gdr_forward_varlen, gdr_trace_enable, gdr_trace_read)
 from channelwise_gated_delta_gb300.inputs import WORKLOADS, draw, draw_workload, pack, to_f64
 from tests.parity_util import assert_close, to_cuda
 
@@ -118,6 +120,123 @@ def test_ragged_b8_packed_f32():
     finally:
         gdr_trace_enable(False)
     assert "gdr_chunk_scan_tc" in tr, tr
+    for n, d in enumerate(seqs):
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d[x]) for x in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d["h0"]))
+        assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.float32)
+        assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.float32)
+
+
+# ------------------------------------------- the segmented scan on this route
+def forward_seg(d, chunk, flags, inplace=False, store_ht=True):
+    c = to_cuda(d)
+    ht = c["h0"] if (inplace and c["h0"] is not None) else None
+    gdr_trace_enable(True)
+    try:
+        out, ht = gdr_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], ht=ht,
+                              chunk=chunk, flags=flags, store_ht=store_ht)
+        gdr_device_check()
+        tr = gdr_trace_read()
+    finally:
+        gdr_trace_enable(False)
+    return out, ht, tr
+
+
+def check_seg(d, chunk, segments, inplace=False):
+    """Forced segments against the fp64 oracle at the float32 bound; the
+    launches are the prep, the two scan waves, the set-up and (three or more
+    segments) the combine."""
+    ref_o, ref_h = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                     to_f64(d["h0"]))
+    out, ht, tr = forward_seg(d, chunk, gdr_flag_segments(segments), inplace=inplace)
+    assert "gdr_segment_init" in tr and tr["gdr_chunk_scan_tc"][0] == 2, tr
+    eff = len(oracle.segment_bounds(d["q"].shape[1], chunk, segments))
+    assert ("gdr_segment_combine" in tr) == (eff >= 3), tr
+    assert_close("o", out, ref_o, d["q"].dtype)
+    assert_close("ht", ht, ref_h, d["q"].dtype)
+    return out, ht
+
+
+@pytest.mark.parametrize("segments", [2, 3, 5])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_segmented_scan_forced(segments, chunk):
+    check_seg(draw(2, 1000, 2, 4, 128, 128, dtype=torch.float32, seed=530 + segments + chunk),
+              chunk, segments)
+
+
+def test_segmented_scan_many_segments_ragged():
+    """Eleven segments of one 32-token chunk and a ragged 8-token tail."""
+    check_seg(draw(1, 328, 1, 2, 128, 128, dtype=torch.float32, seed=540), 32, 11)
+
+
+def test_segmented_scan_conditioning_stress():
+    """Slow decay and beta near 1 over 2048 tokens: the maps M of the middle
+    segments carry the state almost undamped."""
+    check_seg(draw(1, 2048, 2, 4, 128, 128, dtype=torch.float32, seed=541, g_mu=-3.0,
+                   beta_mu=2.0, beta_sigma=0.5), 64, 6)
+
+
+def test_segmented_scan_in_place_and_bf16_off_shape():
+    """In place (ht = h0), and bf16 q/k/v on chunk 32 (the chunk-record route
+    for the model's head shape)."""
+    check_seg(draw(1, 900, 2, 4, 128, 128, dtype=torch.float32, seed=542), 64, 4, inplace=True)
+    check_seg(draw(1, 900, 2, 4, 128, 128, dtype=torch.bfloat16, seed=543), 32, 3)
+
+
+def test_segmented_scan_without_states():
+    d = draw(2, 600, 1, 2, 128, 128, dtype=torch.float32, h0=False, seed=544)
+    ref_o, _ = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")), None)
+    out, ht, tr = forward_seg(d, 64, gdr_flag_segments(3), store_ht=False)
+    assert ht is None and "gdr_segment_combine" in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+
+
+def test_segmented_scan_automatic():
+    """One sequence of 2048 tokens on four value heads leaves most SMs idle:
+    the automatic choice segments it; with GDR_FLAG_NO_SEGMENTS it walks
+    whole; both within the bound."""
+    d = draw(1, 2048, 2, 4, 128, 128, dtype=torch.float32, seed=545)
+    ref_o, ref_h = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                     to_f64(d["h0"]))
+    out, ht, tr = forward_seg(d, 64, 0)
+    assert "gdr_segment_combine" in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+    assert_close("ht", ht, ref_h, torch.float32)
+    out2, ht2, tr2 = forward_seg(d, 64, GDR_FLAG_NO_SEGMENTS)
+    assert "gdr_segment_init" not in tr2, tr2
+    assert_close("o", out2, ref_o, torch.float32)
+
+
+def test_segmented_scan_not_taken():
+    """dk = 64 (the combine holds 128 x 128 states) and the CUDA-core scan
+    walk whole whatever the flags."""
+    for d, flags in [(draw(1, 700, 2, 4, 64, 64, dtype=torch.float32, seed=546), 0),
+                     (draw(1, 700, 2, 4, 128, 128, dtype=torch.float32, seed=547),
+                      GDR_FLAG_FORCE_GENERIC)]:
+        _, _, tr = forward_seg(d, 64, gdr_flag_segments(3) | flags)
+        assert "gdr_segment_init" not in tr, tr
+
+
+@pytest.mark.parametrize("segments", [2, 4])
+def test_segmented_scan_packed(segments):
+    """A packed f32 batch: the sequences over exactly `segments` segments are
+    cut, a short one and a single token are not, and the slots are not in
+    the order the longest-first plan runs them (per-sequence final states)."""
+    gen = torch.Generator()
+    gen.manual_seed(550 + segments)
+    seqs = [draw(1, L, 2, 4, 128, 128, dtype=torch.float32, generator=gen)
+            for L in (700, 1, 1000, 40)]
+    packed, cu = pack(seqs)
+    c = to_cuda(packed)
+    gdr_trace_enable(True)
+    try:
+        out, ht = gdr_forward_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, h0=c["h0"],
+                                     chunk=64, flags=gdr_flag_segments(segments))
+        gdr_device_check()
+        tr = gdr_trace_read()
+    finally:
+        gdr_trace_enable(False)
+    assert "gdr_segment_init" in tr and tr["gdr_chunk_scan_tc"][0] == 3, tr
     for n, d in enumerate(seqs):
         ref_o, ref_h = oracle.recurrence(*(to_f64(d[x]) for x in ("q", "k", "v", "g", "beta")),
                                          to_f64(d["h0"]))
