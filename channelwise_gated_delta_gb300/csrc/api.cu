@@ -375,7 +375,7 @@ const char *kKernelNames[gdr::kNumKernels] = {"gdr_decode_kernel", "gdr_chunk_pr
                                               "gdr_segment_init",  "gdr_segment_combine",
                                               "gdr_tree_tc",       "gdr_tree_path_kernel",
                                               "gdr_tree_gram_kernel", "gdr_tree_solve_kernel",
-                                              "gdr_chunk_scan_tc"};
+                                              "gdr_chunk_scan_tc", "gdr_chunk_prep_tc"};
 
 }  // namespace
 

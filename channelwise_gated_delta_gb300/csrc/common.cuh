@@ -75,7 +75,8 @@ enum KernelId {
     kKernTreeGram = 8,
     kKernTreeSolve = 9,
     kKernChunkScanTc = 10,
-    kNumKernels = 11
+    kKernChunkPrepTc = 11,
+    kNumKernels = 12
 };
 // Called by the launchers around each launch; no-ops unless tracing is on.
 void trace_begin(int kernel, cudaStream_t stream);
@@ -140,6 +141,13 @@ cudaError_t launch_generic_prefill_varlen(const Problem &p, void *records, const
 bool scan_tc_supported(const Problem &p);
 cudaError_t launch_chunk_scan_tc(const Problem &p, const float *records, size_t rec_floats,
                                  const int4 *seqs, int nseq, cudaStream_t stream);
+// The chunk prep of that route on the tensor cores (prep_tc.cu; dk = dv =
+// 128, chunk 64): the same records as gdr_chunk_prep's tensor-core layout,
+// rec_floats floats each; dense batches (chunks == nullptr) or the nchunks
+// chunks {first row, length} of a packed batch.
+bool prep_tc_supported(const Problem &p);
+cudaError_t launch_chunk_prep_tc(const Problem &p, float *records, size_t rec_floats,
+                                 const int2 *chunks, int nchunks, cudaStream_t stream);
 // One run of that scan in a segmented launch: tokens tok0 .. tok0 + T - 1,
 // whose chunk c of value head hv has its record at rec_base + hv * hv_stride
 // + c * c_stride; the state starts from slot `slot` of p.h0 and ends in slot

@@ -710,6 +710,19 @@ cudaError_t launch_generic_t(const Problem &p, void *workspace, const int2 *chun
     const size_t sp = prep_smem_bytes(p.dk, p.dv, C);
     const size_t ss = scan_smem_bytes(p.dk, C);
     cudaError_t e;
+    if (TCREC && !TREE && prep_tc_supported(p)) {
+        // the prep on the tensor cores, then the scan below
+        const ChunkLayout lay{C, p.dk, p.dv};
+        e = launch_chunk_prep_tc(p, ws, lay.floats(), chunks, nchunks, stream);
+        if (e != cudaSuccess) return e;
+        if (seg.whole) {
+            e = launch_chunk_scan_tc(p, ws, lay.floats(), seqs, p.B, stream);
+            if (e != cudaSuccess) return e;
+        }
+        if (seg.P >= 2 && seg.n > 0)
+            e = launch_scan_segmented(p, ws, lay.floats(), seg.seqs, seg.n, seg.P, seg.ws, stream);
+        return e;
+    }
     e = cudaFuncSetAttribute(gdr_chunk_prep<Tin, TREE, TCREC>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e != cudaSuccess) return e;

@@ -242,3 +242,49 @@ def test_segmented_scan_packed(segments):
                                          to_f64(d["h0"]))
         assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.float32)
         assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.float32)
+
+
+# ------------------------------------------ the chunk prep on the tensor cores
+def test_prep_mixed_fast_and_exact_chunks():
+    """f32, dk = dv = 128, chunk 64 (the tensor-core prep): the factored gram
+    for most chunks, the exact pairwise decays for chunks 1 and 4, whose
+    log-decay is scaled so that their half-chunk spans pass 60 nats, and a
+    ragged last chunk; against the oracle, and the launches of the route."""
+    d = draw(2, 64 * 6 + 17, 2, 4, 128, 128, dtype=torch.float32, seed=560)
+    g = d["g"].clone()
+    g[:, 64:128] *= 12.0
+    g[:, 256:320] *= 12.0
+    d["g"] = g
+    ref_o, ref_h = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                     to_f64(d["h0"]))
+    out, ht, tr = forward(d, 64)
+    assert "gdr_chunk_prep_tc" in tr and "gdr_chunk_prep" not in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+    assert_close("ht", ht, ref_h, torch.float32)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129])
+def test_prep_lengths_around_the_chunk(T):
+    """Chunk lengths 1 .. 64 through the tensor-core prep (T = 1 forced onto
+    the chunked route), with and without h0."""
+    from channelwise_gated_delta_gb300 import GDR_FLAG_FORCE_CHUNKED
+    for h0 in (True, False):
+        d = draw(1, T, 1, 2, 128, 128, dtype=torch.float32, h0=h0, seed=570 + T)
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d["h0"]))
+        out, ht, tr = forward(d, 64, flags=GDR_FLAG_FORCE_CHUNKED)
+        assert "gdr_chunk_prep_tc" in tr, tr
+        assert_close("o", out, ref_o, torch.float32)
+        assert_close("ht", ht, ref_h, torch.float32)
+
+
+def test_prep_scalar_gate():
+    """A scalar gate (one log-decay per token and value head) through the
+    tensor-core prep."""
+    d = draw(1, 300, 2, 4, 128, 128, dtype=torch.float32, seed=580, scalar_gate=True)
+    ref_o, ref_h = oracle.scalar_gate_recurrence(
+        *(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")), to_f64(d["h0"]))
+    out, ht, tr = forward(d, 64)
+    assert "gdr_chunk_prep_tc" in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+    assert_close("ht", ht, ref_h, torch.float32)
