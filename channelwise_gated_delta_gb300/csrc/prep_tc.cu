@@ -103,6 +103,9 @@ __device__ __forceinline__ void pt_split8(const float (&x)[8], uint4 &hi, uint4 
     pt_split(x[4], x[5], hi.z, lo.z);
     pt_split(x[6], x[7], hi.w, lo.w);
 }
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void pt_load8(const float *p, float (&x)[8]) {
     const float4 a = *reinterpret_cast<const float4 *>(p);
     const float4 b = *reinterpret_cast<const float4 *>(p + 4);
@@ -173,25 +176,52 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     }
     if (warp == 0) tmem_alloc(tslot, 256);
 
+    // this thread's rows of k and q for step 2 (item tid + 256 u: row
+    // item % 64, channels 8 (item / 64) ..), loaded before anything waits;
+    // the same rows of v go to L2 for the right-hand side built in step 3
+    // (rows past L read row L - 1 and are zeroed after the loads, so that
+    // every load is issued unconditionally and all are in flight at once)
+    float kq[4][16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int item = tid + kPtThreads * u;
+        const int r = item & 63, i0 = 8 * (item >> 6);
+        const int rc = min(r, L - 1);
+        const size_t tk = ((tr0 + rc) * a.HK + hk) * kPtD + i0;
+        float k8[8], q8[8];
+        pt_load8(kp + tk, k8);
+        pt_load8(qp + tk, q8);
+        prefetch_l2(vp + ((tr0 + rc) * HV + hv) * kPtD + i0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            kq[u][e] = k8[e];
+            kq[u][8 + e] = q8[e];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int r = (tid + kPtThreads * u) & 63;
+        if (r >= L) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) kq[u][e] = 0.f;
+        }
+    }
+
     // ---- 1. prefix sums of the log-decay (threads 0-127: channel i), beta
     bool in_range = true;
     if (tid < kPtD) {
         const int i = tid;
+        float x[kPtC];
+#pragma unroll
+        for (int r = 0; r < kPtC; ++r) {
+            const size_t row = tr0 + min(r, L - 1);
+            x[r] = a.g_scalar ? a.g[row * HV + hv] : a.g[(row * HV + hv) * kPtD + i];
+        }
         float run = 0.f;
-        for (int r0 = 0; r0 < kPtC; r0 += 16) {
-            float x[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int r = r0 + u;
-                x[u] = 0.f;
-                if (r < L)
-                    x[u] = a.g_scalar ? a.g[(tr0 + r) * HV + hv] : a.g[((tr0 + r) * HV + hv) * kPtD + i];
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                run += x[u];
-                Gs[(r0 + u) * kPtLdg + i] = run;
-            }
+        for (int r = 0; r < kPtC; ++r) {
+            run += r < L ? x[r] : 0.f;  // a zero gate past L keeps G flat
+            Gs[r * kPtLdg + i] = run;
         }
         const int m = (L - 1) / 2;
         const float gm = Gs[m * kPtLdg + i], gl = Gs[(L - 1) * kPtLdg + i];
@@ -217,17 +247,15 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     // ---- 2. operand tiles and the Qt, Kh records; item = (row r, channels
     // 8o .. 8o + 7), consecutive threads on consecutive rows so that eight
     // of them fill one 128-byte core matrix
+#pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int item = tid + kPtThreads * u;
         const int r = item & 63, o = item >> 6, i0 = 8 * o;
         float kk[8], qq[8], G[8];
-        if (r < L) {
-            const size_t tk = ((tr0 + r) * a.HK + hk) * kPtD + i0;
-            pt_load8(kp + tk, kk);
-            pt_load8(qp + tk, qq);
-        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kk[e] = qq[e] = 0.f;
+        for (int e = 0; e < 8; ++e) {
+            kk[e] = kq[u][e];
+            qq[e] = kq[u][8 + e];
         }
         pt_load8(Gs + r * kPtLdg + i0, G);
         const float br = bsv[r];
@@ -356,25 +384,29 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         __syncthreads();  // G and the staged P read
     }
 
-    // diag(beta) V into the G region (G is no longer read)
-    for (int u = 0; u < 4; ++u) {
-        const int item = tid + kPtThreads * u;
-        const int s = item & 63, o = item >> 6, j0 = 8 * o;
-        float x[8];
-        if (s < L) {
-            pt_load8(vp + ((tr0 + s) * HV + hv) * kPtD + j0, x);
-            const float bs = bsv[s];
+    // diag(beta) V into the G region (G is no longer read); the four rows'
+    // loads in flight together
+    {
+        float vv[4][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] *= bs;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        for (int u = 0; u < 4; ++u) {
+            const int item = tid + kPtThreads * u;
+            const int s = item & 63, j0 = 8 * (item >> 6);
+            pt_load8(vp + ((tr0 + min(s, L - 1)) * HV + hv) * kPtD + j0, vv[u]);
         }
-        uint4 h, l;
-        pt_split8(x, h, l);
-        const uint32_t off = kmajor_off(s, j0, kPtD);
-        *reinterpret_cast<uint4 *>(smem + kPtGs + off) = h;
-        *reinterpret_cast<uint4 *>(smem + kPtGs + 16384 + off) = l;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int item = tid + kPtThreads * u;
+            const int s = item & 63, j0 = 8 * (item >> 6);
+            const float bs = bsv[s];  // zero past L
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vv[u][e] *= bs;
+            uint4 h, l;
+            pt_split8(vv[u], h, l);
+            const uint32_t off = kmajor_off(s, j0, kPtD);
+            *reinterpret_cast<uint4 *>(smem + kPtGs + off) = h;
+            *reinterpret_cast<uint4 *>(smem + kPtGs + 16384 + off) = l;
+        }
     }
 
     // ---- 4. A and P out of tensor memory: warp w reads lanes 32 (w % 4) ..,
@@ -439,24 +471,47 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     }
     __syncthreads();
     float *Xs = reinterpret_cast<float *>(smem + kPtX);
+#pragma unroll
     for (int I = 1; I < 4; ++I) {
-        // X_IJ = sum over rows u of blocks J .. I-1 of A[16I + r][u] T[u][16J + c]
-        // (T is zero above its diagonal, so the sum may start at 16J)
-        for (int idx = tid; idx < 256 * I; idx += kPtThreads) {
-            const int J = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-            float acc = 0.f;
-            for (int uu = 16 * J; uu < 16 * I; ++uu)
-                acc = fmaf(As[(16 * I + r) * kPtLda + uu], Tf[uu * kPtLda + 16 * J + c], acc);
-            Xs[idx] = acc;
+        // X_IJ = sum over the blocks K = J .. I-1 of A_IK T_KJ (T is zero
+        // above its diagonal); a thread takes a 1 x 4 strip (row r, columns
+        // 4 c4 ..) of one block J
+        for (int st = tid; st < 64 * I; st += kPtThreads) {
+            const int J = st >> 6, r = (st >> 2) & 15, c4 = st & 3;
+            const float *arow = As + (16 * I + r) * kPtLda;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int K = J; K < I; ++K) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int uu = 16 * K + t;
+                    const float av = arow[uu];
+                    const float4 tv = *reinterpret_cast<const float4 *>(Tf + uu * kPtLda + 16 * J + 4 * c4);
+                    acc.x = fmaf(av, tv.x, acc.x);
+                    acc.y = fmaf(av, tv.y, acc.y);
+                    acc.z = fmaf(av, tv.z, acc.z);
+                    acc.w = fmaf(av, tv.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(Xs + (J << 8) + (r << 4) + 4 * c4) = acc;
         }
         __syncthreads();
-        // T_IJ = -T_II X_IJ (T_II unit lower)
-        for (int idx = tid; idx < 256 * I; idx += kPtThreads) {
-            const int J = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-            float acc = 0.f;
-            for (int rr = 0; rr <= r; ++rr)
-                acc = fmaf(Tf[(16 * I + r) * kPtLda + 16 * I + rr], Xs[(J << 8) + (rr << 4) + c], acc);
-            Tf[(16 * I + r) * kPtLda + 16 * J + c] = -acc;
+        // T_IJ = -T_II X_IJ (T_II unit lower, stored with zeros above its
+        // diagonal)
+        for (int st = tid; st < 64 * I; st += kPtThreads) {
+            const int J = st >> 6, r = (st >> 2) & 15, c4 = st & 3;
+            const float *trow = Tf + (16 * I + r) * kPtLda + 16 * I;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const float tv = trow[rr];
+                const float4 xv = *reinterpret_cast<const float4 *>(Xs + (J << 8) + (rr << 4) + 4 * c4);
+                acc.x = fmaf(tv, xv.x, acc.x);
+                acc.y = fmaf(tv, xv.y, acc.y);
+                acc.z = fmaf(tv, xv.z, acc.z);
+                acc.w = fmaf(tv, xv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Tf + (16 * I + r) * kPtLda + 16 * J + 4 * c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
@@ -500,7 +555,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         issued = true;
     }
 
-    // ---- 7. Wk and Wv: warps 0, 1 (Wk) and 4, 5 (Wv) read the 64 rows
+    // ---- 7. Wk and Wv: warps 0, 1 (Wk) and 4, 5 (Wv) read the 64 rows;
+    // Wv is staged in the R region (free once the gram is done)
+    float *Wst = reinterpret_cast<float *>(smem + kPtR);
     const int qd = warp & 3, hf = warp >> 2;
     if (qd < 2) {
         wait(1, 0);
@@ -523,12 +580,27 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
                         *reinterpret_cast<uint4 *>(rec_wk + 16384 + off) = l;
                     }
                 } else {
+                    // row r into the staging tile, 16-byte chunks XORed with
+                    // r % 8 so that eight rows at once hit distinct banks
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        *reinterpret_cast<float4 *>(rec_wv + r * kPtD + c0 + 4 * c4) =
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const int ch = ((c0 >> 2) + c4) ^ (r & 7);
+                        *reinterpret_cast<float4 *>(Wst + r * kPtD + 4 * ch) =
                             make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+                    }
                 }
             }
+        }
+    }
+    __syncthreads();
+    // Wv from the staging tile to its record, each warp two full rows per store
+    if (!*abort_flag) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = tid + kPtThreads * u;  // float4 index in [64][32]
+            const int r = idx >> 5, ch = idx & 31;
+            *reinterpret_cast<float4 *>(rec_wv + r * kPtD + 4 * ch) =
+                *reinterpret_cast<const float4 *>(Wst + r * kPtD + 4 * (ch ^ (r & 7)));
         }
     }
 
