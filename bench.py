@@ -60,7 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["all", "prefill", "decode", "prefill_t4k", "tree",
-                                           "ragged_f32"],
+                                           "ragged_f32", "prefill_f32_t16k",
+                                           "prefill_f32_t4k"],
                     default="all",
                     help="prefill: the headline only; decode: only the decode measurement "
                          "(printed as its own line, for profiling the decode kernel); "
@@ -68,7 +69,8 @@ def parse_args():
                          "small-batch case the segmented state scan serves; tree: tree "
                          "verification of 8 beam trees of 512 draft tokens (its own line); "
                          "ragged_f32: the ragged float32 batch through the packed entry "
-                         "(its own line)")
+                         "(its own line); prefill_f32_t16k / prefill_f32_t4k: the long-"
+                         "prefill and the 4k-prefill shapes with float32 q/k/v (own lines)")
     ap.add_argument("--no-segments", action="store_true",
                     help="prefill workloads: one walk per head (GDR_FLAG_NO_SEGMENTS)")
     return ap.parse_args()
@@ -151,7 +153,8 @@ def src_sha(name):
 
 
 KERNEL_SOURCE = {"gdr_decode_kernel": "decode.cu", "gdr_chunk_prep": "prefill_generic.cu",
-                 "gdr_chunk_scan": "prefill_generic.cu", "gdr_prefill_fused": "prefill_tc.cu"}
+                 "gdr_chunk_scan": "prefill_generic.cu", "gdr_prefill_fused": "prefill_tc.cu",
+                 "gdr_chunk_prep_tc": "prep_tc.cu", "gdr_chunk_scan_tc": "scan_tc.cu"}
 
 
 def traffic_for(kernel):
@@ -547,6 +550,42 @@ def bench_ragged_f32(args, dev, hbm_peak, peak_kind):
                      tokens, bytes_step, "f32", ms, trace, clk, hbm_peak, peak_kind)
 
 
+def bench_f32_prefill(args, dev, hbm_peak, peak_kind, long):
+    """A prefill shape with float32 q/k/v through gdr_forward: the chunk prep
+    and the state scan on the tensor cores (BF16x3).  long: the long-prefill
+    stress shape (B4 T16384 HK16 HV32, slow decay, beta near 1, h0 given);
+    else the 4k prefill (B1 T4096, the configs' default decay and beta, h0 =
+    0), whose scan the automatic choice cuts into segments."""
+    from channelwise_gated_delta_gb300 import gdr_forward
+    from channelwise_gated_delta_gb300.inputs import draw
+    HK, HV, d = 16, 32, 128
+    if long:
+        B, T = 4, 16384
+        x = draw(B, T, HK, HV, d, d, dtype=torch.float32, seed=1, g_mu=-3.0, g_sigma=1.0,
+                 beta_mu=2.0, beta_sigma=0.5, h0=True, device=dev)
+    else:
+        B, T = 1, 4096
+        x = draw(B, T, HK, HV, d, d, dtype=torch.float32, seed=1, h0=False, device=dev)
+    out = torch.empty(B, T, HV, d, dtype=torch.float32, device=dev)
+    ht = torch.empty(B, HV, d, d, dtype=torch.float32, device=dev)
+
+    def step():
+        gdr_forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], out=out, ht=ht, chunk=64)
+
+    ms, trace, clk = timed_steps(args, dev, step)
+    per_token = 2 * HK * d * 4 + HV * d * 4 + HV * d * 4 + HV * 4 + HV * d * 4
+    bytes_step = B * T * per_token + (2 if long else 1) * B * HV * d * d * 4
+    if long:
+        return side_line(args, "GDR prefill tokens/s [prefill_t16k shape, f32 q/k/v]",
+                         "B4 T16384 HK16 HV32 dk=dv=128 chunk64, f32 q/k/v/g/beta/state, beta "
+                         "near 1, slow decay, h0 given; chunk prep and state scan on tcgen05",
+                         B * T, bytes_step, "f32", ms, trace, clk, hbm_peak, peak_kind)
+    return side_line(args, "GDR prefill tokens/s [prefill_t4k shape, f32 q/k/v]",
+                     "B1 T4096 HK16 HV32 dk=dv=128 chunk64, f32 q/k/v/g/beta/state, h0 = 0; "
+                     "chunk prep and state scan on tcgen05, scan segmented automatically",
+                     B * T, bytes_step, "f32", ms, trace, clk, hbm_peak, peak_kind)
+
+
 # ----------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -564,9 +603,11 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
     hbm_peak, _, peak_kind = load_peaks()
 
-    if args.workload in ("tree", "ragged_f32"):
+    if args.workload in ("tree", "ragged_f32", "prefill_f32_t16k", "prefill_f32_t4k"):
         if rank == 0:
-            fn = bench_tree if args.workload == "tree" else bench_ragged_f32
+            fn = {"tree": bench_tree, "ragged_f32": bench_ragged_f32,
+                  "prefill_f32_t16k": lambda *a: bench_f32_prefill(*a, long=True),
+                  "prefill_f32_t4k": lambda *a: bench_f32_prefill(*a, long=False)}[args.workload]
             print(json.dumps(fn(args, dev, hbm_peak, peak_kind)), flush=True)
         if ws > 1:
             import torch.distributed as dist
