@@ -74,6 +74,34 @@ def test_prefill_t16k_all_heads():
         assert_close("ht[%d]" % b, ht[b:b + 1], rh, w.dtype)
 
 
+@pytest.mark.slow
+def test_prefill_t16k_f32_all_heads():
+    """The long-prefill stress recipe at full size with float32 q/k/v (the
+    chunk prep and the state scan on the tensor cores, BF16x3), every
+    (batch, value head) of o and ht against the oracle at the float32 bound."""
+    w = WORKLOADS["prefill_t16k"]
+    d = draw(w.B, w.T, w.HK, w.HV, w.dk, w.dv, dtype=torch.float32, h0=True, seed=31,
+             g_mu=w.g_mu, g_sigma=w.g_sigma, beta_mu=w.beta_mu, beta_sigma=w.beta_sigma)
+    out, ht = run_gpu(d, w.chunk)
+    for b in range(w.B):
+        one = lambda x: to_f64(x[b:b + 1])
+        ro, rh = oracle.recurrence(*(one(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                   one(d["h0"]))
+        assert_close("o[%d]" % b, out[b:b + 1], ro, torch.float32)
+        assert_close("ht[%d]" % b, ht[b:b + 1], rh, torch.float32)
+
+
+@pytest.mark.slow
+def test_prefill_t16k_f32_few_heads_segmented():
+    """16384 float32 tokens on four value heads: the automatic choice cuts
+    the tensor-core scan into many segments (the maps chained over ~20
+    segments of the stress recipe); every head against the oracle."""
+    w = WORKLOADS["prefill_t16k"]
+    d = draw(1, w.T, 2, 4, w.dk, w.dv, dtype=torch.float32, h0=True, seed=32,
+             g_mu=w.g_mu, g_sigma=w.g_sigma, beta_mu=w.beta_mu, beta_sigma=w.beta_sigma)
+    check(d, w.chunk)
+
+
 # ------------------------------------------------------------ shapes and edges
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128), (32, 128)])
