@@ -216,6 +216,25 @@ def barrier(ws):
 
 
 # ----------------------------------------------------------------- GPU arm
+def timed_pass(steps, step, stream, dev, ws, traced):
+    """K steps between CUDA events on `stream`, a barrier and a device
+    synchronize on both sides; the library's launch trace on or off."""
+    from channelwise_gated_delta_gb300 import gdr_trace_enable
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(traced)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    gdr_trace_enable(False)
+    barrier(ws)
+    return t0.elapsed_time(t1)
+
+
 def bench_prefill(args, ws, rank, dev, name=PREFILL):
     from channelwise_gated_delta_gb300 import (GDR_FLAG_NO_SEGMENTS, gdr_forward, gdr_trace_enable,
                                                gdr_trace_read)
@@ -238,24 +257,17 @@ def bench_prefill(args, ws, rank, dev, name=PREFILL):
     gdr_trace_read()
     clocks = ClockSampler(dev.index if ws == 1 else int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
-    barrier(ws)
-    torch.cuda.synchronize(dev)
-    gdr_trace_enable(True)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    gdr_trace_enable(False)
-    barrier(ws)
+    # the K steps as a caller runs them, then the same K steps again with the
+    # library's launch trace (two events around each launch) for the
+    # kernels' own times and the launch count
+    ms = timed_pass(args.steps, step, stream, dev, ws, traced=False)
+    ms_traced = timed_pass(args.steps, step, stream, dev, ws, traced=True)
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
     trace = gdr_trace_read()
     ms = max_over_ranks(ms, ws)
     tokens = w.B * w.T * args.steps * ws
-    res = dict(w=w, ms=ms, tokens_per_s=tokens / (ms / 1e3), trace=trace, clocks=clk)
+    res = dict(w=w, ms=ms, ms_traced=ms_traced, tokens_per_s=tokens / (ms / 1e3), trace=trace,
+               clocks=clk)
 
     if not args.no_e2e:
         res["e2e"] = bench_prefill_e2e(args, w, d, out, ht, stream, dev, ws)
@@ -452,7 +464,8 @@ def bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind):
     line = {
         "metric": "GDR prefill tokens/s [prefill_t4k]", "value": round(pre["tokens_per_s"], 1),
         "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(pre["ms"] / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(pre["ms"] / args.steps, 4),
+        "ms_per_step_traced": round(pre["ms_traced"] / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "prefill B1 T4096 HK16 HV32 dk=dv=128 chunk64, bf16 q/k/v, "
                                "f32 g/beta, no h0, final state stored",
@@ -468,8 +481,9 @@ def bench_small_prefill(args, ws, rank, dev, hbm_peak, peak_kind):
 
 def timed_steps(args, dev, step):
     """W untimed steps, then K steps between CUDA events on the current
-    stream, with the library's launch trace and the SM clocks over them."""
-    from channelwise_gated_delta_gb300 import gdr_trace_enable, gdr_trace_read
+    stream (untraced: the value), the same K steps again with the library's
+    launch trace (the kernels' times), and the SM clocks over both."""
+    from channelwise_gated_delta_gb300 import gdr_trace_read
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -477,17 +491,10 @@ def timed_steps(args, dev, step):
     clocks = ClockSampler(dev.index)
     clocks.start()
     stream = torch.cuda.current_stream(dev)
-    gdr_trace_enable(True)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    gdr_trace_enable(False)
+    ms = timed_pass(args.steps, step, stream, dev, 1, traced=False)
+    timed_pass(args.steps, step, stream, dev, 1, traced=True)
     clk = clocks.stop()
-    return t0.elapsed_time(t1), gdr_trace_read(), clk
+    return ms, gdr_trace_read(), clk
 
 
 def side_line(args, metric, workload, tokens, bytes_step, dtype, ms, trace, clk, hbm_peak,
@@ -647,7 +654,8 @@ def main():
     line = {
         "metric": METRIC, "value": round(pre["tokens_per_s"], 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(pre["ms"] / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(pre["ms"] / args.steps, 4),
+        "ms_per_step_traced": round(pre["ms_traced"] / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": prefill_config(w, ws),
         "roofline": roofline(dom[0], dom[1][0], dom[1][1], bytes_launch, hbm_peak, peak_kind),
