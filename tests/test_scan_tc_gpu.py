@@ -288,3 +288,53 @@ def test_prep_scalar_gate():
     assert "gdr_chunk_prep_tc" in tr, tr
     assert_close("o", out, ref_o, torch.float32)
     assert_close("ht", ht, ref_h, torch.float32)
+
+
+@pytest.mark.parametrize("HK,HV", [(2, 2), (1, 4), (4, 8)])
+def test_prep_head_groupings(HK, HV):
+    """Key heads shared by 1, 4 and 2 value heads through the tensor-core
+    prep (each CTA reads its key head's k and q rows)."""
+    d = draw(2, 200, HK, HV, 128, 128, dtype=torch.float32, seed=590 + 10 * HK + HV)
+    ref_o, ref_h = oracle.recurrence(*(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")),
+                                     to_f64(d["h0"]))
+    out, ht, tr = forward(d, 64)
+    assert "gdr_chunk_prep_tc" in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+    assert_close("ht", ht, ref_h, torch.float32)
+
+
+def test_segmented_scan_scalar_gate():
+    """A scalar gate through the tensor-core prep and a segmented scan."""
+    d = draw(1, 900, 2, 4, 128, 128, dtype=torch.float32, seed=600, scalar_gate=True)
+    ref_o, ref_h = oracle.scalar_gate_recurrence(
+        *(to_f64(d[n]) for n in ("q", "k", "v", "g", "beta")), to_f64(d["h0"]))
+    out, ht, tr = forward_seg(d, 64, gdr_flag_segments(4))
+    assert "gdr_segment_combine" in tr and "gdr_chunk_prep_tc" in tr, tr
+    assert_close("o", out, ref_o, torch.float32)
+    assert_close("ht", ht, ref_h, torch.float32)
+
+
+def test_segmented_scan_packed_chunk32_bf16():
+    """Packed bf16 q/k/v at chunk 32 (the CUDA-core prep, then the
+    tensor-core scan in segments): the long sequences cut into 3, a decode
+    token and a short sequence beside them."""
+    gen = torch.Generator()
+    gen.manual_seed(610)
+    seqs = [draw(1, L, 2, 4, 128, 128, dtype=torch.bfloat16, generator=gen)
+            for L in (500, 1, 333, 20)]
+    packed, cu = pack(seqs)
+    c = to_cuda(packed)
+    gdr_trace_enable(True)
+    try:
+        out, ht = gdr_forward_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, h0=c["h0"],
+                                     chunk=32, flags=gdr_flag_segments(3))
+        gdr_device_check()
+        tr = gdr_trace_read()
+    finally:
+        gdr_trace_enable(False)
+    assert "gdr_segment_combine" in tr and "gdr_chunk_prep" in tr, tr
+    for n, d in enumerate(seqs):
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d[x]) for x in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d["h0"]))
+        assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.bfloat16)
+        assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.bfloat16)
