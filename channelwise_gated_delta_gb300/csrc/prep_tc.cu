@@ -16,7 +16,7 @@
 // (the factors of Lk, Lq and R meet in each product, so A and P hold the
 // exact decays e^{G_r - G_s}).
 //
-// One CTA per (chunk, value head), eight warps:
+// One CTA per (chunk, value head), sixteen warps:
 //   1. prefix sums (one thread per key channel) into shared memory;
 //   2. the operand tiles, eight channels of one row per thread: [Lk; Lq] and
 //      R as bf16 hi/lo pairs for the gram, diag(beta) K e^G for the WY
@@ -45,7 +45,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kPtThreads = 256;
+constexpr int kPtThreads = 512;
+constexpr int kPtWarps = kPtThreads / 32;
+constexpr int kPtItems = 64 * 16 / kPtThreads;  // (row, 8-channel octet) items a thread
 constexpr int kPtC = 64;   // chunk
 constexpr int kPtD = 128;  // dk = dv
 constexpr uint64_t kPtWaitNs = 2000000000ull;
@@ -60,8 +62,8 @@ constexpr uint32_t kPtR = 65536;       // R hi | lo, [64][128]
 constexpr uint32_t kPtRk = 98304;      // diag(beta) K e^G hi | lo, [64 s][128 i] (read MN-major)
 constexpr uint32_t kPtGs = 131072;     // G f32 [64][kPtLdg]; then diag(beta) V hi | lo
 constexpr int kPtLdg = 132;
-constexpr uint32_t kPtVec = kPtGs + 64 * kPtLdg * 4;  // beta [64], G_m [128], G_L [128]
-constexpr uint32_t kPtBars = kPtVec + 320 * 4;
+constexpr uint32_t kPtVec = kPtGs + 64 * kPtLdg * 4;  // beta [64], G_m [128], G_L [128], G_31 [128]
+constexpr uint32_t kPtBars = kPtVec + 448 * 4;
 constexpr uint32_t kPtSlot = kPtBars + 64;
 constexpr uint32_t kPtAbort = kPtSlot + 4;
 constexpr uint32_t kPtSmem = kPtAbort + 4 + 1024;  // + alignment slack
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPtAbort);
     float *Gs = reinterpret_cast<float *>(smem + kPtGs);
     float *bsv = reinterpret_cast<float *>(smem + kPtVec);
-    float *gmv = bsv + kPtC, *glv = gmv + kPtD;
+    float *gmv = bsv + kPtC, *glv = gmv + kPtD, *g31 = glv + kPtD;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int HV = a.HV;
 
@@ -181,9 +183,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     // the same rows of v go to L2 for the right-hand side built in step 3
     // (rows past L read row L - 1 and are zeroed after the loads, so that
     // every load is issued unconditionally and all are in flight at once)
-    float kq[4][16];
+    float kq[kPtItems][16];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPtItems; ++u) {
         const int item = tid + kPtThreads * u;
         const int r = item & 63, i0 = 8 * (item >> 6);
         const int rc = min(r, L - 1);
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPtItems; ++u) {
         const int r = (tid + kPtThreads * u) & 63;
         if (r >= L) {
 #pragma unroll
@@ -207,30 +209,47 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         }
     }
 
-    // ---- 1. prefix sums of the log-decay (threads 0-127: channel i), beta
+    // ---- 1. prefix sums of the log-decay: threads 0-255, two per key
+    // channel i (rows 0-31 and 32-63); the second half adds the first's
+    // total after a barrier.  beta on threads 256-319.
     bool in_range = true;
-    if (tid < kPtD) {
-        const int i = tid;
-        float x[kPtC];
+    const int pc = tid & (kPtD - 1), ph = tid >> 7;  // channel, half (tid < 256)
+    float gx[32];
+    if (tid < 2 * kPtD) {
 #pragma unroll
-        for (int r = 0; r < kPtC; ++r) {
+        for (int u = 0; u < 32; ++u) {
+            const int r = 32 * ph + u;
             const size_t row = tr0 + min(r, L - 1);
-            x[r] = a.g_scalar ? a.g[row * HV + hv] : a.g[(row * HV + hv) * kPtD + i];
+            gx[u] = a.g_scalar ? a.g[row * HV + hv] : a.g[(row * HV + hv) * kPtD + pc];
         }
         float run = 0.f;
 #pragma unroll
-        for (int r = 0; r < kPtC; ++r) {
-            run += r < L ? x[r] : 0.f;  // a zero gate past L keeps G flat
-            Gs[r * kPtLdg + i] = run;
+        for (int u = 0; u < 32; ++u) {
+            run += 32 * ph + u < L ? gx[u] : 0.f;  // a zero gate past L keeps G flat
+            gx[u] = run;
         }
-        const int m = (L - 1) / 2;
-        const float gm = Gs[m * kPtLdg + i], gl = Gs[(L - 1) * kPtLdg + i];
-        gmv[i] = gm;
-        glv[i] = gl;
-        in_range = Gs[i] - gm <= kPtRange && gm - gl <= kPtRange;
-    } else if (tid < kPtD + kPtC) {
-        const int r = tid - kPtD;
+        if (ph == 0) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) Gs[u * kPtLdg + pc] = gx[u];
+            g31[pc] = gx[31];
+        }
+    } else if (tid < 2 * kPtD + kPtC) {
+        const int r = tid - 2 * kPtD;
         bsv[r] = r < L ? a.beta[(tr0 + r) * HV + hv] : 0.f;
+    }
+    __syncthreads();
+    if (tid >= kPtD && tid < 2 * kPtD) {
+        const float base = g31[pc];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) Gs[(32 + u) * kPtLdg + pc] = gx[u] + base;
+    }
+    __syncthreads();
+    if (tid < kPtD) {
+        const int m = (L - 1) / 2;
+        const float gm = Gs[m * kPtLdg + pc], gl = Gs[(L - 1) * kPtLdg + pc];
+        gmv[pc] = gm;
+        glv[pc] = gl;
+        in_range = Gs[pc] - gm <= kPtRange && gm - gl <= kPtRange;
     }
     tc_fence_before_sync();
     const bool fast = __syncthreads_and(in_range) != 0;
@@ -248,7 +267,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     // 8o .. 8o + 7), consecutive threads on consecutive rows so that eight
     // of them fill one 128-byte core matrix
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPtItems; ++u) {
         const int item = tid + kPtThreads * u;
         const int r = item & 63, o = item >> 6, i0 = 8 * o;
         float kk[8], qq[8], G[8];
@@ -339,10 +358,11 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
             QT[i * kPtC + r] = qv;
         }
         __syncthreads();
-        float av[8][2], pv[8][2];
+        constexpr int kRowsW = kPtC / kPtWarps;
+        float av[kRowsW][2], pv[kRowsW][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = warp + 8 * j;
+        for (int j = 0; j < kRowsW; ++j) {
+            const int r = warp + kPtWarps * j;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int s = lane + 32 * h;
@@ -361,8 +381,8 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         }
         __syncthreads();  // K^T, Q^T read: A and the staged P may overwrite them
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = warp + 8 * j;
+        for (int j = 0; j < kRowsW; ++j) {
+            const int r = warp + kPtWarps * j;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 As[r * kPtLda + lane + 32 * h] = av[j][h];
@@ -387,15 +407,15 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     // diag(beta) V into the G region (G is no longer read); the four rows'
     // loads in flight together
     {
-        float vv[4][8];
+        float vv[kPtItems][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kPtItems; ++u) {
             const int item = tid + kPtThreads * u;
             const int s = item & 63, j0 = 8 * (item >> 6);
             pt_load8(vp + ((tr0 + min(s, L - 1)) * HV + hv) * kPtD + j0, vv[u]);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kPtItems; ++u) {
             const int item = tid + kPtThreads * u;
             const int s = item & 63, j0 = 8 * (item >> 6);
             const float bs = bsv[s];  // zero past L
@@ -410,22 +430,22 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     }
 
     // ---- 4. A and P out of tensor memory: warp w reads lanes 32 (w % 4) ..,
-    // columns 32 (w / 4) ..; lanes 0-63 are the rows of A, 64-127 those of P
+    // columns 16 (w / 4) ..; lanes 0-63 are the rows of A, 64-127 those of P
     if (fast) {
         wait(0, 0);
         if (!*abort_flag) {
             tc_fence_after_sync();
-            const int qd = warp & 3, hf = warp >> 2;
-            float x[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + 32 * hf, x);
+            const int qd = warp & 3, part = warp >> 2;
+            float x[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + 16 * part, x);
             const int lrow = 32 * qd + lane;
             if (lrow < kPtC) {
                 const int r = lrow;
                 const float br = bsv[r];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
+                for (int c4 = 0; c4 < 4; ++c4) {
                     float4 y;
-                    const int s0 = 32 * hf + 4 * c4;
+                    const int s0 = 16 * part + 4 * c4;
                     y.x = (s0 + 0 < r && r < L) ? br * x[4 * c4 + 0] : 0.f;
                     y.y = (s0 + 1 < r && r < L) ? br * x[4 * c4 + 1] : 0.f;
                     y.z = (s0 + 2 < r && r < L) ? br * x[4 * c4 + 2] : 0.f;
@@ -435,16 +455,16 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
             } else {
                 const int t = lrow - kPtC;
 #pragma unroll
-                for (int oo = 0; oo < 4; ++oo) {
+                for (int oo = 0; oo < 2; ++oo) {
                     float y[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int s = 32 * hf + 8 * oo + e;
+                        const int s = 16 * part + 8 * oo + e;
                         y[e] = (s <= t && t < L) ? x[8 * oo + e] : 0.f;
                     }
                     uint4 h, l;
                     pt_split8(y, h, l);
-                    const uint32_t off = kmajor_off(t, 32 * hf + 8 * oo, kPtC);
+                    const uint32_t off = kmajor_off(t, 16 * part + 8 * oo, kPtC);
                     *reinterpret_cast<uint4 *>(rec_p + off) = h;
                     *reinterpret_cast<uint4 *>(rec_p + 8192 + off) = l;
                 }
@@ -471,7 +491,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     }
     __syncthreads();
     float *Xs = reinterpret_cast<float *>(smem + kPtX);
-#pragma unroll
+#pragma unroll 1
     for (int I = 1; I < 4; ++I) {
         // X_IJ = sum over the blocks K = J .. I-1 of A_IK T_KJ (T is zero
         // above its diagonal); a thread takes a 1 x 4 strip (row r, columns
@@ -555,19 +575,23 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
         issued = true;
     }
 
-    // ---- 7. Wk and Wv: warps 0, 1 (Wk) and 4, 5 (Wv) read the 64 rows;
+    // ---- 7. Wk and Wv: the warps of lane quarters 0 and 1 read the 64 rows,
+    // warp w columns 64 (w / 4 % 2) .. of Wk (w / 8 = 0) or Wv (w / 8 = 1);
     // Wv is staged in the R region (free once the gram is done)
     float *Wst = reinterpret_cast<float *>(smem + kPtR);
-    const int qd = warp & 3, hf = warp >> 2;
+    const int qd = warp & 3, part = warp >> 2;
     if (qd < 2) {
         wait(1, 0);
         if (!*abort_flag) {
             tc_fence_after_sync();
             const int r = 32 * qd + lane;
-            for (int c0 = 0; c0 < kPtD; c0 += 32) {
+            const bool is_v = part >= 2;
+            const int cb = 64 * (part & 1);
+#pragma unroll
+            for (int c0 = cb; c0 < cb + 64; c0 += 32) {
                 float x[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + 128 * hf + c0, x);
-                if (hf == 0) {
+                tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + (is_v ? 128 : 0) + c0, x);
+                if (!is_v) {
 #pragma unroll
                     for (int oo = 0; oo < 4; ++oo) {
                         float y[8];
@@ -596,7 +620,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) gdr_chunk_prep_tc(const __grid_
     // Wv from the staging tile to its record, each warp two full rows per store
     if (!*abort_flag) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 64 * 32 / kPtThreads; ++u) {
             const int idx = tid + kPtThreads * u;  // float4 index in [64][32]
             const int r = idx >> 5, ch = idx & 31;
             *reinterpret_cast<float4 *>(rec_wv + r * kPtD + 4 * ch) =
