@@ -30,10 +30,16 @@
 // first wave drop their outputs.
 //
 // Warps: 0-3 the chain (lane j = value column j: builds the bf16 state pair,
-// U = Wv - Z, reads O out, the final state), 4 the producer (one thread: bulk
-// copies of each chunk's operands), 5 the MMA issuer (one thread).  Wk and Kh
-// are double-buffered (the next chunk's copy overlaps this chunk's work), Qt,
-// P, Wv and gam single.  Every wait is bounded: a timeout sets the CTA's
+// U = Wv - Z, the final state), 4 the producer (one thread: bulk copies of
+// each chunk's operands), 5 the MMA issuer (one thread), 6-9 the writers
+// (O^T out of tensor memory and the outputs to global memory, off the
+// chain's path).  Wk (with
+// the chunk's decay gam) and Kh are double-buffered (the next chunk's copy
+// overlaps this chunk's work), Qt, P and Wv single.  Per chunk the issuer
+// runs Z, then the part of O^T that needs only the state pair (S^T Qt^T)
+// while the chain forms U, then the state product and the rest of O^T
+// (U^T P^T, a second accumulator); the chain builds the next chunk's state
+// pair as soon as the state product is in and reads O^T after it.  Every wait is bounded: a timeout sets the CTA's
 // abort flag and the library's error word, and everyone runs out its loop.
 #include <cuda.h>
 
@@ -45,11 +51,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kScWarps = 6;
+constexpr int kScWarps = 10;
 constexpr int kScThreads = 32 * kScWarps;
 constexpr int kScChainThreads = 128;
 constexpr int kScProducer = 4;
 constexpr int kScIssuer = 5;
+constexpr int kScWriter0 = 6;  // warps 6-9: O^T out of tensor memory, the outputs stored
 constexpr uint64_t kScWaitNs = 2000000000ull;  // 2 s per wait
 
 // shared memory (bytes from a 1024-byte aligned base); regions sized for
@@ -59,16 +66,16 @@ constexpr uint32_t kScKh = 65536;     // [2] x the same for Kh (read MN-major)
 constexpr uint32_t kScQt = 131072;    // hi | lo [C][dk]
 constexpr uint32_t kScP = 163840;     // hi | lo [C][C]
 constexpr uint32_t kScWv = 180224;    // f32 [C][dv]
-constexpr uint32_t kScGam = 212992;   // f32 [dk]
-constexpr uint32_t kScBars = 213504;  // mbarriers
+constexpr uint32_t kScGam = 212992;   // [2] x f32 [dk], with Wk's buffers
+constexpr uint32_t kScBars = 214016;  // mbarriers
 constexpr uint32_t kScSlot = kScBars + 256;
 constexpr uint32_t kScAbort = kScSlot + 4;
 constexpr uint32_t kScSmem = kScAbort + 4 + 1024;  // + alignment slack
 enum {
-    SB_WK = 0,   // [2] Wk copied in (tx)
+    SB_WK = 0,   // [2] Wk and gam copied in (tx)
     SB_KH = 2,   // [2] Kh copied in (tx)
     SB_QP = 4,   // Qt and P copied in (tx)
-    SB_WV = 5,   // Wv and gam copied in (tx)
+    SB_WV = 5,   // Wv copied in (tx)
     SB_WKF = 6,  // [2] the Z product has read Wk buffer b (commit)
     SB_KHF = 8,  // [2] the state product has read Kh buffer b (commit)
     SB_Z = 10,   // Z^T ready (commit)
@@ -85,9 +92,10 @@ constexpr uint32_t kScTmX = 0;      // f32 state^T [dv lanes][dk]
 constexpr uint32_t kScTmShi = 128;  // bf16 pairs of the state^T (A operand)
 constexpr uint32_t kScTmSlo = 192;
 constexpr uint32_t kScTmZ = 256;    // f32 Z^T [dv][C]
-constexpr uint32_t kScTmO = 320;    // f32 O^T [dv][C]
+constexpr uint32_t kScTmO = 320;    // f32 S^T Qt^T, the first part of O^T [dv][C]
 constexpr uint32_t kScTmUhi = 384;  // bf16 pairs of U^T (A operand)
 constexpr uint32_t kScTmUlo = 416;
+constexpr uint32_t kScTmO2 = 448;   // f32 U^T P^T, the second part of O^T
 constexpr uint32_t kScTmCols = 512;
 
 struct ScanTcArgs {
@@ -176,14 +184,21 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const int bf = c & 1;
                 if (c >= 2) wait(SB_WKF + bf, ((c - 2) >> 1) & 1);
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bars[SB_WK + bf], tile);
+                mbar_arrive_expect_tx(&bars[SB_WK + bf], tile + (uint32_t)(dk * 4));
                 bulk_load_1d(smem + kScWk + bf * 32768, rec, tile, &bars[SB_WK + bf]);
+                bulk_load_1d(smem + kScGam + bf * 512, rec + 3 * (size_t)tile + (size_t)C * dv * 4 + (size_t)C * C * 4,
+                             (uint32_t)(dk * 4), &bars[SB_WK + bf]);
                 armed[0] = c;
                 if (c >= 2) wait(SB_KHF + bf, ((c - 2) >> 1) & 1);
                 if (*abort_flag) break;
                 mbar_arrive_expect_tx(&bars[SB_KH + bf], tile);
                 bulk_load_1d(smem + kScKh + bf * 32768, rec + 2 * (size_t)tile, tile, &bars[SB_KH + bf]);
                 armed[1] = c;
+                if (c >= 1) wait(SB_CH, (c - 1) & 1);
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(&bars[SB_WV], (uint32_t)(C * dv * 4));
+                bulk_load_1d(smem + kScWv, rec + 3 * (size_t)tile, (uint32_t)(C * dv * 4), &bars[SB_WV]);
+                armed[3] = c;
                 if (c >= 1) wait(SB_O, (c - 1) & 1);
                 if (*abort_flag) break;
                 mbar_arrive_expect_tx(&bars[SB_QP], tile + (uint32_t)(C * C * 4));
@@ -191,13 +206,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 bulk_load_1d(smem + kScP, rec + 3 * (size_t)tile + (size_t)C * dv * 4,
                              (uint32_t)(C * C * 4), &bars[SB_QP]);
                 armed[2] = c;
-                if (c >= 1) wait(SB_CH, (c - 1) & 1);
-                if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bars[SB_WV], (uint32_t)(C * dv * 4 + dk * 4));
-                bulk_load_1d(smem + kScWv, rec + 3 * (size_t)tile, (uint32_t)(C * dv * 4), &bars[SB_WV]);
-                bulk_load_1d(smem + kScGam, rec + 3 * (size_t)tile + (size_t)C * dv * 4 + (size_t)C * C * 4,
-                             (uint32_t)(dk * 4), &bars[SB_WV]);
-                armed[3] = c;
             }
             if (*abort_flag) {
                 // let the copies already armed land before the CTA leaves
@@ -216,7 +224,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
             const uint32_t idZ = idesc_bf16(128, C, false, false, false);
             const uint32_t idX = idesc_bf16(128, dk, false, true, false);
             const uint32_t sbase = smem_u32(smem);
-            const uint32_t tZ = tmem + kScTmZ, tO = tmem + kScTmO, tX = tmem + kScTmX;
+            const uint32_t tZ = tmem + kScTmZ, tO = tmem + kScTmO, tO2 = tmem + kScTmO2,
+                           tX = tmem + kScTmX;
             const uint32_t tSh = tmem + kScTmShi, tSl = tmem + kScTmSlo;
             const uint32_t tUh = tmem + kScTmUhi, tUl = tmem + kScTmUlo;
             const uint32_t half = (uint32_t)(C * dk * 2);  // lo tile after the hi tile
@@ -241,31 +250,27 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     mma_commit(&bars[SB_WKF + bf]);
                     issued = true;
                 }
-                // O^T = S^T Qt^T + U^T P^T
-                wait(SB_U, c & 1);
+                // O^T = S^T Qt^T + U^T P^T in two accumulators: the first
+                // part needs only the state pair, so it runs while the chain
+                // forms U
                 wait(SB_QP, c & 1);
                 if (c >= 1) wait(SB_OF, (c - 1) & 1);
                 if (*abort_flag) break;
                 tc_fence_after_sync();
                 {
-                    const uint32_t qt = sbase + kScQt, p = sbase + kScP;
+                    const uint32_t qt = sbase + kScQt;
                     const uint64_t qh = smem_desc(qt, 128, dk * 16), ql = smem_desc(qt + half, 128, dk * 16);
-                    const uint64_t ph = smem_desc(p, 128, C * 16), pl = smem_desc(p + C * C * 2, 128, C * 16);
                     for (int ks = 0; ks < dk / 16; ++ks)
                         mma_bf16_ts(tO, tSh + 8 * ks, qh + (uint64_t)(16 * ks), idZ, ks > 0 ? 1u : 0u);
                     for (int ks = 0; ks < dk / 16; ++ks)
                         mma_bf16_ts(tO, tSh + 8 * ks, ql + (uint64_t)(16 * ks), idZ, 1u);
                     for (int ks = 0; ks < dk / 16; ++ks)
                         mma_bf16_ts(tO, tSl + 8 * ks, qh + (uint64_t)(16 * ks), idZ, 1u);
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16_ts(tO, tUh + 8 * ks, ph + (uint64_t)(16 * ks), idZ, 1u);
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16_ts(tO, tUh + 8 * ks, pl + (uint64_t)(16 * ks), idZ, 1u);
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        mma_bf16_ts(tO, tUl + 8 * ks, ph + (uint64_t)(16 * ks), idZ, 1u);
-                    mma_commit(&bars[SB_O]);
                 }
-                // X^T += U^T Kh (X pre-scaled by the chain)
+                // then, with U: X^T += U^T Kh (X pre-scaled by the chain),
+                // whose commit also covers the first part of O^T, the last
+                // reader of the state pair; then the second part of O^T
+                wait(SB_U, c & 1);
                 wait(SB_KH + bf, (c >> 1) & 1);
                 if (*abort_flag) break;
                 tc_fence_after_sync();
@@ -282,6 +287,17 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     mma_commit(&bars[SB_X]);
                     mma_commit(&bars[SB_KHF + bf]);
                 }
+                {
+                    const uint32_t p = sbase + kScP;
+                    const uint64_t ph = smem_desc(p, 128, C * 16), pl = smem_desc(p + C * C * 2, 128, C * 16);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16_ts(tO2, tUh + 8 * ks, ph + (uint64_t)(16 * ks), idZ, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16_ts(tO2, tUh + 8 * ks, pl + (uint64_t)(16 * ks), idZ, 1u);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16_ts(tO2, tUl + 8 * ks, ph + (uint64_t)(16 * ks), idZ, 1u);
+                    mma_commit(&bars[SB_O]);
+                }
             }
             // every MMA issued is done before the tensor memory is released
             if (issued) {
@@ -289,7 +305,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 mbar_wait_bounded(&bars[SB_COUNT], 0, kScWaitNs);
             }
         }
-    } else {
+    } else if (warp < 4) {
         // ================= the chain: lane j = value column j
         const int j = tid;
         const bool jv = j < dv;
@@ -297,7 +313,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const bool outs = jv && !(rflags & kRunNoOutputs);     // outputs stored
         const uint32_t lo = (uint32_t)(32 * warp) << 16;
         const float *Wv = reinterpret_cast<const float *>(smem + kScWv);
-        const float *gam = reinterpret_cast<const float *>(smem + kScGam);
         Tout *out = static_cast<Tout *>(a.out);
         // the initial state (transposed: lane j holds column j of h0)
         for (int g = 0; g < dk / 16; ++g) {
@@ -308,14 +323,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tmem_st16(tmem + lo + kScTmX + 16 * g, x);
         }
         tmem_st_wait();
-        for (int c = 0; c < NC; ++c) {
-            const int t0 = c * C, L = min(C, T - t0);
-            if (c >= 1) wait(SB_X, (c - 1) & 1);
-            wait(SB_WV, c & 1);
-            if (*abort_flag) break;
+        // the state's bf16 pair for chunk cc's products, then the state
+        // pre-scaled by that chunk's decay for its update
+        auto rebuild = [&](int cc) {
+            wait(SB_WK + (cc & 1), (cc >> 1) & 1);  // gam of chunk cc
+            if (*abort_flag) return;
             tc_fence_after_sync();
-            // the state's bf16 pair for this chunk's products, then the state
-            // pre-scaled by the chunk's decay for its update
+            const float *gam = reinterpret_cast<const float *>(smem + kScGam + (cc & 1) * 512);
             for (int g = 0; g < dk / 16; ++g) {
                 float x[16];
                 tmem_ld16(tmem + lo + kScTmX + 16 * g, x);
@@ -331,8 +345,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&bars[SB_S]);
+        };
+        if (NC > 0) rebuild(0);
+        for (int c = 0; c < NC && !*abort_flag; ++c) {
+            const int t0 = c * C, L = min(C, T - t0);
             // U = Wv - Z, as its bf16 pair
             wait(SB_Z, c & 1);
+            wait(SB_WV, c & 1);
             if (*abort_flag) break;
             tc_fence_after_sync();
             for (int g = 0; g < C / 16; ++g) {
@@ -353,21 +372,12 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(&bars[SB_U]);
             mbar_arrive(&bars[SB_CH]);
-            // the chunk's outputs
-            wait(SB_O, c & 1);
-            if (*abort_flag) break;
-            tc_fence_after_sync();
-            for (int g = 0; g < C / 16; ++g) {
-                float o[16];
-                tmem_ld16(tmem + lo + kScTmO + 16 * g, o);
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int s = 16 * g + m;
-                    if (outs && s < L) out[((tok0 + t0 + s) * HV + hv) * dv + j] = from_f32<Tout>(o[m]);
-                }
+            // the next chunk's state pair as soon as the state product (and
+            // with it the first part of O^T) is in
+            if (c + 1 < NC) {
+                wait(SB_X, c & 1);
+                rebuild(c + 1);
             }
-            tc_fence_before_sync();
-            mbar_arrive(&bars[SB_OF]);
         }
         if (STORE_HT && a.ht) {
             if (NC > 0) wait(SB_X, (NC - 1) & 1);
@@ -380,6 +390,38 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     for (int m = 0; m < 16; ++m)
                         if (jv) a.ht[(head * dk + 16 * g + m) * dv + j] = x[m];
                 }
+            }
+        }
+    } else if (warp >= kScWriter0) {
+        // ================= the writers: warp w reads tensor-memory lanes
+        // 32 (w % 4) .., lane j = value column j; each chunk's two parts of
+        // O^T summed into registers, their columns freed, then the outputs
+        // stored while the chain and the issuer go on
+        const int j = 32 * (warp & 3) + lane;
+        const bool outs = j < dv && !(rflags & kRunNoOutputs);
+        const uint32_t lo = (uint32_t)(32 * (warp & 3)) << 16;
+        Tout *out = static_cast<Tout *>(a.out);
+        for (int c = 0; c < NC && !*abort_flag; ++c) {
+            const int t0 = c * C, L = min(C, T - t0);
+            wait(SB_O, c & 1);
+            if (*abort_flag) break;
+            tc_fence_after_sync();
+            float o[64];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                if (16 * g < C) {
+                    float og[16], og2[16];
+                    tmem_ld16(tmem + lo + kScTmO + 16 * g, og);
+                    tmem_ld16(tmem + lo + kScTmO2 + 16 * g, og2);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) o[16 * g + m] = og[m] + og2[m];
+                }
+            tc_fence_before_sync();
+            mbar_arrive(&bars[SB_OF]);
+            if (outs) {
+#pragma unroll
+                for (int s = 0; s < 64; ++s)
+                    if (s < L) out[((tok0 + t0 + s) * HV + hv) * dv + j] = from_f32<Tout>(o[s]);
             }
         }
     }
