@@ -33,14 +33,15 @@
 // U = Wv - Z, the final state), 4 the producer (one thread: bulk copies of
 // each chunk's operands), 5 the MMA issuer (one thread), 6-9 the writers
 // (O^T out of tensor memory and the outputs to global memory, off the
-// chain's path).  Wk (with
-// the chunk's decay gam) and Kh are double-buffered (the next chunk's copy
-// overlaps this chunk's work), Qt, P and Wv single.  Per chunk the issuer
-// runs Z, then the part of O^T that needs only the state pair (S^T Qt^T)
-// while the chain forms U, then the state product and the rest of O^T
-// (U^T P^T, a second accumulator); the chain builds the next chunk's state
-// pair as soon as the state product is in and reads O^T after it.  Every wait is bounded: a timeout sets the CTA's
-// abort flag and the library's error word, and everyone runs out its loop.
+// chain's path).  Kh is double-buffered; Wk and Qt share one buffer
+// (stacked, they are one [2C][dk] operand), P and Wv one each.  Per chunk
+// the issuer runs [Z^T | S^T Qt^T] = S^T [Wk; Qt]^T (Z and the part of O^T
+// that needs only the state pair, one N = 2C product), then, once the chain
+// has formed U, the state product and the rest of O^T (U^T P^T, a second
+// accumulator); the chain builds the next chunk's state pair as soon as the
+// state product is in, and the writers take O^T out.  Every wait is
+// bounded: a timeout sets the CTA's abort flag and the library's error
+// word, and everyone runs out its loop.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -61,22 +62,22 @@ constexpr uint64_t kScWaitNs = 2000000000ull;  // 2 s per wait
 
 // shared memory (bytes from a 1024-byte aligned base); regions sized for
 // C <= 64, dk, dv <= 128
-constexpr uint32_t kScWk = 0;         // [2] x {hi [C][dk] | lo [C][dk]} bf16, K-major
-constexpr uint32_t kScKh = 65536;     // [2] x the same for Kh (read MN-major)
-constexpr uint32_t kScQt = 131072;    // hi | lo [C][dk]
+constexpr uint32_t kScWq = 0;         // {Wk hi | Qt hi | Wk lo | Qt lo}, each [C][dk] bf16
+                                      // K-major: [Wk; Qt] is one [2C][dk] operand
+constexpr uint32_t kScKh = 65536;     // [2] x {hi | lo} [C][dk] for Kh (read MN-major)
 constexpr uint32_t kScP = 163840;     // hi | lo [C][C]
 constexpr uint32_t kScWv = 180224;    // f32 [C][dv]
-constexpr uint32_t kScGam = 212992;   // [2] x f32 [dk], with Wk's buffers
+constexpr uint32_t kScGam = 212992;   // f32 [dk], copied in with Wk and Qt
 constexpr uint32_t kScBars = 214016;  // mbarriers
 constexpr uint32_t kScSlot = kScBars + 256;
 constexpr uint32_t kScAbort = kScSlot + 4;
 constexpr uint32_t kScSmem = kScAbort + 4 + 1024;  // + alignment slack
 enum {
-    SB_WK = 0,   // [2] Wk and gam copied in (tx)
+    SB_WK = 0,   // Wk, Qt and gam copied in (tx)
     SB_KH = 2,   // [2] Kh copied in (tx)
-    SB_QP = 4,   // Qt and P copied in (tx)
+    SB_QP = 4,   // P copied in (tx)
     SB_WV = 5,   // Wv copied in (tx)
-    SB_WKF = 6,  // [2] the Z product has read Wk buffer b (commit)
+    SB_WKF = 6,  // the [Z | O^T] product has read Wk and Qt (commit)
     SB_KHF = 8,  // [2] the state product has read Kh buffer b (commit)
     SB_Z = 10,   // Z^T ready (commit)
     SB_O = 11,   // O^T ready (commit)
@@ -91,8 +92,7 @@ enum {
 constexpr uint32_t kScTmX = 0;      // f32 state^T [dv lanes][dk]
 constexpr uint32_t kScTmShi = 128;  // bf16 pairs of the state^T (A operand)
 constexpr uint32_t kScTmSlo = 192;
-constexpr uint32_t kScTmZ = 256;    // f32 Z^T [dv][C]
-constexpr uint32_t kScTmO = 320;    // f32 S^T Qt^T, the first part of O^T [dv][C]
+constexpr uint32_t kScTmZ = 256;    // f32 [Z^T | S^T Qt^T] [dv][2C]: Z, then the first part of O^T
 constexpr uint32_t kScTmUhi = 384;  // bf16 pairs of U^T (A operand)
 constexpr uint32_t kScTmUlo = 416;
 constexpr uint32_t kScTmO2 = 448;   // f32 U^T P^T, the second part of O^T
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
     };
     const uint32_t tile = (uint32_t)(C * dk * 4);  // a hi | lo operand region, bytes
+    const uint32_t half = (uint32_t)(C * dk * 2);  // one bf16 tile of it
 
     if (warp == kScProducer) {
         // ================= bulk copies of each chunk's operands
@@ -182,12 +183,15 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const unsigned char *rec = reinterpret_cast<const unsigned char *>(
                     a.ws + (rec0 + (size_t)c * rec_step) * a.rec_floats);
                 const int bf = c & 1;
-                if (c >= 2) wait(SB_WKF + bf, ((c - 2) >> 1) & 1);
+                if (c >= 1) wait(SB_WKF, (c - 1) & 1);
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bars[SB_WK + bf], tile + (uint32_t)(dk * 4));
-                bulk_load_1d(smem + kScWk + bf * 32768, rec, tile, &bars[SB_WK + bf]);
-                bulk_load_1d(smem + kScGam + bf * 512, rec + 3 * (size_t)tile + (size_t)C * dv * 4 + (size_t)C * C * 4,
-                             (uint32_t)(dk * 4), &bars[SB_WK + bf]);
+                mbar_arrive_expect_tx(&bars[SB_WK], 2 * tile + (uint32_t)(dk * 4));
+                bulk_load_1d(smem + kScWq, rec, half, &bars[SB_WK]);                       // Wk hi
+                bulk_load_1d(smem + kScWq + 2 * half, rec + half, half, &bars[SB_WK]);     // Wk lo
+                bulk_load_1d(smem + kScWq + half, rec + tile, half, &bars[SB_WK]);         // Qt hi
+                bulk_load_1d(smem + kScWq + 3 * half, rec + tile + half, half, &bars[SB_WK]);  // Qt lo
+                bulk_load_1d(smem + kScGam, rec + 3 * (size_t)tile + (size_t)C * dv * 4 + (size_t)C * C * 4,
+                             (uint32_t)(dk * 4), &bars[SB_WK]);
                 armed[0] = c;
                 if (c >= 2) wait(SB_KHF + bf, ((c - 2) >> 1) & 1);
                 if (*abort_flag) break;
@@ -201,8 +205,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 armed[3] = c;
                 if (c >= 1) wait(SB_O, (c - 1) & 1);
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bars[SB_QP], tile + (uint32_t)(C * C * 4));
-                bulk_load_1d(smem + kScQt, rec + tile, tile, &bars[SB_QP]);
+                mbar_arrive_expect_tx(&bars[SB_QP], (uint32_t)(C * C * 4));
                 bulk_load_1d(smem + kScP, rec + 3 * (size_t)tile + (size_t)C * dv * 4,
                              (uint32_t)(C * C * 4), &bars[SB_QP]);
                 armed[2] = c;
@@ -210,10 +213,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
             if (*abort_flag) {
                 // let the copies already armed land before the CTA leaves
                 // (bounded: each at most one more wait limit)
-                for (int x = 0; x < 2; ++x)  // both buffers of Wk and Kh
-                    for (int c2 = armed[x] - 1; c2 <= armed[x]; ++c2)
-                        if (c2 >= 0)
-                            mbar_wait_bounded(&bars[(x ? SB_KH : SB_WK) + (c2 & 1)], (c2 >> 1) & 1, kScWaitNs);
+                if (armed[0] >= 0) mbar_wait_bounded(&bars[SB_WK], armed[0] & 1, kScWaitNs);
+                for (int c2 = armed[1] - 1; c2 <= armed[1]; ++c2)  // both buffers of Kh
+                    if (c2 >= 0) mbar_wait_bounded(&bars[SB_KH + (c2 & 1)], (c2 >> 1) & 1, kScWaitNs);
                 if (armed[2] >= 0) mbar_wait_bounded(&bars[SB_QP], armed[2] & 1, kScWaitNs);
                 if (armed[3] >= 0) mbar_wait_bounded(&bars[SB_WV], armed[3] & 1, kScWaitNs);
             }
@@ -222,50 +224,34 @@ __global__ void __launch_bounds__(kScThreads, 1)
         // ================= MMA issue (one thread)
         if (lane == 0) {
             const uint32_t idZ = idesc_bf16(128, C, false, false, false);
+            const uint32_t idZO = idesc_bf16(128, 2 * C, false, false, false);
             const uint32_t idX = idesc_bf16(128, dk, false, true, false);
             const uint32_t sbase = smem_u32(smem);
-            const uint32_t tZ = tmem + kScTmZ, tO = tmem + kScTmO, tO2 = tmem + kScTmO2,
-                           tX = tmem + kScTmX;
+            const uint32_t tZ = tmem + kScTmZ, tO2 = tmem + kScTmO2, tX = tmem + kScTmX;
             const uint32_t tSh = tmem + kScTmShi, tSl = tmem + kScTmSlo;
             const uint32_t tUh = tmem + kScTmUhi, tUl = tmem + kScTmUlo;
-            const uint32_t half = (uint32_t)(C * dk * 2);  // lo tile after the hi tile
             bool issued = false;
             for (int c = 0; c < NC && !*abort_flag; ++c) {
                 const int bf = c & 1;
-                wait(SB_WK + bf, (c >> 1) & 1);
+                wait(SB_WK, c & 1);
                 wait(SB_S, c & 1);
+                if (c >= 1) wait(SB_OF, (c - 1) & 1);  // the writers have read O^T of c - 1
                 if (*abort_flag) break;
                 tc_fence_after_sync();
-                // Z^T = S^T Wk^T
+                // [Z^T | S^T Qt^T] = S^T [Wk; Qt]^T: Z and the part of O^T that
+                // needs only the state pair, one N = 2C product
                 {
-                    const uint32_t w = sbase + kScWk + bf * 32768;
-                    const uint64_t dh = smem_desc(w, 128, dk * 16), dl = smem_desc(w + half, 128, dk * 16);
+                    const uint32_t w = sbase + kScWq;
+                    const uint64_t dh = smem_desc(w, 128, dk * 16), dl = smem_desc(w + 2 * half, 128, dk * 16);
                     for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tZ, tSh + 8 * ks, dh + (uint64_t)(16 * ks), idZ, ks > 0 ? 1u : 0u);
+                        mma_bf16_ts(tZ, tSh + 8 * ks, dh + (uint64_t)(16 * ks), idZO, ks > 0 ? 1u : 0u);
                     for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tZ, tSh + 8 * ks, dl + (uint64_t)(16 * ks), idZ, 1u);
+                        mma_bf16_ts(tZ, tSh + 8 * ks, dl + (uint64_t)(16 * ks), idZO, 1u);
                     for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tZ, tSl + 8 * ks, dh + (uint64_t)(16 * ks), idZ, 1u);
+                        mma_bf16_ts(tZ, tSl + 8 * ks, dh + (uint64_t)(16 * ks), idZO, 1u);
                     mma_commit(&bars[SB_Z]);
-                    mma_commit(&bars[SB_WKF + bf]);
+                    mma_commit(&bars[SB_WKF]);
                     issued = true;
-                }
-                // O^T = S^T Qt^T + U^T P^T in two accumulators: the first
-                // part needs only the state pair, so it runs while the chain
-                // forms U
-                wait(SB_QP, c & 1);
-                if (c >= 1) wait(SB_OF, (c - 1) & 1);
-                if (*abort_flag) break;
-                tc_fence_after_sync();
-                {
-                    const uint32_t qt = sbase + kScQt;
-                    const uint64_t qh = smem_desc(qt, 128, dk * 16), ql = smem_desc(qt + half, 128, dk * 16);
-                    for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tO, tSh + 8 * ks, qh + (uint64_t)(16 * ks), idZ, ks > 0 ? 1u : 0u);
-                    for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tO, tSh + 8 * ks, ql + (uint64_t)(16 * ks), idZ, 1u);
-                    for (int ks = 0; ks < dk / 16; ++ks)
-                        mma_bf16_ts(tO, tSl + 8 * ks, qh + (uint64_t)(16 * ks), idZ, 1u);
                 }
                 // then, with U: X^T += U^T Kh (X pre-scaled by the chain),
                 // whose commit also covers the first part of O^T, the last
@@ -287,6 +273,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     mma_commit(&bars[SB_X]);
                     mma_commit(&bars[SB_KHF + bf]);
                 }
+                wait(SB_QP, c & 1);
+                if (*abort_flag) break;
+                tc_fence_after_sync();
                 {
                     const uint32_t p = sbase + kScP;
                     const uint64_t ph = smem_desc(p, 128, C * 16), pl = smem_desc(p + C * C * 2, 128, C * 16);
@@ -310,10 +299,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const int j = tid;
         const bool jv = j < dv;
         const bool vals = jv && !(rflags & kRunZeroValues);    // values read (else zero)
-        const bool outs = jv && !(rflags & kRunNoOutputs);     // outputs stored
         const uint32_t lo = (uint32_t)(32 * warp) << 16;
         const float *Wv = reinterpret_cast<const float *>(smem + kScWv);
-        Tout *out = static_cast<Tout *>(a.out);
         // the initial state (transposed: lane j holds column j of h0)
         for (int g = 0; g < dk / 16; ++g) {
             uint32_t x[16];
@@ -326,10 +313,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
         // the state's bf16 pair for chunk cc's products, then the state
         // pre-scaled by that chunk's decay for its update
         auto rebuild = [&](int cc) {
-            wait(SB_WK + (cc & 1), (cc >> 1) & 1);  // gam of chunk cc
+            wait(SB_WK, cc & 1);  // gam of chunk cc
             if (*abort_flag) return;
             tc_fence_after_sync();
-            const float *gam = reinterpret_cast<const float *>(smem + kScGam + (cc & 1) * 512);
+            const float *gam = reinterpret_cast<const float *>(smem + kScGam);
             for (int g = 0; g < dk / 16; ++g) {
                 float x[16];
                 tmem_ld16(tmem + lo + kScTmX + 16 * g, x);
@@ -411,7 +398,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
             for (int g = 0; g < 4; ++g)
                 if (16 * g < C) {
                     float og[16], og2[16];
-                    tmem_ld16(tmem + lo + kScTmO + 16 * g, og);
+                    tmem_ld16(tmem + lo + kScTmZ + C + 16 * g, og);
                     tmem_ld16(tmem + lo + kScTmO2 + 16 * g, og2);
 #pragma unroll
                     for (int m = 0; m < 16; ++m) o[16 * g + m] = og[m] + og2[m];
