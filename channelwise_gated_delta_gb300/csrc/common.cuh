@@ -123,6 +123,10 @@ cudaError_t tc_encode_seq_maps(const Problem &p, size_t tok0, int L, void *dst,
                                const void *v_row = nullptr, void *o_row = nullptr);
 cudaError_t launch_tc_prefill_varlen(const Problem &p, const void *seq_maps, const int4 *seqs,
                                      int nseq, int *dev_error, cudaStream_t stream);
+// seqs[s].w of that launch: the state the sequence starts from (0: its h0
+// slot; kSeqStartZero: zero; kSeqStartIdentity: the identity, dk = dv).
+constexpr int kSeqStartZero = 1;
+constexpr int kSeqStartIdentity = 2;
 // CUDA-core chunked prefill: chunks[i] = {first token row, length} of every
 // sequence's chunks, seqs[s] = {first token row, length, state slot, index
 // of its first chunk}; records: generic_varlen_record_bytes(p, nchunks).
@@ -153,13 +157,16 @@ cudaError_t launch_chunk_prep_tc(const Problem &p, float *records, size_t rec_fl
 // + c * c_stride; the state starts from slot `slot` of p.h0 and ends in slot
 // `slot` of p.ht.  kRunZeroValues: the values read as zero (the run from
 // the identity then ends in the segment's map M); kRunNoOutputs: the
-// outputs are dropped.
+// outputs are dropped; kRunStartZero / kRunStartIdentity: the state starts
+// at zero / the identity instead of slot `slot` of p.h0.
 struct ScanRun {
     long long tok0, rec_base;
     int T, slot, hv_stride, c_stride, flags, pad;
 };
 constexpr int kRunZeroValues = 1;
 constexpr int kRunNoOutputs = 2;
+constexpr int kRunStartZero = 4;      // the state starts at zero (h0 not read)
+constexpr int kRunStartIdentity = 8;  // the state starts at the identity (dk = dv)
 cudaError_t launch_chunk_scan_runs(const Problem &p, const float *records, size_t rec_floats,
                                    const ScanRun *runs, int nrun, cudaStream_t stream);
 // Tree verification on CUDA cores: p.B trees of p.T <= p.chunk tokens each,

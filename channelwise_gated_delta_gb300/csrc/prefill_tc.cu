@@ -446,12 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int T = T_dense;
     size_t tok0 = (size_t)b * T;    // the sequence's first token row
     size_t shead = head;            // state slot * HV + hv
+    int start = 0;                  // kSeqStartZero / kSeqStartIdentity, else h0
     const TileMaps *mp = &tm;
     if (VARLEN) {
         const int4 sd = seqs[b];
         tok0 = (size_t)sd.x;
         T = sd.y;
         shead = (size_t)sd.z * HV + hv;
+        start = sd.w;
         mp = seq_maps + b;
         b = 0;  // each sequence's maps describe a [1][T][H][128] tensor
     }
@@ -552,7 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i0 = 64 * hh + 32 * p;
             float x[32];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] = HAS_H0 ? h0[(shead * kD + i0 + u) * kD + j] : 0.f;
+            for (int u = 0; u < 32; ++u)
+                x[u] = (start & kSeqStartIdentity) ? (i0 + u == j ? 1.f : 0.f)
+                       : (HAS_H0 && !(start & kSeqStartZero)) ? h0[(shead * kD + i0 + u) * kD + j]
+                                                               : 0.f;
             put_state(i0, x, 1, false);
         }
         tmem_st_wait();

@@ -306,7 +306,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
             uint32_t x[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m)
-                x[m] = __float_as_uint((jv && a.h0) ? a.h0[(head * dk + 16 * g + m) * dv + j] : 0.f);
+                x[m] = __float_as_uint(
+                    (rflags & kRunStartIdentity) ? (16 * g + m == j ? 1.f : 0.f)
+                    : (jv && a.h0 && !(rflags & kRunStartZero)) ? a.h0[(head * dk + 16 * g + m) * dv + j]
+                                                                : 0.f);
             tmem_st16(tmem + lo + kScTmX + 16 * g, x);
         }
         tmem_st_wait();

@@ -23,10 +23,11 @@
 //
 // State slots, a group of 2P-3 per batch element b (each slot HV x [128][128]
 // f32): X_1, M_1, X_2, M_2, X_3, ..., M_{P-2}, X_{P-1} -- X_p at 2(p-1), M_p
-// at 2p-1.  gdr_segment_init fills X_1 = h0[b] (or 0), M_p = I and
-// X_{p+1} = 0; wave A leaves X_1 = S_1, M_p and X_{p+1} = c_p; the combine
-// turns X_{p+1} into S_{p+1} in place; wave B runs segment p in place on X_p,
-// which leaves the final state in X_{P-1}.
+// at 2p-1.  X_1 takes a copy of h0[b] when there is one; the map runs start
+// from the identity and the c runs from zero by their run flags, so no slot
+// needs filling.  Wave A leaves X_1 = S_1, M_p and X_{p+1} = c_p; the
+// combine turns X_{p+1} into S_{p+1} in place; wave B runs segment p in place
+// on X_p, which leaves the final state in X_{P-1}.
 #include <algorithm>
 #include <mutex>
 #include <string.h>
@@ -48,6 +49,30 @@ constexpr int kCombineThreads = 256;
 constexpr int kMtLd = kD + 4;  // transposed M rows, padded (16-byte aligned)
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// A zero value row for the map runs: device memory that is zero at module
+// load and never written, so no call has to clear it (HV x 128 bf16 of it
+// at most; a larger HV clears a row of the workspace instead).
+constexpr size_t kZeroRowBytes = 1u << 20;
+__device__ __align__(256) unsigned char g_zero_row[kZeroRowBytes];
+
+// Its device address on the current device (looked up once per device).
+cudaError_t zero_row_address(void **out) {
+    static std::mutex mu;
+    static std::vector<void *> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, nullptr);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_zero_row)) != cudaSuccess) return e;
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
 
 // SM count of the current device, looked up once per device; 0 if unknown.
 int sm_count() {
@@ -119,50 +144,6 @@ Segments plan_seqs(const Problem &p, int nseq, int P) {
 Segments plan(const Problem &p, int P) {
     const int eff = effective_segments(p.T, P);
     return eff >= 2 ? plan_seqs(p, p.B, eff) : Segments{};
-}
-
-// Four blocks per (slot, head), 32 rows each: slot j of sequence b's group
-// is X_1 (j = 0: a copy of h0[h0_slot[b]], or zeros), M_p (odd j: the
-// identity) or X_{p+1} (even j > 0: zeros).  [128][128] f32 row-major per
-// (slot, head).  Each thread's four loads are issued before its stores.
-// Block 0 also clears the one-row zero value tensor (zero_words 32-bit words).
-constexpr int kInitThreads = 256;
-constexpr int kInitPerThread = (int)(kSlotFloats / 4 / 4 / kInitThreads);  // float4s
-__global__ void __launch_bounds__(kInitThreads) gdr_segment_init(const float *__restrict__ h0,
-                                                                 const int *__restrict__ h0_slot,
-                                                                 float *__restrict__ state,
-                                                                 int HV, int group,
-                                                                 unsigned *__restrict__ zero_row,
-                                                                 int zero_words) {
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < zero_words; i += kInitThreads) zero_row[i] = 0u;
-    const int sh = blockIdx.x >> 2, quarter = blockIdx.x & 3;  // sh = slot * HV + hv
-    const int slot = sh / HV, hv = sh % HV;
-    const int b = slot / group, j = slot % group;
-    const size_t first = (size_t)quarter * (kSlotFloats / 4 / 4);  // float4 index in the slot
-    float4 *dst = reinterpret_cast<float4 *>(state + (size_t)sh * kSlotFloats) + first;
-    const float4 *src = (j == 0 && h0)
-                            ? reinterpret_cast<const float4 *>(h0 + ((size_t)h0_slot[b] * HV + hv) * kSlotFloats) + first
-                            : nullptr;
-    const bool ident = (j & 1) != 0;
-    float4 x[kInitPerThread];
-#pragma unroll
-    for (int u = 0; u < kInitPerThread; ++u) {
-        const int i = threadIdx.x + u * kInitThreads;
-        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (src) {
-            x[u] = src[i];
-        } else if (ident) {
-            const int e = (int)first + i;
-            const int r = e / (kD / 4), c0 = 4 * (e % (kD / 4));
-            if (r == c0) x[u].x = 1.f;
-            if (r == c0 + 1) x[u].y = 1.f;
-            if (r == c0 + 2) x[u].z = 1.f;
-            if (r == c0 + 3) x[u].w = 1.f;
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < kInitPerThread; ++u) dst[threadIdx.x + u * kInitThreads] = x[u];
 }
 
 // S_{p+1} = M_p S_p + c_p for p = 1 .. P-2, in place on the X slots.  One
@@ -306,6 +287,26 @@ cudaError_t copy_final_states(const Problem &p, const float *state, const std::v
     return e;
 }
 
+// h0 of every sequence (slots[b]) into its X_1 slot: one strided copy when
+// the slots are the sequences' order, else one copy per sequence.
+cudaError_t copy_initial_states(const Problem &p, float *state, const std::vector<int> &slots,
+                                int P, cudaStream_t stream) {
+    if (!p.h0) return cudaSuccess;
+    const int nseq = (int)slots.size(), group = 2 * P - 3;
+    const size_t head_bytes = (size_t)p.HV * kSlotFloats * sizeof(float);
+    bool in_order = true;
+    for (int b = 0; b < nseq; ++b) in_order = in_order && slots[b] == b;
+    if (in_order)
+        return cudaMemcpy2DAsync(state, (size_t)group * head_bytes, p.h0, head_bytes, head_bytes,
+                                 nseq, cudaMemcpyDeviceToDevice, stream);
+    cudaError_t e = cudaSuccess;
+    for (int b = 0; b < nseq && e == cudaSuccess; ++b)
+        e = cudaMemcpyAsync(state + (size_t)b * group * p.HV * kSlotFloats,
+                            p.h0 + (size_t)slots[b] * p.HV * kSlotFloats, head_bytes,
+                            cudaMemcpyDeviceToDevice, stream);
+    return e;
+}
+
 // Which of n sequences of `lengths` (chunks of `chunk` tokens) to cut, and
 // into how many segments: forced (flags' segment count), every sequence that
 // spreads over exactly that many; automatic, the largest q >= 3 for which
@@ -408,7 +409,14 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
     for (int i = 0; i < nseq; ++i)
         if (effective_segments(seqs[i].T, P) != P) return cudaErrorInvalidValue;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    const void *zero_row = ws + s.off_zero;  // cleared by gdr_segment_init
+    const size_t row_bytes = (size_t)p.HV * kD * 2;
+    void *zero_row = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (row_bytes <= kZeroRowBytes) {
+        if ((e = zero_row_address(&zero_row)) != cudaSuccess) return e;
+    } else {
+        zero_row = ws + s.off_zero;  // cleared below
+    }
     void *scratch_row = ws + s.off_scratch;
     float *state = reinterpret_cast<float *>(ws + s.off_state);
     const size_t maps = tc_seq_maps_bytes();
@@ -419,7 +427,6 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
     int *slots = reinterpret_cast<int *>(host.data() + s.off_slots);
     int4 *seqA = reinterpret_cast<int4 *>(host.data() + s.off_seqA);
     int4 *seqB = reinterpret_cast<int4 *>(host.data() + s.off_seqB);
-    cudaError_t e = cudaSuccess;
     int a = 0, bb = 0;
     for (int b = 0; b < nseq; ++b) {
         const SegSeq &sq = seqs[b];
@@ -429,34 +436,36 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
         auto seg_t0 = [&](int q) { return q * seg_len; };
         auto seg_len_of = [&](int q) { return std::min(sq.T, (q + 1) * seg_len) - q * seg_len; };
         auto add = [&](int4 *tab, size_t off_map, int &n, int q, int slot_j, const void *v_row,
-                       void *o_row) {
+                       void *o_row, int start) {
             const size_t tok0 = sq.row0 + seg_t0(q);
-            tab[n] = make_int4((int)tok0, seg_len_of(q), base + slot_j, 0);
+            tab[n] = make_int4((int)tok0, seg_len_of(q), base + slot_j, start);
             const cudaError_t r = tc_encode_seq_maps(p, tok0, seg_len_of(q),
                                                      host.data() + off_map + (size_t)n * maps,
                                                      v_row, o_row);
             ++n;
             return r;
         };
-        e = add(seqA, s.off_mapA, a, 0, 0, nullptr, nullptr);
+        e = add(seqA, s.off_mapA, a, 0, 0, nullptr, nullptr, p.h0 ? 0 : kSeqStartZero);
         for (int q = 1; q <= s.P - 2 && e == cudaSuccess; ++q) {
-            e = add(seqA, s.off_mapA, a, q, 2 * q - 1, zero_row, scratch_row);  // M_q
-            if (e == cudaSuccess) e = add(seqA, s.off_mapA, a, q, 2 * q, nullptr, scratch_row);  // c_q
+            e = add(seqA, s.off_mapA, a, q, 2 * q - 1, zero_row, scratch_row, kSeqStartIdentity);  // M_q
+            if (e == cudaSuccess)
+                e = add(seqA, s.off_mapA, a, q, 2 * q, nullptr, scratch_row, kSeqStartZero);  // c_q
         }
         for (int q = 1; q <= s.P - 1 && e == cudaSuccess; ++q)
-            e = add(seqB, s.off_mapB, bb, q, 2 * (q - 1), nullptr, nullptr);
+            e = add(seqB, s.off_mapB, bb, q, 2 * (q - 1), nullptr, nullptr, 0);
         if (e != cudaSuccess) return e;
     }
     // pageable source: the call returns once the bytes have been taken
     e = cudaMemcpyAsync(ws, host.data(), s.table_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return e;
 
-    trace_begin(kKernSegInit, stream);
-    gdr_segment_init<<<(unsigned)(4 * s.nA * p.HV), kInitThreads, 0, stream>>>(
-        p.h0, reinterpret_cast<const int *>(ws + s.off_slots), state, p.HV, s.group,
-        reinterpret_cast<unsigned *>(ws + s.off_zero), p.HV * kD / 2);
-    trace_end(kKernSegInit, stream);
-    e = cudaGetLastError();
+    // h0 into the X_1 slots (and, past the static zero row's size, a zero
+    // row of the workspace for the map runs)
+    std::vector<int> seq_slots((size_t)nseq);
+    for (int b = 0; b < nseq; ++b) seq_slots[b] = seqs[b].slot;
+    if (zero_row == ws + s.off_zero && (e = cudaMemsetAsync(zero_row, 0, row_bytes, stream)) != cudaSuccess)
+        return e;
+    e = copy_initial_states(p, state, seq_slots, s.P, stream);
     if (e != cudaSuccess) return e;
 
     Problem wave = p;
@@ -475,9 +484,7 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
                                  reinterpret_cast<const int4 *>(ws + s.off_seqB), s.nB, dev_error,
                                  stream);
     if (e != cudaSuccess) return e;
-    std::vector<int> ht_slots((size_t)nseq);
-    for (int b = 0; b < nseq; ++b) ht_slots[b] = seqs[b].slot;
-    return copy_final_states(p, state, ht_slots, s.P, stream);
+    return copy_final_states(p, state, seq_slots, s.P, stream);
 }
 
 cudaError_t launch_segmented_prefill(const Problem &p, int segments, void *workspace,
@@ -586,10 +593,10 @@ cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t
             r.pad = 0;
             return r;
         };
-        runA[a++] = run(0, 0, 0);
+        runA[a++] = run(0, 0, p.h0 ? 0 : kRunStartZero);
         for (int q = 1; q <= P - 2; ++q) {
-            runA[a++] = run(q, 2 * q - 1, kRunZeroValues | kRunNoOutputs);  // M_q
-            runA[a++] = run(q, 2 * q, kRunNoOutputs);                       // c_q
+            runA[a++] = run(q, 2 * q - 1, kRunZeroValues | kRunNoOutputs | kRunStartIdentity);  // M_q
+            runA[a++] = run(q, 2 * q, kRunNoOutputs | kRunStartZero);                           // c_q
         }
         for (int q = 1; q <= P - 1; ++q) runB[bb++] = run(q, 2 * (q - 1), 0);
     }
@@ -597,11 +604,9 @@ cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t
     cudaError_t e = cudaMemcpyAsync(ws, host.data(), s.table_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return e;
 
-    trace_begin(kKernSegInit, stream);
-    gdr_segment_init<<<(unsigned)(4 * s.nA * p.HV), kInitThreads, 0, stream>>>(
-        p.h0, reinterpret_cast<const int *>(ws + s.off_slots), state, p.HV, s.group, nullptr, 0);
-    trace_end(kKernSegInit, stream);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    std::vector<int> sl((size_t)nseq);
+    for (int b = 0; b < nseq; ++b) sl[b] = seqs[b].slot;
+    if ((e = copy_initial_states(p, state, sl, P, stream)) != cudaSuccess) return e;
 
     Problem wave = p;
     wave.h0 = state;
@@ -614,8 +619,6 @@ cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t
     e = launch_chunk_scan_runs(wave, records, rec_floats,
                                reinterpret_cast<const ScanRun *>(ws + s.off_runB), s.nB, stream);
     if (e != cudaSuccess) return e;
-    std::vector<int> sl((size_t)nseq);
-    for (int b = 0; b < nseq; ++b) sl[b] = seqs[b].slot;
     return copy_final_states(p, state, sl, P, stream);
 }
 
