@@ -124,8 +124,8 @@ typedef enum gdr_dtype {
  * records are built at once as before and only the state scan is cut: its
  * runs are scan CTAs over those records (the map runs read the values as
  * zero), segments are whole chunks of the call's chunk length, and the
- * launches are the prep, the set-up, the first scan wave, the combine and
- * the second scan wave.  GDR_FLAG_FORCE_GENERIC (the CUDA-core scan) and
+ * launches are the prep, the first scan wave, the combine and the second
+ * scan wave (and, with h0, one copy of it into the first segments' states).  GDR_FLAG_FORCE_GENERIC (the CUDA-core scan) and
  * dk or dv other than 128 never segment.
  *
  * GDR_FLAG_NO_SEGMENTS: never segment.
