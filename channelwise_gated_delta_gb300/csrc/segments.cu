@@ -101,13 +101,14 @@ struct Segments {
     int group = 0;    // state slots per sequence, 2P - 3 (1 when P = 2)
     int nseq = 0;     // sequences
     int nA = 0, nB = 0;                // runs in wave A and wave B
-    size_t off_slots = 0, off_seqA = 0, off_mapA = 0, off_seqB = 0, off_mapB = 0;
+    size_t off_seqA = 0, off_mapA = 0, off_seqB = 0, off_mapB = 0;
     size_t off_zero = 0, off_scratch = 0, off_state = 0, table_bytes = 0, total = 0;
 };
 
-// Workspace of nseq sequences cut into P segments each: the tables (the
-// sequences' h0 / ht slots, both waves' run records and tensor maps), the
-// zero value row, the scratch output row and 2P - 3 state slots per sequence.
+// Workspace of nseq sequences cut into P segments each: the tables (both
+// waves' run records and tensor maps), a zero value row (used when HV is
+// past the static one), the scratch output row and 2P - 3 state slots per
+// sequence.
 Segments plan_seqs(const Problem &p, int nseq, int P) {
     Segments s;
     if (P < 2 || nseq <= 0) return s;
@@ -118,8 +119,6 @@ Segments plan_seqs(const Problem &p, int nseq, int P) {
     s.nB = nseq * (s.P - 1);
     const size_t maps = tc_seq_maps_bytes();
     size_t off = 0;
-    s.off_slots = off;
-    off = align256(off + (size_t)nseq * sizeof(int));
     s.off_seqA = off;
     off = align256(off + (size_t)s.nA * sizeof(int4));
     s.off_mapA = off;
@@ -421,16 +420,14 @@ cudaError_t launch_segmented_list(const Problem &p, const SegSeq *seqs, int nseq
     float *state = reinterpret_cast<float *>(ws + s.off_state);
     const size_t maps = tc_seq_maps_bytes();
 
-    // tables: the sequences' h0 / ht slots; per run {first token row, length,
-    // state slot, 0} and its tensor maps
+    // tables: per run {first token row, length, state slot, start flag} and
+    // its tensor maps
     std::vector<unsigned char> host(s.table_bytes, 0);
-    int *slots = reinterpret_cast<int *>(host.data() + s.off_slots);
     int4 *seqA = reinterpret_cast<int4 *>(host.data() + s.off_seqA);
     int4 *seqB = reinterpret_cast<int4 *>(host.data() + s.off_seqB);
     int a = 0, bb = 0;
     for (int b = 0; b < nseq; ++b) {
         const SegSeq &sq = seqs[b];
-        slots[b] = sq.slot;
         const int base = b * s.group;
         const int seg_len = ((sq.T + kC - 1) / kC + P - 1) / P * kC;  // whole chunks
         auto seg_t0 = [&](int q) { return q * seg_len; };
@@ -509,7 +506,7 @@ namespace {
 
 struct ScanSegments {
     int P = 0, group = 0, nseq = 0, nA = 0, nB = 0;
-    size_t off_slots = 0, off_runA = 0, off_runB = 0, table_bytes = 0, off_state = 0, total = 0;
+    size_t off_runA = 0, off_runB = 0, table_bytes = 0, off_state = 0, total = 0;
 };
 
 ScanSegments plan_scan(const Problem &p, int nseq, int P) {
@@ -521,8 +518,6 @@ ScanSegments plan_scan(const Problem &p, int nseq, int P) {
     s.nA = nseq * s.group;
     s.nB = nseq * (P - 1);
     size_t off = 0;
-    s.off_slots = off;
-    off = align256(off + (size_t)nseq * sizeof(int));
     s.off_runA = off;
     off = align256(off + (size_t)s.nA * sizeof(ScanRun));
     s.off_runB = off;
@@ -571,13 +566,11 @@ cudaError_t launch_scan_segmented(const Problem &p, const float *records, size_t
     float *state = reinterpret_cast<float *>(ws + s.off_state);
 
     std::vector<unsigned char> host(s.table_bytes, 0);
-    int *slots = reinterpret_cast<int *>(host.data() + s.off_slots);
     ScanRun *runA = reinterpret_cast<ScanRun *>(host.data() + s.off_runA);
     ScanRun *runB = reinterpret_cast<ScanRun *>(host.data() + s.off_runB);
     int a = 0, bb = 0;
     for (int b = 0; b < nseq; ++b) {
         const ScanSeq &sq = seqs[b];
-        slots[b] = sq.slot;
         const int base = b * s.group;
         const int per = ((sq.T + C - 1) / C + P - 1) / P;  // chunks per segment
         auto run = [&](int q, int slot_j, int flags) {
