@@ -338,3 +338,30 @@ def test_segmented_scan_packed_chunk32_bf16():
                                          to_f64(d["h0"]))
         assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.bfloat16)
         assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.bfloat16)
+
+
+def test_segmented_scan_packed_in_place():
+    """A packed f32 batch updated in place (ht = h0), cut into three
+    segments: the h0 copies into the first segments' states come before any
+    final state lands, and the sequence that walks whole keeps its own slot."""
+    gen = torch.Generator()
+    gen.manual_seed(620)
+    seqs = [draw(1, L, 2, 4, 128, 128, dtype=torch.float32, generator=gen)
+            for L in (40, 900, 650)]
+    packed, cu = pack(seqs)
+    c = to_cuda(packed)
+    gdr_trace_enable(True)
+    try:
+        out, ht = gdr_forward_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, h0=c["h0"],
+                                     ht=c["h0"], chunk=64, flags=gdr_flag_segments(3))
+        gdr_device_check()
+        tr = gdr_trace_read()
+    finally:
+        gdr_trace_enable(False)
+    assert "gdr_segment_combine" in tr and tr["gdr_chunk_scan_tc"][0] == 3, tr
+    assert ht.data_ptr() == c["h0"].data_ptr()
+    for n, d in enumerate(seqs):
+        ref_o, ref_h = oracle.recurrence(*(to_f64(d[x]) for x in ("q", "k", "v", "g", "beta")),
+                                         to_f64(d["h0"]))
+        assert_close("o[%d]" % n, out[:, cu[n]:cu[n + 1]], ref_o, torch.float32)
+        assert_close("ht[%d]" % n, ht[n:n + 1], ref_h, torch.float32)
