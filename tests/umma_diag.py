@@ -1,6 +1,7 @@
 """Loader of the test-only diagnostic library libgdr_diag.so (built next to
 libgdr.so by build()): one tensor-core GEMM through a chosen pair of
-shared-memory operand layouts."""
+shared-memory operand layouts, and the library's bounded mbarrier wait run
+against a barrier that never completes."""
 import ctypes
 import os
 
@@ -23,6 +24,8 @@ def _load():
         vp, i = ctypes.c_void_p, ctypes.c_int
         _lib.gdr_diag_umma.argtypes = [i, i, i, vp, vp, vp, vp, vp]
         _lib.gdr_diag_umma.restype = i
+        _lib.gdr_diag_wait_limit.argtypes = [ctypes.c_ulonglong, vp, vp]
+        _lib.gdr_diag_wait_limit.restype = i
     return _lib
 
 
@@ -43,3 +46,20 @@ def umma_gemm(A, B, a_mode, b_mode):
     if int(err.item()) != 0:
         raise RuntimeError("gdr_diag_umma: a bounded wait timed out")
     return D
+
+
+def wait_limit(limit_ns, device="cuda"):
+    """Runs the bounded wait on a barrier nothing arrives on (32 threads);
+    returns (threads that gave up, elapsed milliseconds on the stream)."""
+    lib = _load()
+    gave_up = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    st = lib.gdr_diag_wait_limit(int(limit_ns), ctypes.c_void_p(gave_up.data_ptr()),
+                                 ctypes.c_void_p(stream.cuda_stream))
+    e1.record(stream)
+    if st != 0:
+        raise RuntimeError("gdr_diag_wait_limit failed: %d" % st)
+    torch.cuda.synchronize(device)
+    return int(gave_up.item()), e0.elapsed_time(e1)
