@@ -147,7 +147,8 @@ def test_bad_cu_seqlens_rejected():
                            chunk=16)
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64),
+                                     (torch.float32, 128)])
 def test_many_sequences_random_lengths(dtype, d):
     """257 sequences of random lengths 0..70 (tables of hundreds of entries,
     many single-token rows): bit for bit the per-sequence calls, and the
